@@ -1,0 +1,203 @@
+// C-ABI entry points: argument validation, workspace sizing and dispatch to
+// the fp32 (CUDA-core) or bf16 (tensor-core) kernels.  No entry point
+// allocates memory; none synchronises except sda_get_device_status.
+#include <math.h>
+
+#include "internal.h"
+
+using namespace sda;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validate a problem and derive sizes.  Returns SDA_OK or the error to report.
+sda_status make_prob(const sda_problem* pp, Prob* out) {
+  if (!pp || !out) return SDA_ERR_INVALID_ARG;
+  const sda_problem& p = *pp;
+  if (p.B < 1 || p.heads < 1 || p.T < 1 || p.H < 1 || p.W < 1 || p.head_dim < 1) return SDA_ERR_INVALID_ARG;
+  if (p.bt < 1 || p.bh < 1 || p.bw < 1 || p.rank < 1) return SDA_ERR_INVALID_ARG;
+  if (!(p.keep_ratio > 0.f) || !isfinite(p.keep_ratio)) return SDA_ERR_INVALID_ARG;
+  if (p.dtype != SDA_F32 && p.dtype != SDA_BF16) return SDA_ERR_INVALID_ARG;
+  if (!(p.softmax_scale >= 0.f) || !isfinite(p.softmax_scale)) return SDA_ERR_INVALID_ARG;
+  Prob q;
+  q.g.T = p.T;
+  q.g.H = p.H;
+  q.g.W = p.W;
+  q.g.bt = p.bt;
+  q.g.bh = p.bh;
+  q.g.bw = p.bw;
+  q.g.nT = (p.T + p.bt - 1) / p.bt;
+  q.g.nH = (p.H + p.bh - 1) / p.bh;
+  q.g.nW = (p.W + p.bw - 1) / p.bw;
+  long long nb = (long long)q.g.nT * q.g.nH * q.g.nW;
+  long long bs = (long long)p.bt * p.bh * p.bw;
+  q.N = (long long)p.T * p.H * p.W;
+  if (nb > (1 << 20) || bs > (1 << 20) || q.N > (1LL << 31) - 1) return SDA_ERR_UNSUPPORTED;
+  q.g.nb = (int)nb;
+  q.g.bs = (int)bs;
+  q.B = p.B;
+  q.Hh = p.heads;
+  q.d = p.head_dim;
+  q.r = p.rank;
+  q.dtype = p.dtype;
+  q.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
+  long long k = (long long)floor((double)p.keep_ratio * (double)nb + 1e-9);
+  if (k < 1) k = 1;
+  if (k > nb) k = nb;
+  q.k = (int)k;
+  *out = q;
+  return SDA_OK;
+}
+
+// Which kernels cover the problem.
+sda_status check_supported(const Prob& q) {
+  if (q.g.nb > 8192) return SDA_ERR_UNSUPPORTED;  // score row of a query block lives in shared memory
+  if (q.dtype == SDA_BF16) {
+    if (q.g.bs != 128) return SDA_ERR_UNSUPPORTED;
+    if (q.d != 64 && q.d != 128) return SDA_ERR_UNSUPPORTED;
+    if (q.r % 16 != 0 || q.r > 64) return SDA_ERR_UNSUPPORTED;
+    if (q.k > 4096) return SDA_ERR_UNSUPPORTED;
+  } else {
+    if (q.g.bs > 1024 || q.d > 128 || q.r > 64) return SDA_ERR_UNSUPPORTED;
+    if ((size_t)(q.g.bs * q.r + q.g.nb) * 4 > 160 * 1024) return SDA_ERR_UNSUPPORTED;
+  }
+  return SDA_OK;
+}
+
+sda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SDA_OK : SDA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* sda_status_string(sda_status s) {
+  switch (s) {
+    case SDA_OK:
+      return "ok";
+    case SDA_ERR_INVALID_ARG:
+      return "invalid argument";
+    case SDA_ERR_UNSUPPORTED:
+      return "unsupported problem";
+    case SDA_ERR_WORKSPACE:
+      return "workspace too small";
+    case SDA_ERR_CUDA:
+      return "CUDA error";
+    case SDA_ERR_DEVICE_TIMEOUT:
+      return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+sda_status sda_num_blocks(const sda_problem* p, int* n_blocks, int* k) {
+  Prob q;
+  sda_status s = make_prob(p, &q);
+  if (s != SDA_OK) return s;
+  if (n_blocks) *n_blocks = q.g.nb;
+  if (k) *k = q.k;
+  return SDA_OK;
+}
+
+sda_status sda_workspace_size(const sda_problem* p, int op, size_t* bytes) {
+  Prob q;
+  sda_status s = make_prob(p, &q);
+  if (s != SDA_OK) return s;
+  if (!bytes) return SDA_ERR_INVALID_ARG;
+  if ((s = check_supported(q)) != SDA_OK) return s;
+  if (op == SDA_OP_PREDICT)
+    *bytes = q.dtype == SDA_BF16 ? predict_ws_tc(q) : predict_ws_f32(q);
+  else if (op == SDA_OP_BWD)
+    *bytes = q.dtype == SDA_BF16 ? bwd_ws_tc(q) : bwd_ws_f32(q);
+  else
+    return SDA_ERR_INVALID_ARG;
+  return SDA_OK;
+}
+
+sda_status sda_predict_blocks(const sda_problem* p, const void* Q, const void* K, const void* Wq, const void* Wk,
+                              int32_t* block_idx, float* block_score, void* ws, size_t ws_bytes, void* stream) {
+  Prob q;
+  sda_status s = make_prob(p, &q);
+  if (s != SDA_OK) return s;
+  if (!Q || !K || !Wq || !Wk || !block_idx || !ws) return SDA_ERR_INVALID_ARG;
+  if ((s = check_supported(q)) != SDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q.dtype == SDA_BF16) {
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(ws))
+      return SDA_ERR_INVALID_ARG;
+    if (ws_bytes < predict_ws_tc(q)) return SDA_ERR_WORKSPACE;
+    return from_cuda(predict_tc(q, Q, K, Wq, Wk, block_idx, block_score, ws, st));
+  }
+  if (ws_bytes < predict_ws_f32(q)) return SDA_ERR_WORKSPACE;
+  return from_cuda(predict_f32(q, static_cast<const float*>(Q), static_cast<const float*>(K),
+                               static_cast<const float*>(Wq), static_cast<const float*>(Wk), block_idx, block_score,
+                               ws, st));
+}
+
+sda_status sda_attn_fwd(const sda_problem* p, const void* Q, const void* K, const void* V, const int32_t* block_idx,
+                        int kb_begin, int kb_end, const uint8_t* qb_active, void* O, float* LSE, void* stream) {
+  Prob q;
+  sda_status s = make_prob(p, &q);
+  if (s != SDA_OK) return s;
+  if (!Q || !K || !V || !block_idx || !O || !LSE) return SDA_ERR_INVALID_ARG;
+  if (kb_begin < 0 || kb_end < kb_begin || kb_end > q.g.nb) return SDA_ERR_INVALID_ARG;
+  if ((s = check_supported(q)) != SDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q.dtype == SDA_BF16) {
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SDA_ERR_INVALID_ARG;
+    return from_cuda(fwd_tc(q, Q, K, V, block_idx, kb_begin, kb_end, qb_active, O, LSE, st));
+  }
+  return from_cuda(fwd_f32(q, static_cast<const float*>(Q), static_cast<const float*>(K),
+                           static_cast<const float*>(V), block_idx, kb_begin, kb_end, qb_active,
+                           static_cast<float*>(O), LSE, st));
+}
+
+sda_status sda_attn_bwd(const sda_problem* p, const void* Q, const void* K, const void* V, const void* O,
+                        const float* LSE, const void* dO, const int32_t* block_idx, void* dQ, void* dK, void* dV,
+                        int grad_dtype, void* ws, size_t ws_bytes, void* stream) {
+  Prob q;
+  sda_status s = make_prob(p, &q);
+  if (s != SDA_OK) return s;
+  if (!Q || !K || !V || !O || !LSE || !dO || !block_idx || !dQ || !dK || !dV || !ws) return SDA_ERR_INVALID_ARG;
+  if (grad_dtype != SDA_F32 && grad_dtype != q.dtype) return SDA_ERR_INVALID_ARG;
+  if ((s = check_supported(q)) != SDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q.dtype == SDA_BF16) {
+    const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV, ws};
+    for (const void* x : ptrs)
+      if (!aligned16(x)) return SDA_ERR_INVALID_ARG;
+    if (ws_bytes < bwd_ws_tc(q)) return SDA_ERR_WORKSPACE;
+    return from_cuda(bwd_tc(q, Q, K, V, O, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, st));
+  }
+  if (ws_bytes < bwd_ws_f32(q)) return SDA_ERR_WORKSPACE;
+  return from_cuda(bwd_f32(q, static_cast<const float*>(Q), static_cast<const float*>(K),
+                           static_cast<const float*>(V), static_cast<const float*>(O), LSE,
+                           static_cast<const float*>(dO), block_idx, static_cast<float*>(dQ),
+                           static_cast<float*>(dK), static_cast<float*>(dV), ws, st));
+}
+
+sda_status sda_merge_states(int n_states, const void* const* O_parts, const float* const* LSE_parts, int B, int N,
+                            int heads, int head_dim, int dtype, void* O_out, float* LSE_out, void* stream) {
+  if (n_states < 1 || n_states > kMaxStates || !O_parts || !LSE_parts || !O_out || !LSE_out)
+    return SDA_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || heads < 1 || head_dim < 1) return SDA_ERR_INVALID_ARG;
+  if (dtype != SDA_F32 && dtype != SDA_BF16) return SDA_ERR_INVALID_ARG;
+  const int es = dtype == SDA_BF16 ? 2 : 4;
+  if ((head_dim * es) % 16 != 0 || head_dim * es > 16 * 32 * 8) return SDA_ERR_UNSUPPORTED;
+  MergeArgs a;
+  for (int s = 0; s < n_states; ++s) {
+    if (!O_parts[s] || !LSE_parts[s] || !aligned16(O_parts[s])) return SDA_ERR_INVALID_ARG;
+    a.O[s] = O_parts[s];
+    a.L[s] = LSE_parts[s];
+  }
+  if (!aligned16(O_out)) return SDA_ERR_INVALID_ARG;
+  a.n_states = n_states;
+  a.B = B;
+  a.N = N;
+  a.Hh = heads;
+  a.d = head_dim;
+  a.O_out = O_out;
+  a.L_out = LSE_out;
+  return from_cuda(launch_merge(a, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,383 @@
+// Block-sparse flash-attention forward on the 5th-generation tensor cores.
+//
+// "DSV: Exploiting Dynamic Sparsity to Accelerate Large-Scale Video DiT
+// Training", section 4 (stage 2): attention is computed only on the key blocks
+// the predictor kept.  For row i of query block I and the kept key blocks J
+// with kb_begin <= J < kb_end:  S = scale Q K^T,  LSE_i = log sum_j exp(S_ij),
+// O_i = sum_j exp(S_ij - LSE_i) v_j.  The key range and the query-block mask
+// give the per-partition states of "DiTango: Cost-Effective Parallel Diffusion
+// Generation with Selective Attention State Reuse".
+//
+// One CTA per (query block, head); 8 warps:
+//   warp 0      TMA producer: Q tile once, then K/V tiles of each kept block
+//               through an ST-deep ring (the tile box *is* the space-time
+//               tile, so no token reordering pass exists).
+//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
+//               S buffers, O += P_j V_j with P_j read from TMEM.
+//   warps 4-7   softmax: thread = query row = TMEM lane.  Online softmax in
+//               base 2 with a lazy rescale: O and l are rescaled only when a
+//               row max grows by more than 2^8, which is exact because O and l
+//               always share the same reference max.  P (bf16) overwrites S.
+//   warps 2-3   idle.
+// TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,256+D) O.
+#include "internal.h"
+
+namespace sda {
+
+namespace {
+
+struct FwdArgs {
+  Geom g;
+  int Hh, k, b, kb_begin, kb_end;
+  long long N;
+  float scale_log2;  // softmax scale * log2(e)
+  const int32_t* idx;
+  const uint8_t* qb_active;
+  float* LSE;
+  unsigned* status;
+};
+
+constexpr int kThreads = 256;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D>
+struct FwdCfg {
+  static constexpr int CH = D / 64;                  // 128-byte chunks of the head dim
+  static constexpr int TILE = 128 * D * 2;           // bytes of one 128-row bf16 tile
+  static constexpr int ST = D == 128 ? 2 : 4;        // K/V ring depth
+  static constexpr int SMEM_TILES = TILE * (1 + 2 * ST);
+};
+
+__device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
+  uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > SDA_WAIT_LIMIT_NS) return false;
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, FwdArgs a) {
+  using C = FwdCfg<D>;
+  constexpr int ST = C::ST;
+  const int I = blockIdx.x, h = blockIdx.y;
+  if (a.qb_active && !a.qb_active[I]) return;  // cached state stays untouched
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + C::TILE;
+  uint8_t* sV = sK + ST * C::TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_TILES);
+  uint64_t* qfull = bars;
+  uint64_t* kfull = bars + 1;
+  uint64_t* vfull = kfull + ST;
+  uint64_t* empty = vfull + ST;
+  uint64_t* sfull = empty + ST;   // 2
+  uint64_t* pfull = sfull + 2;    // 2
+  uint64_t* odone = pfull + 2;    // 1
+  uint64_t* drain = odone + 1;    // 1
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int* n_sel_s = abort_flag + 1;
+  int* warp_cnt = n_sel_s + 1;  // 8
+  int* sel = warp_cnt + 8;      // k
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(qfull, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(kfull + s, 1);
+      mbar_init(vfull + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sfull + s, 1);
+      mbar_init(pfull + s, 128);
+    }
+    mbar_init(odone, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *n_sel_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  // Kept blocks of this query block that fall in the key range, in list order.
+  const int32_t* row = a.idx + (((long long)a.b * a.Hh + h) * a.g.nb + I) * a.k;
+  __syncthreads();
+  for (int base = 0; base < a.k; base += kThreads) {
+    const int j = base + tid;
+    int J = j < a.k ? row[j] : -1;
+    bool keep = j < a.k && J >= a.kb_begin && J < a.kb_end && J >= 0 && J < a.g.nb;
+    unsigned m = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) warp_cnt[warp] = __popc(m);
+    __syncthreads();
+    int pos = *n_sel_s + __popc(m & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) pos += warp_cnt[w];
+    if (keep) sel[pos] = J;
+    __syncthreads();
+    if (tid == 0) {
+      int tot = 0;
+      for (int w = 0; w < kThreads / 32; ++w) tot += warp_cnt[w];
+      *n_sel_s += tot;
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_sel = *n_sel_s;
+  int t0, h0, w0;
+  block_origin(a.g, I, t0, h0, w0);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0 && n_sel > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_expect_tx(qfull, C::TILE);
+#pragma unroll
+      for (int c = 0; c < C::CH; ++c) tma_load_5d(sQ + c * 16384, &tmQ, qfull, c * 64, h, w0, h0, t0);
+      int issued = 0;
+      for (int j = 0; j < n_sel; ++j) {
+        const int s = j % ST;
+        if (j >= ST && !mbar_wait(empty + s, ((j / ST) - 1) & 1, a.status, abort_flag)) break;
+        int jt0, jh0, jw0;
+        block_origin(a.g, sel[j], jt0, jh0, jw0);
+        mbar_expect_tx(kfull + s, C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_5d(sK + s * C::TILE + c * 16384, &tmK, kfull + s, c * 64, h, jw0, jh0, jt0);
+        mbar_expect_tx(vfull + s, C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_5d(sV + s * C::TILE + c * 16384, &tmV, vfull + s, c * 64, h, jw0, jh0, jt0);
+        issued = j + 1;
+      }
+      if (*abort_flag) {  // let copies in flight land before the CTA exits
+        wait_plain(qfull, 0);
+        for (int j = issued - ST < 0 ? 0 : issued - ST; j < issued; ++j) {
+          wait_plain(kfull + j % ST, (j / ST) & 1);
+          wait_plain(vfull + j % ST, (j / ST) & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_sel > 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
+      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      const uint32_t tO = tmem + 256;
+      bool ok = mbar_wait(qfull, 0, a.status, abort_flag);
+      auto issue_S = [&](int j) -> bool {
+        const int s = j % ST;
+        if (!mbar_wait(kfull + s, (j / ST) & 1, a.status, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t tS = tmem + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tS, smem_desc(aQ + off, 16, 1024, 2), smem_desc(aK + s * C::TILE + off, 16, 1024, 2), idS,
+                 kk > 0);
+        }
+        mma_commit(sfull + (j & 1));
+        return true;
+      };
+      if (ok) ok = issue_S(0);
+      for (int j = 0; ok && j < n_sel; ++j) {
+        if (j + 1 < n_sel && !issue_S(j + 1)) break;
+        const int s = j % ST;
+        if (!mbar_wait(pfull + (j & 1), (j >> 1) & 1, a.status, abort_flag)) break;
+        if (!mbar_wait(vfull + s, (j / ST) & 1, a.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t tP = tmem + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tO, tP + kk * 8, smem_desc(aV + s * C::TILE + kk * 2048, 16384, 1024, 2), idO, (j > 0 || kk > 0));
+        mma_commit(empty + s);
+        mma_commit(odone);
+      }
+      mma_commit(drain);
+      wait_plain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------- softmax + epilogue
+    const int r = tid - 128;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_sel; ++j) {
+      if (!mbar_wait(sfull + (j & 1), (j >> 1) & 1, a.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tS = tmem + (j & 1) * 128 + lane_base;
+      float sv[128];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t u[32];
+        tmem_ld32(tS + cc * 32, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sv[cc * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
+      }
+      const int J = sel[j];
+      if (!block_is_full(a.g, J)) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (block_row_token(a.g, J, c) < 0) sv[c] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+      const float m_new = fmaxf(m, mx);
+      if (j == 0) {
+        m = m_new;
+      } else {
+        const bool need = m_new > m + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          // O holds sum_{<j} P V relative to m: wait for the last P V, then rescale.
+          if (!mbar_wait(odone, (j - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = need ? ex2(m - m_new) : 1.f;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t u[32];
+            tmem_ld32(tmem + 256 + lane_base + cc * 32, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            tmem_st32(tmem + 256 + lane_base + cc * 32, u);
+          }
+          tmem_wait_st();
+          l *= alpha;
+          if (need) m = m_new;
+        }
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(sv[cc * 32 + 2 * e] - m);
+          const float p1 = ex2(sv[cc * 32 + 2 * e + 1] - m);
+          sum += p0 + p1;
+          pk[e] = pack_bf16(p0, p1);
+        }
+        tmem_st16(tS + cc * 16, pk);
+      }
+      l += sum;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(pfull + (j & 1));
+    }
+    // Epilogue: O / l -> bf16 -> swizzled staging tile (reusing the Q tile) -> TMA store.
+    // `drain` completes once every MMA of the CTA has finished (the MMA warp commits it last).
+    if (n_sel > 0) ok = mbar_wait(drain, 0, a.status, abort_flag) && ok;
+    tc_fence_after();
+    const float inv = (n_sel > 0 && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t u[32];
+      if (n_sel > 0) {
+        tmem_ld32(tmem + 256 + lane_base + cc * 32, u);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) u[e] = 0u;
+      }
+      uint8_t* dst = sQ + (cc >> 1) * 16384;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint4 v;
+        v.x = pack_bf16(__uint_as_float(u[q4 * 8 + 0]) * inv, __uint_as_float(u[q4 * 8 + 1]) * inv);
+        v.y = pack_bf16(__uint_as_float(u[q4 * 8 + 2]) * inv, __uint_as_float(u[q4 * 8 + 3]) * inv);
+        v.z = pack_bf16(__uint_as_float(u[q4 * 8 + 4]) * inv, __uint_as_float(u[q4 * 8 + 5]) * inv);
+        v.w = pack_bf16(__uint_as_float(u[q4 * 8 + 6]) * inv, __uint_as_float(u[q4 * 8 + 7]) * inv);
+        *reinterpret_cast<uint4*>(dst + sw128_offset(r, (cc & 1) * 4 + q4)) = v;
+      }
+    }
+    const int n = block_row_token(a.g, I, r);
+    if (n >= 0)
+      a.LSE[((long long)a.b * a.Hh + h) * a.N + n] =
+          (n_sel > 0 && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    fence_async_smem();
+    named_bar(1, 128);
+    if (r == 0) {
+#pragma unroll
+      for (int c = 0; c < C::CH; ++c) tma_store_5d(&tmO, sQ + c * 16384, c * 64, h, w0, h0, t0);
+      bulk_commit();
+      bulk_wait_all();
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
+                       int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 3 * C::ST + 6) + 4 * (3 + 8) + 4 * (size_t)p.k + 64;
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  const size_t per_batch = (size_t)p.N * p.Hh * p.d * 2;
+  for (int b = 0; b < p.B; ++b) {
+    CUtensorMap mQ, mK, mV, mO;
+    const char* q = static_cast<const char*>(Q) + b * per_batch;
+    const char* k = static_cast<const char*>(K) + b * per_batch;
+    const char* v = static_cast<const char*>(V) + b * per_batch;
+    char* o = static_cast<char*>(O) + b * per_batch;
+    const Geom& g = p.g;
+    if (!make_token_map(&mQ, q, 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
+        !make_token_map(&mK, k, 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
+        !make_token_map(&mV, v, 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
+        !make_token_map(&mO, o, 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw))
+      return cudaErrorInvalidValue;
+    FwdArgs a;
+    a.g = g;
+    a.Hh = p.Hh;
+    a.k = p.k;
+    a.b = b;
+    a.kb_begin = kb_begin;
+    a.kb_end = kb_end;
+    a.N = p.N;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.idx = idx;
+    a.qb_active = qb_active;
+    a.LSE = LSE;
+    a.status = status;
+    dim3 grid(g.nb, p.Hh);
+    fwd_tc_kernel<D><<<grid, kThreads, smem, st>>>(mQ, mK, mV, mO, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t fwd_tc(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
+                   int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st) {
+  if (p.d == 64) return launch_fwd<64>(p, Q, K, V, idx, kb_begin, kb_end, qb_active, O, LSE, st);
+  return launch_fwd<128>(p, Q, K, V, idx, kb_begin, kb_end, qb_active, O, LSE, st);
+}
+
+}  // namespace sda

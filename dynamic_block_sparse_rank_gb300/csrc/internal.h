@@ -1,0 +1,74 @@
+// Internal host-side interfaces between the C-ABI layer (api.cu) and the
+// kernel translation units.  Nothing here is exported.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/sda.h"
+#include "common.cuh"
+
+namespace sda {
+
+// Validated problem with derived sizes.
+struct Prob {
+  Geom g;
+  int B, Hh, d, r, k, dtype;
+  float scale;  // softmax scale
+  long long N;  // tokens per batch entry
+};
+
+constexpr int kMaxStates = 16;
+
+struct MergeArgs {
+  const void* O[kMaxStates];
+  const float* L[kMaxStates];
+  int n_states;
+  int B, N, Hh, d;
+  void* O_out;
+  float* L_out;
+};
+
+// Device status word of the current device (see status.cu).
+unsigned* status_ptr();
+
+// ---- merge.cu
+cudaError_t launch_merge(const MergeArgs& a, int dtype, cudaStream_t st);
+
+// ---- simt.cu (fp32 problems)
+size_t predict_ws_f32(const Prob& p);
+cudaError_t predict_f32(const Prob& p, const float* Q, const float* K, const float* Wq, const float* Wk,
+                        int32_t* idx, float* score, void* ws, cudaStream_t st);
+cudaError_t fwd_f32(const Prob& p, const float* Q, const float* K, const float* V, const int32_t* idx,
+                    int kb_begin, int kb_end, const uint8_t* qb_active, float* O, float* LSE, cudaStream_t st);
+size_t bwd_ws_f32(const Prob& p);
+cudaError_t bwd_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* O,
+                    const float* LSE, const float* dO, const int32_t* idx, float* dQ, float* dK, float* dV,
+                    void* ws, cudaStream_t st);
+
+// ---- tensor maps (tmap.cu)
+// 5-D map over a [.., T, H, W, heads, d] bf16 or fp32 tensor of one batch
+// entry; box = (64B-or-128B of d) x 1 head x bw x bh x bt with 128B swizzle.
+bool make_token_map(CUtensorMap* m, const void* base, int dtype_bytes, int T, int H, int W, int Hh, int d,
+                    int bt, int bh, int bw);
+
+// ---- predict_tc.cu (bf16 problems)
+size_t predict_ws_tc(const Prob& p);
+cudaError_t predict_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, int32_t* idx,
+                       float* score, void* ws, cudaStream_t st);
+
+// ---- attn_fwd_tc.cu
+cudaError_t fwd_tc(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
+                   int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st);
+
+// ---- attn_bwd_tc.cu
+size_t bwd_ws_tc(const Prob& p);
+cudaError_t bwd_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                   const void* dO, const int32_t* idx, void* dQ, void* dK, void* dV, int grad_dtype, void* ws,
+                   cudaStream_t st);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace sda

@@ -1,0 +1,155 @@
+"""Thin ctypes binding of libsda.so (include/sda.h): argument marshalling only.
+
+Every entry point keeps the C name and takes device tensors (torch) or raw
+device pointers (int).  Outputs and workspace are allocated by the caller;
+nothing here computes.  A missing or unloadable library raises immediately:
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsda.so")
+
+SDA_OK, SDA_ERR_INVALID_ARG, SDA_ERR_UNSUPPORTED, SDA_ERR_WORKSPACE, SDA_ERR_CUDA, SDA_ERR_DEVICE_TIMEOUT = range(6)
+SDA_F32, SDA_BF16 = 0, 1
+SDA_OP_PREDICT, SDA_OP_BWD = 0, 1
+
+EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_attn_fwd", "sda_attn_bwd",
+           "sda_merge_states", "sda_get_device_status", "sda_status_string")
+
+
+class SdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("heads", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("W", ctypes.c_int), ("head_dim", ctypes.c_int), ("bt", ctypes.c_int), ("bh", ctypes.c_int),
+                ("bw", ctypes.c_int), ("rank", ctypes.c_int), ("keep_ratio", ctypes.c_float),
+                ("dtype", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libsda.so (built by `dynamic_block_sparse_rank_gb300.build`); raise if it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m dynamic_block_sparse_rank_gb300.build` (no CPU fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, i32, pr = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(Problem)
+        L.sda_num_blocks.argtypes = [pr, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        L.sda_workspace_size.argtypes = [pr, i32, ctypes.POINTER(sz)]
+        L.sda_predict_blocks.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sda_attn_fwd.argtypes = [pr, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
+        L.sda_attn_bwd.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+        L.sda_merge_states.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i32, i32, i32, vp, vp, vp]
+        L.sda_get_device_status.argtypes = [vp]
+        L.sda_status_string.argtypes = [i32]
+        L.sda_status_string.restype = ctypes.c_char_p
+        for name in EXPORTS[:-1]:
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().sda_status_string(int(s)).decode()
+
+
+def problem(B, heads, T, H, W, head_dim, bt, bh, bw, rank, keep_ratio, dtype, softmax_scale=0.0) -> Problem:
+    dt = {"f32": SDA_F32, "bf16": SDA_BF16}.get(dtype, dtype)
+    return Problem(B, heads, T, H, W, head_dim, bt, bh, bw, rank, float(keep_ratio), int(dt), float(softmax_scale))
+
+
+def problem_from_workload(wl, softmax_scale=0.0) -> Problem:
+    return problem(wl.B, wl.heads, wl.T, wl.H, wl.W, wl.d, wl.bt, wl.bh, wl.bw, wl.rank, wl.keep, wl.dtype,
+                   softmax_scale)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != SDA_OK:
+        raise SdaError(st, where)
+
+
+def sda_num_blocks(p: Problem) -> tuple[int, int]:
+    nb, k = ctypes.c_int(), ctypes.c_int()
+    _check(lib().sda_num_blocks(ctypes.byref(p), ctypes.byref(nb), ctypes.byref(k)), "sda_num_blocks")
+    return nb.value, k.value
+
+
+def sda_workspace_size(p: Problem, op: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().sda_workspace_size(ctypes.byref(p), int(op), ctypes.byref(b)), "sda_workspace_size")
+    return b.value
+
+
+def _nbytes(ws):
+    if ws is None:
+        return 0
+    if isinstance(ws, tuple):  # (pointer, bytes)
+        return ws[1]
+    return ws.numel() * ws.element_size()
+
+
+def _wsptr(ws):
+    return ws[0] if isinstance(ws, tuple) else _ptr(ws)
+
+
+def sda_predict_blocks(p, Q, K, Wq, Wk, block_idx, block_score=None, ws=None, stream=None):
+    _check(lib().sda_predict_blocks(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), _ptr(block_idx),
+                                    _ptr(block_score), _wsptr(ws), _nbytes(ws), _stream(stream)),
+           "sda_predict_blocks")
+
+
+def sda_attn_fwd(p, Q, K, V, block_idx, O, LSE, kb_begin=0, kb_end=None, qb_active=None, stream=None):
+    if kb_end is None:
+        kb_end = sda_num_blocks(p)[0]
+    _check(lib().sda_attn_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(block_idx), int(kb_begin),
+                              int(kb_end), _ptr(qb_active), _ptr(O), _ptr(LSE), _stream(stream)), "sda_attn_fwd")
+
+
+def sda_attn_bwd(p, Q, K, V, O, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, stream=None):
+    gd = {"f32": SDA_F32, "bf16": SDA_BF16}.get(grad_dtype, grad_dtype)
+    _check(lib().sda_attn_bwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO),
+                              _ptr(block_idx), _ptr(dQ), _ptr(dK), _ptr(dV), int(gd), _wsptr(ws), _nbytes(ws),
+                              _stream(stream)), "sda_attn_bwd")
+
+
+def sda_merge_states(O_parts, LSE_parts, B, N, heads, head_dim, dtype, O_out, LSE_out, stream=None):
+    n = len(O_parts)
+    dt = {"f32": SDA_F32, "bf16": SDA_BF16}.get(dtype, dtype)
+    optrs = (ctypes.c_void_p * max(n, 1))(*[_ptr(x) for x in O_parts])
+    lptrs = (ctypes.c_void_p * max(n, 1))(*[_ptr(x) for x in LSE_parts])
+    _check(lib().sda_merge_states(n, optrs, lptrs, int(B), int(N), int(heads), int(head_dim), int(dt), _ptr(O_out),
+                                  _ptr(LSE_out), _stream(stream)), "sda_merge_states")
+
+
+def sda_get_device_status(stream=None) -> int:
+    return lib().sda_get_device_status(_stream(stream))

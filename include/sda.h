@@ -1,0 +1,143 @@
+/*
+ * sda.h — C ABI of the dynamic block-sparse attention library (sm_103a).
+ *
+ * The library computes the three steps of learned block-sparse attention for
+ * video diffusion transformers:
+ *
+ *   1. sda_predict_blocks — a low-rank predictor picks, for every query block,
+ *      the key blocks worth attending to.  "DSV: Exploiting Dynamic Sparsity to
+ *      Accelerate Large-Scale Video DiT Training", section 3a ("low-rank
+ *      predictor": a cheap estimate guesses which ~10% matters before the
+ *      expensive attention runs) and section 3b ("query grouping": neighbouring
+ *      tokens share the decision).  Form used: q~ = Q Wq, k~ = K Wk (rank r);
+ *      s(I, J) = max over i in I, j in J of q~_i . k~_j; keep the k highest J
+ *      per I, ties to the lower J, k = clamp(floor(keep_ratio * n_b + 1e-9), 1, n_b).
+ *   2. sda_attn_fwd / sda_attn_bwd — flash attention restricted to the kept
+ *      blocks (DSV section 4, stage 2: compute only on the predicted parts),
+ *      emitting O and the natural-log log-sum-exp, and the gradients dQ, dK, dV
+ *      with the block map held fixed.
+ *   3. sda_merge_states — the log-sum-exp merge of partial attention states
+ *      computed over separate key partitions: the state-reuse primitive of
+ *      "DiTango: Cost-Effective Parallel Diffusion Generation with Selective
+ *      Attention State Reuse" (near partitions recomputed, far ones reused).
+ *
+ * Conventions shared by every call
+ *   - Tokens of a T x H x W latent grid are in raster order n = (t*H + h)*W + w.
+ *     Q, K, V, O, dO, dQ, dK, dV are contiguous row-major [B, N, heads, d].
+ *     LSE is [B, heads, N] (fp32, natural log).
+ *   - Blocks are compact bt x bh x bw space-time tiles numbered t-major,
+ *     I = (it*nH + ih)*nW + iw with nT = ceil(T/bt) etc.; edge tiles of a
+ *     non-divisible grid are clipped (they hold only real tokens).
+ *   - All device pointers are owned by the caller; the library allocates no
+ *     device or host memory.  Scratch comes from the caller's workspace (ws).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Argument errors are reported synchronously and nothing is
+ *     launched.  A device-side bounded wait that runs out sets a latched status
+ *     word that sda_get_device_status reports.
+ *   - dtype SDA_F32 runs fp32 CUDA-core kernels (any d <= 128, any tile up to
+ *     1024 tokens); SDA_BF16 runs the tensor-core path, which requires
+ *     bt*bh*bw == 128, d in {64, 128} and rank in {16, 32, 48, 64}.
+ *     Unsupported shapes return SDA_ERR_UNSUPPORTED.
+ *   - Pointers used by the tensor-core path must be 16-byte aligned.
+ */
+#ifndef SDA_H_
+#define SDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDA_OK = 0,
+  SDA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad range */
+  SDA_ERR_UNSUPPORTED = 2,   /* valid problem the kernels do not cover */
+  SDA_ERR_WORKSPACE = 3,     /* ws_bytes smaller than sda_workspace_size */
+  SDA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  SDA_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait ran out (see sda_get_device_status) */
+} sda_status;
+
+typedef enum { SDA_F32 = 0, SDA_BF16 = 1 } sda_dtype;
+
+/* Problem description (DSV problem statement: a T x H x W latent grid with
+ * heads and head dim, query/key block sizes, predictor rank, keep ratio). */
+typedef struct {
+  int B, heads, T, H, W, head_dim;
+  int bt, bh, bw;      /* block (tile) extent along t, h, w */
+  int rank;            /* predictor rank r */
+  float keep_ratio;    /* fraction of key blocks kept per query block */
+  int dtype;           /* sda_dtype of Q, K, V, O, dO, Wq, Wk */
+  float softmax_scale; /* 0 selects 1/sqrt(head_dim) */
+} sda_problem;
+
+/* Workspace queries (op argument of sda_workspace_size). */
+enum { SDA_OP_PREDICT = 0, SDA_OP_BWD = 1 };
+
+/* Host only.  n_blocks = nT*nH*nW and k = kept key blocks per query block. */
+sda_status sda_num_blocks(const sda_problem* p, int* n_blocks, int* k);
+
+/* Host only.  Bytes of device workspace that `op` needs for problem p. */
+sda_status sda_workspace_size(const sda_problem* p, int op, size_t* bytes);
+
+/* Step 1: predictor + top-k.
+ *   Q, K        [B, N, heads, d] (dtype)
+ *   Wq, Wk      [heads, d, r]    (dtype)
+ *   block_idx   out [B, heads, n_b, k] int32, each row ascending
+ *   block_score optional out [B, heads, n_b, n_b] fp32 block scores s(I, J)
+ *               (pass NULL to skip; it is for inspection, O(n_b^2) bytes)
+ *   ws          device workspace of at least sda_workspace_size(SDA_OP_PREDICT).
+ * For bf16 problems q~ and k~ are stored in bf16 (round to nearest even)
+ * before the score products, which accumulate in fp32. */
+sda_status sda_predict_blocks(const sda_problem* p, const void* Q, const void* K, const void* Wq,
+                              const void* Wk, int32_t* block_idx, float* block_score, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* Step 2a: block-sparse attention forward over the kept blocks J of each query
+ * block I that satisfy kb_begin <= J < kb_end (0, n_b = all keys).
+ *   block_idx  [B, heads, n_b, k] int32 (as written by sda_predict_blocks;
+ *              entries must be distinct and in [0, n_b); order is free)
+ *   qb_active  optional [n_b] uint8; query blocks with 0 are not written at all
+ *              (their O and LSE rows keep the caller's previous contents — the
+ *              cached state of DiTango's reuse).  NULL = all active.
+ *   O          out [B, N, heads, d] (dtype);  LSE out [B, heads, N] fp32.
+ * A row whose block has no kept key in the range gets O = 0, LSE = -inf. */
+sda_status sda_attn_fwd(const sda_problem* p, const void* Q, const void* K, const void* V,
+                        const int32_t* block_idx, int kb_begin, int kb_end, const uint8_t* qb_active,
+                        void* O, float* LSE, void* stream);
+
+/* Step 2b: gradients of sda_attn_fwd (full key range) with the map fixed.
+ *   O, LSE      the forward outputs;  dO [B, N, heads, d] (dtype)
+ *   dQ, dK, dV  out [B, N, heads, d] in grad_dtype (SDA_F32, or p->dtype)
+ *   ws          device workspace of at least sda_workspace_size(SDA_OP_BWD).
+ * Deterministic: no atomics on gradient values. */
+sda_status sda_attn_bwd(const sda_problem* p, const void* Q, const void* K, const void* V,
+                        const void* O, const float* LSE, const void* dO, const int32_t* block_idx,
+                        void* dQ, void* dK, void* dV, int grad_dtype, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* Step 3: LSE merge of n_states partial states (DiTango state reuse).
+ *   O_parts[s]   device pointer, [B, N, heads, d] (dtype)
+ *   LSE_parts[s] device pointer, [B, heads, N] fp32
+ *   (the two pointer arrays themselves are host memory; 1 <= n_states <= 16)
+ *   O_out, LSE_out  same layouts.  LSE = log sum_s exp(LSE_s),
+ *   O = sum_s exp(LSE_s - LSE) O_s; rows with every LSE_s = -inf give (0, -inf).
+ * O_out may alias O_parts[0] and LSE_out may alias LSE_parts[0]. */
+sda_status sda_merge_states(int n_states, const void* const* O_parts, const float* const* LSE_parts,
+                            int B, int N, int heads, int head_dim, int dtype, void* O_out,
+                            float* LSE_out, void* stream);
+
+/* Synchronises `stream`, then returns SDA_ERR_DEVICE_TIMEOUT if any kernel of
+ * this library on the current device ran out of a bounded wait since the last
+ * call (and clears the latch), SDA_ERR_CUDA on a CUDA error, else SDA_OK. */
+sda_status sda_get_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* sda_status_string(sda_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDA_H_ */

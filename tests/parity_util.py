@@ -1,0 +1,78 @@
+"""Helpers shared by the GPU parity tests and the smoke check.
+
+Tolerances: bf16 problems max-abs <= 2e-2 and relative Frobenius <= 1e-2;
+fp32 problems 1e-4 for both.  Block selection: exact wherever the oracle's gap
+between the k-th and (k+1)-th score exceeds 1e-3 relative; otherwise (a
+near-tie) every selected block must score within 1e-3 of the (k+1)-th.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TOL = {"bf16": (2e-2, 1e-2), "f32": (1e-4, 1e-4)}
+GAP_REL = 1e-3
+
+
+def dev(x: np.ndarray, dtype: str):
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x)).to("cuda")
+    return t.to(torch.bfloat16) if dtype == "bf16" else t.float()
+
+
+def host(t) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def errors(got: np.ndarray, ref: np.ndarray) -> tuple[float, float]:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    fin = np.isfinite(ref)
+    if not np.array_equal(fin, np.isfinite(got)) or not np.array_equal(got[~fin], ref[~fin]):
+        return float("inf"), float("inf")
+    d = got[fin] - ref[fin]
+    mx = float(np.abs(d).max()) if d.size else 0.0
+    nrm = float(np.linalg.norm(ref[fin]))
+    rel = float(np.linalg.norm(d) / nrm) if nrm > 0 else float(np.linalg.norm(d))
+    return mx, rel
+
+
+def assert_close(got, ref, dtype: str, what: str):
+    atol, rtol = TOL[dtype]
+    mx, rel = errors(got, ref)
+    assert mx <= atol and rel <= rtol, f"{what}: max-abs {mx:.3e} (tol {atol}), rel-frob {rel:.3e} (tol {rtol})"
+    return mx, rel
+
+
+def check_selection(gpu_idx: np.ndarray, scores: np.ndarray, k: int) -> dict:
+    """Compare GPU index rows [..., k] with the oracle's scores [..., n_b] under the gap rule."""
+    gi = gpu_idx.reshape(-1, k)
+    sc = scores.reshape(-1, scores.shape[-1])
+    nb = sc.shape[1]
+    stats = {"rows": gi.shape[0], "exact": 0, "near_tie": 0, "near_tie_differs": 0, "fail": 0}
+    for row in range(gi.shape[0]):
+        s = sc[row]
+        order = np.lexsort((np.arange(nb), -s))
+        want = np.sort(order[:k])
+        got = gi[row]
+        if k == nb:
+            rel = np.inf
+        else:
+            sk, sk1 = s[order[k - 1]], s[order[k]]
+            rel = (sk - sk1) / max(abs(sk), abs(sk1), 1e-30)
+        if rel > GAP_REL:
+            if np.array_equal(got, want):
+                stats["exact"] += 1
+            else:
+                stats["fail"] += 1
+            continue
+        stats["near_tie"] += 1
+        sk, sk1 = s[order[k - 1]], s[order[k]]
+        floor = sk1 - GAP_REL * max(abs(sk), abs(sk1))
+        valid = (len(set(got.tolist())) == k and np.all(np.diff(got) > 0) and np.all(got >= 0) and np.all(got < nb)
+                 and np.all(s[got] >= floor))
+        if not valid:
+            stats["fail"] += 1
+        elif not np.array_equal(got, want):
+            stats["near_tie_differs"] += 1
+    return stats

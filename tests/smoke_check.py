@@ -1,0 +1,73 @@
+"""One small pass of the whole path on cuda:0 through the C ABI, checked against the oracle.
+
+A 2-head bf16 problem on a ragged 3 x 10 x 12 grid (2x8x8 tiles, 8 blocks,
+d = 64, r = 16, 4 of 8 key blocks kept): predictor + top-k, forward, backward,
+two key-partition states and their merge.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def run(device: int = 0) -> dict:
+    import torch
+
+    import oracle as orc
+    from dynamic_block_sparse_rank_gb300 import inputs, sda
+    from tests.parity_util import assert_close, check_selection, dev, host
+
+    torch.cuda.set_device(device)
+    wl = inputs.Workload("smoke", 1, 2, 3, 10, 12, 64, 2, 8, 8, 16, 0.5, "bf16", 3.0, 16, backward=True)
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk"))
+    geom = orc.Geometry(wl.T, wl.H, wl.W, wl.bt, wl.bh, wl.bw)
+    p = sda.problem_from_workload(wl)
+    nb, k = sda.sda_num_blocks(p)
+    Q, K, V, dO, Wq, Wk = (dev(x[n], "bf16") for n in ("Q", "K", "V", "dO", "Wq", "Wk"))
+
+    # 1. predictor
+    idx = torch.empty((1, wl.heads, nb, k), dtype=torch.int32, device="cuda")
+    score = torch.empty((1, wl.heads, nb, nb), dtype=torch.float32, device="cuda")
+    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICT), dtype=torch.uint8, device="cuda")
+    sda.sda_predict_blocks(p, Q, K, Wq, Wk, idx, score, ws)
+    ref_idx, ref_scores = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, "bf16")
+    sel = check_selection(idx.cpu().numpy(), ref_scores, k)
+    assert sel["fail"] == 0, sel
+    s_err = np.abs(host(score) - ref_scores).max() / np.abs(ref_scores).max()
+    assert s_err < 1e-4, s_err
+
+    # 2. forward on the oracle's map
+    idx_t = torch.from_numpy(ref_idx).cuda()
+    O = torch.empty_like(Q)
+    LSE = torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_attn_fwd(p, Q, K, V, idx_t, O, LSE)
+    O_ref, L_ref = orc.attn_fwd(x["Q"], x["K"], x["V"], ref_idx, geom)
+    assert_close(host(O), O_ref, "bf16", "smoke O")
+    assert_close(host(LSE), L_ref, "bf16", "smoke LSE")
+
+    # 3. backward
+    dQ, dK, dV = (torch.empty(Q.shape, dtype=torch.float32, device="cuda") for _ in range(3))
+    wsb = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device="cuda")
+    sda.sda_attn_bwd(p, Q, K, V, O, LSE, dO, idx_t, dQ, dK, dV, "f32", wsb)
+    gref = orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], ref_idx, geom)
+    for name, got, ref in zip(("dQ", "dK", "dV"), (dQ, dK, dV), gref):
+        assert_close(host(got), ref, "bf16", "smoke " + name)
+
+    # 4. two key partitions and their merge
+    cut = nb // 2
+    parts = []
+    for b0, b1 in ((0, cut), (cut, nb)):
+        Op = torch.empty_like(Q)
+        Lp = torch.empty_like(LSE)
+        sda.sda_attn_fwd(p, Q, K, V, idx_t, Op, Lp, kb_begin=b0, kb_end=b1)
+        parts.append((Op, Lp))
+    Om, Lm = torch.empty_like(Q), torch.empty_like(LSE)
+    sda.sda_merge_states([q[0] for q in parts], [q[1] for q in parts], 1, wl.N, wl.heads, wl.d, "bf16", Om, Lm)
+    assert_close(host(Om), O_ref, "bf16", "smoke merged O")
+    assert_close(host(Lm), L_ref, "bf16", "smoke merged LSE")
+    st = sda.sda_get_device_status()
+    assert st == sda.SDA_OK, sda.status_string(st)
+    return {"selection": sel, "score_rel_err": float(s_err)}
+
+
+if __name__ == "__main__":
+    print(run())

@@ -1,0 +1,118 @@
+"""The C-ABI library: it loads, exports every symbol include/sda.h declares, and its
+host-only calls (block counts, workspace sizes, argument validation) behave
+without a GPU.  No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dynamic_block_sparse_rank_gb300 import inputs, sda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from dynamic_block_sparse_rank_gb300 import build
+
+    build.build()
+    return sda.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sda_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert set(names) >= set(sda.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_exported_symbols_have_c_linkage(L):
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", sda.LIB_PATH], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in _declared():
+        assert n in syms, n
+
+
+@pytest.mark.parametrize("name,nb,k", [("tiny_f32_256", 4, 2), ("fwd_8k", 64, 6), ("fwd_61k", 480, 24),
+                                       ("train_524k", 4096, 204), ("merge_131k", 1144, 114)])
+def test_block_counts(L, name, nb, k):
+    wl = inputs.WORKLOADS[name]
+    assert sda.sda_num_blocks(sda.problem_from_workload(wl)) == (nb, k)
+    assert wl.n_blocks == nb and wl.k == k
+
+
+def test_workspace_sizes(L):
+    wl = inputs.WORKLOADS["train_524k"]
+    p = sda.problem_from_workload(wl)
+    pred = sda.sda_workspace_size(p, sda.SDA_OP_PREDICT)
+    assert pred == 2 * wl.heads * wl.n_blocks * 128 * wl.rank * 2  # q~ and k~ in bf16, tile order
+    bwd = sda.sda_workspace_size(p, sda.SDA_OP_BWD)
+    assert bwd >= wl.heads * wl.n_blocks * (2 * 128 * 4 + wl.k * 4)
+    f32 = sda.problem_from_workload(inputs.WORKLOADS["tiny_f32_256"])
+    assert sda.sda_workspace_size(f32, sda.SDA_OP_PREDICT) > 0 and sda.sda_workspace_size(f32, sda.SDA_OP_BWD) > 0
+    with pytest.raises(sda.SdaError) as e:
+        sda.sda_workspace_size(p, 7)
+    assert e.value.status == sda.SDA_ERR_INVALID_ARG
+
+
+def _bad(p_kw):
+    base = dict(B=1, heads=2, T=4, H=8, W=8, head_dim=64, bt=2, bh=8, bw=8, rank=16, keep_ratio=0.5, dtype="bf16")
+    base.update(p_kw)
+    return sda.problem(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({"B": 0}, sda.SDA_ERR_INVALID_ARG), ({"T": -1}, sda.SDA_ERR_INVALID_ARG), ({"bw": 0}, sda.SDA_ERR_INVALID_ARG),
+    ({"keep_ratio": 0.0}, sda.SDA_ERR_INVALID_ARG), ({"keep_ratio": float("nan")}, sda.SDA_ERR_INVALID_ARG),
+    ({"dtype": 7}, sda.SDA_ERR_INVALID_ARG), ({"softmax_scale": -1.0}, sda.SDA_ERR_INVALID_ARG),
+    ({"head_dim": 96}, sda.SDA_ERR_UNSUPPORTED), ({"bt": 1}, sda.SDA_ERR_UNSUPPORTED),
+    ({"rank": 24}, sda.SDA_ERR_UNSUPPORTED), ({"dtype": "f32", "head_dim": 256}, sda.SDA_ERR_UNSUPPORTED),
+])
+def test_invalid_problems_are_rejected_on_the_host(L, kw, status):
+    p = _bad(kw)
+    with pytest.raises(sda.SdaError) as e:
+        sda.sda_workspace_size(p, sda.SDA_OP_PREDICT)
+    assert e.value.status == status
+
+
+def test_null_and_range_arguments_return_before_any_launch(L):
+    p = _bad({})
+    # null tensors: rejected synchronously, no CUDA call is made
+    assert L.sda_predict_blocks(ctypes.byref(p), None, None, None, None, None, None, None, 0, None) == \
+        sda.SDA_ERR_INVALID_ARG
+    assert L.sda_attn_fwd(ctypes.byref(p), 16, 16, 16, 16, 0, 99, None, 16, 16, None) == sda.SDA_ERR_INVALID_ARG
+    assert L.sda_attn_fwd(ctypes.byref(p), 16, 16, 16, 16, 3, 2, None, 16, 16, None) == sda.SDA_ERR_INVALID_ARG
+    # misaligned pointers on the tensor-core path
+    assert L.sda_attn_fwd(ctypes.byref(p), 18, 16, 16, 16, 0, 2, None, 16, 16, None) == sda.SDA_ERR_INVALID_ARG
+    # workspace too small
+    assert L.sda_predict_blocks(ctypes.byref(p), 16, 16, 16, 16, 16, None, 16, 8, None) == sda.SDA_ERR_WORKSPACE
+    # bad gradient dtype
+    assert L.sda_attn_bwd(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, 16, 16, 16, 5, 16, 1 << 40, None) == \
+        sda.SDA_ERR_INVALID_ARG
+    # merge: bad state count, unsupported width
+    arr = (ctypes.c_void_p * 1)(16)
+    assert L.sda_merge_states(0, arr, arr, 1, 4, 1, 64, 1, 16, 16, None) == sda.SDA_ERR_INVALID_ARG
+    assert L.sda_merge_states(17, arr, arr, 1, 4, 1, 64, 1, 16, 16, None) == sda.SDA_ERR_INVALID_ARG
+    assert L.sda_merge_states(1, arr, arr, 1, 4, 1, 12, 1, 16, 16, None) == sda.SDA_ERR_UNSUPPORTED
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert sda.status_string(s)
+    assert "unknown" in sda.status_string(42)
+
+
+def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(sda, "_lib", None)
+    monkeypatch.setattr(sda, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        sda.lib()

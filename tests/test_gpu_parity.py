@@ -1,0 +1,193 @@
+"""GPU vs oracle parity through the C ABI on small problems that span several tiles and ragged edges.
+
+Every case draws seeded inputs, runs the CUDA path and the fp64 CPU oracle on
+the same arrays and compares element by element (tolerances in parity_util).
+Forward and backward run on the oracle's own block map, so no oracle input
+comes from the GPU.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+from dynamic_block_sparse_rank_gb300 import inputs
+from tests.parity_util import TOL, assert_close, check_selection, dev, errors, host
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dynamic_block_sparse_rank_gb300 import sda as s
+
+    s.lib()
+    return s
+
+
+def _geom(wl):
+    return orc.Geometry(wl.T, wl.H, wl.W, wl.bt, wl.bh, wl.bw)
+
+
+def _run_predict(sda, wl, x, with_score=True):
+    p = sda.problem_from_workload(wl)
+    nb, k = sda.sda_num_blocks(p)
+    idx = torch.full((wl.B, wl.heads, nb, k), -1, dtype=torch.int32, device="cuda")
+    score = torch.empty((wl.B, wl.heads, nb, nb), dtype=torch.float32, device="cuda") if with_score else None
+    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICT), dtype=torch.uint8, device="cuda")
+    sda.sda_predict_blocks(p, dev(x["Q"], wl.dtype), dev(x["K"], wl.dtype), dev(x["Wq"], wl.dtype),
+                           dev(x["Wk"], wl.dtype), idx, score, ws)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), (host(score) if with_score else None)
+
+
+def _run_fwd(sda, wl, x, idx, kb=(0, None), qb_active=None, init=None):
+    p = sda.problem_from_workload(wl)
+    Q, K, V = (dev(x[n], wl.dtype) for n in ("Q", "K", "V"))
+    if init is None:
+        O = torch.full_like(Q, float("nan"))
+        LSE = torch.full((wl.B, wl.heads, wl.N), float("nan"), dtype=torch.float32, device="cuda")
+    else:
+        O, LSE = init
+    act = None if qb_active is None else torch.from_numpy(qb_active.astype(np.uint8)).cuda()
+    sda.sda_attn_fwd(p, Q, K, V, torch.from_numpy(idx).cuda(), O, LSE, kb_begin=kb[0], kb_end=kb[1], qb_active=act)
+    torch.cuda.synchronize()
+    return O, LSE
+
+
+# ---------------------------------------------------------------------------- cases
+RAGGED_D64 = inputs.Workload("ragged_d64", 1, 3, 5, 12, 20, 64, 2, 8, 8, 16, 0.4, "bf16", 3.0, 16, backward=True)
+RAGGED_D128 = inputs.Workload("ragged_d128", 1, 2, 4, 16, 17, 128, 2, 8, 8, 32, 0.3, "bf16", 4.0, 32, backward=True)
+FULL_D128 = inputs.Workload("full_d128", 1, 2, 4, 16, 32, 128, 2, 8, 8, 32, 0.25, "bf16", 4.0, 32, backward=True)
+TWO_BATCH = inputs.Workload("two_batch", 2, 2, 4, 8, 24, 64, 2, 8, 8, 16, 0.5, "bf16", 3.0, 16, backward=True)
+SMALL = [RAGGED_D64, RAGGED_D128, FULL_D128, TWO_BATCH]
+
+
+def test_smoke_path():
+    from tests import smoke_check
+
+    smoke_check.run()
+
+
+@pytest.mark.parametrize("wl", SMALL + [inputs.WORKLOADS["tiny_f32_256"]], ids=lambda w: w.name)
+def test_predictor_matches_oracle(sda, wl):
+    x = inputs.generate(wl, names=("Q", "K", "Wq", "Wk"))
+    idx, score = _run_predict(sda, wl, x)
+    ref_idx, ref_sc = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], _geom(wl), wl.keep, wl.dtype)
+    sel = check_selection(idx, ref_sc, wl.k)
+    assert sel["fail"] == 0, sel
+    rel = np.abs(score - ref_sc).max() / np.abs(ref_sc).max()
+    assert rel < (1e-5 if wl.dtype == "bf16" else 1e-5), rel
+
+
+@pytest.mark.parametrize("wl", SMALL + [inputs.WORKLOADS["tiny_f32_256"]], ids=lambda w: w.name)
+def test_forward_matches_oracle(sda, wl):
+    x = inputs.generate(wl, names=("Q", "K", "V", "Wq", "Wk"))
+    geom = _geom(wl)
+    ref_idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    O, LSE = _run_fwd(sda, wl, x, ref_idx)
+    O_ref, L_ref = orc.attn_fwd(x["Q"], x["K"], x["V"], ref_idx, geom)
+    assert_close(host(O), O_ref, wl.dtype, "O")
+    assert_close(host(LSE), L_ref, wl.dtype, "LSE")
+
+
+@pytest.mark.parametrize("wl", SMALL + [inputs.WORKLOADS["tiny_f32_256"]], ids=lambda w: w.name)
+@pytest.mark.parametrize("gdt", ["f32", "same"])
+def test_backward_matches_oracle(sda, wl, gdt):
+    gdt = wl.dtype if gdt == "same" else gdt
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk"))
+    geom = _geom(wl)
+    ref_idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    O, LSE = _run_fwd(sda, wl, x, ref_idx)
+    p = sda.problem_from_workload(wl)
+    gt = torch.float32 if gdt == "f32" else torch.bfloat16
+    dQ, dK, dV = (torch.full(O.shape, float("nan"), dtype=gt, device="cuda") for _ in range(3))
+    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device="cuda")
+    sda.sda_attn_bwd(p, dev(x["Q"], wl.dtype), dev(x["K"], wl.dtype), dev(x["V"], wl.dtype), O, LSE,
+                     dev(x["dO"], wl.dtype), torch.from_numpy(ref_idx).cuda(), dQ, dK, dV, gdt, ws)
+    torch.cuda.synchronize()
+    refs = orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], ref_idx, geom)
+    for name, got, ref in zip(("dQ", "dK", "dV"), (dQ, dK, dV), refs):
+        assert_close(host(got), ref, wl.dtype, name)
+    assert sda.sda_get_device_status() == sda.SDA_OK
+
+
+def test_forward_empty_selection_and_inactive_blocks(sda):
+    wl = RAGGED_D64
+    x = inputs.generate(wl, names=("Q", "K", "V", "Wq", "Wk"))
+    geom = _geom(wl)
+    nb = geom.n_blocks
+    ref_idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    # a key range that some query blocks keep nothing from
+    b0, b1 = nb - 2, nb
+    O, LSE = _run_fwd(sda, wl, x, ref_idx, kb=(b0, b1))
+    O_ref, L_ref = orc.attn_fwd(x["Q"], x["K"], x["V"], ref_idx, geom, kb_begin=b0, kb_end=b1)
+    assert np.isneginf(L_ref).any() and np.isfinite(L_ref).any()
+    assert_close(host(O), O_ref, "bf16", "O range")
+    assert_close(host(LSE), L_ref, "bf16", "LSE range")
+    # inactive query blocks keep the caller's contents
+    act = np.zeros(nb, dtype=bool)
+    act[::3] = True
+    Q = dev(x["Q"], "bf16")
+    O0 = torch.full_like(Q, 7.0)
+    L0 = torch.full((1, wl.heads, wl.N), 5.0, dtype=torch.float32, device="cuda")
+    O, LSE = _run_fwd(sda, wl, x, ref_idx, qb_active=act, init=(O0, L0))
+    Oh, Lh = host(O), host(LSE)
+    O_ref, L_ref = orc.attn_fwd(x["Q"], x["K"], x["V"], ref_idx, geom, qb_active=act)
+    for I in range(nb):
+        rows = geom.tokens(I)
+        if act[I]:
+            assert errors(Oh[:, rows], O_ref[:, rows])[0] <= TOL["bf16"][0]
+            assert errors(Lh[:, :, rows], L_ref[:, :, rows])[0] <= TOL["bf16"][0]
+        else:
+            assert np.all(Oh[:, rows] == 7.0) and np.all(Lh[:, :, rows] == 5.0)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 64), ("f32", 128)])
+@pytest.mark.parametrize("n_states", [1, 3, 4, 16])
+def test_merge_matches_oracle(sda, dtype, d, n_states):
+    rng = np.random.default_rng(n_states * 7 + d)
+    B, N, Hh = 2, 333, 3
+    Os = [rng.standard_normal((B, N, Hh, d)) * 2 for _ in range(n_states)]
+    Ls = [rng.standard_normal((B, Hh, N)) * 3 for _ in range(n_states)]
+    for s in range(n_states):  # empty partitions: some rows -inf in some states, some rows in all
+        Ls[s][rng.random((B, Hh, N)) < 0.2] = -np.inf
+    for L in Ls:
+        L[:, 0, :5] = -np.inf
+    if dtype == "bf16":
+        Os = [inputs.round_to_bf16(o) for o in Os]
+    Ls = [x.astype(np.float32) for x in Ls]
+    Od = [dev(o.astype(np.float32), dtype) for o in Os]
+    Ld = [torch.from_numpy(x).cuda() for x in Ls]
+    Oo = torch.empty_like(Od[0])
+    Lo = torch.empty_like(Ld[0])
+    sda.sda_merge_states(Od, Ld, B, N, Hh, d, dtype, Oo, Lo)
+    torch.cuda.synchronize()
+    Or, Lr = orc.merge_states(Os, [np.transpose(x, (0, 2, 1)) for x in Ls])
+    assert_close(host(Oo), Or, dtype, "merged O")
+    assert_close(host(Lo), np.transpose(Lr, (0, 2, 1)), dtype, "merged LSE")
+    # in place: the output may alias the first state
+    sda.sda_merge_states(Od, Ld, B, N, Hh, d, dtype, Od[0], Ld[0])
+    torch.cuda.synchronize()
+    assert_close(host(Od[0]), Or, dtype, "merged O in place")
+
+
+def test_predict_is_deterministic_and_tie_exact(sda):
+    # integer inputs with identical key blocks: every score ties, the lowest k indices win
+    wl = inputs.Workload("ties", 1, 1, 4, 16, 16, 64, 2, 8, 8, 16, 0.25, "bf16", 0.0, 1)
+    geom = _geom(wl)
+    rng = np.random.default_rng(5)
+    Q = rng.integers(-3, 4, size=(1, wl.N, 1, wl.d)).astype(np.float32)
+    blk = rng.integers(-3, 4, size=(128, wl.d)).astype(np.float32)
+    K = np.empty_like(Q)
+    for J in range(geom.n_blocks):
+        K[0, geom.tokens(J), 0] = blk
+    W = np.zeros((1, wl.d, wl.rank), dtype=np.float32)
+    W[0, :16, :16] = np.eye(16)
+    x = {"Q": Q, "K": K, "Wq": W, "Wk": W}
+    idx1, _ = _run_predict(sda, wl, x, with_score=False)
+    idx2, _ = _run_predict(sda, wl, x, with_score=False)
+    assert np.array_equal(idx1, idx2)
+    assert np.all(idx1 == np.arange(wl.k, dtype=np.int32))
