@@ -151,28 +151,82 @@ sda_status sda_attn_fwd(const sda_problem* p, const void* Q, const void* K, cons
                            static_cast<float*>(O), LSE, st));
 }
 
+namespace {
+// Shared argument checks of the backward entry points.
+// ptrs[0 .. n_tensors) are token tensors (16-byte alignment on the tensor-core
+// path); the rest (LSE, block_idx) only need to be non-null.
+sda_status bwd_common(const sda_problem* p, Prob* q, const void* const* ptrs, int nptrs, int n_tensors, int grad_dtype,
+                      void* ws, size_t ws_bytes) {
+  sda_status s = make_prob(p, q);
+  if (s != SDA_OK) return s;
+  for (int i = 0; i < nptrs; ++i)
+    if (!ptrs[i]) return SDA_ERR_INVALID_ARG;
+  if (!ws) return SDA_ERR_INVALID_ARG;
+  if (grad_dtype != SDA_F32 && grad_dtype != q->dtype) return SDA_ERR_INVALID_ARG;
+  if ((s = check_supported(*q)) != SDA_OK) return s;
+  if (q->dtype == SDA_BF16) {
+    for (int i = 0; i < n_tensors; ++i)
+      if (!aligned16(ptrs[i])) return SDA_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return SDA_ERR_INVALID_ARG;
+    if (ws_bytes < bwd_ws_tc(*q)) return SDA_ERR_WORKSPACE;
+  } else if (ws_bytes < bwd_ws_f32(*q)) {
+    return SDA_ERR_WORKSPACE;
+  }
+  return SDA_OK;
+}
+}  // namespace
+
+sda_status sda_attn_bwd_prepare(const sda_problem* p, const void* Q, const void* K, const void* V, const void* O,
+                                const float* LSE, const void* dO, const int32_t* block_idx, void* ws,
+                                size_t ws_bytes, void* stream) {
+  Prob q;
+  const void* ptrs[] = {Q, K, V, O, dO, LSE, block_idx};
+  sda_status s = bwd_common(p, &q, ptrs, 7, 5, p ? p->dtype : SDA_F32, ws, ws_bytes);
+  if (s != SDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q.dtype == SDA_BF16) return from_cuda(bwd_prepare_tc(q, Q, K, V, O, LSE, dO, block_idx, ws, st));
+  return from_cuda(bwd_prepare_f32(q, static_cast<const float*>(O), static_cast<const float*>(dO), ws, st));
+}
+
+sda_status sda_attn_bwd_dq(const sda_problem* p, const void* Q, const void* K, const void* V, const float* LSE,
+                           const void* dO, const int32_t* block_idx, void* dQ, int grad_dtype, void* ws,
+                           size_t ws_bytes, void* stream) {
+  Prob q;
+  const void* ptrs[] = {Q, K, V, dO, dQ, LSE, block_idx};
+  sda_status s = bwd_common(p, &q, ptrs, 7, 5, grad_dtype, ws, ws_bytes);
+  if (s != SDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q.dtype == SDA_BF16) return from_cuda(bwd_dq_tc(q, V, dO, block_idx, dQ, grad_dtype, ws, st));
+  return from_cuda(bwd_dq_f32(q, static_cast<const float*>(Q), static_cast<const float*>(K),
+                              static_cast<const float*>(V), LSE, static_cast<const float*>(dO), block_idx,
+                              static_cast<float*>(dQ), ws, st));
+}
+
+sda_status sda_attn_bwd_dkdv(const sda_problem* p, const void* Q, const void* K, const void* V, const float* LSE,
+                             const void* dO, const int32_t* block_idx, void* dK, void* dV, int grad_dtype, void* ws,
+                             size_t ws_bytes, void* stream) {
+  Prob q;
+  const void* ptrs[] = {Q, K, V, dO, dK, dV, LSE, block_idx};
+  sda_status s = bwd_common(p, &q, ptrs, 8, 6, grad_dtype, ws, ws_bytes);
+  if (s != SDA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q.dtype == SDA_BF16) return from_cuda(bwd_dkdv_tc(q, V, dO, dK, dV, grad_dtype, ws, st));
+  return from_cuda(bwd_dkdv_f32(q, static_cast<const float*>(Q), static_cast<const float*>(K),
+                                static_cast<const float*>(V), LSE, static_cast<const float*>(dO), block_idx,
+                                static_cast<float*>(dK), static_cast<float*>(dV), ws, st));
+}
+
 sda_status sda_attn_bwd(const sda_problem* p, const void* Q, const void* K, const void* V, const void* O,
                         const float* LSE, const void* dO, const int32_t* block_idx, void* dQ, void* dK, void* dV,
                         int grad_dtype, void* ws, size_t ws_bytes, void* stream) {
   Prob q;
-  sda_status s = make_prob(p, &q);
+  const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV, LSE, block_idx};
+  sda_status s = bwd_common(p, &q, ptrs, 10, 8, grad_dtype, ws, ws_bytes);
   if (s != SDA_OK) return s;
-  if (!Q || !K || !V || !O || !LSE || !dO || !block_idx || !dQ || !dK || !dV || !ws) return SDA_ERR_INVALID_ARG;
-  if (grad_dtype != SDA_F32 && grad_dtype != q.dtype) return SDA_ERR_INVALID_ARG;
-  if ((s = check_supported(q)) != SDA_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (q.dtype == SDA_BF16) {
-    const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV, ws};
-    for (const void* x : ptrs)
-      if (!aligned16(x)) return SDA_ERR_INVALID_ARG;
-    if (ws_bytes < bwd_ws_tc(q)) return SDA_ERR_WORKSPACE;
-    return from_cuda(bwd_tc(q, Q, K, V, O, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, st));
-  }
-  if (ws_bytes < bwd_ws_f32(q)) return SDA_ERR_WORKSPACE;
-  return from_cuda(bwd_f32(q, static_cast<const float*>(Q), static_cast<const float*>(K),
-                           static_cast<const float*>(V), static_cast<const float*>(O), LSE,
-                           static_cast<const float*>(dO), block_idx, static_cast<float*>(dQ),
-                           static_cast<float*>(dK), static_cast<float*>(dV), ws, st));
+  if ((s = sda_attn_bwd_prepare(p, Q, K, V, O, LSE, dO, block_idx, ws, ws_bytes, stream)) != SDA_OK) return s;
+  if ((s = sda_attn_bwd_dq(p, Q, K, V, LSE, dO, block_idx, dQ, grad_dtype, ws, ws_bytes, stream)) != SDA_OK)
+    return s;
+  return sda_attn_bwd_dkdv(p, Q, K, V, LSE, dO, block_idx, dK, dV, grad_dtype, ws, ws_bytes, stream);
 }
 
 sda_status sda_merge_states(int n_states, const void* const* O_parts, const float* const* LSE_parts, int B, int N,

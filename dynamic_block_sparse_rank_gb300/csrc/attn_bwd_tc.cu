@@ -6,19 +6,24 @@
 // kept blocks and D_i = dO_i . O_i,
 //   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
 //
-// Deterministic, no atomics on gradient values.  Kernels, in stream order:
-//   pre_kernel      D_i and LSE_i * log2(e) per row, tile-ordered (+inf for
-//                   rows outside the grid so that their P is exactly zero).
-//   csr kernels     transpose the block map: for every key block J the query
-//                   blocks that kept it, ascending; key blocks are then visited
-//                   longest list first (LPT) to balance the dK/dV CTAs.
-//   dq_kernel       per query block: S = Q K_J^T and dP = dO V_J^T (M=128,
-//                   N=128, K=d), dS in TMEM, dQ += dS K_J; 8 compute warps.
-//   dkdv_kernel     per key block: S^T = K Q_I^T and dP^T = V dO_I^T, P^T and
-//                   dS^T in TMEM, dV += P^T dO_I, dK += dS^T Q_I.  For d = 128
-//                   the four 128-column accumulators fill all 512 TMEM columns.
-// The dq kernel repeats the S and dP products of the dK/dV kernel (7 GEMMs per
-// block pair instead of 5) in exchange for no fp32 dQ reduction buffer.
+// Deterministic, no atomics on gradient values.  Every MMA of the backward
+// takes fp16 operands: prepare writes fp16 copies of Q, K, V and dO (exact for
+// bf16 values inside fp16's normal range), so that P and dS can be rounded to
+// fp16 (8x finer than bf16) for the products that consume them — one MMA
+// needs A and B of the same type.  Phases, in stream order:
+//   prepare   block-map transpose (for every key block, the query blocks that
+//             kept it, ascending; key blocks visited longest list first),
+//             D~_i = dO_i . O_i from the stored O and LSE_i * log2(e), both in
+//             tile order (+inf LSE for rows outside the grid, so their P is 0),
+//             and the fp16 copies.
+//   dq        per query block: S = Q K_J^T and dP = dO V_J^T (M=128, N=128,
+//             K=d), then dQ with the exact-D correction (see dq_kernel); it also
+//             writes the exact D_i for the next phase.
+//   dkdv      per key block: S^T = K Q_I^T and dP^T = V dO_I^T, P^T and dS^T in
+//             TMEM, dV += P^T dO_I, dK += dS^T Q_I.  For d = 128 the four
+//             128-column accumulators fill all 512 TMEM columns.
+// The dq kernel repeats the S and dP products of the dK/dV kernel in exchange
+// for no fp32 dQ reduction buffer.
 #include "internal.h"
 
 namespace sda {
@@ -35,7 +40,7 @@ struct BwdArgs {
   float scale_log2;  // softmax scale * log2(e)
   float scale;
   const int32_t* idx;     // [B, Hh, nb, k]
-  const float* Dv;        // [B, Hh, nb, 128]
+  float* Dv;              // [B, Hh, nb, 128]: D~ after prepare, exact D after dq
   const float* L2v;       // [B, Hh, nb, 128]
   const int32_t* offsets; // [B, Hh, nb + 1]
   const int32_t* lists;   // [B, Hh, nb * k]
@@ -77,6 +82,18 @@ __global__ void __launch_bounds__(128) pre_kernel(Geom g, int Hh, long long N, i
   const long long o = (((long long)b * Hh + h) * g.nb + I) * 128 + r;
   Dv[o] = dsum;
   L2v[o] = l2;
+}
+
+// bf16 -> fp16, 8 elements per thread-iteration.
+__global__ void half_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n8) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+    const uint4 v = src[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = pack_f16(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u));
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // ------------------------------------------------------------------ block-map transpose
@@ -169,6 +186,12 @@ __global__ void csr_fill_kernel(const unsigned* __restrict__ bitmap, const int32
 }
 
 // ------------------------------------------------------------------ shared pieces
+// The two compute warpgroups each own 64 of the 128 columns of an S / dP tile
+// and write their packed bf16 results (P, dS) into the first half of their own
+// column range, never into columns the other group may still be reading.
+// TMEM column of the K-step `kk` (16 elements = 8 packed columns) of such an operand:
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8); }
+
 template <int D>
 struct Cfg {
   static constexpr int CH = D / 64;
@@ -176,48 +199,61 @@ struct Cfg {
   static constexpr int ST = D == 128 ? 2 : 4;
 };
 
-// Store a 128 x D accumulator slice (this thread's row, columns [c_lo, c_lo + ncols))
-// scaled by `mul` into a 128B-swizzled staging area laid out as TMA boxes of 128
-// bytes of the row (bf16: 64 columns per box, fp32: 32 columns per box).
+// Store this thread's row of a 128 x D accumulator, columns [c_lo, c_lo + ncols),
+// as mul * (a + coef * b) (b only when tb != 0) into a 128B-swizzled staging
+// area laid out as TMA boxes of 128 bytes of the row (bf16: 64 columns per
+// box, fp32: 32 columns per box).  zero writes zeros.
 template <bool F32>
-__device__ __forceinline__ void stage_row(uint8_t* stage, uint32_t taddr, int row, int c_lo, int ncols, float mul,
-                                          bool zero) {
+__device__ __forceinline__ void stage_row(uint8_t* stage, uint32_t ta, uint32_t tb, float coef, int row, int c_lo,
+                                          int ncols, float mul, bool zero) {
   for (int c0 = c_lo; c0 < c_lo + ncols; c0 += 32) {
-    uint32_t u[32];
+    float f[32];
     if (!zero) {
-      tmem_ld32(taddr + c0, u);
+      uint32_t u[32];
+      tmem_ld32(ta + c0, u);
       tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(u[e]);
+      if (tb) {
+        tmem_ld32(tb + c0, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = fmaf(coef, __uint_as_float(u[e]), f[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) f[e] *= mul;
     } else {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) u[e] = 0u;
+      for (int e = 0; e < 32; ++e) f[e] = 0.f;
     }
     if (F32) {
       uint8_t* box = stage + (c0 >> 5) * 16384;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        uint4 v = make_uint4(__float_as_uint(__uint_as_float(u[4 * q]) * mul),
-                             __float_as_uint(__uint_as_float(u[4 * q + 1]) * mul),
-                             __float_as_uint(__uint_as_float(u[4 * q + 2]) * mul),
-                             __float_as_uint(__uint_as_float(u[4 * q + 3]) * mul));
-        *reinterpret_cast<uint4*>(box + sw128_offset(row, q)) = v;
-      }
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(box + sw128_offset(row, q)) =
+            make_uint4(__float_as_uint(f[4 * q]), __float_as_uint(f[4 * q + 1]), __float_as_uint(f[4 * q + 2]),
+                       __float_as_uint(f[4 * q + 3]));
     } else {
       uint8_t* box = stage + (c0 >> 6) * 16384;
       const int cbase = ((c0 & 63) >> 3);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 v;
-        v.x = pack_bf16(__uint_as_float(u[8 * q + 0]) * mul, __uint_as_float(u[8 * q + 1]) * mul);
-        v.y = pack_bf16(__uint_as_float(u[8 * q + 2]) * mul, __uint_as_float(u[8 * q + 3]) * mul);
-        v.z = pack_bf16(__uint_as_float(u[8 * q + 4]) * mul, __uint_as_float(u[8 * q + 5]) * mul);
-        v.w = pack_bf16(__uint_as_float(u[8 * q + 6]) * mul, __uint_as_float(u[8 * q + 7]) * mul);
-        *reinterpret_cast<uint4*>(box + sw128_offset(row, cbase + q)) = v;
-      }
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(box + sw128_offset(row, cbase + q)) =
+            make_uint4(pack_bf16(f[8 * q], f[8 * q + 1]), pack_bf16(f[8 * q + 2], f[8 * q + 3]),
+                       pack_bf16(f[8 * q + 4], f[8 * q + 5]), pack_bf16(f[8 * q + 6], f[8 * q + 7]));
     }
   }
 }
 
 // ------------------------------------------------------------------ dQ
+// D_i has to be known before dS can be formed, but the D~_i that prepare
+// derives from the stored bf16 O carries that output's rounding.  This kernel
+// therefore uses D~ for dS~ = P o (dP - D~), accumulates the exact
+// D_i = sum_j P_ij dP_ij in fp32 over the same pass, and corrects at the end:
+//   dQ_i = scale * ( sum_j dS~_ij k_j + (D~_i - D_i) sum_j P_ij k_j ),
+// which equals scale * sum_j P_ij (dP_ij - D_i) k_j.  The exact D is written
+// back for the dK/dV kernel.  TMEM: S [0,128), dP [128,256), dQ~ [256,256+D),
+// P K [256+D, 256+2D).
 template <int D, bool F32OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -239,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sdpfull = kvempty + ST;   // 1
   uint64_t* dsfull = sdpfull + 1;     // 1
   uint64_t* drain = dsfull + 1;       // 1
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  float* dpart = reinterpret_cast<float*>(drain + 1);  // 2 x 128 partial row sums of P dP
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dpart + 256);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -264,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tPK = tmem + 256 + D;
   int t0, h0, w0;
   block_origin(a.g, I, t0, h0, w0);
 
@@ -298,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
+      constexpr uint32_t idS = idesc_f16(128, 128, 0, 0);  // Q K^T and dO V^T
+      constexpr uint32_t idQ = idesc_f16(128, D, 0, 1);    // dS~ K and P K
       const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO), aK = smem_u32(sK), aV = smem_u32(sV);
       bool ok = mbar_wait(qfull, 0, a.status, abort_flag);
       for (int j = 0; ok && j < n; ++j) {
@@ -321,8 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(dsfull, j & 1, a.status, abort_flag)) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tdQ, tS + kk * 8, smem_desc(aK + s * C::TILE + kk * 2048, 16384, 1024, 2), idQ, (j > 0 || kk > 0));
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bK = smem_desc(aK + s * C::TILE + kk * 2048, 16384, 1024, 2);
+          mma_ts(tdQ, tS + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
+          mma_ts(tPK, tdP + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
+        }
         mma_commit(kvempty + s);
       }
       mma_commit(drain);
@@ -335,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const long long tile_row = (((long long)a.b * a.Hh + h) * a.g.nb + I) * 128 + row;
     const float l2 = a.L2v[tile_row];
-    const float Di = a.Dv[tile_row];
+    const float Dt = a.Dv[tile_row];  // D~ from the stored O
+    float dsum = 0.f;                 // this group's share of D = sum_j P_ij dP_ij
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait(sdpfull, j & 1, a.status, abort_flag)) break;
       tc_fence_after();
@@ -348,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + lane_base + col0, us);
         tmem_ld32(tdP + lane_base + col0, up);
         tmem_wait_ld();
-        uint32_t pk[16];
+        uint32_t pds[16], pp[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), a.scale_log2, -l2));
@@ -357,18 +398,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (block_row_token(a.g, J, col0 + 2 * e) < 0) p0 = 0.f;
             if (block_row_token(a.g, J, col0 + 2 * e + 1) < 0) p1 = 0.f;
           }
-          pk[e] = pack_bf16(p0 * (__uint_as_float(up[2 * e]) - Di), p1 * (__uint_as_float(up[2 * e + 1]) - Di));
+          const float dp0 = __uint_as_float(up[2 * e]), dp1 = __uint_as_float(up[2 * e + 1]);
+          dsum = fmaf(p0, dp0, fmaf(p1, dp1, dsum));
+          pds[e] = pack_f16(p0 * (dp0 - Dt), p1 * (dp1 - Dt));
+          pp[e] = pack_f16(p0, p1);
         }
-        tmem_st16(tS + lane_base + col0 / 2, pk);
+        tmem_st16(tS + lane_base + grp * 64 + cc * 16, pds);
+        tmem_st16(tdP + lane_base + grp * 64 + cc * 16, pp);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(dsfull);
     }
-    // epilogue: dQ = scale * (dS K) -> staging (Q and dO tiles are free once all MMAs are done)
+    dpart[grp * 128 + row] = dsum;
     mbar_wait(drain, 0, a.status, abort_flag);
     tc_fence_after();
-    stage_row<F32OUT>(sQ, tdQ + lane_base, row, grp * (D / 2), D / 2, a.scale, n == 0);
+    named_bar(1, 256);
+    const float Dx = dpart[row] + dpart[128 + row];
+    if (grp == 0) a.Dv[tile_row] = Dx;  // exact D for the dK/dV kernel
+    // dQ = scale * (dQ~ + (D~ - D) P K) -> staging (Q and dO tiles are free once all MMAs are done)
+    stage_row<F32OUT>(sQ, tdQ + lane_base, tPK + lane_base, Dt - Dx, row, grp * (D / 2), D / 2, a.scale, n == 0);
     fence_async_smem();
     named_bar(1, 256);
     if (tid == 128) {
@@ -478,8 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idG = idesc_bf16(128, D, 0, 1);
+      constexpr uint32_t idS = idesc_f16(128, 128, 0, 0);    // K Q^T and V dO^T
+      constexpr uint32_t idP = idS;
+      constexpr uint32_t idV = idesc_f16(128, D, 0, 1);      // P^T dO and dS^T Q
+      constexpr uint32_t idK = idV;
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aR = smem_u32(ring);
       bool ok = mbar_wait(kvfull, 0, a.status, abort_flag);
       for (int u = 0; ok && u < n; ++u) {
@@ -495,15 +546,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tdP, smem_desc(aV + off, 16, 1024, 2), smem_desc(adO + off, 16, 1024, 2), idS, kk > 0);
+          mma_ss(tdP, smem_desc(aV + off, 16, 1024, 2), smem_desc(adO + off, 16, 1024, 2), idP, kk > 0);
         }
         mma_commit(sdpfull);
         if (!mbar_wait(pdsfull, u & 1, a.status, abort_flag)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tdV, tS + kk * 8, smem_desc(adO + kk * 2048, 16384, 1024, 2), idG, (u > 0 || kk > 0));
-          mma_ts(tdK, tdP + kk * 8, smem_desc(aQ + kk * 2048, 16384, 1024, 2), idG, (u > 0 || kk > 0));
+          mma_ts(tdV, tS + packed_col(kk), smem_desc(adO + kk * 2048, 16384, 1024, 2), idV, (u > 0 || kk > 0));
+          mma_ts(tdK, tdP + packed_col(kk), smem_desc(aQ + kk * 2048, 16384, 1024, 2), idK, (u > 0 || kk > 0));
         }
         mma_commit(qempty + s);
       }
@@ -536,11 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), a.scale_log2, -l2[c]));
           float p1 = ex2(fmaf(__uint_as_float(us[2 * e + 1]), a.scale_log2, -l2[c + 1]));
           if (!row_ok) p0 = p1 = 0.f;
-          pp[e] = pack_bf16(p0, p1);
-          pd[e] = pack_bf16(p0 * (__uint_as_float(up[2 * e]) - dv[c]), p1 * (__uint_as_float(up[2 * e + 1]) - dv[c + 1]));
+          pp[e] = pack_f16(p0, p1);
+          pd[e] = pack_f16(p0 * (__uint_as_float(up[2 * e]) - dv[c]), p1 * (__uint_as_float(up[2 * e + 1]) - dv[c + 1]));
         }
-        tmem_st16(tS + lane_base + col0 / 2, pp);
-        tmem_st16(tdP + lane_base + col0 / 2, pd);
+        tmem_st16(tS + lane_base + grp * 64 + cc * 16, pp);
+        tmem_st16(tdP + lane_base + grp * 64 + cc * 16, pd);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -550,8 +601,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     // staging: dK boxes then dV boxes, starting at sK (K, V and the ring are free now)
     constexpr int GB = F32OUT ? 128 * D * 4 : 128 * D * 2;  // bytes of one staged gradient tile
-    stage_row<F32OUT>(sK, tdK + lane_base, row, grp * (D / 2), D / 2, a.scale, n == 0);
-    stage_row<F32OUT>(sK + GB, tdV + lane_base, row, grp * (D / 2), D / 2, 1.f, n == 0);
+    stage_row<F32OUT>(sK, tdK + lane_base, 0u, 0.f, row, grp * (D / 2), D / 2, a.scale, n == 0);
+    stage_row<F32OUT>(sK + GB, tdV + lane_base, 0u, 0.f, row, grp * (D / 2), D / 2, 1.f, n == 0);
     fence_async_smem();
     named_bar(1, 256);
     if (tid == 128) {
@@ -582,6 +633,10 @@ struct WsLayout {
   int32_t* lists;
   int32_t* order;
   unsigned* bitmap;
+  char* Q16;
+  char* K16;
+  char* V16;
+  char* dO16;
   size_t bytes;
 };
 
@@ -603,14 +658,96 @@ WsLayout ws_layout(const Prob& p, void* base) {
   w.lists = reinterpret_cast<int32_t*>(take(bh * nb * p.k * 4));
   w.order = reinterpret_cast<int32_t*>(take(bh * nb * 4));
   w.bitmap = reinterpret_cast<unsigned*>(take(bh * nb * words * 4));
+  w.Q16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
+  w.K16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
+  w.V16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
+  w.dO16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
   w.bytes = off;
   return w;
 }
 
+BwdArgs make_args(const Prob& p, const WsLayout& w, const int32_t* idx, unsigned* status, int b) {
+  BwdArgs a;
+  a.g = p.g;
+  a.Hh = p.Hh;
+  a.k = p.k;
+  a.b = b;
+  a.N = p.N;
+  a.scale = p.scale;
+  a.scale_log2 = p.scale * kLog2e;
+  a.idx = idx;
+  a.Dv = w.Dv;
+  a.L2v = w.L2v;
+  a.offsets = w.offsets;
+  a.lists = w.lists;
+  a.order = w.order;
+  a.status = status;
+  return a;
+}
+
+bool token_map(CUtensorMap* m, const Prob& p, const void* base, int b, TokType t) {
+  const size_t es = t == kTokF32 ? 4 : 2;
+  const char* x = static_cast<const char*>(base) + (size_t)b * p.N * p.Hh * p.d * es;
+  const Geom& g = p.g;
+  return make_token_map(m, x, t, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw);
+}
+
 template <int D, bool F32OUT>
-cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
-                       const void* dO, const int32_t* idx, void* dQ, void* dK, void* dV, void* ws, cudaStream_t st) {
+cudaError_t launch_dq(const Prob& p, const void* V, const void* dO, const int32_t* idx, void* dQ, void* ws,
+                      cudaStream_t st) {
   using C = Cfg<D>;
+  WsLayout w = ws_layout(p, ws);
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  const size_t smem = 1024 + (size_t)C::TILE * (2 + 2 * C::ST) + 8 * (4 + 2 * C::ST) + 1024 + 64;
+  cudaError_t e = cudaFuncSetAttribute(dq_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const TokType gt = F32OUT ? kTokF32 : kTokBF16;
+  for (int b = 0; b < p.B; ++b) {
+    CUtensorMap mQ, mK, mV, mdO, mdQ;
+    if (!token_map(&mQ, p, w.Q16, b, kTokF16) || !token_map(&mK, p, w.K16, b, kTokF16) ||
+        !token_map(&mV, p, w.V16, b, kTokF16) || !token_map(&mdO, p, w.dO16, b, kTokF16) ||
+        !token_map(&mdQ, p, dQ, b, gt))
+      return cudaErrorInvalidValue;
+    dq_kernel<D, F32OUT><<<dim3(p.g.nb, p.Hh), kThreads, smem, st>>>(mQ, mK, mV, mdO, mdQ,
+                                                                     make_args(p, w, idx, status, b));
+    note_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <int D, bool F32OUT>
+cudaError_t launch_dkdv(const Prob& p, const void* V, const void* dO, void* dK, void* dV, void* ws, cudaStream_t st) {
+  using C = Cfg<D>;
+  WsLayout w = ws_layout(p, ws);
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  const size_t smem = 1024 + (size_t)C::TILE * 2 + (size_t)C::ST * (2 * C::TILE + 1024) + 8 * (4 + 2 * C::ST) + 64;
+  cudaError_t e =
+      cudaFuncSetAttribute(dkdv_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const TokType gt = F32OUT ? kTokF32 : kTokBF16;
+  for (int b = 0; b < p.B; ++b) {
+    CUtensorMap mQ, mK, mV, mdO, mdK, mdV;
+    if (!token_map(&mQ, p, w.Q16, b, kTokF16) || !token_map(&mK, p, w.K16, b, kTokF16) ||
+        !token_map(&mV, p, w.V16, b, kTokF16) || !token_map(&mdO, p, w.dO16, b, kTokF16) ||
+        !token_map(&mdK, p, dK, b, gt) || !token_map(&mdV, p, dV, b, gt))
+      return cudaErrorInvalidValue;
+    dkdv_kernel<D, F32OUT><<<dim3(p.g.nb, p.Hh), kThreads, smem, st>>>(mQ, mK, mV, mdO, mdK, mdV,
+                                                                       make_args(p, w, nullptr, status, b));
+    note_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t bwd_ws_tc(const Prob& p) { return ws_layout(p, nullptr).bytes; }
+
+cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O,
+                           const float* LSE, const void* dO, const int32_t* idx, void* ws, cudaStream_t st) {
   const Geom& g = p.g;
   WsLayout w = ws_layout(p, ws);
   unsigned* status = status_ptr();
@@ -626,68 +763,37 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   csr_count_kernel<<<(int)((bhn + 255) / 256), 256, 0, st>>>(w.bitmap, g.nb, words, bhn, w.counts);
   csr_scan_kernel<<<p.B * p.Hh, 1024, g.nb * sizeof(int32_t), st>>>(w.counts, g.nb, w.offsets, w.order);
   csr_fill_kernel<<<(int)((bhn + 255) / 256), 256, 0, st>>>(w.bitmap, w.offsets, g.nb, p.k, words, bhn, w.lists);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-  const size_t smem_dq = 1024 + (size_t)C::TILE * (2 + 2 * C::ST) + 8 * (4 + 2 * C::ST) + 64;
-  const size_t smem_dkdv = 1024 + (size_t)C::TILE * 2 + (size_t)C::ST * (2 * C::TILE + 1024) + 8 * (4 + 2 * C::ST) + 64;
-  if ((e = cudaFuncSetAttribute(dq_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_dq)) !=
-      cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(dkdv_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem_dkdv)) != cudaSuccess)
-    return e;
-  const size_t per_batch = (size_t)p.N * p.Hh * p.d * 2;
-  const size_t per_batch_g = (size_t)p.N * p.Hh * p.d * (F32OUT ? 4 : 2);
-  const int ges = F32OUT ? 4 : 2;
+  const long long n8 = (long long)p.B * p.N * p.Hh * p.d / 8;
+  const int cb = (int)std::min<long long>((n8 + 255) / 256, 152LL * 16);
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(Q), reinterpret_cast<uint4*>(w.Q16), n8);
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(K), reinterpret_cast<uint4*>(w.K16), n8);
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(V), reinterpret_cast<uint4*>(w.V16), n8);
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(dO), reinterpret_cast<uint4*>(w.dO16), n8);
   for (int b = 0; b < p.B; ++b) {
-    auto at = [&](const void* x, size_t pb) { return static_cast<const char*>(x) + b * pb; };
-    pre_kernel<D><<<dim3(g.nb, p.Hh), 128, 0, st>>>(
-        g, p.Hh, p.N, b, static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), LSE, w.Dv, w.L2v);
-    CUtensorMap mQ, mK, mV, mdO, mdQ, mdK, mdV;
-    if (!make_token_map(&mQ, at(Q, per_batch), 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mK, at(K, per_batch), 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mV, at(V, per_batch), 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mdO, at(dO, per_batch), 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mdQ, at(dQ, per_batch_g), ges, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mdK, at(dK, per_batch_g), ges, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mdV, at(dV, per_batch_g), ges, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw))
-      return cudaErrorInvalidValue;
-    BwdArgs a;
-    a.g = g;
-    a.Hh = p.Hh;
-    a.k = p.k;
-    a.b = b;
-    a.N = p.N;
-    a.scale = p.scale;
-    a.scale_log2 = p.scale * kLog2e;
-    a.idx = idx;
-    a.Dv = w.Dv;
-    a.L2v = w.L2v;
-    a.offsets = w.offsets;
-    a.lists = w.lists;
-    a.order = w.order;
-    a.status = status;
-    dim3 grid(g.nb, p.Hh);
-    dq_kernel<D, F32OUT><<<grid, kThreads, smem_dq, st>>>(mQ, mK, mV, mdO, mdQ, a);
-    dkdv_kernel<D, F32OUT><<<grid, kThreads, smem_dkdv, st>>>(mQ, mK, mV, mdO, mdK, mdV, a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (p.d == 64)
+      pre_kernel<64><<<dim3(g.nb, p.Hh), 128, 0, st>>>(g, p.Hh, p.N, b, static_cast<const __nv_bfloat16*>(O),
+                                                       static_cast<const __nv_bfloat16*>(dO), LSE, w.Dv, w.L2v);
+    else
+      pre_kernel<128><<<dim3(g.nb, p.Hh), 128, 0, st>>>(g, p.Hh, p.N, b, static_cast<const __nv_bfloat16*>(O),
+                                                        static_cast<const __nv_bfloat16*>(dO), LSE, w.Dv, w.L2v);
   }
-  return cudaSuccess;
+  note_launches(8 + p.B);
+  return cudaGetLastError();
 }
 
-}  // namespace
+cudaError_t bwd_dq_tc(const Prob& p, const void* V, const void* dO, const int32_t* idx, void* dQ, int grad_dtype,
+                      void* ws, cudaStream_t st) {
+  const bool f32 = grad_dtype == SDA_F32;
+  if (p.d == 64) return f32 ? launch_dq<64, true>(p, V, dO, idx, dQ, ws, st) : launch_dq<64, false>(p, V, dO, idx, dQ, ws, st);
+  return f32 ? launch_dq<128, true>(p, V, dO, idx, dQ, ws, st) : launch_dq<128, false>(p, V, dO, idx, dQ, ws, st);
+}
 
-size_t bwd_ws_tc(const Prob& p) { return ws_layout(p, nullptr).bytes; }
-
-cudaError_t bwd_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
-                   const void* dO, const int32_t* idx, void* dQ, void* dK, void* dV, int grad_dtype, void* ws,
-                   cudaStream_t st) {
+cudaError_t bwd_dkdv_tc(const Prob& p, const void* V, const void* dO, void* dK, void* dV, int grad_dtype, void* ws,
+                        cudaStream_t st) {
   const bool f32 = grad_dtype == SDA_F32;
   if (p.d == 64)
-    return f32 ? launch_bwd<64, true>(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, ws, st)
-               : launch_bwd<64, false>(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, ws, st);
-  return f32 ? launch_bwd<128, true>(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, ws, st)
-             : launch_bwd<128, false>(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, ws, st);
+    return f32 ? launch_dkdv<64, true>(p, V, dO, dK, dV, ws, st) : launch_dkdv<64, false>(p, V, dO, dK, dV, ws, st);
+  return f32 ? launch_dkdv<128, true>(p, V, dO, dK, dV, ws, st) : launch_dkdv<128, false>(p, V, dO, dK, dV, ws, st);
 }
 
 }  // namespace sda

@@ -347,10 +347,10 @@ cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* 
     const char* v = static_cast<const char*>(V) + b * per_batch;
     char* o = static_cast<char*>(O) + b * per_batch;
     const Geom& g = p.g;
-    if (!make_token_map(&mQ, q, 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mK, k, 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mV, v, 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mO, o, 2, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw))
+    if (!make_token_map(&mQ, q, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
+        !make_token_map(&mK, k, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
+        !make_token_map(&mV, v, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
+        !make_token_map(&mO, o, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw))
       return cudaErrorInvalidValue;
     FwdArgs a;
     a.g = g;
@@ -367,6 +367,7 @@ cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* 
     a.status = status;
     dim3 grid(g.nb, p.Hh);
     fwd_tc_kernel<D><<<grid, kThreads, smem, st>>>(mQ, mK, mV, mO, a);
+    note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -33,6 +33,8 @@ struct MergeArgs {
 
 // Device status word of the current device (see status.cu).
 unsigned* status_ptr();
+// Count kernels launched by the library (reported by sda_kernel_launch_count).
+void note_launches(int n);
 
 // ---- merge.cu
 cudaError_t launch_merge(const MergeArgs& a, int dtype, cudaStream_t st);
@@ -44,15 +46,18 @@ cudaError_t predict_f32(const Prob& p, const float* Q, const float* K, const flo
 cudaError_t fwd_f32(const Prob& p, const float* Q, const float* K, const float* V, const int32_t* idx,
                     int kb_begin, int kb_end, const uint8_t* qb_active, float* O, float* LSE, cudaStream_t st);
 size_t bwd_ws_f32(const Prob& p);
-cudaError_t bwd_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* O,
-                    const float* LSE, const float* dO, const int32_t* idx, float* dQ, float* dK, float* dV,
-                    void* ws, cudaStream_t st);
+cudaError_t bwd_prepare_f32(const Prob& p, const float* O, const float* dO, void* ws, cudaStream_t st);
+cudaError_t bwd_dq_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
+                       const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st);
+cudaError_t bwd_dkdv_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
+                         const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st);
 
 // ---- tensor maps (tmap.cu)
-// 5-D map over a [.., T, H, W, heads, d] bf16 or fp32 tensor of one batch
-// entry; box = (64B-or-128B of d) x 1 head x bw x bh x bt with 128B swizzle.
-bool make_token_map(CUtensorMap* m, const void* base, int dtype_bytes, int T, int H, int W, int Hh, int d,
-                    int bt, int bh, int bw);
+// 5-D map over a [T, H, W, heads, d] tensor of one batch entry; box = 128
+// bytes of d x 1 head x bw x bh x bt tokens, 128B swizzle.
+enum TokType { kTokBF16 = 0, kTokF16 = 1, kTokF32 = 2 };
+bool make_token_map(CUtensorMap* m, const void* base, TokType t, int T, int H, int W, int Hh, int d, int bt, int bh,
+                    int bw);
 
 // ---- predict_tc.cu (bf16 problems)
 size_t predict_ws_tc(const Prob& p);
@@ -64,10 +69,16 @@ cudaError_t fwd_tc(const Prob& p, const void* Q, const void* K, const void* V, c
                    int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st);
 
 // ---- attn_bwd_tc.cu
+// Backward in three phases sharing the workspace, in this order: prepare
+// (block-map transpose, D and LSE rows, fp16 copies of Q, K, V, dO), dQ (also
+// writes the exact D rows), dK/dV.
 size_t bwd_ws_tc(const Prob& p);
-cudaError_t bwd_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
-                   const void* dO, const int32_t* idx, void* dQ, void* dK, void* dV, int grad_dtype, void* ws,
-                   cudaStream_t st);
+cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O,
+                           const float* LSE, const void* dO, const int32_t* idx, void* ws, cudaStream_t st);
+cudaError_t bwd_dq_tc(const Prob& p, const void* V, const void* dO, const int32_t* idx, void* dQ, int grad_dtype,
+                      void* ws, cudaStream_t st);
+cudaError_t bwd_dkdv_tc(const Prob& p, const void* V, const void* dO, void* dK, void* dV, int grad_dtype, void* ws,
+                        cudaStream_t st);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

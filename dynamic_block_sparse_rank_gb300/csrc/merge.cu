@@ -110,6 +110,7 @@ cudaError_t launch_ns(const MergeArgs& a, cudaStream_t st) {
   while (lpr < nvec && lpr < 32) lpr <<= 1;
   dim3 grid((a.N + kRowsPerCta - 1) / kRowsPerCta, a.Hh, a.B);
   merge_kernel<T, NS><<<grid, kThreads, 0, st>>>(a, lpr);
+  note_launches(1);
   return cudaGetLastError();
 }
 

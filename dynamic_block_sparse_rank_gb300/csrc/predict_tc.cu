@@ -314,6 +314,7 @@ cudaError_t launch_predict(const Prob& p, const void* Q, const void* K, const vo
     a.b = b;
     score_kernel<R><<<sg, kScoreThreads, ssmem, st>>>(a);
   }
+  note_launches(3 * p.B);
   return cudaGetLastError();
 }
 

@@ -158,13 +158,27 @@ __global__ void fwd_f32_kernel(Geom g, int Hh, int d, int k, float scale, const 
   LSE[((long long)b * Hh + h) * N + n] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
-// dQ for each query row; also writes D_i = dO_i . O_i to Dbuf [B, Hh, N].
+// D_i = dO_i . O_i for every token row, into Dbuf [B, Hh, N].
+__global__ void bwd_pre_f32_kernel(long long rows, int Hh, long long N, int d, const float* __restrict__ O,
+                                   const float* __restrict__ dO, float* __restrict__ Dbuf) {
+  for (long long r = blockIdx.x * (long long)blockDim.x + threadIdx.x; r < rows; r += (long long)gridDim.x * blockDim.x) {
+    // r enumerates (b, n, h) in memory order
+    const int h = (int)(r % Hh);
+    const long long bn = r / Hh;
+    const long long b = bn / N, n = bn % N;
+    float acc = 0.f;
+    for (int c = 0; c < d; ++c) acc = fmaf(dO[r * d + c], O[r * d + c], acc);
+    Dbuf[(b * Hh + h) * N + n] = acc;
+  }
+}
+
+// dQ for each query row.
 template <int DM>
 __global__ void bwd_dq_f32_kernel(Geom g, int Hh, int d, int k, float scale, const float* __restrict__ Q,
                                   const float* __restrict__ K, const float* __restrict__ V,
-                                  const float* __restrict__ O, const float* __restrict__ LSE,
-                                  const float* __restrict__ dO, const int32_t* __restrict__ idx,
-                                  float* __restrict__ dQ, float* __restrict__ Dbuf, int b) {
+                                  const float* __restrict__ LSE, const float* __restrict__ dO,
+                                  const int32_t* __restrict__ idx, float* __restrict__ dQ,
+                                  const float* __restrict__ Dbuf, int b) {
   extern __shared__ float smem[];
   const int I = blockIdx.x, h = blockIdx.y;
   float* ks = smem;
@@ -184,10 +198,9 @@ __global__ void bwd_dq_f32_kernel(Geom g, int Hh, int d, int k, float scale, con
       q[c] = c < d ? Q[off + c] : 0.f;
       go[c] = c < d ? dO[off + c] : 0.f;
       dq[c] = 0.f;
-      if (c < d) Di = fmaf(go[c], O[off + c], Di);
     }
     lse = LSE[((long long)b * Hh + h) * N + n];
-    Dbuf[((long long)b * Hh + h) * N + n] = Di;
+    Di = Dbuf[((long long)b * Hh + h) * N + n];
   }
   for (int s = 0; s < n_sel; ++s) {
     const int J = sel[s];
@@ -342,6 +355,7 @@ cudaError_t predict_f32(const Prob& p, const float* Q, const float* K, const flo
   }
   dim3 grid(p.g.nb, p.B * p.Hh);
   scores_topk_f32_kernel<<<grid, 256, smem, st>>>(p.g, p.Hh, p.r, p.k, qt, kt, idx, score);
+  note_launches(3);
   return cudaGetLastError();
 }
 
@@ -359,6 +373,7 @@ static cudaError_t fwd_f32_t(const Prob& p, const float* Q, const float* K, cons
   for (int b = 0; b < p.B; ++b)
     fwd_f32_kernel<DM><<<grid, threads_for(p.g.bs), smem, st>>>(p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, idx,
                                                                 kb_begin, kb_end, qb_active, O, LSE, b);
+  note_launches(p.B);
   return cudaGetLastError();
 }
 
@@ -370,37 +385,56 @@ cudaError_t fwd_f32(const Prob& p, const float* Q, const float* K, const float* 
 
 size_t bwd_ws_f32(const Prob& p) { return align_up((size_t)p.B * p.Hh * p.N * sizeof(float), 256); }
 
-template <int DM>
-static cudaError_t bwd_f32_t(const Prob& p, const float* Q, const float* K, const float* V, const float* O,
-                             const float* LSE, const float* dO, const int32_t* idx, float* dQ, float* dK, float* dV,
-                             void* ws, cudaStream_t st) {
-  float* Dbuf = static_cast<float*>(ws);
-  size_t smem1 = (size_t)2 * kChunk * p.d * sizeof(float) + (kChunk + p.k) * sizeof(int);
-  size_t smem2 = (size_t)2 * kChunk * p.d * sizeof(float) + 3 * kChunk * sizeof(float) + p.g.nb * sizeof(int);
-  cudaError_t e;
-  if (smem1 > 48 * 1024 &&
-      (e = cudaFuncSetAttribute(bwd_dq_f32_kernel<DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1)) !=
-          cudaSuccess)
-    return e;
-  if (smem2 > 48 * 1024 &&
-      (e = cudaFuncSetAttribute(bwd_dkdv_f32_kernel<DM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem2)) != cudaSuccess)
-    return e;
-  dim3 grid(p.g.nb, p.Hh);
-  for (int b = 0; b < p.B; ++b) {
-    bwd_dq_f32_kernel<DM><<<grid, threads_for(p.g.bs), smem1, st>>>(p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, O, LSE,
-                                                                   dO, idx, dQ, Dbuf, b);
-    bwd_dkdv_f32_kernel<DM><<<grid, threads_for(p.g.bs), smem2, st>>>(p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, LSE,
-                                                                     dO, idx, Dbuf, dK, dV, b);
-  }
+cudaError_t bwd_prepare_f32(const Prob& p, const float* O, const float* dO, void* ws, cudaStream_t st) {
+  const long long rows = (long long)p.B * p.N * p.Hh;
+  const int blocks = (int)std::min<long long>((rows + 255) / 256, 152LL * 32);
+  bwd_pre_f32_kernel<<<blocks, 256, 0, st>>>(rows, p.Hh, p.N, p.d, O, dO, static_cast<float*>(ws));
+  note_launches(1);
   return cudaGetLastError();
 }
 
-cudaError_t bwd_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* O,
-                    const float* LSE, const float* dO, const int32_t* idx, float* dQ, float* dK, float* dV,
-                    void* ws, cudaStream_t st) {
-  if (p.d <= 64) return bwd_f32_t<64>(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, ws, st);
-  return bwd_f32_t<128>(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, ws, st);
+template <int DM>
+static cudaError_t dq_f32_t(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
+                            const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st) {
+  size_t smem = (size_t)2 * kChunk * p.d * sizeof(float) + (kChunk + p.k) * sizeof(int);
+  cudaError_t e;
+  if (smem > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(bwd_dq_f32_kernel<DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+          cudaSuccess)
+    return e;
+  for (int b = 0; b < p.B; ++b)
+    bwd_dq_f32_kernel<DM><<<dim3(p.g.nb, p.Hh), threads_for(p.g.bs), smem, st>>>(
+        p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, LSE, dO, idx, dQ, static_cast<const float*>(ws), b);
+  note_launches(p.B);
+  return cudaGetLastError();
+}
+
+template <int DM>
+static cudaError_t dkdv_f32_t(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
+                              const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st) {
+  size_t smem = (size_t)2 * kChunk * p.d * sizeof(float) + 3 * kChunk * sizeof(float) + p.g.nb * sizeof(int);
+  cudaError_t e;
+  if (smem > 48 * 1024 &&
+      (e = cudaFuncSetAttribute(bwd_dkdv_f32_kernel<DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+          cudaSuccess)
+    return e;
+  for (int b = 0; b < p.B; ++b)
+    bwd_dkdv_f32_kernel<DM><<<dim3(p.g.nb, p.Hh), threads_for(p.g.bs), smem, st>>>(
+        p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, LSE, dO, idx, static_cast<const float*>(ws), dK, dV, b);
+  note_launches(p.B);
+  return cudaGetLastError();
+}
+
+cudaError_t bwd_dq_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
+                       const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st) {
+  if (p.d <= 64) return dq_f32_t<64>(p, Q, K, V, LSE, dO, idx, dQ, ws, st);
+  return dq_f32_t<128>(p, Q, K, V, LSE, dO, idx, dQ, ws, st);
+}
+
+cudaError_t bwd_dkdv_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
+                         const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st) {
+  if (p.d <= 64) return dkdv_f32_t<64>(p, Q, K, V, LSE, dO, idx, dK, dV, ws, st);
+  return dkdv_f32_t<128>(p, Q, K, V, LSE, dO, idx, dK, dV, ws, st);
 }
 
 }  // namespace sda

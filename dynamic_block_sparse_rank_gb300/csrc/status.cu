@@ -1,9 +1,15 @@
 // Device status latch: one word per device that kernels of this library set
 // (atomicOr) when a bounded wait runs out.  sda_get_device_status reads and
 // clears it.
+#include <atomic>
+
 #include "internal.h"
 
 namespace sda {
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 __device__ unsigned g_status_word;
 
@@ -33,3 +39,5 @@ extern "C" sda_status sda_get_device_status(void* stream) {
   }
   return SDA_OK;
 }
+
+extern "C" unsigned long long sda_kernel_launch_count(void) { return sda::g_launches.load(std::memory_order_relaxed); }

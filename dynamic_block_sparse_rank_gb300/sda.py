@@ -18,7 +18,8 @@ SDA_F32, SDA_BF16 = 0, 1
 SDA_OP_PREDICT, SDA_OP_BWD = 0, 1
 
 EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_attn_fwd", "sda_attn_bwd",
-           "sda_merge_states", "sda_get_device_status", "sda_status_string")
+           "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_merge_states",
+           "sda_get_device_status", "sda_kernel_launch_count", "sda_status_string")
 
 
 class SdaError(RuntimeError):
@@ -51,12 +52,18 @@ def lib() -> ctypes.CDLL:
         L.sda_predict_blocks.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.sda_attn_fwd.argtypes = [pr, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
         L.sda_attn_bwd.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+        L.sda_attn_bwd_prepare.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sda_attn_bwd_dq.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+        L.sda_attn_bwd_dkdv.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
+        L.sda_kernel_launch_count.argtypes = []
+        L.sda_kernel_launch_count.restype = ctypes.c_ulonglong
         L.sda_merge_states.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i32, i32, i32, vp, vp, vp]
         L.sda_get_device_status.argtypes = [vp]
         L.sda_status_string.argtypes = [i32]
         L.sda_status_string.restype = ctypes.c_char_p
-        for name in EXPORTS[:-1]:
-            getattr(L, name).restype = i32
+        for name in EXPORTS:
+            if name not in ("sda_status_string", "sda_kernel_launch_count"):
+                getattr(L, name).restype = i32
         _lib = L
     return _lib
 
@@ -140,6 +147,29 @@ def sda_attn_bwd(p, Q, K, V, O, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, 
     _check(lib().sda_attn_bwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO),
                               _ptr(block_idx), _ptr(dQ), _ptr(dK), _ptr(dV), int(gd), _wsptr(ws), _nbytes(ws),
                               _stream(stream)), "sda_attn_bwd")
+
+
+def sda_attn_bwd_prepare(p, Q, K, V, O, LSE, dO, block_idx, ws, stream=None):
+    _check(lib().sda_attn_bwd_prepare(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO),
+                                      _ptr(block_idx), _wsptr(ws), _nbytes(ws), _stream(stream)),
+           "sda_attn_bwd_prepare")
+
+
+def sda_attn_bwd_dq(p, Q, K, V, LSE, dO, block_idx, dQ, grad_dtype, ws, stream=None):
+    gd = {"f32": SDA_F32, "bf16": SDA_BF16}.get(grad_dtype, grad_dtype)
+    _check(lib().sda_attn_bwd_dq(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(LSE), _ptr(dO), _ptr(block_idx),
+                                 _ptr(dQ), int(gd), _wsptr(ws), _nbytes(ws), _stream(stream)), "sda_attn_bwd_dq")
+
+
+def sda_attn_bwd_dkdv(p, Q, K, V, LSE, dO, block_idx, dK, dV, grad_dtype, ws, stream=None):
+    gd = {"f32": SDA_F32, "bf16": SDA_BF16}.get(grad_dtype, grad_dtype)
+    _check(lib().sda_attn_bwd_dkdv(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(LSE), _ptr(dO),
+                                   _ptr(block_idx), _ptr(dK), _ptr(dV), int(gd), _wsptr(ws), _nbytes(ws),
+                                   _stream(stream)), "sda_attn_bwd_dkdv")
+
+
+def sda_kernel_launch_count() -> int:
+    return int(lib().sda_kernel_launch_count())
 
 
 def sda_merge_states(O_parts, LSE_parts, B, N, heads, head_dim, dtype, O_out, LSE_out, stream=None):

@@ -117,6 +117,33 @@ sda_status sda_attn_bwd(const sda_problem* p, const void* Q, const void* K, cons
                         void* dQ, void* dK, void* dV, int grad_dtype, void* ws, size_t ws_bytes,
                         void* stream);
 
+/* Step 2b in phases.  sda_attn_bwd is exactly these three calls, in this
+ * order, on one workspace; they are exposed so that a caller can time them or
+ * interleave other work between them.  All three take the same problem,
+ * inputs and workspace.
+ *   prepare: transposes the block map (for every key block, the query blocks
+ *            that kept it, ascending), computes D~_i = dO_i . O_i from the
+ *            stored O and the LSE rows in tile order, and (tensor-core path)
+ *            fp16 copies of Q, K, V and dO.
+ *   dq:      dQ = scale * sum_j dS_ij k_j over each query block's kept blocks;
+ *            it forms D_i = sum_j P_ij dP_ij exactly in the same pass (the
+ *            stored bf16 O would carry its rounding into D~) and writes it
+ *            back for the next phase.
+ *   dkdv:    dK = scale * sum_i dS_ij q_i and dV = sum_i P_ij dO_i over the
+ *            query blocks that kept each key block.
+ * On the tensor-core path every product runs on fp16 operands (P and dS are
+ * rounded to fp16), so Q, K, V, dO and dP - D must stay inside fp16's range
+ * (|x| < 65504). */
+sda_status sda_attn_bwd_prepare(const sda_problem* p, const void* Q, const void* K, const void* V, const void* O,
+                                const float* LSE, const void* dO, const int32_t* block_idx, void* ws,
+                                size_t ws_bytes, void* stream);
+sda_status sda_attn_bwd_dq(const sda_problem* p, const void* Q, const void* K, const void* V, const float* LSE,
+                           const void* dO, const int32_t* block_idx, void* dQ, int grad_dtype, void* ws,
+                           size_t ws_bytes, void* stream);
+sda_status sda_attn_bwd_dkdv(const sda_problem* p, const void* Q, const void* K, const void* V, const float* LSE,
+                             const void* dO, const int32_t* block_idx, void* dK, void* dV, int grad_dtype, void* ws,
+                             size_t ws_bytes, void* stream);
+
 /* Step 3: LSE merge of n_states partial states (DiTango state reuse).
  *   O_parts[s]   device pointer, [B, N, heads, d] (dtype)
  *   LSE_parts[s] device pointer, [B, heads, N] fp32
@@ -135,6 +162,10 @@ sda_status sda_get_device_status(void* stream);
 
 /* Static description of a status code. */
 const char* sda_status_string(sda_status s);
+
+/* Host only.  Number of CUDA kernels the library has launched in this process
+ * (all devices, all calls); a caller can difference it around a region. */
+unsigned long long sda_kernel_launch_count(void);
 
 #ifdef __cplusplus
 }
