@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of one training step of dynamic block-sparse attention on GB300.
+
+A step is the whole path on the 524,288-token workload (batch 1, 8 heads,
+grid 32 x 128 x 128, d = 128, bf16, 2x8x8 tiles, rank 32, keep 0.05 = 204 of
+4,096 key blocks per query block): low-rank predictor + top-k, block-sparse
+forward, backward (prepare, dQ, dK/dV; fp32 gradients).  Inputs are the
+seeded synthetic generator's arrays, resident in HBM before timing; each
+input tensor (1.07 GB) is larger than L2, so no flush is needed.
+
+The reported metric is sparse-attention TFLOP/s: the algorithmic forward +
+backward FLOPs of the kept blocks (4 d and 10 d per kept (query, key) token
+pair) divided by the step time, which also contains the predictor.  The same
+line carries tokens/s, per-phase times, the roofline of the dominant kernel,
+the end-to-end figure through host buffers, clocks, and the CPU oracle timed
+on a bounded sample (rank 0, one GPU only).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+With N > 1 (torchrun), every rank runs an independent replica of the step
+(the path has no exchange step in this build): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from dynamic_block_sparse_rank_gb300 import inputs  # noqa: E402
+
+WORKLOAD = "train_524k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the CPU oracle sample")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- work counting
+def block_sizes(wl) -> np.ndarray:
+    nT, nH, nW = wl.grid
+    it, ih, iw = np.meshgrid(np.arange(nT), np.arange(nH), np.arange(nW), indexing="ij")
+    st = np.minimum(wl.bt, wl.T - it * wl.bt)
+    sh = np.minimum(wl.bh, wl.H - ih * wl.bh)
+    sw = np.minimum(wl.bw, wl.W - iw * wl.bw)
+    return (st * sh * sw).reshape(-1).astype(np.int64)
+
+
+def kept_pairs(wl, idx: np.ndarray) -> int:
+    """Sum over (b, h, I) of |I| * sum_{J kept} |J|: the (query, key) token pairs attended."""
+    sz = block_sizes(wl)
+    per_row = sz[idx.astype(np.int64)].sum(axis=-1)  # [B, Hh, nb]
+    return int((per_row * sz[None, None, :]).sum())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        loaded = [s for s in sm if s > 0.5 * (max(mx) if mx else 1)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+def cpu_oracle_sample(wl, seconds: float) -> dict:
+    """Time the oracle (as it stands) on query blocks of head 0 until `seconds` of work are done."""
+    import oracle as orc
+
+    cores = len(os.sched_getaffinity(0))
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk"), heads=[0])
+    geom = orc.Geometry(wl.T, wl.H, wl.W, wl.bt, wl.bh, wl.bw)
+    sz = block_sizes(wl)
+    rng = np.random.default_rng(0)
+    order = rng.permutation(geom.n_blocks)
+    t0 = time.perf_counter()
+    flops = 0.0
+    done = []
+    for I in order:
+        I = int(I)
+        idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype, query_blocks=[I])
+        orc.attn_fwd(x["Q"], x["K"], x["V"], idx, geom, query_blocks=[I])
+        orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], idx, geom, query_blocks=[I])
+        flops += 14.0 * wl.d * sz[I] * sz[idx[0, 0, 0]].sum()
+        done.append(I)
+        if time.perf_counter() - t0 > seconds and len(done) >= 2:
+            break
+    dt = time.perf_counter() - t0
+    return {"tflops": flops / dt / 1e12, "seconds": dt, "cores": cores, "cpu_count": os.cpu_count(),
+            "query_blocks": len(done),
+            "sample": f"{len(done)} random query blocks of head 0 of {wl.name}: oracle predictor row "
+                      f"(scores against all {geom.n_blocks} key blocks) + forward + backward of their kept "
+                      f"blocks, fp64 NumPy"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, wl):
+    """The oracle on the host cores, each step a bounded sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, per_step)
+    res = [cpu_oracle_sample(wl, per_step) for _ in range(args.steps)]
+    tfl = statistics.median(r["tflops"] for r in res)
+    tokens = wl.B * wl.N
+    line = {"impl": "reference", "metric": "sparse attn fwd+bwd TFLOP/s (step incl. predictor), 524,288 tokens",
+            "value": tfl, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Fourier-field Q/K + Gaussian V, dO)",
+            "config": {"workload": wl.name, "tokens": tokens, "grid": [wl.T, wl.H, wl.W], "heads": wl.heads,
+                       "head_dim": wl.d, "tile": [wl.bt, wl.bh, wl.bw], "rank": wl.rank, "keep": wl.keep,
+                       "k": wl.k, "sample": res[0]["sample"]},
+            "cpu_baseline": {"value": tfl, "unit": "TFLOP/s", "cores": res[0]["cores"], "kind": "oracle",
+                             "sample": res[0]["sample"]},
+            "e2e": {"value": tfl, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- native arm
+def main():
+    args = parse()
+    wl = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+
+    from dynamic_block_sparse_rank_gb300 import build, sda
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if not os.path.exists(sda.LIB_PATH):
+        build.build()
+    sda.lib()
+
+    # ---- inputs (host generation, then resident in HBM)
+    t_gen = time.perf_counter()
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk"))
+    t_gen = time.perf_counter() - t_gen
+    dev = torch.device("cuda", local)
+    host_bf16 = {n: torch.from_numpy(x[n]).to(torch.bfloat16) for n in ("Q", "K", "V", "dO", "Wq", "Wk")}
+    del x
+    d_in = {n: t.to(dev) for n, t in host_bf16.items()}
+    Q, K, V, dO, Wq, Wk = (d_in[n] for n in ("Q", "K", "V", "dO", "Wq", "Wk"))
+    p = sda.problem_from_workload(wl)
+    nb, k = sda.sda_num_blocks(p)
+    idx = torch.empty((wl.B, wl.heads, nb, k), dtype=torch.int32, device=dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device=dev)
+    dQ, dK, dV = (torch.empty(Q.shape, dtype=torch.float32, device=dev) for _ in range(3))
+    ws_p = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICT), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        sda.sda_predict_blocks(p, Q, K, Wq, Wk, idx, None, ws_p, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        sda.sda_attn_fwd(p, Q, K, V, idx, O, LSE, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        sda.sda_attn_bwd_prepare(p, Q, K, V, O, LSE, dO, idx, ws_b, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        sda.sda_attn_bwd_dq(p, Q, K, V, LSE, dO, idx, dQ, "f32", ws_b, stream)
+        if ev is not None:
+            ev[4].record(stream)
+        sda.sda_attn_bwd_dkdv(p, Q, K, V, LSE, dO, idx, dK, dV, "f32", ws_b, stream)
+        if ev is not None:
+            ev[5].record(stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if sda.sda_get_device_status(stream.cuda_stream) != sda.SDA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+    pairs = kept_pairs(wl, idx.cpu().numpy())
+    f_fwd = 4.0 * wl.d * pairs
+    f_bwd = 10.0 * wl.d * pairs
+    f_dkdv = 8.0 * wl.d * pairs
+    f_dq = 2.0 * wl.d * pairs
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = sda.sda_kernel_launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    launches = sda.sda_kernel_launch_count() - launches0
+    ms = start.elapsed_time(end) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    phase_names = ["predict", "fwd", "bwd_prepare", "bwd_dq", "bwd_dkdv"]
+    phase_ms = {n: statistics.median(e[i].elapsed_time(e[i + 1]) for e in evs) for i, n in enumerate(phase_names)}
+    status = sda.sda_get_device_status(stream.cuda_stream)
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: t.pin_memory() for n, t in host_bf16.items()}
+        out_host = [torch.empty(dQ.shape, dtype=torch.float32).pin_memory() for _ in range(3)]
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in out_host)
+
+        def e2e_step():
+            for n, t in pin.items():
+                d_in[n].copy_(t, non_blocking=True)
+            step()
+            for h, g in zip(out_host, (dQ, dK, dV)):
+                h.copy_(g, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_e2e = e0.elapsed_time(e1) / args.steps
+        if dist is not None:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": world * (f_fwd + f_bwd) / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "tokens_per_s": world * wl.B * wl.N / (ms_e2e / 1e3)}
+
+    # ---- merge of partial states on the 4-partition workload's shapes (HBM-bound kernel)
+    merge = None
+    if rank == 0:
+        mw = inputs.WORKLOADS["merge_131k"]
+        n_st = mw.partitions
+        g = torch.Generator(device=dev).manual_seed(0)
+        Os = [torch.randn((1, mw.N, mw.heads, mw.d), device=dev, generator=g).to(torch.bfloat16) for _ in range(n_st)]
+        Ls = [torch.randn((1, mw.heads, mw.N), device=dev, generator=g) for _ in range(n_st)]
+        Oo, Lo = torch.empty_like(Os[0]), torch.empty_like(Ls[0])
+        for _ in range(3):
+            sda.sda_merge_states(Os, Ls, 1, mw.N, mw.heads, mw.d, "bf16", Oo, Lo, stream)
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        m0.record(stream)
+        for _ in range(reps):
+            sda.sda_merge_states(Os, Ls, 1, mw.N, mw.heads, mw.d, "bf16", Oo, Lo, stream)
+        m1.record(stream)
+        torch.cuda.synchronize()
+        mms = m0.elapsed_time(m1) / reps
+        rows = mw.N * mw.heads
+        mbytes = (n_st + 1) * rows * (2 * mw.d + 4)
+        merge = {"workload": mw.name, "states": n_st, "ms": mms, "bytes": mbytes, "gbs": mbytes / (mms / 1e3) / 1e9}
+        del Os, Ls, Oo, Lo
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    pk, pk_src = peaks()
+    tc_peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    kern = {"attn_fwd (fwd_tc_kernel)": (phase_ms["fwd"], f_fwd),
+            "attn_bwd_dkdv (dkdv_kernel)": (phase_ms["bwd_dkdv"], f_dkdv),
+            "attn_bwd_dq (dq_kernel)": (phase_ms["bwd_dq"], f_dq)}
+    dom = max(kern, key=lambda n: kern[n][0])
+    dom_ms, dom_flops = kern[dom]
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    if merge:
+        merge["frac_of_hbm_peak"] = merge["gbs"] / hbm_peak
+    attn_ms = phase_ms["fwd"] + phase_ms["bwd_prepare"] + phase_ms["bwd_dq"] + phase_ms["bwd_dkdv"]
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        c = cpu_oracle_sample(wl, args.cpu_seconds)
+        cpu = {"value": c["tflops"], "unit": "TFLOP/s", "cores": c["cores"], "kind": "oracle", "sample": c["sample"],
+               "seconds": c["seconds"]}
+    line = {
+        "metric": "sparse attn fwd+bwd TFLOP/s (step incl. predictor), 524,288 tokens",
+        "value": world * (f_fwd + f_bwd) / (ms / 1e3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded Fourier-field Q/K + Gaussian V, dO; random-init Wq, Wk)",
+        "config": {"workload": wl.name, "tokens": wl.B * wl.N, "grid": [wl.T, wl.H, wl.W], "heads": wl.heads,
+                   "head_dim": wl.d, "tile": [wl.bt, wl.bh, wl.bw], "rank": wl.rank, "keep": wl.keep, "k": k,
+                   "grad_dtype": "f32", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (1.07 GB per tensor), no flush"},
+        "tokens_per_s": world * wl.B * wl.N / (ms / 1e3),
+        "attn_only": {"ms": attn_ms, "tflops": (f_fwd + f_bwd) / (attn_ms / 1e3) / 1e12,
+                      "frac_of_peak": (f_fwd + f_bwd) / (attn_ms / 1e3) / 1e12 / tc_peak},
+        "phase_ms": phase_ms,
+        "flops": {"fwd": f_fwd, "bwd": f_bwd, "kept_pairs": pairs},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tc_peak, "traffic": None,
+                     "peak_source": f"{pk_src} bf16_tflops_sustained (fp16 and bf16 share the dense rate)"},
+        "merge": merge,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clk.summary(),
+        "gpu_launches": launches,
+        "device_status": sda.status_string(status),
+        "input_generation_s": t_gen,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

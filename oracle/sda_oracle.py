@@ -218,13 +218,15 @@ def attn_fwd(Q, K, V, idx, geom: Geometry, scale=None, kb_begin=0, kb_end=None, 
     return O, LSE
 
 
-def attn_bwd(Q, K, V, dO, idx, geom: Geometry, scale=None):
+def attn_bwd(Q, K, V, dO, idx, geom: Geometry, scale=None, query_blocks=None):
     """Gradients of block-sparse attention with the block map held fixed (reading 6).
 
     With P_ij = exp(S_ij - LSE_i) over the kept keys and D_i = dO_i . O_i:
     dV_j = sum_i P_ij dO_i, dP_ij = dO_i . v_j, dS_ij = P_ij (dP_ij - D_i),
     dQ_i = scale sum_j dS_ij k_j, dK_j = scale sum_i dS_ij q_i.
-    Returns (dQ, dK, dV), each [B, N, Hh, d] fp64.
+    query_blocks restricts the sums over i to those query blocks (idx rows
+    then follow that list); by linearity the full gradient is the sum over any
+    split of the query blocks.  Returns (dQ, dK, dV), each [B, N, Hh, d] fp64.
     """
     Q = np.asarray(Q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
@@ -235,11 +237,12 @@ def attn_bwd(Q, K, V, dO, idx, geom: Geometry, scale=None):
     dQ = np.zeros_like(Q)
     dK = np.zeros_like(K)
     dV = np.zeros_like(V)
+    qb = list(range(geom.n_blocks)) if query_blocks is None else list(query_blocks)
     for b in range(B):
         for h in range(Hh):
-            for I in range(geom.n_blocks):
+            for a, I in enumerate(qb):
                 rows = geom.tokens(I)
-                keys = _kept_keys(geom, idx[b, h, I], 0, geom.n_blocks)
+                keys = _kept_keys(geom, idx[b, h, a], 0, geom.n_blocks)
                 if len(keys) == 0:
                     continue
                 q, kk, v, do = Q[b, rows, h], K[b, keys, h], V[b, keys, h], dO[b, rows, h]

@@ -460,3 +460,17 @@ def test_generator_is_seeded_and_head_separable():
     assert abs(np.corrcoef(q, k)[0, 1] - 0.9) < 0.05
     assert abs(q.var() - 10.0) < 1.5
     assert 0.03 < np.std(g["Qp"] - g["Q"]) < 0.07
+
+
+def test_backward_is_the_sum_over_query_block_splits():
+    geom = orc.Geometry(2, 4, 6, 1, 2, 2)
+    B, Hh, d = 1, 1, 4
+    Q, K, V, dO = (_rand((B, geom.N, Hh, d), s) for s in (90, 91, 92, 93))
+    idx = _random_map(geom, B, Hh, 3, 94)
+    full = orc.attn_bwd(Q, K, V, dO, idx, geom)
+    part_a = [0, 2, 5]
+    part_b = [I for I in range(geom.n_blocks) if I not in part_a]
+    ga = orc.attn_bwd(Q, K, V, dO, idx[:, :, part_a], geom, query_blocks=part_a)
+    gb = orc.attn_bwd(Q, K, V, dO, idx[:, :, part_b], geom, query_blocks=part_b)
+    for f, a, b in zip(full, ga, gb):
+        assert np.abs(a + b - f).max() < 1e-12
