@@ -163,6 +163,31 @@ sda_status sda_get_device_status(void* stream);
 /* Static description of a status code. */
 const char* sda_status_string(sda_status s);
 
+/* sda_predict_blocks for callers that cannot allocate device memory.  The
+ * paper has no counterpart: this is a deployment convenience.
+ *
+ * Hosts that own all device memory themselves (a server that reserves one
+ * arena at start-up, a plugin whose framework forbids device allocation, a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device
+ * synchronisation) may have no buffer to pass as workspace.  This call runs
+ * the same kernels as sda_predict_blocks but takes the q~ / k~ scratch from a
+ * fixed array of SDA_NOALLOC_SCRATCH_BYTES compiled into the library, which
+ * every GPU that loads the library keeps until process exit.  The caller still
+ * passes inputs and outputs (same meaning as sda_predict_blocks); it allocates
+ * nothing itself.
+ *   - Problems whose predictor workspace (sda_workspace_size, SDA_OP_PREDICT)
+ *     exceeds SDA_NOALLOC_SCRATCH_BYTES return SDA_ERR_WORKSPACE, launching
+ *     nothing.
+ *   - The first call on a device looks up the array's device address for that
+ *     device (cudaGetSymbolAddress, with the device current); make that first
+ *     call before any stream capture.
+ *   - All calls share the one array on a device: calls that overlap on the GPU
+ *     (other streams, other threads) race on it.  Calls ordered on one stream
+ *     are safe; nothing in the array needs clearing between calls. */
+#define SDA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+sda_status sda_predict_blocks_noalloc(const sda_problem* p, const void* Q, const void* K, const void* Wq,
+                                      const void* Wk, int32_t* block_idx, float* block_score, void* stream);
+
 /* Host only.  Number of CUDA kernels the library has launched in this process
  * (all devices, all calls); a caller can difference it around a region. */
 unsigned long long sda_kernel_launch_count(void);
