@@ -1,0 +1,81 @@
+"""Run the whole path (predictor, forward, and optionally backward) on one workload.
+
+    python -m dynamic_block_sparse_rank_gb300.run_step --workload fwd_61k [--heads 10] [--backward] [--steps 1]
+
+A small driver for inspecting the kernels (e.g. under a profiler) on a chosen
+workload: inputs come from the seeded generator, every step runs all the
+calls of the path on the current stream, and the per-call times (CUDA
+events) are printed as one JSON line.  The library must be built.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import statistics
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="fwd_61k")
+    ap.add_argument("--heads", type=int, default=0, help="override the workload's head count")
+    ap.add_argument("--backward", action="store_true", help="also run the backward (always on for training workloads)")
+    ap.add_argument("--steps", type=int, default=1)
+    ap.add_argument("--warmup", type=int, default=1)
+    args = ap.parse_args()
+
+    import torch
+
+    from . import inputs, sda
+
+    wl = inputs.WORKLOADS[args.workload]
+    if args.heads:
+        wl = wl.with_(heads=args.heads)
+    backward = args.backward or wl.backward
+    names = ("Q", "K", "V", "Wq", "Wk") + (("dO",) if backward else ())
+    x = inputs.generate(wl, names=names)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    d = {n: torch.from_numpy(a).to(tdt).cuda() for n, a in x.items()}
+    p = sda.problem_from_workload(wl)
+    nb, k = sda.sda_num_blocks(p)
+    idx = torch.empty((wl.B, wl.heads, nb, k), dtype=torch.int32, device="cuda")
+    O = torch.empty_like(d["Q"])
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    ws_p = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICT), dtype=torch.uint8, device="cuda")
+    if backward:
+        grads = [torch.empty(d["Q"].shape, dtype=torch.float32, device="cuda") for _ in range(3)]
+        ws_b = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    names_t = ["predict", "fwd"] + (["bwd_prepare", "bwd_dq", "bwd_dkdv"] if backward else [])
+
+    def step(ev):
+        ev[0].record(st)
+        sda.sda_predict_blocks(p, d["Q"], d["K"], d["Wq"], d["Wk"], idx, None, ws_p, st)
+        ev[1].record(st)
+        sda.sda_attn_fwd(p, d["Q"], d["K"], d["V"], idx, O, LSE, stream=st)
+        ev[2].record(st)
+        if backward:
+            sda.sda_attn_bwd_prepare(p, d["Q"], d["K"], d["V"], O, LSE, d["dO"], idx, ws_b, st)
+            ev[3].record(st)
+            sda.sda_attn_bwd_dq(p, d["Q"], d["K"], d["V"], LSE, d["dO"], idx, grads[0], "f32", ws_b, st)
+            ev[4].record(st)
+            sda.sda_attn_bwd_dkdv(p, d["Q"], d["K"], d["V"], LSE, d["dO"], idx, grads[1], grads[2], "f32", ws_b, st)
+            ev[5].record(st)
+
+    times = {n: [] for n in names_t}
+    for s in range(args.warmup + args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        step(ev)
+        torch.cuda.synchronize()
+        if s >= args.warmup:
+            for i, n in enumerate(names_t):
+                times[n].append(ev[i].elapsed_time(ev[i + 1]))
+    status = sda.sda_get_device_status()
+    print(json.dumps({"workload": wl.name, "heads": wl.heads, "tokens": wl.N, "k": k,
+                      "ms": {n: statistics.median(v) for n, v in times.items()},
+                      "status": sda.status_string(status)}))
+    if status != sda.SDA_OK:
+        raise SystemExit(1)
+
+
+if __name__ == "__main__":
+    main()
