@@ -358,7 +358,11 @@ def main():
     pk, pk_src = peaks()
     tc_peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    kern = {"attn_fwd (fwd_tc_kernel)": (phase_ms["fwd"], f_fwd),
+    # algorithmic FLOPs per launch: predictor 2 r per token pair (all pairs of a head), forward 4 d and
+    # dK/dV 8 d per kept pair, dQ 2 d per kept pair (its S, dP and P K products are recomputation)
+    f_pred = 2.0 * wl.rank * wl.B * wl.heads * float(wl.N) ** 2
+    kern = {"predict (score_kernel; phase incl. 2 proj_kernel)": (phase_ms["predict"], f_pred),
+            "attn_fwd (fwd_tc_kernel)": (phase_ms["fwd"], f_fwd),
             "attn_bwd_dkdv (dkdv_kernel)": (phase_ms["bwd_dkdv"], f_dkdv),
             "attn_bwd_dq (dq_kernel)": (phase_ms["bwd_dq"], f_dq)}
     dom = max(kern, key=lambda n: kern[n][0])
@@ -397,6 +401,8 @@ def main():
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                      "frac": achieved / tc_peak, "traffic": None,
                      "peak_source": f"{pk_src} bf16_tflops_sustained (fp16 and bf16 share the dense rate)"},
+        "kernels": {n: {"ms": t, "tflops": f / (t / 1e3) / 1e12, "frac": f / (t / 1e3) / 1e12 / tc_peak}
+                    for n, (t, f) in kern.items()},
         "merge": merge,
         "e2e": e2e,
         "cpu_baseline": cpu,

@@ -36,6 +36,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct BwdArgs {
   Geom g;
   int Hh, k, b;
+  int all_full;  // every tile lies inside the grid (no clipped edge tiles)
   long long N;
   float scale_log2;  // softmax scale * log2(e)
   float scale;
@@ -272,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qfull = bars;
   uint64_t* kvfull = qfull + 1;       // ST
   uint64_t* kvempty = kvfull + ST;    // ST
-  uint64_t* sdpfull = kvempty + ST;   // 1
-  uint64_t* dsfull = sdpfull + 1;     // 1
-  uint64_t* drain = dsfull + 1;       // 1
+  uint64_t* sdpfull = kvempty + ST;   // 2: S/dP columns of half h are ready
+  uint64_t* dsfull = sdpfull + 2;     // 2: packed dS~ / P of half h are written
+  uint64_t* drain = dsfull + 2;       // 1
   float* dpart = reinterpret_cast<float*>(drain + 1);  // 2 x 128 partial row sums of P dP
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dpart + 256);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -288,8 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(kvfull + s, 1);
       mbar_init(kvempty + s, 1);
     }
-    mbar_init(sdpfull, 1);
-    mbar_init(dsfull, 256);
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(sdpfull + hh, 1);
+      mbar_init(dsfull + hh, 128);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -335,35 +338,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_f16(128, 128, 0, 0);  // Q K^T and dO V^T
+      // Half-tile ping-pong: S/dP are produced and consumed in two column halves
+      // (keys [0,64) and [64,128) of the block), one per compute warpgroup, so the
+      // tensor pipe works on one half while a warpgroup works on the other.
+      constexpr uint32_t idS = idesc_f16(128, 64, 0, 0);   // Q K^T and dO V^T, one 64-key half
       constexpr uint32_t idQ = idesc_f16(128, D, 0, 1);    // dS~ K and P K
       const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO), aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(qfull, 0, a.status, abort_flag);
-      for (int j = 0; ok && j < n; ++j) {
+      auto issue_sdp = [&](int j, int hh) {
         const int s = j % ST;
-        if (!mbar_wait(kvfull + s, (j / ST) & 1, a.status, abort_flag)) break;
-        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS, smem_desc(aQ + off, 16, 1024, 2), smem_desc(aK + s * C::TILE + off, 16, 1024, 2), idS, kk > 0);
+          mma_ss(tS + hh * 64, smem_desc(aQ + off, 16, 1024, 2),
+                 smem_desc(aK + s * C::TILE + off + hh * 8192, 16, 1024, 2), idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tdP, smem_desc(adO + off, 16, 1024, 2), smem_desc(aV + s * C::TILE + off, 16, 1024, 2), idS,
-                 kk > 0);
+          mma_ss(tdP + hh * 64, smem_desc(adO + off, 16, 1024, 2),
+                 smem_desc(aV + s * C::TILE + off + hh * 8192, 16, 1024, 2), idS, kk > 0);
         }
-        mma_commit(sdpfull);
-        if (!mbar_wait(dsfull, j & 1, a.status, abort_flag)) break;
-        tc_fence_after();
+        mma_commit(sdpfull + hh);
+      };
+      auto issue_dq = [&](int j, int hh) {
+        const int s = j % ST;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int q = 0; q < 4; ++q) {
+          const int kk = hh * 4 + q;
           const uint64_t bK = smem_desc(aK + s * C::TILE + kk * 2048, 16384, 1024, 2);
           mma_ts(tdQ, tS + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
           mma_ts(tPK, tdP + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
         }
+      };
+      bool ok = mbar_wait(qfull, 0, a.status, abort_flag) && mbar_wait(kvfull, 0, a.status, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0, 0);
+        issue_sdp(0, 1);
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int s = j % ST;
+        const bool more = j + 1 < n;
+        if (!mbar_wait(dsfull, j & 1, a.status, abort_flag)) break;
+        tc_fence_after();
+        issue_dq(j, 0);
+        if (more && !mbar_wait(kvfull + (j + 1) % ST, ((j + 1) / ST) & 1, a.status, abort_flag)) break;
+        tc_fence_after();
+        if (more) issue_sdp(j + 1, 0);
+        if (!mbar_wait(dsfull + 1, j & 1, a.status, abort_flag)) break;
+        tc_fence_after();
+        issue_dq(j, 1);
         mma_commit(kvempty + s);
+        if (more) issue_sdp(j + 1, 1);
       }
       mma_commit(drain);
       wait_plain(drain, 0);
@@ -378,10 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float Dt = a.Dv[tile_row];  // D~ from the stored O
     float dsum = 0.f;                 // this group's share of D = sum_j P_ij dP_ij
     for (int j = 0; j < n; ++j) {
-      if (!mbar_wait(sdpfull, j & 1, a.status, abort_flag)) break;
+      if (!mbar_wait(sdpfull + grp, j & 1, a.status, abort_flag)) break;
       tc_fence_after();
-      const int J = sel[j];
-      const bool full = block_is_full(a.g, J);
+      const bool full = a.all_full || block_is_full(a.g, sel[j]);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = grp * 64 + cc * 32;
@@ -395,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), a.scale_log2, -l2));
           float p1 = ex2(fmaf(__uint_as_float(us[2 * e + 1]), a.scale_log2, -l2));
           if (!full) {
-            if (block_row_token(a.g, J, col0 + 2 * e) < 0) p0 = 0.f;
-            if (block_row_token(a.g, J, col0 + 2 * e + 1) < 0) p1 = 0.f;
+            if (block_row_token(a.g, sel[j], col0 + 2 * e) < 0) p0 = 0.f;
+            if (block_row_token(a.g, sel[j], col0 + 2 * e + 1) < 0) p1 = 0.f;
           }
           const float dp0 = __uint_as_float(up[2 * e]), dp1 = __uint_as_float(up[2 * e + 1]);
           dsum = fmaf(p0, dp0, fmaf(p1, dp1, dsum));
@@ -408,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(dsfull);
+      mbar_arrive(dsfull + grp);
     }
     dpart[grp * 128 + row] = dsum;
     mbar_wait(drain, 0, a.status, abort_flag);
@@ -462,9 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kvfull = bars;
   uint64_t* qfull = kvfull + 1;     // ST
   uint64_t* qempty = qfull + ST;    // ST
-  uint64_t* sdpfull = qempty + ST;  // 1
-  uint64_t* pdsfull = sdpfull + 1;  // 1
-  uint64_t* drain = pdsfull + 1;    // 1
+  uint64_t* sdpfull = qempty + ST;  // 2: S^T/dP^T columns of half h are ready
+  uint64_t* pdsfull = sdpfull + 2;  // 2: packed P^T / dS^T of half h are written
+  uint64_t* drain = pdsfull + 2;    // 1
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -475,8 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(qfull + s, 1);
       mbar_init(qempty + s, 1);
     }
-    mbar_init(sdpfull, 1);
-    mbar_init(pdsfull, 256);
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(sdpfull + hh, 1);
+      mbar_init(pdsfull + hh, 128);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -527,36 +554,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idS = idesc_f16(128, 128, 0, 0);    // K Q^T and V dO^T
-      constexpr uint32_t idP = idS;
-      constexpr uint32_t idV = idesc_f16(128, D, 0, 1);      // P^T dO and dS^T Q
-      constexpr uint32_t idK = idV;
+      // Half-tile ping-pong over the query columns [0,64) / [64,128) of S^T and dP^T
+      // (one per compute warpgroup), as in dq_kernel.
+      constexpr uint32_t idS = idesc_f16(128, 64, 0, 0);     // K Q^T and V dO^T, one 64-query half
+      constexpr uint32_t idG = idesc_f16(128, D, 0, 1);      // P^T dO and dS^T Q
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aR = smem_u32(ring);
-      bool ok = mbar_wait(kvfull, 0, a.status, abort_flag);
+      auto issue_sdp = [&](int u, int hh) {
+        const uint32_t aQ = aR + (u % ST) * STAGE, adO = aQ + C::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tS + hh * 64, smem_desc(aK + off, 16, 1024, 2), smem_desc(aQ + off + hh * 8192, 16, 1024, 2), idS,
+                 kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tdP + hh * 64, smem_desc(aV + off, 16, 1024, 2), smem_desc(adO + off + hh * 8192, 16, 1024, 2),
+                 idS, kk > 0);
+        }
+        mma_commit(sdpfull + hh);
+      };
+      auto issue_grad = [&](int u, int hh) {
+        const uint32_t aQ = aR + (u % ST) * STAGE, adO = aQ + C::TILE;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int kk = hh * 4 + q;
+          mma_ts(tdV, tS + packed_col(kk), smem_desc(adO + kk * 2048, 16384, 1024, 2), idG, (u > 0 || kk > 0));
+          mma_ts(tdK, tdP + packed_col(kk), smem_desc(aQ + kk * 2048, 16384, 1024, 2), idG, (u > 0 || kk > 0));
+        }
+      };
+      bool ok = mbar_wait(kvfull, 0, a.status, abort_flag) && mbar_wait(qfull, 0, a.status, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_sdp(0, 0);
+        issue_sdp(0, 1);
+      }
       for (int u = 0; ok && u < n; ++u) {
         const int s = u % ST;
-        const uint32_t aQ = aR + s * STAGE, adO = aQ + C::TILE;
-        if (!mbar_wait(qfull + s, (u / ST) & 1, a.status, abort_flag)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS, smem_desc(aK + off, 16, 1024, 2), smem_desc(aQ + off, 16, 1024, 2), idS, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tdP, smem_desc(aV + off, 16, 1024, 2), smem_desc(adO + off, 16, 1024, 2), idP, kk > 0);
-        }
-        mma_commit(sdpfull);
+        const bool more = u + 1 < n;
         if (!mbar_wait(pdsfull, u & 1, a.status, abort_flag)) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tdV, tS + packed_col(kk), smem_desc(adO + kk * 2048, 16384, 1024, 2), idV, (u > 0 || kk > 0));
-          mma_ts(tdK, tdP + packed_col(kk), smem_desc(aQ + kk * 2048, 16384, 1024, 2), idK, (u > 0 || kk > 0));
-        }
+        issue_grad(u, 0);
+        if (more && !mbar_wait(qfull + (u + 1) % ST, ((u + 1) / ST) & 1, a.status, abort_flag)) break;
+        tc_fence_after();
+        if (more) issue_sdp(u + 1, 0);
+        if (!mbar_wait(pdsfull + 1, u & 1, a.status, abort_flag)) break;
+        tc_fence_after();
+        issue_grad(u, 1);
         mma_commit(qempty + s);
+        if (more) issue_sdp(u + 1, 1);
       }
       mma_commit(drain);
       wait_plain(drain, 0);
@@ -568,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const bool row_ok = block_row_token(a.g, J, row) >= 0;
     for (int u = 0; u < n; ++u) {
-      if (!mbar_wait(sdpfull, u & 1, a.status, abort_flag)) break;
+      if (!mbar_wait(sdpfull + grp, u & 1, a.status, abort_flag)) break;
       tc_fence_after();
       const uint8_t* st = ring + (u % ST) * STAGE;
       const float* l2 = reinterpret_cast<const float*>(st + 2 * C::TILE);
@@ -595,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(pdsfull);
+      mbar_arrive(pdsfull + grp);
     }
     if (n > 0) mbar_wait(drain, 0, a.status, abort_flag);
     tc_fence_after();
@@ -675,6 +722,7 @@ BwdArgs make_args(const Prob& p, const WsLayout& w, const int32_t* idx, unsigned
   a.N = p.N;
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
+  a.all_full = (p.g.T % p.g.bt == 0 && p.g.H % p.g.bh == 0 && p.g.W % p.g.bw == 0) ? 1 : 0;
   a.idx = idx;
   a.Dv = w.Dv;
   a.L2v = w.L2v;
@@ -699,7 +747,7 @@ cudaError_t launch_dq(const Prob& p, const void* V, const void* dO, const int32_
   WsLayout w = ws_layout(p, ws);
   unsigned* status = status_ptr();
   if (!status) return cudaErrorUnknown;
-  const size_t smem = 1024 + (size_t)C::TILE * (2 + 2 * C::ST) + 8 * (4 + 2 * C::ST) + 1024 + 64;
+  const size_t smem = 1024 + (size_t)C::TILE * (2 + 2 * C::ST) + 8 * (6 + 2 * C::ST) + 1024 + 64;
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const TokType gt = F32OUT ? kTokF32 : kTokBF16;
@@ -723,7 +771,7 @@ cudaError_t launch_dkdv(const Prob& p, const void* V, const void* dO, void* dK, 
   WsLayout w = ws_layout(p, ws);
   unsigned* status = status_ptr();
   if (!status) return cudaErrorUnknown;
-  const size_t smem = 1024 + (size_t)C::TILE * 2 + (size_t)C::ST * (2 * C::TILE + 1024) + 8 * (4 + 2 * C::ST) + 64;
+  const size_t smem = 1024 + (size_t)C::TILE * 2 + (size_t)C::ST * (2 * C::TILE + 1024) + 8 * (6 + 2 * C::ST) + 64;
   cudaError_t e =
       cudaFuncSetAttribute(dkdv_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -17,7 +17,8 @@
 //   warps 4-7   softmax: thread = query row = TMEM lane.  Online softmax in
 //               base 2 with a lazy rescale: O and l are rescaled only when a
 //               row max grows by more than 2^8, which is exact because O and l
-//               always share the same reference max.  P (bf16) overwrites S.
+//               always share the same reference max.  P overwrites S as a
+//               bf16 pair P_hi + P_lo, and O accumulates P_hi V + P_lo V.
 //   warps 2-3   idle.
 // TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,256+D) O.
 #include "internal.h"
@@ -29,6 +30,7 @@ namespace {
 struct FwdArgs {
   Geom g;
   int Hh, k, b, kb_begin, kb_end;
+  int all_full;  // every tile lies inside the grid (no clipped edge tiles)
   long long N;
   float scale_log2;  // softmax scale * log2(e)
   const int32_t* idx;
@@ -198,8 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tP = tmem + (j & 1) * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO, tP + kk * 8, smem_desc(aV + s * C::TILE + kk * 2048, 16384, 1024, 2), idO, (j > 0 || kk > 0));
+        for (int kk = 0; kk < 8; ++kk) {  // keys 16 kk .. 16 kk + 15: P_hi, then P_lo, times the same V rows
+          const uint64_t bV = smem_desc(aV + s * C::TILE + kk * 2048, 16384, 1024, 2);
+          const uint32_t col = (kk >> 1) * 32 + (kk & 1) * 8;
+          mma_ts(tO, tP + col, bV, idO, (j > 0 || kk > 0));
+          mma_ts(tO, tP + col + 16, bV, idO, 1);
+        }
         mma_commit(empty + s);
         mma_commit(odone);
       }
@@ -220,24 +226,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t tS = tmem + (j & 1) * 128 + lane_base;
-      float sv[128];
+      const int J = sel[j];
+      const bool full = a.all_full || block_is_full(a.g, J);
+      // pass 1: this block's row max (S is read from TMEM twice rather than held in 128 registers)
+      float mx = -INFINITY;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t u[32];
         tmem_ld32(tS + cc * 32, u);
         tmem_wait_ld();
+        if (full) {
+          float m0 = __uint_as_float(u[0]), m1 = __uint_as_float(u[1]);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sv[cc * 32 + e] = __uint_as_float(u[e]) * a.scale_log2;
+          for (int e = 2; e < 32; e += 4) {
+            m0 = fmaxf(m0, fmaxf(__uint_as_float(u[e]), __uint_as_float(u[e + 1])));
+            m1 = fmaxf(m1, fmaxf(__uint_as_float(u[e + 2]), __uint_as_float(u[e + 3])));
+          }
+          mx = fmaxf(mx, fmaxf(m0, m1));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (block_row_token(a.g, J, cc * 32 + e) >= 0) mx = fmaxf(mx, __uint_as_float(u[e]));
+        }
       }
-      const int J = sel[j];
-      if (!block_is_full(a.g, J)) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (block_row_token(a.g, J, c) < 0) sv[c] = -INFINITY;
-      }
-      float mx = sv[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+      mx *= a.scale_log2;
       const float m_new = fmaxf(m, mx);
       if (j == 0) {
         m = m_new;
@@ -265,18 +277,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (need) m = m_new;
         }
       }
+      // pass 2: P = 2^(s - m) split as P_hi + P_lo (both bf16, P_lo = bf16(P - P_hi)) so that the
+      // P V product keeps ~16 significant bits of P: with the lazy reference max the dominant
+      // entries are not 1 and a single bf16 rounding would cost up to 2^-8 of O.  Chunk cc's
+      // 32 columns hold P_hi in their first 16 and P_lo in their last 16 (packed pairs).
       float sum = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        uint32_t pk[16];
+        uint32_t u[32];
+        tmem_ld32(tS + cc * 32, u);
+        tmem_wait_ld();
+        uint32_t ph[16], pl[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(sv[cc * 32 + 2 * e] - m);
-          const float p1 = ex2(sv[cc * 32 + 2 * e + 1] - m);
+          float s0 = fmaf(__uint_as_float(u[2 * e]), a.scale_log2, -m);
+          float s1 = fmaf(__uint_as_float(u[2 * e + 1]), a.scale_log2, -m);
+          if (!full) {
+            if (block_row_token(a.g, J, cc * 32 + 2 * e) < 0) s0 = -INFINITY;
+            if (block_row_token(a.g, J, cc * 32 + 2 * e + 1) < 0) s1 = -INFINITY;
+          }
+          const float p0 = ex2(s0), p1 = ex2(s1);
           sum += p0 + p1;
-          pk[e] = pack_bf16(p0, p1);
+          ph[e] = pack_bf16(p0, p1);
+          pl[e] = pack_bf16(p0 - __uint_as_float(ph[e] << 16), p1 - __uint_as_float(ph[e] & 0xFFFF0000u));
         }
-        tmem_st16(tS + cc * 16, pk);
+        tmem_st16(tS + cc * 32, ph);
+        tmem_st16(tS + cc * 32 + 16, pl);
       }
       l += sum;
       tmem_wait_st();
@@ -359,6 +385,7 @@ cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* 
     a.b = b;
     a.kb_begin = kb_begin;
     a.kb_end = kb_end;
+    a.all_full = (g.T % g.bt == 0 && g.H % g.bh == 0 && g.W % g.bw == 0) ? 1 : 0;
     a.N = p.N;
     a.scale_log2 = p.scale * 1.4426950408889634f;
     a.idx = idx;

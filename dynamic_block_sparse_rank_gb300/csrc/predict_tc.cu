@@ -16,11 +16,12 @@
 //   score_kernel  per (two query blocks, head): streams every k~ tile through
 //                 an 8-deep ring; for each key block J two MMAs (one per query
 //                 block, M=128, N=128, K=r) land in a double-buffered TMEM
-//                 accumulator; 8 epilogue warps reduce each 128x128 tile to
-//                 its max (three-input max, then a warp shuffle, then a
-//                 shared-memory atomic max on order-preserving keys).  When the
-//                 row of n_b scores is complete, each half of the epilogue
-//                 selects the top k of its query block (radix select).
+//                 accumulator; 16 epilogue warps (one per TMEM lane quarter,
+//                 query block and column half) reduce each 128x128 tile to its
+//                 max: four independent three-input max chains per thread, then
+//                 one redux.sync over order-preserving keys and a shared-memory
+//                 atomic max.  When the row of n_b scores is complete, the 8
+//                 warps of each query block select its top k (radix select).
 #include "internal.h"
 #include "topk.cuh"
 
@@ -86,7 +87,10 @@ template <int R>
 struct ScoreCfg {
   static constexpr int ST = R <= 32 ? 8 : 4;  // k~ ring depth
 };
-constexpr int kScoreThreads = 384;  // warp 0 producer, warp 1 MMA, warps 4-7 / 8-11 epilogue
+// warp 0 producer, warp 1 MMA, warps 2..17 epilogue: 4 warps per TMEM lane
+// quarter, one for each (query block, column half) pair.
+constexpr int kEpiWarps = 16;
+constexpr int kScoreThreads = (2 + kEpiWarps) * 32;
 
 struct ScoreArgs {
   Geom g;
@@ -101,6 +105,12 @@ struct ScoreArgs {
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ unsigned warp_max_u32(unsigned v) {
+  unsigned r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
   return r;
 }
 
@@ -135,6 +145,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   uint64_t* drain = acce + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint8_t* full = reinterpret_cast<uint8_t*>(abort_flag + 1);  // nb: key block J lies inside the grid
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -145,13 +156,14 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(accf + s, 1);
-      mbar_init(acce + s, 8);
+      mbar_init(acce + s, kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   for (int e = tid; e < 2 * nb; e += kScoreThreads) keys[e] = 0u;  // below every real key
+  for (int J = tid; J < nb; J += kScoreThreads) full[J] = block_is_full(a.g, J) ? 1 : 0;
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -208,62 +220,68 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
       wait_plain(drain, 0);
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    const int grp = (warp - 4) >> 2;  // 0: query block I0, 1: I1
+  } else {
+    // epilogue warp e: TMEM lane quarter = warp % 4, (query block, column half) = e / 4
+    const int e = warp - 2;
+    const int quarter = warp & 3;
+    const int grp = (e >> 2) >> 1, half = (e >> 2) & 1;
     const int I = grp ? I1 : I0;
-    const int row = tid - 128 - grp * 128;
+    const int row = quarter * 32 + lane;
     const bool row_ok = block_row_token(a.g, I, row) >= 0;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     unsigned* mykeys = keys + grp * nb;
     for (int J = 0; J < nb; ++J) {
       const int buf = J & 1;
       if (!mbar_wait(accf + buf, (J >> 1) & 1, a.status, abort_flag)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + buf * 256 + grp * 128 + lane_base;
+      const uint32_t taddr = tmem + buf * 256 + grp * 128 + half * 64 + lane_base;
       uint32_t u0[32], u1[32];
-      float m = -INFINITY;
-      const bool full = block_is_full(a.g, J);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld32(taddr + half * 64, u0);
-        tmem_ld32(taddr + half * 64 + 32, u1);
-        tmem_wait_ld();
-        if (full) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            m = max3(m, __uint_as_float(u0[e]), __uint_as_float(u0[e + 1]));
-            m = max3(m, __uint_as_float(u1[e]), __uint_as_float(u1[e + 1]));
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if (block_row_token(a.g, J, half * 64 + e) >= 0) m = fmaxf(m, __uint_as_float(u0[e]));
-            if (block_row_token(a.g, J, half * 64 + 32 + e) >= 0) m = fmaxf(m, __uint_as_float(u1[e]));
-          }
-        }
-      }
+      tmem_ld32(taddr, u0);
+      tmem_ld32(taddr + 32, u1);
+      tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce + buf);
-      if (!row_ok) m = -INFINITY;
+      if (lane == 0) mbar_arrive(acce + buf);  // values are in registers: the buffer may be refilled
+      float m;
+      if (full[J]) {
+        float m0 = __uint_as_float(u0[0]), m1 = __uint_as_float(u0[1]);
+        float m2 = __uint_as_float(u1[0]), m3 = __uint_as_float(u1[1]);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0 && m > -INFINITY) atomicMax(mykeys + J, order_key(m));
+        for (int c = 2; c < 32; c += 4) {
+          m0 = max3(m0, __uint_as_float(u0[c]), __uint_as_float(u0[c + 1]));
+          m1 = max3(m1, __uint_as_float(u0[c + 2]), __uint_as_float(u0[c + 3]));
+          m2 = max3(m2, __uint_as_float(u1[c]), __uint_as_float(u1[c + 1]));
+          m3 = max3(m3, __uint_as_float(u1[c + 2]), __uint_as_float(u1[c + 3]));
+        }
+        m = fmaxf(max3(m0, m1, m2), m3);
+      } else {
+        m = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (block_row_token(a.g, J, half * 64 + c) >= 0) m = fmaxf(m, __uint_as_float(u0[c]));
+          if (block_row_token(a.g, J, half * 64 + 32 + c) >= 0) m = fmaxf(m, __uint_as_float(u1[c]));
+        }
+      }
+      // order-preserving key; 0 (below every real key) for rows/columns outside the grid
+      const unsigned key = (row_ok && m > -INFINITY) ? order_key(m) : 0u;
+      const unsigned wmax = warp_max_u32(key);
+      if (lane == 0 && wmax != 0u) atomicMax(mykeys + J, wmax);
     }
-    named_bar(1, 256);
-    // keys -> scores (inverse of order_key), in place
+    named_bar(1, kEpiWarps * 32);
+    // keys -> scores (inverse of order_key), in place; then top-k per query block by its 8 warps
+    const int tg = (e & 7) * 32 + lane;  // thread index inside this query block's 8 warps
     float* srow = reinterpret_cast<float*>(mykeys);
-    for (int J = row; J < nb; J += 128) {
+    for (int J = tg; J < nb; J += 256) {
       const unsigned kq = mykeys[J];
       const unsigned u = (kq & 0x80000000u) ? (kq & 0x7FFFFFFFu) : ~kq;
       srow[J] = kq == 0u ? -INFINITY : __uint_as_float(u);
     }
-    named_bar(2 + grp, 128);
+    named_bar(2 + grp, 256);
     const bool write = grp == 0 || I1 != I0;
     if (write) {
       if (a.score)
-        for (int J = row; J < nb; J += 128) a.score[(head_tiles + I) * nb + J] = srow[J];
-      topk_select(srow, nb, a.k, a.idx + (head_tiles + I) * a.k, row, 128, 2 + grp, tks + grp);
+        for (int J = tg; J < nb; J += 256) a.score[(head_tiles + I) * nb + J] = srow[J];
+      topk_select(srow, nb, a.k, a.idx + (head_tiles + I) * a.k, tg, 256, 2 + grp, tks + grp);
     }
   }
   __syncthreads();
@@ -292,7 +310,7 @@ cudaError_t launch_predict(const Prob& p, const void* Q, const void* K, const vo
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   constexpr int kStages = ScoreCfg<R>::ST;
   const size_t ssmem_raw = 1024 + (size_t)(2 + kStages) * 128 * R * 2 + 2 * (size_t)p.g.nb * 4 + 2 * sizeof(TopkScratch) +
-                       8 * (1 + 2 * kStages + 5) + 16 + 64;
+                       8 * (1 + 2 * kStages + 5) + 16 + (size_t)p.g.nb + 64;
   // Keep one CTA per SM: each CTA owns all 512 TMEM columns.
   const size_t ssmem = ssmem_raw > 120 * 1024 ? ssmem_raw : 120 * 1024;
   if ((e = cudaFuncSetAttribute(score_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem)) !=

@@ -219,6 +219,25 @@ def generate(wl: Workload, seed: int = 0, names=("Q", "K", "V", "Wq", "Wk"), hea
     return out
 
 
+def local_block_map(wl: Workload, seed: int = 0) -> np.ndarray:
+    """A seeded block map [B, heads, n_b, k] (int32, rows ascending) with the local structure the
+    predictor produces on these inputs: each query block keeps the k key blocks nearest to it in tile
+    coordinates, distances perturbed by U(0, 2) tiles of jitter.  Used where a test needs one fixed
+    map shared by both sides (for instance the backward at full size)."""
+    nT, nH, nW = wl.grid
+    it, ih, iw = np.meshgrid(np.arange(nT), np.arange(nH), np.arange(nW), indexing="ij")
+    coords = np.stack([it.ravel(), ih.ravel(), iw.ravel()], axis=1).astype(np.float64)
+    nb, k = wl.n_blocks, wl.k
+    out = np.empty((wl.B, wl.heads, nb, k), dtype=np.int32)
+    for b in range(wl.B):
+        for h in range(wl.heads):
+            rng = _rng(seed, 100, b, h)
+            for I in range(nb):
+                dist = np.abs(coords - coords[I]).sum(axis=1) + rng.uniform(0.0, 2.0, nb)
+                out[b, h, I] = np.sort(np.argpartition(dist, k - 1)[:k])
+    return out
+
+
 def digest(arrays: dict[str, np.ndarray]) -> str:
     """sha256 over the named arrays' bytes (sorted by name), to log that both sides saw the same inputs."""
     import hashlib

@@ -1,0 +1,253 @@
+"""GPU vs oracle parity at the five workloads' full sizes, in the launch configuration bench.py times.
+
+The CUDA path runs the whole problem; the fp64 oracle recomputes sampled
+outputs one query block (or key block) at a time.  Where a GPU call needs a
+full block map but the oracle only computes some rows, the GPU map's sampled
+rows are replaced by the oracle's own rows before the call, so every compared
+GPU output derives from oracle-selected blocks and no oracle input comes from
+the GPU.  The backward at 524K tokens runs on a seeded local block map shared by
+both sides (the oracle cannot produce the full map in test time); its unsampled
+rows are still checked through the exact sum invariants.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+from dynamic_block_sparse_rank_gb300 import inputs
+from tests.parity_util import TOL, assert_close, check_selection, dev, errors, host
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dynamic_block_sparse_rank_gb300 import sda as s
+
+    s.lib()
+    return s
+
+
+def _geom(wl):
+    return orc.Geometry(wl.T, wl.H, wl.W, wl.bt, wl.bh, wl.bw)
+
+
+def _samples(wl, n, seed):
+    rng = np.random.default_rng(seed)
+    nb = wl.n_blocks
+    picks = {0, nb - 1, nb // 2} | set(int(x) for x in rng.choice(nb, n, replace=False))
+    return sorted(picks)
+
+
+def _head(x, h):
+    return {k: (v[:, :, h:h + 1] if v.ndim == 4 and k not in ("Wq", "Wk") else v[h:h + 1]) for k, v in x.items()}
+
+
+def _check_scores(got, ref):
+    """Block scores: fp32 accumulation of exact bf16 products, so they match the oracle to ~1e-6 except
+    where a q~ or k~ element was rounded to the neighbouring bf16 value (the GPU rounds an fp32-accumulated
+    projection, the oracle an exact one): such a flip moves a score by about 2^-8 of one of its r terms.
+    Nearly every score must agree to 1e-5 of the largest, and every one to 4e-3."""
+    err = np.abs(got - ref) / np.abs(ref).max()
+    assert np.mean(err > 1e-5) < 0.02, np.mean(err > 1e-5)
+    assert err.max() < 4e-3, err.max()
+
+
+def _gpu_predict(sda, wl, Q, K, Wq, Wk, with_score=True):
+    p = sda.problem_from_workload(wl)
+    nb, k = sda.sda_num_blocks(p)
+    idx = torch.empty((wl.B, wl.heads, nb, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((wl.B, wl.heads, nb, nb), dtype=torch.float32, device="cuda") if with_score else None
+    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICT), dtype=torch.uint8, device="cuda")
+    sda.sda_predict_blocks(p, Q, K, Wq, Wk, idx, sc, ws)
+    torch.cuda.synchronize()
+    return idx, sc
+
+
+def _check_predictor_and_forward(sda, wl, heads, n_blocks_sampled, seed=0):
+    x = inputs.generate(wl, names=("Q", "K", "V", "Wq", "Wk"))
+    geom = _geom(wl)
+    Q, K, V, Wq, Wk = (dev(x[n], wl.dtype) for n in ("Q", "K", "V", "Wq", "Wk"))
+    idx, sc = _gpu_predict(sda, wl, Q, K, Wq, Wk)
+    qb = _samples(wl, n_blocks_sampled, seed)
+    sel_stats = []
+    ref_rows = {}
+    for h in heads:
+        xh = _head(x, h)
+        ridx, rsc = orc.predict_blocks(xh["Q"], xh["K"], xh["Wq"], xh["Wk"], geom, wl.keep, wl.dtype, query_blocks=qb)
+        gi = idx[0, h, qb].cpu().numpy()
+        st = check_selection(gi, rsc, wl.k)
+        assert st["fail"] == 0, (h, st)
+        sel_stats.append(st)
+        _check_scores(sc[0, h, qb].cpu().numpy().astype(np.float64), rsc)
+        ref_rows[h] = ridx
+        idx[0, h, qb] = torch.from_numpy(ridx[0, 0]).cuda()  # compared rows use the oracle's selection
+    p = sda.problem_from_workload(wl)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_attn_fwd(p, Q, K, V, idx, O, LSE)
+    torch.cuda.synchronize()
+    for h in heads:
+        xh = _head(x, h)
+        Or, Lr = orc.attn_fwd(xh["Q"], xh["K"], xh["V"], ref_rows[h], geom, query_blocks=qb)
+        rows = np.concatenate([geom.tokens(I) for I in qb])
+        assert_close(host(O[0, rows, h]), Or[0, rows, 0], wl.dtype, f"O head {h}")
+        assert_close(host(LSE[0, h, rows]), Lr[0, 0, rows], wl.dtype, f"LSE head {h}")
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    return sel_stats
+
+
+def test_fwd_8k_full_oracle(sda):
+    wl = inputs.WORKLOADS["fwd_8k"]
+    x = inputs.generate(wl, names=("Q", "K", "V", "Wq", "Wk"))
+    geom = _geom(wl)
+    Q, K, V, Wq, Wk = (dev(x[n], wl.dtype) for n in ("Q", "K", "V", "Wq", "Wk"))
+    idx, sc = _gpu_predict(sda, wl, Q, K, Wq, Wk)
+    ridx, rsc = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    st = check_selection(idx.cpu().numpy(), rsc, wl.k)
+    assert st["fail"] == 0, st
+    _check_scores(host(sc), rsc)
+    p = sda.problem_from_workload(wl)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_attn_fwd(p, Q, K, V, torch.from_numpy(ridx).cuda(), O, LSE)
+    torch.cuda.synchronize()
+    Or, Lr = orc.attn_fwd(x["Q"], x["K"], x["V"], ridx, geom)
+    assert_close(host(O), Or, "bf16", "O")
+    assert_close(host(LSE), Lr, "bf16", "LSE")
+
+
+def test_fwd_61k_sampled(sda):
+    _check_predictor_and_forward(sda, inputs.WORKLOADS["fwd_61k"], heads=[0, 13, 23], n_blocks_sampled=5)
+
+
+def test_train_524k_predictor_and_forward_sampled(sda):
+    _check_predictor_and_forward(sda, inputs.WORKLOADS["train_524k"], heads=[0, 5], n_blocks_sampled=3)
+
+
+def test_train_524k_backward_sampled(sda):
+    wl = inputs.WORKLOADS["train_524k"]
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO"))
+    geom = _geom(wl)
+    m = inputs.local_block_map(wl, seed=1)
+    p = sda.problem_from_workload(wl)
+    Q, K, V, dO = (dev(x[n], wl.dtype) for n in ("Q", "K", "V", "dO"))
+    idx = torch.from_numpy(m).cuda()
+    O = torch.empty_like(Q)
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_attn_fwd(p, Q, K, V, idx, O, LSE)
+    dQ, dK, dV = (torch.empty(Q.shape, dtype=torch.float32, device="cuda") for _ in range(3))
+    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device="cuda")
+    sda.sda_attn_bwd(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, "f32", ws)
+    torch.cuda.synchronize()
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    # exact invariants over every row of every head: sum_j dK_j = 0, sum_j dV_j = sum_i dO_i
+    sk = dK.double().sum(dim=1)
+    sv = dV.double().sum(dim=1) - dO.double().sum(dim=1)
+    scale_k = dK.double().abs().sum(dim=1)
+    scale_v = dV.double().abs().sum(dim=1)
+    assert float((sk.abs() / scale_k).max()) < 1e-4
+    assert float((sv.abs() / scale_v).max()) < 1e-4
+    # sampled rows against the oracle (head 0): dQ of three query blocks, dK/dV of two key blocks
+    h = 0
+    xh = _head(x, h)
+    mh = m[:, h:h + 1]
+    qbs = _samples(wl, 0, 3)[:3]
+    fan_in = np.bincount(m[0, h].ravel(), minlength=geom.n_blocks)
+    kbs = [int(np.argmax(fan_in)), geom.n_blocks // 3]
+    dq_ref, dkv_ref = orc.attn_bwd_blocks(xh["Q"], xh["K"], xh["V"], xh["dO"], mh, geom, query_blocks=qbs,
+                                          key_blocks=kbs)
+    for (_, _, I), ref in dq_ref.items():
+        assert_close(host(dQ[0, geom.tokens(I), h]), ref, "bf16", f"dQ block {I}")
+    for (_, _, J), (rk, rv) in dkv_ref.items():
+        assert_close(host(dK[0, geom.tokens(J), h]), rk, "bf16", f"dK block {J}")
+        assert_close(host(dV[0, geom.tokens(J), h]), rv, "bf16", f"dV block {J}")
+    # forward on the shared map, sampled rows
+    Or, Lr = orc.attn_fwd(xh["Q"], xh["K"], xh["V"], mh[:, :, qbs], geom, query_blocks=qbs)
+    rows = np.concatenate([geom.tokens(I) for I in qbs])
+    assert_close(host(O[0, rows, h]), Or[0, rows, 0], "bf16", "O")
+    assert_close(host(LSE[0, h, rows]), Lr[0, 0, rows], "bf16", "LSE")
+
+
+def test_merge_131k_partition_states_and_reuse_sampled(sda):
+    wl = inputs.WORKLOADS["merge_131k"]
+    x = inputs.generate(wl, names=("Q", "K", "V", "Qp", "Kp", "Vp", "Wq", "Wk"))
+    geom = _geom(wl)
+    P = wl.partitions
+    bounds = orc.frame_partitions(geom, P)
+    reuse = orc.reuse_mask(geom, P, wl.n_reuse)
+    p = sda.problem_from_workload(wl)
+    T = {n: dev(x[n], wl.dtype) for n in ("Q", "K", "V", "Qp", "Kp", "Vp", "Wq", "Wk")}
+    heads = [0, 9]
+    qb = _samples(wl, 4, 5) + [int(np.flatnonzero(reuse[0])[-1])]  # includes ragged edge tiles
+    qb = sorted(set(qb))
+
+    def gpu_map(Qn, Kn):
+        idx, _ = _gpu_predict(sda, wl, T[Qn], T[Kn], T["Wq"], T["Wk"], with_score=False)
+        rows = {}
+        for h in heads:
+            xh = _head(x, h)
+            r, sc = orc.predict_blocks(xh[Qn], xh[Kn], xh["Wq"], xh["Wk"], geom, wl.keep, wl.dtype, query_blocks=qb)
+            st = check_selection(idx[0, h, qb].cpu().numpy(), sc, wl.k)
+            assert st["fail"] == 0, (Qn, h, st)
+            idx[0, h, qb] = torch.from_numpy(r[0, 0]).cuda()
+            rows[h] = r
+        return idx, rows
+
+    idx_prev, rows_prev = gpu_map("Qp", "Kp")
+    idx_now, rows_now = gpu_map("Q", "K")
+    # previous step: every partition state for every query block (the reuse cache)
+    states = [(torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda"))
+              for _ in range(P)]
+    for (b0, b1), (Op, Lp) in zip(bounds, states):
+        sda.sda_attn_fwd(p, T["Qp"], T["Kp"], T["Vp"], idx_prev, Op, Lp, kb_begin=b0, kb_end=b1)
+    # current step: recompute the near partitions only, in place
+    for q, ((b0, b1), (Op, Lp)) in enumerate(zip(bounds, states)):
+        act = torch.from_numpy((~reuse[q]).astype(np.uint8)).cuda()
+        sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Op, Lp, kb_begin=b0, kb_end=b1, qb_active=act)
+    Om, Lm = torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_merge_states([s[0] for s in states], [s[1] for s in states], 1, wl.N, wl.heads, wl.d, "bf16", Om, Lm)
+    # exact merge of fresh states equals the full-range forward
+    fresh = [(torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda"))
+             for _ in range(P)]
+    for (b0, b1), (Op, Lp) in zip(bounds, fresh):
+        sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Op, Lp, kb_begin=b0, kb_end=b1)
+    Oe, Le = torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_merge_states([s[0] for s in fresh], [s[1] for s in fresh], 1, wl.N, wl.heads, wl.d, "bf16", Oe, Le)
+    Of, Lf = torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Of, Lf)
+    torch.cuda.synchronize()
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    rows = np.concatenate([geom.tokens(I) for I in qb])
+    deviation = []
+    for h in heads:
+        xh = _head(x, h)
+        ref_states = []
+        for q, (b0, b1) in enumerate(bounds):
+            prev = orc.attn_fwd(xh["Qp"], xh["Kp"], xh["Vp"], rows_prev[h], geom, kb_begin=b0, kb_end=b1, query_blocks=qb)
+            now = orc.attn_fwd(xh["Q"], xh["K"], xh["V"], rows_now[h], geom, kb_begin=b0, kb_end=b1, query_blocks=qb)
+            O_q, L_q = now[0].copy(), now[1].copy()
+            for I in qb:
+                if reuse[q, I]:
+                    t = geom.tokens(I)
+                    O_q[:, t] = prev[0][:, t]
+                    L_q[:, :, t] = prev[1][:, :, t]
+            ref_states.append((O_q[0, rows, 0], L_q[0, 0, rows], now[0][0, rows, 0], now[1][0, 0, rows]))
+            # each state the GPU keeps equals the oracle's (reused or fresh)
+            assert_close(host(states[q][0][0, rows, h]), ref_states[-1][0], "bf16", f"state O p{q} h{h}")
+            assert_close(host(states[q][1][0, h, rows]), ref_states[-1][1], "bf16", f"state LSE p{q} h{h}")
+        Ro, Rl = orc.merge_states([s[0] for s in ref_states], [s[1] for s in ref_states])
+        assert_close(host(Om[0, rows, h]), Ro, "bf16", f"reuse-merged O h{h}")
+        assert_close(host(Lm[0, h, rows]), Rl, "bf16", f"reuse-merged LSE h{h}")
+        Eo, El = orc.merge_states([s[2] for s in ref_states], [s[3] for s in ref_states])
+        assert_close(host(Oe[0, rows, h]), Eo, "bf16", f"exact-merged O h{h}")
+        assert_close(host(Le[0, h, rows]), El, "bf16", f"exact-merged LSE h{h}")
+        Fo, Fl = orc.attn_fwd(xh["Q"], xh["K"], xh["V"], rows_now[h], geom, query_blocks=qb)
+        assert_close(host(Of[0, rows, h]), Fo[0, rows, 0], "bf16", f"full-range O h{h}")
+        assert_close(Eo, Fo[0, rows, 0], "bf16", "oracle: merge of partitions equals the union")
+        deviation.append(errors(Ro, Eo))
+    # the reuse approximation's deviation from the exact merge is reported, not graded
+    print("reuse vs exact merge (max-abs, rel-frob) per sampled head:", deviation)
