@@ -317,11 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_5d(sdO + c * 16384, &tmdO, qfull, c * 64, h, w0, h0, t0);
       }
       int issued = 0;
+      int Jn = sel[0];  // block index read one iteration ahead of its use
       for (int j = 0; j < n; ++j) {
         const int s = j % ST;
+        const int Jc = Jn;
+        if (j + 1 < n) Jn = sel[j + 1];
         if (j >= ST && !mbar_wait(kvempty + s, ((j / ST) - 1) & 1, a.status, abort_flag)) break;
         int jt0, jh0, jw0;
-        block_origin(a.g, sel[j], jt0, jh0, jw0);
+        block_origin(a.g, Jc, jt0, jh0, jw0);
         mbar_expect_tx(kvfull + s, 2 * C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
@@ -402,11 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const long long tile_row = (((long long)a.b * a.Hh + h) * a.g.nb + I) * 128 + row;
     const float l2 = a.L2v[tile_row];
     const float Dt = a.Dv[tile_row];  // D~ from the stored O
-    float dsum = 0.f;                 // this group's share of D = sum_j P_ij dP_ij
+    float dsum0 = 0.f, dsum1 = 0.f;   // this group's share of D = sum_j P_ij dP_ij
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait(sdpfull + grp, j & 1, a.status, abort_flag)) break;
       tc_fence_after();
-      const bool full = a.all_full || block_is_full(a.g, sel[j]);
+      const int J = a.all_full ? 0 : sel[j];
+      const bool full = a.all_full || block_is_full(a.g, J);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = grp * 64 + cc * 32;
@@ -415,16 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tdP + lane_base + col0, up);
         tmem_wait_ld();
         uint32_t pds[16], pp[16];
+        const uint32_t vm = full ? 0xffffffffu : block_rows_mask32(a.g, J, col0);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), a.scale_log2, -l2));
           float p1 = ex2(fmaf(__uint_as_float(us[2 * e + 1]), a.scale_log2, -l2));
-          if (!full) {
-            if (block_row_token(a.g, sel[j], col0 + 2 * e) < 0) p0 = 0.f;
-            if (block_row_token(a.g, sel[j], col0 + 2 * e + 1) < 0) p1 = 0.f;
-          }
+          if (!((vm >> (2 * e)) & 1u)) p0 = 0.f;
+          if (!((vm >> (2 * e + 1)) & 1u)) p1 = 0.f;
           const float dp0 = __uint_as_float(up[2 * e]), dp1 = __uint_as_float(up[2 * e + 1]);
-          dsum = fmaf(p0, dp0, fmaf(p1, dp1, dsum));
+          dsum0 = fmaf(p0, dp0, dsum0);
+          dsum1 = fmaf(p1, dp1, dsum1);
           pds[e] = pack_f16(p0 * (dp0 - Dt), p1 * (dp1 - Dt));
           pp[e] = pack_f16(p0, p1);
         }
@@ -435,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(dsfull + grp);
     }
-    dpart[grp * 128 + row] = dsum;
+    dpart[grp * 128 + row] = dsum0 + dsum1;
     mbar_wait(drain, 0, a.status, abort_flag);
     tc_fence_after();
     named_bar(1, 256);
@@ -528,10 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_5d(sV + c * 16384, &tmV, kvfull, c * 64, h, w0, h0, t0);
       }
       int issued = 0;
+      int In = users[0];  // query block index read one iteration ahead of its use
       for (int u = 0; u < n; ++u) {
         const int s = u % ST;
+        const int I = In;
+        if (u + 1 < n) In = users[u + 1];
         if (u >= ST && !mbar_wait(qempty + s, ((u / ST) - 1) & 1, a.status, abort_flag)) break;
-        const int I = users[u];
         int it0, ih0, iw0;
         block_origin(a.g, I, it0, ih0, iw0);
         uint8_t* st = ring + s * STAGE;

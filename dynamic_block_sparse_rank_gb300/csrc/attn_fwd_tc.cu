@@ -244,9 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mx = fmaxf(mx, fmaxf(m0, m1));
         } else {
+          const uint32_t vm = block_rows_mask32(a.g, J, cc * 32);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (block_row_token(a.g, J, cc * 32 + e) >= 0) mx = fmaxf(mx, __uint_as_float(u[e]));
+            if ((vm >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u[e]));
         }
       }
       mx *= a.scale_log2;
@@ -288,14 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + cc * 32, u);
         tmem_wait_ld();
         uint32_t ph[16], pl[16];
+        const uint32_t vm = full ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float s0 = fmaf(__uint_as_float(u[2 * e]), a.scale_log2, -m);
           float s1 = fmaf(__uint_as_float(u[2 * e + 1]), a.scale_log2, -m);
-          if (!full) {
-            if (block_row_token(a.g, J, cc * 32 + 2 * e) < 0) s0 = -INFINITY;
-            if (block_row_token(a.g, J, cc * 32 + 2 * e + 1) < 0) s1 = -INFINITY;
-          }
+          if (!((vm >> (2 * e)) & 1u)) s0 = -INFINITY;
+          if (!((vm >> (2 * e + 1)) & 1u)) s1 = -INFINITY;
           const float p0 = ex2(s0), p1 = ex2(s1);
           sum += p0 + p1;
           ph[e] = pack_bf16(p0, p1);

@@ -64,6 +64,15 @@ __host__ __device__ __forceinline__ bool block_is_full(const Geom& g, int I) {
   return t0 + g.bt <= g.T && h0 + g.bh <= g.H && w0 + g.bw <= g.W;
 }
 
+// Bit c set when row (col0 + c) of block I lies inside the grid, c = 0..31.
+// Out of line on purpose: it runs only for clipped edge tiles and keeps the
+// unrolled inner loops that call it small.
+__device__ __noinline__ inline uint32_t block_rows_mask32(const Geom& g, int I, int col0) {
+  uint32_t m = 0;
+  for (int c = 0; c < 32; ++c) m |= (block_row_token(g, I, col0 + c) >= 0 ? 1u : 0u) << c;
+  return m;
+}
+
 // ----------------------------------------------------------------------------
 // Shared-memory addresses and mbarriers.
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -87,14 +96,19 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// One bounded test of the phase; the thread may be suspended by the hardware for
+// up to kSuspendHintNs while the phase is incomplete (it resumes as soon as the
+// phase completes), so waiting warps do not spin on the issue slots.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -108,7 +122,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u) {
+    if ((it & 7u) == 7u) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > SDA_WAIT_LIMIT_NS) {
         atomicOr(status, kStatusWaitTimeout);

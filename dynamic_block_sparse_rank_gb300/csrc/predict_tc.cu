@@ -256,10 +256,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
         m = fmaxf(max3(m0, m1, m2), m3);
       } else {
         m = -INFINITY;
+        const uint32_t v0 = block_rows_mask32(a.g, J, half * 64), v1 = block_rows_mask32(a.g, J, half * 64 + 32);
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          if (block_row_token(a.g, J, half * 64 + c) >= 0) m = fmaxf(m, __uint_as_float(u0[c]));
-          if (block_row_token(a.g, J, half * 64 + 32 + c) >= 0) m = fmaxf(m, __uint_as_float(u1[c]));
+          if ((v0 >> c) & 1u) m = fmaxf(m, __uint_as_float(u0[c]));
+          if ((v1 >> c) & 1u) m = fmaxf(m, __uint_as_float(u1[c]));
         }
       }
       // order-preserving key; 0 (below every real key) for rows/columns outside the grid
