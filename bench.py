@@ -309,6 +309,18 @@ def main():
 
         e2e_step()
         torch.cuda.synchronize()
+        # one instrumented pass: time of the host->device and device->host copies alone
+        c = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        c[0].record(stream)
+        for n, t in pin.items():
+            d_in[n].copy_(t, non_blocking=True)
+        c[1].record(stream)
+        c[2].record(stream)
+        for h, g in zip(out_host, (dQ, dK, dV)):
+            h.copy_(g, non_blocking=True)
+        c[3].record(stream)
+        torch.cuda.synchronize()
+        h2d_ms, d2h_ms = c[0].elapsed_time(c[1]), c[2].elapsed_time(c[3])
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -324,6 +336,7 @@ def main():
             ms_e2e = float(t.item())
         e2e = {"value": world * (f_fwd + f_bwd) / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "h2d_ms": h2d_ms, "d2h_ms": d2h_ms,
                "tokens_per_s": world * wl.B * wl.N / (ms_e2e / 1e3)}
 
     # ---- merge of partial states on the 4-partition workload's shapes (HBM-bound kernel)
