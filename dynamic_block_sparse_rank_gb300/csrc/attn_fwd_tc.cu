@@ -233,16 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t u[32];
-        tmem_ld32(tS + cc * 32, u);
+        float cmax;
+        tmem_ld32_max(tS + cc * 32, u, cmax);
         tmem_wait_ld();
         if (full) {
-          float m0 = __uint_as_float(u[0]), m1 = __uint_as_float(u[1]);
-#pragma unroll
-          for (int e = 2; e < 32; e += 4) {
-            m0 = fmaxf(m0, fmaxf(__uint_as_float(u[e]), __uint_as_float(u[e + 1])));
-            m1 = fmaxf(m1, fmaxf(__uint_as_float(u[e + 2]), __uint_as_float(u[e + 3])));
-          }
-          mx = fmaxf(mx, fmaxf(m0, m1));
+          mx = fmaxf(mx, cmax);
         } else {
           const uint32_t vm = block_rows_mask32(a.g, J, cc * 32);
 #pragma unroll

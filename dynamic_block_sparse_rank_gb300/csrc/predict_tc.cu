@@ -18,9 +18,9 @@
 //                 block, M=128, N=128, K=r) land in a double-buffered TMEM
 //                 accumulator; 16 epilogue warps (one per TMEM lane quarter,
 //                 query block and column half) reduce each 128x128 tile to its
-//                 max: four independent three-input max chains per thread, then
-//                 one redux.sync over order-preserving keys and a shared-memory
-//                 atomic max.  When the row of n_b scores is complete, the 8
+//                 max: the reducing TMEM load gives each thread the max of its
+//                 columns, then one redux.sync over order-preserving keys and a
+//                 shared-memory atomic max per warp.  When the row of n_b scores is complete, the 8
 //                 warps of each query block select its top k (radix select).
 #include "internal.h"
 #include "topk.cuh"
@@ -236,24 +236,16 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
       tc_fence_after();
       const uint32_t taddr = tmem + buf * 256 + grp * 128 + half * 64 + lane_base;
       uint32_t u0[32], u1[32];
-      tmem_ld32(taddr, u0);
-      tmem_ld32(taddr + 32, u1);
+      float mx0, mx1;
+      tmem_ld32_max(taddr, u0, mx0);  // the load also reduces each thread's 32 values to their max
+      tmem_ld32_max(taddr + 32, u1, mx1);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce + buf);  // values are in registers: the buffer may be refilled
       float m;
       if (full[J]) {
-        float m0 = __uint_as_float(u0[0]), m1 = __uint_as_float(u0[1]);
-        float m2 = __uint_as_float(u1[0]), m3 = __uint_as_float(u1[1]);
-#pragma unroll
-        for (int c = 2; c < 32; c += 4) {
-          m0 = max3(m0, __uint_as_float(u0[c]), __uint_as_float(u0[c + 1]));
-          m1 = max3(m1, __uint_as_float(u0[c + 2]), __uint_as_float(u0[c + 3]));
-          m2 = max3(m2, __uint_as_float(u1[c]), __uint_as_float(u1[c + 1]));
-          m3 = max3(m3, __uint_as_float(u1[c + 2]), __uint_as_float(u1[c + 3]));
-        }
-        m = fmaxf(max3(m0, m1, m2), m3);
+        m = fmaxf(mx0, mx1);
       } else {
         m = -INFINITY;
         const uint32_t v0 = block_rows_mask32(a.g, J, half * 64), v1 = block_rows_mask32(a.g, J, half * 64 + 32);
