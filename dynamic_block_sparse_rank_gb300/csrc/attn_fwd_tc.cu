@@ -8,18 +8,21 @@
 // give the per-partition states of "DiTango: Cost-Effective Parallel Diffusion
 // Generation with Selective Attention State Reuse".
 //
-// One CTA per (query block, head); 8 warps:
-//   warp 0      TMA producer: Q tile once, then K/V tiles of each kept block
-//               through an ST-deep ring (the tile box *is* the space-time
-//               tile, so no token reordering pass exists).
+// One CTA per (query block, head); 12 warps:
+//   warps 0, 2  TMA producers: Q once and the K tiles of each kept block
+//               (warp 0), the V tiles (warp 2), through separate rings so K
+//               can be fetched further ahead (the tile box *is* the
+//               space-time tile, so no token reordering pass exists).
 //   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
 //               S buffers, O += P_j V_j with P_j read from TMEM.
-//   warps 4-7   softmax: thread = query row = TMEM lane.  Online softmax in
-//               base 2 with a lazy rescale: O and l are rescaled only when a
-//               row max grows by more than 2^8, which is exact because O and l
-//               always share the same reference max.  P overwrites S as a
-//               bf16 pair P_hi + P_lo, and O accumulates P_hi V + P_lo V.
-//   warps 2-3   idle.
+//   warps 4-11  softmax: two warps per query row quarter, each owning 64 of
+//               the 128 key columns (thread = row = TMEM lane).  Online
+//               softmax in base 2 with a lazy rescale: O and l are rescaled
+//               only when a row max grows by more than 2^8, which is exact
+//               because O and l always share the same reference max.  P
+//               overwrites S as a bf16 pair P_hi + P_lo, and O accumulates
+//               P_hi V + P_lo V.
+//   warp 3      idle.
 // TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,256+D) O.
 #include "internal.h"
 
@@ -39,15 +42,16 @@ struct FwdArgs {
   unsigned* status;
 };
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 softmax
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct FwdCfg {
   static constexpr int CH = D / 64;                  // 128-byte chunks of the head dim
   static constexpr int TILE = 128 * D * 2;           // bytes of one 128-row bf16 tile
-  static constexpr int ST = D == 128 ? 2 : 4;        // K/V ring depth
-  static constexpr int SMEM_TILES = TILE * (1 + 2 * ST);
+  static constexpr int KST = D == 128 ? 3 : 5;       // K ring depth (K is consumed first)
+  static constexpr int VST = D == 128 ? 2 : 4;       // V ring depth
+  static constexpr int SMEM_TILES = TILE * (1 + KST + VST);
 };
 
 __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
@@ -62,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, FwdArgs a) {
   using C = FwdCfg<D>;
-  constexpr int ST = C::ST;
+  constexpr int KST = C::KST, VST = C::VST;
   const int I = blockIdx.x, h = blockIdx.y;
   if (a.qb_active && !a.qb_active[I]) return;  // cached state stays untouched
 
@@ -70,36 +74,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + C::TILE;
-  uint8_t* sV = sK + ST * C::TILE;
+  uint8_t* sV = sK + KST * C::TILE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_TILES);
   uint64_t* qfull = bars;
-  uint64_t* kfull = bars + 1;
-  uint64_t* vfull = kfull + ST;
-  uint64_t* empty = vfull + ST;
-  uint64_t* sfull = empty + ST;   // 2
+  uint64_t* kfull = bars + 1;     // KST
+  uint64_t* kempty = kfull + KST; // KST
+  uint64_t* vfull = kempty + KST; // VST
+  uint64_t* vempty = vfull + VST; // VST
+  uint64_t* sfull = vempty + VST; // 2
   uint64_t* pfull = sfull + 2;    // 2
   uint64_t* odone = pfull + 2;    // 1
   uint64_t* drain = odone + 1;    // 1
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* pairbar = drain + 1;  // 4: the two softmax warps of a lane quarter meet here
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pairbar + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* n_sel_s = abort_flag + 1;
-  int* warp_cnt = n_sel_s + 1;  // 8
-  int* sel = warp_cnt + 8;      // k
+  int* warp_cnt = n_sel_s + 1;  // 16
+  float* half_max = reinterpret_cast<float*>(warp_cnt + 16);  // [2 parities][2 halves][128 rows]
+  float* half_l = half_max + 512;                             // [2 halves][128 rows]
+  int* sel = reinterpret_cast<int*>(half_l + 256);            // k
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     mbar_init(qfull, 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(kfull + s, 1);
+      mbar_init(kempty + s, 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(vfull + s, 1);
-      mbar_init(empty + s, 1);
+      mbar_init(vempty + s, 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sfull + s, 1);
-      mbar_init(pfull + s, 128);
+      mbar_init(pfull + s, 256);
     }
     mbar_init(odone, 1);
     mbar_init(drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(pairbar + q, 2);
     *abort_flag = 0;
     *n_sel_s = 0;
     fence_mbar_init();
@@ -135,37 +147,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   int t0, h0, w0;
   block_origin(a.g, I, t0, h0, w0);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------- producers
+    // warp 0: Q once, then the K tiles of the kept blocks (a KST-deep ring, freed as
+    // soon as S_j is computed); warp 2: the V tiles (a VST-deep ring, freed after P_j V_j).
+    const bool is_k = warp == 0;
     if (lane == 0 && n_sel > 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      mbar_expect_tx(qfull, C::TILE);
+      const int RS = is_k ? KST : VST;
+      uint8_t* ring = is_k ? sK : sV;
+      uint64_t* full = is_k ? kfull : vfull;
+      uint64_t* emp = is_k ? kempty : vempty;
+      const CUtensorMap* map = is_k ? &tmK : &tmV;
+      prefetch_tmap(map);
+      if (is_k) {
+        prefetch_tmap(&tmQ);
+        mbar_expect_tx(qfull, C::TILE);
 #pragma unroll
-      for (int c = 0; c < C::CH; ++c) tma_load_5d(sQ + c * 16384, &tmQ, qfull, c * 64, h, w0, h0, t0);
+        for (int c = 0; c < C::CH; ++c) tma_load_5d(sQ + c * 16384, &tmQ, qfull, c * 64, h, w0, h0, t0);
+      }
       int issued = 0;
       for (int j = 0; j < n_sel; ++j) {
-        const int s = j % ST;
-        if (j >= ST && !mbar_wait(empty + s, ((j / ST) - 1) & 1, a.status, abort_flag)) break;
+        const int s = j % RS;
+        if (j >= RS && !mbar_wait(emp + s, ((j / RS) - 1) & 1, a.status, abort_flag)) break;
         int jt0, jh0, jw0;
         block_origin(a.g, sel[j], jt0, jh0, jw0);
-        mbar_expect_tx(kfull + s, C::TILE);
+        mbar_expect_tx(full + s, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c)
-          tma_load_5d(sK + s * C::TILE + c * 16384, &tmK, kfull + s, c * 64, h, jw0, jh0, jt0);
-        mbar_expect_tx(vfull + s, C::TILE);
-#pragma unroll
-        for (int c = 0; c < C::CH; ++c)
-          tma_load_5d(sV + s * C::TILE + c * 16384, &tmV, vfull + s, c * 64, h, jw0, jh0, jt0);
+          tma_load_5d(ring + s * C::TILE + c * 16384, map, full + s, c * 64, h, jw0, jh0, jt0);
         issued = j + 1;
       }
       if (*abort_flag) {  // let copies in flight land before the CTA exits
-        wait_plain(qfull, 0);
-        for (int j = issued - ST < 0 ? 0 : issued - ST; j < issued; ++j) {
-          wait_plain(kfull + j % ST, (j / ST) & 1);
-          wait_plain(vfull + j % ST, (j / ST) & 1);
-        }
+        if (is_k) wait_plain(qfull, 0);
+        for (int j = issued - RS < 0 ? 0 : issued - RS; j < issued; ++j) wait_plain(full + j % RS, (j / RS) & 1);
       }
     }
     __syncwarp();
@@ -178,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tO = tmem + 256;
       bool ok = mbar_wait(qfull, 0, a.status, abort_flag);
       auto issue_S = [&](int j) -> bool {
-        const int s = j % ST;
-        if (!mbar_wait(kfull + s, (j / ST) & 1, a.status, abort_flag)) return false;
+        const int s = j % KST;
+        if (!mbar_wait(kfull + s, (j / KST) & 1, a.status, abort_flag)) return false;
         tc_fence_after();
         const uint32_t tS = tmem + (j & 1) * 128;
 #pragma unroll
@@ -189,14 +203,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                  kk > 0);
         }
         mma_commit(sfull + (j & 1));
+        mma_commit(kempty + s);  // K_j is no longer needed once S_j is done
         return true;
       };
       if (ok) ok = issue_S(0);
       for (int j = 0; ok && j < n_sel; ++j) {
         if (j + 1 < n_sel && !issue_S(j + 1)) break;
-        const int s = j % ST;
+        const int s = j % VST;
         if (!mbar_wait(pfull + (j & 1), (j >> 1) & 1, a.status, abort_flag)) break;
-        if (!mbar_wait(vfull + s, (j / ST) & 1, a.status, abort_flag)) break;
+        if (!mbar_wait(vfull + s, (j / VST) & 1, a.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t tP = tmem + (j & 1) * 128;
 #pragma unroll
@@ -206,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tO, tP + col, bV, idO, (j > 0 || kk > 0));
           mma_ts(tO, tP + col + 16, bV, idO, 1);
         }
-        mma_commit(empty + s);
+        mma_commit(vempty + s);
         mma_commit(odone);
       }
       mma_commit(drain);
@@ -215,8 +230,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax + epilogue
-    const int r = tid - 128;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // Two warps per TMEM lane quarter: warp half hf owns S columns [64 hf, 64 hf + 64)
+    // and O columns [hf D/2, (hf + 1) D/2) of the quarter's 32 rows.  The pair swaps
+    // its half-row maxima through shared memory (double-buffered by block parity) and
+    // keeps separate partial row sums l, added at the end.
+    const int quarter = warp & 3, hf = (warp - 4) >> 2;
+    const int r = quarter * 32 + lane;
+    // bounded meeting point of the pair: phase j for block j, phase n_sel for the epilogue
+    auto pair_sync = [&](uint32_t phase) -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pairbar + quarter);
+      return mbar_wait(pairbar + quarter, phase & 1, a.status, abort_flag);
+    };
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_sel; ++j) {
@@ -225,34 +251,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t tS = tmem + (j & 1) * 128 + lane_base;
+      const uint32_t tS = tmem + (j & 1) * 128 + lane_base + hf * 64;
       const int J = sel[j];
       const bool full = a.all_full || block_is_full(a.g, J);
-      // pass 1: this block's row max (S is read from TMEM twice rather than held in 128 registers)
-      float mx = -INFINITY;
+      // both 32-column chunks of this warp's half: loaded once, reduced by the load itself
+      uint32_t u0[32], u1[32];
+      float c0, c1;
+      tmem_ld32_max(tS, u0, c0);
+      tmem_ld32_max(tS + 32, u1, c1);
+      tmem_wait_ld();
+      const uint32_t vm0 = full ? 0xffffffffu : block_rows_mask32(a.g, J, hf * 64);
+      const uint32_t vm1 = full ? 0xffffffffu : block_rows_mask32(a.g, J, hf * 64 + 32);
+      float mx;
+      if (full) {
+        mx = fmaxf(c0, c1);
+      } else {
+        mx = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t u[32];
-        float cmax;
-        tmem_ld32_max(tS + cc * 32, u, cmax);
-        tmem_wait_ld();
-        if (full) {
-          mx = fmaxf(mx, cmax);
-        } else {
-          const uint32_t vm = block_rows_mask32(a.g, J, cc * 32);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if ((vm >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u[e]));
+        for (int e = 0; e < 32; ++e) {
+          if ((vm0 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u0[e]));
+          if ((vm1 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u1[e]));
         }
       }
-      mx *= a.scale_log2;
+      half_max[((j & 1) * 2 + hf) * 128 + r] = mx;
+      if (!pair_sync(j)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, half_max[((j & 1) * 2 + (hf ^ 1)) * 128 + r]) * a.scale_log2;
       const float m_new = fmaxf(m, mx);
       if (j == 0) {
         m = m_new;
       } else {
+        // both warps of the pair see the same row maxima, so they take the same decision
         const bool need = m_new > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          // O holds sum_{<j} P V relative to m: wait for the last P V, then rescale.
+          // O holds sum_{<j} P V relative to m: wait for the last P V, then rescale this half.
           if (!mbar_wait(odone, (j - 1) & 1, a.status, abort_flag)) {
             ok = false;
             break;
@@ -260,31 +294,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const float alpha = need ? ex2(m - m_new) : 1.f;
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < D / 64; ++cc) {
             uint32_t u[32];
-            tmem_ld32(tmem + 256 + lane_base + cc * 32, u);
+            const uint32_t tO = tmem + 256 + lane_base + hf * (D / 2) + cc * 32;
+            tmem_ld32(tO, u);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            tmem_st32(tmem + 256 + lane_base + cc * 32, u);
+            tmem_st32(tO, u);
           }
           tmem_wait_st();
           l *= alpha;
           if (need) m = m_new;
         }
       }
-      // pass 2: P = 2^(s - m) split as P_hi + P_lo (both bf16, P_lo = bf16(P - P_hi)) so that the
+      // P = 2^(s - m) split as P_hi + P_lo (both bf16, P_lo = bf16(P - P_hi)) so that the
       // P V product keeps ~16 significant bits of P: with the lazy reference max the dominant
-      // entries are not 1 and a single bf16 rounding would cost up to 2^-8 of O.  Chunk cc's
-      // 32 columns hold P_hi in their first 16 and P_lo in their last 16 (packed pairs).
-      float sum = 0.f;
+      // entries are not 1 and a single bf16 rounding would cost up to 2^-8 of O.  Each 32-column
+      // chunk holds P_hi in its first 16 columns and P_lo in its last 16 (packed pairs).
+      float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t u[32];
-        tmem_ld32(tS + cc * 32, u);
-        tmem_wait_ld();
+      for (int cc = 0; cc < 2; ++cc) {
+        const uint32_t(&u)[32] = cc ? u1 : u0;
+        const uint32_t vm = cc ? vm1 : vm0;
         uint32_t ph[16], pl[16];
-        const uint32_t vm = full ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float s0 = fmaf(__uint_as_float(u[2 * e]), a.scale_log2, -m);
@@ -292,14 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!((vm >> (2 * e)) & 1u)) s0 = -INFINITY;
           if (!((vm >> (2 * e + 1)) & 1u)) s1 = -INFINITY;
           const float p0 = ex2(s0), p1 = ex2(s1);
-          sum += p0 + p1;
+          sum0 += p0;
+          sum1 += p1;
           ph[e] = pack_bf16(p0, p1);
           pl[e] = pack_bf16(p0 - __uint_as_float(ph[e] << 16), p1 - __uint_as_float(ph[e] & 0xFFFF0000u));
         }
         tmem_st16(tS + cc * 32, ph);
         tmem_st16(tS + cc * 32 + 16, pl);
       }
-      l += sum;
+      l += sum0 + sum1;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(pfull + (j & 1));
@@ -308,18 +342,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // `drain` completes once every MMA of the CTA has finished (the MMA warp commits it last).
     if (n_sel > 0) ok = mbar_wait(drain, 0, a.status, abort_flag) && ok;
     tc_fence_after();
-    const float inv = (n_sel > 0 && l > 0.f) ? 1.f / l : 0.f;
+    half_l[hf * 128 + r] = l;
+    ok = pair_sync(n_sel) && ok;
+    const float lt = l + half_l[(hf ^ 1) * 128 + r];
+    const float inv = (n_sel > 0 && lt > 0.f) ? 1.f / lt : 0.f;
 #pragma unroll
-    for (int cc = 0; cc < D / 32; ++cc) {
+    for (int cc = 0; cc < D / 64; ++cc) {
+      const int col = hf * (D / 2) + cc * 32;  // first O column of this 32-column chunk
       uint32_t u[32];
       if (n_sel > 0) {
-        tmem_ld32(tmem + 256 + lane_base + cc * 32, u);
+        tmem_ld32(tmem + 256 + lane_base + col, u);
         tmem_wait_ld();
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) u[e] = 0u;
       }
-      uint8_t* dst = sQ + (cc >> 1) * 16384;
+      uint8_t* dst = sQ + (col >> 6) * 16384;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint4 v;
@@ -327,16 +365,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         v.y = pack_bf16(__uint_as_float(u[q4 * 8 + 2]) * inv, __uint_as_float(u[q4 * 8 + 3]) * inv);
         v.z = pack_bf16(__uint_as_float(u[q4 * 8 + 4]) * inv, __uint_as_float(u[q4 * 8 + 5]) * inv);
         v.w = pack_bf16(__uint_as_float(u[q4 * 8 + 6]) * inv, __uint_as_float(u[q4 * 8 + 7]) * inv);
-        *reinterpret_cast<uint4*>(dst + sw128_offset(r, (cc & 1) * 4 + q4)) = v;
+        *reinterpret_cast<uint4*>(dst + sw128_offset(r, ((col & 63) >> 3) + q4)) = v;
       }
     }
     const int n = block_row_token(a.g, I, r);
-    if (n >= 0)
+    if (hf == 0 && n >= 0)
       a.LSE[((long long)a.b * a.Hh + h) * a.N + n] =
-          (n_sel > 0 && l > 0.f) ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+          (n_sel > 0 && lt > 0.f) ? (m + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
     fence_async_smem();
-    named_bar(1, 128);
-    if (r == 0) {
+    named_bar(1, 256);
+    if (warp == 4 && lane == 0) {
 #pragma unroll
       for (int c = 0; c < C::CH; ++c) tma_store_5d(&tmO, sQ + c * 16384, c * 64, h, w0, h0, t0);
       bulk_commit();
@@ -355,7 +393,8 @@ template <int D>
 cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
                        int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 3 * C::ST + 6) + 4 * (3 + 8) + 4 * (size_t)p.k + 64;
+  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * (512 + 256) +
+                      4 * (size_t)p.k + 64;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   unsigned* status = status_ptr();
