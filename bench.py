@@ -82,6 +82,23 @@ def kept_pairs(wl, idx: np.ndarray) -> int:
     return int((per_row * sz[None, None, :]).sum())
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest value of x over all ranks (the slowest replica sets the step time)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_replica: float, ms: float) -> float:
+    """Aggregate throughput of `world` replicas that each do `flops_per_replica` in `ms`."""
+    return world * flops_per_replica / (ms / 1e3) / 1e12
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
@@ -286,11 +303,7 @@ def main():
         torch.cuda.synchronize()
     barrier()
     launches = sda.sda_kernel_launch_count() - launches0
-    ms = start.elapsed_time(end) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end) / args.steps, dist, dev)
     phase_names = ["predict", "fwd", "bwd_prepare", "bwd_dq", "bwd_dkdv"]
     phase_ms = {n: statistics.median(e[i].elapsed_time(e[i + 1]) for e in evs) for i, n in enumerate(phase_names)}
     status = sda.sda_get_device_status(stream.cuda_stream)
@@ -364,11 +377,8 @@ def main():
         barrier()
         ms_e2e = run_e2e(args.steps) / args.steps
         barrier()
-        if dist is not None:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": world * (f_fwd + f_bwd) / (ms_e2e / 1e3) / 1e12, "unit": "TFLOP/s",
+        ms_e2e = max_over_ranks(ms_e2e, dist, dev)
+        e2e = {"value": whole_job_tflops(world, f_fwd + f_bwd, ms_e2e), "unit": "TFLOP/s",
                "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "copies": "two copy streams, double-buffered device sets",
                "tokens_per_s": world * wl.B * wl.N / (ms_e2e / 1e3)}
@@ -426,7 +436,7 @@ def main():
                "seconds": c["seconds"]}
     line = {
         "metric": "sparse attn fwd+bwd TFLOP/s (step incl. predictor), 524,288 tokens",
-        "value": world * (f_fwd + f_bwd) / (ms / 1e3) / 1e12,
+        "value": whole_job_tflops(world, f_fwd + f_bwd, ms),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,

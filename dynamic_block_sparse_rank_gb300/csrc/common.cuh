@@ -117,14 +117,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // SDA_WAIT_LIMIT_NS, latches kStatusWaitTimeout into *status, raises the CTA's
 // abort flag and returns false; callers then stop issuing work.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, uint64_t limit_ns = SDA_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 7u) == 7u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > SDA_WAIT_LIMIT_NS) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicOr(status, kStatusWaitTimeout);
         *abort_flag = 1;
         return false;

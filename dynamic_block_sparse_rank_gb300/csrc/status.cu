@@ -41,3 +41,32 @@ extern "C" sda_status sda_get_device_status(void* stream) {
 }
 
 extern "C" unsigned long long sda_kernel_launch_count(void) { return sda::g_launches.load(std::memory_order_relaxed); }
+
+namespace sda {
+namespace {
+// A wait that nothing completes: the mbarrier expects one arrival that never
+// comes, so the bounded wait (the same code every kernel here uses) must run
+// out, latch the timeout bit and return.
+__global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_ns, int* result) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *result = mbar_wait(&bar, 0, status, &abort_flag, limit_ns) ? 1 : 0;
+}
+}  // namespace
+}  // namespace sda
+
+extern "C" sda_status sda_selftest_wait_timeout(unsigned limit_us, int* completed, void* stream) {
+  if (limit_us == 0 || limit_us > 1000000u || !completed) return SDA_ERR_INVALID_ARG;
+  unsigned* status = sda::status_ptr();
+  if (!status) return SDA_ERR_CUDA;
+  sda::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      status, 1000ull * limit_us, completed);
+  sda::note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? SDA_OK : SDA_ERR_CUDA;
+}

@@ -19,7 +19,7 @@ SDA_OP_PREDICT, SDA_OP_BWD = 0, 1
 
 EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_attn_fwd", "sda_attn_bwd",
            "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_merge_states",
-           "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_status_string")
+           "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_selftest_wait_timeout", "sda_status_string")
 
 
 class SdaError(RuntimeError):
@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
         L.sda_attn_bwd_dq.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
         L.sda_attn_bwd_dkdv.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
         L.sda_predict_blocks_noalloc.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp]
+        L.sda_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp, vp]
         L.sda_kernel_launch_count.argtypes = []
         L.sda_kernel_launch_count.restype = ctypes.c_ulonglong
         L.sda_merge_states.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i32, i32, i32, vp, vp, vp]
@@ -173,6 +174,11 @@ def sda_predict_blocks_noalloc(p, Q, K, Wq, Wk, block_idx, block_score=None, str
     """sda_predict_blocks with the library's built-in scratch instead of a caller workspace."""
     _check(lib().sda_predict_blocks_noalloc(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), _ptr(block_idx),
                                             _ptr(block_score), _stream(stream)), "sda_predict_blocks_noalloc")
+
+
+def sda_selftest_wait_timeout(limit_us, completed, stream=None):
+    _check(lib().sda_selftest_wait_timeout(int(limit_us), _ptr(completed), _stream(stream)),
+           "sda_selftest_wait_timeout")
 
 
 def sda_kernel_launch_count() -> int:

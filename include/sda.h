@@ -188,6 +188,14 @@ const char* sda_status_string(sda_status s);
 sda_status sda_predict_blocks_noalloc(const sda_problem* p, const void* Q, const void* K, const void* Wq,
                                       const void* Wk, int32_t* block_idx, float* block_score, void* stream);
 
+/* Diagnostic: launches one small kernel whose mbarrier wait can never complete
+ * and lets the bounded wait that every kernel of this library uses run out
+ * after limit_us microseconds (1 .. 1e6).  The kernel writes 0 to the device
+ * int *completed (1 would mean the wait completed) and latches the timeout
+ * bit, so a following sda_get_device_status returns SDA_ERR_DEVICE_TIMEOUT
+ * (and clears it).  Nothing faults or hangs; the context stays usable. */
+sda_status sda_selftest_wait_timeout(unsigned limit_us, int* completed, void* stream);
+
 /* Host only.  Number of CUDA kernels the library has launched in this process
  * (all devices, all calls); a caller can difference it around a region. */
 unsigned long long sda_kernel_launch_count(void);

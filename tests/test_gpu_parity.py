@@ -217,3 +217,18 @@ def test_backward_phases_equal_the_single_call_bitwise(sda):
     before = sda.sda_kernel_launch_count()
     sda.sda_attn_bwd(p, Q, K, V, O, LSE, dO, idx, *one, "f32", ws)
     assert sda.sda_kernel_launch_count() - before == 8 + 1 + 1 + 1  # prepare (8 + B), dq (B), dkdv (B)
+
+
+def test_bounded_wait_runs_out_and_reports_a_timeout(sda):
+    # the wait is made to run out on purpose (nothing ever arrives); the kernel returns,
+    # the status word reports it once, and the device keeps working afterwards
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    done = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    sda.sda_selftest_wait_timeout(2000, done)
+    torch.cuda.synchronize()
+    assert int(done.item()) == 0
+    assert sda.sda_get_device_status() == sda.SDA_ERR_DEVICE_TIMEOUT
+    assert sda.sda_get_device_status() == sda.SDA_OK  # latch cleared
+    from tests import smoke_check
+
+    smoke_check.run()  # the context is still usable
