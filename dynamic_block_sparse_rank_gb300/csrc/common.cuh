@@ -133,6 +133,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   }
 }
 
+// Non-blocking test of the phase (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_wait, but polling without suspension: for short, latency-critical
+// waits on a pipeline partner (the wake-up from a suspended wait is slower).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, unsigned* status,
+                                               volatile int* abort_flag, uint64_t limit_ns = SDA_WAIT_LIMIT_NS) {
+  if (mbar_test_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicOr(status, kStatusWaitTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA (bulk tensor copies).  Destination/source shared addresses are CTA-local.
 __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
@@ -257,6 +289,55 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// Warp-converged issue.  Every lane of the MMA warp runs the issue loop with the
+// same operands; only the lane whose `leader` is nonzero issues.  The leader is
+// elected once (elect_leader) and reused, so the lane that issues the MMAs is the
+// lane that commits them.  Keeping the loop converged lets the operands live in
+// warp-uniform registers: the issue rate then matches the tensor pipe instead of
+// being limited by per-instruction operand moves.
+__device__ __forceinline__ uint32_t elect_leader() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred;
+}
+
+__device__ __forceinline__ void mma_ss_by(uint32_t leader, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accum), "r"(leader)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_by(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 e, %5, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accum), "r"(leader)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_by(uint32_t leader, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+      "r"(leader)
+      : "memory");
+}
+
+// Bounded wait by a whole warp; the result is the same on every lane.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* status, volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
+}
+__device__ __forceinline__ bool warp_wait_spin(uint64_t* bar, uint32_t parity, unsigned* status,
+                                               volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait_spin(bar, parity, status, abort_flag));
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane (base lane + i).

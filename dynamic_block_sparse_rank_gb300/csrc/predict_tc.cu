@@ -13,15 +13,18 @@
 //                 (no-swizzle K-major core matrices, tile after tile), so the
 //                 score kernel fetches each tile with one bulk copy.  Rows
 //                 outside the grid are written as zeros.
-//   score_kernel  per (two query blocks, head): streams every k~ tile through
-//                 an 8-deep ring; for each key block J two MMAs (one per query
-//                 block, M=128, N=128, K=r) land in a double-buffered TMEM
-//                 accumulator; 16 epilogue warps (one per TMEM lane quarter,
-//                 query block and column half) reduce each 128x128 tile to its
-//                 max: the reducing TMEM load gives each thread the max of its
-//                 columns, then one redux.sync over order-preserving keys and a
-//                 shared-memory atomic max per warp.  When the row of n_b scores is complete, the 8
-//                 warps of each query block select its top k (radix select).
+//   score_kernel  per (QB query blocks, head), QB = 4 when its score rows fit in
+//                 shared memory (else 2 or 1): streams every k~ tile through a
+//                 ring; each (key block, query block) pair is one M=128, N=128,
+//                 K=r accumulation in one of four 128-column TMEM buffers, issued
+//                 by a warp-converged MMA warp.  Four epilogue groups of four
+//                 warps (one per TMEM lane quarter) each drain one buffer: the
+//                 reducing TMEM load gives each thread the max of its columns,
+//                 then one redux.sync over order-preserving keys and a shared-
+//                 memory atomic max per warp.  Four buffers let the MMA run
+//                 three pairs ahead of the slowest group.  When the rows of n_b
+//                 scores are complete, each query block's team of warps selects
+//                 its top k (radix select).
 #include "internal.h"
 #include "topk.cuh"
 
@@ -85,12 +88,14 @@ __global__ void __launch_bounds__(256) proj_kernel(Geom g, int Hh, int d, long l
 // ------------------------------------------------------------------ scores + top-k
 template <int R>
 struct ScoreCfg {
+  static constexpr int TB = 128 * R * 2;      // bytes of one operand tile
   static constexpr int ST = R <= 32 ? 8 : 4;  // k~ ring depth
 };
-// warp 0 producer, warp 1 MMA, warps 2..17 epilogue: 4 warps per TMEM lane
-// quarter, one for each (query block, column half) pair.
+// warp 0 producer, warp 1 MMA, warps 2..17 epilogue in 4 groups of 4 (one warp
+// per TMEM lane quarter); group g drains accumulator buffer g.
 constexpr int kEpiWarps = 16;
 constexpr int kScoreThreads = (2 + kEpiWarps) * 32;
+constexpr int kAccBufs = 4;  // TMEM accumulators of 128 columns: one (query block, key block) pair each
 
 struct ScoreArgs {
   Geom g;
@@ -102,10 +107,14 @@ struct ScoreArgs {
   unsigned* status;
 };
 
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
+// Shared memory of one CTA: QB query tiles, the k~ ring, QB rows of nb keys,
+// top-k scratch, barriers, flags.  The first 1024 bytes absorb the alignment.
+__host__ __device__ inline size_t score_smem_bytes(int R, int ST, int QB, int nb) {
+  const size_t TB = (size_t)128 * R * 2;
+  size_t off = 1024 + (QB + ST) * TB + (size_t)QB * nb * 4 + QB * sizeof(TopkScratch);
+  off = (off + 7) & ~size_t(7);
+  off += 8 * (1 + 2 * ST + 2 * kAccBufs + 1) + 8 + nb;
+  return off + 64;
 }
 
 __device__ __forceinline__ unsigned warp_max_u32(unsigned v) {
@@ -121,28 +130,42 @@ __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-template <int R>
+// Max of the loaded values whose column bit is set in v0 (u0) or v1 (u1).
+__device__ __forceinline__ float masked_max64(uint32_t v0, uint32_t v1, const uint32_t (&u0)[32],
+                                              const uint32_t (&u1)[32]) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    if ((v0 >> c) & 1u) m = fmaxf(m, __uint_as_float(u0[c]));
+    if ((v1 >> c) & 1u) m = fmaxf(m, __uint_as_float(u1[c]));
+  }
+  return m;
+}
+
+// One CTA per (QB consecutive query blocks, head).  For every key block J and
+// query block q the pair P = J QB + q is accumulated (M=128 query rows, N=128
+// key rows, K=r) in TMEM buffer P mod 4 and reduced to its max by group P mod 4.
+template <int R, int QB>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
-  constexpr int TB = 128 * R * 2;  // bytes of one operand tile
+  constexpr int TB = ScoreCfg<R>::TB;
   constexpr int kStages = ScoreCfg<R>::ST;
   const int nb = a.g.nb;
   const int h = blockIdx.y;
-  const int I0 = 2 * blockIdx.x;
-  const int I1 = I0 + 1 < nb ? I0 + 1 : I0;
+  const int I0 = QB * blockIdx.x;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                      // 2 query tiles
-  uint8_t* sB = sA + 2 * TB;               // kStages key tiles
-  unsigned* keys = reinterpret_cast<unsigned*>(sB + kStages * TB);  // 2 x nb
-  TopkScratch* tks = reinterpret_cast<TopkScratch*>(keys + 2 * nb);  // 2
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tks + 2);
-  uint64_t* afull_q = bars;                // query tiles loaded
-  uint64_t* kfull = bars + 1;              // kStages
-  uint64_t* kempty = kfull + kStages;      // kStages
-  uint64_t* accf = kempty + kStages;       // 2: accumulator buffer ready
-  uint64_t* acce = accf + 2;               // 2: accumulator buffer drained
-  uint64_t* drain = acce + 2;
+  uint8_t* sA = smem;                                                // QB query tiles
+  uint8_t* sB = sA + QB * TB;                                        // kStages key tiles
+  unsigned* keys = reinterpret_cast<unsigned*>(sB + kStages * TB);  // QB x nb
+  TopkScratch* tks = reinterpret_cast<TopkScratch*>(keys + QB * nb);
+  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(tks + QB) + 7) & ~uintptr_t(7));
+  uint64_t* afull_q = bars;            // query tiles loaded
+  uint64_t* kfull = bars + 1;          // kStages
+  uint64_t* kempty = kfull + kStages;  // kStages
+  uint64_t* accf = kempty + kStages;   // kAccBufs: accumulator holds a finished pair
+  uint64_t* acce = accf + kAccBufs;    // kAccBufs: accumulator read out
+  uint64_t* drain = acce + kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   uint8_t* full = reinterpret_cast<uint8_t*>(abort_flag + 1);  // nb: key block J lies inside the grid
@@ -154,15 +177,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
       mbar_init(kfull + s, 1);
       mbar_init(kempty + s, 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(accf + s, 1);
-      mbar_init(acce + s, kEpiWarps);
+      mbar_init(acce + s, kEpiWarps / kAccBufs);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  for (int e = tid; e < 2 * nb; e += kScoreThreads) keys[e] = 0u;  // below every real key
+  for (int e = tid; e < QB * nb; e += kScoreThreads) keys[e] = 0u;  // below every real key
   for (int J = tid; J < nb; J += kScoreThreads) full[J] = block_is_full(a.g, J) ? 1 : 0;
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -172,12 +195,15 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long head_tiles = ((long long)a.b * a.Hh + h) * nb;
+  const int n_pairs = nb * QB;
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_expect_tx(afull_q, 2 * TB);
-      bulk_load(sA, a.qt + (head_tiles + I0) * TB, TB, afull_q);
-      bulk_load(sA + TB, a.qt + (head_tiles + I1) * TB, TB, afull_q);
+      mbar_expect_tx(afull_q, QB * TB);
+      for (int q = 0; q < QB; ++q) {
+        const int I = I0 + q < nb ? I0 + q : nb - 1;
+        bulk_load(sA + q * TB, a.qt + (head_tiles + I) * TB, TB, afull_q);
+      }
       int issued = 0;
       for (int J = 0; J < nb; ++J) {
         const int s = J % kStages;
@@ -194,87 +220,93 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t SBO = (R / 8) * 128;
-      const uint32_t aA = smem_u32(sA), aB = smem_u32(sB);
-      bool ok = mbar_wait(afull_q, 0, a.status, abort_flag);
-      for (int J = 0; ok && J < nb; ++J) {
-        const int s = J % kStages, buf = J & 1;
-        if (!mbar_wait(kfull + s, (J / kStages) & 1, a.status, abort_flag)) break;
-        if (J >= 2 && !mbar_wait(acce + buf, ((J >> 1) - 1) & 1, a.status, abort_flag)) break;
+    // Whole warp, one elected lane issues; descriptors advance by adding to the
+    // start-address field (16-byte units).
+    const uint32_t leader = elect_leader();
+    constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t SBO = (R / 8) * 128;
+    const uint64_t dA = smem_desc(smem_u32(sA), 128, SBO, 0), dB = smem_desc(smem_u32(sB), 128, SBO, 0);
+    bool ok = warp_wait(afull_q, 0, a.status, abort_flag);
+    for (int J = 0; ok && J < nb; ++J) {
+      const int s = J % kStages;
+      if (!(ok = warp_wait(kfull + s, (J / kStages) & 1, a.status, abort_flag))) break;
+#pragma unroll
+      for (int q = 0; q < QB; ++q) {
+        const int P = J * QB + q, buf = P & (kAccBufs - 1);
+        if (P >= kAccBufs && !(ok = warp_wait(acce + buf, ((P >> 2) - 1) & 1, a.status, abort_flag))) break;
         tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-#pragma unroll
-          for (int kk = 0; kk < R / 16; ++kk) {
-            const uint64_t da = smem_desc(aA + q * TB + kk * 256, 128, SBO, 0);
-            const uint64_t db = smem_desc(aB + s * TB + kk * 256, 128, SBO, 0);
-            mma_ss(tmem + buf * 256 + q * 128, da, db, id, kk > 0);
-          }
-        }
-        mma_commit(accf + buf);
-        mma_commit(kempty + s);
+        for (int kk = 0; kk < R / 16; ++kk)
+          mma_ss_by(leader, tmem + buf * 128, dA + (uint64_t)((q * TB + kk * 256) >> 4),
+                    dB + (uint64_t)((s * TB + kk * 256) >> 4), id, kk > 0);
+        mma_commit_by(leader, accf + buf);
       }
-      mma_commit(drain);
-      wait_plain(drain, 0);
+      mma_commit_by(leader, kempty + s);
     }
+    mma_commit_by(leader, drain);
+    wait_plain(drain, 0);
     __syncwarp();
   } else {
-    // epilogue warp e: TMEM lane quarter = warp % 4, (query block, column half) = e / 4
     const int e = warp - 2;
-    const int quarter = warp & 3;
-    const int grp = (e >> 2) >> 1, half = (e >> 2) & 1;
-    const int I = grp ? I1 : I0;
+    const int grp = e >> 2;         // accumulator buffer this warp drains
+    const int quarter = warp & 3;   // TMEM lanes 32 quarter .. 32 quarter + 31 (query rows)
     const int row = quarter * 32 + lane;
-    const bool row_ok = block_row_token(a.g, I, row) >= 0;
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    unsigned* mykeys = keys + grp * nb;
-    for (int J = 0; J < nb; ++J) {
-      const int buf = J & 1;
-      if (!mbar_wait(accf + buf, (J >> 1) & 1, a.status, abort_flag)) break;
+    unsigned rowok = 0;
+#pragma unroll
+    for (int q = 0; q < QB; ++q) {
+      const int I = I0 + q < nb ? I0 + q : nb - 1;
+      rowok |= (block_row_token(a.g, I, row) >= 0 ? 1u : 0u) << q;
+    }
+    const uint32_t taddr = tmem + grp * 128 + ((uint32_t)(quarter * 32) << 16);
+    for (int P = grp; P < n_pairs; P += kAccBufs) {
+      const int J = P / QB, q = P % QB;
+      if (!mbar_wait(accf + grp, (P >> 2) & 1, a.status, abort_flag)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + buf * 256 + grp * 128 + half * 64 + lane_base;
+      const bool fj = full[J] != 0;
+      uint32_t v0 = ~0u, v1 = ~0u, v2 = ~0u, v3 = ~0u;  // key rows of J inside the grid, per 32 columns
+      if (!fj) {
+        v0 = block_rows_mask32(a.g, J, 0);
+        v1 = block_rows_mask32(a.g, J, 32);
+        v2 = block_rows_mask32(a.g, J, 64);
+        v3 = block_rows_mask32(a.g, J, 96);
+      }
       uint32_t u0[32], u1[32];
-      float mx0, mx1;
-      tmem_ld32_max(taddr, u0, mx0);  // the load also reduces each thread's 32 values to their max
-      tmem_ld32_max(taddr + 32, u1, mx1);
+      float m0, m1;
+      tmem_ld32_max(taddr, u0, m0);  // the load also reduces each thread's 32 values to their max
+      tmem_ld32_max(taddr + 32, u1, m1);
+      tmem_wait_ld();
+      float m = fj ? fmaxf(m0, m1) : masked_max64(v0, v1, u0, u1);
+      tmem_ld32_max(taddr + 64, u0, m0);
+      tmem_ld32_max(taddr + 96, u1, m1);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce + buf);  // values are in registers: the buffer may be refilled
-      float m;
-      if (full[J]) {
-        m = fmaxf(mx0, mx1);
-      } else {
-        m = -INFINITY;
-        const uint32_t v0 = block_rows_mask32(a.g, J, half * 64), v1 = block_rows_mask32(a.g, J, half * 64 + 32);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if ((v0 >> c) & 1u) m = fmaxf(m, __uint_as_float(u0[c]));
-          if ((v1 >> c) & 1u) m = fmaxf(m, __uint_as_float(u1[c]));
-        }
-      }
+      if (lane == 0) mbar_arrive(acce + grp);  // values are in registers: the buffer may be refilled
+      m = fmaxf(m, fj ? fmaxf(m0, m1) : masked_max64(v2, v3, u0, u1));
       // order-preserving key; 0 (below every real key) for rows/columns outside the grid
-      const unsigned key = (row_ok && m > -INFINITY) ? order_key(m) : 0u;
+      const unsigned key = (((rowok >> q) & 1u) && m > -INFINITY) ? order_key(m) : 0u;
       const unsigned wmax = warp_max_u32(key);
-      if (lane == 0 && wmax != 0u) atomicMax(mykeys + J, wmax);
+      if (lane == 0 && wmax != 0u) atomicMax(keys + q * nb + J, wmax);
     }
     named_bar(1, kEpiWarps * 32);
-    // keys -> scores (inverse of order_key), in place; then top-k per query block by its 8 warps
-    const int tg = (e & 7) * 32 + lane;  // thread index inside this query block's 8 warps
+    // keys -> scores (inverse of order_key), in place; then top-k per query block
+    // by its team of kEpiWarps / QB warps
+    constexpr int kTeam = (kEpiWarps / QB) * 32;
+    const int q = e % QB;
+    const int tg = (e / QB) * 32 + lane;
+    unsigned* mykeys = keys + q * nb;
     float* srow = reinterpret_cast<float*>(mykeys);
-    for (int J = tg; J < nb; J += 256) {
+    for (int J = tg; J < nb; J += kTeam) {
       const unsigned kq = mykeys[J];
       const unsigned u = (kq & 0x80000000u) ? (kq & 0x7FFFFFFFu) : ~kq;
       srow[J] = kq == 0u ? -INFINITY : __uint_as_float(u);
     }
-    named_bar(2 + grp, 256);
-    const bool write = grp == 0 || I1 != I0;
-    if (write) {
+    named_bar(2 + q, kTeam);
+    const int I = I0 + q;
+    if (I < nb) {
       if (a.score)
-        for (int J = tg; J < nb; J += 256) a.score[(head_tiles + I) * nb + J] = srow[J];
-      topk_select(srow, nb, a.k, a.idx + (head_tiles + I) * a.k, tg, 256, 2 + grp, tks + grp);
+        for (int J = tg; J < nb; J += kTeam) a.score[(head_tiles + I) * nb + J] = srow[J];
+      topk_select(srow, nb, a.k, a.idx + (head_tiles + I) * a.k, tg, kTeam, 2 + q, tks + q);
     }
   }
   __syncthreads();
@@ -283,6 +315,24 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     tmem_dealloc(tmem, 512);
   }
 }
+
+template <int R, int QB>
+cudaError_t launch_score(const Prob& p, ScoreArgs& a, cudaStream_t st) {
+  constexpr int kStages = ScoreCfg<R>::ST;
+  const size_t raw = score_smem_bytes(R, kStages, QB, p.g.nb);
+  // Keep one CTA per SM: each CTA owns all 512 TMEM columns.
+  const size_t smem = raw > 120 * 1024 ? raw : 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(score_kernel<R, QB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 sg((p.g.nb + QB - 1) / QB, p.Hh);
+  for (int b = 0; b < p.B; ++b) {
+    a.b = b;
+    score_kernel<R, QB><<<sg, kScoreThreads, smem, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+constexpr size_t kMaxScoreSmem = 227 * 1024;
 
 template <int R>
 cudaError_t launch_predict(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, int32_t* idx,
@@ -301,14 +351,6 @@ cudaError_t launch_predict(const Prob& p, const void* Q, const void* K, const vo
                                            static_cast<const __nv_bfloat16*>(Wk), kt, b);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  constexpr int kStages = ScoreCfg<R>::ST;
-  const size_t ssmem_raw = 1024 + (size_t)(2 + kStages) * 128 * R * 2 + 2 * (size_t)p.g.nb * 4 + 2 * sizeof(TopkScratch) +
-                       8 * (1 + 2 * kStages + 5) + 16 + (size_t)p.g.nb + 64;
-  // Keep one CTA per SM: each CTA owns all 512 TMEM columns.
-  const size_t ssmem = ssmem_raw > 120 * 1024 ? ssmem_raw : 120 * 1024;
-  if ((e = cudaFuncSetAttribute(score_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssmem)) !=
-      cudaSuccess)
-    return e;
   unsigned* status = status_ptr();
   if (!status) return cudaErrorUnknown;
   ScoreArgs a;
@@ -320,13 +362,16 @@ cudaError_t launch_predict(const Prob& p, const void* Q, const void* K, const vo
   a.idx = idx;
   a.score = score;
   a.status = status;
-  dim3 sg((p.g.nb + 1) / 2, p.Hh);
-  for (int b = 0; b < p.B; ++b) {
-    a.b = b;
-    score_kernel<R><<<sg, kScoreThreads, ssmem, st>>>(a);
-  }
+  constexpr int kStages = ScoreCfg<R>::ST;
+  // As many query blocks per CTA as their score rows allow in shared memory.
+  if (score_smem_bytes(R, kStages, 4, p.g.nb) <= kMaxScoreSmem)
+    e = launch_score<R, 4>(p, a, st);
+  else if (score_smem_bytes(R, kStages, 2, p.g.nb) <= kMaxScoreSmem)
+    e = launch_score<R, 2>(p, a, st);
+  else
+    e = launch_score<R, 1>(p, a, st);
   note_launches(3 * p.B);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
