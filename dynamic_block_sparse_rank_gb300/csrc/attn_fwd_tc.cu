@@ -12,17 +12,23 @@
 //   warps 0, 2  TMA producers: Q once and the K tiles of each kept block
 //               (warp 0), the V tiles (warp 2), through separate rings so K
 //               can be fetched further ahead (the tile box *is* the
-//               space-time tile, so no token reordering pass exists).
-//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
-//               S buffers, O += P_j V_j with P_j read from TMEM.
+//               space-time tile, so no token reordering pass exists).  Warp 0
+//               also arrives on P_j's barrier once K_{j+2} has landed.
+//   warp 1      TMEM owner and MMA issuer (converged warp, one elected lane):
+//               S_j = Q K_j^T into one of two TMEM S buffers, then, once P_j
+//               is ready, O += P_j V_j with P_j read from TMEM.
 //   warps 4-11  softmax: two warps per query row quarter, each owning 64 of
-//               the 128 key columns (thread = row = TMEM lane).  Online
-//               softmax in base 2 with a lazy rescale: O and l are rescaled
-//               only when a row max grows by more than 2^8, which is exact
-//               because O and l always share the same reference max.  P
-//               overwrites S as a bf16 pair P_hi + P_lo, and O accumulates
-//               P_hi V + P_lo V.
-//   warp 3      idle.
+//               the 128 key columns (thread = row = TMEM lane); each also
+//               reads the other half's maximum, so the pair never waits on
+//               each other inside the loop.  Online softmax in base 2 with a
+//               lazy rescale: O and l are rescaled only when a row max grows
+//               by more than 2^8, which is exact because O and l always share
+//               the same reference max.  P overwrites S in bf16; O is divided
+//               by the sum of those bf16 weights (so the rounding of a
+//               dominant weight cancels), LSE uses the fp32 sum.
+//   warp 3      arrives on P_j's barrier once V_j has landed: with the two
+//               producer arrivals that barrier covers every input of P_j V_j
+//               and of S_{j+2}, so the MMA warp waits once per block.
 // TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,256+D) O.
 #include "internal.h"
 
@@ -42,7 +48,9 @@ struct FwdArgs {
   unsigned* status;
 };
 
-constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 softmax
+constexpr int kThreads = 384;  // warps 0, 2 TMA, warp 1 MMA, warps 4-11 softmax
+// P_j barrier: the 256 softmax threads, the K producer (K_{j+2} landed) and warp 3 (V_j landed).
+constexpr int kPfullCount = 256 + 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
@@ -90,9 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* n_sel_s = abort_flag + 1;
   int* warp_cnt = n_sel_s + 1;  // 16
-  float* half_max = reinterpret_cast<float*>(warp_cnt + 16);  // [2 parities][2 halves][128 rows]
-  float* half_l = half_max + 512;                             // [2 halves][128 rows]
-  int* sel = reinterpret_cast<int*>(half_l + 256);            // k
+  float* half_l = reinterpret_cast<float*>(warp_cnt + 16);  // [2 halves][l, l of bf16 P][128 rows]
+  int* sel = reinterpret_cast<int*>(half_l + 512);           // k
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -107,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sfull + s, 1);
-      mbar_init(pfull + s, 256);
+      mbar_init(pfull + s, kPfullCount);
     }
     mbar_init(odone, 1);
     mbar_init(drain, 1);
@@ -165,17 +172,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) tma_load_5d(sQ + c * 16384, &tmQ, qfull, c * 64, h, w0, h0, t0);
       }
-      int issued = 0;
-      for (int j = 0; j < n_sel; ++j) {
-        const int s = j % RS;
-        if (j >= RS && !mbar_wait(emp + s, ((j / RS) - 1) & 1, a.status, abort_flag)) break;
+      auto issue = [&](int i) {
+        const int s = i % RS;
         int jt0, jh0, jw0;
-        block_origin(a.g, sel[j], jt0, jh0, jw0);
+        block_origin(a.g, sel[i], jt0, jh0, jw0);
         mbar_expect_tx(full + s, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c)
           tma_load_5d(ring + s * C::TILE + c * 16384, map, full + s, c * 64, h, jw0, jh0, jt0);
-        issued = j + 1;
+      };
+      int issued = 0;
+      for (; issued < RS && issued < n_sel; ++issued) issue(issued);
+      if (is_k) {
+        // Arrive on pfull_j once K_{j+2} has landed (S_{j+2} is issued after the MMA
+        // warp's pfull_j wait, without a wait of its own); then refill the slot of K_j.
+        for (int j = 0; j < n_sel; ++j) {
+          const int t = j + 2;  // issued already: t < j + KST
+          if (t < n_sel && !mbar_wait(kfull + t % KST, (t / KST) & 1, a.status, abort_flag)) break;
+          // phase j - 2 of the same barrier completes before this arrival for phase j
+          if (j >= 2 && !mbar_wait(pfull + (j & 1), ((j >> 1) - 1) & 1, a.status, abort_flag)) break;
+          mbar_arrive(pfull + (j & 1));
+          if (issued < n_sel) {  // issued == j + KST: it reuses the slot of K_j
+            if (!mbar_wait(kempty + j % KST, (j / KST) & 1, a.status, abort_flag)) break;
+            issue(issued++);
+          }
+        }
+      } else {
+        for (; issued < n_sel; ++issued) {
+          const int i = issued;
+          if (!mbar_wait(vempty + i % VST, ((i / VST) - 1) & 1, a.status, abort_flag)) break;
+          issue(i);
+        }
       }
       if (*abort_flag) {  // let copies in flight land before the CTA exits
         if (is_k) wait_plain(qfull, 0);
@@ -183,67 +210,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------- V arrivals
+    // Arrive on pfull_j once V_j has landed, so the MMA warp's pfull_j wait covers it.
+    if (lane == 0) {
+      for (int j = 0; j < n_sel; ++j) {
+        if (!mbar_wait(vfull + j % VST, (j / VST) & 1, a.status, abort_flag)) break;
+        if (j >= 2 && !mbar_wait(pfull + (j & 1), ((j >> 1) - 1) & 1, a.status, abort_flag)) break;
+        mbar_arrive(pfull + (j & 1));
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0 && n_sel > 0) {
+    // Whole warp, one elected lane issues; descriptors advance by adding to the
+    // start-address field (16-byte units).  One wait per block: pfull_j (softmax of
+    // block j done, V_j and K_{j+2} landed); only K_0 and K_1 are waited on directly.
+    if (n_sel > 0) {
+      const uint32_t leader = elect_leader();
       constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+      const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024, 2);
+      const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, 2);
+      const uint64_t dV = smem_desc(smem_u32(sV), 16384, 1024, 2);
       const uint32_t tO = tmem + 256;
-      bool ok = mbar_wait(qfull, 0, a.status, abort_flag);
-      auto issue_S = [&](int j) -> bool {
+      auto issue_S = [&](int j) {
         const int s = j % KST;
-        if (!mbar_wait(kfull + s, (j / KST) & 1, a.status, abort_flag)) return false;
         tc_fence_after();
         const uint32_t tS = tmem + (j & 1) * 128;
+        const uint64_t dKs = dK + (uint64_t)((s * C::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS, smem_desc(aQ + off, 16, 1024, 2), smem_desc(aK + s * C::TILE + off, 16, 1024, 2), idS,
-                 kk > 0);
+          constexpr int kChunk = 16384 >> 4;
+          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 2;  // 64-column chunk, 16-column step
+          mma_ss_by(leader, tS, dQ + off, dKs + off, idS, kk > 0);
         }
-        mma_commit(sfull + (j & 1));
-        mma_commit(kempty + s);  // K_j is no longer needed once S_j is done
-        return true;
+        mma_commit_by(leader, sfull + (j & 1));
+        mma_commit_by(leader, kempty + s);  // K_j is no longer needed once S_j is done
       };
-      if (ok) ok = issue_S(0);
+      bool ok = warp_wait(qfull, 0, a.status, abort_flag) && warp_wait(kfull, 0, a.status, abort_flag);
+      if (ok) issue_S(0);
       for (int j = 0; ok && j < n_sel; ++j) {
-        if (j + 1 < n_sel && !issue_S(j + 1)) break;
-        const int s = j % VST;
-        if (!mbar_wait(pfull + (j & 1), (j >> 1) & 1, a.status, abort_flag)) break;
-        if (!mbar_wait(vfull + s, (j / VST) & 1, a.status, abort_flag)) break;
-        tc_fence_after();
-        const uint32_t tP = tmem + (j & 1) * 128;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // keys 16 kk .. 16 kk + 15: P_hi, then P_lo, times the same V rows
-          const uint64_t bV = smem_desc(aV + s * C::TILE + kk * 2048, 16384, 1024, 2);
-          const uint32_t col = (kk >> 1) * 32 + (kk & 1) * 8;
-          mma_ts(tO, tP + col, bV, idO, (j > 0 || kk > 0));
-          mma_ts(tO, tP + col + 16, bV, idO, 1);
+        if (j + 1 < n_sel) {
+          // K_{j+1} landed: waited directly for K_1, implied by pfull_{j-1} after that
+          if (j == 0 && !(ok = warp_wait(kfull + 1 % KST, (1 / KST) & 1, a.status, abort_flag))) break;
+          issue_S(j + 1);
         }
-        mma_commit(vempty + s);
-        mma_commit(odone);
+        if (!(ok = warp_wait(pfull + (j & 1), (j >> 1) & 1, a.status, abort_flag))) break;
+        tc_fence_after();
+        const int s = j % VST;
+        const uint32_t tP = tmem + (j & 1) * 128;
+        const uint64_t dVs = dV + (uint64_t)((s * C::TILE) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // keys 16 kk .. 16 kk + 15
+          mma_ts_by(leader, tO, tP + (kk >> 1) * 32 + (kk & 1) * 8, dVs + (uint64_t)(kk * (2048 >> 4)), idO,
+                    (j > 0 || kk > 0));
+        mma_commit_by(leader, vempty + s);
+        mma_commit_by(leader, odone);
       }
-      mma_commit(drain);
+      mma_commit_by(leader, drain);
       wait_plain(drain, 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax + epilogue
     // Two warps per TMEM lane quarter: warp half hf owns S columns [64 hf, 64 hf + 64)
-    // and O columns [hf D/2, (hf + 1) D/2) of the quarter's 32 rows.  The pair swaps
-    // its half-row maxima through shared memory (double-buffered by block parity) and
-    // keeps separate partial row sums l, added at the end.
+    // and O columns [hf D/2, (hf + 1) D/2) of the quarter's 32 rows.  Each warp also
+    // reads the maximum of the other half (the reducing load returns it without
+    // keeping the values), so both warps of a pair hold the same row maxima and take
+    // the same rescale decisions without meeting.  They meet once, for the epilogue.
     const int quarter = warp & 3, hf = (warp - 4) >> 2;
     const int r = quarter * 32 + lane;
-    // bounded meeting point of the pair: phase j for block j, phase n_sel for the epilogue
     auto pair_sync = [&](uint32_t phase) -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(pairbar + quarter);
       return mbar_wait(pairbar + quarter, phase & 1, a.status, abort_flag);
     };
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY;
+    float l = 0.f;   // sum of P (fp32): gives LSE
+    float lr = 0.f;  // sum of bf16(P), the weights the P V product uses: divides O
     bool ok = true;
     for (int j = 0; j < n_sel; ++j) {
       if (!mbar_wait(sfull + (j & 1), (j >> 1) & 1, a.status, abort_flag)) {
@@ -251,17 +297,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t tS = tmem + (j & 1) * 128 + lane_base + hf * 64;
+      const uint32_t tSb = tmem + (j & 1) * 128 + lane_base;
+      const uint32_t tS = tSb + hf * 64;
       const int J = sel[j];
       const bool full = a.all_full || block_is_full(a.g, J);
-      // both 32-column chunks of this warp's half: loaded once, reduced by the load itself
+      uint32_t vo0 = ~0u, vo1 = ~0u, vm0 = ~0u, vm1 = ~0u;  // key rows of J inside the grid
+      if (!full) {
+        vo0 = block_rows_mask32(a.g, J, (hf ^ 1) * 64);
+        vo1 = block_rows_mask32(a.g, J, (hf ^ 1) * 64 + 32);
+        vm0 = block_rows_mask32(a.g, J, hf * 64);
+        vm1 = block_rows_mask32(a.g, J, hf * 64 + 32);
+      }
       uint32_t u0[32], u1[32];
       float c0, c1;
+      // the other half: only its maximum is kept
+      tmem_ld32_max(tSb + (hf ^ 1) * 64, u0, c0);
+      tmem_ld32_max(tSb + (hf ^ 1) * 64 + 32, u1, c1);
+      tmem_wait_ld();
+      float mo;
+      if (full) {
+        mo = fmaxf(c0, c1);
+      } else {
+        mo = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          if ((vo0 >> e) & 1u) mo = fmaxf(mo, __uint_as_float(u0[e]));
+          if ((vo1 >> e) & 1u) mo = fmaxf(mo, __uint_as_float(u1[e]));
+        }
+      }
+      // this warp's half: values and maximum
       tmem_ld32_max(tS, u0, c0);
       tmem_ld32_max(tS + 32, u1, c1);
       tmem_wait_ld();
-      const uint32_t vm0 = full ? 0xffffffffu : block_rows_mask32(a.g, J, hf * 64);
-      const uint32_t vm1 = full ? 0xffffffffu : block_rows_mask32(a.g, J, hf * 64 + 32);
       float mx;
       if (full) {
         mx = fmaxf(c0, c1);
@@ -273,17 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((vm1 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u1[e]));
         }
       }
-      half_max[((j & 1) * 2 + hf) * 128 + r] = mx;
-      if (!pair_sync(j)) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, half_max[((j & 1) * 2 + (hf ^ 1)) * 128 + r]) * a.scale_log2;
+      mx = fmaxf(mx, mo) * a.scale_log2;  // the same value in both warps of the pair
       const float m_new = fmaxf(m, mx);
       if (j == 0) {
         m = m_new;
       } else {
-        // both warps of the pair see the same row maxima, so they take the same decision
         const bool need = m_new > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
           // O holds sum_{<j} P V relative to m: wait for the last P V, then rescale this half.
@@ -305,19 +366,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
           l *= alpha;
+          lr *= alpha;
           if (need) m = m_new;
         }
       }
-      // P = 2^(s - m) split as P_hi + P_lo (both bf16, P_lo = bf16(P - P_hi)) so that the
-      // P V product keeps ~16 significant bits of P: with the lazy reference max the dominant
-      // entries are not 1 and a single bf16 rounding would cost up to 2^-8 of O.  Each 32-column
-      // chunk holds P_hi in its first 16 columns and P_lo in its last 16 (packed pairs).
-      float sum0 = 0.f, sum1 = 0.f;
+      // P = 2^(s - m) in bf16, packed in pairs: each 32-column chunk of S holds the
+      // P of its 32 keys in its first 16 columns.
+      float sa = 0.f, sb = 0.f, ra = 0.f, rb = 0.f;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const uint32_t(&u)[32] = cc ? u1 : u0;
         const uint32_t vm = cc ? vm1 : vm0;
-        uint32_t ph[16], pl[16];
+        uint32_t ph[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float s0 = fmaf(__uint_as_float(u[2 * e]), a.scale_log2, -m);
@@ -325,27 +385,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!((vm >> (2 * e)) & 1u)) s0 = -INFINITY;
           if (!((vm >> (2 * e + 1)) & 1u)) s1 = -INFINITY;
           const float p0 = ex2(s0), p1 = ex2(s1);
-          sum0 += p0;
-          sum1 += p1;
+          sa += p0;
+          sb += p1;
           ph[e] = pack_bf16(p0, p1);
-          pl[e] = pack_bf16(p0 - __uint_as_float(ph[e] << 16), p1 - __uint_as_float(ph[e] & 0xFFFF0000u));
+          ra += __uint_as_float(ph[e] << 16);
+          rb += __uint_as_float(ph[e] & 0xFFFF0000u);
         }
         tmem_st16(tS + cc * 32, ph);
-        tmem_st16(tS + cc * 32 + 16, pl);
       }
-      l += sum0 + sum1;
+      l += sa + sb;
+      lr += ra + rb;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(pfull + (j & 1));
     }
-    // Epilogue: O / l -> bf16 -> swizzled staging tile (reusing the Q tile) -> TMA store.
+    // Epilogue: O / l(bf16 P) -> bf16 -> swizzled staging tile (reusing the Q tile) -> TMA store.
     // `drain` completes once every MMA of the CTA has finished (the MMA warp commits it last).
     if (n_sel > 0) ok = mbar_wait(drain, 0, a.status, abort_flag) && ok;
     tc_fence_after();
-    half_l[hf * 128 + r] = l;
-    ok = pair_sync(n_sel) && ok;
-    const float lt = l + half_l[(hf ^ 1) * 128 + r];
-    const float inv = (n_sel > 0 && lt > 0.f) ? 1.f / lt : 0.f;
+    half_l[(hf * 2) * 128 + r] = l;
+    half_l[(hf * 2 + 1) * 128 + r] = lr;
+    ok = pair_sync(0) && ok;
+    const float lt = l + half_l[((hf ^ 1) * 2) * 128 + r];
+    const float ltr = lr + half_l[((hf ^ 1) * 2 + 1) * 128 + r];
+    const float inv = (n_sel > 0 && ltr > 0.f) ? 1.f / ltr : 0.f;
 #pragma unroll
     for (int cc = 0; cc < D / 64; ++cc) {
       const int col = hf * (D / 2) + cc * 32;  // first O column of this 32-column chunk
@@ -393,7 +456,7 @@ template <int D>
 cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
                        int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * (512 + 256) +
+  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * 512 +
                       4 * (size_t)p.k + 64;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
