@@ -340,63 +340,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // Half-tile ping-pong: S/dP are produced and consumed in two column halves
-      // (keys [0,64) and [64,128) of the block), one per compute warpgroup, so the
-      // tensor pipe works on one half while a warpgroup works on the other.
-      constexpr uint32_t idS = idesc_f16(128, 64, 0, 0);   // Q K^T and dO V^T, one 64-key half
-      constexpr uint32_t idQ = idesc_f16(128, D, 0, 1);    // dS~ K and P K
-      const uint32_t aQ = smem_u32(sQ), adO = smem_u32(sdO), aK = smem_u32(sK), aV = smem_u32(sV);
-      auto issue_sdp = [&](int j, int hh) {
-        const int s = j % ST;
+    // Half-tile ping-pong: S/dP are produced and consumed in two column halves
+    // (keys [0,64) and [64,128) of the block), one per compute warpgroup, so the
+    // tensor pipe works on one half while a warpgroup works on the other.  Whole
+    // warp, one elected lane issues; descriptors advance by adding to the
+    // start-address field (16-byte units).
+    const uint32_t leader = elect_leader();
+    constexpr uint32_t idS = idesc_f16(128, 64, 0, 0);  // Q K^T and dO V^T, one 64-key half
+    constexpr uint32_t idQ = idesc_f16(128, D, 0, 1);   // dS~ K and P K
+    const uint64_t dQk = smem_desc(smem_u32(sQ), 16, 1024, 2), ddOk = smem_desc(smem_u32(sdO), 16, 1024, 2);
+    const uint64_t dKk = smem_desc(smem_u32(sK), 16, 1024, 2), dVk = smem_desc(smem_u32(sV), 16, 1024, 2);
+    const uint64_t dKm = smem_desc(smem_u32(sK), 16384, 1024, 2);  // K as the MN-major B of dS~ K
+    auto issue_sdp = [&](int j, int hh) {
+      const uint32_t so = (uint32_t)(((j % ST) * C::TILE + hh * 8192) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS + hh * 64, smem_desc(aQ + off, 16, 1024, 2),
-                 smem_desc(aK + s * C::TILE + off + hh * 8192, 16, 1024, 2), idS, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tdP + hh * 64, smem_desc(adO + off, 16, 1024, 2),
-                 smem_desc(aV + s * C::TILE + off + hh * 8192, 16, 1024, 2), idS, kk > 0);
-        }
-        mma_commit(sdpfull + hh);
-      };
-      auto issue_dq = [&](int j, int hh) {
-        const int s = j % ST;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int kk = hh * 4 + q;
-          const uint64_t bK = smem_desc(aK + s * C::TILE + kk * 2048, 16384, 1024, 2);
-          mma_ts(tdQ, tS + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
-          mma_ts(tPK, tdP + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
-        }
-      };
-      bool ok = mbar_wait(qfull, 0, a.status, abort_flag) && mbar_wait(kvfull, 0, a.status, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        issue_sdp(0, 0);
-        issue_sdp(0, 1);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+        mma_ss_by(leader, tS + hh * 64, dQk + off, dKk + so + off, idS, kk > 0);
       }
-      for (int j = 0; ok && j < n; ++j) {
-        const int s = j % ST;
-        const bool more = j + 1 < n;
-        if (!mbar_wait(dsfull, j & 1, a.status, abort_flag)) break;
-        tc_fence_after();
-        issue_dq(j, 0);
-        if (more && !mbar_wait(kvfull + (j + 1) % ST, ((j + 1) / ST) & 1, a.status, abort_flag)) break;
-        tc_fence_after();
-        if (more) issue_sdp(j + 1, 0);
-        if (!mbar_wait(dsfull + 1, j & 1, a.status, abort_flag)) break;
-        tc_fence_after();
-        issue_dq(j, 1);
-        mma_commit(kvempty + s);
-        if (more) issue_sdp(j + 1, 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+        mma_ss_by(leader, tdP + hh * 64, ddOk + off, dVk + so + off, idS, kk > 0);
       }
-      mma_commit(drain);
-      wait_plain(drain, 0);
+      mma_commit_by(leader, sdpfull + hh);
+    };
+    auto issue_dq = [&](int j, int hh) {
+      const uint64_t bK0 = dKm + (uint64_t)(((j % ST) * C::TILE) >> 4);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int kk = hh * 4 + q;
+        const uint64_t bK = bK0 + (uint64_t)(kk * (2048 >> 4));
+        mma_ts_by(leader, tdQ, tS + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
+        mma_ts_by(leader, tPK, tdP + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
+      }
+    };
+    bool ok = warp_wait(qfull, 0, a.status, abort_flag) && warp_wait(kvfull, 0, a.status, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      issue_sdp(0, 0);
+      issue_sdp(0, 1);
     }
+    for (int j = 0; ok && j < n; ++j) {
+      const int s = j % ST;
+      const bool more = j + 1 < n;
+      if (!(ok = warp_wait(dsfull, j & 1, a.status, abort_flag))) break;
+      tc_fence_after();
+      issue_dq(j, 0);
+      if (more && !(ok = warp_wait(kvfull + (j + 1) % ST, ((j + 1) / ST) & 1, a.status, abort_flag))) break;
+      tc_fence_after();
+      if (more) issue_sdp(j + 1, 0);
+      if (!(ok = warp_wait(dsfull + 1, j & 1, a.status, abort_flag))) break;
+      tc_fence_after();
+      issue_dq(j, 1);
+      mma_commit_by(leader, kvempty + s);
+      if (more) issue_sdp(j + 1, 1);
+    }
+    mma_commit_by(leader, drain);
+    wait_plain(drain, 0);
     __syncwarp();
   } else if (warp >= 4) {
     const int grp = (warp - 4) >> 2;                 // key columns [64 grp, 64 grp + 64)
@@ -559,38 +560,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && n > 0) {
-      // Half-tile ping-pong over the query columns [0,64) / [64,128) of S^T and dP^T
-      // (one per compute warpgroup), as in dq_kernel.
-      constexpr uint32_t idS = idesc_f16(128, 64, 0, 0);     // K Q^T and V dO^T, one 64-query half
-      constexpr uint32_t idG = idesc_f16(128, D, 0, 1);      // P^T dO and dS^T Q
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aR = smem_u32(ring);
+    // Half-tile ping-pong over the query columns [0,64) / [64,128) of S^T and dP^T
+    // (one per compute warpgroup), as in dq_kernel; converged-warp issue.
+    if (n > 0) {
+      const uint32_t leader = elect_leader();
+      constexpr uint32_t idS = idesc_f16(128, 64, 0, 0);  // K Q^T and V dO^T, one 64-query half
+      constexpr uint32_t idG = idesc_f16(128, D, 0, 1);   // P^T dO and dS^T Q
+      const uint64_t dKk = smem_desc(smem_u32(sK), 16, 1024, 2), dVk = smem_desc(smem_u32(sV), 16, 1024, 2);
+      const uint64_t dRk = smem_desc(smem_u32(ring), 16, 1024, 2);     // Q / dO of a stage, K-major
+      const uint64_t dRm = smem_desc(smem_u32(ring), 16384, 1024, 2);  // the same tiles as MN-major B
       auto issue_sdp = [&](int u, int hh) {
-        const uint32_t aQ = aR + (u % ST) * STAGE, adO = aQ + C::TILE;
+        const uint32_t sq = (uint32_t)(((u % ST) * STAGE + hh * 8192) >> 4), sd = sq + (uint32_t)(C::TILE >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS + hh * 64, smem_desc(aK + off, 16, 1024, 2), smem_desc(aQ + off + hh * 8192, 16, 1024, 2), idS,
-                 kk > 0);
+          const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+          mma_ss_by(leader, tS + hh * 64, dKk + off, dRk + sq + off, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tdP + hh * 64, smem_desc(aV + off, 16, 1024, 2), smem_desc(adO + off + hh * 8192, 16, 1024, 2),
-                 idS, kk > 0);
+          const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+          mma_ss_by(leader, tdP + hh * 64, dVk + off, dRk + sd + off, idS, kk > 0);
         }
-        mma_commit(sdpfull + hh);
+        mma_commit_by(leader, sdpfull + hh);
       };
       auto issue_grad = [&](int u, int hh) {
-        const uint32_t aQ = aR + (u % ST) * STAGE, adO = aQ + C::TILE;
+        const uint32_t sq = (uint32_t)(((u % ST) * STAGE) >> 4), sd = sq + (uint32_t)(C::TILE >> 4);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int kk = hh * 4 + q;
-          mma_ts(tdV, tS + packed_col(kk), smem_desc(adO + kk * 2048, 16384, 1024, 2), idG, (u > 0 || kk > 0));
-          mma_ts(tdK, tdP + packed_col(kk), smem_desc(aQ + kk * 2048, 16384, 1024, 2), idG, (u > 0 || kk > 0));
+          const uint32_t ko = (uint32_t)(kk * (2048 >> 4));
+          mma_ts_by(leader, tdV, tS + packed_col(kk), dRm + sd + ko, idG, (u > 0 || kk > 0));
+          mma_ts_by(leader, tdK, tdP + packed_col(kk), dRm + sq + ko, idG, (u > 0 || kk > 0));
         }
       };
-      bool ok = mbar_wait(kvfull, 0, a.status, abort_flag) && mbar_wait(qfull, 0, a.status, abort_flag);
+      bool ok = warp_wait(kvfull, 0, a.status, abort_flag) && warp_wait(qfull, 0, a.status, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_sdp(0, 0);
@@ -599,19 +602,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; ok && u < n; ++u) {
         const int s = u % ST;
         const bool more = u + 1 < n;
-        if (!mbar_wait(pdsfull, u & 1, a.status, abort_flag)) break;
+        if (!(ok = warp_wait(pdsfull, u & 1, a.status, abort_flag))) break;
         tc_fence_after();
         issue_grad(u, 0);
-        if (more && !mbar_wait(qfull + (u + 1) % ST, ((u + 1) / ST) & 1, a.status, abort_flag)) break;
+        if (more && !(ok = warp_wait(qfull + (u + 1) % ST, ((u + 1) / ST) & 1, a.status, abort_flag))) break;
         tc_fence_after();
         if (more) issue_sdp(u + 1, 0);
-        if (!mbar_wait(pdsfull + 1, u & 1, a.status, abort_flag)) break;
+        if (!(ok = warp_wait(pdsfull + 1, u & 1, a.status, abort_flag))) break;
         tc_fence_after();
         issue_grad(u, 1);
-        mma_commit(qempty + s);
+        mma_commit_by(leader, qempty + s);
         if (more) issue_sdp(u + 1, 1);
       }
-      mma_commit(drain);
+      mma_commit_by(leader, drain);
       wait_plain(drain, 0);
     }
     __syncwarp();
