@@ -30,7 +30,7 @@ namespace sda {
 
 namespace {
 
-constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 4-11 compute
+constexpr int kThreads = 384;  // warp 0 TMA, warp 1 MMA, warp 2 arrival helper, warps 4-11 compute
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdArgs {
@@ -197,7 +197,9 @@ template <int D>
 struct Cfg {
   static constexpr int CH = D / 64;
   static constexpr int TILE = 128 * D * 2;
-  static constexpr int ST = D == 128 ? 2 : 4;
+  static constexpr int ST = D == 128 ? 2 : 4;   // dK/dV: Q + dO stages
+  static constexpr int KST = D == 128 ? 3 : 4;  // dQ: K ring (K is read until the block's dQ MMAs)
+  static constexpr int VST = D == 128 ? 2 : 4;  // dQ: V ring (V is read by dP only)
 };
 
 // Store this thread's row of a 128 x D accumulator, columns [c_lo, c_lo + ncols),
@@ -261,19 +263,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const __grid_constant__ CUtensorMap tmdQ, BwdArgs a) {
   using C = Cfg<D>;
-  constexpr int ST = C::ST;
+  constexpr int KST = C::KST, VST = C::VST;
   const int I = blockIdx.x, h = blockIdx.y;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sdO = sQ + C::TILE;
-  uint8_t* sK = sdO + C::TILE;        // ST tiles
-  uint8_t* sV = sK + ST * C::TILE;    // ST tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + ST * C::TILE);
+  uint8_t* sK = sdO + C::TILE;        // KST tiles
+  uint8_t* sV = sK + KST * C::TILE;   // VST tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VST * C::TILE);
   uint64_t* qfull = bars;
-  uint64_t* kvfull = qfull + 1;       // ST
-  uint64_t* kvempty = kvfull + ST;    // ST
-  uint64_t* sdpfull = kvempty + ST;   // 2: S/dP columns of half h are ready
+  uint64_t* kvfull = qfull + 1;       // KST: K_j and V_j of block j landed (index j mod KST)
+  uint64_t* kempty = kvfull + KST;    // KST
+  uint64_t* vempty = kempty + KST;    // VST
+  uint64_t* sdpfull = vempty + VST;   // 2: S/dP columns of half h are ready
   uint64_t* dsfull = sdpfull + 2;     // 2: packed dS~ / P of half h are written
   uint64_t* drain = dsfull + 2;       // 1
   float* dpart = reinterpret_cast<float*>(drain + 1);  // 2 x 128 partial row sums of P dP
@@ -285,13 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = a.k;
   if (tid == 0) {
     mbar_init(qfull, 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(kvfull + s, 1);
-      mbar_init(kvempty + s, 1);
+      mbar_init(kempty + s, 1);
     }
+    for (int s = 0; s < VST; ++s) mbar_init(vempty + s, 1);
     for (int hh = 0; hh < 2; ++hh) {
       mbar_init(sdpfull + hh, 1);
-      mbar_init(dsfull + hh, 128);
+      mbar_init(dsfull + hh, hh == 0 ? 128 + 1 : 128);  // + warp 2: K/V of the next block landed
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -319,23 +323,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       int Jn = sel[0];  // block index read one iteration ahead of its use
       for (int j = 0; j < n; ++j) {
-        const int s = j % ST;
+        const int sk = j % KST, sv = j % VST;
         const int Jc = Jn;
         if (j + 1 < n) Jn = sel[j + 1];
-        if (j >= ST && !mbar_wait(kvempty + s, ((j / ST) - 1) & 1, a.status, abort_flag)) break;
+        if (j >= KST && !mbar_wait(kempty + sk, ((j / KST) - 1) & 1, a.status, abort_flag)) break;
+        if (j >= VST && !mbar_wait(vempty + sv, ((j / VST) - 1) & 1, a.status, abort_flag)) break;
         int jt0, jh0, jw0;
         block_origin(a.g, Jc, jt0, jh0, jw0);
-        mbar_expect_tx(kvfull + s, 2 * C::TILE);
+        mbar_expect_tx(kvfull + sk, 2 * C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          tma_load_5d(sK + s * C::TILE + c * 16384, &tmK, kvfull + s, c * 64, h, jw0, jh0, jt0);
-          tma_load_5d(sV + s * C::TILE + c * 16384, &tmV, kvfull + s, c * 64, h, jw0, jh0, jt0);
+          tma_load_5d(sK + sk * C::TILE + c * 16384, &tmK, kvfull + sk, c * 64, h, jw0, jh0, jt0);
+          tma_load_5d(sV + sv * C::TILE + c * 16384, &tmV, kvfull + sk, c * 64, h, jw0, jh0, jt0);
         }
         issued = j + 1;
       }
       if (*abort_flag) {
         wait_plain(qfull, 0);
-        for (int j = issued - ST < 0 ? 0 : issued - ST; j < issued; ++j) wait_plain(kvfull + j % ST, (j / ST) & 1);
+        for (int j = issued - KST < 0 ? 0 : issued - KST; j < issued; ++j) wait_plain(kvfull + j % KST, (j / KST) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // Arrive on dsfull[0] of block j once K/V of block j + 1 have landed, so the MMA
+    // warp's wait for block j's first dS half also covers the next block's tiles.
+    if (lane == 0) {
+      for (int j = 0; j < n; ++j) {
+        const int t = j + 1;
+        if (t < n && !mbar_wait(kvfull + t % KST, (t / KST) & 1, a.status, abort_flag)) break;
+        // phase j - 1 completes before this arrival for phase j
+        if (j >= 1 && !mbar_wait(dsfull, (j - 1) & 1, a.status, abort_flag)) break;
+        mbar_arrive(dsfull);
       }
     }
     __syncwarp();
@@ -352,27 +370,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dKk = smem_desc(smem_u32(sK), 16, 1024, 2), dVk = smem_desc(smem_u32(sV), 16, 1024, 2);
     const uint64_t dKm = smem_desc(smem_u32(sK), 16384, 1024, 2);  // K as the MN-major B of dS~ K
     auto issue_sdp = [&](int j, int hh) {
-      const uint32_t so = (uint32_t)(((j % ST) * C::TILE + hh * 8192) >> 4);
+      const uint32_t sko = (uint32_t)(((j % KST) * C::TILE + hh * 8192) >> 4);
+      const uint32_t svo = (uint32_t)(((j % VST) * C::TILE + hh * 8192) >> 4);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
-        mma_ss_by(leader, tS + hh * 64, dQk + off, dKk + so + off, idS, kk > 0);
+        mma_ss_by(leader, tS + hh * 64, dQk + off, dKk + sko + off, idS, kk > 0);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
-        mma_ss_by(leader, tdP + hh * 64, ddOk + off, dVk + so + off, idS, kk > 0);
+        mma_ss_by(leader, tdP + hh * 64, ddOk + off, dVk + svo + off, idS, kk > 0);
       }
       mma_commit_by(leader, sdpfull + hh);
+      if (hh == 1) mma_commit_by(leader, vempty + j % VST);  // V_j is read by dP only
     };
     auto issue_dq = [&](int j, int hh) {
-      const uint64_t bK0 = dKm + (uint64_t)(((j % ST) * C::TILE) >> 4);
+      const uint64_t bK0 = dKm + (uint64_t)(((j % KST) * C::TILE) >> 4);
+      // four MMAs into one accumulator, then four into the other (alternating
+      // accumulators issues measurably slower than a run into one)
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int kk = hh * 4 + q;
-        const uint64_t bK = bK0 + (uint64_t)(kk * (2048 >> 4));
-        mma_ts_by(leader, tdQ, tS + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
-        mma_ts_by(leader, tPK, tdP + packed_col(kk), bK, idQ, (j > 0 || kk > 0));
+        mma_ts_by(leader, tdQ, tS + packed_col(kk), bK0 + (uint64_t)(kk * (2048 >> 4)), idQ, (j > 0 || kk > 0));
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int kk = hh * 4 + q;
+        mma_ts_by(leader, tPK, tdP + packed_col(kk), bK0 + (uint64_t)(kk * (2048 >> 4)), idQ, (j > 0 || kk > 0));
       }
     };
     bool ok = warp_wait(qfull, 0, a.status, abort_flag) && warp_wait(kvfull, 0, a.status, abort_flag);
@@ -382,18 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue_sdp(0, 1);
     }
     for (int j = 0; ok && j < n; ++j) {
-      const int s = j % ST;
       const bool more = j + 1 < n;
       if (!(ok = warp_wait(dsfull, j & 1, a.status, abort_flag))) break;
       tc_fence_after();
       issue_dq(j, 0);
-      if (more && !(ok = warp_wait(kvfull + (j + 1) % ST, ((j + 1) / ST) & 1, a.status, abort_flag))) break;
-      tc_fence_after();
+      // dsfull[0] of block j also means K/V_{j+1} landed (warp 2 arrives on it)
       if (more) issue_sdp(j + 1, 0);
       if (!(ok = warp_wait(dsfull + 1, j & 1, a.status, abort_flag))) break;
       tc_fence_after();
       issue_dq(j, 1);
-      mma_commit_by(leader, kvempty + s);
+      mma_commit_by(leader, kempty + j % KST);  // K_j: last read by this block's dQ MMAs
       if (more) issue_sdp(j + 1, 1);
     }
     mma_commit_by(leader, drain);
@@ -585,12 +608,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_grad = [&](int u, int hh) {
         const uint32_t sq = (uint32_t)(((u % ST) * STAGE) >> 4), sd = sq + (uint32_t)(C::TILE >> 4);
+        // a run into dV, then a run into dK (see issue_dq)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int kk = hh * 4 + q;
-          const uint32_t ko = (uint32_t)(kk * (2048 >> 4));
-          mma_ts_by(leader, tdV, tS + packed_col(kk), dRm + sd + ko, idG, (u > 0 || kk > 0));
-          mma_ts_by(leader, tdK, tdP + packed_col(kk), dRm + sq + ko, idG, (u > 0 || kk > 0));
+          mma_ts_by(leader, tdV, tS + packed_col(kk), dRm + sd + (uint32_t)(kk * (2048 >> 4)), idG, (u > 0 || kk > 0));
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int kk = hh * 4 + q;
+          mma_ts_by(leader, tdK, tdP + packed_col(kk), dRm + sq + (uint32_t)(kk * (2048 >> 4)), idG, (u > 0 || kk > 0));
         }
       };
       bool ok = warp_wait(kvfull, 0, a.status, abort_flag) && warp_wait(qfull, 0, a.status, abort_flag);
@@ -756,7 +783,7 @@ cudaError_t launch_dq(const Prob& p, const void* V, const void* dO, const int32_
   WsLayout w = ws_layout(p, ws);
   unsigned* status = status_ptr();
   if (!status) return cudaErrorUnknown;
-  const size_t smem = 1024 + (size_t)C::TILE * (2 + 2 * C::ST) + 8 * (6 + 2 * C::ST) + 1024 + 64;
+  const size_t smem = 1024 + (size_t)C::TILE * (2 + C::KST + C::VST) + 8 * (6 + 2 * C::KST + C::VST) + 1024 + 8 + 64;
   cudaError_t e = cudaFuncSetAttribute(dq_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const TokType gt = F32OUT ? kTokF32 : kTokBF16;

@@ -234,9 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, 2);
       const uint64_t dV = smem_desc(smem_u32(sV), 16384, 1024, 2);
       const uint32_t tO = tmem + 256;
+      // Every issue_S follows a wait and its tcgen05 fence: kfull for K_0 and K_1,
+      // pfull_{j-2} (K_j landed, P_{j-2} consumed) after that.
       auto issue_S = [&](int j) {
         const int s = j % KST;
-        tc_fence_after();
         const uint32_t tS = tmem + (j & 1) * 128;
         const uint64_t dKs = dK + (uint64_t)((s * C::TILE) >> 4);
 #pragma unroll
@@ -249,11 +250,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_by(leader, kempty + s);  // K_j is no longer needed once S_j is done
       };
       bool ok = warp_wait(qfull, 0, a.status, abort_flag) && warp_wait(kfull, 0, a.status, abort_flag);
-      if (ok) issue_S(0);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
+      }
       for (int j = 0; ok && j < n_sel; ++j) {
         if (j + 1 < n_sel) {
           // K_{j+1} landed: waited directly for K_1, implied by pfull_{j-1} after that
-          if (j == 0 && !(ok = warp_wait(kfull + 1 % KST, (1 / KST) & 1, a.status, abort_flag))) break;
+          if (j == 0) {
+            if (!(ok = warp_wait(kfull + 1 % KST, (1 / KST) & 1, a.status, abort_flag))) break;
+            tc_fence_after();
+          }
           issue_S(j + 1);
         }
         if (!(ok = warp_wait(pfull + (j & 1), (j >> 1) & 1, a.status, abort_flag))) break;
