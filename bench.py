@@ -43,6 +43,20 @@ WORKLOAD = "train_524k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel that can be the
+# dominant one, from a single-pass ncu capture of this full-size step:
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none \
+#       -k regex:"score_kernel|fwd_tc_kernel|dq_kernel|dkdv_kernel" -s 12 -c 4 \
+#       python bench.py --steps 2 --warmup 3 --no-e2e --no-cpu-baseline
+# An entry goes back to None whenever its kernel changes, until it is captured again.
+NCU_DRAM_BYTES = {
+    "score_kernel": 0.583e9 + 0.102e9,
+    "fwd_tc_kernel": 63.553e9 + 2.500e9,
+    "dq_kernel": 157.946e9 + 2.164e9,
+    "dkdv_kernel": 173.260e9 + 4.275e9,
+}
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,6 +439,7 @@ def main():
             "attn_bwd_dq (dq_kernel)": (phase_ms["bwd_dq"], f_dq)}
     dom = max(kern, key=lambda n: kern[n][0])
     dom_ms, dom_flops = kern[dom]
+    traffic = next((v for key, v in NCU_DRAM_BYTES.items() if key in dom), None)
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     if merge:
         merge["frac_of_hbm_peak"] = merge["gbs"] / hbm_peak
@@ -457,7 +472,7 @@ def main():
         "phase_ms": phase_ms,
         "flops": {"fwd": f_fwd, "bwd": f_bwd, "kept_pairs": pairs},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tc_peak, "traffic": None,
+                     "frac": achieved / tc_peak, "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
                      "peak_source": f"{pk_src} bf16_tflops_sustained (fp16 and bf16 share the dense rate)"},
         "kernels": {n: {"ms": t, "tflops": f / (t / 1e3) / 1e12, "frac": f / (t / 1e3) / 1e12 / tc_peak}
                     for n, (t, f) in kern.items()},
