@@ -47,6 +47,9 @@ struct BwdArgs {
   const int32_t* lists;   // [B, Hh, nb * k]
   const int32_t* order;   // [B, Hh, nb]
   unsigned* status;
+  // dK/dV half tiles: query rows [0,64) and [64,128) of a tile are the two halves of
+  // its slowest even extent (0: tt, 1: hh, 2: ww); the second half starts hoff further.
+  int hdim, hoff;
 };
 
 __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
@@ -497,8 +500,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV, BwdArgs a) {
   using C = Cfg<D>;
-  constexpr int ST = C::ST;
-  constexpr int STAGE = 2 * C::TILE + 2 * 512;  // Q, dO, L2 row, D row
+  // The ring holds half stages: for one query block that kept this key block, query
+  // rows [64 hh, 64 hh + 64) of Q and dO and of the LSE and D rows.  Half hh is read
+  // only by the products of column half hh (S^T, dP^T halves and their dV, dK terms),
+  // so it is released as soon as those are done.
+  constexpr int HST = 2 * C::ST;        // half-stage slots
+  constexpr int HTILE = C::TILE;        // Q half + dO half (64 rows each)
+  constexpr int HCHUNK = 64 * 128;      // one 64-column chunk of a 64-row half tile
   const int h = blockIdx.y;
   const long long bh = (long long)a.b * a.Hh + h;
   const int J = a.order[bh * a.g.nb + blockIdx.x];
@@ -510,12 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::TILE;
-  uint8_t* ring = sV + C::TILE;  // ST stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + ST * STAGE);
+  uint8_t* ring = sV + C::TILE;           // HST half tiles (Q half, then dO half)
+  uint8_t* rows = ring + HST * HTILE;     // HST x (64 LSE*log2e, 64 D)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rows + HST * 512);
   uint64_t* kvfull = bars;
-  uint64_t* qfull = kvfull + 1;     // ST
-  uint64_t* qempty = qfull + ST;    // ST
-  uint64_t* sdpfull = qempty + ST;  // 2: S^T/dP^T columns of half h are ready
+  uint64_t* qfull = kvfull + 1;      // HST
+  uint64_t* qempty = qfull + HST;    // HST
+  uint64_t* sdpfull = qempty + HST;  // 2: S^T/dP^T columns of half h are ready
   uint64_t* pdsfull = sdpfull + 2;  // 2: packed P^T / dS^T of half h are written
   uint64_t* drain = pdsfull + 2;    // 1
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -524,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     mbar_init(kvfull, 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < HST; ++s) {
       mbar_init(qfull + s, 1);
       mbar_init(qempty + s, 1);
     }
@@ -556,29 +565,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_5d(sV + c * 16384, &tmV, kvfull, c * 64, h, w0, h0, t0);
       }
       int issued = 0;
-      int In = users[0];  // query block index read one iteration ahead of its use
-      for (int u = 0; u < n; ++u) {
-        const int s = u % ST;
-        const int I = In;
-        if (u + 1 < n) In = users[u + 1];
-        if (u >= ST && !mbar_wait(qempty + s, ((u / ST) - 1) & 1, a.status, abort_flag)) break;
+      for (int i = 0; i < 2 * n; ++i) {  // half stage i: query block users[i / 2], half i % 2
+        const int s = i % HST, hh = i & 1;
+        if (i >= HST && !mbar_wait(qempty + s, ((i / HST) - 1) & 1, a.status, abort_flag)) break;
+        const int I = users[i >> 1];
         int it0, ih0, iw0;
         block_origin(a.g, I, it0, ih0, iw0);
-        uint8_t* st = ring + s * STAGE;
-        mbar_expect_tx(qfull + s, STAGE);
+        const int ho = hh * a.hoff;
+        it0 += a.hdim == 0 ? ho : 0;
+        ih0 += a.hdim == 1 ? ho : 0;
+        iw0 += a.hdim == 2 ? ho : 0;
+        uint8_t* st = ring + s * HTILE;
+        mbar_expect_tx(qfull + s, HTILE + 512);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          tma_load_5d(st + c * 16384, &tmQ, qfull + s, c * 64, h, iw0, ih0, it0);
-          tma_load_5d(st + C::TILE + c * 16384, &tmdO, qfull + s, c * 64, h, iw0, ih0, it0);
+          tma_load_5d(st + c * HCHUNK, &tmQ, qfull + s, c * 64, h, iw0, ih0, it0);
+          tma_load_5d(st + HTILE / 2 + c * HCHUNK, &tmdO, qfull + s, c * 64, h, iw0, ih0, it0);
         }
-        const long long trow = (bh * a.g.nb + I) * 128;
-        bulk_load(st + 2 * C::TILE, a.L2v + trow, 512, qfull + s);
-        bulk_load(st + 2 * C::TILE + 512, a.Dv + trow, 512, qfull + s);
-        issued = u + 1;
+        const long long trow = (bh * a.g.nb + I) * 128 + hh * 64;
+        bulk_load(rows + s * 512, a.L2v + trow, 256, qfull + s);
+        bulk_load(rows + s * 512 + 256, a.Dv + trow, 256, qfull + s);
+        issued = i + 1;
       }
       if (*abort_flag) {
         wait_plain(kvfull, 0);
-        for (int u = issued - ST < 0 ? 0 : issued - ST; u < issued; ++u) wait_plain(qfull + u % ST, (u / ST) & 1);
+        for (int i = issued - HST < 0 ? 0 : issued - HST; i < issued; ++i) wait_plain(qfull + i % HST, (i / HST) & 1);
       }
     }
     __syncwarp();
@@ -590,56 +601,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idS = idesc_f16(128, 64, 0, 0);  // K Q^T and V dO^T, one 64-query half
       constexpr uint32_t idG = idesc_f16(128, D, 0, 1);   // P^T dO and dS^T Q
       const uint64_t dKk = smem_desc(smem_u32(sK), 16, 1024, 2), dVk = smem_desc(smem_u32(sV), 16, 1024, 2);
-      const uint64_t dRk = smem_desc(smem_u32(ring), 16, 1024, 2);     // Q / dO of a stage, K-major
-      const uint64_t dRm = smem_desc(smem_u32(ring), 16384, 1024, 2);  // the same tiles as MN-major B
+      const uint64_t dRk = smem_desc(smem_u32(ring), 16, 1024, 2);      // half tiles, K-major
+      const uint64_t dRm = smem_desc(smem_u32(ring), HCHUNK, 1024, 2);  // the same as MN-major B
       auto issue_sdp = [&](int u, int hh) {
-        const uint32_t sq = (uint32_t)(((u % ST) * STAGE + hh * 8192) >> 4), sd = sq + (uint32_t)(C::TILE >> 4);
+        const uint32_t sq = (uint32_t)((((2 * u + hh) % HST) * HTILE) >> 4), sd = sq + (uint32_t)((HTILE / 2) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
-          mma_ss_by(leader, tS + hh * 64, dKk + off, dRk + sq + off, idS, kk > 0);
+          const uint32_t offA = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;   // K, V: 128-row tiles
+          const uint32_t offB = (kk >> 2) * (HCHUNK >> 4) + (kk & 3) * 2;  // 64-row half tiles
+          mma_ss_by(leader, tS + hh * 64, dKk + offA, dRk + sq + offB, idS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
-          mma_ss_by(leader, tdP + hh * 64, dVk + off, dRk + sd + off, idS, kk > 0);
+          const uint32_t offA = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+          const uint32_t offB = (kk >> 2) * (HCHUNK >> 4) + (kk & 3) * 2;
+          mma_ss_by(leader, tdP + hh * 64, dVk + offA, dRk + sd + offB, idS, kk > 0);
         }
         mma_commit_by(leader, sdpfull + hh);
       };
       auto issue_grad = [&](int u, int hh) {
-        const uint32_t sq = (uint32_t)(((u % ST) * STAGE) >> 4), sd = sq + (uint32_t)(C::TILE >> 4);
-        // a run into dV, then a run into dK (see issue_dq)
+        const int s = (2 * u + hh) % HST;
+        const uint32_t sq = (uint32_t)((s * HTILE) >> 4), sd = sq + (uint32_t)((HTILE / 2) >> 4);
+        // a run into dV, then a run into dK; K-step q covers query rows 64 hh + 16 q ..
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int kk = hh * 4 + q;
-          mma_ts_by(leader, tdV, tS + packed_col(kk), dRm + sd + (uint32_t)(kk * (2048 >> 4)), idG, (u > 0 || kk > 0));
+          mma_ts_by(leader, tdV, tS + packed_col(kk), dRm + sd + (uint32_t)(q * (2048 >> 4)), idG, (u > 0 || kk > 0));
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int kk = hh * 4 + q;
-          mma_ts_by(leader, tdK, tdP + packed_col(kk), dRm + sq + (uint32_t)(kk * (2048 >> 4)), idG, (u > 0 || kk > 0));
+          mma_ts_by(leader, tdK, tdP + packed_col(kk), dRm + sq + (uint32_t)(q * (2048 >> 4)), idG, (u > 0 || kk > 0));
         }
+        mma_commit_by(leader, qempty + s);  // this half stage is no longer read
       };
-      bool ok = warp_wait(kvfull, 0, a.status, abort_flag) && warp_wait(qfull, 0, a.status, abort_flag);
+      auto wait_half = [&](int u, int hh) -> bool {
+        const int i = 2 * u + hh;
+        return warp_wait(qfull + i % HST, (i / HST) & 1, a.status, abort_flag);
+      };
+      bool ok = warp_wait(kvfull, 0, a.status, abort_flag) && wait_half(0, 0) && wait_half(0, 1);
       if (ok) {
         tc_fence_after();
         issue_sdp(0, 0);
         issue_sdp(0, 1);
       }
       for (int u = 0; ok && u < n; ++u) {
-        const int s = u % ST;
         const bool more = u + 1 < n;
-        if (!(ok = warp_wait(pdsfull, u & 1, a.status, abort_flag))) break;
-        tc_fence_after();
-        issue_grad(u, 0);
-        if (more && !(ok = warp_wait(qfull + (u + 1) % ST, ((u + 1) / ST) & 1, a.status, abort_flag))) break;
-        tc_fence_after();
-        if (more) issue_sdp(u + 1, 0);
-        if (!(ok = warp_wait(pdsfull + 1, u & 1, a.status, abort_flag))) break;
-        tc_fence_after();
-        issue_grad(u, 1);
-        mma_commit_by(leader, qempty + s);
-        if (more) issue_sdp(u + 1, 1);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!(ok = warp_wait(pdsfull + hh, u & 1, a.status, abort_flag))) break;
+          tc_fence_after();
+          issue_grad(u, hh);
+          if (more) {
+            if (!(ok = wait_half(u + 1, hh))) break;
+            tc_fence_after();
+            issue_sdp(u + 1, hh);
+          }
+        }
       }
       mma_commit_by(leader, drain);
       wait_plain(drain, 0);
@@ -653,9 +671,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = 0; u < n; ++u) {
       if (!mbar_wait(sdpfull + grp, u & 1, a.status, abort_flag)) break;
       tc_fence_after();
-      const uint8_t* st = ring + (u % ST) * STAGE;
-      const float* l2 = reinterpret_cast<const float*>(st + 2 * C::TILE);
-      const float* dv = l2 + 128;
+      // LSE*log2e and D of this group's 64 query rows, indexed by the column c as l2[c]
+      const float* l2 = reinterpret_cast<const float*>(rows + ((2 * u + grp) % HST) * 512) - grp * 64;
+      const float* dv = l2 + 64;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int col0 = grp * 64 + cc * 32;
@@ -766,6 +784,9 @@ BwdArgs make_args(const Prob& p, const WsLayout& w, const int32_t* idx, unsigned
   a.lists = w.lists;
   a.order = w.order;
   a.status = status;
+  const Geom& g = p.g;
+  a.hdim = g.bt % 2 == 0 ? 0 : (g.bh % 2 == 0 ? 1 : 2);
+  a.hoff = a.hdim == 0 ? g.bt / 2 : (a.hdim == 1 ? g.bh / 2 : g.bw / 2);
   return a;
 }
 
@@ -807,15 +828,24 @@ cudaError_t launch_dkdv(const Prob& p, const void* V, const void* dO, void* dK, 
   WsLayout w = ws_layout(p, ws);
   unsigned* status = status_ptr();
   if (!status) return cudaErrorUnknown;
-  const size_t smem = 1024 + (size_t)C::TILE * 2 + (size_t)C::ST * (2 * C::TILE + 1024) + 8 * (6 + 2 * C::ST) + 64;
+  // K, V tiles; 2 ST half-stage tiles; their LSE/D rows; barriers; TMEM slot and abort flag
+  const size_t smem = 1024 + (size_t)C::TILE * 2 + (size_t)C::ST * (2 * C::TILE + 1024) + 8 * (6 + 4 * C::ST) + 8 + 64;
   cudaError_t e =
       cudaFuncSetAttribute(dkdv_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const TokType gt = F32OUT ? kTokF32 : kTokBF16;
+  const Geom& g = p.g;
+  const BwdArgs a0 = make_args(p, w, nullptr, status, 0);
+  const int hbt = a0.hdim == 0 ? g.bt / 2 : g.bt, hbh = a0.hdim == 1 ? g.bh / 2 : g.bh,
+            hbw = a0.hdim == 2 ? g.bw / 2 : g.bw;
+  auto half_map = [&](CUtensorMap* m, const void* base, int b) {
+    const char* x = static_cast<const char*>(base) + (size_t)b * p.N * p.Hh * p.d * 2;
+    return make_token_map(m, x, kTokF16, g.T, g.H, g.W, p.Hh, p.d, hbt, hbh, hbw);
+  };
   for (int b = 0; b < p.B; ++b) {
-    CUtensorMap mQ, mK, mV, mdO, mdK, mdV;
-    if (!token_map(&mQ, p, w.Q16, b, kTokF16) || !token_map(&mK, p, w.K16, b, kTokF16) ||
-        !token_map(&mV, p, w.V16, b, kTokF16) || !token_map(&mdO, p, w.dO16, b, kTokF16) ||
+    CUtensorMap mQ, mK, mV, mdO, mdK, mdV;  // Q and dO maps load 64-row half tiles
+    if (!half_map(&mQ, w.Q16, b) || !token_map(&mK, p, w.K16, b, kTokF16) ||
+        !token_map(&mV, p, w.V16, b, kTokF16) || !half_map(&mdO, w.dO16, b) ||
         !token_map(&mdK, p, dK, b, gt) || !token_map(&mdV, p, dV, b, gt))
       return cudaErrorInvalidValue;
     dkdv_kernel<D, F32OUT><<<dim3(p.g.nb, p.Hh), kThreads, smem, st>>>(mQ, mK, mV, mdO, mdK, mdV,

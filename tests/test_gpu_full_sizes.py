@@ -14,7 +14,7 @@ import pytest
 
 import oracle as orc
 from dynamic_block_sparse_rank_gb300 import inputs
-from tests.parity_util import TOL, assert_close, check_selection, dev, errors, host
+from tests.parity_util import TOL, assert_close, check_scores, check_selection, dev, errors, host
 
 pytestmark = pytest.mark.gpu
 
@@ -46,16 +46,6 @@ def _head(x, h):
     return {k: (v[:, :, h:h + 1] if v.ndim == 4 and k not in ("Wq", "Wk") else v[h:h + 1]) for k, v in x.items()}
 
 
-def _check_scores(got, ref):
-    """Block scores: fp32 accumulation of exact bf16 products, so they match the oracle to ~1e-6 except
-    where a q~ or k~ element was rounded to the neighbouring bf16 value (the GPU rounds an fp32-accumulated
-    projection, the oracle an exact one): such a flip moves a score by about 2^-8 of one of its r terms.
-    Nearly every score must agree to 1e-5 of the largest, and every one to 4e-3."""
-    err = np.abs(got - ref) / np.abs(ref).max()
-    assert np.mean(err > 1e-5) < 0.02, np.mean(err > 1e-5)
-    assert err.max() < 4e-3, err.max()
-
-
 def _gpu_predict(sda, wl, Q, K, Wq, Wk, with_score=True):
     p = sda.problem_from_workload(wl)
     nb, k = sda.sda_num_blocks(p)
@@ -82,7 +72,7 @@ def _check_predictor_and_forward(sda, wl, heads, n_blocks_sampled, seed=0):
         st = check_selection(gi, rsc, wl.k)
         assert st["fail"] == 0, (h, st)
         sel_stats.append(st)
-        _check_scores(sc[0, h, qb].cpu().numpy().astype(np.float64), rsc)
+        check_scores(sc[0, h, qb].cpu().numpy().astype(np.float64), rsc)
         ref_rows[h] = ridx
         idx[0, h, qb] = torch.from_numpy(ridx[0, 0]).cuda()  # compared rows use the oracle's selection
     p = sda.problem_from_workload(wl)
@@ -109,7 +99,7 @@ def test_fwd_8k_full_oracle(sda):
     ridx, rsc = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
     st = check_selection(idx.cpu().numpy(), rsc, wl.k)
     assert st["fail"] == 0, st
-    _check_scores(host(sc), rsc)
+    check_scores(host(sc), rsc)
     p = sda.problem_from_workload(wl)
     O = torch.empty_like(Q)
     LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
