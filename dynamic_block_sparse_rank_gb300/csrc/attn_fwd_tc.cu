@@ -18,9 +18,8 @@
 //               S_j = Q K_j^T into one of two TMEM S buffers, then, once P_j
 //               is ready, O += P_j V_j with P_j read from TMEM.
 //   warps 4-11  softmax: two warps per query row quarter, each owning 64 of
-//               the 128 key columns (thread = row = TMEM lane); each also
-//               reads the other half's maximum, so the pair never waits on
-//               each other inside the loop.  Online softmax in base 2 with a
+//               the 128 key columns (thread = row = TMEM lane); the pair swaps
+//               its half-row maxima at a named barrier.  Online softmax in base 2 with a
 //               lazy rescale: O and l are rescaled only when a row max grows
 //               by more than 2^8, which is exact because O and l always share
 //               the same reference max.  P overwrites S in bf16; O is divided
@@ -99,7 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* n_sel_s = abort_flag + 1;
   int* warp_cnt = n_sel_s + 1;  // 16
   float* half_l = reinterpret_cast<float*>(warp_cnt + 16);  // [2 halves][l, l of bf16 P][128 rows]
-  int* sel = reinterpret_cast<int*>(half_l + 512);           // k
+  float* half_max = half_l + 512;                            // [2 block parities][2 halves][128 rows]
+  int* sel = reinterpret_cast<int*>(half_max + 512);         // k
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -282,10 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax + epilogue
     // Two warps per TMEM lane quarter: warp half hf owns S columns [64 hf, 64 hf + 64)
-    // and O columns [hf D/2, (hf + 1) D/2) of the quarter's 32 rows.  Each warp also
-    // reads the maximum of the other half (the reducing load returns it without
-    // keeping the values), so both warps of a pair hold the same row maxima and take
-    // the same rescale decisions without meeting.  They meet once, for the epilogue.
+    // and O columns [hf D/2, (hf + 1) D/2) of the quarter's 32 rows.  The pair swaps
+    // its half-row maxima through shared memory (double-buffered by block parity) at a
+    // named barrier, so both warps hold the same row maxima and take the same rescale
+    // decisions.
     const int quarter = warp & 3, hf = (warp - 4) >> 2;
     const int r = quarter * 32 + lane;
     auto pair_sync = [&](uint32_t phase) -> bool {
@@ -299,63 +299,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     float lr = 0.f;  // sum of bf16(P), the weights the P V product uses: divides O
     bool ok = true;
     for (int j = 0; j < n_sel; ++j) {
-      if (!mbar_wait(sfull + (j & 1), (j >> 1) & 1, a.status, abort_flag)) {
+      // Every iteration of both warps of a pair passes the pair's named barrier exactly
+      // once (twice when rescaling), with the success of its bounded waits ANDed into it:
+      // a wait that gives up stops both warps at the same point.
+      const bool okw = mbar_wait(sfull + (j & 1), (j >> 1) & 1, a.status, abort_flag);
+      const uint32_t tS = tmem + (j & 1) * 128 + lane_base + hf * 64;
+      uint32_t u0[32], u1[32];
+      uint32_t vm0 = ~0u, vm1 = ~0u;  // key rows of J inside the grid
+      float mx = -INFINITY;
+      if (okw) {
+        tc_fence_after();
+        const int J = sel[j];
+        const bool full = a.all_full || block_is_full(a.g, J);
+        if (!full) {
+          vm0 = block_rows_mask32(a.g, J, hf * 64);
+          vm1 = block_rows_mask32(a.g, J, hf * 64 + 32);
+        }
+        float c0, c1;
+        tmem_ld32_max(tS, u0, c0);  // values and, from the same load, their maximum
+        tmem_ld32_max(tS + 32, u1, c1);
+        tmem_wait_ld();
+        if (full) {
+          mx = fmaxf(c0, c1);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if ((vm0 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u0[e]));
+            if ((vm1 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u1[e]));
+          }
+        }
+        half_max[((j & 1) * 2 + hf) * 128 + r] = mx;
+      }
+      if (!named_bar_and(2 + quarter, 64, okw)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const uint32_t tSb = tmem + (j & 1) * 128 + lane_base;
-      const uint32_t tS = tSb + hf * 64;
-      const int J = sel[j];
-      const bool full = a.all_full || block_is_full(a.g, J);
-      uint32_t vo0 = ~0u, vo1 = ~0u, vm0 = ~0u, vm1 = ~0u;  // key rows of J inside the grid
-      if (!full) {
-        vo0 = block_rows_mask32(a.g, J, (hf ^ 1) * 64);
-        vo1 = block_rows_mask32(a.g, J, (hf ^ 1) * 64 + 32);
-        vm0 = block_rows_mask32(a.g, J, hf * 64);
-        vm1 = block_rows_mask32(a.g, J, hf * 64 + 32);
-      }
-      uint32_t u0[32], u1[32];
-      float c0, c1;
-      // the other half: only its maximum is kept
-      tmem_ld32_max(tSb + (hf ^ 1) * 64, u0, c0);
-      tmem_ld32_max(tSb + (hf ^ 1) * 64 + 32, u1, c1);
-      tmem_wait_ld();
-      float mo;
-      if (full) {
-        mo = fmaxf(c0, c1);
-      } else {
-        mo = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if ((vo0 >> e) & 1u) mo = fmaxf(mo, __uint_as_float(u0[e]));
-          if ((vo1 >> e) & 1u) mo = fmaxf(mo, __uint_as_float(u1[e]));
-        }
-      }
-      // this warp's half: values and maximum
-      tmem_ld32_max(tS, u0, c0);
-      tmem_ld32_max(tS + 32, u1, c1);
-      tmem_wait_ld();
-      float mx;
-      if (full) {
-        mx = fmaxf(c0, c1);
-      } else {
-        mx = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if ((vm0 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u0[e]));
-          if ((vm1 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u1[e]));
-        }
-      }
-      mx = fmaxf(mx, mo) * a.scale_log2;  // the same value in both warps of the pair
+      mx = fmaxf(mx, half_max[((j & 1) * 2 + (hf ^ 1)) * 128 + r]) * a.scale_log2;  // same in both warps
       const float m_new = fmaxf(m, mx);
       if (j == 0) {
         m = m_new;
       } else {
         const bool need = m_new > m + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
+        if (__any_sync(0xffffffffu, need)) {  // both warps of the pair take this branch together
           // O holds sum_{<j} P V relative to m: wait for the last P V, then rescale this half.
-          if (!mbar_wait(odone, (j - 1) & 1, a.status, abort_flag)) {
+          if (!named_bar_and(2 + quarter, 64, mbar_wait(odone, (j - 1) & 1, a.status, abort_flag))) {
             ok = false;
             break;
           }
@@ -463,7 +450,7 @@ template <int D>
 cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
                        int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * 512 +
+  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * 1024 +
                       4 * (size_t)p.k + 64;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

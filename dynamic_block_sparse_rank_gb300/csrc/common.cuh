@@ -213,6 +213,19 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also returns the AND of `v` over the participating threads,
+// so a group can take a decision (continue or stop) uniformly.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %3, 0;\n\t"
+      "bar.red.and.pred p, %1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(nthreads), "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
 // ----------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation MMA.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
