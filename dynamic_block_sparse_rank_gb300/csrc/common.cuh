@@ -165,6 +165,36 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, u
   }
 }
 
+// Release/acquire counters in shared memory: a cheaper hand-off than an mbarrier
+// when the waiter usually finds the count already reached (one shared load).
+__device__ __forceinline__ void count_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned count_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Whole warp: wait until *p >= target (bounded like mbar_wait); the same result on every lane.
+__device__ __forceinline__ bool warp_wait_count(const unsigned* p, unsigned target, unsigned* status,
+                                                volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, count_acquire(p) >= target)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (__all_sync(0xffffffffu, count_acquire(p) >= target)) return true;
+    if ((it & 63u) == 63u) {
+      const bool stop = *abort_flag != 0 || globaltimer_ns() - t0 > SDA_WAIT_LIMIT_NS;
+      if (__any_sync(0xffffffffu, stop)) {
+        if ((threadIdx.x & 31) == 0 && !*abort_flag) {
+          atomicOr(status, kStatusWaitTimeout);
+          *abort_flag = 1;
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA (bulk tensor copies).  Destination/source shared addresses are CTA-local.
 __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,

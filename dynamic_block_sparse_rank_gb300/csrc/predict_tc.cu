@@ -164,8 +164,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   uint64_t* kfull = bars + 1;          // kStages
   uint64_t* kempty = kfull + kStages;  // kStages
   uint64_t* accf = kempty + kStages;   // kAccBufs: accumulator holds a finished pair
-  uint64_t* acce = accf + kAccBufs;    // kAccBufs: accumulator read out
-  uint64_t* drain = acce + kAccBufs;
+  // kAccBufs counters (in the space of as many barriers): warps that have read buffer b
+  // out, 4 per use.  The MMA warp usually finds the count reached, and one shared load
+  // costs far less than a wait on an already completed mbarrier.
+  unsigned* drained = reinterpret_cast<unsigned*>(accf + kAccBufs);
+  uint64_t* drain = accf + 2 * kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   uint8_t* full = reinterpret_cast<uint8_t*>(abort_flag + 1);  // nb: key block J lies inside the grid
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     }
     for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(accf + s, 1);
-      mbar_init(acce + s, kEpiWarps / kAccBufs);
+      drained[s] = 0u;
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -233,7 +236,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
 #pragma unroll
       for (int q = 0; q < QB; ++q) {
         const int P = J * QB + q, buf = P & (kAccBufs - 1);
-        if (P >= kAccBufs && !(ok = warp_wait(acce + buf, ((P >> 2) - 1) & 1, a.status, abort_flag))) break;
+        // buffer `buf` was read out for its previous (P >> 2) uses: 4 warps each
+        if (P >= kAccBufs && !(ok = warp_wait_count(drained + buf, 4u * (unsigned)(P >> 2), a.status, abort_flag)))
+          break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < R / 16; ++kk)
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce + grp);  // values are in registers: the buffer may be refilled
+      if (lane == 0) count_release_add(drained + grp, 1u);  // values are in registers: the buffer may be refilled
       m = fmaxf(m, fj ? fmaxf(m0, m1) : masked_max64(v2, v3, u0, u1));
       // order-preserving key; 0 (below every real key) for rows/columns outside the grid
       const unsigned key = (((rowok >> q) & 1u) && m > -INFINITY) ? order_key(m) : 0u;
