@@ -51,10 +51,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 #       python bench.py --steps 2 --warmup 3 --no-e2e --no-cpu-baseline
 # An entry goes back to None whenever its kernel changes, until it is captured again.
 NCU_DRAM_BYTES = {
-    "score_kernel": None,  # drain counters since that capture
-    "fwd_tc_kernel": None,  # pair exchange at a named barrier since that capture
-    "dq_kernel": 157.946e9 + 2.164e9,
-    "dkdv_kernel": None,  # half-stage ring since that capture
+    "score_kernel": 0.579e9 + 0.095e9,
+    "fwd_tc_kernel": 75.773e9 + 2.501e9,
+    "dq_kernel": 153.500e9 + 2.163e9,
+    "dkdv_kernel": 144.373e9 + 4.274e9,
 }
 
 def parse():
