@@ -68,6 +68,38 @@ __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// P = 2^(s scale_log2 - m) for one thread's 64 keys (two 32-column chunks of S in u0,
+// u1), stored as bf16 pairs in the first 16 TMEM columns of each chunk at tS; adds the
+// sums of P (sa + sb) and of bf16(P) (ra + rb).  kMask: keys whose bit in vm0 / vm1 is
+// clear (outside the grid) get P = 0.
+template <bool kMask>
+__device__ __forceinline__ void softmax_p(const uint32_t (&u0)[32], const uint32_t (&u1)[32], uint32_t vm0,
+                                          uint32_t vm1, float m, float scale_log2, uint32_t tS, float& sa, float& sb,
+                                          float& ra, float& rb) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const uint32_t(&u)[32] = cc ? u1 : u0;
+    const uint32_t vm = cc ? vm1 : vm0;
+    uint32_t ph[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float s0 = fmaf(__uint_as_float(u[2 * e]), scale_log2, -m);
+      float s1 = fmaf(__uint_as_float(u[2 * e + 1]), scale_log2, -m);
+      if (kMask) {
+        if (!((vm >> (2 * e)) & 1u)) s0 = -INFINITY;
+        if (!((vm >> (2 * e + 1)) & 1u)) s1 = -INFINITY;
+      }
+      const float p0 = ex2(s0), p1 = ex2(s1);
+      sa += p0;
+      sb += p1;
+      ph[e] = pack_bf16(p0, p1);
+      ra += __uint_as_float(ph[e] << 16);
+      rb += __uint_as_float(ph[e] & 0xFFFF0000u);
+    }
+    tmem_st16(tS + cc * 32, ph);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -307,10 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t u0[32], u1[32];
       uint32_t vm0 = ~0u, vm1 = ~0u;  // key rows of J inside the grid
       float mx = -INFINITY;
+      bool fullj = true;
       if (okw) {
         tc_fence_after();
         const int J = sel[j];
         const bool full = a.all_full || block_is_full(a.g, J);
+        fullj = full;
         if (!full) {
           vm0 = block_rows_mask32(a.g, J, hf * 64);
           vm1 = block_rows_mask32(a.g, J, hf * 64 + 32);
@@ -365,28 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // P = 2^(s - m) in bf16, packed in pairs: each 32-column chunk of S holds the
-      // P of its 32 keys in its first 16 columns.
+      // P of its 32 keys in its first 16 columns.  Full tiles skip the per-key mask.
       float sa = 0.f, sb = 0.f, ra = 0.f, rb = 0.f;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t(&u)[32] = cc ? u1 : u0;
-        const uint32_t vm = cc ? vm1 : vm0;
-        uint32_t ph[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float s0 = fmaf(__uint_as_float(u[2 * e]), a.scale_log2, -m);
-          float s1 = fmaf(__uint_as_float(u[2 * e + 1]), a.scale_log2, -m);
-          if (!((vm >> (2 * e)) & 1u)) s0 = -INFINITY;
-          if (!((vm >> (2 * e + 1)) & 1u)) s1 = -INFINITY;
-          const float p0 = ex2(s0), p1 = ex2(s1);
-          sa += p0;
-          sb += p1;
-          ph[e] = pack_bf16(p0, p1);
-          ra += __uint_as_float(ph[e] << 16);
-          rb += __uint_as_float(ph[e] & 0xFFFF0000u);
-        }
-        tmem_st16(tS + cc * 32, ph);
-      }
+      if (fullj)
+        softmax_p<false>(u0, u1, vm0, vm1, m, a.scale_log2, tS, sa, sb, ra, rb);
+      else
+        softmax_p<true>(u0, u1, vm0, vm1, m, a.scale_log2, tS, sa, sb, ra, rb);
       l += sa + sb;
       lr += ra + rb;
       tmem_wait_st();
