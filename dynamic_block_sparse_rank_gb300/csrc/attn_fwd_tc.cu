@@ -195,7 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int RS = is_k ? KST : VST;
       uint8_t* ring = is_k ? sK : sV;
       uint64_t* full = is_k ? kfull : vfull;
-      uint64_t* emp = is_k ? kempty : vempty;
       const CUtensorMap* map = is_k ? &tmK : &tmV;
       prefetch_tmap(map);
       if (is_k) {
