@@ -51,10 +51,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 #       python bench.py --steps 2 --warmup 3 --no-e2e --no-cpu-baseline
 # An entry goes back to None whenever its kernel changes, until it is captured again.
 NCU_DRAM_BYTES = {
-    "score_kernel": 0.579e9 + 0.095e9,
-    "fwd_tc_kernel": None,  # mask-free softmax loop since that capture
-    "dq_kernel": 153.500e9 + 2.163e9,
-    "dkdv_kernel": 144.373e9 + 4.274e9,
+    "score_kernel": 0.590e9 + 0.103e9,
+    "fwd_tc_kernel": 58.458e9 + 2.501e9,
+    "dq_kernel": 148.651e9 + 2.164e9,
+    "dkdv_kernel": 143.121e9 + 4.275e9,
 }
 
 def parse():
