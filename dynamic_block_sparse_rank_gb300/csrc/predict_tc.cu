@@ -8,11 +8,12 @@
 // ties to the lower J, reported ascending.
 //
 // Two kernels:
-//   proj_kernel   q~ (and k~) per (tile, head): fp32 FMA over d, rounded to
-//                 bf16 and written straight into the tensor-core operand layout
+//   proj_kernel   q~ (and k~) per (tile, head): d/16 tensor-core MMAs of the
+//                 TMA-loaded tile with W^T (fp32 accumulation), rounded to bf16
+//                 and written straight into the tensor-core operand layout
 //                 (no-swizzle K-major core matrices, tile after tile), so the
 //                 score kernel fetches each tile with one bulk copy.  Rows
-//                 outside the grid are written as zeros.
+//                 outside the grid are zeros.
 //   score_kernel  per (QB query blocks, head), QB = 4 when its score rows fit in
 //                 shared memory (else 2 or 1): streams every k~ tile through a
 //                 ring; each (key block, query block) pair is one M=128, N=128,
@@ -40,48 +41,97 @@ __device__ __forceinline__ uint32_t op_offset(int row, int col, int r) {
   return (uint32_t)((row >> 3) * (r >> 3) * 128 + (col >> 3) * 128 + (row & 7) * 16 + (col & 7) * 2);
 }
 
-template <int R>
-__global__ void __launch_bounds__(256) proj_kernel(Geom g, int Hh, int d, long long N, const __nv_bfloat16* __restrict__ X,
-                                                   const __nv_bfloat16* __restrict__ Wt, uint8_t* __restrict__ out, int b) {
-  extern __shared__ float psm[];
-  float* ws = psm;               // d x R
-  float* xs = ws + d * R;        // 128 x (d + 1)
-  const int I = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  const int ld = d + 1;
-  for (int e = tid; e < d * R; e += 256) ws[e] = __bfloat162float(Wt[(long long)h * d * R + e]);
-  const int vpr = d / 8;  // 16-byte vectors per row
-  for (int e = tid; e < 128 * vpr; e += 256) {
-    const int row = e / vpr, v = e % vpr;
-    const int n = block_row_token(g, I, row);
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (n >= 0) raw = *reinterpret_cast<const uint4*>(X + (((long long)b * N + n) * Hh + h) * d + v * 8);
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+// One CTA per (128-token tile, head): the tile arrives by TMA (the 5-D box of one
+// space-time tile, 128-byte swizzled, zero outside the grid), W^T is written to shared
+// memory in the operand layout, and d/16 MMAs (M=128, N=R) accumulate q~ (or k~) in
+// TMEM; each thread then rounds its row to bf16 and writes it in the score kernel's
+// operand layout.  fp32 accumulation of exact bf16 products, as the product of the
+// projection needs.
+template <int R, int D>
+__global__ void __launch_bounds__(128) proj_kernel(const __grid_constant__ CUtensorMap tmX, Geom g, int Hh,
+                                                   const __nv_bfloat16* __restrict__ W, uint8_t* __restrict__ out,
+                                                   int b, unsigned* status) {
+  constexpr int CH = D / 64;
+  constexpr uint32_t kCols = R <= 32 ? 32 : 64;  // TMEM allocation (a power of two)
+  const int I = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sX = smem;                 // 128 x D bf16, CH chunks of 16 KB
+  uint8_t* sW = sX + CH * 16384;      // W^T: R x D bf16, no-swizzle K-major core matrices
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sW + R * D * 2);
+  uint64_t* xfull = bars;
+  uint64_t* done = bars + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  int t0, h0, w0;
+  block_origin(g, I, t0, h0, w0);
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(xfull, 1);
+    mbar_init(done, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmX);
+    mbar_expect_tx(xfull, CH * 16384);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      xs[row * ld + v * 8 + 2 * q] = __uint_as_float(w4[q] << 16);
-      xs[row * ld + v * 8 + 2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
+    for (int c = 0; c < CH; ++c) tma_load_5d(sX + c * 16384, &tmX, xfull, c * 64, h, w0, h0, t0);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  // W[h] is [D, R] row-major; element (k, n) goes to row n, column k of W^T.
+  const __nv_bfloat16* Wh = W + (long long)h * D * R;
+  for (int e = tid; e < D * R; e += 128) {
+    const int k = e / R, n = e % R;
+    *reinterpret_cast<__nv_bfloat16*>(sW + op_offset(n, k, D)) = Wh[e];
+  }
+  fence_async_smem();  // W^T (generic stores) is read by the MMA (async proxy)
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+  if (warp == 0) {
+    const uint32_t leader = elect_leader();
+    ok = warp_wait(xfull, 0, status, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      constexpr uint32_t id = idesc_bf16(128, R, 0, 0);
+      const uint64_t dX = smem_desc(smem_u32(sX), 16, 1024, 2);
+      const uint64_t dW = smem_desc(smem_u32(sW), 128, (D / 8) * 128, 0);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_by(leader, tmem, dX + (uint64_t)((kk >> 2) * (16384 >> 4) + (kk & 3) * 2),
+                  dW + (uint64_t)(kk * (256 >> 4)), id, kk > 0);
+      mma_commit_by(leader, done);
     }
   }
-  __syncthreads();
-  constexpr int PER = R / 2;  // outputs per thread: 128 rows x R cols over 256 threads
-  const int row = tid >> 1, c0 = (tid & 1) * PER;
-  float acc[PER];
+  // every thread: row = TMEM lane = tid
+  ok = mbar_wait(done, 0, status, abort_flag) && ok;
+  tc_fence_after();
+  if (__all_sync(0xffffffffu, ok)) {
+    uint8_t* tile = out + (((long long)b * Hh + h) * g.nb + I) * (128LL * R * 2);
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll
-  for (int a = 0; a < PER; ++a) acc[a] = 0.f;
-  for (int c = 0; c < d; ++c) {
-    const float x = xs[row * ld + c];
+    for (int c = 0; c < R; c += 16) {
+      uint32_t u[16];
+      tmem_ld16(taddr + c, u);
+      tmem_wait_ld();
 #pragma unroll
-    for (int a = 0; a < PER; ++a) acc[a] = fmaf(x, ws[c * R + c0 + a], acc[a]);
+      for (int a = 0; a < 16; a += 8) {
+        uint4 v;
+        v.x = pack_bf16(__uint_as_float(u[a + 0]), __uint_as_float(u[a + 1]));
+        v.y = pack_bf16(__uint_as_float(u[a + 2]), __uint_as_float(u[a + 3]));
+        v.z = pack_bf16(__uint_as_float(u[a + 4]), __uint_as_float(u[a + 5]));
+        v.w = pack_bf16(__uint_as_float(u[a + 6]), __uint_as_float(u[a + 7]));
+        *reinterpret_cast<uint4*>(tile + op_offset(tid, c + a, R)) = v;
+      }
+    }
   }
-  uint8_t* tile = out + (((long long)b * Hh + h) * g.nb + I) * (128LL * R * 2);
-#pragma unroll
-  for (int a = 0; a < PER; a += 8) {
-    uint4 v;
-    v.x = pack_bf16(acc[a + 0], acc[a + 1]);
-    v.y = pack_bf16(acc[a + 2], acc[a + 3]);
-    v.z = pack_bf16(acc[a + 4], acc[a + 5]);
-    v.w = pack_bf16(acc[a + 6], acc[a + 7]);
-    *reinterpret_cast<uint4*>(tile + op_offset(row, c0 + a, R)) = v;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
   }
 }
 
@@ -337,6 +387,28 @@ cudaError_t launch_score(const Prob& p, ScoreArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int R, int D>
+cudaError_t launch_proj(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, uint8_t* qt,
+                        uint8_t* kt, unsigned* status, cudaStream_t st) {
+  const size_t smem = 1024 + (size_t)(D / 64) * 16384 + (size_t)R * D * 2 + 8 * 2 + 8;
+  cudaError_t e = cudaFuncSetAttribute(proj_kernel<R, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const size_t per_batch = (size_t)p.N * p.Hh * p.d * 2;
+  const Geom& g = p.g;
+  dim3 grid(g.nb, p.Hh);
+  for (int b = 0; b < p.B; ++b) {
+    CUtensorMap mQ, mK;
+    if (!make_token_map(&mQ, static_cast<const char*>(Q) + b * per_batch, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt,
+                        g.bh, g.bw) ||
+        !make_token_map(&mK, static_cast<const char*>(K) + b * per_batch, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt,
+                        g.bh, g.bw))
+      return cudaErrorInvalidValue;
+    proj_kernel<R, D><<<grid, 128, smem, st>>>(mQ, g, p.Hh, static_cast<const __nv_bfloat16*>(Wq), qt, b, status);
+    proj_kernel<R, D><<<grid, 128, smem, st>>>(mK, g, p.Hh, static_cast<const __nv_bfloat16*>(Wk), kt, b, status);
+  }
+  return cudaGetLastError();
+}
+
 constexpr size_t kMaxScoreSmem = 227 * 1024;
 
 template <int R>
@@ -345,19 +417,11 @@ cudaError_t launch_predict(const Prob& p, const void* Q, const void* K, const vo
   const size_t tiles = (size_t)p.B * p.Hh * p.g.nb;
   uint8_t* qt = static_cast<uint8_t*>(ws);
   uint8_t* kt = qt + align_up(tiles * 128 * R * 2, 256);
-  const size_t psmem = ((size_t)p.d * R + 128 * (p.d + 1)) * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(proj_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
-  if (e != cudaSuccess) return e;
-  dim3 pg(p.g.nb, p.Hh);
-  for (int b = 0; b < p.B; ++b) {
-    proj_kernel<R><<<pg, 256, psmem, st>>>(p.g, p.Hh, p.d, p.N, static_cast<const __nv_bfloat16*>(Q),
-                                           static_cast<const __nv_bfloat16*>(Wq), qt, b);
-    proj_kernel<R><<<pg, 256, psmem, st>>>(p.g, p.Hh, p.d, p.N, static_cast<const __nv_bfloat16*>(K),
-                                           static_cast<const __nv_bfloat16*>(Wk), kt, b);
-  }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   unsigned* status = status_ptr();
   if (!status) return cudaErrorUnknown;
+  cudaError_t e = p.d == 64 ? launch_proj<R, 64>(p, Q, K, Wq, Wk, qt, kt, status, st)
+                            : launch_proj<R, 128>(p, Q, K, Wq, Wk, qt, kt, status, st);
+  if (e != cudaSuccess) return e;
   ScoreArgs a;
   a.g = p.g;
   a.Hh = p.Hh;
