@@ -115,24 +115,28 @@ __global__ void csr_bitmap_kernel(const int32_t* __restrict__ idx, long long ent
   }
 }
 
-// counts[bh, J] = number of query blocks that kept J.
+// counts[bh, J] = number of query blocks that kept J.  One warp per (bh, J): lane i
+// reads row I0 + i of the bitmap column, the warp counts with a ballot.
 __global__ void csr_count_kernel(const unsigned* __restrict__ bitmap, int nb, int words, long long total,
                                  int32_t* __restrict__ counts) {
-  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  if (t >= total) return;
+  const long long t = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= total) return;  // whole warps: t is the same on every lane
   const long long bh = t / nb;
   const int J = (int)(t % nb);
   const unsigned* col = bitmap + bh * nb * words + (J >> 5);
   const unsigned bit = 1u << (J & 31);
   int c = 0;
-  for (int I = 0; I < nb; ++I) c += (col[(long long)I * words] & bit) ? 1 : 0;
-  counts[t] = c;
+  for (int I0 = 0; I0 < nb; I0 += 32) {
+    const int I = I0 + lane;
+    c += __popc(__ballot_sync(0xffffffffu, I < nb && (col[(long long)I * words] & bit)));
+  }
+  if (lane == 0) counts[t] = c;
 }
 
-// Per (batch, head): exclusive scan of counts -> offsets, and the visiting order
-// of key blocks by descending count (ties by ascending J).
+// Per (batch, head): exclusive scan of counts -> offsets.
 __global__ void __launch_bounds__(1024) csr_scan_kernel(const int32_t* __restrict__ counts, int nb,
-                                                        int32_t* __restrict__ offsets, int32_t* __restrict__ order) {
+                                                        int32_t* __restrict__ offsets) {
   extern __shared__ int32_t cs[];  // nb
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
@@ -164,29 +168,47 @@ __global__ void __launch_bounds__(1024) csr_scan_kernel(const int32_t* __restric
     __syncthreads();
   }
   if (tid == 0) offsets[bh * (nb + 1) + nb] = carry;
-  for (int J = tid; J < nb; J += blockDim.x) {
-    const int c = cs[J];
-    int rank = 0;
-    for (int J2 = 0; J2 < nb; ++J2) {
-      const int c2 = cs[J2];
-      rank += (c2 > c) || (c2 == c && J2 < J);
-    }
-    order[bh * nb + rank] = J;
-  }
 }
 
+// The visiting order of key blocks: descending count, ties by ascending J (the rank
+// of J counts the blocks before it).  Grid (chunks of 256 key blocks, B * heads).
+__global__ void __launch_bounds__(256) csr_order_kernel(const int32_t* __restrict__ counts, int nb,
+                                                        int32_t* __restrict__ order) {
+  extern __shared__ int32_t cs[];  // nb
+  const long long bh = blockIdx.y;
+  for (int J = threadIdx.x; J < nb; J += blockDim.x) cs[J] = counts[bh * nb + J];
+  __syncthreads();
+  const int J = blockIdx.x * blockDim.x + threadIdx.x;
+  if (J >= nb) return;
+  const int c = cs[J];
+  int rank = 0;
+  for (int J2 = 0; J2 < nb; ++J2) {
+    const int c2 = cs[J2];
+    rank += (c2 > c) || (c2 == c && J2 < J);
+  }
+  order[bh * nb + rank] = J;
+}
+
+// lists: for each key block J, the query blocks that kept it, ascending.  One warp
+// per (bh, J); each 32-row step's hits are written contiguously.
 __global__ void csr_fill_kernel(const unsigned* __restrict__ bitmap, const int32_t* __restrict__ offsets, int nb,
                                 int k, int words, long long total, int32_t* __restrict__ lists) {
-  const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  if (t >= total) return;
+  const long long t = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= total) return;  // whole warps
   const long long bh = t / nb;
   const int J = (int)(t % nb);
   const unsigned* col = bitmap + bh * nb * words + (J >> 5);
   const unsigned bit = 1u << (J & 31);
   int pos = offsets[bh * (nb + 1) + J];
   int32_t* out = lists + bh * nb * k;
-  for (int I = 0; I < nb; ++I)
-    if (col[(long long)I * words] & bit) out[pos++] = I;
+  for (int I0 = 0; I0 < nb; I0 += 32) {
+    const int I = I0 + lane;
+    const bool hit = I < nb && (col[(long long)I * words] & bit);
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (hit) out[pos + __popc(m & ((1u << lane) - 1u))] = I;
+    pos += __popc(m);
+  }
 }
 
 // ------------------------------------------------------------------ shared pieces
@@ -874,9 +896,11 @@ cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const vo
   const long long entries = bhn * p.k;
   csr_bitmap_kernel<<<(int)std::min<long long>((entries + 255) / 256, 1 << 20), 256, 0, st>>>(idx, entries, g.nb, p.k,
                                                                                               words, w.bitmap, status);
-  csr_count_kernel<<<(int)((bhn + 255) / 256), 256, 0, st>>>(w.bitmap, g.nb, words, bhn, w.counts);
-  csr_scan_kernel<<<p.B * p.Hh, 1024, g.nb * sizeof(int32_t), st>>>(w.counts, g.nb, w.offsets, w.order);
-  csr_fill_kernel<<<(int)((bhn + 255) / 256), 256, 0, st>>>(w.bitmap, w.offsets, g.nb, p.k, words, bhn, w.lists);
+  csr_count_kernel<<<(int)((bhn * 32 + 255) / 256), 256, 0, st>>>(w.bitmap, g.nb, words, bhn, w.counts);
+  csr_scan_kernel<<<p.B * p.Hh, 1024, g.nb * sizeof(int32_t), st>>>(w.counts, g.nb, w.offsets);
+  csr_order_kernel<<<dim3((g.nb + 255) / 256, p.B * p.Hh), 256, g.nb * sizeof(int32_t), st>>>(w.counts, g.nb,
+                                                                                               w.order);
+  csr_fill_kernel<<<(int)((bhn * 32 + 255) / 256), 256, 0, st>>>(w.bitmap, w.offsets, g.nb, p.k, words, bhn, w.lists);
   const long long n8 = (long long)p.B * p.N * p.Hh * p.d / 8;
   const int cb = (int)std::min<long long>((n8 + 255) / 256, 152LL * 16);
   half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(Q), reinterpret_cast<uint4*>(w.Q16), n8);
@@ -891,7 +915,7 @@ cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const vo
       pre_kernel<128><<<dim3(g.nb, p.Hh), 128, 0, st>>>(g, p.Hh, p.N, b, static_cast<const __nv_bfloat16*>(O),
                                                         static_cast<const __nv_bfloat16*>(dO), LSE, w.Dv, w.L2v);
   }
-  note_launches(8 + p.B);
+  note_launches(9 + p.B);  // 5 block-map kernels, 4 fp16 copies, one pre_kernel per batch entry
   return cudaGetLastError();
 }
 

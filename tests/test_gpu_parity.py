@@ -225,7 +225,7 @@ def test_backward_phases_equal_the_single_call_bitwise(sda):
         assert torch.equal(a, b)
     before = sda.sda_kernel_launch_count()
     sda.sda_attn_bwd(p, Q, K, V, O, LSE, dO, idx, *one, "f32", ws)
-    assert sda.sda_kernel_launch_count() - before == 8 + 1 + 1 + 1  # prepare (8 + B), dq (B), dkdv (B)
+    assert sda.sda_kernel_launch_count() - before == 9 + 1 + 1 + 1  # prepare (9 + B), dq (B), dkdv (B)
 
 
 def test_bounded_wait_runs_out_and_reports_a_timeout(sda):
