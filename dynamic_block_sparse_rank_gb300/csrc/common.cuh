@@ -133,38 +133,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   }
 }
 
-// Non-blocking test of the phase (no suspension).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// As mbar_wait, but polling without suspension: for short, latency-critical
-// waits on a pipeline partner (the wake-up from a suspended wait is slower).
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, unsigned* status,
-                                               volatile int* abort_flag, uint64_t limit_ns = SDA_WAIT_LIMIT_NS) {
-  if (mbar_test_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        atomicOr(status, kStatusWaitTimeout);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
 // Release/acquire counters in shared memory: a cheaper hand-off than an mbarrier
 // when the waiter usually finds the count already reached (one shared load).
 __device__ __forceinline__ void count_release_add(unsigned* p, unsigned v) {
@@ -377,10 +345,6 @@ __device__ __forceinline__ void mma_commit_by(uint32_t leader, uint64_t* bar) {
 // Bounded wait by a whole warp; the result is the same on every lane.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* status, volatile int* abort_flag) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort_flag));
-}
-__device__ __forceinline__ bool warp_wait_spin(uint64_t* bar, uint32_t parity, unsigned* status,
-                                               volatile int* abort_flag) {
-  return __all_sync(0xffffffffu, mbar_wait_spin(bar, parity, status, abort_flag));
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane (base lane + i).
