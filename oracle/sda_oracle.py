@@ -43,6 +43,11 @@ Readings taken where the pages are silent (each is restated in the design notes)
    partition p from query block I is |p - p(I)|, and the n_reuse partitions
    of largest distance (ties to the lower p) are taken from the previous
    step, whose states come from its own inputs and its own block selection.
+9. Training through the merge: the pages describe the reuse for generation
+   only.  Read for training, the reused states are constants of this step
+   (they were computed from an earlier step's inputs) and carry no gradient;
+   the fresh states are differentiated by the chain rule through the merge
+   and through softmax attention restricted to their key range.
 """
 from __future__ import annotations
 
@@ -218,7 +223,8 @@ def attn_fwd(Q, K, V, idx, geom: Geometry, scale=None, kb_begin=0, kb_end=None, 
     return O, LSE
 
 
-def attn_bwd(Q, K, V, dO, idx, geom: Geometry, scale=None, query_blocks=None):
+def attn_bwd(Q, K, V, dO, idx, geom: Geometry, scale=None, query_blocks=None, kb_begin=0, kb_end=None,
+             qb_active=None, dLSE=None):
     """Gradients of block-sparse attention with the block map held fixed (reading 6).
 
     With P_ij = exp(S_ij - LSE_i) over the kept keys and D_i = dO_i . O_i:
@@ -227,6 +233,12 @@ def attn_bwd(Q, K, V, dO, idx, geom: Geometry, scale=None, query_blocks=None):
     query_blocks restricts the sums over i to those query blocks (idx rows
     then follow that list); by linearity the full gradient is the sum over any
     split of the query blocks.  Returns (dQ, dK, dV), each [B, N, Hh, d] fp64.
+
+    Partition states (reading 9): kb_begin, kb_end and qb_active select the
+    state (O_p, LSE_p) that attn_fwd computes with the same arguments; dO is
+    then dL/dO_p and dLSE ([B, Hh, N], None = 0) is dL/dLSE_p.  Since
+    d LSE_i / d S_ij = P_ij, the LSE gradient enters as dS_ij = P_ij (dP_ij -
+    D_i + dLSE_i).  Query blocks with qb_active[I] == 0 contribute nothing.
     """
     Q = np.asarray(Q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
@@ -237,12 +249,15 @@ def attn_bwd(Q, K, V, dO, idx, geom: Geometry, scale=None, query_blocks=None):
     dQ = np.zeros_like(Q)
     dK = np.zeros_like(K)
     dV = np.zeros_like(V)
+    kb_end = geom.n_blocks if kb_end is None else kb_end
     qb = list(range(geom.n_blocks)) if query_blocks is None else list(query_blocks)
     for b in range(B):
         for h in range(Hh):
             for a, I in enumerate(qb):
+                if qb_active is not None and not qb_active[I]:
+                    continue
                 rows = geom.tokens(I)
-                keys = _kept_keys(geom, idx[b, h, a], 0, geom.n_blocks)
+                keys = _kept_keys(geom, idx[b, h, a], kb_begin, kb_end)
                 if len(keys) == 0:
                     continue
                 q, kk, v, do = Q[b, rows, h], K[b, keys, h], V[b, keys, h], dO[b, rows, h]
@@ -252,8 +267,9 @@ def attn_bwd(Q, K, V, dO, idx, geom: Geometry, scale=None, query_blocks=None):
                 P = np.exp(S - lse)
                 o = P @ v
                 D = (do * o).sum(axis=1, keepdims=True)
+                g = 0.0 if dLSE is None else np.asarray(dLSE, dtype=np.float64)[b, h, rows][:, None]
                 dP = do @ v.T
-                dS = P * (dP - D)
+                dS = P * (dP - D + g)
                 dV[b, keys, h] += P.T @ do
                 dQ[b, rows, h] += scale * (dS @ kk)
                 dK[b, keys, h] += scale * (dS.T @ q)
@@ -311,6 +327,18 @@ def attn_bwd_blocks(Q, K, V, dO, idx, geom: Geometry, scale=None, query_blocks=(
 
 
 # --------------------------------------------------------------------------- step 3: state merge
+def _merge_weights(L):
+    """Per row of the stacked LSE_p [P, rows...]: (LSE, w_p = exp(LSE_p - LSE)); all -inf rows give (-inf, 0)."""
+    m = L.max(axis=0)
+    empty = np.isneginf(m)
+    m_safe = np.where(empty, 0.0, m)
+    s = np.exp(L - m_safe).sum(axis=0)
+    with np.errstate(divide="ignore"):
+        lse = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, s)))
+    w = np.where(empty[None], 0.0, np.exp(L - np.where(empty, 0.0, lse)[None]))
+    return lse, w
+
+
 def merge_states(O_parts, LSE_parts):
     """LSE merge of partial attention states (DiTango's state reuse, reading 7).
 
@@ -320,15 +348,31 @@ def merge_states(O_parts, LSE_parts):
     """
     L = np.stack([np.asarray(x, dtype=np.float64) for x in LSE_parts])  # [P, rows...]
     O = np.stack([np.asarray(x, dtype=np.float64) for x in O_parts])  # [P, rows..., d]
-    m = L.max(axis=0)
-    empty = np.isneginf(m)
-    m_safe = np.where(empty, 0.0, m)
-    s = np.exp(L - m_safe).sum(axis=0)
-    with np.errstate(divide="ignore"):
-        lse = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, s)))
-    w = np.where(empty[None], 0.0, np.exp(L - np.where(empty, 0.0, lse)[None]))
+    lse, w = _merge_weights(L)
     out = (w[..., None] * O).sum(axis=0)
     return out, lse
+
+
+def merge_states_bwd(O_parts, LSE_parts, dO, dLSE=None):
+    """Gradient of merge_states (training through DiTango's merge, reading 9).
+
+    With w_p = exp(LSE_p - LSE) and O = sum_p w_p O_p, the chain rule gives
+    dLSE/dLSE_p = w_p and dO/dLSE_p = w_p (O_p - O), so
+      dL/dO_p = w_p dO,   dL/dLSE_p = w_p (dO . (O_p - O) + dLSE).
+    Shapes as merge_states; dO matches O's rows x d, dLSE the LSE rows (None =
+    0).  Rows where every LSE_p is -inf give zeros.  Returns (list of dO_p,
+    list of dLSE_p).
+    """
+    L = np.stack([np.asarray(x, dtype=np.float64) for x in LSE_parts])
+    O = np.stack([np.asarray(x, dtype=np.float64) for x in O_parts])
+    dO = np.asarray(dO, dtype=np.float64)
+    _, w = _merge_weights(L)
+    Om = (w[..., None] * O).sum(axis=0)
+    g = 0.0 if dLSE is None else np.asarray(dLSE, dtype=np.float64)
+    dot = (dO[None] * (np.where(w[..., None] > 0, O, 0.0) - Om[None])).sum(axis=-1)
+    dL = w * (dot + g)
+    dOp = w[..., None] * dO[None]
+    return [dOp[p] for p in range(len(O_parts))], [dL[p] for p in range(len(O_parts))]
 
 
 def frame_partitions(geom: Geometry, P):
@@ -381,3 +425,35 @@ def reuse_merge(states_now, states_prev, geom, P, n_reuse):
         Ls.append(np.transpose(L_p, (0, 2, 1)))  # [B, N, Hh] to match O's row layout
     O, L = merge_states(Os, Ls)
     return O, np.transpose(L, (0, 2, 1))
+
+
+def reuse_bwd(Q, K, V, dO, idx, geom, P, n_reuse, states_prev, dLSE=None, scale=None):
+    """Gradient of reuse_merge with respect to this step's Q, K, V (reading 9).
+
+    The reused states come from an earlier step and are constants here; only
+    the fresh ones carry gradient.  dL/d(state) comes from merge_states_bwd of
+    the states reuse_merge merged, then each fresh partition state (key range
+    of partition p, query blocks that recompute it) is differentiated with
+    attn_bwd.  dO: [B, N, Hh, d]; dLSE: [B, Hh, N] or None.  Returns (dQ, dK, dV).
+    """
+    now = partition_states(Q, K, V, idx, geom, P, scale)
+    reuse = reuse_mask(geom, P, n_reuse)
+    Os, Ls = [], []
+    for p in range(P):
+        O_p, L_p = now[p][0].copy(), now[p][1].copy()
+        for I in range(geom.n_blocks):
+            if reuse[p, I]:
+                rows = geom.tokens(I)
+                O_p[:, rows] = states_prev[p][0][:, rows]
+                L_p[:, :, rows] = states_prev[p][1][:, :, rows]
+        Os.append(O_p)
+        Ls.append(np.transpose(L_p, (0, 2, 1)))
+    g = None if dLSE is None else np.transpose(np.asarray(dLSE, dtype=np.float64), (0, 2, 1))
+    dOs, dLs = merge_states_bwd(Os, Ls, dO, g)
+    grads = [np.zeros(np.shape(X)) for X in (Q, K, V)]
+    for p, (b0, b1) in enumerate(frame_partitions(geom, P)):
+        part = attn_bwd(Q, K, V, dOs[p], idx, geom, scale, kb_begin=b0, kb_end=b1, qb_active=~reuse[p],
+                        dLSE=np.transpose(dLs[p], (0, 2, 1)))
+        for acc, x in zip(grads, part):
+            acc += x
+    return tuple(grads)

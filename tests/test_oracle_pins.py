@@ -474,3 +474,140 @@ def test_backward_is_the_sum_over_query_block_splits():
     gb = orc.attn_bwd(Q, K, V, dO, idx[:, :, part_b], geom, query_blocks=part_b)
     for f, a, b in zip(full, ga, gb):
         assert np.abs(a + b - f).max() < 1e-12
+
+
+# ------------------------------------------------------------------ training through the merge
+def _merge_loss(Os, Ls, dO, dLSE):
+    O, L = orc.merge_states(Os, Ls)
+    live = np.isfinite(L)
+    return float((O * dO).sum() + (np.where(live, L, 0.0) * dLSE).sum())
+
+
+def _merge_case(seed, P=3, rows=(2, 3), d=4):
+    rng = np.random.default_rng(seed)
+    Os = [rng.standard_normal(rows + (d,)) for _ in range(P)]
+    Ls = [rng.standard_normal(rows) * 2 for _ in range(P)]
+    Ls[1][0, 1] = -np.inf  # one empty part in a live row
+    for L in Ls:
+        L[1, 2] = -np.inf  # one row where every part is empty
+    dO = rng.standard_normal(rows + (d,))
+    dLSE = rng.standard_normal(rows)
+    return Os, Ls, dO, dLSE
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_merge_bwd_finite_differences(seed):
+    Os, Ls, dO, dLSE = _merge_case(seed)
+    dOs, dLs = orc.merge_states_bwd(Os, Ls, dO, dLSE)
+    h = 1e-6
+    for p in range(len(Os)):
+        for X, G in ((Os[p], dOs[p]), (Ls[p], dLs[p])):
+            num = np.zeros_like(X)
+            for pos in np.ndindex(X.shape):
+                x0 = X[pos]
+                if np.isneginf(x0):  # an empty part stays empty under any finite change of the others
+                    continue
+                X[pos] = x0 + h
+                lp = _merge_loss(Os, Ls, dO, dLSE)
+                X[pos] = x0 - h
+                lm = _merge_loss(Os, Ls, dO, dLSE)
+                X[pos] = x0
+                num[pos] = (lp - lm) / (2 * h)
+            assert np.abs(num - G).max() <= 1e-6 * max(1.0, np.abs(G).max())
+
+
+def test_merge_bwd_invariants_and_special_cases():
+    Os, Ls, dO, dLSE = _merge_case(3)
+    dOs, dLs = orc.merge_states_bwd(Os, Ls, dO, dLSE)
+    live = np.isfinite(orc.merge_states(Os, Ls)[1])
+    # the weights sum to 1 and sum_p w_p (O_p - O) = 0 on every live row
+    assert np.abs((sum(dOs) - dO)[live]).max() < 1e-12
+    assert np.abs((sum(dLs) - dLSE)[live]).max() < 1e-12
+    # empty rows and empty parts get nothing
+    assert all(np.all(x[~live] == 0) for x in dOs) and all(np.all(x[~live] == 0) for x in dLs)
+    assert np.all(dOs[1][0, 1] == 0) and dLs[1][0, 1] == 0
+    # one state: the merge is the identity
+    a, b = orc.merge_states_bwd(Os[:1], [np.zeros((2, 3))], dO, dLSE)
+    assert np.array_equal(a[0], dO) and np.abs(b[0] - dLSE).max() < 1e-15
+
+
+def _lse_loss_torch(q, k, v, mask, dO, dLSE, scale):
+    s = (q @ k.T) * scale
+    s = s.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(s, dim=1)
+    o = torch.softmax(s, dim=1) @ v
+    return (o * dO).sum() + (lse * dLSE).sum()
+
+
+def test_partition_backward_matches_torch_autograd():
+    """A key range, inactive query blocks and an LSE gradient, against autograd through logsumexp + softmax."""
+    geom = orc.Geometry(4, 2, 4, 1, 2, 2)  # 4 slabs of 2 blocks
+    B, Hh, d = 1, 2, 4
+    Q, K, V, dO = (_rand((B, geom.N, Hh, d), s, 1.5) for s in (110, 111, 112, 113))
+    dLSE = _rand((B, Hh, geom.N), 114)
+    idx = _random_map(geom, B, Hh, 4, 115)
+    kb0, kb1 = 2, 6
+    active = np.array([1, 0, 1, 1, 0, 1, 1, 1], dtype=bool)
+    dQ, dK, dV = orc.attn_bwd(Q, K, V, dO, idx, geom, kb_begin=kb0, kb_end=kb1, qb_active=active, dLSE=dLSE)
+    ids = _block_id_brute(geom)
+    scale = 1.0 / math.sqrt(d)
+    for h in range(Hh):
+        mask = _mask_from_map(geom, idx[0, h]) & ((ids >= kb0) & (ids < kb1))[None, :]
+        rows = active[ids] & mask.any(axis=1)  # rows of active blocks with at least one key in the range
+        q, k, v = (torch.tensor(X[0, :, h], requires_grad=True) for X in (Q, K, V))
+        r = torch.from_numpy(np.nonzero(rows)[0])
+        loss = _lse_loss_torch(q[r], k, v, torch.from_numpy(mask[rows]), torch.from_numpy(dO[0, rows, h]),
+                               torch.from_numpy(dLSE[0, h, rows]), scale)
+        loss.backward()
+        assert np.abs(q.grad.numpy() - dQ[0, :, h]).max() < 1e-12
+        assert np.abs(k.grad.numpy() - dK[0, :, h]).max() < 1e-12
+        assert np.abs(v.grad.numpy() - dV[0, :, h]).max() < 1e-12
+
+
+def test_merge_and_partition_backward_compose_to_full():
+    """Partitions covering every key, merged: the chain rule through the merge gives the full gradient."""
+    geom = orc.Geometry(5, 2, 4, 1, 2, 2)
+    B, Hh, d, P = 1, 2, 4, 3
+    Q, K, V, dO = (_rand((B, geom.N, Hh, d), s) for s in (120, 121, 122, 123))
+    dLSE = _rand((B, Hh, geom.N), 124)
+    idx = _random_map(geom, B, Hh, 5, 125)
+    states = orc.partition_states(Q, K, V, idx, geom, P)
+    tr = lambda L: np.transpose(L, (0, 2, 1))  # [B, Hh, N] <-> [B, N, Hh]
+    dOs, dLs = orc.merge_states_bwd([s[0] for s in states], [tr(s[1]) for s in states], dO, tr(dLSE))
+    total = [np.zeros_like(X) for X in (Q, K, V)]
+    for p, (b0, b1) in enumerate(orc.frame_partitions(geom, P)):
+        part = orc.attn_bwd(Q, K, V, dOs[p], idx, geom, kb_begin=b0, kb_end=b1, dLSE=tr(dLs[p]))
+        for acc, x in zip(total, part):
+            acc += x
+    full = orc.attn_bwd(Q, K, V, dO, idx, geom, dLSE=dLSE)
+    for a, b in zip(total, full):
+        assert np.abs(a - b).max() < 1e-12
+
+
+def test_reuse_backward_finite_differences():
+    """The reuse-aware training gradient: reused states are constants, fresh ones carry the gradient."""
+    geom = orc.Geometry(4, 2, 2, 1, 2, 2)  # 4 slabs of 1 block
+    B, Hh, d, P, n_reuse = 1, 1, 3, 4, 2
+    Q, K, V, dO = (_rand((B, geom.N, Hh, d), s) for s in (130, 131, 132, 133))
+    dLSE = _rand((B, Hh, geom.N), 134)
+    idx = _random_map(geom, B, Hh, 3, 135)
+    prev = orc.partition_states(Q + 0.3, K - 0.2, V * 1.1, _random_map(geom, B, Hh, 3, 136), geom, P)
+    dQ, dK, dV = orc.reuse_bwd(Q, K, V, dO, idx, geom, P, n_reuse, prev, dLSE=dLSE)
+
+    def loss():
+        O, L = orc.reuse_merge(orc.partition_states(Q, K, V, idx, geom, P), prev, geom, P, n_reuse)
+        return float((O * dO).sum() + (L * dLSE).sum())
+
+    h = 1e-6
+    for X, G in ((Q, dQ), (K, dK), (V, dV)):
+        num = np.zeros_like(X)
+        for pos in np.ndindex(X.shape):
+            x0 = X[pos]
+            X[pos] = x0 + h
+            lp = loss()
+            X[pos] = x0 - h
+            lm = loss()
+            X[pos] = x0
+            num[pos] = (lp - lm) / (2 * h)
+        assert np.abs(num - G).max() <= 1e-6 * max(1.0, np.abs(G).max())
+    assert np.abs(dK).max() > 0 and np.abs(dV).max() > 0
