@@ -430,7 +430,23 @@ def main():
         rows = mw.N * mw.heads
         mbytes = (n_st + 1) * rows * (2 * mw.d + 4)
         merge = {"workload": mw.name, "states": n_st, "ms": mms, "bytes": mbytes, "gbs": mbytes / (mms / 1e3) / 1e9}
-        del Os, Ls, Oo, Lo
+        del Oo, Lo
+        # its gradient: reads the states, dO and dLSE, writes dO_p and dLSE_p for every state
+        dO = torch.randn((1, mw.N, mw.heads, mw.d), device=dev, generator=g).to(torch.bfloat16)
+        dL = torch.randn((1, mw.heads, mw.N), device=dev, generator=g)
+        gO = [torch.empty_like(Os[0]) for _ in range(n_st)]
+        gL = [torch.empty_like(Ls[0]) for _ in range(n_st)]
+        for _ in range(3):
+            sda.sda_merge_states_bwd(Os, Ls, dO, dL, 1, mw.N, mw.heads, mw.d, "bf16", gO, gL, stream)
+        m0.record(stream)
+        for _ in range(reps):
+            sda.sda_merge_states_bwd(Os, Ls, dO, dL, 1, mw.N, mw.heads, mw.d, "bf16", gO, gL, stream)
+        m1.record(stream)
+        torch.cuda.synchronize()
+        bms = m0.elapsed_time(m1) / reps
+        bbytes = (2 * n_st + 1) * rows * (2 * mw.d + 4)
+        merge["bwd"] = {"ms": bms, "bytes": bbytes, "gbs": bbytes / (bms / 1e3) / 1e9}
+        del Os, Ls, dO, dL, gO, gL
 
     if rank != 0:
         if dist is not None:
@@ -453,6 +469,7 @@ def main():
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     if merge:
         merge["frac_of_hbm_peak"] = merge["gbs"] / hbm_peak
+        merge["bwd"]["frac_of_hbm_peak"] = merge["bwd"]["gbs"] / hbm_peak
     attn_ms = phase_ms["fwd"] + phase_ms["bwd_prepare"] + phase_ms["bwd_dq"] + phase_ms["bwd_dkdv"]
     cpu = None
     if not args.no_cpu_baseline and world == 1:

@@ -254,4 +254,33 @@ sda_status sda_merge_states(int n_states, const void* const* O_parts, const floa
   return from_cuda(launch_merge(a, dtype, static_cast<cudaStream_t>(stream)));
 }
 
+sda_status sda_merge_states_bwd(int n_states, const void* const* O_parts, const float* const* LSE_parts,
+                                const void* dO, const float* dLSE, int B, int N, int heads, int head_dim,
+                                int dtype, void* const* dO_parts, float* const* dLSE_parts, void* stream) {
+  if (n_states < 1 || n_states > kMaxStates || !O_parts || !LSE_parts || !dO || !dO_parts || !dLSE_parts)
+    return SDA_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || heads < 1 || head_dim < 1) return SDA_ERR_INVALID_ARG;
+  if (dtype != SDA_F32 && dtype != SDA_BF16) return SDA_ERR_INVALID_ARG;
+  const int es = dtype == SDA_BF16 ? 2 : 4;
+  if ((head_dim * es) % 16 != 0 || head_dim * es > 16 * 32 * 8) return SDA_ERR_UNSUPPORTED;
+  if (!aligned16(dO)) return SDA_ERR_INVALID_ARG;
+  MergeBwdArgs a;
+  for (int s = 0; s < n_states; ++s) {
+    if (!O_parts[s] || !LSE_parts[s] || !dO_parts[s] || !dLSE_parts[s]) return SDA_ERR_INVALID_ARG;
+    if (!aligned16(O_parts[s]) || !aligned16(dO_parts[s])) return SDA_ERR_INVALID_ARG;
+    a.O[s] = O_parts[s];
+    a.L[s] = LSE_parts[s];
+    a.dO_out[s] = dO_parts[s];
+    a.dL_out[s] = dLSE_parts[s];
+  }
+  a.dO = dO;
+  a.dL = dLSE;
+  a.n_states = n_states;
+  a.B = B;
+  a.N = N;
+  a.Hh = heads;
+  a.d = head_dim;
+  return from_cuda(launch_merge_bwd(a, dtype, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

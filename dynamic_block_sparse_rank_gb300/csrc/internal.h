@@ -39,6 +39,18 @@ void note_launches(int n);
 // ---- merge.cu
 cudaError_t launch_merge(const MergeArgs& a, int dtype, cudaStream_t st);
 
+struct MergeBwdArgs {
+  const void* O[kMaxStates];
+  const float* L[kMaxStates];
+  const void* dO;
+  const float* dL;  // may be null (zero LSE gradient)
+  void* dO_out[kMaxStates];
+  float* dL_out[kMaxStates];
+  int n_states;
+  int B, N, Hh, d;
+};
+cudaError_t launch_merge_bwd(const MergeBwdArgs& a, int dtype, cudaStream_t st);
+
 // ---- simt.cu (fp32 problems)
 size_t predict_ws_f32(const Prob& p);
 cudaError_t predict_f32(const Prob& p, const float* Q, const float* K, const float* Wq, const float* Wk,

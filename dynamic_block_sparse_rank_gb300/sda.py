@@ -18,7 +18,7 @@ SDA_F32, SDA_BF16 = 0, 1
 SDA_OP_PREDICT, SDA_OP_BWD = 0, 1
 
 EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_attn_fwd", "sda_attn_bwd",
-           "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_merge_states",
+           "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_merge_states", "sda_merge_states_bwd",
            "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_selftest_wait_timeout", "sda_status_string")
 
 
@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.sda_kernel_launch_count.argtypes = []
         L.sda_kernel_launch_count.restype = ctypes.c_ulonglong
         L.sda_merge_states.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i32, i32, i32, vp, vp, vp]
+        L.sda_merge_states_bwd.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp, i32, i32, i32, i32,
+                                           i32, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
         L.sda_get_device_status.argtypes = [vp]
         L.sda_status_string.argtypes = [i32]
         L.sda_status_string.restype = ctypes.c_char_p
@@ -192,6 +194,16 @@ def sda_merge_states(O_parts, LSE_parts, B, N, heads, head_dim, dtype, O_out, LS
     lptrs = (ctypes.c_void_p * max(n, 1))(*[_ptr(x) for x in LSE_parts])
     _check(lib().sda_merge_states(n, optrs, lptrs, int(B), int(N), int(heads), int(head_dim), int(dt), _ptr(O_out),
                                   _ptr(LSE_out), _stream(stream)), "sda_merge_states")
+
+
+def sda_merge_states_bwd(O_parts, LSE_parts, dO, dLSE, B, N, heads, head_dim, dtype, dO_parts, dLSE_parts,
+                         stream=None):
+    n = len(O_parts)
+    dt = {"f32": SDA_F32, "bf16": SDA_BF16}.get(dtype, dtype)
+    arr = lambda xs: (ctypes.c_void_p * max(n, 1))(*[_ptr(x) for x in xs])
+    _check(lib().sda_merge_states_bwd(n, arr(O_parts), arr(LSE_parts), _ptr(dO), _ptr(dLSE), int(B), int(N),
+                                      int(heads), int(head_dim), int(dt), arr(dO_parts), arr(dLSE_parts),
+                                      _stream(stream)), "sda_merge_states_bwd")
 
 
 def sda_get_device_status(stream=None) -> int:

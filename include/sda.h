@@ -19,7 +19,8 @@
  *   3. sda_merge_states — the log-sum-exp merge of partial attention states
  *      computed over separate key partitions: the state-reuse primitive of
  *      "DiTango: Cost-Effective Parallel Diffusion Generation with Selective
- *      Attention State Reuse" (near partitions recomputed, far ones reused).
+ *      Attention State Reuse" (near partitions recomputed, far ones reused),
+ *      and sda_merge_states_bwd, its gradient for training through the reuse.
  *
  * Conventions shared by every call
  *   - Tokens of a T x H x W latent grid are in raster order n = (t*H + h)*W + w.
@@ -154,6 +155,24 @@ sda_status sda_attn_bwd_dkdv(const sda_problem* p, const void* Q, const void* K,
 sda_status sda_merge_states(int n_states, const void* const* O_parts, const float* const* LSE_parts,
                             int B, int N, int heads, int head_dim, int dtype, void* O_out,
                             float* LSE_out, void* stream);
+
+/* Gradient of sda_merge_states, for training through DiTango's state reuse:
+ * the fresh partition states carry the gradient (reused states are constants
+ * of the step and need none).  Same states and layouts as sda_merge_states:
+ *   O_parts[s], LSE_parts[s]  the merged states (1 <= n_states <= 16)
+ *   dO         [B, N, heads, d] (dtype): gradient of the merged O
+ *   dLSE       [B, heads, N] fp32, or NULL for a zero gradient of the merged LSE
+ *   dO_parts[s]   [B, N, heads, d] (dtype): w_s dO
+ *   dLSE_parts[s] [B, heads, N] fp32:       w_s (dO . (O_s - O) + dLSE)
+ * with w_s = exp(LSE_s - LSE), LSE and O recomputed from the states in fp32 as
+ * the merge computes them.  Parts with LSE_s = -inf, and rows where every
+ * LSE_s is -inf, get zero gradients.  Each dO_parts[s] / dLSE_parts[s] pair is
+ * then the (dO, dLSE) input of that partition's backward.  Outputs must not
+ * overlap any input or each other; the pointer arrays are host memory; O, dO
+ * and dO_parts 16-byte aligned. */
+sda_status sda_merge_states_bwd(int n_states, const void* const* O_parts, const float* const* LSE_parts,
+                                const void* dO, const float* dLSE, int B, int N, int heads, int head_dim,
+                                int dtype, void* const* dO_parts, float* const* dLSE_parts, void* stream);
 
 /* Synchronises `stream`, then returns SDA_ERR_DEVICE_TIMEOUT if any kernel of
  * this library on the current device ran out of a bounded wait since the last

@@ -184,6 +184,40 @@ def test_merge_matches_oracle(sda, dtype, d, n_states):
     assert_close(host(Od[0]), Or, dtype, "merged O in place")
 
 
+@pytest.mark.parametrize("dtype,d,n_states", [("bf16", 128, 4), ("bf16", 64, 2), ("f32", 64, 3), ("bf16", 128, 16),
+                                              ("f32", 128, 1)])
+def test_merge_bwd_matches_oracle(sda, dtype, d, n_states):
+    rng = np.random.default_rng(n_states * 11 + d)
+    B, N, Hh = 2, 333, 3
+    Os = [rng.uniform(-3.0, 3.0, (B, N, Hh, d)) for _ in range(n_states)]
+    Ls = [rng.standard_normal((B, Hh, N)) * 3 for _ in range(n_states)]
+    for s in range(n_states):  # empty parts in live rows, and rows where every part is empty
+        Ls[s][rng.random((B, Hh, N)) < 0.2] = -np.inf
+    for L in Ls:
+        L[:, 0, :5] = -np.inf
+    dO = rng.standard_normal((B, N, Hh, d))
+    dL = rng.standard_normal((B, Hh, N)).astype(np.float32)
+    if dtype == "bf16":
+        Os = [inputs.round_to_bf16(o) for o in Os]
+        dO = inputs.round_to_bf16(dO)
+    Ls = [x.astype(np.float32) for x in Ls]
+    Od = [dev(o.astype(np.float32), dtype) for o in Os]
+    Ld = [torch.from_numpy(x).cuda() for x in Ls]
+    dOd = dev(dO.astype(np.float32), dtype)
+    tr = lambda x: np.transpose(x, (0, 2, 1))
+    for with_dl in (True, False):
+        gO = [torch.full_like(Od[0], float("nan")) for _ in range(n_states)]
+        gL = [torch.full_like(Ld[0], float("nan")) for _ in range(n_states)]
+        sda.sda_merge_states_bwd(Od, Ld, dOd, torch.from_numpy(dL).cuda() if with_dl else None, B, N, Hh, d, dtype,
+                                 gO, gL)
+        torch.cuda.synchronize()
+        rO, rL = orc.merge_states_bwd(Os, [tr(x) for x in Ls], dO, tr(dL) if with_dl else None)
+        for s in range(n_states):
+            assert_close(host(gO[s]), rO[s], dtype, f"dO_{s}")
+            assert_close(host(gL[s]), tr(rL[s]), dtype, f"dLSE_{s}")
+    assert sda.sda_get_device_status() == sda.SDA_OK
+
+
 def test_predict_is_deterministic_and_tie_exact(sda):
     # integer inputs with identical key blocks: every score ties, the lowest k indices win
     wl = inputs.Workload("ties", 1, 1, 4, 16, 16, 64, 2, 8, 8, 16, 0.25, "bf16", 0.0, 1)
