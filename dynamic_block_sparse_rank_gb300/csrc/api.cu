@@ -229,6 +229,32 @@ sda_status sda_attn_bwd(const sda_problem* p, const void* Q, const void* K, cons
   return sda_attn_bwd_dkdv(p, Q, K, V, LSE, dO, block_idx, dK, dV, grad_dtype, ws, ws_bytes, stream);
 }
 
+sda_status sda_attn_bwd_partition(const sda_problem* p, const void* Q, const void* K, const void* V, const void* O,
+                                  const float* LSE, const void* dO, const float* dLSE, const int32_t* block_idx,
+                                  int kb_begin, int kb_end, const uint8_t* qb_active, void* dQ, void* dK, void* dV,
+                                  int grad_dtype, void* ws, size_t ws_bytes, void* stream) {
+  Prob q;
+  const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV, LSE, block_idx};
+  sda_status s = bwd_common(p, &q, ptrs, 10, 8, grad_dtype, ws, ws_bytes);
+  if (s != SDA_OK) return s;
+  if (kb_begin < 0 || kb_end < kb_begin || kb_end > q.g.nb) return SDA_ERR_INVALID_ARG;
+  const Part part{kb_begin, kb_end, qb_active, dLSE};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (q.dtype == SDA_BF16) {
+    if ((e = bwd_prepare_tc(q, Q, K, V, O, LSE, dO, block_idx, ws, st, &part)) != cudaSuccess) return from_cuda(e);
+    if ((e = bwd_dq_tc(q, V, dO, block_idx, dQ, grad_dtype, ws, st, &part)) != cudaSuccess) return from_cuda(e);
+    return from_cuda(bwd_dkdv_tc(q, V, dO, dK, dV, grad_dtype, ws, st));
+  }
+  const float *Qf = static_cast<const float*>(Q), *Kf = static_cast<const float*>(K),
+              *Vf = static_cast<const float*>(V), *dOf = static_cast<const float*>(dO);
+  if ((e = bwd_prepare_f32(q, static_cast<const float*>(O), dOf, ws, st, dLSE)) != cudaSuccess) return from_cuda(e);
+  if ((e = bwd_dq_f32(q, Qf, Kf, Vf, LSE, dOf, block_idx, static_cast<float*>(dQ), ws, st, &part)) != cudaSuccess)
+    return from_cuda(e);
+  return from_cuda(bwd_dkdv_f32(q, Qf, Kf, Vf, LSE, dOf, block_idx, static_cast<float*>(dK), static_cast<float*>(dV),
+                                ws, st, &part));
+}
+
 sda_status sda_merge_states(int n_states, const void* const* O_parts, const float* const* LSE_parts, int B, int N,
                             int heads, int head_dim, int dtype, void* O_out, float* LSE_out, void* stream) {
   if (n_states < 1 || n_states > kMaxStates || !O_parts || !LSE_parts || !O_out || !LSE_out)

@@ -46,6 +46,11 @@ struct BwdArgs {
   const int32_t* offsets; // [B, Hh, nb + 1]
   const int32_t* lists;   // [B, Hh, nb * k]
   const int32_t* order;   // [B, Hh, nb]
+  // A partition state's backward: each query block's kept blocks inside the key range
+  // (none for an inactive block), compacted, and dL/dLSE in tile order; null otherwise.
+  const int32_t* qlist;   // [B, Hh, nb, k]
+  const int32_t* qcount;  // [B, Hh, nb]
+  const float* G;         // [B, Hh, nb, 128]
   unsigned* status;
   // dK/dV half tiles: query rows [0,64) and [64,128) of a tile are the two halves of
   // its slowest even extent (0: tt, 1: hh, 2: ww); the second half starts hoff further.
@@ -60,13 +65,16 @@ __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
 }
 
 // ------------------------------------------------------------------ preprocess
+// D~_i = dO_i . O_i - dLSE_i (dLSE of a partition state's backward, else 0) and
+// LSE_i log2(e) in tile order; G receives dLSE_i in tile order when given.
 template <int D>
 __global__ void __launch_bounds__(128) pre_kernel(Geom g, int Hh, long long N, int b, const __nv_bfloat16* __restrict__ O,
                                                   const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LSE,
-                                                  float* __restrict__ Dv, float* __restrict__ L2v) {
+                                                  const float* __restrict__ dLSE, float* __restrict__ Dv,
+                                                  float* __restrict__ L2v, float* __restrict__ G) {
   const int I = blockIdx.x, h = blockIdx.y, r = threadIdx.x;
   const int n = block_row_token(g, I, r);
-  float dsum = 0.f, l2 = INFINITY;
+  float dsum = 0.f, l2 = INFINITY, gl = 0.f;
   if (n >= 0) {
     const uint4* o = reinterpret_cast<const uint4*>(O + (((long long)b * N + n) * Hh + h) * D);
     const uint4* go = reinterpret_cast<const uint4*>(dO + (((long long)b * N + n) * Hh + h) * D);
@@ -82,10 +90,12 @@ __global__ void __launch_bounds__(128) pre_kernel(Geom g, int Hh, long long N, i
     }
     const float lse = LSE[((long long)b * Hh + h) * N + n];
     l2 = lse == -INFINITY ? INFINITY : lse * kLog2e;
+    if (dLSE) gl = dLSE[((long long)b * Hh + h) * N + n];
   }
   const long long o = (((long long)b * Hh + h) * g.nb + I) * 128 + r;
-  Dv[o] = dsum;
+  Dv[o] = dsum - gl;
   L2v[o] = l2;
+  if (G) G[o] = gl;
 }
 
 // bf16 -> fp16, 8 elements per thread-iteration.
@@ -101,7 +111,10 @@ __global__ void half_kernel(const uint4* __restrict__ src, uint4* __restrict__ d
 }
 
 // ------------------------------------------------------------------ block-map transpose
+// bitmap[bh, I, J] = query block I kept key block J (for a partition state: J in
+// [kb_begin, kb_end) and I active).
 __global__ void csr_bitmap_kernel(const int32_t* __restrict__ idx, long long entries, int nb, int k, int words,
+                                  int kb_begin, int kb_end, const uint8_t* __restrict__ qb_active,
                                   unsigned* __restrict__ bitmap, unsigned* __restrict__ status) {
   for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < entries;
        e += (long long)gridDim.x * blockDim.x) {
@@ -111,7 +124,25 @@ __global__ void csr_bitmap_kernel(const int32_t* __restrict__ idx, long long ent
       atomicOr(status, kStatusBadIndex);
       continue;
     }
+    if (J < kb_begin || J >= kb_end || (qb_active && !qb_active[row % nb])) continue;
     atomicOr(bitmap + row * words + (J >> 5), 1u << (J & 31));
+  }
+}
+
+// A partition state's dQ rows: each query block's kept blocks inside [kb_begin,
+// kb_end), in list order, and their count (0 for an inactive block).
+__global__ void rowlist_kernel(const int32_t* __restrict__ idx, long long rows, int nb, int k, int kb_begin,
+                               int kb_end, const uint8_t* __restrict__ qb_active, int32_t* __restrict__ qlist,
+                               int32_t* __restrict__ qcount) {
+  for (long long row = blockIdx.x * (long long)blockDim.x + threadIdx.x; row < rows;
+       row += (long long)gridDim.x * blockDim.x) {
+    int c = 0;
+    if (!qb_active || qb_active[row % nb])
+      for (int s = 0; s < k; ++s) {
+        const int J = idx[row * k + s];
+        if (J >= kb_begin && J < kb_end) qlist[row * k + c++] = J;
+      }
+    qcount[row] = c;
   }
 }
 
@@ -309,8 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int32_t* sel = a.idx + (((long long)a.b * a.Hh + h) * a.g.nb + I) * a.k;
-  const int n = a.k;
+  const long long qrow = ((long long)a.b * a.Hh + h) * a.g.nb + I;
+  const int32_t* sel = (a.qlist ? a.qlist : a.idx) + qrow * a.k;
+  const int n = a.qcount ? a.qcount[qrow] : a.k;  // 0 only for a partition state's empty rows
   if (tid == 0) {
     mbar_init(qfull, 1);
     for (int s = 0; s < KST; ++s) {
@@ -338,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   block_origin(a.g, I, t0, h0, w0);
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && n > 0) {  // with no block nothing is loaded: the epilogue reuses sQ at once
       mbar_expect_tx(qfull, 2 * C::TILE);
 #pragma unroll
       for (int c = 0; c < C::CH; ++c) {
@@ -425,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_ts_by(leader, tPK, tdP + packed_col(kk), bK0 + (uint64_t)(kk * (2048 >> 4)), idQ, (j > 0 || kk > 0));
       }
     };
-    bool ok = warp_wait(qfull, 0, a.status, abort_flag) && warp_wait(kvfull, 0, a.status, abort_flag);
+    bool ok = n > 0 && warp_wait(qfull, 0, a.status, abort_flag) && warp_wait(kvfull, 0, a.status, abort_flag);
     if (ok) {
       tc_fence_after();
       issue_sdp(0, 0);
@@ -444,8 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_by(leader, kempty + j % KST);  // K_j: last read by this block's dQ MMAs
       if (more) issue_sdp(j + 1, 1);
     }
-    mma_commit_by(leader, drain);
-    wait_plain(drain, 0);
+    if (n > 0) {  // no MMA was issued for an empty row: nothing to drain
+      mma_commit_by(leader, drain);
+      wait_plain(drain, 0);
+    }
     __syncwarp();
   } else if (warp >= 4) {
     const int grp = (warp - 4) >> 2;                 // key columns [64 grp, 64 grp + 64)
@@ -489,10 +523,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(dsfull + grp);
     }
     dpart[grp * 128 + row] = dsum0 + dsum1;
-    mbar_wait(drain, 0, a.status, abort_flag);
+    if (n > 0) mbar_wait(drain, 0, a.status, abort_flag);
     tc_fence_after();
     named_bar(1, 256);
-    const float Dx = dpart[row] + dpart[128 + row];
+    // exact D; a partition state's LSE gradient enters it as D - dLSE, as in D~
+    const float Dx = dpart[row] + dpart[128 + row] - (a.G ? a.G[tile_row] : 0.f);
     if (grp == 0) a.Dv[tile_row] = Dx;  // exact D for the dK/dV kernel
     // dQ = scale * (dQ~ + (D~ - D) P K) -> staging (Q and dO tiles are free once all MMAs are done)
     stage_row<F32OUT>(sQ, tdQ + lane_base, tPK + lane_base, Dt - Dx, row, grp * (D / 2), D / 2, a.scale, n == 0);
@@ -756,6 +791,9 @@ struct WsLayout {
   int32_t* lists;
   int32_t* order;
   unsigned* bitmap;
+  int32_t* qlist;   // partition states only
+  int32_t* qcount;
+  float* G;
   char* Q16;
   char* K16;
   char* V16;
@@ -781,6 +819,9 @@ WsLayout ws_layout(const Prob& p, void* base) {
   w.lists = reinterpret_cast<int32_t*>(take(bh * nb * p.k * 4));
   w.order = reinterpret_cast<int32_t*>(take(bh * nb * 4));
   w.bitmap = reinterpret_cast<unsigned*>(take(bh * nb * words * 4));
+  w.qlist = reinterpret_cast<int32_t*>(take(bh * nb * p.k * 4));
+  w.qcount = reinterpret_cast<int32_t*>(take(bh * nb * 4));
+  w.G = reinterpret_cast<float*>(take(bh * nb * 128 * 4));
   w.Q16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
   w.K16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
   w.V16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
@@ -789,7 +830,8 @@ WsLayout ws_layout(const Prob& p, void* base) {
   return w;
 }
 
-BwdArgs make_args(const Prob& p, const WsLayout& w, const int32_t* idx, unsigned* status, int b) {
+BwdArgs make_args(const Prob& p, const WsLayout& w, const int32_t* idx, unsigned* status, int b,
+                  const Part* part = nullptr) {
   BwdArgs a;
   a.g = p.g;
   a.Hh = p.Hh;
@@ -805,6 +847,9 @@ BwdArgs make_args(const Prob& p, const WsLayout& w, const int32_t* idx, unsigned
   a.offsets = w.offsets;
   a.lists = w.lists;
   a.order = w.order;
+  a.qlist = part ? w.qlist : nullptr;
+  a.qcount = part ? w.qcount : nullptr;
+  a.G = part && part->dLSE ? w.G : nullptr;
   a.status = status;
   const Geom& g = p.g;
   a.hdim = g.bt % 2 == 0 ? 0 : (g.bh % 2 == 0 ? 1 : 2);
@@ -821,7 +866,7 @@ bool token_map(CUtensorMap* m, const Prob& p, const void* base, int b, TokType t
 
 template <int D, bool F32OUT>
 cudaError_t launch_dq(const Prob& p, const void* V, const void* dO, const int32_t* idx, void* dQ, void* ws,
-                      cudaStream_t st) {
+                      cudaStream_t st, const Part* part) {
   using C = Cfg<D>;
   WsLayout w = ws_layout(p, ws);
   unsigned* status = status_ptr();
@@ -837,7 +882,7 @@ cudaError_t launch_dq(const Prob& p, const void* V, const void* dO, const int32_
         !token_map(&mdQ, p, dQ, b, gt))
       return cudaErrorInvalidValue;
     dq_kernel<D, F32OUT><<<dim3(p.g.nb, p.Hh), kThreads, smem, st>>>(mQ, mK, mV, mdO, mdQ,
-                                                                     make_args(p, w, idx, status, b));
+                                                                     make_args(p, w, idx, status, b, part));
     note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -883,7 +928,8 @@ cudaError_t launch_dkdv(const Prob& p, const void* V, const void* dO, void* dK, 
 size_t bwd_ws_tc(const Prob& p) { return ws_layout(p, nullptr).bytes; }
 
 cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O,
-                           const float* LSE, const void* dO, const int32_t* idx, void* ws, cudaStream_t st) {
+                           const float* LSE, const void* dO, const int32_t* idx, void* ws, cudaStream_t st,
+                           const Part* part) {
   const Geom& g = p.g;
   WsLayout w = ws_layout(p, ws);
   unsigned* status = status_ptr();
@@ -894,8 +940,15 @@ cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const vo
   const long long bhn = (long long)p.B * p.Hh * g.nb;
   if ((e = cudaMemsetAsync(w.bitmap, 0, (size_t)bhn * words * 4, st)) != cudaSuccess) return e;
   const long long entries = bhn * p.k;
-  csr_bitmap_kernel<<<(int)std::min<long long>((entries + 255) / 256, 1 << 20), 256, 0, st>>>(idx, entries, g.nb, p.k,
-                                                                                              words, w.bitmap, status);
+  const int kb0 = part ? part->kb_begin : 0, kb1 = part ? part->kb_end : g.nb;
+  const uint8_t* act = part ? part->qb_active : nullptr;
+  csr_bitmap_kernel<<<(int)std::min<long long>((entries + 255) / 256, 1 << 20), 256, 0, st>>>(
+      idx, entries, g.nb, p.k, words, kb0, kb1, act, w.bitmap, status);
+  if (part) {
+    rowlist_kernel<<<(int)std::min<long long>((bhn + 255) / 256, 152LL * 16), 256, 0, st>>>(idx, bhn, g.nb, p.k, kb0,
+                                                                                           kb1, act, w.qlist, w.qcount);
+    note_launches(1);
+  }
   csr_count_kernel<<<(int)((bhn * 32 + 255) / 256), 256, 0, st>>>(w.bitmap, g.nb, words, bhn, w.counts);
   csr_scan_kernel<<<p.B * p.Hh, 1024, g.nb * sizeof(int32_t), st>>>(w.counts, g.nb, w.offsets);
   csr_order_kernel<<<dim3((g.nb + 255) / 256, p.B * p.Hh), 256, g.nb * sizeof(int32_t), st>>>(w.counts, g.nb,
@@ -907,23 +960,30 @@ cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const vo
   half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(K), reinterpret_cast<uint4*>(w.K16), n8);
   half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(V), reinterpret_cast<uint4*>(w.V16), n8);
   half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(dO), reinterpret_cast<uint4*>(w.dO16), n8);
+  const float* dLSE = part ? part->dLSE : nullptr;
+  float* G = dLSE ? w.G : nullptr;
   for (int b = 0; b < p.B; ++b) {
     if (p.d == 64)
       pre_kernel<64><<<dim3(g.nb, p.Hh), 128, 0, st>>>(g, p.Hh, p.N, b, static_cast<const __nv_bfloat16*>(O),
-                                                       static_cast<const __nv_bfloat16*>(dO), LSE, w.Dv, w.L2v);
+                                                       static_cast<const __nv_bfloat16*>(dO), LSE, dLSE, w.Dv, w.L2v,
+                                                       G);
     else
       pre_kernel<128><<<dim3(g.nb, p.Hh), 128, 0, st>>>(g, p.Hh, p.N, b, static_cast<const __nv_bfloat16*>(O),
-                                                        static_cast<const __nv_bfloat16*>(dO), LSE, w.Dv, w.L2v);
+                                                        static_cast<const __nv_bfloat16*>(dO), LSE, dLSE, w.Dv, w.L2v,
+                                                        G);
   }
   note_launches(9 + p.B);  // 5 block-map kernels, 4 fp16 copies, one pre_kernel per batch entry
   return cudaGetLastError();
 }
 
 cudaError_t bwd_dq_tc(const Prob& p, const void* V, const void* dO, const int32_t* idx, void* dQ, int grad_dtype,
-                      void* ws, cudaStream_t st) {
+                      void* ws, cudaStream_t st, const Part* part) {
   const bool f32 = grad_dtype == SDA_F32;
-  if (p.d == 64) return f32 ? launch_dq<64, true>(p, V, dO, idx, dQ, ws, st) : launch_dq<64, false>(p, V, dO, idx, dQ, ws, st);
-  return f32 ? launch_dq<128, true>(p, V, dO, idx, dQ, ws, st) : launch_dq<128, false>(p, V, dO, idx, dQ, ws, st);
+  if (p.d == 64)
+    return f32 ? launch_dq<64, true>(p, V, dO, idx, dQ, ws, st, part)
+               : launch_dq<64, false>(p, V, dO, idx, dQ, ws, st, part);
+  return f32 ? launch_dq<128, true>(p, V, dO, idx, dQ, ws, st, part)
+             : launch_dq<128, false>(p, V, dO, idx, dQ, ws, st, part);
 }
 
 cudaError_t bwd_dkdv_tc(const Prob& p, const void* V, const void* dO, void* dK, void* dV, int grad_dtype, void* ws,

@@ -51,6 +51,16 @@ struct MergeBwdArgs {
 };
 cudaError_t launch_merge_bwd(const MergeBwdArgs& a, int dtype, cudaStream_t st);
 
+// The backward of one partition state (DiTango reuse, training): the state that
+// sda_attn_fwd computes with key range [kb_begin, kb_end) and the active query
+// blocks, given dL/dO of that state and dL/dLSE (dLSE, may be null).  A null Part
+// is the whole map with no LSE gradient.
+struct Part {
+  int kb_begin, kb_end;
+  const uint8_t* qb_active;
+  const float* dLSE;
+};
+
 // ---- simt.cu (fp32 problems)
 size_t predict_ws_f32(const Prob& p);
 cudaError_t predict_f32(const Prob& p, const float* Q, const float* K, const float* Wq, const float* Wk,
@@ -58,11 +68,14 @@ cudaError_t predict_f32(const Prob& p, const float* Q, const float* K, const flo
 cudaError_t fwd_f32(const Prob& p, const float* Q, const float* K, const float* V, const int32_t* idx,
                     int kb_begin, int kb_end, const uint8_t* qb_active, float* O, float* LSE, cudaStream_t st);
 size_t bwd_ws_f32(const Prob& p);
-cudaError_t bwd_prepare_f32(const Prob& p, const float* O, const float* dO, void* ws, cudaStream_t st);
+cudaError_t bwd_prepare_f32(const Prob& p, const float* O, const float* dO, void* ws, cudaStream_t st,
+                            const float* dLSE = nullptr);
 cudaError_t bwd_dq_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
-                       const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st);
+                       const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st,
+                       const Part* part = nullptr);
 cudaError_t bwd_dkdv_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
-                         const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st);
+                         const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st,
+                         const Part* part = nullptr);
 
 // ---- tensor maps (tmap.cu)
 // 5-D map over a [T, H, W, heads, d] tensor of one batch entry; box = 128
@@ -86,9 +99,10 @@ cudaError_t fwd_tc(const Prob& p, const void* Q, const void* K, const void* V, c
 // writes the exact D rows), dK/dV.
 size_t bwd_ws_tc(const Prob& p);
 cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O,
-                           const float* LSE, const void* dO, const int32_t* idx, void* ws, cudaStream_t st);
+                           const float* LSE, const void* dO, const int32_t* idx, void* ws, cudaStream_t st,
+                           const Part* part = nullptr);
 cudaError_t bwd_dq_tc(const Prob& p, const void* V, const void* dO, const int32_t* idx, void* dQ, int grad_dtype,
-                      void* ws, cudaStream_t st);
+                      void* ws, cudaStream_t st, const Part* part = nullptr);
 cudaError_t bwd_dkdv_tc(const Prob& p, const void* V, const void* dO, void* dK, void* dV, int grad_dtype, void* ws,
                         cudaStream_t st);
 

@@ -158,9 +158,11 @@ __global__ void fwd_f32_kernel(Geom g, int Hh, int d, int k, float scale, const 
   LSE[((long long)b * Hh + h) * N + n] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
-// D_i = dO_i . O_i for every token row, into Dbuf [B, Hh, N].
+// D_i = dO_i . O_i - dLSE_i for every token row, into Dbuf [B, Hh, N] (the LSE
+// gradient of a partition state enters dS = P (dP - D + dLSE) with D's sign).
 __global__ void bwd_pre_f32_kernel(long long rows, int Hh, long long N, int d, const float* __restrict__ O,
-                                   const float* __restrict__ dO, float* __restrict__ Dbuf) {
+                                   const float* __restrict__ dO, const float* __restrict__ dLSE,
+                                   float* __restrict__ Dbuf) {
   for (long long r = blockIdx.x * (long long)blockDim.x + threadIdx.x; r < rows; r += (long long)gridDim.x * blockDim.x) {
     // r enumerates (b, n, h) in memory order
     const int h = (int)(r % Hh);
@@ -168,7 +170,8 @@ __global__ void bwd_pre_f32_kernel(long long rows, int Hh, long long N, int d, c
     const long long b = bn / N, n = bn % N;
     float acc = 0.f;
     for (int c = 0; c < d; ++c) acc = fmaf(dO[r * d + c], O[r * d + c], acc);
-    Dbuf[(b * Hh + h) * N + n] = acc;
+    const long long t = (b * Hh + h) * N + n;
+    Dbuf[t] = dLSE ? acc - dLSE[t] : acc;
   }
 }
 
@@ -178,7 +181,8 @@ __global__ void bwd_dq_f32_kernel(Geom g, int Hh, int d, int k, float scale, con
                                   const float* __restrict__ K, const float* __restrict__ V,
                                   const float* __restrict__ LSE, const float* __restrict__ dO,
                                   const int32_t* __restrict__ idx, float* __restrict__ dQ,
-                                  const float* __restrict__ Dbuf, int b) {
+                                  const float* __restrict__ Dbuf, int b, int kb_begin, int kb_end,
+                                  const uint8_t* __restrict__ qb_active) {
   extern __shared__ float smem[];
   const int I = blockIdx.x, h = blockIdx.y;
   float* ks = smem;
@@ -186,7 +190,8 @@ __global__ void bwd_dq_f32_kernel(Geom g, int Hh, int d, int k, float scale, con
   int* kv_ok = reinterpret_cast<int*>(vs + kChunk * d);
   int* sel = kv_ok + kChunk;
   const long long N = (long long)g.T * g.H * g.W;
-  const int n_sel = filter_sel(idx + (((long long)b * Hh + h) * g.nb + I) * k, k, 0, g.nb, sel);
+  int n_sel = filter_sel(idx + (((long long)b * Hh + h) * g.nb + I) * k, k, kb_begin, kb_end, sel);
+  if (qb_active && !qb_active[I]) n_sel = 0;  // an inactive query block contributes nothing
   const int row = threadIdx.x;
   const int n = row < g.bs ? valid_token(g, I, row) : -1;
   float q[DM], go[DM], dq[DM];
@@ -246,7 +251,8 @@ __global__ void bwd_dkdv_f32_kernel(Geom g, int Hh, int d, int k, float scale, c
                                     const float* __restrict__ K, const float* __restrict__ V,
                                     const float* __restrict__ LSE, const float* __restrict__ dO,
                                     const int32_t* __restrict__ idx, const float* __restrict__ Dbuf,
-                                    float* __restrict__ dK, float* __restrict__ dV, int b) {
+                                    float* __restrict__ dK, float* __restrict__ dV, int b, int kb_begin, int kb_end,
+                                    const uint8_t* __restrict__ qb_active) {
   extern __shared__ float smem[];
   const int J = blockIdx.x, h = blockIdx.y;
   float* qs = smem;                   // kChunk * d
@@ -260,12 +266,15 @@ __global__ void bwd_dkdv_f32_kernel(Geom g, int Hh, int d, int k, float scale, c
   const int32_t* rows = idx + ((long long)b * Hh + h) * g.nb * k;
   if (threadIdx.x == 0) {
     int cnt = 0;
-    for (int I = 0; I < g.nb; ++I)
-      for (int s = 0; s < k; ++s)
-        if (rows[(long long)I * k + s] == J) {
-          users[cnt++] = I;
-          break;
-        }
+    if (J >= kb_begin && J < kb_end)  // outside the key range: no user, zero gradient
+      for (int I = 0; I < g.nb; ++I) {
+        if (qb_active && !qb_active[I]) continue;
+        for (int s = 0; s < k; ++s)
+          if (rows[(long long)I * k + s] == J) {
+            users[cnt++] = I;
+            break;
+          }
+      }
     n_users = cnt;
   }
   __syncthreads();
@@ -385,17 +394,19 @@ cudaError_t fwd_f32(const Prob& p, const float* Q, const float* K, const float* 
 
 size_t bwd_ws_f32(const Prob& p) { return align_up((size_t)p.B * p.Hh * p.N * sizeof(float), 256); }
 
-cudaError_t bwd_prepare_f32(const Prob& p, const float* O, const float* dO, void* ws, cudaStream_t st) {
+cudaError_t bwd_prepare_f32(const Prob& p, const float* O, const float* dO, void* ws, cudaStream_t st,
+                            const float* dLSE) {
   const long long rows = (long long)p.B * p.N * p.Hh;
   const int blocks = (int)std::min<long long>((rows + 255) / 256, 152LL * 32);
-  bwd_pre_f32_kernel<<<blocks, 256, 0, st>>>(rows, p.Hh, p.N, p.d, O, dO, static_cast<float*>(ws));
+  bwd_pre_f32_kernel<<<blocks, 256, 0, st>>>(rows, p.Hh, p.N, p.d, O, dO, dLSE, static_cast<float*>(ws));
   note_launches(1);
   return cudaGetLastError();
 }
 
 template <int DM>
 static cudaError_t dq_f32_t(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
-                            const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st) {
+                            const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st,
+                            const Part* part) {
   size_t smem = (size_t)2 * kChunk * p.d * sizeof(float) + (kChunk + p.k) * sizeof(int);
   cudaError_t e;
   if (smem > 48 * 1024 &&
@@ -404,14 +415,16 @@ static cudaError_t dq_f32_t(const Prob& p, const float* Q, const float* K, const
     return e;
   for (int b = 0; b < p.B; ++b)
     bwd_dq_f32_kernel<DM><<<dim3(p.g.nb, p.Hh), threads_for(p.g.bs), smem, st>>>(
-        p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, LSE, dO, idx, dQ, static_cast<const float*>(ws), b);
+        p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, LSE, dO, idx, dQ, static_cast<const float*>(ws), b,
+        part ? part->kb_begin : 0, part ? part->kb_end : p.g.nb, part ? part->qb_active : nullptr);
   note_launches(p.B);
   return cudaGetLastError();
 }
 
 template <int DM>
 static cudaError_t dkdv_f32_t(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
-                              const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st) {
+                              const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st,
+                              const Part* part) {
   size_t smem = (size_t)2 * kChunk * p.d * sizeof(float) + 3 * kChunk * sizeof(float) + p.g.nb * sizeof(int);
   cudaError_t e;
   if (smem > 48 * 1024 &&
@@ -420,21 +433,23 @@ static cudaError_t dkdv_f32_t(const Prob& p, const float* Q, const float* K, con
     return e;
   for (int b = 0; b < p.B; ++b)
     bwd_dkdv_f32_kernel<DM><<<dim3(p.g.nb, p.Hh), threads_for(p.g.bs), smem, st>>>(
-        p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, LSE, dO, idx, static_cast<const float*>(ws), dK, dV, b);
+        p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, LSE, dO, idx, static_cast<const float*>(ws), dK, dV, b,
+        part ? part->kb_begin : 0, part ? part->kb_end : p.g.nb, part ? part->qb_active : nullptr);
   note_launches(p.B);
   return cudaGetLastError();
 }
 
 cudaError_t bwd_dq_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
-                       const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st) {
-  if (p.d <= 64) return dq_f32_t<64>(p, Q, K, V, LSE, dO, idx, dQ, ws, st);
-  return dq_f32_t<128>(p, Q, K, V, LSE, dO, idx, dQ, ws, st);
+                       const float* dO, const int32_t* idx, float* dQ, void* ws, cudaStream_t st, const Part* part) {
+  if (p.d <= 64) return dq_f32_t<64>(p, Q, K, V, LSE, dO, idx, dQ, ws, st, part);
+  return dq_f32_t<128>(p, Q, K, V, LSE, dO, idx, dQ, ws, st, part);
 }
 
 cudaError_t bwd_dkdv_f32(const Prob& p, const float* Q, const float* K, const float* V, const float* LSE,
-                         const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st) {
-  if (p.d <= 64) return dkdv_f32_t<64>(p, Q, K, V, LSE, dO, idx, dK, dV, ws, st);
-  return dkdv_f32_t<128>(p, Q, K, V, LSE, dO, idx, dK, dV, ws, st);
+                         const float* dO, const int32_t* idx, float* dK, float* dV, void* ws, cudaStream_t st,
+                         const Part* part) {
+  if (p.d <= 64) return dkdv_f32_t<64>(p, Q, K, V, LSE, dO, idx, dK, dV, ws, st, part);
+  return dkdv_f32_t<128>(p, Q, K, V, LSE, dO, idx, dK, dV, ws, st, part);
 }
 
 }  // namespace sda

@@ -18,7 +18,7 @@ SDA_F32, SDA_BF16 = 0, 1
 SDA_OP_PREDICT, SDA_OP_BWD = 0, 1
 
 EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_attn_fwd", "sda_attn_bwd",
-           "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_merge_states", "sda_merge_states_bwd",
+           "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_attn_bwd_partition", "sda_merge_states", "sda_merge_states_bwd",
            "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_selftest_wait_timeout", "sda_status_string")
 
 
@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.sda_attn_fwd.argtypes = [pr, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
         L.sda_attn_bwd.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
         L.sda_attn_bwd_prepare.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sda_attn_bwd_partition.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, vp, sz,
+                                             vp]
         L.sda_attn_bwd_dq.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
         L.sda_attn_bwd_dkdv.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
         L.sda_predict_blocks_noalloc.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp]
@@ -151,6 +153,17 @@ def sda_attn_bwd(p, Q, K, V, O, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, 
     _check(lib().sda_attn_bwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO),
                               _ptr(block_idx), _ptr(dQ), _ptr(dK), _ptr(dV), int(gd), _wsptr(ws), _nbytes(ws),
                               _stream(stream)), "sda_attn_bwd")
+
+
+def sda_attn_bwd_partition(p, Q, K, V, O, LSE, dO, dLSE, block_idx, dQ, dK, dV, grad_dtype, ws, kb_begin=0,
+                           kb_end=None, qb_active=None, stream=None):
+    gd = {"f32": SDA_F32, "bf16": SDA_BF16}.get(grad_dtype, grad_dtype)
+    if kb_end is None:
+        kb_end = sda_num_blocks(p)[0]
+    _check(lib().sda_attn_bwd_partition(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO),
+                                        _ptr(dLSE), _ptr(block_idx), int(kb_begin), int(kb_end), _ptr(qb_active),
+                                        _ptr(dQ), _ptr(dK), _ptr(dV), int(gd), _wsptr(ws), _nbytes(ws),
+                                        _stream(stream)), "sda_attn_bwd_partition")
 
 
 def sda_attn_bwd_prepare(p, Q, K, V, O, LSE, dO, block_idx, ws, stream=None):

@@ -145,6 +145,26 @@ sda_status sda_attn_bwd_dkdv(const sda_problem* p, const void* Q, const void* K,
                              const void* dO, const int32_t* block_idx, void* dK, void* dV, int grad_dtype, void* ws,
                              size_t ws_bytes, void* stream);
 
+/* Backward of one partition state, for training through DiTango's state reuse:
+ * the gradient with respect to Q, K, V of the state (O_p, LSE_p) that
+ * sda_attn_fwd computes with the same block_idx, kb_begin, kb_end and
+ * qb_active, given
+ *   dO    [B, N, heads, d] (dtype): dL/dO_p (from sda_merge_states_bwd)
+ *   dLSE  [B, heads, N] fp32: dL/dLSE_p, or NULL for zero
+ *   O, LSE the state itself (rows of inactive query blocks are not read for
+ *          anything that reaches an output)
+ * Since d LSE_i / d S_ij = P_ij, dS_ij = P_ij (dP_ij - D_i + dLSE_i) over the
+ * kept keys in [kb_begin, kb_end).  dQ is written for every row (zero for
+ * inactive query blocks and rows with no key in the range), dK and dV for every
+ * key row (zero outside the range); the gradient of a step sums these over its
+ * fresh partitions.  Workspace, grad_dtype, alignment and errors as
+ * sda_attn_bwd; 0 <= kb_begin <= kb_end <= n_b.  With the whole range, no
+ * qb_active and no dLSE it computes what sda_attn_bwd computes. */
+sda_status sda_attn_bwd_partition(const sda_problem* p, const void* Q, const void* K, const void* V, const void* O,
+                                  const float* LSE, const void* dO, const float* dLSE, const int32_t* block_idx,
+                                  int kb_begin, int kb_end, const uint8_t* qb_active, void* dQ, void* dK, void* dV,
+                                  int grad_dtype, void* ws, size_t ws_bytes, void* stream);
+
 /* Step 3: LSE merge of n_states partial states (DiTango state reuse).
  *   O_parts[s]   device pointer, [B, N, heads, d] (dtype)
  *   LSE_parts[s] device pointer, [B, heads, N] fp32

@@ -10,7 +10,8 @@ import pytest
 
 import oracle as orc
 from dynamic_block_sparse_rank_gb300 import inputs
-from tests.parity_util import TOL, assert_close, assert_close_stored, check_scores, check_selection, dev, errors, host
+from tests.parity_util import (TOL, assert_close, assert_close_stored, assert_close_through_stored_states,
+                                 check_scores, check_selection, dev, errors, host)
 
 pytestmark = pytest.mark.gpu
 
@@ -215,6 +216,110 @@ def test_merge_bwd_matches_oracle(sda, dtype, d, n_states):
         for s in range(n_states):
             assert_close(host(gO[s]), rO[s], dtype, f"dO_{s}")
             assert_close(host(gL[s]), tr(rL[s]), dtype, f"dLSE_{s}")
+    assert sda.sda_get_device_status() == sda.SDA_OK
+
+
+def _ws_bwd(sda, p):
+    return torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("wl", [RAGGED_D64, TILE_4X4X8, inputs.WORKLOADS["tiny_f32_256"]], ids=lambda w: w.name)
+def test_partition_backward_matches_oracle(sda, wl):
+    """One partition state: a key range, some inactive query blocks and an LSE gradient."""
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk"))
+    geom = _geom(wl)
+    idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    P = min(3, geom.nT)
+    b0, b1 = orc.frame_partitions(geom, P)[P // 2]
+    rng = np.random.default_rng(5)
+    act = rng.random(geom.n_blocks) < 0.7
+    dLSE = rng.standard_normal((wl.B, wl.heads, wl.N)).astype(np.float32)
+    odt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    init = (torch.zeros((wl.B, wl.N, wl.heads, wl.d), dtype=odt, device="cuda"),
+            torch.zeros((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda"))
+    O, LSE = _run_fwd(sda, wl, x, idx, kb=(b0, b1), qb_active=act, init=init)
+    p = sda.problem_from_workload(wl)
+    dQ, dK, dV = (torch.full(O.shape, float("nan"), dtype=torch.float32, device="cuda") for _ in range(3))
+    sda.sda_attn_bwd_partition(p, dev(x["Q"], wl.dtype), dev(x["K"], wl.dtype), dev(x["V"], wl.dtype), O, LSE,
+                               dev(x["dO"], wl.dtype), torch.from_numpy(dLSE).cuda(), torch.from_numpy(idx).cuda(),
+                               dQ, dK, dV, "f32", _ws_bwd(sda, p), kb_begin=b0, kb_end=b1,
+                               qb_active=torch.from_numpy(act.astype(np.uint8)).cuda())
+    torch.cuda.synchronize()
+    refs = orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], idx, geom, kb_begin=b0, kb_end=b1, qb_active=act,
+                        dLSE=dLSE)
+    for name, got, ref in zip(("dQ", "dK", "dV"), (dQ, dK, dV), refs):
+        assert_close(host(got), ref, wl.dtype, name)
+    # nothing outside the range or from inactive blocks
+    ids = np.array([I for I in range(geom.n_blocks) for _ in geom.tokens(I)])
+    tok = np.concatenate([geom.tokens(I) for I in range(geom.n_blocks)])
+    outside = tok[(ids < b0) | (ids >= b1)]
+    assert np.all(host(dK)[:, outside] == 0) and np.all(host(dV)[:, outside] == 0)
+    assert np.all(host(dQ)[:, tok[~act[ids]]] == 0)
+    assert sda.sda_get_device_status() == sda.SDA_OK
+
+
+def test_partition_backward_of_the_whole_map_is_the_backward(sda):
+    wl = RAGGED_D128
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk"))
+    idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], _geom(wl), wl.keep, wl.dtype)
+    O, LSE = _run_fwd(sda, wl, x, idx)
+    p = sda.problem_from_workload(wl)
+    t = {n: dev(x[n], wl.dtype) for n in ("Q", "K", "V", "dO")}
+    ti = torch.from_numpy(idx).cuda()
+    a = [torch.empty(O.shape, dtype=torch.float32, device="cuda") for _ in range(3)]
+    b = [torch.empty(O.shape, dtype=torch.float32, device="cuda") for _ in range(3)]
+    sda.sda_attn_bwd(p, t["Q"], t["K"], t["V"], O, LSE, t["dO"], ti, *a, "f32", _ws_bwd(sda, p))
+    sda.sda_attn_bwd_partition(p, t["Q"], t["K"], t["V"], O, LSE, t["dO"], None, ti, *b, "f32", _ws_bwd(sda, p))
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("wl,P,n_reuse", [(RAGGED_D128, 2, 1), (TILE_4X4X8, 3, 1)], ids=lambda v: str(v))
+def test_reuse_training_gradient_matches_oracle(sda, wl, P, n_reuse):
+    """DiTango reuse, trained through: the merge backward and the partition backwards of the fresh states (GPU)
+    against the oracle's gradient of the reuse merge; the reused states are the previous step's."""
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk", "Qp", "Kp", "Vp"))
+    geom = _geom(wl)
+    idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    idxp, _ = orc.predict_blocks(x["Qp"], x["Kp"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    # the previous step's states, stored in the problem's dtype as a cache would hold them
+    prev = [(inputs.round_to_bf16(O), L.astype(np.float32).astype(np.float64))
+            for O, L in orc.partition_states(x["Qp"], x["Kp"], x["Vp"], idxp, geom, P)]
+    rng = np.random.default_rng(9)
+    dLSE = rng.standard_normal((wl.B, wl.heads, wl.N)).astype(np.float32)
+    reuse = orc.reuse_mask(geom, P, n_reuse)
+    bounds = orc.frame_partitions(geom, P)
+    p = sda.problem_from_workload(wl)
+    tid = torch.from_numpy(idx).cuda()
+    t = {n: dev(x[n], wl.dtype) for n in ("Q", "K", "V", "dO")}
+    tok_rows = [torch.from_numpy(np.asarray(geom.tokens(I))).cuda() for I in range(geom.n_blocks)]
+    fresh, used = [], []
+    for pp, (b0, b1) in enumerate(bounds):
+        O, LSE = _run_fwd(sda, wl, x, idx, kb=(b0, b1))
+        fresh.append((O, LSE))
+        Ou, Lu = O.clone(), LSE.clone()
+        Opr, Lpr = dev(prev[pp][0].astype(np.float32), wl.dtype), torch.from_numpy(prev[pp][1].astype(np.float32)).cuda()
+        for I in np.nonzero(reuse[pp])[0]:
+            Ou[:, tok_rows[I]] = Opr[:, tok_rows[I]]
+            Lu[:, :, tok_rows[I]] = Lpr[:, :, tok_rows[I]]
+        used.append((Ou, Lu))
+    gO = [torch.empty_like(used[0][0]) for _ in range(P)]
+    gL = [torch.empty_like(used[0][1]) for _ in range(P)]
+    sda.sda_merge_states_bwd([u[0] for u in used], [u[1] for u in used], t["dO"], torch.from_numpy(dLSE).cuda(),
+                             wl.B, wl.N, wl.heads, wl.d, wl.dtype, gO, gL)
+    total = [torch.zeros(t["Q"].shape, dtype=torch.float32, device="cuda") for _ in range(3)]
+    for pp, (b0, b1) in enumerate(bounds):
+        part = [torch.empty_like(total[0]) for _ in range(3)]
+        act = torch.from_numpy((~reuse[pp]).astype(np.uint8)).cuda()
+        sda.sda_attn_bwd_partition(p, t["Q"], t["K"], t["V"], fresh[pp][0], fresh[pp][1], gO[pp], gL[pp], tid,
+                                   *part, "f32", _ws_bwd(sda, p), kb_begin=b0, kb_end=b1, qb_active=act)
+        for acc, v in zip(total, part):
+            acc += v
+    torch.cuda.synchronize()
+    refs = orc.reuse_bwd(x["Q"], x["K"], x["V"], x["dO"], idx, geom, P, n_reuse, prev, dLSE=dLSE)
+    for name, got, ref in zip(("dQ", "dK", "dV"), total, refs):
+        assert_close_through_stored_states(host(got), ref, wl.dtype, name)
     assert sda.sda_get_device_status() == sda.SDA_OK
 
 
