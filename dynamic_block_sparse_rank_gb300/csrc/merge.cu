@@ -109,24 +109,29 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(MergeArgs a, int lpr) {
 // Gradient of the merge for one row per group of lpr consecutive lanes: the row's
 // weights as in merge_kernel; per 16-byte vector, O = sum_s w_s O_s, the partial
 // dot products dO . (O_s - O) and the stores of w_s dO; the dot products are summed
-// over the row's lanes by shuffles within the lane group.  Parts with w_s = 0 (an
+// over the row's lanes by shuffles within the lane group.  Every state's vector is
+// loaded whatever its weight, so the loads of a row go out together with its LSE
+// loads instead of after them.  Parts with w_s = 0 (an
 // empty part, or an empty row) are skipped and get zero gradients.  The weights use
 // the accurate expf / logf: dLSE_s scales with |dO| |O_s - O| d, so their error shows.
 template <typename T, int NS>
-__global__ void __launch_bounds__(kThreads) merge_bwd_kernel(MergeBwdArgs a, int lpr) {
+__global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_kernel(MergeBwdArgs a, int lpr) {
   constexpr int VN = Vec<T>::n;
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int n0 = blockIdx.x * kRowsPerCta;
+  const long long rows = (long long)a.B * a.N * a.Hh;
+  const long long r0 = (long long)blockIdx.x * kRowsPerCta;  // rows in memory order: (b, n, h)
   const int rows_per_pass = kThreads / lpr;
   const int sub = threadIdx.x / lpr, lane = threadIdx.x % lpr;
   const int wl = threadIdx.x & 31;
   const unsigned grp = lpr == 32 ? 0xffffffffu : (((1u << lpr) - 1u) << (wl & ~(lpr - 1)));
   const int nvec = a.d / VN;
   for (int rr = sub; rr < kRowsPerCta; rr += rows_per_pass) {
-    const int n = n0 + rr;
-    if (n >= a.N) break;  // the whole lane group leaves together
+    const long long r = r0 + rr;
+    if (r >= rows) break;  // the whole lane group leaves together
+    const int h = (int)(r % a.Hh);
+    const long long bn = r / a.Hh;
+    const long long n = bn % a.N, b = bn / a.N;
     const size_t lrow = ((size_t)b * a.Hh + h) * a.N + n;
-    const size_t orow = (((size_t)b * a.N + n) * a.Hh + h) * (size_t)a.d;
+    const size_t orow = (size_t)r * a.d;
     float ls[NS];
     float m = -INFINITY;
 #pragma unroll
@@ -150,11 +155,10 @@ __global__ void __launch_bounds__(kThreads) merge_bwd_kernel(MergeBwdArgs a, int
 #pragma unroll
     for (int s = 0; s < NS; ++s) dot[s] = 0.f;
     for (int v = lane; v < nvec; v += lpr) {
+      // loaded whatever the weight, so the loads need not wait for the LSE rows
       uint4 raw[NS];
 #pragma unroll
-      for (int s = 0; s < NS; ++s)
-        raw[s] = w[s] != 0.f ? __ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.O[s]) + orow) + v)
-                             : make_uint4(0u, 0u, 0u, 0u);
+      for (int s = 0; s < NS; ++s) raw[s] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.O[s]) + orow) + v);
       float g[VN], o[VN];
       unpack(__ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dO) + orow) + v), g,
              static_cast<const T*>(nullptr));
@@ -162,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) merge_bwd_kernel(MergeBwdArgs a, int
       for (int e = 0; e < VN; ++e) o[e] = 0.f;
 #pragma unroll
       for (int s = 0; s < NS; ++s) {
+        if (w[s] == 0.f) continue;  // an empty part's stored values never enter
         float f[VN];
         unpack(raw[s], f, static_cast<const T*>(nullptr));
 #pragma unroll
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) merge_bwd_kernel(MergeBwdArgs a, int
           out[e] = w[s] * g[e];
         }
         if (w[s] != 0.f) dot[s] += acc;
-        __stcs(reinterpret_cast<uint4*>(static_cast<T*>(a.dO_out[s]) + orow) + v, pack(out, static_cast<const T*>(nullptr)));
+        reinterpret_cast<uint4*>(static_cast<T*>(a.dO_out[s]) + orow)[v] = pack(out, static_cast<const T*>(nullptr));
       }
     }
 #pragma unroll
@@ -192,14 +197,156 @@ __global__ void __launch_bounds__(kThreads) merge_bwd_kernel(MergeBwdArgs a, int
   }
 }
 
+// The same gradient with the row data staged through shared memory by cp.async, for
+// rows of at most one 16-byte vector per lane (d * size(T) <= 512).  Each thread
+// copies its own vector of every state and of dO for the pass kAhead passes ahead and
+// later reads back only what it copied, so it waits on its own copy groups and no
+// CTA barrier is needed; the LSE rows of the next pass are loaded a pass early.
+// Keeps (kAhead + 1) passes of loads in flight instead of one.
+constexpr int kPasses = 16;  // passes of kThreads / lpr rows per CTA
+constexpr int kAhead = 2;   // stage slots
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <typename T, int NS>
+__global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_async_kernel(MergeBwdArgs a, int lpr) {
+  constexpr int VN = Vec<T>::n;
+  extern __shared__ uint4 stage[];  // [kAhead][NS + 1][kThreads]
+  const long long rows = (long long)a.B * a.N * a.Hh;
+  const int rpp = kThreads / lpr;  // rows per pass
+  const long long r0 = (long long)blockIdx.x * kPasses * rpp;
+  const int tid = threadIdx.x, sub = tid / lpr, lane = tid % lpr;
+  const int wl = tid & 31;
+  const unsigned grp = lpr == 32 ? 0xffffffffu : (((1u << lpr) - 1u) << (wl & ~(lpr - 1)));
+  const bool has_vec = lane < a.d / VN;
+  auto row_of = [&](int pass) { return r0 + (long long)pass * rpp + sub; };
+  auto lse_row = [&](long long r) {
+    const long long h = r % a.Hh, bn = r / a.Hh;
+    return ((bn / a.N) * a.Hh + h) * a.N + bn % a.N;
+  };
+  auto issue = [&](int pass) {  // always commits a group, so group counting stays uniform
+    const long long r = row_of(pass);
+    if (pass < kPasses && r < rows && has_vec) {
+      uint4* slot = stage + (size_t)(pass % kAhead) * (NS + 1) * kThreads;
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+        cp_async16(slot + s * kThreads + tid, static_cast<const T*>(a.O[s]) + (size_t)r * a.d + lane * VN);
+      cp_async16(slot + NS * kThreads + tid, static_cast<const T*>(a.dO) + (size_t)r * a.d + lane * VN);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int q = 0; q < kAhead; ++q) issue(q);
+  float ls_next[NS], gl_next = 0.f;
+  {
+    const long long r = row_of(0);
+    const long long lr = r < rows ? lse_row(r) : 0;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) ls_next[s] = r < rows ? a.L[s][lr] : -INFINITY;
+    if (a.dL && r < rows) gl_next = a.dL[lr];
+  }
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const long long r = row_of(pass);
+    const bool valid = r < rows;  // the same on the lane group's lanes
+    float ls[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) ls[s] = ls_next[s];
+    const float gl = gl_next;
+    const long long lr = valid ? lse_row(r) : 0;
+    {  // the next pass's LSE rows, a pass early
+      const long long r2 = row_of(pass + 1);
+      const bool v2 = pass + 1 < kPasses && r2 < rows;
+      const long long lr2 = v2 ? lse_row(r2) : 0;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) ls_next[s] = v2 ? a.L[s][lr2] : -INFINITY;
+      gl_next = (a.dL && v2) ? a.dL[lr2] : 0.f;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) m = fmaxf(m, ls[s]);
+    float w[NS];
+    if (m == -INFINITY) {
+#pragma unroll
+      for (int s = 0; s < NS; ++s) w[s] = 0.f;
+    } else {
+      float sum = 0.f;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) sum += expf(ls[s] - m);
+      const float lse = m + logf(sum);
+#pragma unroll
+      for (int s = 0; s < NS; ++s) w[s] = expf(ls[s] - lse);
+    }
+    cp_async_wait<kAhead - 1>();  // this pass's group (and every older one) has landed
+    float dot[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) dot[s] = 0.f;
+    if (valid && has_vec) {
+      const uint4* slot = stage + (size_t)(pass % kAhead) * (NS + 1) * kThreads;
+      float g[VN], o[VN];
+      unpack(slot[NS * kThreads + tid], g, static_cast<const T*>(nullptr));
+#pragma unroll
+      for (int e = 0; e < VN; ++e) o[e] = 0.f;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        if (w[s] == 0.f) continue;  // an empty part's stored values never enter
+        float f[VN];
+        unpack(slot[s * kThreads + tid], f, static_cast<const T*>(nullptr));
+#pragma unroll
+        for (int e = 0; e < VN; ++e) o[e] = fmaf(w[s], f[e], o[e]);
+      }
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        float f[VN], out[VN];
+        unpack(slot[s * kThreads + tid], f, static_cast<const T*>(nullptr));
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < VN; ++e) {
+          acc = fmaf(g[e], f[e] - o[e], acc);
+          out[e] = w[s] * g[e];
+        }
+        if (w[s] != 0.f) dot[s] = acc;
+        reinterpret_cast<uint4*>(static_cast<T*>(a.dO_out[s]) + (size_t)r * a.d)[lane] =
+            pack(out, static_cast<const T*>(nullptr));
+      }
+    }
+    issue(pass + kAhead);  // the slot just read takes the pass kAhead ahead
+    if (valid) {
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+        for (int off = lpr >> 1; off > 0; off >>= 1) dot[s] += __shfl_xor_sync(grp, dot[s], off);
+      if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < NS; ++s) a.dL_out[s][lr] = w[s] != 0.f ? w[s] * (dot[s] + gl) : 0.f;
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
 template <typename T, int NS>
 cudaError_t launch_bwd_ns(const MergeBwdArgs& a, cudaStream_t st) {
   constexpr int VN = Vec<T>::n;
   int nvec = a.d / VN;
   int lpr = 1;
   while (lpr < nvec && lpr < 32) lpr <<= 1;
-  dim3 grid((a.N + kRowsPerCta - 1) / kRowsPerCta, a.Hh, a.B);
-  merge_bwd_kernel<T, NS><<<grid, kThreads, 0, st>>>(a, lpr);
+  const long long rows = (long long)a.B * a.N * a.Hh;
+  if (nvec <= lpr) {  // one vector per lane: the staged kernel
+    const size_t smem = (size_t)kAhead * (NS + 1) * kThreads * sizeof(uint4);
+    cudaError_t e = cudaFuncSetAttribute(merge_bwd_async_kernel<T, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long per_cta = (long long)kPasses * (kThreads / lpr);
+    merge_bwd_async_kernel<T, NS><<<(unsigned)((rows + per_cta - 1) / per_cta), kThreads, smem, st>>>(a, lpr);
+  } else {
+    merge_bwd_kernel<T, NS><<<(unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta), kThreads, 0, st>>>(a, lpr);
+  }
   note_launches(1);
   return cudaGetLastError();
 }

@@ -186,8 +186,10 @@ def test_merge_matches_oracle(sda, dtype, d, n_states):
 
 
 @pytest.mark.parametrize("dtype,d,n_states", [("bf16", 128, 4), ("bf16", 64, 2), ("f32", 64, 3), ("bf16", 128, 16),
-                                              ("f32", 128, 1)])
+                                              ("f32", 128, 1), ("bf16", 512, 3), ("f32", 256, 2)])
 def test_merge_bwd_matches_oracle(sda, dtype, d, n_states):
+    """Rows of up to one 16-byte vector per lane take the shared-memory-staged kernel; d = 512 bf16 and
+    d = 256 fp32 rows (two vectors per lane) take the register kernel."""
     rng = np.random.default_rng(n_states * 11 + d)
     B, N, Hh = 2, 333, 3
     Os = [rng.uniform(-3.0, 3.0, (B, N, Hh, d)) for _ in range(n_states)]
