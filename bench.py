@@ -51,10 +51,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 #       python bench.py --steps 2 --warmup 3 --no-e2e --no-cpu-baseline
 # An entry goes back to None whenever its kernel changes, until it is captured again.
 NCU_DRAM_BYTES = {
-    "score_kernel": 0.590e9 + 0.103e9,
-    "fwd_tc_kernel": 58.458e9 + 2.501e9,
-    "dq_kernel": 148.651e9 + 2.164e9,
-    "dkdv_kernel": 143.121e9 + 4.275e9,
+    "score_kernel": 0.583e9 + 0.105e9,
+    "fwd_tc_kernel": 58.465e9 + 2.501e9,
+    "dq_kernel": 167.622e9 + 2.165e9,
+    "dkdv_kernel": 143.499e9 + 4.275e9,
 }
 
 def parse():
