@@ -107,9 +107,10 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(MergeArgs a, int lpr) {
 }
 
 // Gradient of the merge for one row per group of lpr consecutive lanes: the row's
-// weights as in merge_kernel; per 16-byte vector, O = sum_s w_s O_s, the partial
-// dot products dO . (O_s - O) and the stores of w_s dO; the dot products are summed
-// over the row's lanes by shuffles within the lane group.  Every state's vector is
+// weights as in merge_kernel; per 16-byte vector, the partial dot products dO . O_s
+// and the stores of w_s dO; the dot products are summed over the row's lanes by
+// shuffles within the lane group, and dO . (O_s - O) = dO . O_s - sum_t w_t dO . O_t
+// is formed from the sums (O itself is never built: fewer instructions per byte).  Every state's vector is
 // loaded whatever its weight, so the loads of a row go out together with its LSE
 // loads instead of after them.  Parts with w_s = 0 (an
 // empty part, or an empty row) are skipped and get zero gradients.  The weights use
@@ -159,19 +160,9 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_kernel(Me
       uint4 raw[NS];
 #pragma unroll
       for (int s = 0; s < NS; ++s) raw[s] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.O[s]) + orow) + v);
-      float g[VN], o[VN];
+      float g[VN];
       unpack(__ldcs(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dO) + orow) + v), g,
              static_cast<const T*>(nullptr));
-#pragma unroll
-      for (int e = 0; e < VN; ++e) o[e] = 0.f;
-#pragma unroll
-      for (int s = 0; s < NS; ++s) {
-        if (w[s] == 0.f) continue;  // an empty part's stored values never enter
-        float f[VN];
-        unpack(raw[s], f, static_cast<const T*>(nullptr));
-#pragma unroll
-        for (int e = 0; e < VN; ++e) o[e] = fmaf(w[s], f[e], o[e]);
-      }
 #pragma unroll
       for (int s = 0; s < NS; ++s) {
         float f[VN], out[VN];
@@ -179,10 +170,10 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_kernel(Me
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < VN; ++e) {
-          acc = fmaf(g[e], f[e] - o[e], acc);
+          acc = fmaf(g[e], f[e], acc);
           out[e] = w[s] * g[e];
         }
-        if (w[s] != 0.f) dot[s] += acc;
+        if (w[s] != 0.f) dot[s] += acc;  // an empty part's stored values never enter
         reinterpret_cast<uint4*>(static_cast<T*>(a.dO_out[s]) + orow)[v] = pack(out, static_cast<const T*>(nullptr));
       }
     }
@@ -191,8 +182,11 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_kernel(Me
       for (int off = lpr >> 1; off > 0; off >>= 1) dot[s] += __shfl_xor_sync(grp, dot[s], off);
     if (lane == 0) {
       const float gl = a.dL ? a.dL[lrow] : 0.f;
+      float go = 0.f;  // dO . O = sum_s w_s dO . O_s
 #pragma unroll
-      for (int s = 0; s < NS; ++s) a.dL_out[s][lrow] = w[s] != 0.f ? w[s] * (dot[s] + gl) : 0.f;
+      for (int s = 0; s < NS; ++s) go = fmaf(w[s], dot[s], go);
+#pragma unroll
+      for (int s = 0; s < NS; ++s) a.dL_out[s][lrow] = w[s] != 0.f ? w[s] * (dot[s] - go + gl) : 0.f;
     }
   }
 }
@@ -227,10 +221,31 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_async_ker
   const unsigned grp = lpr == 32 ? 0xffffffffu : (((1u << lpr) - 1u) << (wl & ~(lpr - 1)));
   const bool has_vec = lane < a.d / VN;
   auto row_of = [&](int pass) { return r0 + (long long)pass * rpp + sub; };
-  auto lse_row = [&](long long r) {
-    const long long h = r % a.Hh, bn = r / a.Hh;
-    return ((bn / a.N) * a.Hh + h) * a.N + bn % a.N;
+  // (b, n, h) of this lane group's row, divided out once and then advanced by rpp rows
+  // per pass with carries (memory order (b, n, h)): the LSE index needs no division
+  // per pass.
+  int hh, bb;
+  long long nn;
+  {
+    const long long r = row_of(0);
+    hh = (int)(r % a.Hh);
+    const long long bn = r / a.Hh;
+    nn = bn % a.N;
+    bb = (int)(bn / a.N);
+  }
+  auto advance = [&]() {
+    hh += rpp;
+    if (hh >= a.Hh) {
+      const int q = hh / a.Hh;
+      hh -= q * a.Hh;
+      nn += q;
+      if (nn >= a.N) {
+        bb += (int)(nn / a.N);
+        nn %= a.N;
+      }
+    }
   };
+  auto lse_index = [&]() { return ((long long)bb * a.Hh + hh) * a.N + nn; };
   auto issue = [&](int pass) {  // always commits a group, so group counting stays uniform
     const long long r = row_of(pass);
     if (pass < kPasses && r < rows && has_vec) {
@@ -245,12 +260,13 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_async_ker
 #pragma unroll
   for (int q = 0; q < kAhead; ++q) issue(q);
   float ls_next[NS], gl_next = 0.f;
+  long long lr_next;  // LSE index of the row the next pass handles
   {
     const long long r = row_of(0);
-    const long long lr = r < rows ? lse_row(r) : 0;
+    lr_next = r < rows ? lse_index() : 0;
 #pragma unroll
-    for (int s = 0; s < NS; ++s) ls_next[s] = r < rows ? a.L[s][lr] : -INFINITY;
-    if (a.dL && r < rows) gl_next = a.dL[lr];
+    for (int s = 0; s < NS; ++s) ls_next[s] = r < rows ? a.L[s][lr_next] : -INFINITY;
+    if (a.dL && r < rows) gl_next = a.dL[lr_next];
   }
   for (int pass = 0; pass < kPasses; ++pass) {
     const long long r = row_of(pass);
@@ -259,14 +275,15 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_async_ker
 #pragma unroll
     for (int s = 0; s < NS; ++s) ls[s] = ls_next[s];
     const float gl = gl_next;
-    const long long lr = valid ? lse_row(r) : 0;
+    const long long lr = lr_next;
     {  // the next pass's LSE rows, a pass early
       const long long r2 = row_of(pass + 1);
       const bool v2 = pass + 1 < kPasses && r2 < rows;
-      const long long lr2 = v2 ? lse_row(r2) : 0;
+      advance();
+      lr_next = v2 ? lse_index() : 0;
 #pragma unroll
-      for (int s = 0; s < NS; ++s) ls_next[s] = v2 ? a.L[s][lr2] : -INFINITY;
-      gl_next = (a.dL && v2) ? a.dL[lr2] : 0.f;
+      for (int s = 0; s < NS; ++s) ls_next[s] = v2 ? a.L[s][lr_next] : -INFINITY;
+      gl_next = (a.dL && v2) ? a.dL[lr_next] : 0.f;
     }
     float m = -INFINITY;
 #pragma unroll
@@ -288,19 +305,11 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_async_ker
 #pragma unroll
     for (int s = 0; s < NS; ++s) dot[s] = 0.f;
     if (valid && has_vec) {
+      // dot[s] = this lane's share of dO . O_s; dO . O = sum_s w_s dO . O_s is formed
+      // after the row reduction, so O itself is never built
       const uint4* slot = stage + (size_t)(pass % kAhead) * (NS + 1) * kThreads;
-      float g[VN], o[VN];
+      float g[VN];
       unpack(slot[NS * kThreads + tid], g, static_cast<const T*>(nullptr));
-#pragma unroll
-      for (int e = 0; e < VN; ++e) o[e] = 0.f;
-#pragma unroll
-      for (int s = 0; s < NS; ++s) {
-        if (w[s] == 0.f) continue;  // an empty part's stored values never enter
-        float f[VN];
-        unpack(slot[s * kThreads + tid], f, static_cast<const T*>(nullptr));
-#pragma unroll
-        for (int e = 0; e < VN; ++e) o[e] = fmaf(w[s], f[e], o[e]);
-      }
 #pragma unroll
       for (int s = 0; s < NS; ++s) {
         float f[VN], out[VN];
@@ -308,10 +317,10 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_async_ker
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < VN; ++e) {
-          acc = fmaf(g[e], f[e] - o[e], acc);
+          acc = fmaf(g[e], f[e], acc);
           out[e] = w[s] * g[e];
         }
-        if (w[s] != 0.f) dot[s] = acc;
+        if (w[s] != 0.f) dot[s] = acc;  // an empty part's stored values never enter
         reinterpret_cast<uint4*>(static_cast<T*>(a.dO_out[s]) + (size_t)r * a.d)[lane] =
             pack(out, static_cast<const T*>(nullptr));
       }
@@ -322,8 +331,11 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_async_ker
       for (int s = 0; s < NS; ++s)
         for (int off = lpr >> 1; off > 0; off >>= 1) dot[s] += __shfl_xor_sync(grp, dot[s], off);
       if (lane == 0) {
+        float go = 0.f;  // dO . O
 #pragma unroll
-        for (int s = 0; s < NS; ++s) a.dL_out[s][lr] = w[s] != 0.f ? w[s] * (dot[s] + gl) : 0.f;
+        for (int s = 0; s < NS; ++s) go = fmaf(w[s], dot[s], go);
+#pragma unroll
+        for (int s = 0; s < NS; ++s) a.dL_out[s][lr] = w[s] != 0.f ? w[s] * (dot[s] - go + gl) : 0.f;
       }
     }
   }

@@ -1,6 +1,11 @@
 """Run the whole path (predictor, forward, and optionally backward) on one workload.
 
     python -m dynamic_block_sparse_rank_gb300.run_step --workload fwd_61k [--heads 10] [--backward] [--steps 1]
+    python -m dynamic_block_sparse_rank_gb300.run_step --workload merge_131k --merge [--heads 4]
+
+With --merge it runs the state merge and its gradient instead: the workload's
+partition count of random (O, LSE) states of its shapes, then sda_merge_states
+and sda_merge_states_bwd once per step.
 
 A small driver for inspecting the kernels (e.g. under a profiler) on a chosen
 workload: inputs come from the seeded generator, every step runs all the
@@ -21,6 +26,7 @@ def main():
     ap.add_argument("--backward", action="store_true", help="also run the backward (always on for training workloads)")
     ap.add_argument("--steps", type=int, default=1)
     ap.add_argument("--warmup", type=int, default=1)
+    ap.add_argument("--merge", action="store_true", help="run the state merge and its gradient instead")
     args = ap.parse_args()
 
     import torch
@@ -30,6 +36,8 @@ def main():
     wl = inputs.WORKLOADS[args.workload]
     if args.heads:
         wl = wl.with_(heads=args.heads)
+    if args.merge:
+        return merge_steps(wl, args)
     backward = args.backward or wl.backward
     names = ("Q", "K", "V", "Wq", "Wk") + (("dO",) if backward else ())
     x = inputs.generate(wl, names=names)
@@ -72,6 +80,44 @@ def main():
     status = sda.sda_get_device_status()
     print(json.dumps({"workload": wl.name, "heads": wl.heads, "tokens": wl.N, "k": k,
                       "ms": {n: statistics.median(v) for n, v in times.items()},
+                      "status": sda.status_string(status)}))
+    if status != sda.SDA_OK:
+        raise SystemExit(1)
+
+
+def merge_steps(wl, args):
+    import torch
+
+    from . import sda
+
+    n = max(wl.partitions, 2)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    shape, lshape = (wl.B, wl.N, wl.heads, wl.d), (wl.B, wl.heads, wl.N)
+    Os = [torch.randn(shape, device="cuda", generator=g).to(torch.bfloat16) for _ in range(n)]
+    Ls = [torch.randn(lshape, device="cuda", generator=g) for _ in range(n)]
+    dO = torch.randn(shape, device="cuda", generator=g).to(torch.bfloat16)
+    dL = torch.randn(lshape, device="cuda", generator=g)
+    Oo, Lo = torch.empty_like(Os[0]), torch.empty_like(Ls[0])
+    gO = [torch.empty_like(Os[0]) for _ in range(n)]
+    gL = [torch.empty_like(Ls[0]) for _ in range(n)]
+    st = torch.cuda.current_stream()
+    times = {"merge": [], "merge_bwd": []}
+    for s in range(args.warmup + args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(st)
+        sda.sda_merge_states(Os, Ls, wl.B, wl.N, wl.heads, wl.d, "bf16", Oo, Lo, st)
+        ev[1].record(st)
+        sda.sda_merge_states_bwd(Os, Ls, dO, dL, wl.B, wl.N, wl.heads, wl.d, "bf16", gO, gL, st)
+        ev[2].record(st)
+        torch.cuda.synchronize()
+        if s >= args.warmup:
+            times["merge"].append(ev[0].elapsed_time(ev[1]))
+            times["merge_bwd"].append(ev[1].elapsed_time(ev[2]))
+    rows = wl.B * wl.N * wl.heads
+    status = sda.sda_get_device_status()
+    print(json.dumps({"workload": wl.name, "heads": wl.heads, "tokens": wl.N, "states": n,
+                      "ms": {k: statistics.median(v) for k, v in times.items()},
+                      "bytes": {"merge": (n + 1) * rows * (2 * wl.d + 4), "merge_bwd": (2 * n + 1) * rows * (2 * wl.d + 4)},
                       "status": sda.status_string(status)}))
     if status != sda.SDA_OK:
         raise SystemExit(1)
