@@ -8,7 +8,9 @@
 // dLSE_s = w_s (dO . (O_s - O) + dLSE).
 //
 // HBM-bound: every byte of every state is read once and the result written
-// once.  A CTA covers 64 consecutive tokens of one (batch, head): the LSE
+// once.  Rows of at most one 16-byte vector per lane go through the staged kernels
+// (merge_async_kernel, merge_bwd_async_kernel: each thread's loads run two passes
+// ahead through shared memory); wider rows through the register kernels below.  A CTA covers 64 consecutive tokens of one (batch, head): the LSE
 // reads are 256-byte runs and each O row is a contiguous d-element run read
 // with 16-byte vector loads by a group of lanes (LPR lanes per row).
 #include "internal.h"
@@ -342,6 +344,113 @@ __global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_bwd_async_ker
   cp_async_wait<0>();
 }
 
+// The merge itself, staged the same way (rows of at most one 16-byte vector per lane).
+// In place is safe: a row's data is staged before that row is written, and no write
+// touches a row still to be staged.
+template <typename T, int NS>
+__global__ void __launch_bounds__(kThreads, NS <= 4 ? 4 : 1) merge_async_kernel(MergeArgs a, int lpr) {
+  constexpr int VN = Vec<T>::n;
+  extern __shared__ uint4 stage[];  // [kAhead][NS][kThreads]
+  const long long rows = (long long)a.B * a.N * a.Hh;
+  const int rpp = kThreads / lpr;
+  const long long r0 = (long long)blockIdx.x * kPasses * rpp;
+  const int tid = threadIdx.x, sub = tid / lpr, lane = tid % lpr;
+  const bool has_vec = lane < a.d / VN;
+  auto row_of = [&](int pass) { return r0 + (long long)pass * rpp + sub; };
+  int hh, bb;
+  long long nn;
+  {
+    const long long r = row_of(0);
+    hh = (int)(r % a.Hh);
+    const long long bn = r / a.Hh;
+    nn = bn % a.N;
+    bb = (int)(bn / a.N);
+  }
+  auto advance = [&]() {
+    hh += rpp;
+    if (hh >= a.Hh) {
+      const int q = hh / a.Hh;
+      hh -= q * a.Hh;
+      nn += q;
+      if (nn >= a.N) {
+        bb += (int)(nn / a.N);
+        nn %= a.N;
+      }
+    }
+  };
+  auto lse_index = [&]() { return ((long long)bb * a.Hh + hh) * a.N + nn; };
+  auto issue = [&](int pass) {
+    const long long r = row_of(pass);
+    if (pass < kPasses && r < rows && has_vec) {
+      uint4* slot = stage + (size_t)(pass % kAhead) * NS * kThreads;
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+        cp_async16(slot + s * kThreads + tid, static_cast<const T*>(a.O[s]) + (size_t)r * a.d + lane * VN);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int q = 0; q < kAhead; ++q) issue(q);
+  float ls_next[NS];
+  long long lr_next;
+  {
+    const long long r = row_of(0);
+    lr_next = r < rows ? lse_index() : 0;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) ls_next[s] = r < rows ? a.L[s][lr_next] : -INFINITY;
+  }
+  for (int pass = 0; pass < kPasses; ++pass) {
+    const long long r = row_of(pass);
+    const bool valid = r < rows;
+    float ls[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) ls[s] = ls_next[s];
+    const long long lr = lr_next;
+    {
+      const long long r2 = row_of(pass + 1);
+      const bool v2 = pass + 1 < kPasses && r2 < rows;
+      advance();
+      lr_next = v2 ? lse_index() : 0;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) ls_next[s] = v2 ? a.L[s][lr_next] : -INFINITY;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < NS; ++s) m = fmaxf(m, ls[s]);
+    float lse, w[NS];
+    if (m == -INFINITY) {
+      lse = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) w[s] = 0.f;
+    } else {
+      float sum = 0.f;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) sum += __expf(ls[s] - m);
+      lse = m + __logf(sum);
+#pragma unroll
+      for (int s = 0; s < NS; ++s) w[s] = __expf(ls[s] - lse);
+    }
+    cp_async_wait<kAhead - 1>();
+    if (valid && has_vec) {
+      const uint4* slot = stage + (size_t)(pass % kAhead) * NS * kThreads;
+      float acc[VN];
+#pragma unroll
+      for (int e = 0; e < VN; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        float f[VN];
+        unpack(slot[s * kThreads + tid], f, static_cast<const T*>(nullptr));
+#pragma unroll
+        for (int e = 0; e < VN; ++e) acc[e] = fmaf(w[s], f[e], acc[e]);
+      }
+      reinterpret_cast<uint4*>(static_cast<T*>(a.O_out) + (size_t)r * a.d)[lane] = pack(acc, static_cast<const T*>(nullptr));
+    }
+    issue(pass + kAhead);
+    if (valid && lane == 0) a.L_out[lr] = lse;
+  }
+  cp_async_wait<0>();
+}
+
 template <typename T, int NS>
 cudaError_t launch_bwd_ns(const MergeBwdArgs& a, cudaStream_t st) {
   constexpr int VN = Vec<T>::n;
@@ -383,8 +492,18 @@ cudaError_t launch_ns(const MergeArgs& a, cudaStream_t st) {
   int nvec = a.d / VN;
   int lpr = 1;
   while (lpr < nvec && lpr < 32) lpr <<= 1;
-  dim3 grid((a.N + kRowsPerCta - 1) / kRowsPerCta, a.Hh, a.B);
-  merge_kernel<T, NS><<<grid, kThreads, 0, st>>>(a, lpr);
+  if (nvec <= lpr) {  // one vector per lane: the staged kernel
+    const size_t smem = (size_t)kAhead * NS * kThreads * sizeof(uint4);
+    cudaError_t e =
+        cudaFuncSetAttribute(merge_async_kernel<T, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const long long rows = (long long)a.B * a.N * a.Hh;
+    const long long per_cta = (long long)kPasses * (kThreads / lpr);
+    merge_async_kernel<T, NS><<<(unsigned)((rows + per_cta - 1) / per_cta), kThreads, smem, st>>>(a, lpr);
+  } else {
+    dim3 grid((a.N + kRowsPerCta - 1) / kRowsPerCta, a.Hh, a.B);
+    merge_kernel<T, NS><<<grid, kThreads, 0, st>>>(a, lpr);
+  }
   note_launches(1);
   return cudaGetLastError();
 }
