@@ -105,6 +105,37 @@ def test_null_and_range_arguments_return_before_any_launch(L):
     assert L.sda_merge_states(1, arr, arr, 1, 4, 1, 12, 1, 16, 16, None) == sda.SDA_ERR_UNSUPPORTED
 
 
+def test_training_through_the_merge_validates_on_the_host(L):
+    """sda_merge_states_bwd and sda_attn_bwd_partition reject bad arguments before any launch."""
+    arr = (ctypes.c_void_p * 1)(16)
+    farr = (ctypes.c_void_p * 1)(16)
+    mb = L.sda_merge_states_bwd
+    assert mb(0, arr, arr, 16, None, 1, 4, 1, 64, 1, arr, farr, None) == sda.SDA_ERR_INVALID_ARG
+    assert mb(17, arr, arr, 16, None, 1, 4, 1, 64, 1, arr, farr, None) == sda.SDA_ERR_INVALID_ARG
+    assert mb(1, arr, arr, None, None, 1, 4, 1, 64, 1, arr, farr, None) == sda.SDA_ERR_INVALID_ARG  # no dO
+    assert mb(1, arr, arr, 16, None, 1, 4, 1, 12, 1, arr, farr, None) == sda.SDA_ERR_UNSUPPORTED  # 24-byte rows
+    assert mb(1, arr, arr, 18, None, 1, 4, 1, 64, 1, arr, farr, None) == sda.SDA_ERR_INVALID_ARG  # misaligned dO
+    none = (ctypes.c_void_p * 1)(None)
+    assert mb(1, arr, arr, 16, None, 1, 4, 1, 64, 1, none, farr, None) == sda.SDA_ERR_INVALID_ARG  # no dO_0
+    p = _bad({})  # n_b = 2
+    bp = L.sda_attn_bwd_partition
+    t = [16] * 5
+    # key range outside [0, n_b] or reversed
+    assert bp(ctypes.byref(p), *t[:4], 16, t[4], None, 16, 0, 3, None, 16, 16, 16, 1, 16, 1 << 40, None) == \
+        sda.SDA_ERR_INVALID_ARG
+    assert bp(ctypes.byref(p), *t[:4], 16, t[4], None, 16, 2, 1, None, 16, 16, 16, 1, 16, 1 << 40, None) == \
+        sda.SDA_ERR_INVALID_ARG
+    assert bp(ctypes.byref(p), *t[:4], 16, t[4], None, 16, -1, 1, None, 16, 16, 16, 1, 16, 1 << 40, None) == \
+        sda.SDA_ERR_INVALID_ARG
+    # bad gradient dtype, small workspace, missing dQ
+    assert bp(ctypes.byref(p), *t[:4], 16, t[4], None, 16, 0, 2, None, 16, 16, 16, 5, 16, 1 << 40, None) == \
+        sda.SDA_ERR_INVALID_ARG
+    assert bp(ctypes.byref(p), *t[:4], 16, t[4], None, 16, 0, 2, None, 16, 16, 16, 1, 16, 8, None) == \
+        sda.SDA_ERR_WORKSPACE
+    assert bp(ctypes.byref(p), *t[:4], 16, t[4], None, 16, 0, 2, None, None, 16, 16, 1, 16, 1 << 40, None) == \
+        sda.SDA_ERR_INVALID_ARG
+
+
 def test_status_strings(L):
     for s in range(6):
         assert sda.status_string(s)
