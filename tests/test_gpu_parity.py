@@ -155,9 +155,10 @@ def test_forward_empty_selection_and_inactive_blocks(sda):
             assert np.all(Oh[:, rows] == 7.0) and np.all(Lh[:, :, rows] == 5.0)
 
 
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 64), ("f32", 128)])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 64), ("f32", 128), ("bf16", 512)])
 @pytest.mark.parametrize("n_states", [1, 3, 4, 16])
 def test_merge_matches_oracle(sda, dtype, d, n_states):
+    """Rows of up to 512 bytes take the shared-memory-staged kernel; d = 512 bf16 rows the register kernel."""
     rng = np.random.default_rng(n_states * 7 + d)
     B, N, Hh = 2, 333, 3
     # partial states are convex combinations of V rows: keep them in a realistic range (|O| < 3)
