@@ -48,6 +48,13 @@ Readings taken where the pages are silent (each is restated in the design notes)
    (they were computed from an earlier step's inputs) and carry no gradient;
    the fresh states are differentiated by the chain rule through the merge
    and through softmax attention restricted to their key range.
+10. The predictor's own training signal (DSV trains it in a stage of its
+    own; the pages give no loss): the block score s(I, J) is read as an
+    estimate of the full-rank block-max logit t(I, J) = max over i in I,
+    j in J of q_i . k_j (with r = d and identity projections the two
+    coincide), distilled by L = 1/2 sum (s - t)^2.  The max passes its
+    gradient to its maximising pair, the first in token order on ties; the
+    bf16 rounding of q~, k~ passes it unchanged.
 """
 from __future__ import annotations
 
@@ -170,6 +177,47 @@ def predict_blocks(Q, K, Wq, Wk, geom: Geometry, keep, dtype, query_blocks=None)
             for a in range(nq):
                 idx[b, h, a] = topk_blocks(scores[b, h, a], k)
     return idx, scores
+
+
+def predictor_distill_grad(Q, K, Wq, Wk, geom: Geometry, dtype):
+    """Training signal of the low-rank predictor (DSV stage 1, reading 10).
+
+    For every (b, h, I, J): s = q~_i* . k~_j* at the pair maximising q~_i . k~_j
+    over i in I, j in J (first in the tiles' token order on ties), and the
+    target t = max over the same pairs of q_i . k_j.  With e = s - t and
+    L = 1/2 sum e^2:
+      dL/dWq[h] = sum e Q_i*^T k~_j*,   dL/dWk[h] = sum e K_j*^T q~_i*.
+    Returns (L, dWq [Hh, d, r], dWk [Hh, d, r], s, t), s and t [B, Hh, n_b, n_b].
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    qt, kt = project(Q, Wq, dtype), project(K, Wk, dtype)
+    B, N, Hh, d = Q.shape
+    r = qt.shape[3]
+    nb = geom.n_blocks
+    dWq = np.zeros((Hh, d, r))
+    dWk = np.zeros((Hh, d, r))
+    s_all = np.empty((B, Hh, nb, nb))
+    t_all = np.empty((B, Hh, nb, nb))
+    L = 0.0
+    for b in range(B):
+        for h in range(Hh):
+            for I in range(nb):
+                rows = geom.tokens(I)
+                qI, QI = qt[b, h][rows], Q[b, rows, h]
+                for J in range(nb):
+                    cols = geom.tokens(J)
+                    kJ, KJ = kt[b, h][cols], K[b, cols, h]
+                    S = qI @ kJ.T
+                    i, j = divmod(int(np.argmax(S)), len(cols))  # first maximum in row-major (i, j) order
+                    t = (QI @ KJ.T).max()
+                    e = S[i, j] - t
+                    s_all[b, h, I, J] = S[i, j]
+                    t_all[b, h, I, J] = t
+                    L += 0.5 * e * e
+                    dWq[h] += e * np.outer(QI[i], kJ[j])
+                    dWk[h] += e * np.outer(KJ[j], qI[i])
+    return L, dWq, dWk, s_all, t_all
 
 
 # --------------------------------------------------------------------------- step 2: sparse attention

@@ -611,3 +611,59 @@ def test_reuse_backward_finite_differences():
             num[pos] = (lp - lm) / (2 * h)
         assert np.abs(num - G).max() <= 1e-6 * max(1.0, np.abs(G).max())
     assert np.abs(dK).max() > 0 and np.abs(dV).max() > 0
+
+
+# ------------------------------------------------------------------ predictor training signal
+def _distill_case(seed, dims=(2, 4, 4, 1, 2, 2), d=5, r=3, Hh=2):
+    geom = orc.Geometry(*dims)
+    Q, K = (_rand((1, geom.N, Hh, d), seed + s) for s in (0, 1))
+    Wq, Wk = (_rand((Hh, d, r), seed + s, 0.5) for s in (2, 3))
+    return geom, Q, K, Wq, Wk
+
+
+def test_distill_gradient_finite_differences():
+    geom, Q, K, Wq, Wk = _distill_case(140)
+    L, dWq, dWk, _, _ = orc.predictor_distill_grad(Q, K, Wq, Wk, geom, "f32")
+    h = 1e-6
+    for W, G in ((Wq, dWq), (Wk, dWk)):
+        num = np.zeros_like(W)
+        for pos in np.ndindex(W.shape):
+            w0 = W[pos]
+            W[pos] = w0 + h
+            lp = orc.predictor_distill_grad(Q, K, Wq, Wk, geom, "f32")[0]
+            W[pos] = w0 - h
+            lm = orc.predictor_distill_grad(Q, K, Wq, Wk, geom, "f32")[0]
+            W[pos] = w0
+            num[pos] = (lp - lm) / (2 * h)
+        assert np.abs(num - G).max() <= 1e-6 * max(1.0, np.abs(G).max())
+
+
+def test_distill_gradient_matches_torch_autograd():
+    geom, Q, K, Wq, Wk = _distill_case(150, dims=(3, 4, 6, 1, 2, 3), d=6, r=4)
+    L, dWq, dWk, s, t = orc.predictor_distill_grad(Q, K, Wq, Wk, geom, "f32")
+    order = np.concatenate([geom.tokens(J) for J in range(geom.n_blocks)])
+    sizes = [len(geom.tokens(J)) for J in range(geom.n_blocks)]
+    loss = 0.0
+    wq, wk = torch.tensor(Wq, requires_grad=True), torch.tensor(Wk, requires_grad=True)
+    for h in range(Q.shape[2]):
+        q, k = torch.from_numpy(Q[0, order, h]), torch.from_numpy(K[0, order, h])
+        S = (q @ wq[h]) @ (k @ wk[h]).T
+        T = q @ k.T
+        for Sb, Tb in zip(torch.split(S, sizes, 0), torch.split(T, sizes, 0)):
+            for Sbb, Tbb in zip(torch.split(Sb, sizes, 1), torch.split(Tb, sizes, 1)):
+                loss = loss + 0.5 * (Sbb.amax() - Tbb.amax()) ** 2
+    loss.backward()
+    assert abs(loss.item() - L) < 1e-9 * max(1.0, L)
+    assert np.abs(wq.grad.numpy() - dWq).max() < 1e-10
+    assert np.abs(wk.grad.numpy() - dWk).max() < 1e-10
+
+
+def test_distill_scores_are_the_predictor_scores_and_identity_is_exact():
+    geom, Q, K, Wq, Wk = _distill_case(160)
+    _, _, _, s, t = orc.predictor_distill_grad(Q, K, Wq, Wk, geom, "f32")
+    assert np.array_equal(s, orc.block_scores(orc.project(Q, Wq, "f32"), orc.project(K, Wk, "f32"), geom))
+    d = Q.shape[3]
+    eye = np.stack([np.eye(d)] * Q.shape[2])
+    L, dWq, dWk, s, t = orc.predictor_distill_grad(Q, K, eye, eye, geom, "f32")
+    assert L < 1e-20 and np.abs(dWq).max() < 1e-12 and np.abs(dWk).max() < 1e-12
+    assert np.abs(s - t).max() < 1e-12
