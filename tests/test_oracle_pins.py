@@ -495,6 +495,21 @@ def _merge_case(seed, P=3, rows=(2, 3), d=4):
     return Os, Ls, dO, dLSE
 
 
+def test_golden_merge_bwd():
+    g = _read_golden("merge_states_bwd.txt")
+    for r in ("row0", "row1"):
+        lse = [_num(t) for t in g[r + "_lse"].split()]
+        os_ = [np.array([_num(t) for t in part.split()]) for part in g[r + "_o"].split("|")]
+        dO = np.array([[_num(t) for t in g[r + "_do"].split()]])
+        dL = np.array([_num(g[r + "_dlse"])])
+        dOs, dLs = orc.merge_states_bwd([o[None] for o in os_], [np.array([x]) for x in lse], dO, dL)
+        want_do = [np.array([_num(t) for t in part.split()]) for part in g[r + "_expect_do"].split("|")]
+        want_dl = [_num(t) for t in g[r + "_expect_dlse"].split()]
+        for p in range(len(os_)):
+            assert np.abs(dOs[p][0] - want_do[p]).max() < 1e-14
+            assert abs(dLs[p][0] - want_dl[p]) < 1e-14
+
+
 @pytest.mark.parametrize("seed", [0, 1])
 def test_merge_bwd_finite_differences(seed):
     Os, Ls, dO, dLSE = _merge_case(seed)
