@@ -18,7 +18,7 @@ on a bounded sample (rank 0, one GPU only).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
 With N > 1 (torchrun), every rank runs an independent replica of the step
-(the path has no exchange step in this build): weak scaling.
+(the path has no exchange step: query blocks, heads and batches are independent): weak scaling.
 """
 from __future__ import annotations
 
