@@ -44,18 +44,24 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel that can be the
-# dominant one, from a single-pass ncu capture of this full-size step:
-#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none \
-#       -k regex:"score_kernel|fwd_tc_kernel|dq_kernel|dkdv_kernel" -s 12 -c 4 \
-#       python bench.py --steps 2 --warmup 3 --no-e2e --no-cpu-baseline
+# Per-launch counters of the kernels that can be the dominant one, each from its own ncu capture of ONE
+# kernel on a small case of the same workload (one head of the 524,288-token step, so every tensor is
+# 134 MB, larger than L2), scaled to the eight-head launch by the units processed (DRAM bytes grow in
+# proportion to the heads), and the tensor pipe's active fraction as ncu reports it:
+#   python profile_step.py --workload train_524k --heads 1 --steps 1 --warmup 1 &&
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed \
+#       --clock-control none -k regex:<kernel> -s <launches before it> -c 1 \
+#       python profile_step.py --workload train_524k --heads 1 --steps 1 --warmup 1
 # An entry goes back to None whenever its kernel changes, until it is captured again.
-NCU_DRAM_BYTES = {
-    "score_kernel": 0.583e9 + 0.105e9,
-    "fwd_tc_kernel": 58.465e9 + 2.501e9,
-    "dq_kernel": 167.622e9 + 2.165e9,
-    "dkdv_kernel": 143.499e9 + 4.275e9,
+NCU_COUNTERS = {
+    "score_kernel": {"dram_bytes": 0.583e9 + 0.105e9, "tensor_active": 0.429},
+    "fwd_tc_kernel": {"dram_bytes": 58.465e9 + 2.501e9, "tensor_active": 0.518},
+    "dq_kernel": {"dram_bytes": 167.622e9 + 2.165e9, "tensor_active": 0.57},
+    "dkdv_kernel": {"dram_bytes": 143.499e9 + 4.275e9, "tensor_active": 0.55},
 }
+
+GAP_REL = 1e-3  # selection rows whose k-th / (k+1)-th score gap is below this (relative) are near-ties
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -178,8 +184,31 @@ def _head0_inputs(wl):
     return _HEAD0[wl.name]
 
 
-def cpu_oracle_sample(wl, seconds: float) -> dict:
-    """Time the oracle (as it stands) on query blocks of head 0 until `seconds` of work are done."""
+def selection_outcome(gpu_row, scores, k) -> str:
+    """The gap rule for one query block: 'exact' when the GPU's kept blocks equal the oracle's top k and the
+    oracle's k-th / (k+1)-th score gap exceeds GAP_REL (relative); 'near_tie' / 'near_tie_differs' when the
+    gap is smaller and every GPU-kept block scores within GAP_REL of the (k+1)-th; otherwise 'fail'."""
+    nb = scores.shape[0]
+    order = np.lexsort((np.arange(nb), -scores))
+    want = np.sort(order[:k])
+    got = np.asarray(gpu_row)
+    if k == nb:
+        return "exact" if np.array_equal(got, want) else "fail"
+    sk, sk1 = scores[order[k - 1]], scores[order[k]]
+    big = max(abs(sk), abs(sk1), 1e-30)
+    if (sk - sk1) / big > GAP_REL:
+        return "exact" if np.array_equal(got, want) else "fail"
+    ok = (len(set(got.tolist())) == k and np.all(got >= 0) and np.all(got < nb)
+          and np.all(scores[got] >= sk1 - GAP_REL * big))
+    if not ok:
+        return "fail"
+    return "near_tie" if np.array_equal(got, want) else "near_tie_differs"
+
+
+def cpu_oracle_sample(wl, seconds: float, gpu_idx_head0=None) -> dict:
+    """Time the oracle (as it stands) on query blocks of head 0 until `seconds` of work are done.  With the
+    GPU's block map of head 0 ([n_b, k]), the oracle's predictor rows of the sampled query blocks also grade
+    the GPU's selection of those rows (near-ties counted)."""
     import oracle as orc
 
     cores = len(os.sched_getaffinity(0))
@@ -191,9 +220,13 @@ def cpu_oracle_sample(wl, seconds: float) -> dict:
     t0 = time.perf_counter()
     flops = 0.0
     done = []
+    outcomes = {"rows": 0, "exact": 0, "near_tie": 0, "near_tie_differs": 0, "fail": 0}
     for I in order:
         I = int(I)
-        idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype, query_blocks=[I])
+        idx, sc = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype, query_blocks=[I])
+        if gpu_idx_head0 is not None:
+            outcomes["rows"] += 1
+            outcomes[selection_outcome(gpu_idx_head0[I], sc[0, 0, 0], idx.shape[-1])] += 1
         orc.attn_fwd(x["Q"], x["K"], x["V"], idx, geom, query_blocks=[I])
         orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], idx, geom, query_blocks=[I])
         flops += 14.0 * wl.d * sz[I] * sz[idx[0, 0, 0]].sum()
@@ -202,7 +235,7 @@ def cpu_oracle_sample(wl, seconds: float) -> dict:
             break
     dt = time.perf_counter() - t0
     return {"tflops": flops / dt / 1e12, "seconds": dt, "cores": cores, "cpu_count": os.cpu_count(),
-            "query_blocks": len(done),
+            "query_blocks": len(done), "selection": outcomes if gpu_idx_head0 is not None else None,
             "sample": f"{len(done)} random query blocks of head 0 of {wl.name}: oracle predictor row "
                       f"(scores against all {geom.n_blocks} key blocks) + forward + backward of their kept "
                       f"blocks, fp64 NumPy"}
@@ -308,7 +341,8 @@ def main():
     torch.cuda.synchronize()
     if sda.sda_get_device_status(stream.cuda_stream) != sda.SDA_OK:
         raise RuntimeError("device status not OK after warm-up")
-    pairs = kept_pairs(wl, idx.cpu().numpy())
+    idx_host = idx.cpu().numpy()
+    pairs = kept_pairs(wl, idx_host)
     f_fwd = 4.0 * wl.d * pairs
     f_bwd = 10.0 * wl.d * pairs
     f_dkdv = 8.0 * wl.d * pairs
@@ -465,17 +499,27 @@ def main():
             "attn_bwd_dq (dq_kernel)": (phase_ms["bwd_dq"], f_dq)}
     dom = max(kern, key=lambda n: kern[n][0])
     dom_ms, dom_flops = kern[dom]
-    traffic = next((v for key, v in NCU_DRAM_BYTES.items() if key in dom), None)
+    counters = next((v for key, v in NCU_COUNTERS.items() if key in dom), None)
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    burst_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    clocks = clk.summary()
+    # the sustained peak was taken at the clock its own loop ran at (power-capped); this step's kernels ran at
+    # the median clock sampled above, so the fraction is also given against that peak scaled to this clock
+    peak_mhz = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
+    run_mhz = clocks.get("sm_mhz")
+    scaled = tc_peak * run_mhz / peak_mhz if peak_mhz and run_mhz else None
     if merge:
         merge["frac_of_hbm_peak"] = merge["gbs"] / hbm_peak
         merge["bwd"]["frac_of_hbm_peak"] = merge["bwd"]["gbs"] / hbm_peak
     attn_ms = phase_ms["fwd"] + phase_ms["bwd_prepare"] + phase_ms["bwd_dq"] + phase_ms["bwd_dkdv"]
     cpu = None
+    selection = None
     if not args.no_cpu_baseline and world == 1:
-        c = cpu_oracle_sample(wl, args.cpu_seconds)
+        c = cpu_oracle_sample(wl, args.cpu_seconds, gpu_idx_head0=idx_host[0, 0])
         cpu = {"value": c["tflops"], "unit": "TFLOP/s", "cores": c["cores"], "kind": "oracle", "sample": c["sample"],
                "seconds": c["seconds"]}
+        selection = dict(c["selection"], rule=f"gap rule, {GAP_REL:g} relative; rows = the oracle sample's "
+                                              f"query blocks (head 0)")
     line = {
         "metric": "sparse attn fwd+bwd TFLOP/s (step incl. predictor), 524,288 tokens",
         "value": whole_job_tflops(world, f_fwd + f_bwd, ms),
@@ -499,14 +543,21 @@ def main():
         "phase_ms": phase_ms,
         "flops": {"fwd": f_fwd, "bwd": f_bwd, "kept_pairs": pairs},
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": achieved / tc_peak, "traffic": traffic, "traffic_unit": "bytes per launch (ncu)",
-                     "peak_source": f"{pk_src} bf16_tflops_sustained (fp16 and bf16 share the dense rate)"},
+                     "frac": achieved / tc_peak,
+                     "traffic": counters["dram_bytes"] if counters else None,
+                     "traffic_unit": "DRAM bytes per launch (ncu, one head scaled to eight)",
+                     "peak_source": f"{pk_src} bf16_tflops_sustained (fp16 and bf16 share the dense rate)",
+                     "peak_burst": burst_peak, "frac_vs_burst": achieved / burst_peak,
+                     "peak_sm_mhz": peak_mhz, "run_sm_mhz": run_mhz,
+                     "frac_vs_sustained_at_run_clock": achieved / scaled if scaled else None,
+                     "ncu_tensor_pipe_active": counters["tensor_active"] if counters else None},
+        "selection": selection,
         "kernels": {n: {"ms": t, "tflops": f / (t / 1e3) / 1e12, "frac": f / (t / 1e3) / 1e12 / tc_peak}
                     for n, (t, f) in kern.items()},
         "merge": merge,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "gpu_launches": launches,
         "device_status": sda.status_string(status),
         "input_generation_s": t_gen,

@@ -17,7 +17,7 @@ sda_status make_prob(const sda_problem* pp, Prob* out) {
   const sda_problem& p = *pp;
   if (p.B < 1 || p.heads < 1 || p.T < 1 || p.H < 1 || p.W < 1 || p.head_dim < 1) return SDA_ERR_INVALID_ARG;
   if (p.bt < 1 || p.bh < 1 || p.bw < 1 || p.rank < 1) return SDA_ERR_INVALID_ARG;
-  if (!(p.keep_ratio > 0.f) || !isfinite(p.keep_ratio)) return SDA_ERR_INVALID_ARG;
+  if (!(p.keep_ratio > 0.0) || !isfinite(p.keep_ratio)) return SDA_ERR_INVALID_ARG;
   if (p.dtype != SDA_F32 && p.dtype != SDA_BF16) return SDA_ERR_INVALID_ARG;
   if (!(p.softmax_scale >= 0.f) || !isfinite(p.softmax_scale)) return SDA_ERR_INVALID_ARG;
   Prob q;
@@ -42,7 +42,12 @@ sda_status make_prob(const sda_problem* pp, Prob* out) {
   q.r = p.rank;
   q.dtype = p.dtype;
   q.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.head_dim);
-  long long k = (long long)floor((double)p.keep_ratio * (double)nb + 1e-9);
+  // Two roundings, as plain double arithmetic does them: the product is stored
+  // through a volatile so that no compiler fuses it with the sum into an FMA
+  // (aarch64 compilers contract by default), which could move k by one.
+  volatile double kprod = p.keep_ratio * (double)nb;
+  const double kval = floor(kprod + 1e-9);
+  long long k = kval > (double)nb ? nb : (long long)kval;
   if (k < 1) k = 1;
   if (k > nb) k = nb;
   q.k = (int)k;
@@ -85,6 +90,10 @@ const char* sda_status_string(sda_status s) {
       return "CUDA error";
     case SDA_ERR_DEVICE_TIMEOUT:
       return "device wait timed out";
+    case SDA_ERR_DEVICE_BAD_INDEX:
+      return "block index out of range or repeated";
+    case SDA_ERR_DEVICE_RANGE:
+      return "input value outside fp16 range";
   }
   return "unknown status";
 }

@@ -98,16 +98,24 @@ __global__ void __launch_bounds__(128) pre_kernel(Geom g, int Hh, long long N, i
   if (G) G[o] = gl;
 }
 
-// bf16 -> fp16, 8 elements per thread-iteration.
-__global__ void half_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n8) {
+// bf16 -> fp16, 8 elements per thread-iteration.  A value outside fp16's finite
+// range becomes inf (or stays NaN); the thread then latches kStatusRange once.
+__global__ void half_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n8,
+                            unsigned* __restrict__ status) {
+  uint32_t bad = 0;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const uint4 v = src[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) o[q] = pack_f16(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u));
+    for (int q = 0; q < 4; ++q) {
+      o[q] = pack_f16(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xFFFF0000u));
+      // an all-ones fp16 exponent field: inf or NaN
+      bad |= ((o[q] & 0x7C00u) == 0x7C00u) | ((o[q] & 0x7C000000u) == 0x7C000000u);
+    }
     dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  if (bad) atomicOr(status, kStatusRange);
 }
 
 // ------------------------------------------------------------------ block-map transpose
@@ -125,7 +133,8 @@ __global__ void csr_bitmap_kernel(const int32_t* __restrict__ idx, long long ent
       continue;
     }
     if (J < kb_begin || J >= kb_end || (qb_active && !qb_active[row % nb])) continue;
-    atomicOr(bitmap + row * words + (J >> 5), 1u << (J & 31));
+    if (atomicOr(bitmap + row * words + (J >> 5), 1u << (J & 31)) & (1u << (J & 31)))
+      atomicOr(status, kStatusBadIndex);  // the same block twice in one row
   }
 }
 
@@ -956,10 +965,10 @@ cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const vo
   csr_fill_kernel<<<(int)((bhn * 32 + 255) / 256), 256, 0, st>>>(w.bitmap, w.offsets, g.nb, p.k, words, bhn, w.lists);
   const long long n8 = (long long)p.B * p.N * p.Hh * p.d / 8;
   const int cb = (int)std::min<long long>((n8 + 255) / 256, 152LL * 16);
-  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(Q), reinterpret_cast<uint4*>(w.Q16), n8);
-  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(K), reinterpret_cast<uint4*>(w.K16), n8);
-  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(V), reinterpret_cast<uint4*>(w.V16), n8);
-  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(dO), reinterpret_cast<uint4*>(w.dO16), n8);
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(Q), reinterpret_cast<uint4*>(w.Q16), n8, status);
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(K), reinterpret_cast<uint4*>(w.K16), n8, status);
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(V), reinterpret_cast<uint4*>(w.V16), n8, status);
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(dO), reinterpret_cast<uint4*>(w.dO16), n8, status);
   const float* dLSE = part ? part->dLSE : nullptr;
   float* G = dLSE ? w.G : nullptr;
   for (int b = 0; b < p.B; ++b) {

@@ -51,6 +51,7 @@ constexpr int kThreads = 384;  // warps 0, 2 TMA, warp 1 MMA, warps 4-11 softmax
 // P_j barrier: the 256 softmax threads, the K producer (K_{j+2} landed) and warp 3 (V_j landed).
 constexpr int kPfullCount = 256 + 2;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kSeenWords = 8192 / 32;       // one bit per key block (n_b <= 8192)
 
 template <int D>
 struct FwdCfg {
@@ -131,7 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* warp_cnt = n_sel_s + 1;  // 16
   float* half_l = reinterpret_cast<float*>(warp_cnt + 16);  // [2 halves][l, l of bf16 P][128 rows]
   float* half_max = half_l + 512;                            // [2 block parities][2 halves][128 rows]
-  int* sel = reinterpret_cast<int*>(half_max + 512);         // k
+  unsigned* seen = reinterpret_cast<unsigned*>(half_max + 512);  // kSeenWords: blocks met in this row
+  int* sel = reinterpret_cast<int*>(seen + kSeenWords);      // k
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -155,17 +157,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     *n_sel_s = 0;
     fence_mbar_init();
   }
+  for (int e = tid; e < kSeenWords; e += kThreads) seen[e] = 0u;
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
-  // Kept blocks of this query block that fall in the key range, in list order.
+  // Kept blocks of this query block that fall in the key range, in list order.  An
+  // entry outside [0, n_b), or one met before in the row, is skipped and latched.
   const int32_t* row = a.idx + (((long long)a.b * a.Hh + h) * a.g.nb + I) * a.k;
   __syncthreads();
   for (int base = 0; base < a.k; base += kThreads) {
     const int j = base + tid;
     int J = j < a.k ? row[j] : -1;
-    bool keep = j < a.k && J >= a.kb_begin && J < a.kb_end && J >= 0 && J < a.g.nb;
+    const bool valid = j < a.k && J >= 0 && J < a.g.nb;
+    bool repeated = false;
+    if (valid) repeated = (atomicOr(seen + (J >> 5), 1u << (J & 31)) >> (J & 31)) & 1u;
+    if (j < a.k && (!valid || repeated)) atomicOr(a.status, kStatusBadIndex);
+    bool keep = valid && !repeated && J >= a.kb_begin && J < a.kb_end;
     unsigned m = __ballot_sync(0xffffffffu, keep);
     if (lane == 0) warp_cnt[warp] = __popc(m);
     __syncthreads();
@@ -468,7 +476,7 @@ cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* 
                        int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st) {
   using C = FwdCfg<D>;
   const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * 1024 +
-                      4 * (size_t)p.k + 64;
+                      4 * kSeenWords + 4 * (size_t)p.k + 64;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   unsigned* status = status_ptr();

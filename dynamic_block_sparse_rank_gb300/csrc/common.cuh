@@ -12,11 +12,12 @@
 namespace sda {
 
 // ----------------------------------------------------------------------------
-// Status latch (one word per device, see status.cu).  Bits record which kind
-// of bounded wait ran out; the host reads and clears it.
+// Status latch (one word per device, see status.cu).  Bits record what went
+// wrong on the device; the host reads and clears it.
 enum : unsigned {
-  kStatusWaitTimeout = 1u,
-  kStatusBadIndex = 2u,
+  kStatusWaitTimeout = 1u,  // a bounded wait ran out
+  kStatusBadIndex = 2u,     // a block_idx entry outside [0, n_b), or repeated in its row
+  kStatusRange = 4u,        // an input value outside fp16's finite range met an fp16 conversion
 };
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.

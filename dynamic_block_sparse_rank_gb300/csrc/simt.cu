@@ -79,12 +79,16 @@ __global__ void __launch_bounds__(256) scores_topk_f32_kernel(Geom g, int Hh, in
 }
 
 // Compact the kept blocks of row I that fall in [kb_begin, kb_end) into sel (ascending input order kept).
-__device__ int filter_sel(const int32_t* row, int k, int kb_begin, int kb_end, int* sel) {
+// With a status word, an entry outside [0, nb) latches kStatusBadIndex (it is skipped either way, as
+// 0 <= kb_begin <= kb_end <= nb).
+__device__ int filter_sel(const int32_t* row, int k, int kb_begin, int kb_end, int* sel, int nb = 0,
+                          unsigned* status = nullptr) {
   __shared__ int n_sel;
   if (threadIdx.x == 0) {
     int n = 0;
     for (int s = 0; s < k; ++s) {
       int J = row[s];
+      if (status && (J < 0 || J >= nb)) atomicOr(status, kStatusBadIndex);
       if (J >= kb_begin && J < kb_end) sel[n++] = J;
     }
     n_sel = n;
@@ -98,7 +102,7 @@ __global__ void fwd_f32_kernel(Geom g, int Hh, int d, int k, float scale, const 
                                const float* __restrict__ K, const float* __restrict__ V,
                                const int32_t* __restrict__ idx, int kb_begin, int kb_end,
                                const uint8_t* __restrict__ qb_active, float* __restrict__ O,
-                               float* __restrict__ LSE, int b) {
+                               float* __restrict__ LSE, int b, unsigned* __restrict__ status) {
   extern __shared__ float smem[];
   const int I = blockIdx.x, h = blockIdx.y;
   if (qb_active && !qb_active[I]) return;
@@ -107,7 +111,8 @@ __global__ void fwd_f32_kernel(Geom g, int Hh, int d, int k, float scale, const 
   int* kv_ok = reinterpret_cast<int*>(vs + kChunk * d);  // kChunk
   int* sel = kv_ok + kChunk;        // k
   const long long N = (long long)g.T * g.H * g.W;
-  const int n_sel = filter_sel(idx + (((long long)b * Hh + h) * g.nb + I) * k, k, kb_begin, kb_end, sel);
+  const int n_sel =
+      filter_sel(idx + (((long long)b * Hh + h) * g.nb + I) * k, k, kb_begin, kb_end, sel, g.nb, status);
   const int row = threadIdx.x;
   const int n = row < g.bs ? valid_token(g, I, row) : -1;
   float q[DM], o[DM];
@@ -378,10 +383,12 @@ static cudaError_t fwd_f32_t(const Prob& p, const float* Q, const float* K, cons
         cudaFuncSetAttribute(fwd_f32_kernel<DM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
   dim3 grid(p.g.nb, p.Hh);
   for (int b = 0; b < p.B; ++b)
     fwd_f32_kernel<DM><<<grid, threads_for(p.g.bs), smem, st>>>(p.g, p.Hh, p.d, p.k, p.scale, Q, K, V, idx,
-                                                                kb_begin, kb_end, qb_active, O, LSE, b);
+                                                                kb_begin, kb_end, qb_active, O, LSE, b, status);
   note_launches(p.B);
   return cudaGetLastError();
 }

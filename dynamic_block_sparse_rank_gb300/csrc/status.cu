@@ -35,7 +35,9 @@ extern "C" sda_status sda_get_device_status(void* stream) {
   if (v != 0) {
     unsigned zero = 0;
     if (cudaMemcpyToSymbol(sda::g_status_word, &zero, sizeof(zero)) != cudaSuccess) return SDA_ERR_CUDA;
-    return SDA_ERR_DEVICE_TIMEOUT;
+    if (v & sda::kStatusWaitTimeout) return SDA_ERR_DEVICE_TIMEOUT;
+    if (v & sda::kStatusBadIndex) return SDA_ERR_DEVICE_BAD_INDEX;
+    return SDA_ERR_DEVICE_RANGE;
   }
   return SDA_OK;
 }

@@ -13,7 +13,8 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsda.so")
 
-SDA_OK, SDA_ERR_INVALID_ARG, SDA_ERR_UNSUPPORTED, SDA_ERR_WORKSPACE, SDA_ERR_CUDA, SDA_ERR_DEVICE_TIMEOUT = range(6)
+(SDA_OK, SDA_ERR_INVALID_ARG, SDA_ERR_UNSUPPORTED, SDA_ERR_WORKSPACE, SDA_ERR_CUDA, SDA_ERR_DEVICE_TIMEOUT,
+ SDA_ERR_DEVICE_BAD_INDEX, SDA_ERR_DEVICE_RANGE) = range(8)
 SDA_F32, SDA_BF16 = 0, 1
 SDA_OP_PREDICT, SDA_OP_BWD = 0, 1
 
@@ -31,7 +32,7 @@ class SdaError(RuntimeError):
 class Problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("heads", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
                 ("W", ctypes.c_int), ("head_dim", ctypes.c_int), ("bt", ctypes.c_int), ("bh", ctypes.c_int),
-                ("bw", ctypes.c_int), ("rank", ctypes.c_int), ("keep_ratio", ctypes.c_float),
+                ("bw", ctypes.c_int), ("rank", ctypes.c_int), ("keep_ratio", ctypes.c_double),
                 ("dtype", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
 
 

@@ -40,6 +40,10 @@
  *     bt*bh*bw == 128, d in {64, 128} and rank in {16, 32, 48, 64}.
  *     Unsupported shapes return SDA_ERR_UNSUPPORTED.
  *   - Pointers used by the tensor-core path must be 16-byte aligned.
+ *   - The library keeps per-device addresses of its own device objects (the
+ *     status word) for the life of the process; a cudaDeviceReset makes them
+ *     stale, so a process that resets a device must not call the library on
+ *     that device afterwards.
  */
 #ifndef SDA_H_
 #define SDA_H_
@@ -57,7 +61,11 @@ typedef enum {
   SDA_ERR_UNSUPPORTED = 2,   /* valid problem the kernels do not cover */
   SDA_ERR_WORKSPACE = 3,     /* ws_bytes smaller than sda_workspace_size */
   SDA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
-  SDA_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait ran out (see sda_get_device_status) */
+  SDA_ERR_DEVICE_TIMEOUT = 5, /* a kernel's bounded wait ran out (see sda_get_device_status) */
+  SDA_ERR_DEVICE_BAD_INDEX = 6, /* a kernel met a block_idx entry outside [0, n_b) or a repeated
+                                   entry in one row (see sda_get_device_status) */
+  SDA_ERR_DEVICE_RANGE = 7    /* the tensor-core backward met an input value outside fp16's
+                                 finite range (|x| > 65504, inf or NaN) */
 } sda_status;
 
 typedef enum { SDA_F32 = 0, SDA_BF16 = 1 } sda_dtype;
@@ -68,7 +76,11 @@ typedef struct {
   int B, heads, T, H, W, head_dim;
   int bt, bh, bw;      /* block (tile) extent along t, h, w */
   int rank;            /* predictor rank r */
-  float keep_ratio;    /* fraction of key blocks kept per query block */
+  double keep_ratio;   /* fraction of key blocks kept per query block; k is
+                          floor(keep_ratio * n_b + 1e-9) in IEEE double with
+                          the product and the sum each rounded once, so a
+                          caller's decimal keep ratio (a double) gives the
+                          same k in any language that does that arithmetic */
   int dtype;           /* sda_dtype of Q, K, V, O, dO, Wq, Wk */
   float softmax_scale; /* 0 selects 1/sqrt(head_dim) */
 } sda_problem;
@@ -98,7 +110,10 @@ sda_status sda_predict_blocks(const sda_problem* p, const void* Q, const void* K
 /* Step 2a: block-sparse attention forward over the kept blocks J of each query
  * block I that satisfy kb_begin <= J < kb_end (0, n_b = all keys).
  *   block_idx  [B, heads, n_b, k] int32 (as written by sda_predict_blocks;
- *              entries must be distinct and in [0, n_b); order is free)
+ *              entries must be distinct and in [0, n_b); order is free).  An
+ *              entry outside that range is skipped, and so is (on the bf16
+ *              path) a repeat of an entry earlier in its row; either latches
+ *              SDA_ERR_DEVICE_BAD_INDEX for sda_get_device_status.
  *   qb_active  optional [n_b] uint8; query blocks with 0 are not written at all
  *              (their O and LSE rows keep the caller's previous contents — the
  *              cached state of DiTango's reuse).  NULL = all active.
@@ -194,9 +209,18 @@ sda_status sda_merge_states_bwd(int n_states, const void* const* O_parts, const 
                                 const void* dO, const float* dLSE, int B, int N, int heads, int head_dim,
                                 int dtype, void* const* dO_parts, float* const* dLSE_parts, void* stream);
 
-/* Synchronises `stream`, then returns SDA_ERR_DEVICE_TIMEOUT if any kernel of
- * this library on the current device ran out of a bounded wait since the last
- * call (and clears the latch), SDA_ERR_CUDA on a CUDA error, else SDA_OK. */
+/* Synchronises `stream`, then reads and clears the current device's status
+ * latch, which kernels of this library set since the last call:
+ *   SDA_ERR_DEVICE_TIMEOUT    a bounded wait ran out (the kernel stopped early,
+ *                             its outputs are incomplete);
+ *   SDA_ERR_DEVICE_BAD_INDEX  a block_idx entry was outside [0, n_b) or repeated
+ *                             within its row (the forward skips such entries;
+ *                             other results computed from that map are undefined);
+ *   SDA_ERR_DEVICE_RANGE      the tensor-core backward converted a Q, K, V or dO
+ *                             value outside fp16's finite range (the gradients
+ *                             hold inf or NaN).
+ * When several were latched the first in this order is returned.  SDA_ERR_CUDA
+ * on a CUDA error, else SDA_OK.  None of these leaves the context unusable. */
 sda_status sda_get_device_status(void* stream);
 
 /* Static description of a status code. */
@@ -219,7 +243,10 @@ const char* sda_status_string(sda_status s);
  *     nothing.
  *   - The first call on a device looks up the array's device address for that
  *     device (cudaGetSymbolAddress, with the device current); make that first
- *     call before any stream capture.
+ *     call before any stream capture.  The address is kept for the life of the
+ *     process: after a cudaDeviceReset of that device (which destroys the
+ *     array with the context) the kept address is stale, so do not call this
+ *     entry point again in a process that has reset the device.
  *   - All calls share the one array on a device: calls that overlap on the GPU
  *     (other streams, other threads) race on it.  Calls ordered on one stream
  *     are safe; nothing in the array needs clearing between calls. */

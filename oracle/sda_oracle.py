@@ -47,7 +47,10 @@ Readings taken where the pages are silent (each is restated in the design notes)
    only.  Read for training, the reused states are constants of this step
    (they were computed from an earlier step's inputs) and carry no gradient;
    the fresh states are differentiated by the chain rule through the merge
-   and through softmax attention restricted to their key range.
+   and through softmax attention restricted to their key range.  A state is
+   read by the merge's backward as it is stored: in the problem's dtype, so a
+   bf16 problem's fresh O_p enters it rounded to bf16 (the reused states are
+   stored the same way by the step that computed them).
 10. The predictor's own training signal (DSV trains it in a stage of its
     own; the pages give no loss): the block score s(I, J) is read as an
     estimate of the full-rank block-max logit t(I, J) = max over i in I,
@@ -358,19 +361,24 @@ def attn_bwd_blocks(Q, K, V, dO, idx, geom: Geometry, scale=None, query_blocks=(
             for I in query_blocks:
                 sel, q, kk, do, P, dS = row_terms(b, h, I)
                 dq_out[(b, h, I)] = scale * (dS @ kk)
-            for J in key_blocks:
-                nJ = len(geom.tokens(J))
-                dk = np.zeros((nJ, d))
-                dv = np.zeros((nJ, V.shape[3]))
-                for I in range(geom.n_blocks):
-                    sel = [int(x) for x in idx[b, h, I]]
-                    if J not in sel:
-                        continue
-                    _, q, kk, do, P, dS = row_terms(b, h, I)
+            # dK/dV of each requested key block J: a sum over the query blocks that kept J; every such
+            # query block's terms are formed once and added to each requested block it kept
+            acc = {J: (np.zeros((len(geom.tokens(J)), d)), np.zeros((len(geom.tokens(J)), V.shape[3])))
+                   for J in key_blocks}
+            for I in range(geom.n_blocks):
+                sel = [int(x) for x in idx[b, h, I]]
+                hit = [J for J in key_blocks if J in sel]
+                if not hit:
+                    continue
+                _, q, kk, do, P, dS = row_terms(b, h, I)
+                for J in hit:
+                    nJ = len(geom.tokens(J))
                     off = sum(len(geom.tokens(x)) for x in sel if x < J)
+                    dk, dv = acc[J]
                     dv += P[:, off:off + nJ].T @ do
                     dk += scale * (dS[:, off:off + nJ].T @ q)
-                dkv_out[(b, h, J)] = (dk, dv)
+            for J in key_blocks:
+                dkv_out[(b, h, J)] = acc[J]
     return dq_out, dkv_out
 
 
@@ -475,20 +483,24 @@ def reuse_merge(states_now, states_prev, geom, P, n_reuse):
     return O, np.transpose(L, (0, 2, 1))
 
 
-def reuse_bwd(Q, K, V, dO, idx, geom, P, n_reuse, states_prev, dLSE=None, scale=None):
+def reuse_bwd(Q, K, V, dO, idx, geom, P, n_reuse, states_prev, dLSE=None, scale=None, state_dtype=None):
     """Gradient of reuse_merge with respect to this step's Q, K, V (reading 9).
 
     The reused states come from an earlier step and are constants here; only
     the fresh ones carry gradient.  dL/d(state) comes from merge_states_bwd of
     the states reuse_merge merged, then each fresh partition state (key range
     of partition p, query blocks that recompute it) is differentiated with
-    attn_bwd.  dO: [B, N, Hh, d]; dLSE: [B, Hh, N] or None.  Returns (dQ, dK, dV).
+    attn_bwd.  dO: [B, N, Hh, d]; dLSE: [B, Hh, N] or None.  state_dtype
+    "bf16": the fresh O_p are read by the merge's backward as stored in bf16
+    (reading 9); None or "f32": as computed.  Returns (dQ, dK, dV).
     """
     now = partition_states(Q, K, V, idx, geom, P, scale)
     reuse = reuse_mask(geom, P, n_reuse)
     Os, Ls = [], []
     for p in range(P):
         O_p, L_p = now[p][0].copy(), now[p][1].copy()
+        if state_dtype == "bf16":
+            O_p = to_bf16(O_p)
         for I in range(geom.n_blocks):
             if reuse[p, I]:
                 rows = geom.tokens(I)

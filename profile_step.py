@@ -1,7 +1,7 @@
 """Run the whole path (predictor, forward, and optionally backward) on one workload.
 
-    python -m dynamic_block_sparse_rank_gb300.run_step --workload fwd_61k [--heads 10] [--backward] [--steps 1]
-    python -m dynamic_block_sparse_rank_gb300.run_step --workload merge_131k --merge [--heads 4]
+    python profile_step.py --workload fwd_61k [--heads 10] [--backward] [--steps 1]
+    python profile_step.py --workload merge_131k --merge [--heads 4]
 
 With --merge it runs the state merge and its gradient instead: the workload's
 partition count of random (O, LSE) states of its shapes, then sda_merge_states
@@ -16,7 +16,11 @@ from __future__ import annotations
 
 import argparse
 import json
+import os
 import statistics
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
 
 
 def main():
@@ -31,7 +35,7 @@ def main():
 
     import torch
 
-    from . import inputs, sda
+    from dynamic_block_sparse_rank_gb300 import inputs, sda
 
     wl = inputs.WORKLOADS[args.workload]
     if args.heads:
@@ -88,7 +92,7 @@ def main():
 def merge_steps(wl, args):
     import torch
 
-    from . import sda
+    from dynamic_block_sparse_rank_gb300 import sda
 
     n = max(wl.partitions, 2)
     g = torch.Generator(device="cuda").manual_seed(0)

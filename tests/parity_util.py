@@ -59,18 +59,6 @@ def assert_close_stored(got, ref, dtype: str, out_dtype: str, what: str):
     return rel
 
 
-def assert_close_through_stored_states(got, ref, dtype: str, what: str):
-    """Gradients taken through a merge of partition states that are stored in the problem's dtype (the reuse
-    cache and the forward's outputs).  The merge backward reads each state as stored, and a bf16 state differs
-    from its exact value by its rounding (2^-9 relative) plus the forward's own error of about the same size;
-    through dLSE_p = w_p (dO . (O_p - O) + dLSE) that difference reaches every gradient in proportion to it.
-    So, as for a bf16-stored result, each element may differ by atol + 2^-8 |ref|; rel-Frobenius keeps its
-    bound.  fp32 problems keep the plain fp32 tolerances."""
-    if dtype != "bf16":
-        return assert_close(got, ref, dtype, what)
-    return assert_close_stored(got, ref, dtype, "bf16", what)
-
-
 def check_scores(got, ref):
     """Block scores of a bf16 problem: fp32 accumulation of exact bf16 products, so they match the oracle
     to ~1e-6 except where a q~ or k~ element was rounded to the neighbouring bf16 value (the GPU rounds an

@@ -15,7 +15,7 @@ def run(device: int = 0) -> dict:
 
     import oracle as orc
     from dynamic_block_sparse_rank_gb300 import inputs, sda
-    from tests.parity_util import assert_close, assert_close_through_stored_states, check_selection, dev, host
+    from tests.parity_util import assert_close, check_selection, dev, host
 
     torch.cuda.set_device(device)
     wl = inputs.Workload("smoke", 1, 2, 3, 10, 12, 64, 2, 8, 8, 16, 0.5, "bf16", 3.0, 16, backward=True)
@@ -66,8 +66,8 @@ def run(device: int = 0) -> dict:
     assert_close(host(Om), O_ref, "bf16", "smoke merged O")
     assert_close(host(Lm), L_ref, "bf16", "smoke merged LSE")
 
-    # 5. training through the merge: the partitions cover every key, so the summed partition gradients are
-    # the full gradient (states as stored in bf16: the stored-state bound)
+    # 5. training through the merge: the two partitions are the grid's two frame slabs and cover every key;
+    # the oracle's reference is the same composition with the fresh states read as stored (bf16)
     gO = [torch.empty_like(Q) for _ in parts]
     gL = [torch.empty_like(LSE) for _ in parts]
     sda.sda_merge_states_bwd([q[0] for q in parts], [q[1] for q in parts], dO, None, 1, wl.N, wl.heads, wl.d, "bf16",
@@ -78,8 +78,10 @@ def run(device: int = 0) -> dict:
         sda.sda_attn_bwd_partition(p, Q, K, V, Op, Lp, g_o, g_l, idx_t, *part, "f32", wsb, kb_begin=b0, kb_end=b1)
         for acc, v in zip(total, part):
             acc += v
-    for name, got, ref in zip(("dQ", "dK", "dV"), total, gref):
-        assert_close_through_stored_states(host(got), ref, "bf16", "smoke merged-partition " + name)
+    assert orc.frame_partitions(geom, 2) == [(0, cut), (cut, nb)]
+    mref = orc.reuse_bwd(x["Q"], x["K"], x["V"], x["dO"], ref_idx, geom, 2, 0, None, state_dtype="bf16")
+    for name, got, ref in zip(("dQ", "dK", "dV"), total, mref):
+        assert_close(host(got), ref, "bf16", "smoke merged-partition " + name)
     st = sda.sda_get_device_status()
     assert st == sda.SDA_OK, sda.status_string(st)
     return {"selection": sel, "score_rel_err": float(s_err)}

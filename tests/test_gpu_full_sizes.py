@@ -1,20 +1,24 @@
 """GPU vs oracle parity at the five workloads' full sizes, in the launch configuration bench.py times.
 
-The CUDA path runs the whole problem; the fp64 oracle recomputes sampled
-outputs one query block (or key block) at a time.  Where a GPU call needs a
-full block map but the oracle only computes some rows, the GPU map's sampled
-rows are replaced by the oracle's own rows before the call, so every compared
-GPU output derives from oracle-selected blocks and no oracle input comes from
-the GPU.  The backward at 524K tokens runs on a seeded local block map shared by
-both sides (the oracle cannot produce the full map in test time); its unsampled
-rows are still checked through the exact sum invariants.
+The CUDA path runs the whole problem; the fp64 oracle recomputes sampled outputs, a batch of query blocks
+(or key blocks) at a time.  Where a GPU call needs a full block map but the oracle only computes some
+rows, the sampled rows come from the oracle's own predictor: for the forward the GPU map's sampled rows
+are replaced by them before the call; for the backward at 524K tokens (whose key-block sums need every
+row of the map) the other rows come from the seeded scattered map generator, whose rows are spread over
+the grid with heavy-tailed key-block popularity like the predictor's.  So every compared GPU output
+derives from oracle-selected (or seeded) blocks and no oracle input comes from the GPU.
+
+Each test adds its figures (rows compared, selection outcome including near-ties, max-abs and relative
+Frobenius error per output, oracle seconds and the sampled fraction) to the session's parity report.
 """
+import time
+
 import numpy as np
 import pytest
 
 import oracle as orc
 from dynamic_block_sparse_rank_gb300 import inputs
-from tests.parity_util import TOL, assert_close, check_scores, check_selection, dev, errors, host
+from tests.parity_util import assert_close, check_scores, check_selection, dev, errors, host
 
 pytestmark = pytest.mark.gpu
 
@@ -31,19 +35,57 @@ def sda():
     return s
 
 
+_INPUTS = {}
+
+
+def _inputs(wl, names):
+    """The workload's inputs, generated once per module for every name asked so far."""
+    have = _INPUTS.setdefault(wl.name, {})
+    missing = tuple(n for n in names if n not in have)
+    if missing:
+        have.update(inputs.generate(wl, names=missing))
+    return {n: have[n] for n in names}
+
+
 def _geom(wl):
     return orc.Geometry(wl.T, wl.H, wl.W, wl.bt, wl.bh, wl.bw)
 
 
-def _samples(wl, n, seed):
+def _samples(wl, n, seed, extra=()):
     rng = np.random.default_rng(seed)
     nb = wl.n_blocks
-    picks = {0, nb - 1, nb // 2} | set(int(x) for x in rng.choice(nb, n, replace=False))
+    picks = {0, nb - 1, nb // 2} | set(int(x) for x in rng.choice(nb, n, replace=False)) | set(extra)
     return sorted(picks)
 
 
 def _head(x, h):
     return {k: (v[:, :, h:h + 1] if v.ndim == 4 and k not in ("Wq", "Wk") else v[h:h + 1]) for k, v in x.items()}
+
+
+class _Record:
+    """One workload's entry of the parity report."""
+
+    def __init__(self, report, name, fraction_note):
+        self.e = report.setdefault(name, {"outputs": {}, "selection": {}, "oracle_seconds": 0.0,
+                                          "sampled": fraction_note})
+        self.t = 0.0
+
+    def oracle(self, fn, *a, **kw):
+        t0 = time.perf_counter()
+        out = fn(*a, **kw)
+        self.e["oracle_seconds"] += time.perf_counter() - t0
+        return out
+
+    def selection(self, st):
+        for k, v in st.items():
+            self.e["selection"][k] = self.e["selection"].get(k, 0) + int(v)
+
+    def close(self, got, ref, dtype, what, key):
+        mx, rel = assert_close(got, ref, dtype, what)
+        o = self.e["outputs"].setdefault(key, {"max_abs": 0.0, "rel_frob_max": 0.0, "values": 0})
+        o["max_abs"] = max(o["max_abs"], float(mx))
+        o["rel_frob_max"] = max(o["rel_frob_max"], float(rel))
+        o["values"] += int(np.size(ref))
 
 
 def _gpu_predict(sda, wl, Q, K, Wq, Wk, with_score=True):
@@ -57,47 +99,49 @@ def _gpu_predict(sda, wl, Q, K, Wq, Wk, with_score=True):
     return idx, sc
 
 
-def _check_predictor_and_forward(sda, wl, heads, n_blocks_sampled, seed=0):
-    x = inputs.generate(wl, names=("Q", "K", "V", "Wq", "Wk"))
+def _check_predictor_and_forward(sda, rec, wl, heads, qb):
+    """Predictor rows (gap rule) and forward rows of query blocks qb on every head in `heads`."""
+    x = _inputs(wl, ("Q", "K", "V", "Wq", "Wk"))
     geom = _geom(wl)
     Q, K, V, Wq, Wk = (dev(x[n], wl.dtype) for n in ("Q", "K", "V", "Wq", "Wk"))
     idx, sc = _gpu_predict(sda, wl, Q, K, Wq, Wk)
-    qb = _samples(wl, n_blocks_sampled, seed)
-    sel_stats = []
     ref_rows = {}
     for h in heads:
         xh = _head(x, h)
-        ridx, rsc = orc.predict_blocks(xh["Q"], xh["K"], xh["Wq"], xh["Wk"], geom, wl.keep, wl.dtype, query_blocks=qb)
-        gi = idx[0, h, qb].cpu().numpy()
-        st = check_selection(gi, rsc, wl.k)
+        ridx, rsc = rec.oracle(orc.predict_blocks, xh["Q"], xh["K"], xh["Wq"], xh["Wk"], geom, wl.keep, wl.dtype,
+                               query_blocks=qb)
+        st = check_selection(idx[0, h, qb].cpu().numpy(), rsc, wl.k)
+        rec.selection(st)
         assert st["fail"] == 0, (h, st)
-        sel_stats.append(st)
         check_scores(sc[0, h, qb].cpu().numpy().astype(np.float64), rsc)
         ref_rows[h] = ridx
         idx[0, h, qb] = torch.from_numpy(ridx[0, 0]).cuda()  # compared rows use the oracle's selection
+    del sc
     p = sda.problem_from_workload(wl)
     O = torch.empty_like(Q)
     LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
     sda.sda_attn_fwd(p, Q, K, V, idx, O, LSE)
     torch.cuda.synchronize()
+    rows = np.concatenate([geom.tokens(I) for I in qb])
     for h in heads:
         xh = _head(x, h)
-        Or, Lr = orc.attn_fwd(xh["Q"], xh["K"], xh["V"], ref_rows[h], geom, query_blocks=qb)
-        rows = np.concatenate([geom.tokens(I) for I in qb])
-        assert_close(host(O[0, rows, h]), Or[0, rows, 0], wl.dtype, f"O head {h}")
-        assert_close(host(LSE[0, h, rows]), Lr[0, 0, rows], wl.dtype, f"LSE head {h}")
+        Or, Lr = rec.oracle(orc.attn_fwd, xh["Q"], xh["K"], xh["V"], ref_rows[h], geom, query_blocks=qb)
+        rec.close(host(O[0, rows, h]), Or[0, rows, 0], wl.dtype, f"O head {h}", "O")
+        rec.close(host(LSE[0, h, rows]), Lr[0, 0, rows], wl.dtype, f"LSE head {h}", "LSE")
     assert sda.sda_get_device_status() == sda.SDA_OK
-    return sel_stats
 
 
-def test_fwd_8k_full_oracle(sda):
+def test_fwd_8k_full_oracle(sda, parity_report):
+    """The 8,192-token workload in full: every head, every query block."""
     wl = inputs.WORKLOADS["fwd_8k"]
-    x = inputs.generate(wl, names=("Q", "K", "V", "Wq", "Wk"))
+    rec = _Record(parity_report, wl.name, "all 12 heads x all 64 query blocks (fraction 1.0)")
+    x = _inputs(wl, ("Q", "K", "V", "Wq", "Wk"))
     geom = _geom(wl)
     Q, K, V, Wq, Wk = (dev(x[n], wl.dtype) for n in ("Q", "K", "V", "Wq", "Wk"))
     idx, sc = _gpu_predict(sda, wl, Q, K, Wq, Wk)
-    ridx, rsc = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    ridx, rsc = rec.oracle(orc.predict_blocks, x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
     st = check_selection(idx.cpu().numpy(), rsc, wl.k)
+    rec.selection(st)
     assert st["fail"] == 0, st
     check_scores(host(sc), rsc)
     p = sda.problem_from_workload(wl)
@@ -105,24 +149,50 @@ def test_fwd_8k_full_oracle(sda):
     LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
     sda.sda_attn_fwd(p, Q, K, V, torch.from_numpy(ridx).cuda(), O, LSE)
     torch.cuda.synchronize()
-    Or, Lr = orc.attn_fwd(x["Q"], x["K"], x["V"], ridx, geom)
-    assert_close(host(O), Or, "bf16", "O")
-    assert_close(host(LSE), Lr, "bf16", "LSE")
+    Or, Lr = rec.oracle(orc.attn_fwd, x["Q"], x["K"], x["V"], ridx, geom)
+    rec.close(host(O), Or, "bf16", "O", "O")
+    rec.close(host(LSE), Lr, "bf16", "LSE", "LSE")
 
 
-def test_fwd_61k_sampled(sda):
-    _check_predictor_and_forward(sda, inputs.WORKLOADS["fwd_61k"], heads=[0, 13, 23], n_blocks_sampled=5)
+def test_fwd_61k_every_head_sampled(sda, parity_report):
+    """61,440 tokens: all 24 heads, 48 seeded query blocks each plus the first, middle and last."""
+    wl = inputs.WORKLOADS["fwd_61k"]
+    qb = _samples(wl, 48, 3)
+    rec = _Record(parity_report, wl.name, f"all 24 heads x {len(qb)} of 480 query blocks "
+                                          f"(fraction {len(qb) / 480:.3f})")
+    _check_predictor_and_forward(sda, rec, wl, list(range(wl.heads)), qb)
 
 
-def test_train_524k_predictor_and_forward_sampled(sda):
-    _check_predictor_and_forward(sda, inputs.WORKLOADS["train_524k"], heads=[0, 5], n_blocks_sampled=3)
-
-
-def test_train_524k_backward_sampled(sda):
+def test_train_524k_predictor_and_forward_sampled(sda, parity_report):
+    """524,288 tokens: 3 of 8 heads, 16 seeded query blocks each plus the first, middle and last."""
     wl = inputs.WORKLOADS["train_524k"]
-    x = inputs.generate(wl, names=("Q", "K", "V", "dO"))
+    qb = _samples(wl, 16, 4)
+    rec = _Record(parity_report, wl.name + " predictor+forward",
+                  f"heads 0, 3, 6 x {len(qb)} of 4096 query blocks (fraction {3 * len(qb) / (8 * 4096):.4f})")
+    _check_predictor_and_forward(sda, rec, wl, [0, 3, 6], qb)
+
+
+def test_train_524k_backward_on_predictor_rows(sda, parity_report):
+    """The backward at 524,288 tokens, as bench.py runs it (fp32 gradients).  The map: for heads 1 and 6,
+    16 seeded query blocks (plus first, middle, last) keep the oracle predictor's own rows; every other
+    row comes from the seeded scattered generator.  Checked: dQ of those query blocks; dK and dV of 8 key
+    blocks per head, among them the key block with the shortest list of query blocks (both heads) and
+    with the longest (head 1); the forward's rows; and, on every row of every head, the exact sums
+    sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i."""
+    wl = inputs.WORKLOADS["train_524k"]
+    x = _inputs(wl, ("Q", "K", "V", "dO", "Wq", "Wk"))
     geom = _geom(wl)
-    m = inputs.local_block_map(wl, seed=1)
+    heads = [1, 6]
+    qb = _samples(wl, 16, 6)
+    rec = _Record(parity_report, wl.name + " backward",
+                  f"heads 1, 6: dQ of {len(qb)} query blocks and dK/dV of 8 key blocks per head, on a map whose "
+                  f"sampled rows are the oracle predictor's; all rows of all heads through the exact sums")
+    m = inputs.scattered_block_map(wl, seed=1)
+    for h in heads:
+        xh = _head(x, h)
+        ridx, _ = rec.oracle(orc.predict_blocks, xh["Q"], xh["K"], xh["Wq"], xh["Wk"], geom, wl.keep, wl.dtype,
+                             query_blocks=qb)
+        m[0, h, qb] = ridx[0, 0]
     p = sda.problem_from_workload(wl)
     Q, K, V, dO = (dev(x[n], wl.dtype) for n in ("Q", "K", "V", "dO"))
     idx = torch.from_numpy(m).cuda()
@@ -133,81 +203,113 @@ def test_train_524k_backward_sampled(sda):
     ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device="cuda")
     sda.sda_attn_bwd(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, "f32", ws)
     torch.cuda.synchronize()
+    del ws
     assert sda.sda_get_device_status() == sda.SDA_OK
     # exact invariants over every row of every head: sum_j dK_j = 0, sum_j dV_j = sum_i dO_i
     sk = dK.double().sum(dim=1)
     sv = dV.double().sum(dim=1) - dO.double().sum(dim=1)
-    scale_k = dK.double().abs().sum(dim=1)
-    scale_v = dV.double().abs().sum(dim=1)
-    assert float((sk.abs() / scale_k).max()) < 1e-4
-    assert float((sv.abs() / scale_v).max()) < 1e-4
-    # sampled rows against the oracle (head 0): dQ of three query blocks, dK/dV of two key blocks
-    h = 0
-    xh = _head(x, h)
-    mh = m[:, h:h + 1]
-    qbs = _samples(wl, 0, 3)[:3]
-    fan_in = np.bincount(m[0, h].ravel(), minlength=geom.n_blocks)
-    kbs = [int(np.argmax(fan_in)), geom.n_blocks // 3]
-    dq_ref, dkv_ref = orc.attn_bwd_blocks(xh["Q"], xh["K"], xh["V"], xh["dO"], mh, geom, query_blocks=qbs,
-                                          key_blocks=kbs)
-    for (_, _, I), ref in dq_ref.items():
-        assert_close(host(dQ[0, geom.tokens(I), h]), ref, "bf16", f"dQ block {I}")
-    for (_, _, J), (rk, rv) in dkv_ref.items():
-        assert_close(host(dK[0, geom.tokens(J), h]), rk, "bf16", f"dK block {J}")
-        assert_close(host(dV[0, geom.tokens(J), h]), rv, "bf16", f"dV block {J}")
-    # forward on the shared map, sampled rows
-    Or, Lr = orc.attn_fwd(xh["Q"], xh["K"], xh["V"], mh[:, :, qbs], geom, query_blocks=qbs)
-    rows = np.concatenate([geom.tokens(I) for I in qbs])
-    assert_close(host(O[0, rows, h]), Or[0, rows, 0], "bf16", "O")
-    assert_close(host(LSE[0, h, rows]), Lr[0, 0, rows], "bf16", "LSE")
+    assert float((sk.abs() / dK.double().abs().sum(dim=1)).max()) < 1e-4
+    assert float((sv.abs() / dV.double().abs().sum(dim=1)).max()) < 1e-4
+    rng = np.random.default_rng(7)
+    rows = np.concatenate([geom.tokens(I) for I in qb])
+    lengths = {}
+    for h in heads:
+        xh = _head(x, h)
+        mh = m[:, h:h + 1]
+        fan_in = np.bincount(m[0, h].ravel(), minlength=geom.n_blocks)
+        order = np.argsort(fan_in, kind="stable")
+        picks = [int(order[0])]  # the shortest list
+        if h == heads[0]:
+            picks.append(int(order[-1]))  # the longest list
+        in_oracle_rows = sorted(set(int(J) for J in m[0, h, qb].ravel()) - set(picks))
+        picks += [int(J) for J in rng.choice(in_oracle_rows, 2, replace=False)]
+        short_half = [int(J) for J in order[1:geom.n_blocks // 2] if int(J) not in picks]
+        picks += [int(J) for J in rng.choice(short_half, 8 - len(picks), replace=False)]
+        lengths[h] = sorted(int(fan_in[J]) for J in picks)
+        dq_ref, dkv_ref = rec.oracle(orc.attn_bwd_blocks, xh["Q"], xh["K"], xh["V"], xh["dO"], mh, geom,
+                                     query_blocks=qb, key_blocks=picks)
+        for (_, _, I), ref in dq_ref.items():
+            rec.close(host(dQ[0, geom.tokens(I), h]), ref, "bf16", f"dQ h{h} block {I}", "dQ")
+        for (_, _, J), (rk, rv) in dkv_ref.items():
+            rec.close(host(dK[0, geom.tokens(J), h]), rk, "bf16", f"dK h{h} block {J}", "dK")
+            rec.close(host(dV[0, geom.tokens(J), h]), rv, "bf16", f"dV h{h} block {J}", "dV")
+        Or, Lr = rec.oracle(orc.attn_fwd, xh["Q"], xh["K"], xh["V"], mh[:, :, qb], geom, query_blocks=qb)
+        rec.close(host(O[0, rows, h]), Or[0, rows, 0], "bf16", f"O h{h}", "O")
+        rec.close(host(LSE[0, h, rows]), Lr[0, 0, rows], "bf16", f"LSE h{h}", "LSE")
+    rec.e["key_block_list_lengths"] = {str(h): v for h, v in lengths.items()}
 
 
-def test_merge_131k_partition_states_and_reuse_sampled(sda):
+def _tile_classes(geom):
+    """Query blocks grouped by their clipped extent (t, h, w) on a non-divisible grid."""
+    classes = {}
+    for I in range(geom.n_blocks):
+        it, ih, iw = geom.block_coords(I)
+        ext = (min(geom.bt, geom.T - it * geom.bt), min(geom.bh, geom.H - ih * geom.bh),
+               min(geom.bw, geom.W - iw * geom.bw))
+        classes.setdefault(ext, []).append(I)
+    return classes
+
+
+def test_merge_131k_partition_states_and_reuse_every_head(sda, parity_report):
+    """131,040 tokens on a ragged grid, 4 frame partitions, the 2 farthest reused from the previous step:
+    all 16 heads, each on 8 seeded query blocks plus one block of every clipped-tile class (full 2x8x8,
+    1x8x8, 2x4x8, 1x4x8) and the last block of partition 0's reuse set.  Checked per head: the selection
+    of both steps (gap rule), every partition state the GPU keeps (reused or fresh), the reuse merge, the
+    exact merge of fresh states, and the full-range forward; the reuse merge's deviation from the exact
+    merge is reported, not graded."""
     wl = inputs.WORKLOADS["merge_131k"]
-    x = inputs.generate(wl, names=("Q", "K", "V", "Qp", "Kp", "Vp", "Wq", "Wk"))
+    x = _inputs(wl, ("Q", "K", "V", "Qp", "Kp", "Vp", "Wq", "Wk"))
     geom = _geom(wl)
     P = wl.partitions
     bounds = orc.frame_partitions(geom, P)
     reuse = orc.reuse_mask(geom, P, wl.n_reuse)
+    classes = _tile_classes(geom)
+    assert len(classes) == 4, sorted(classes)
+    rng = np.random.default_rng(5)
+    extra = [int(rng.choice(v)) for v in classes.values()] + [int(np.flatnonzero(reuse[0])[-1])]
+    qb = _samples(wl, 8, 5, extra)
+    heads = list(range(wl.heads))
+    rec = _Record(parity_report, wl.name, f"all 16 heads x {len(qb)} of 1144 query blocks (every clipped-tile "
+                                          f"class) x 4 partition states, both steps (fraction {len(qb) / 1144:.3f})")
     p = sda.problem_from_workload(wl)
     T = {n: dev(x[n], wl.dtype) for n in ("Q", "K", "V", "Qp", "Kp", "Vp", "Wq", "Wk")}
-    heads = [0, 9]
-    qb = _samples(wl, 4, 5) + [int(np.flatnonzero(reuse[0])[-1])]  # includes ragged edge tiles
-    qb = sorted(set(qb))
 
     def gpu_map(Qn, Kn):
         idx, _ = _gpu_predict(sda, wl, T[Qn], T[Kn], T["Wq"], T["Wk"], with_score=False)
         rows = {}
         for h in heads:
             xh = _head(x, h)
-            r, sc = orc.predict_blocks(xh[Qn], xh[Kn], xh["Wq"], xh["Wk"], geom, wl.keep, wl.dtype, query_blocks=qb)
+            r, sc = rec.oracle(orc.predict_blocks, xh[Qn], xh[Kn], xh["Wq"], xh["Wk"], geom, wl.keep, wl.dtype,
+                               query_blocks=qb)
             st = check_selection(idx[0, h, qb].cpu().numpy(), sc, wl.k)
+            rec.selection(st)
             assert st["fail"] == 0, (Qn, h, st)
             idx[0, h, qb] = torch.from_numpy(r[0, 0]).cuda()
             rows[h] = r
         return idx, rows
 
+    def new_state():
+        return torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+
     idx_prev, rows_prev = gpu_map("Qp", "Kp")
     idx_now, rows_now = gpu_map("Q", "K")
     # previous step: every partition state for every query block (the reuse cache)
-    states = [(torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda"))
-              for _ in range(P)]
+    states = [new_state() for _ in range(P)]
     for (b0, b1), (Op, Lp) in zip(bounds, states):
         sda.sda_attn_fwd(p, T["Qp"], T["Kp"], T["Vp"], idx_prev, Op, Lp, kb_begin=b0, kb_end=b1)
     # current step: recompute the near partitions only, in place
     for q, ((b0, b1), (Op, Lp)) in enumerate(zip(bounds, states)):
         act = torch.from_numpy((~reuse[q]).astype(np.uint8)).cuda()
         sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Op, Lp, kb_begin=b0, kb_end=b1, qb_active=act)
-    Om, Lm = torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    Om, Lm = new_state()
     sda.sda_merge_states([s[0] for s in states], [s[1] for s in states], 1, wl.N, wl.heads, wl.d, "bf16", Om, Lm)
     # exact merge of fresh states equals the full-range forward
-    fresh = [(torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda"))
-             for _ in range(P)]
+    fresh = [new_state() for _ in range(P)]
     for (b0, b1), (Op, Lp) in zip(bounds, fresh):
         sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Op, Lp, kb_begin=b0, kb_end=b1)
-    Oe, Le = torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    Oe, Le = new_state()
     sda.sda_merge_states([s[0] for s in fresh], [s[1] for s in fresh], 1, wl.N, wl.heads, wl.d, "bf16", Oe, Le)
-    Of, Lf = torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    Of, Lf = new_state()
     sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Of, Lf)
     torch.cuda.synchronize()
     assert sda.sda_get_device_status() == sda.SDA_OK
@@ -217,8 +319,10 @@ def test_merge_131k_partition_states_and_reuse_sampled(sda):
         xh = _head(x, h)
         ref_states = []
         for q, (b0, b1) in enumerate(bounds):
-            prev = orc.attn_fwd(xh["Qp"], xh["Kp"], xh["Vp"], rows_prev[h], geom, kb_begin=b0, kb_end=b1, query_blocks=qb)
-            now = orc.attn_fwd(xh["Q"], xh["K"], xh["V"], rows_now[h], geom, kb_begin=b0, kb_end=b1, query_blocks=qb)
+            prev = rec.oracle(orc.attn_fwd, xh["Qp"], xh["Kp"], xh["Vp"], rows_prev[h], geom, kb_begin=b0, kb_end=b1,
+                              query_blocks=qb)
+            now = rec.oracle(orc.attn_fwd, xh["Q"], xh["K"], xh["V"], rows_now[h], geom, kb_begin=b0, kb_end=b1,
+                             query_blocks=qb)
             O_q, L_q = now[0].copy(), now[1].copy()
             for I in qb:
                 if reuse[q, I]:
@@ -227,17 +331,17 @@ def test_merge_131k_partition_states_and_reuse_sampled(sda):
                     L_q[:, :, t] = prev[1][:, :, t]
             ref_states.append((O_q[0, rows, 0], L_q[0, 0, rows], now[0][0, rows, 0], now[1][0, 0, rows]))
             # each state the GPU keeps equals the oracle's (reused or fresh)
-            assert_close(host(states[q][0][0, rows, h]), ref_states[-1][0], "bf16", f"state O p{q} h{h}")
-            assert_close(host(states[q][1][0, h, rows]), ref_states[-1][1], "bf16", f"state LSE p{q} h{h}")
+            rec.close(host(states[q][0][0, rows, h]), ref_states[-1][0], "bf16", f"state O p{q} h{h}", "state O")
+            rec.close(host(states[q][1][0, h, rows]), ref_states[-1][1], "bf16", f"state LSE p{q} h{h}", "state LSE")
         Ro, Rl = orc.merge_states([s[0] for s in ref_states], [s[1] for s in ref_states])
-        assert_close(host(Om[0, rows, h]), Ro, "bf16", f"reuse-merged O h{h}")
-        assert_close(host(Lm[0, h, rows]), Rl, "bf16", f"reuse-merged LSE h{h}")
+        rec.close(host(Om[0, rows, h]), Ro, "bf16", f"reuse-merged O h{h}", "reuse-merged O")
+        rec.close(host(Lm[0, h, rows]), Rl, "bf16", f"reuse-merged LSE h{h}", "reuse-merged LSE")
         Eo, El = orc.merge_states([s[2] for s in ref_states], [s[3] for s in ref_states])
-        assert_close(host(Oe[0, rows, h]), Eo, "bf16", f"exact-merged O h{h}")
-        assert_close(host(Le[0, h, rows]), El, "bf16", f"exact-merged LSE h{h}")
-        Fo, Fl = orc.attn_fwd(xh["Q"], xh["K"], xh["V"], rows_now[h], geom, query_blocks=qb)
-        assert_close(host(Of[0, rows, h]), Fo[0, rows, 0], "bf16", f"full-range O h{h}")
+        rec.close(host(Oe[0, rows, h]), Eo, "bf16", f"exact-merged O h{h}", "exact-merged O")
+        rec.close(host(Le[0, h, rows]), El, "bf16", f"exact-merged LSE h{h}", "exact-merged LSE")
+        Fo, Fl = rec.oracle(orc.attn_fwd, xh["Q"], xh["K"], xh["V"], rows_now[h], geom, query_blocks=qb)
+        rec.close(host(Of[0, rows, h]), Fo[0, rows, 0], "bf16", f"full-range O h{h}", "full-range O")
         assert_close(Eo, Fo[0, rows, 0], "bf16", "oracle: merge of partitions equals the union")
         deviation.append(errors(Ro, Eo))
     # the reuse approximation's deviation from the exact merge is reported, not graded
-    print("reuse vs exact merge (max-abs, rel-frob) per sampled head:", deviation)
+    rec.e["reuse_vs_exact_merge_max_abs_rel_frob"] = [max(d[0] for d in deviation), max(d[1] for d in deviation)]

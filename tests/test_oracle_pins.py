@@ -628,6 +628,31 @@ def test_reuse_backward_finite_differences():
     assert np.abs(dK).max() > 0 and np.abs(dV).max() > 0
 
 
+def test_reuse_backward_reads_fresh_states_as_stored():
+    """Reading 9: a bf16 problem's fresh O_p enters the merge's backward rounded to bf16.  Special case: with
+    one-token blocks and one kept key block per query block, each fresh state is a single v_j, which is
+    already a bf16 value when V is, so the rounding changes nothing.  With several keys per state O_p is an
+    average that bf16 cannot hold; the gradient then moves, by no more than the rounding's first-order effect
+    (states move by 2^-9 relative, so gradients by a few 2^-9 of their scale)."""
+    geom = orc.Geometry(4, 1, 4, 1, 1, 1)  # one-token blocks, 4 slabs of 4
+    B, Hh, d, P, n_reuse = 1, 1, 4, 4, 2
+    Q, K, dO = (_rand((B, geom.N, Hh, d), s) for s in (150, 151, 152))
+    V = orc.to_bf16(_rand((B, geom.N, Hh, d), 153))
+    idx = _random_map(geom, B, Hh, 1, 154)
+    prev = orc.partition_states(Q + 0.1, K, V, _random_map(geom, B, Hh, 1, 155), geom, P)
+    plain = orc.reuse_bwd(Q, K, V, dO, idx, geom, P, n_reuse, prev)
+    stored = orc.reuse_bwd(Q, K, V, dO, idx, geom, P, n_reuse, prev, state_dtype="bf16")
+    for a, b in zip(plain, stored):
+        assert np.array_equal(a, b)
+    V2 = _rand((B, geom.N, Hh, d), 156)
+    idx3 = _random_map(geom, B, Hh, 6, 157)
+    plain = orc.reuse_bwd(Q, K, V2, dO, idx3, geom, P, n_reuse, prev)
+    stored = orc.reuse_bwd(Q, K, V2, dO, idx3, geom, P, n_reuse, prev, state_dtype="bf16")
+    diffs = [np.abs(a - b).max() for a, b in zip(plain, stored)]
+    scale = max(np.abs(x).max() for x in plain + stored)
+    assert max(diffs) > 0 and max(diffs) < 8 * 2.0 ** -9 * scale, (diffs, scale)
+
+
 # ------------------------------------------------------------------ predictor training signal
 def _distill_case(seed, dims=(2, 4, 4, 1, 2, 2), d=5, r=3, Hh=2):
     geom = orc.Geometry(*dims)
