@@ -55,8 +55,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # An entry goes back to None whenever its kernel changes, until it is captured again.
 NCU_COUNTERS = {
     "score_kernel": {"dram_bytes": 0.583e9 + 0.105e9, "tensor_active": 0.429},
-    "fwd_tc_kernel": {"dram_bytes": 58.465e9 + 2.501e9, "tensor_active": 0.518},
-    "dq_kernel": {"dram_bytes": 167.622e9 + 2.165e9, "tensor_active": 0.57},
+    "fwd_tc_kernel": None,
+    "dqx_kernel": None,
     "dkdv_kernel": {"dram_bytes": 143.499e9 + 4.275e9, "tensor_active": 0.55},
 }
 
@@ -307,7 +307,7 @@ def main():
     LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device=dev)
     dQ, dK, dV = (torch.empty(Q.shape, dtype=torch.float32, device=dev) for _ in range(3))
     ws_p = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICT), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device=dev)
+    ws_t = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_TRAIN), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     main_set = dict(Q=Q, K=K, V=V, dO=dO, Wq=Wq, Wk=Wk, dQ=dQ, dK=dK, dV=dV)
@@ -319,18 +319,14 @@ def main():
         sda.sda_predict_blocks(p, b["Q"], b["K"], b["Wq"], b["Wk"], idx, None, ws_p, stream)
         if ev is not None:
             ev[1].record(stream)
-        sda.sda_attn_fwd(p, b["Q"], b["K"], b["V"], idx, O, LSE, stream=stream)
+        sda.sda_attn_fwd_train(p, b["Q"], b["K"], b["V"], idx, O, LSE, ws_t, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        sda.sda_attn_bwd_prepare(p, b["Q"], b["K"], b["V"], O, LSE, b["dO"], idx, ws_b, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        sda.sda_attn_bwd_dq(p, b["Q"], b["K"], b["V"], LSE, b["dO"], idx, b["dQ"], "f32", ws_b, stream)
-        if ev is not None:
-            ev[4].record(stream)
-        sda.sda_attn_bwd_dkdv(p, b["Q"], b["K"], b["V"], LSE, b["dO"], idx, b["dK"], b["dV"], "f32", ws_b, stream)
-        if ev is not None:
-            ev[5].record(stream)
+        for i, ph in enumerate((1, 2, 4)):  # prepare, dQ, dK/dV: one call each so every phase is timed
+            sda.sda_attn_bwd_train(p, LSE, b["dO"], idx, b["dQ"], b["dK"], b["dV"], "f32", ws_t, phases=ph,
+                                   stream=stream)
+            if ev is not None:
+                ev[3 + i].record(stream)
 
     def barrier():
         if dist is not None:
@@ -491,15 +487,15 @@ def main():
     tc_peak = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm_peak = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     # algorithmic FLOPs per launch: predictor 2 r per token pair (all pairs of a head), forward 4 d and
-    # dK/dV 8 d per kept pair, dQ 2 d per kept pair (its S, dP and P K products are recomputation)
+    # dK/dV 8 d per kept pair, dQ 2 d per kept pair (its S and dP products are recomputation)
     f_pred = 2.0 * wl.rank * wl.B * wl.heads * float(wl.N) ** 2
     kern = {"predict (score_kernel; phase incl. 2 proj_kernel)": (phase_ms["predict"], f_pred),
-            "attn_fwd (fwd_tc_kernel)": (phase_ms["fwd"], f_fwd),
-            "attn_bwd_dkdv (dkdv_kernel)": (phase_ms["bwd_dkdv"], f_dkdv),
-            "attn_bwd_dq (dq_kernel)": (phase_ms["bwd_dq"], f_dq)}
+            "attn_fwd_train (fwd_tc_kernel; phase incl. 3 fp16 copies)": (phase_ms["fwd"], f_fwd),
+            "attn_bwd_train dK/dV (dkdv_kernel)": (phase_ms["bwd_dkdv"], f_dkdv),
+            "attn_bwd_train dQ (dqx_kernel)": (phase_ms["bwd_dq"], f_dq)}
     dom = max(kern, key=lambda n: kern[n][0])
     dom_ms, dom_flops = kern[dom]
-    counters = next((v for key, v in NCU_COUNTERS.items() if key in dom), None)
+    counters = next((v for key, v in NCU_COUNTERS.items() if key in dom and v), None)
     achieved = dom_flops / (dom_ms / 1e3) / 1e12
     burst_peak = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     clocks = clk.summary()

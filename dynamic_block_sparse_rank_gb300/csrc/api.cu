@@ -117,7 +117,10 @@ sda_status sda_workspace_size(const sda_problem* p, int op, size_t* bytes) {
     *bytes = q.dtype == SDA_BF16 ? predict_ws_tc(q) : predict_ws_f32(q);
   else if (op == SDA_OP_BWD)
     *bytes = q.dtype == SDA_BF16 ? bwd_ws_tc(q) : bwd_ws_f32(q);
-  else
+  else if (op == SDA_OP_TRAIN) {
+    if (q.dtype != SDA_BF16) return SDA_ERR_UNSUPPORTED;
+    *bytes = train_ws_tc(q);
+  } else
     return SDA_ERR_INVALID_ARG;
   return SDA_OK;
 }
@@ -143,17 +146,19 @@ sda_status sda_predict_blocks(const sda_problem* p, const void* Q, const void* K
 }
 
 sda_status sda_attn_fwd(const sda_problem* p, const void* Q, const void* K, const void* V, const int32_t* block_idx,
-                        int kb_begin, int kb_end, const uint8_t* qb_active, void* O, float* LSE, void* stream) {
+                        int kb_begin, int kb_end, const uint8_t* qb_active, void* O, float* LSE, int out_dtype,
+                        void* stream) {
   Prob q;
   sda_status s = make_prob(p, &q);
   if (s != SDA_OK) return s;
   if (!Q || !K || !V || !block_idx || !O || !LSE) return SDA_ERR_INVALID_ARG;
   if (kb_begin < 0 || kb_end < kb_begin || kb_end > q.g.nb) return SDA_ERR_INVALID_ARG;
+  if (out_dtype != SDA_F32 && out_dtype != q.dtype) return SDA_ERR_INVALID_ARG;
   if ((s = check_supported(q)) != SDA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (q.dtype == SDA_BF16) {
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SDA_ERR_INVALID_ARG;
-    return from_cuda(fwd_tc(q, Q, K, V, block_idx, kb_begin, kb_end, qb_active, O, LSE, st));
+    return from_cuda(fwd_tc(q, Q, K, V, block_idx, kb_begin, kb_end, qb_active, O, out_dtype == SDA_F32, LSE, st));
   }
   return from_cuda(fwd_f32(q, static_cast<const float*>(Q), static_cast<const float*>(K),
                            static_cast<const float*>(V), block_idx, kb_begin, kb_end, qb_active,
@@ -236,6 +241,39 @@ sda_status sda_attn_bwd(const sda_problem* p, const void* Q, const void* K, cons
   if ((s = sda_attn_bwd_dq(p, Q, K, V, LSE, dO, block_idx, dQ, grad_dtype, ws, ws_bytes, stream)) != SDA_OK)
     return s;
   return sda_attn_bwd_dkdv(p, Q, K, V, LSE, dO, block_idx, dK, dV, grad_dtype, ws, ws_bytes, stream);
+}
+
+sda_status sda_attn_fwd_train(const sda_problem* p, const void* Q, const void* K, const void* V,
+                              const int32_t* block_idx, void* O, float* LSE, void* ws, size_t ws_bytes,
+                              void* stream) {
+  Prob q;
+  sda_status s = make_prob(p, &q);
+  if (s != SDA_OK) return s;
+  if (!Q || !K || !V || !block_idx || !O || !LSE || !ws) return SDA_ERR_INVALID_ARG;
+  if ((s = check_supported(q)) != SDA_OK) return s;
+  if (q.dtype != SDA_BF16) return SDA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(ws)) return SDA_ERR_INVALID_ARG;
+  if (ws_bytes < train_ws_tc(q)) return SDA_ERR_WORKSPACE;
+  return from_cuda(fwd_train_tc(q, Q, K, V, block_idx, O, LSE, ws, static_cast<cudaStream_t>(stream)));
+}
+
+sda_status sda_attn_bwd_train(const sda_problem* p, const float* LSE, const void* dO, const int32_t* block_idx,
+                              void* dQ, void* dK, void* dV, int grad_dtype, int phases, void* ws, size_t ws_bytes,
+                              void* stream) {
+  Prob q;
+  sda_status s = make_prob(p, &q);
+  if (s != SDA_OK) return s;
+  if (!LSE || !dO || !block_idx || !ws) return SDA_ERR_INVALID_ARG;
+  if (phases < 1 || phases > 7) return SDA_ERR_INVALID_ARG;
+  if (((phases & 2) && !dQ) || ((phases & 4) && (!dK || !dV))) return SDA_ERR_INVALID_ARG;
+  if ((s = check_supported(q)) != SDA_OK) return s;
+  if (q.dtype != SDA_BF16) return SDA_ERR_UNSUPPORTED;
+  if (grad_dtype != SDA_F32 && grad_dtype != q.dtype) return SDA_ERR_INVALID_ARG;
+  if (!aligned16(dO) || !aligned16(ws) || (dQ && !aligned16(dQ)) || (dK && !aligned16(dK)) || (dV && !aligned16(dV)))
+    return SDA_ERR_INVALID_ARG;
+  if (ws_bytes < train_ws_tc(q)) return SDA_ERR_WORKSPACE;
+  return from_cuda(bwd_train_tc(q, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, phases,
+                                static_cast<cudaStream_t>(stream)));
 }
 
 sda_status sda_attn_bwd_partition(const sda_problem* p, const void* Q, const void* K, const void* V, const void* O,

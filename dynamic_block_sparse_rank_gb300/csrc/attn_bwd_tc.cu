@@ -66,9 +66,10 @@ __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ preprocess
 // D~_i = dO_i . O_i - dLSE_i (dLSE of a partition state's backward, else 0) and
-// LSE_i log2(e) in tile order; G receives dLSE_i in tile order when given.
-template <int D>
-__global__ void __launch_bounds__(128) pre_kernel(Geom g, int Hh, long long N, int b, const __nv_bfloat16* __restrict__ O,
+// LSE_i log2(e) in tile order; G receives dLSE_i in tile order when given.  O is the
+// stored bf16 output, or (kO32) the training forward's fp32 copy of it.
+template <int D, bool kO32>
+__global__ void __launch_bounds__(128) pre_kernel(Geom g, int Hh, long long N, int b, const void* __restrict__ O,
                                                   const __nv_bfloat16* __restrict__ dO, const float* __restrict__ LSE,
                                                   const float* __restrict__ dLSE, float* __restrict__ Dv,
                                                   float* __restrict__ L2v, float* __restrict__ G) {
@@ -76,16 +77,31 @@ __global__ void __launch_bounds__(128) pre_kernel(Geom g, int Hh, long long N, i
   const int n = block_row_token(g, I, r);
   float dsum = 0.f, l2 = INFINITY, gl = 0.f;
   if (n >= 0) {
-    const uint4* o = reinterpret_cast<const uint4*>(O + (((long long)b * N + n) * Hh + h) * D);
-    const uint4* go = reinterpret_cast<const uint4*>(dO + (((long long)b * N + n) * Hh + h) * D);
+    const long long row = ((long long)b * N + n) * Hh + h;
+    const uint4* go = reinterpret_cast<const uint4*>(dO + row * D);
 #pragma unroll 4
     for (int v = 0; v < D / 8; ++v) {
-      const uint4 a = o[v], c = go[v];
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+      const uint4 c = go[v];
+      const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+      float ov[8];
+      if (kO32) {
+        const float4* o = reinterpret_cast<const float4*>(static_cast<const float*>(O) + row * D) + 2 * v;
+        const float4 a0 = o[0], a1 = o[1];
+        ov[0] = a0.x, ov[1] = a0.y, ov[2] = a0.z, ov[3] = a0.w, ov[4] = a1.x, ov[5] = a1.y, ov[6] = a1.z,
+        ov[7] = a1.w;
+      } else {
+        const uint4 a = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(O) + row * D)[v];
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          ov[2 * q] = __uint_as_float(aw[q] << 16);
+          ov[2 * q + 1] = __uint_as_float(aw[q] & 0xFFFF0000u);
+        }
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        dsum = fmaf(__uint_as_float(aw[q] << 16), __uint_as_float(cw[q] << 16), dsum);
-        dsum = fmaf(__uint_as_float(aw[q] & 0xFFFF0000u), __uint_as_float(cw[q] & 0xFFFF0000u), dsum);
+        dsum = fmaf(ov[2 * q], __uint_as_float(cw[q] << 16), dsum);
+        dsum = fmaf(ov[2 * q + 1], __uint_as_float(cw[q] & 0xFFFF0000u), dsum);
       }
     }
     const float lse = LSE[((long long)b * Hh + h) * N + n];
@@ -559,6 +575,250 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ dQ with the exact D (training pair)
+// After the training forward, which kept O in fp32 with P rounded to fp16, D_i = dO_i . O_i
+// (prepare) is exact to well within the tolerance, so dS = P o (dP - D) needs no correction
+// and each block takes three products (S, dP, dQ) instead of four.  Q and dO are copied into
+// TMEM once and serve as the A operand of S = Q K^T and dP = dO V^T: those 64-key half
+// products then read only their B tile from shared memory and run at the tensor pipe's
+// full rate.  TMEM: S [0,128), dP [128,256), dQ [256,256+D), Q [256+D,256+3D/2),
+// dO [256+3D/2,256+2D) (A-operand layout: row = lane, elements 2c and 2c+1 in column c).
+template <int D, bool F32OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    dqx_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+               const __grid_constant__ CUtensorMap tmdQ, BwdArgs a) {
+  using C = Cfg<D>;
+  constexpr int KST = C::KST, VST = C::VST;
+  const int I = blockIdx.x, h = blockIdx.y;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sdO = sQ + C::TILE;
+  uint8_t* sK = sdO + C::TILE;        // KST tiles
+  uint8_t* sV = sK + KST * C::TILE;   // VST tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VST * C::TILE);
+  uint64_t* qfull = bars;
+  uint64_t* kvfull = qfull + 1;       // KST: K_j and V_j of block j landed (index j mod KST)
+  uint64_t* kempty = kvfull + KST;    // KST
+  uint64_t* vempty = kempty + KST;    // VST
+  uint64_t* sdpfull = vempty + VST;   // 2: S/dP columns of half h are ready
+  uint64_t* dsfull = sdpfull + 2;     // 2: packed dS of half h is written
+  uint64_t* qtmem = dsfull + 2;       // 1: Q and dO are in TMEM
+  uint64_t* drain = qtmem + 1;        // 1
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long qrow = ((long long)a.b * a.Hh + h) * a.g.nb + I;
+  const int32_t* sel = a.idx + qrow * a.k;
+  const int n = a.k;
+  if (tid == 0) {
+    mbar_init(qfull, 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(kvfull + s, 1);
+      mbar_init(kempty + s, 1);
+    }
+    for (int s = 0; s < VST; ++s) mbar_init(vempty + s, 1);
+    for (int hh = 0; hh < 2; ++hh) {
+      mbar_init(sdpfull + hh, 1);
+      mbar_init(dsfull + hh, hh == 0 ? 128 + 1 : 128);  // + warp 2: K/V of the next block landed
+    }
+    mbar_init(qtmem, 256);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tQt = tmem + 256 + D, tdOt = tQt + D / 2;
+  int t0, h0, w0;
+  block_origin(a.g, I, t0, h0, w0);
+
+  if (warp == 0) {
+    if (lane == 0 && n > 0) {
+      mbar_expect_tx(qfull, 2 * C::TILE);
+#pragma unroll
+      for (int c = 0; c < C::CH; ++c) {
+        tma_load_5d(sQ + c * 16384, &tmQ, qfull, c * 64, h, w0, h0, t0);
+        tma_load_5d(sdO + c * 16384, &tmdO, qfull, c * 64, h, w0, h0, t0);
+      }
+      int issued = 0;
+      int Jn = sel[0];  // block index read one iteration ahead of its use
+      for (int j = 0; j < n; ++j) {
+        const int sk = j % KST, sv = j % VST;
+        const int Jc = Jn;
+        if (j + 1 < n) Jn = sel[j + 1];
+        if (j >= KST && !mbar_wait(kempty + sk, ((j / KST) - 1) & 1, a.status, abort_flag)) break;
+        if (j >= VST && !mbar_wait(vempty + sv, ((j / VST) - 1) & 1, a.status, abort_flag)) break;
+        int jt0, jh0, jw0;
+        block_origin(a.g, Jc, jt0, jh0, jw0);
+        mbar_expect_tx(kvfull + sk, 2 * C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c) {
+          tma_load_5d(sK + sk * C::TILE + c * 16384, &tmK, kvfull + sk, c * 64, h, jw0, jh0, jt0);
+          tma_load_5d(sV + sv * C::TILE + c * 16384, &tmV, kvfull + sk, c * 64, h, jw0, jh0, jt0);
+        }
+        issued = j + 1;
+      }
+      if (*abort_flag) {
+        wait_plain(qfull, 0);
+        for (int j = issued - KST < 0 ? 0 : issued - KST; j < issued; ++j) wait_plain(kvfull + j % KST, (j / KST) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // Arrive on dsfull[0] of block j once K/V of block j + 1 have landed, so the MMA
+    // warp's wait for block j's first dS half also covers the next block's tiles.
+    if (lane == 0) {
+      for (int j = 0; j < n; ++j) {
+        const int t = j + 1;
+        if (t < n && !mbar_wait(kvfull + t % KST, (t / KST) & 1, a.status, abort_flag)) break;
+        if (j >= 1 && !mbar_wait(dsfull, (j - 1) & 1, a.status, abort_flag)) break;
+        mbar_arrive(dsfull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // Half-tile ping-pong as in dq_kernel; S and dP take A from TMEM.
+    const uint32_t leader = elect_leader();
+    constexpr uint32_t idS = idesc_f16(128, 64, 0, 0);  // Q K^T and dO V^T, one 64-key half
+    constexpr uint32_t idQ = idesc_f16(128, D, 0, 1);   // dS K
+    const uint64_t dKk = smem_desc(smem_u32(sK), 16, 1024, 2), dVk = smem_desc(smem_u32(sV), 16, 1024, 2);
+    const uint64_t dKm = smem_desc(smem_u32(sK), 16384, 1024, 2);  // K as the MN-major B of dS K
+    auto issue_sdp = [&](int j, int hh) {
+      const uint32_t sko = (uint32_t)(((j % KST) * C::TILE + hh * 8192) >> 4);
+      const uint32_t svo = (uint32_t)(((j % VST) * C::TILE + hh * 8192) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+        mma_ts_by(leader, tS + hh * 64, tQt + kk * 8, dKk + sko + off, idS, kk > 0);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+        mma_ts_by(leader, tdP + hh * 64, tdOt + kk * 8, dVk + svo + off, idS, kk > 0);
+      }
+      mma_commit_by(leader, sdpfull + hh);
+      if (hh == 1) mma_commit_by(leader, vempty + j % VST);  // V_j is read by dP only
+    };
+    auto issue_dq = [&](int j, int hh) {
+      const uint64_t bK0 = dKm + (uint64_t)(((j % KST) * C::TILE) >> 4);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int kk = hh * 4 + q;
+        mma_ts_by(leader, tdQ, tS + packed_col(kk), bK0 + (uint64_t)(kk * (2048 >> 4)), idQ, (j > 0 || kk > 0));
+      }
+    };
+    bool ok = n > 0 && warp_wait(qtmem, 0, a.status, abort_flag) && warp_wait(kvfull, 0, a.status, abort_flag);
+    if (ok) {
+      tc_fence_after();
+      issue_sdp(0, 0);
+      issue_sdp(0, 1);
+    }
+    for (int j = 0; ok && j < n; ++j) {
+      const bool more = j + 1 < n;
+      if (!(ok = warp_wait(dsfull, j & 1, a.status, abort_flag))) break;
+      tc_fence_after();
+      issue_dq(j, 0);
+      // dsfull[0] of block j also means K/V_{j+1} landed (warp 2 arrives on it)
+      if (more) issue_sdp(j + 1, 0);
+      if (!(ok = warp_wait(dsfull + 1, j & 1, a.status, abort_flag))) break;
+      tc_fence_after();
+      issue_dq(j, 1);
+      mma_commit_by(leader, kempty + j % KST);  // K_j: last read by this block's dQ MMAs
+      if (more) issue_sdp(j + 1, 1);
+    }
+    if (n > 0) {
+      mma_commit_by(leader, drain);
+      wait_plain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int grp = (warp - 4) >> 2;                 // key columns [64 grp, 64 grp + 64)
+    const int row = (warp & 3) * 32 + lane;          // query row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // Q (group 0) or dO (group 1) into TMEM: this thread's row, 16-byte vectors of the
+    // swizzled tile, 8 fp16 = 4 packed columns each.
+    if (n > 0 && mbar_wait(qfull, 0, a.status, abort_flag)) {
+      const uint8_t* src = grp == 0 ? sQ : sdO;
+#pragma unroll
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t u[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int qq = c0 / 4 + q;  // 16-byte vector of the row
+          const uint4 v = *reinterpret_cast<const uint4*>(src + (qq >> 3) * 16384 + sw128_offset(row, qq & 7));
+          u[4 * q] = v.x;
+          u[4 * q + 1] = v.y;
+          u[4 * q + 2] = v.z;
+          u[4 * q + 3] = v.w;
+        }
+        tmem_st32(tQt + grp * (D / 2) + lane_base + c0, u);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(qtmem);
+    }
+    const long long tile_row = qrow * 128 + row;
+    const float l2 = a.L2v[tile_row];
+    const float Dx = a.Dv[tile_row];  // exact D (from the fp32 O)
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait(sdpfull + grp, j & 1, a.status, abort_flag)) break;
+      tc_fence_after();
+      const int J = a.all_full ? 0 : sel[j];
+      const bool full = a.all_full || block_is_full(a.g, J);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col0 = grp * 64 + cc * 32;
+        uint32_t us[32], up[32];
+        tmem_ld32(tS + lane_base + col0, us);
+        tmem_ld32(tdP + lane_base + col0, up);
+        tmem_wait_ld();
+        uint32_t pds[16];
+        const uint32_t vm = full ? 0xffffffffu : block_rows_mask32(a.g, J, col0);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), a.scale_log2, -l2));
+          float p1 = ex2(fmaf(__uint_as_float(us[2 * e + 1]), a.scale_log2, -l2));
+          if (!((vm >> (2 * e)) & 1u)) p0 = 0.f;
+          if (!((vm >> (2 * e + 1)) & 1u)) p1 = 0.f;
+          pds[e] = pack_f16(p0 * (__uint_as_float(up[2 * e]) - Dx), p1 * (__uint_as_float(up[2 * e + 1]) - Dx));
+        }
+        tmem_st16(tS + lane_base + grp * 64 + cc * 16, pds);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(dsfull + grp);
+    }
+    if (n > 0) mbar_wait(drain, 0, a.status, abort_flag);
+    tc_fence_after();
+    // dQ = scale * dQ~ -> staging (the Q and dO tiles are free: they were copied to TMEM)
+    stage_row<F32OUT>(sQ, tdQ + lane_base, 0u, 0.f, row, grp * (D / 2), D / 2, a.scale, n == 0);
+    fence_async_smem();
+    named_bar(1, 256);
+    if (tid == 128) {
+      constexpr int boxes = F32OUT ? D / 32 : D / 64;
+      constexpr int per = F32OUT ? 32 : 64;
+#pragma unroll
+      for (int c = 0; c < boxes; ++c) tma_store_5d(&tmdQ, sQ + c * 16384, c * per, h, w0, h0, t0);
+      bulk_commit();
+      bulk_wait_all();
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ------------------------------------------------------------------ dK, dV
 template <int D, bool F32OUT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -807,10 +1067,13 @@ struct WsLayout {
   char* K16;
   char* V16;
   char* dO16;
+  float* O32;  // the training forward's fp32 O (training workspace only)
   size_t bytes;
 };
 
-WsLayout ws_layout(const Prob& p, void* base) {
+// train: also the fp32 O of the training forward, placed last so that every other
+// region sits at the same offset in both workspaces.
+WsLayout ws_layout(const Prob& p, void* base, bool train = false) {
   WsLayout w;
   const size_t bh = (size_t)p.B * p.Hh;
   const size_t nb = p.g.nb;
@@ -835,6 +1098,7 @@ WsLayout ws_layout(const Prob& p, void* base) {
   w.K16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
   w.V16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
   w.dO16 = take((size_t)p.B * p.N * p.Hh * p.d * 2);
+  w.O32 = train ? reinterpret_cast<float*>(take((size_t)p.B * p.N * p.Hh * p.d * 4)) : nullptr;
   w.bytes = off;
   return w;
 }
@@ -899,6 +1163,30 @@ cudaError_t launch_dq(const Prob& p, const void* V, const void* dO, const int32_
 }
 
 template <int D, bool F32OUT>
+cudaError_t launch_dqx(const Prob& p, const int32_t* idx, void* dQ, void* ws, cudaStream_t st) {
+  using C = Cfg<D>;
+  WsLayout w = ws_layout(p, ws);
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  const size_t smem = 1024 + (size_t)C::TILE * (2 + C::KST + C::VST) + 8 * (7 + 2 * C::KST + C::VST) + 8 + 64;
+  cudaError_t e = cudaFuncSetAttribute(dqx_kernel<D, F32OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const TokType gt = F32OUT ? kTokF32 : kTokBF16;
+  for (int b = 0; b < p.B; ++b) {
+    CUtensorMap mQ, mK, mV, mdO, mdQ;
+    if (!token_map(&mQ, p, w.Q16, b, kTokF16) || !token_map(&mK, p, w.K16, b, kTokF16) ||
+        !token_map(&mV, p, w.V16, b, kTokF16) || !token_map(&mdO, p, w.dO16, b, kTokF16) ||
+        !token_map(&mdQ, p, dQ, b, gt))
+      return cudaErrorInvalidValue;
+    dqx_kernel<D, F32OUT><<<dim3(p.g.nb, p.Hh), kThreads, smem, st>>>(mQ, mK, mV, mdO, mdQ,
+                                                                      make_args(p, w, idx, status, b));
+    note_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <int D, bool F32OUT>
 cudaError_t launch_dkdv(const Prob& p, const void* V, const void* dO, void* dK, void* dV, void* ws, cudaStream_t st) {
   using C = Cfg<D>;
   WsLayout w = ws_layout(p, ws);
@@ -935,16 +1223,15 @@ cudaError_t launch_dkdv(const Prob& p, const void* V, const void* dO, void* dK, 
 }  // namespace
 
 size_t bwd_ws_tc(const Prob& p) { return ws_layout(p, nullptr).bytes; }
+size_t train_ws_tc(const Prob& p) { return ws_layout(p, nullptr, true).bytes; }
 
-cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O,
-                           const float* LSE, const void* dO, const int32_t* idx, void* ws, cudaStream_t st,
-                           const Part* part) {
+namespace {
+// The block-map transpose (all batches and heads at once): for every key block the query
+// blocks that kept it, ascending, their counts and offsets, and the visiting order.
+cudaError_t build_csr(const Prob& p, const WsLayout& w, const int32_t* idx, const Part* part, unsigned* status,
+                      cudaStream_t st) {
   const Geom& g = p.g;
-  WsLayout w = ws_layout(p, ws);
-  unsigned* status = status_ptr();
-  if (!status) return cudaErrorUnknown;
   cudaError_t e;
-  // block-map transpose (all batches and heads at once)
   const int words = (g.nb + 31) / 32;
   const long long bhn = (long long)p.B * p.Hh * g.nb;
   if ((e = cudaMemsetAsync(w.bitmap, 0, (size_t)bhn * words * 4, st)) != cudaSuccess) return e;
@@ -963,26 +1250,98 @@ cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const vo
   csr_order_kernel<<<dim3((g.nb + 255) / 256, p.B * p.Hh), 256, g.nb * sizeof(int32_t), st>>>(w.counts, g.nb,
                                                                                                w.order);
   csr_fill_kernel<<<(int)((bhn * 32 + 255) / 256), 256, 0, st>>>(w.bitmap, w.offsets, g.nb, p.k, words, bhn, w.lists);
+  note_launches(5);
+  return cudaGetLastError();
+}
+
+// bf16 -> fp16 copy of one [B, N, heads, d] tensor (range latched into status).
+void half_copy(const Prob& p, const void* src, char* dst, unsigned* status, cudaStream_t st) {
   const long long n8 = (long long)p.B * p.N * p.Hh * p.d / 8;
   const int cb = (int)std::min<long long>((n8 + 255) / 256, 152LL * 16);
-  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(Q), reinterpret_cast<uint4*>(w.Q16), n8, status);
-  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(K), reinterpret_cast<uint4*>(w.K16), n8, status);
-  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(V), reinterpret_cast<uint4*>(w.V16), n8, status);
-  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(dO), reinterpret_cast<uint4*>(w.dO16), n8, status);
-  const float* dLSE = part ? part->dLSE : nullptr;
+  half_kernel<<<cb, 256, 0, st>>>(static_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), n8, status);
+  note_launches(1);
+}
+
+// D and the LSE rows in tile order, one launch per batch entry.
+void row_terms(const Prob& p, const WsLayout& w, const void* O, bool o32, const float* LSE, const void* dO,
+               const float* dLSE, cudaStream_t st) {
+  const Geom& g = p.g;
   float* G = dLSE ? w.G : nullptr;
+  const __nv_bfloat16* gO = static_cast<const __nv_bfloat16*>(dO);
   for (int b = 0; b < p.B; ++b) {
-    if (p.d == 64)
-      pre_kernel<64><<<dim3(g.nb, p.Hh), 128, 0, st>>>(g, p.Hh, p.N, b, static_cast<const __nv_bfloat16*>(O),
-                                                       static_cast<const __nv_bfloat16*>(dO), LSE, dLSE, w.Dv, w.L2v,
-                                                       G);
+    const dim3 grid(g.nb, p.Hh);
+    if (p.d == 64 && o32)
+      pre_kernel<64, true><<<grid, 128, 0, st>>>(g, p.Hh, p.N, b, O, gO, LSE, dLSE, w.Dv, w.L2v, G);
+    else if (p.d == 64)
+      pre_kernel<64, false><<<grid, 128, 0, st>>>(g, p.Hh, p.N, b, O, gO, LSE, dLSE, w.Dv, w.L2v, G);
+    else if (o32)
+      pre_kernel<128, true><<<grid, 128, 0, st>>>(g, p.Hh, p.N, b, O, gO, LSE, dLSE, w.Dv, w.L2v, G);
     else
-      pre_kernel<128><<<dim3(g.nb, p.Hh), 128, 0, st>>>(g, p.Hh, p.N, b, static_cast<const __nv_bfloat16*>(O),
-                                                        static_cast<const __nv_bfloat16*>(dO), LSE, dLSE, w.Dv, w.L2v,
-                                                        G);
+      pre_kernel<128, false><<<grid, 128, 0, st>>>(g, p.Hh, p.N, b, O, gO, LSE, dLSE, w.Dv, w.L2v, G);
   }
-  note_launches(9 + p.B);  // 5 block-map kernels, 4 fp16 copies, one pre_kernel per batch entry
+  note_launches(p.B);
+}
+}  // namespace
+
+cudaError_t bwd_prepare_tc(const Prob& p, const void* Q, const void* K, const void* V, const void* O,
+                           const float* LSE, const void* dO, const int32_t* idx, void* ws, cudaStream_t st,
+                           const Part* part) {
+  WsLayout w = ws_layout(p, ws);
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  cudaError_t e = build_csr(p, w, idx, part, status, st);
+  if (e != cudaSuccess) return e;
+  half_copy(p, Q, w.Q16, status, st);
+  half_copy(p, K, w.K16, status, st);
+  half_copy(p, V, w.V16, status, st);
+  half_copy(p, dO, w.dO16, status, st);
+  row_terms(p, w, O, false, LSE, dO, part ? part->dLSE : nullptr, st);
   return cudaGetLastError();
+}
+
+cudaError_t fwd_train_tc(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, void* O,
+                         float* LSE, void* ws, cudaStream_t st) {
+  WsLayout w = ws_layout(p, ws, true);
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  half_copy(p, Q, w.Q16, status, st);
+  half_copy(p, K, w.K16, status, st);
+  half_copy(p, V, w.V16, status, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return fwd_tc_f16(p, w.Q16, w.K16, w.V16, idx, O, LSE, w.O32, st);
+}
+
+cudaError_t bwd_train_tc(const Prob& p, const float* LSE, const void* dO, const int32_t* idx, void* dQ, void* dK,
+                         void* dV, int grad_dtype, void* ws, int phases, cudaStream_t st) {
+  WsLayout w = ws_layout(p, ws, true);
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  cudaError_t e;
+  const bool f32 = grad_dtype == SDA_F32;
+  if (phases & 1) {
+    if ((e = build_csr(p, w, idx, nullptr, status, st)) != cudaSuccess) return e;
+    half_copy(p, dO, w.dO16, status, st);
+    row_terms(p, w, w.O32, true, LSE, dO, nullptr, st);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (phases & 2) {
+    if (p.d == 64)
+      e = f32 ? launch_dqx<64, true>(p, idx, dQ, ws, st) : launch_dqx<64, false>(p, idx, dQ, ws, st);
+    else
+      e = f32 ? launch_dqx<128, true>(p, idx, dQ, ws, st) : launch_dqx<128, false>(p, idx, dQ, ws, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (phases & 4) {
+    if (p.d == 64)
+      e = f32 ? launch_dkdv<64, true>(p, nullptr, nullptr, dK, dV, ws, st)
+              : launch_dkdv<64, false>(p, nullptr, nullptr, dK, dV, ws, st);
+    else
+      e = f32 ? launch_dkdv<128, true>(p, nullptr, nullptr, dK, dV, ws, st)
+              : launch_dkdv<128, false>(p, nullptr, nullptr, dK, dV, ws, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t bwd_dq_tc(const Prob& p, const void* V, const void* dO, const int32_t* idx, void* dQ, int grad_dtype,

@@ -8,6 +8,13 @@
 // give the per-partition states of "DiTango: Cost-Effective Parallel Diffusion
 // Generation with Selective Attention State Reuse".
 //
+// Two operand types.  The inference forward reads the caller's bf16 Q, K, V
+// and splits P into two bf16 terms for the P V product.  The training forward reads fp16
+// copies of Q, K, V (exact for bf16 values inside fp16's range) and rounds P
+// to fp16, eight times finer, and also writes O in fp32: the backward then
+// takes D_i = dO_i . O_i from that O, which is close enough to the exact
+// sum_j P_ij dP_ij that no correction pass is needed.
+//
 // One CTA per (query block, head); 12 warps:
 //   warps 0, 2  TMA producers: Q once and the K tiles of each kept block
 //               (warp 0), the V tiles (warp 2), through separate rings so K
@@ -16,19 +23,26 @@
 //               also arrives on P_j's barrier once K_{j+2} has landed.
 //   warp 1      TMEM owner and MMA issuer (converged warp, one elected lane):
 //               S_j = Q K_j^T into one of two TMEM S buffers, then, once P_j
-//               is ready, O += P_j V_j with P_j read from TMEM.
-//   warps 4-11  softmax: two warps per query row quarter, each owning 64 of
-//               the 128 key columns (thread = row = TMEM lane); the pair swaps
-//               its half-row maxima at a named barrier.  Online softmax in base 2 with a
-//               lazy rescale: O and l are rescaled only when a row max grows
-//               by more than 2^8, which is exact because O and l always share
-//               the same reference max.  P overwrites S in bf16; O is divided
-//               by the sum of those bf16 weights (so the rounding of a
-//               dominant weight cancels), LSE uses the fp32 sum.
+//               is ready, O_0 += P_j[:, keys 0-63] V_j[0-63] and
+//               O_1 += P_j[:, keys 64-127] V_j[64-127] with P_j read from TMEM
+//               (in bf16 twice, P_hi then P_lo).
+//   warps 4-11  softmax: two warps per query row quarter (thread = row = TMEM
+//               lane); warp half hf owns key columns [64 hf, 64 hf + 64) of
+//               every S tile, with its own running max, its own sums and its
+//               own accumulator O_hf, so the two warps never wait for each
+//               other inside the loop; the two partial states merge once at
+//               the end with log-sum-exp weights.  Online softmax in base 2
+//               with a lazy rescale: O_hf and its sums are rescaled only when
+//               the half-row max grows by more than 2^8, which is exact because
+//               they always share one reference max.  P overwrites S: in fp16,
+//               or in bf16 as P_hi + P_lo (the remainder), both fed to the P V
+//               product, so that O is accurate to fp32 accumulation and not to
+//               bf16's 8 bits; one fp32 sum of P divides O and gives LSE.
 //   warp 3      arrives on P_j's barrier once V_j has landed: with the two
 //               producer arrivals that barrier covers every input of P_j V_j
 //               and of S_{j+2}, so the MMA warp waits once per block.
-// TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,256+D) O.
+// TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,256+D) O_0,
+// [256+D,256+2D) O_1.
 #include "internal.h"
 
 namespace sda {
@@ -56,7 +70,7 @@ constexpr int kSeenWords = 8192 / 32;       // one bit per key block (n_b <= 819
 template <int D>
 struct FwdCfg {
   static constexpr int CH = D / 64;                  // 128-byte chunks of the head dim
-  static constexpr int TILE = 128 * D * 2;           // bytes of one 128-row bf16 tile
+  static constexpr int TILE = 128 * D * 2;           // bytes of one 128-row 16-bit tile
   static constexpr int KST = D == 128 ? 3 : 5;       // K ring depth (K is consumed first)
   static constexpr int VST = D == 128 ? 2 : 4;       // V ring depth
   static constexpr int SMEM_TILES = TILE * (1 + KST + VST);
@@ -70,18 +84,20 @@ __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
 }
 
 // P = 2^(s scale_log2 - m) for one thread's 64 keys (two 32-column chunks of S in u0,
-// u1), stored as bf16 pairs in the first 16 TMEM columns of each chunk at tS; adds the
-// sums of P (sa + sb) and of bf16(P) (ra + rb).  kMask: keys whose bit in vm0 / vm1 is
-// clear (outside the grid) get P = 0.
-template <bool kMask>
+// u1), written over S and added to l.  kF16: P in fp16, in the first 16 TMEM columns of
+// each chunk.  Otherwise P = P_hi + P_lo, two bf16 values (P_lo the rounding remainder
+// of P_hi), in the first and the second 16 columns of each chunk: the P V product takes
+// both, so P enters it with about 16 bits instead of bf16's 8.  kMask: keys whose bit in
+// vm0 / vm1 is clear (outside the grid) get P = 0.
+template <bool kMask, bool kF16>
 __device__ __forceinline__ void softmax_p(const uint32_t (&u0)[32], const uint32_t (&u1)[32], uint32_t vm0,
-                                          uint32_t vm1, float m, float scale_log2, uint32_t tS, float& sa, float& sb,
-                                          float& ra, float& rb) {
+                                          uint32_t vm1, float m, float scale_log2, uint32_t tS, float& l) {
+  float sa = 0.f, sb = 0.f;
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     const uint32_t(&u)[32] = cc ? u1 : u0;
     const uint32_t vm = cc ? vm1 : vm0;
-    uint32_t ph[16];
+    uint32_t ph[16], pl[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       float s0 = fmaf(__uint_as_float(u[2 * e]), scale_log2, -m);
@@ -93,18 +109,27 @@ __device__ __forceinline__ void softmax_p(const uint32_t (&u0)[32], const uint32
       const float p0 = ex2(s0), p1 = ex2(s1);
       sa += p0;
       sb += p1;
-      ph[e] = pack_bf16(p0, p1);
-      ra += __uint_as_float(ph[e] << 16);
-      rb += __uint_as_float(ph[e] & 0xFFFF0000u);
+      if (kF16) {
+        ph[e] = pack_f16(p0, p1);
+      } else {
+        ph[e] = pack_bf16(p0, p1);
+        pl[e] = pack_bf16(p0 - __uint_as_float(ph[e] << 16), p1 - __uint_as_float(ph[e] & 0xFFFF0000u));
+      }
     }
     tmem_st16(tS + cc * 32, ph);
+    if (!kF16) tmem_st16(tS + cc * 32 + 16, pl);
   }
+  l += sa + sb;
 }
 
-template <int D>
+// kF16: operands and P in fp16 (training), otherwise bf16.  kO16: O is written in bf16
+// through tmO; kO32: O is written in fp32 through tmO32 (the training forward writes
+// both; an fp32 partition state only the second).
+template <int D, bool kF16, bool kO16, bool kO32>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ CUtensorMap tmO32, FwdArgs a) {
   using C = FwdCfg<D>;
   constexpr int KST = C::KST, VST = C::VST;
   const int I = blockIdx.x, h = blockIdx.y;
@@ -125,15 +150,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pfull = sfull + 2;    // 2
   uint64_t* odone = pfull + 2;    // 1
   uint64_t* drain = odone + 1;    // 1
-  uint64_t* pairbar = drain + 1;  // 4: the two softmax warps of a lane quarter meet here
+  uint64_t* pairbar = drain + 1;  // 4: the two softmax warps of a lane quarter meet here at the end
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pairbar + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* n_sel_s = abort_flag + 1;
   int* warp_cnt = n_sel_s + 1;  // 16
-  float* half_l = reinterpret_cast<float*>(warp_cnt + 16);  // [2 halves][l, l of bf16 P][128 rows]
-  float* half_max = half_l + 512;                            // [2 block parities][2 halves][128 rows]
-  unsigned* seen = reinterpret_cast<unsigned*>(half_max + 512);  // kSeenWords: blocks met in this row
-  int* sel = reinterpret_cast<int*>(seen + kSeenWords);      // k
+  float* half_st = reinterpret_cast<float*>(warp_cnt + 16);  // [2 halves][m, l][128 rows]
+  unsigned* seen = reinterpret_cast<unsigned*>(half_st + 512);  // kSeenWords: blocks met in this row
+  int* sel = reinterpret_cast<int*>(seen + kSeenWords);         // k
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -267,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // block j done, V_j and K_{j+2} landed); only K_0 and K_1 are waited on directly.
     if (n_sel > 0) {
       const uint32_t leader = elect_leader();
-      constexpr uint32_t idS = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
+      constexpr uint32_t idS = kF16 ? idesc_f16(128, 128, 0, 0) : idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idO = kF16 ? idesc_f16(128, D, 0, 1) : idesc_bf16(128, D, 0, 1);
       const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024, 2);
       const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, 2);
       const uint64_t dV = smem_desc(smem_u32(sV), 16384, 1024, 2);
@@ -307,10 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = j % VST;
         const uint32_t tP = tmem + (j & 1) * 128;
         const uint64_t dVs = dV + (uint64_t)((s * C::TILE) >> 4);
+        // keys 16 kk .. 16 kk + 15: kk < 4 feed O_0 (the first softmax warp's keys), kk >= 4 O_1;
+        // in bf16 each step takes P_hi, then P_lo (16 columns further)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // keys 16 kk .. 16 kk + 15
-          mma_ts_by(leader, tO, tP + (kk >> 1) * 32 + (kk & 1) * 8, dVs + (uint64_t)(kk * (2048 >> 4)), idO,
-                    (j > 0 || kk > 0));
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t tA = tP + (kk >> 1) * 32 + (kk & 1) * 8;
+          const uint64_t bV = dVs + (uint64_t)(kk * (2048 >> 4));
+          mma_ts_by(leader, tO + (kk >> 2) * D, tA, bV, idO, (j > 0 || (kk & 3) > 0));
+          if (!kF16) mma_ts_by(leader, tO + (kk >> 2) * D, tA + 16, bV, idO, 1u);
+        }
         mma_commit_by(leader, vempty + s);
         mma_commit_by(leader, odone);
       }
@@ -320,145 +349,148 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax + epilogue
-    // Two warps per TMEM lane quarter: warp half hf owns S columns [64 hf, 64 hf + 64)
-    // and O columns [hf D/2, (hf + 1) D/2) of the quarter's 32 rows.  The pair swaps
-    // its half-row maxima through shared memory (double-buffered by block parity) at a
-    // named barrier, so both warps hold the same row maxima and take the same rescale
-    // decisions.
+    // Two warps per TMEM lane quarter; warp half hf owns S columns [64 hf, 64 hf + 64) of
+    // the quarter's 32 rows and its own accumulator O_hf (all D columns).
     const int quarter = warp & 3, hf = (warp - 4) >> 2;
     const int r = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tOh = tmem + 256 + hf * D + lane_base;
     auto pair_sync = [&](uint32_t phase) -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(pairbar + quarter);
       return mbar_wait(pairbar + quarter, phase & 1, a.status, abort_flag);
     };
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    float m = -INFINITY;
-    float l = 0.f;   // sum of P (fp32): gives LSE
-    float lr = 0.f;  // sum of bf16(P), the weights the P V product uses: divides O
+    float m = -INFINITY;  // half-row max, log2 units (scaled)
+    float l = 0.f;        // sum of P (fp32): divides O and gives LSE
     bool ok = true;
     for (int j = 0; j < n_sel; ++j) {
-      // Every iteration of both warps of a pair passes the pair's named barrier exactly
-      // once (twice when rescaling), with the success of its bounded waits ANDed into it:
-      // a wait that gives up stops both warps at the same point.
-      const bool okw = mbar_wait(sfull + (j & 1), (j >> 1) & 1, a.status, abort_flag);
+      if (!(ok = warp_wait(sfull + (j & 1), (j >> 1) & 1, a.status, abort_flag))) break;
+      tc_fence_after();
       const uint32_t tS = tmem + (j & 1) * 128 + lane_base + hf * 64;
-      uint32_t u0[32], u1[32];
+      const int J = sel[j];
+      const bool full = a.all_full || block_is_full(a.g, J);
       uint32_t vm0 = ~0u, vm1 = ~0u;  // key rows of J inside the grid
+      if (!full) {
+        vm0 = block_rows_mask32(a.g, J, hf * 64);
+        vm1 = block_rows_mask32(a.g, J, hf * 64 + 32);
+      }
+      uint32_t u0[32], u1[32];
+      float c0, c1;
+      tmem_ld32_max(tS, u0, c0);  // values and, from the same load, their maximum
+      tmem_ld32_max(tS + 32, u1, c1);
+      tmem_wait_ld();
       float mx = -INFINITY;
-      bool fullj = true;
-      if (okw) {
-        tc_fence_after();
-        const int J = sel[j];
-        const bool full = a.all_full || block_is_full(a.g, J);
-        fullj = full;
-        if (!full) {
-          vm0 = block_rows_mask32(a.g, J, hf * 64);
-          vm1 = block_rows_mask32(a.g, J, hf * 64 + 32);
-        }
-        float c0, c1;
-        tmem_ld32_max(tS, u0, c0);  // values and, from the same load, their maximum
-        tmem_ld32_max(tS + 32, u1, c1);
-        tmem_wait_ld();
-        if (full) {
-          mx = fmaxf(c0, c1);
-        } else {
+      if (full) {
+        mx = fmaxf(c0, c1);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if ((vm0 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u0[e]));
-            if ((vm1 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u1[e]));
-          }
+        for (int e = 0; e < 32; ++e) {
+          if ((vm0 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u0[e]));
+          if ((vm1 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u1[e]));
         }
-        half_max[((j & 1) * 2 + hf) * 128 + r] = mx;
       }
-      if (!named_bar_and(2 + quarter, 64, okw)) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, half_max[((j & 1) * 2 + (hf ^ 1)) * 128 + r]) * a.scale_log2;  // same in both warps
-      const float m_new = fmaxf(m, mx);
+      const float m_new = fmaxf(m, mx * a.scale_log2);
       if (j == 0) {
         m = m_new;
       } else {
         const bool need = m_new > m + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {  // both warps of the pair take this branch together
-          // O holds sum_{<j} P V relative to m: wait for the last P V, then rescale this half.
-          if (!named_bar_and(2 + quarter, 64, mbar_wait(odone, (j - 1) & 1, a.status, abort_flag))) {
-            ok = false;
-            break;
-          }
+        if (__any_sync(0xffffffffu, need)) {
+          // O_hf holds sum_{<j} P V relative to m: wait for the last P V, then rescale it.
+          if (!(ok = warp_wait(odone, (j - 1) & 1, a.status, abort_flag))) break;
           tc_fence_after();
           const float alpha = need ? ex2(m - m_new) : 1.f;
 #pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc) {
+          for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t u[32];
-            const uint32_t tO = tmem + 256 + lane_base + hf * (D / 2) + cc * 32;
-            tmem_ld32(tO, u);
+            tmem_ld32(tOh + cc * 32, u);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            tmem_st32(tO, u);
+            tmem_st32(tOh + cc * 32, u);
           }
           tmem_wait_st();
           l *= alpha;
-          lr *= alpha;
           if (need) m = m_new;
         }
       }
-      // P = 2^(s - m) in bf16, packed in pairs: each 32-column chunk of S holds the
-      // P of its 32 keys in its first 16 columns.  Full tiles skip the per-key mask.
-      float sa = 0.f, sb = 0.f, ra = 0.f, rb = 0.f;
-      if (fullj)
-        softmax_p<false>(u0, u1, vm0, vm1, m, a.scale_log2, tS, sa, sb, ra, rb);
+      // P in 16-bit pairs: each 32-column chunk of S holds the P of its 32 keys in its
+      // first 16 columns.  Full tiles skip the per-key mask.
+      if (full)
+        softmax_p<false, kF16>(u0, u1, vm0, vm1, m, a.scale_log2, tS, l);
       else
-        softmax_p<true>(u0, u1, vm0, vm1, m, a.scale_log2, tS, sa, sb, ra, rb);
-      l += sa + sb;
-      lr += ra + rb;
+        softmax_p<true, kF16>(u0, u1, vm0, vm1, m, a.scale_log2, tS, l);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(pfull + (j & 1));
     }
-    // Epilogue: O / l(bf16 P) -> bf16 -> swizzled staging tile (reusing the Q tile) -> TMA store.
-    // `drain` completes once every MMA of the CTA has finished (the MMA warp commits it last).
+    // Epilogue: merge the two half states, O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1)
+    // with a_h = 2^(m_h - max(m_0, m_1)) -> bf16 (and fp32) -> swizzled staging tiles
+    // (the Q tile, and the K ring for fp32) -> TMA stores.  `drain` completes once every
+    // MMA of the CTA has finished (the MMA warp commits it last).
     if (n_sel > 0) ok = mbar_wait(drain, 0, a.status, abort_flag) && ok;
     tc_fence_after();
-    half_l[(hf * 2) * 128 + r] = l;
-    half_l[(hf * 2 + 1) * 128 + r] = lr;
+    half_st[(hf * 2 + 0) * 128 + r] = m;
+    half_st[(hf * 2 + 1) * 128 + r] = l;
     ok = pair_sync(0) && ok;
-    const float lt = l + half_l[((hf ^ 1) * 2) * 128 + r];
-    const float ltr = lr + half_l[((hf ^ 1) * 2 + 1) * 128 + r];
-    const float inv = (n_sel > 0 && ltr > 0.f) ? 1.f / ltr : 0.f;
+    const float mo = half_st[((hf ^ 1) * 2 + 0) * 128 + r];
+    const float lo = half_st[((hf ^ 1) * 2 + 1) * 128 + r];
+    const float M = fmaxf(m, mo);
+    const float as = M == -INFINITY ? 0.f : ex2(m - M);
+    const float ao = M == -INFINITY ? 0.f : ex2(mo - M);
+    const float L = as * l + ao * lo;
+    const float inv = (n_sel > 0 && L > 0.f) ? 1.f / L : 0.f;
+    const float w0c = (hf == 0 ? as : ao) * inv, w1c = (hf == 0 ? ao : as) * inv;  // weights of O_0, O_1
 #pragma unroll
     for (int cc = 0; cc < D / 64; ++cc) {
       const int col = hf * (D / 2) + cc * 32;  // first O column of this 32-column chunk
-      uint32_t u[32];
+      float f[32];
       if (n_sel > 0) {
-        tmem_ld32(tmem + 256 + lane_base + col, u);
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tmem + 256 + lane_base + col, u0);
+        tmem_ld32(tmem + 256 + D + lane_base + col, u1);
         tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] = w0c * __uint_as_float(u0[e]) + w1c * __uint_as_float(u1[e]);
       } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) u[e] = 0u;
+        for (int e = 0; e < 32; ++e) f[e] = 0.f;
       }
-      uint8_t* dst = sQ + (col >> 6) * 16384;
+      if (kO16) {
+        uint8_t* dst = sQ + (col >> 6) * 16384;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint4 v;
-        v.x = pack_bf16(__uint_as_float(u[q4 * 8 + 0]) * inv, __uint_as_float(u[q4 * 8 + 1]) * inv);
-        v.y = pack_bf16(__uint_as_float(u[q4 * 8 + 2]) * inv, __uint_as_float(u[q4 * 8 + 3]) * inv);
-        v.z = pack_bf16(__uint_as_float(u[q4 * 8 + 4]) * inv, __uint_as_float(u[q4 * 8 + 5]) * inv);
-        v.w = pack_bf16(__uint_as_float(u[q4 * 8 + 6]) * inv, __uint_as_float(u[q4 * 8 + 7]) * inv);
-        *reinterpret_cast<uint4*>(dst + sw128_offset(r, ((col & 63) >> 3) + q4)) = v;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 v;
+          v.x = pack_bf16(f[q4 * 8 + 0], f[q4 * 8 + 1]);
+          v.y = pack_bf16(f[q4 * 8 + 2], f[q4 * 8 + 3]);
+          v.z = pack_bf16(f[q4 * 8 + 4], f[q4 * 8 + 5]);
+          v.w = pack_bf16(f[q4 * 8 + 6], f[q4 * 8 + 7]);
+          *reinterpret_cast<uint4*>(dst + sw128_offset(r, ((col & 63) >> 3) + q4)) = v;
+        }
+      }
+      if (kO32) {  // fp32 boxes of 32 columns
+        uint8_t* box = sK + (col >> 5) * 16384;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(box + sw128_offset(r, q)) =
+              make_uint4(__float_as_uint(f[4 * q]), __float_as_uint(f[4 * q + 1]), __float_as_uint(f[4 * q + 2]),
+                         __float_as_uint(f[4 * q + 3]));
       }
     }
     const int n = block_row_token(a.g, I, r);
     if (hf == 0 && n >= 0)
       a.LSE[((long long)a.b * a.Hh + h) * a.N + n] =
-          (n_sel > 0 && lt > 0.f) ? (m + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+          (n_sel > 0 && L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
     fence_async_smem();
     named_bar(1, 256);
     if (warp == 4 && lane == 0) {
+      if (kO16) {
 #pragma unroll
-      for (int c = 0; c < C::CH; ++c) tma_store_5d(&tmO, sQ + c * 16384, c * 64, h, w0, h0, t0);
+        for (int c = 0; c < C::CH; ++c) tma_store_5d(&tmO, sQ + c * 16384, c * 64, h, w0, h0, t0);
+      }
+      if (kO32) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tma_store_5d(&tmO32, sK + c * 16384, c * 32, h, w0, h0, t0);
+      }
       bulk_commit();
       bulk_wait_all();
     }
@@ -471,29 +503,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kF16, bool kO16, bool kO32>
 cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
-                       int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st) {
+                       int kb_end, const uint8_t* qb_active, void* O, float* LSE, float* O32, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * 1024 +
+  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * 512 +
                       4 * kSeenWords + 4 * (size_t)p.k + 64;
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = fwd_tc_kernel<D, kF16, kO16, kO32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   unsigned* status = status_ptr();
   if (!status) return cudaErrorUnknown;
   const size_t per_batch = (size_t)p.N * p.Hh * p.d * 2;
+  const TokType in_t = kF16 ? kTokF16 : kTokBF16;
   for (int b = 0; b < p.B; ++b) {
-    CUtensorMap mQ, mK, mV, mO;
+    CUtensorMap mQ, mK, mV, mO, mO32;
     const char* q = static_cast<const char*>(Q) + b * per_batch;
     const char* k = static_cast<const char*>(K) + b * per_batch;
     const char* v = static_cast<const char*>(V) + b * per_batch;
-    char* o = static_cast<char*>(O) + b * per_batch;
     const Geom& g = p.g;
-    if (!make_token_map(&mQ, q, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mK, k, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mV, v, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
-        !make_token_map(&mO, o, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw))
+    if (!make_token_map(&mQ, q, in_t, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
+        !make_token_map(&mK, k, in_t, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw) ||
+        !make_token_map(&mV, v, in_t, g.T, g.H, g.W, p.Hh, p.d, g.bt, g.bh, g.bw))
       return cudaErrorInvalidValue;
+    if (kO16 && !make_token_map(&mO, static_cast<char*>(O) + b * per_batch, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt,
+                                g.bh, g.bw))
+      return cudaErrorInvalidValue;
+    if (kO32 && !make_token_map(&mO32, O32 + (size_t)b * p.N * p.Hh * p.d, kTokF32, g.T, g.H, g.W, p.Hh, p.d, g.bt,
+                                g.bh, g.bw))
+      return cudaErrorInvalidValue;
+    if (!kO16) mO = mQ;   // not read
+    if (!kO32) mO32 = mQ;  // not read
     FwdArgs a;
     a.g = g;
     a.Hh = p.Hh;
@@ -509,7 +549,7 @@ cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* 
     a.LSE = LSE;
     a.status = status;
     dim3 grid(g.nb, p.Hh);
-    fwd_tc_kernel<D><<<grid, kThreads, smem, st>>>(mQ, mK, mV, mO, a);
+    kern<<<grid, kThreads, smem, st>>>(mQ, mK, mV, mO, mO32, a);
     note_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -519,9 +559,23 @@ cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* 
 }  // namespace
 
 cudaError_t fwd_tc(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
-                   int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st) {
-  if (p.d == 64) return launch_fwd<64>(p, Q, K, V, idx, kb_begin, kb_end, qb_active, O, LSE, st);
-  return launch_fwd<128>(p, Q, K, V, idx, kb_begin, kb_end, qb_active, O, LSE, st);
+                   int kb_end, const uint8_t* qb_active, void* O, bool out_f32, float* LSE, cudaStream_t st) {
+  float* O32 = static_cast<float*>(O);
+  if (p.d == 64)
+    return out_f32 ? launch_fwd<64, false, false, true>(p, Q, K, V, idx, kb_begin, kb_end, qb_active, nullptr, LSE, O32,
+                                                        st)
+                   : launch_fwd<64, false, true, false>(p, Q, K, V, idx, kb_begin, kb_end, qb_active, O, LSE, nullptr,
+                                                        st);
+  return out_f32 ? launch_fwd<128, false, false, true>(p, Q, K, V, idx, kb_begin, kb_end, qb_active, nullptr, LSE, O32,
+                                                       st)
+                 : launch_fwd<128, false, true, false>(p, Q, K, V, idx, kb_begin, kb_end, qb_active, O, LSE, nullptr,
+                                                       st);
+}
+
+cudaError_t fwd_tc_f16(const Prob& p, const void* Q16, const void* K16, const void* V16, const int32_t* idx, void* O,
+                       float* LSE, float* O32, cudaStream_t st) {
+  if (p.d == 64) return launch_fwd<64, true, true, true>(p, Q16, K16, V16, idx, 0, p.g.nb, nullptr, O, LSE, O32, st);
+  return launch_fwd<128, true, true, true>(p, Q16, K16, V16, idx, 0, p.g.nb, nullptr, O, LSE, O32, st);
 }
 
 }  // namespace sda

@@ -90,8 +90,12 @@ cudaError_t predict_tc(const Prob& p, const void* Q, const void* K, const void* 
                        float* score, void* ws, cudaStream_t st);
 
 // ---- attn_fwd_tc.cu
+// O in bf16, or (out_f32) in fp32.
 cudaError_t fwd_tc(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
-                   int kb_end, const uint8_t* qb_active, void* O, float* LSE, cudaStream_t st);
+                   int kb_end, const uint8_t* qb_active, void* O, bool out_f32, float* LSE, cudaStream_t st);
+// The training forward's kernel: fp16 copies of Q, K, V, P in fp16, O also written in fp32.
+cudaError_t fwd_tc_f16(const Prob& p, const void* Q16, const void* K16, const void* V16, const int32_t* idx, void* O,
+                       float* LSE, float* O32, cudaStream_t st);
 
 // ---- attn_bwd_tc.cu
 // Backward in three phases sharing the workspace, in this order: prepare
@@ -105,6 +109,13 @@ cudaError_t bwd_dq_tc(const Prob& p, const void* V, const void* dO, const int32_
                       void* ws, cudaStream_t st, const Part* part = nullptr);
 cudaError_t bwd_dkdv_tc(const Prob& p, const void* V, const void* dO, void* dK, void* dV, int grad_dtype, void* ws,
                         cudaStream_t st);
+// The training pair: the forward writes fp16 copies of Q, K, V and an fp32 O into the
+// training workspace; the backward (phases: 1 prepare, 2 dQ, 4 dK/dV) reads them.
+size_t train_ws_tc(const Prob& p);
+cudaError_t fwd_train_tc(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, void* O,
+                         float* LSE, void* ws, cudaStream_t st);
+cudaError_t bwd_train_tc(const Prob& p, const float* LSE, const void* dO, const int32_t* idx, void* dQ, void* dK,
+                         void* dV, int grad_dtype, void* ws, int phases, cudaStream_t st);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -16,9 +16,10 @@ LIB_PATH = os.path.join(_HERE, "libsda.so")
 (SDA_OK, SDA_ERR_INVALID_ARG, SDA_ERR_UNSUPPORTED, SDA_ERR_WORKSPACE, SDA_ERR_CUDA, SDA_ERR_DEVICE_TIMEOUT,
  SDA_ERR_DEVICE_BAD_INDEX, SDA_ERR_DEVICE_RANGE) = range(8)
 SDA_F32, SDA_BF16 = 0, 1
-SDA_OP_PREDICT, SDA_OP_BWD = 0, 1
+SDA_OP_PREDICT, SDA_OP_BWD, SDA_OP_TRAIN = 0, 1, 2
 
 EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_attn_fwd", "sda_attn_bwd",
+           "sda_attn_fwd_train", "sda_attn_bwd_train",
            "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_attn_bwd_partition", "sda_merge_states", "sda_merge_states_bwd",
            "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_selftest_wait_timeout", "sda_status_string")
 
@@ -51,9 +52,11 @@ def lib() -> ctypes.CDLL:
         L.sda_num_blocks.argtypes = [pr, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         L.sda_workspace_size.argtypes = [pr, i32, ctypes.POINTER(sz)]
         L.sda_predict_blocks.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, sz, vp]
-        L.sda_attn_fwd.argtypes = [pr, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp]
+        L.sda_attn_fwd.argtypes = [pr, vp, vp, vp, vp, i32, i32, vp, vp, vp, i32, vp]
         L.sda_attn_bwd.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
         L.sda_attn_bwd_prepare.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sda_attn_fwd_train.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sda_attn_bwd_train.argtypes = [pr, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, vp]
         L.sda_attn_bwd_partition.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, vp, sz,
                                              vp]
         L.sda_attn_bwd_dq.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
@@ -142,11 +145,15 @@ def sda_predict_blocks(p, Q, K, Wq, Wk, block_idx, block_score=None, ws=None, st
            "sda_predict_blocks")
 
 
-def sda_attn_fwd(p, Q, K, V, block_idx, O, LSE, kb_begin=0, kb_end=None, qb_active=None, stream=None):
+def sda_attn_fwd(p, Q, K, V, block_idx, O, LSE, kb_begin=0, kb_end=None, qb_active=None, stream=None,
+                 out_dtype=None):
+    """out_dtype: None (the problem's dtype), "f32" or "bf16"."""
     if kb_end is None:
         kb_end = sda_num_blocks(p)[0]
+    od = p.dtype if out_dtype is None else {"f32": SDA_F32, "bf16": SDA_BF16}.get(out_dtype, out_dtype)
     _check(lib().sda_attn_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(block_idx), int(kb_begin),
-                              int(kb_end), _ptr(qb_active), _ptr(O), _ptr(LSE), _stream(stream)), "sda_attn_fwd")
+                              int(kb_end), _ptr(qb_active), _ptr(O), _ptr(LSE), int(od), _stream(stream)),
+           "sda_attn_fwd")
 
 
 def sda_attn_bwd(p, Q, K, V, O, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, stream=None):
@@ -154,6 +161,18 @@ def sda_attn_bwd(p, Q, K, V, O, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, 
     _check(lib().sda_attn_bwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO),
                               _ptr(block_idx), _ptr(dQ), _ptr(dK), _ptr(dV), int(gd), _wsptr(ws), _nbytes(ws),
                               _stream(stream)), "sda_attn_bwd")
+
+
+def sda_attn_fwd_train(p, Q, K, V, block_idx, O, LSE, ws, stream=None):
+    _check(lib().sda_attn_fwd_train(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(block_idx), _ptr(O), _ptr(LSE),
+                                    _wsptr(ws), _nbytes(ws), _stream(stream)), "sda_attn_fwd_train")
+
+
+def sda_attn_bwd_train(p, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, phases=7, stream=None):
+    gd = {"f32": SDA_F32, "bf16": SDA_BF16}.get(grad_dtype, grad_dtype)
+    _check(lib().sda_attn_bwd_train(ctypes.byref(p), _ptr(LSE), _ptr(dO), _ptr(block_idx), _ptr(dQ), _ptr(dK),
+                                    _ptr(dV), int(gd), int(phases), _wsptr(ws), _nbytes(ws), _stream(stream)),
+           "sda_attn_bwd_train")
 
 
 def sda_attn_bwd_partition(p, Q, K, V, O, LSE, dO, dLSE, block_idx, dQ, dK, dV, grad_dtype, ws, kb_begin=0,

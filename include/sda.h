@@ -86,7 +86,7 @@ typedef struct {
 } sda_problem;
 
 /* Workspace queries (op argument of sda_workspace_size). */
-enum { SDA_OP_PREDICT = 0, SDA_OP_BWD = 1 };
+enum { SDA_OP_PREDICT = 0, SDA_OP_BWD = 1, SDA_OP_TRAIN = 2 };
 
 /* Host only.  n_blocks = nT*nH*nW and k = kept key blocks per query block. */
 sda_status sda_num_blocks(const sda_problem* p, int* n_blocks, int* k);
@@ -117,11 +117,17 @@ sda_status sda_predict_blocks(const sda_problem* p, const void* Q, const void* K
  *   qb_active  optional [n_b] uint8; query blocks with 0 are not written at all
  *              (their O and LSE rows keep the caller's previous contents — the
  *              cached state of DiTango's reuse).  NULL = all active.
- *   O          out [B, N, heads, d] (dtype);  LSE out [B, heads, N] fp32.
- * A row whose block has no kept key in the range gets O = 0, LSE = -inf. */
+ *   O          out [B, N, heads, d] in out_dtype: p->dtype, or SDA_F32 (for
+ *              a bf16 problem: O before any rounding to bf16 — the form to
+ *              keep partition states in when they will be merged, so that
+ *              the merged result is rounded once, not twice);
+ *   LSE        out [B, heads, N] fp32.
+ * A row whose block has no kept key in the range gets O = 0, LSE = -inf.  On
+ * the bf16 path P enters the P V product as two bf16 terms (the value and its
+ * rounding remainder), so O is exact to fp32 accumulation. */
 sda_status sda_attn_fwd(const sda_problem* p, const void* Q, const void* K, const void* V,
                         const int32_t* block_idx, int kb_begin, int kb_end, const uint8_t* qb_active,
-                        void* O, float* LSE, void* stream);
+                        void* O, float* LSE, int out_dtype, void* stream);
 
 /* Step 2b: gradients of sda_attn_fwd (full key range) with the map fixed.
  *   O, LSE      the forward outputs;  dO [B, N, heads, d] (dtype)
@@ -159,6 +165,36 @@ sda_status sda_attn_bwd_dq(const sda_problem* p, const void* Q, const void* K, c
 sda_status sda_attn_bwd_dkdv(const sda_problem* p, const void* Q, const void* K, const void* V, const float* LSE,
                              const void* dO, const int32_t* block_idx, void* dK, void* dV, int grad_dtype, void* ws,
                              size_t ws_bytes, void* stream);
+
+/* The training pair: a forward that keeps what its backward needs, and that
+ * backward.  Same attention as sda_attn_fwd over the whole key range and
+ * sda_attn_bwd, computed with finer intermediates and fewer products
+ * (tensor-core path only: dtype SDA_BF16).
+ *
+ * sda_attn_fwd_train writes fp16 copies of Q, K and V into ws (exact for bf16
+ * values inside fp16's range; a value outside it latches SDA_ERR_DEVICE_RANGE),
+ * runs the forward on them with P rounded to fp16 (eight times finer than the
+ * bf16 P of sda_attn_fwd), writes O (dtype) and LSE like sda_attn_fwd and also
+ * keeps O in fp32 in ws.
+ *
+ * sda_attn_bwd_train then computes dQ, dK, dV (grad_dtype: SDA_F32 or dtype)
+ * for the same problem, block_idx and ws: D_i = dO_i . O_i is taken from the
+ * fp32 O, which is exact enough that dS = P (dP - D) needs no correction, so
+ * the dQ pass runs three products per kept block instead of the four of
+ * sda_attn_bwd.  Deterministic, no atomics on gradient values.  `phases`
+ * selects its steps, in this order (pass 7 for all): 1 prepares (block-map
+ * transpose, fp16 copy of dO, D and the LSE rows), 2 computes dQ, 4 computes dK
+ * and dV; a call with a subset is for timing the steps.
+ *   ws   at least sda_workspace_size(SDA_OP_TRAIN) bytes, 16-byte aligned;
+ *        between the two calls the caller keeps it (and block_idx, LSE) intact.
+ * Errors and alignment as sda_attn_fwd / sda_attn_bwd; SDA_ERR_UNSUPPORTED for
+ * SDA_F32 problems. */
+sda_status sda_attn_fwd_train(const sda_problem* p, const void* Q, const void* K, const void* V,
+                              const int32_t* block_idx, void* O, float* LSE, void* ws, size_t ws_bytes,
+                              void* stream);
+sda_status sda_attn_bwd_train(const sda_problem* p, const float* LSE, const void* dO, const int32_t* block_idx,
+                              void* dQ, void* dK, void* dV, int grad_dtype, int phases, void* ws, size_t ws_bytes,
+                              void* stream);
 
 /* Backward of one partition state, for training through DiTango's state reuse:
  * the gradient with respect to Q, K, V of the state (O_p, LSE_p) that

@@ -109,10 +109,12 @@ def test_null_and_range_arguments_return_before_any_launch(L):
     # null tensors: rejected synchronously, no CUDA call is made
     assert L.sda_predict_blocks(ctypes.byref(p), None, None, None, None, None, None, None, 0, None) == \
         sda.SDA_ERR_INVALID_ARG
-    assert L.sda_attn_fwd(ctypes.byref(p), 16, 16, 16, 16, 0, 99, None, 16, 16, None) == sda.SDA_ERR_INVALID_ARG
-    assert L.sda_attn_fwd(ctypes.byref(p), 16, 16, 16, 16, 3, 2, None, 16, 16, None) == sda.SDA_ERR_INVALID_ARG
+    assert L.sda_attn_fwd(ctypes.byref(p), 16, 16, 16, 16, 0, 99, None, 16, 16, 1, None) == sda.SDA_ERR_INVALID_ARG
+    assert L.sda_attn_fwd(ctypes.byref(p), 16, 16, 16, 16, 3, 2, None, 16, 16, 1, None) == sda.SDA_ERR_INVALID_ARG
     # misaligned pointers on the tensor-core path
-    assert L.sda_attn_fwd(ctypes.byref(p), 18, 16, 16, 16, 0, 2, None, 16, 16, None) == sda.SDA_ERR_INVALID_ARG
+    assert L.sda_attn_fwd(ctypes.byref(p), 18, 16, 16, 16, 0, 2, None, 16, 16, 1, None) == sda.SDA_ERR_INVALID_ARG
+    # bad output dtype
+    assert L.sda_attn_fwd(ctypes.byref(p), 16, 16, 16, 16, 0, 2, None, 16, 16, 5, None) == sda.SDA_ERR_INVALID_ARG
     # workspace too small
     assert L.sda_predict_blocks(ctypes.byref(p), 16, 16, 16, 16, 16, None, 16, 8, None) == sda.SDA_ERR_WORKSPACE
     # bad gradient dtype
@@ -154,6 +156,25 @@ def test_training_through_the_merge_validates_on_the_host(L):
         sda.SDA_ERR_WORKSPACE
     assert bp(ctypes.byref(p), *t[:4], 16, t[4], None, 16, 0, 2, None, None, 16, 16, 1, 16, 1 << 40, None) == \
         sda.SDA_ERR_INVALID_ARG
+
+
+def test_training_pair_validates_on_the_host(L):
+    p = _bad({})
+    ws_need = sda.sda_workspace_size(p, sda.SDA_OP_TRAIN)
+    assert ws_need > sda.sda_workspace_size(p, sda.SDA_OP_BWD)  # + the fp32 O
+    fw, bw = L.sda_attn_fwd_train, L.sda_attn_bwd_train
+    assert fw(ctypes.byref(p), None, 16, 16, 16, 16, 16, 16, ws_need, None) == sda.SDA_ERR_INVALID_ARG
+    assert fw(ctypes.byref(p), 18, 16, 16, 16, 16, 16, 16, ws_need, None) == sda.SDA_ERR_INVALID_ARG  # misaligned
+    assert fw(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, ws_need - 1, None) == sda.SDA_ERR_WORKSPACE
+    assert bw(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 1, 0, 16, ws_need, None) == sda.SDA_ERR_INVALID_ARG  # phases
+    assert bw(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 1, 8, 16, ws_need, None) == sda.SDA_ERR_INVALID_ARG
+    assert bw(ctypes.byref(p), 16, 16, 16, None, 16, 16, 1, 2, 16, ws_need, None) == sda.SDA_ERR_INVALID_ARG  # dQ
+    assert bw(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 5, 7, 16, ws_need, None) == sda.SDA_ERR_INVALID_ARG  # dtype
+    assert bw(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 1, 7, 16, ws_need - 1, None) == sda.SDA_ERR_WORKSPACE
+    f32 = _bad({"dtype": "f32"})
+    with pytest.raises(sda.SdaError) as e:
+        sda.sda_workspace_size(f32, sda.SDA_OP_TRAIN)
+    assert e.value.status == sda.SDA_ERR_UNSUPPORTED
 
 
 def test_status_strings(L):

@@ -173,7 +173,7 @@ def test_train_524k_predictor_and_forward_sampled(sda, parity_report):
 
 
 def test_train_524k_backward_on_predictor_rows(sda, parity_report):
-    """The backward at 524,288 tokens, as bench.py runs it (fp32 gradients).  The map: for heads 1 and 6,
+    """The training pair (forward and backward) at 524,288 tokens, as bench.py runs it (fp32 gradients).  The map: for heads 1 and 6,
     16 seeded query blocks (plus first, middle, last) keep the oracle predictor's own rows; every other
     row comes from the seeded scattered generator.  Checked: dQ of those query blocks; dK and dV of 8 key
     blocks per head, among them the key block with the shortest list of query blocks (both heads) and
@@ -198,10 +198,10 @@ def test_train_524k_backward_on_predictor_rows(sda, parity_report):
     idx = torch.from_numpy(m).cuda()
     O = torch.empty_like(Q)
     LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
-    sda.sda_attn_fwd(p, Q, K, V, idx, O, LSE)
     dQ, dK, dV = (torch.empty(Q.shape, dtype=torch.float32, device="cuda") for _ in range(3))
-    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device="cuda")
-    sda.sda_attn_bwd(p, Q, K, V, O, LSE, dO, idx, dQ, dK, dV, "f32", ws)
+    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_TRAIN), dtype=torch.uint8, device="cuda")
+    sda.sda_attn_fwd_train(p, Q, K, V, idx, O, LSE, ws)  # the training pair, as bench.py runs it
+    sda.sda_attn_bwd_train(p, LSE, dO, idx, dQ, dK, dV, "f32", ws)
     torch.cuda.synchronize()
     del ws
     assert sda.sda_get_device_status() == sda.SDA_OK
@@ -251,8 +251,8 @@ def _tile_classes(geom):
 
 
 def test_merge_131k_partition_states_and_reuse_every_head(sda, parity_report):
-    """131,040 tokens on a ragged grid, 4 frame partitions, the 2 farthest reused from the previous step:
-    all 16 heads, each on 8 seeded query blocks plus one block of every clipped-tile class (full 2x8x8,
+    """131,040 tokens on a ragged grid, 4 frame partitions, the 2 farthest reused from the previous step, the
+    partition states kept in fp32 (so the merged result is rounded once): all 16 heads, each on 8 seeded query blocks plus one block of every clipped-tile class (full 2x8x8,
     1x8x8, 2x4x8, 1x4x8) and the last block of partition 0's reuse set.  Checked per head: the selection
     of both steps (gap rule), every partition state the GPU keeps (reused or fresh), the reuse merge, the
     exact merge of fresh states, and the full-range forward; the reuse merge's deviation from the exact
@@ -288,28 +288,31 @@ def test_merge_131k_partition_states_and_reuse_every_head(sda, parity_report):
             rows[h] = r
         return idx, rows
 
-    def new_state():
-        return torch.empty_like(T["Q"]), torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    def new_state():  # partition states are kept in fp32 (sda_attn_fwd's out_dtype), merged in fp32
+        return (torch.empty(T["Q"].shape, dtype=torch.float32, device="cuda"),
+                torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda"))
 
     idx_prev, rows_prev = gpu_map("Qp", "Kp")
     idx_now, rows_now = gpu_map("Q", "K")
     # previous step: every partition state for every query block (the reuse cache)
     states = [new_state() for _ in range(P)]
     for (b0, b1), (Op, Lp) in zip(bounds, states):
-        sda.sda_attn_fwd(p, T["Qp"], T["Kp"], T["Vp"], idx_prev, Op, Lp, kb_begin=b0, kb_end=b1)
+        sda.sda_attn_fwd(p, T["Qp"], T["Kp"], T["Vp"], idx_prev, Op, Lp, kb_begin=b0, kb_end=b1, out_dtype="f32")
     # current step: recompute the near partitions only, in place
     for q, ((b0, b1), (Op, Lp)) in enumerate(zip(bounds, states)):
         act = torch.from_numpy((~reuse[q]).astype(np.uint8)).cuda()
-        sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Op, Lp, kb_begin=b0, kb_end=b1, qb_active=act)
+        sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Op, Lp, kb_begin=b0, kb_end=b1, qb_active=act,
+                         out_dtype="f32")
     Om, Lm = new_state()
-    sda.sda_merge_states([s[0] for s in states], [s[1] for s in states], 1, wl.N, wl.heads, wl.d, "bf16", Om, Lm)
+    sda.sda_merge_states([s[0] for s in states], [s[1] for s in states], 1, wl.N, wl.heads, wl.d, "f32", Om, Lm)
     # exact merge of fresh states equals the full-range forward
     fresh = [new_state() for _ in range(P)]
     for (b0, b1), (Op, Lp) in zip(bounds, fresh):
-        sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Op, Lp, kb_begin=b0, kb_end=b1)
+        sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Op, Lp, kb_begin=b0, kb_end=b1, out_dtype="f32")
     Oe, Le = new_state()
-    sda.sda_merge_states([s[0] for s in fresh], [s[1] for s in fresh], 1, wl.N, wl.heads, wl.d, "bf16", Oe, Le)
-    Of, Lf = new_state()
+    sda.sda_merge_states([s[0] for s in fresh], [s[1] for s in fresh], 1, wl.N, wl.heads, wl.d, "f32", Oe, Le)
+    Of = torch.empty_like(T["Q"])  # the full-range forward in the problem's dtype
+    Lf = torch.empty((1, wl.heads, wl.N), dtype=torch.float32, device="cuda")
     sda.sda_attn_fwd(p, T["Q"], T["K"], T["V"], idx_now, Of, Lf)
     torch.cuda.synchronize()
     assert sda.sda_get_device_status() == sda.SDA_OK

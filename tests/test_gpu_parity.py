@@ -445,3 +445,100 @@ def test_value_outside_fp16_range_is_reported(sda):
     refs = orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], ref_idx, geom)
     for name, got, ref in zip(("dQ", "dK", "dV"), g, refs):
         assert_close(host(got), ref, wl.dtype, name)
+
+
+def _ws(sda, p, op):
+    return torch.empty(sda.sda_workspace_size(p, op), dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("wl", [w for w in SMALL if w.dtype == "bf16"], ids=lambda w: w.name)
+@pytest.mark.parametrize("gdt", ["f32", "same"])
+def test_training_pair_matches_oracle(sda, wl, gdt):
+    """sda_attn_fwd_train + sda_attn_bwd_train (fp16 operand copies, fp16 P, D from the fp32 O) against the
+    oracle's forward and backward on the oracle's map, at the same bounds as the other paths."""
+    gdt = wl.dtype if gdt == "same" else gdt
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk"))
+    geom = _geom(wl)
+    ref_idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    p = sda.problem_from_workload(wl)
+    t = {n: dev(x[n], wl.dtype) for n in ("Q", "K", "V", "dO")}
+    ti = torch.from_numpy(ref_idx).cuda()
+    ws = _ws(sda, p, sda.SDA_OP_TRAIN)
+    O = torch.full_like(t["Q"], float("nan"))
+    LSE = torch.full((wl.B, wl.heads, wl.N), float("nan"), dtype=torch.float32, device="cuda")
+    sda.sda_attn_fwd_train(p, t["Q"], t["K"], t["V"], ti, O, LSE, ws)
+    gt = torch.float32 if gdt == "f32" else torch.bfloat16
+    dQ, dK, dV = (torch.full(O.shape, float("nan"), dtype=gt, device="cuda") for _ in range(3))
+    sda.sda_attn_bwd_train(p, LSE, t["dO"], ti, dQ, dK, dV, gdt, ws)
+    torch.cuda.synchronize()
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    O_ref, L_ref = orc.attn_fwd(x["Q"], x["K"], x["V"], ref_idx, geom)
+    assert_close(host(O), O_ref, wl.dtype, "O (training forward)")
+    assert_close(host(LSE), L_ref, wl.dtype, "LSE (training forward)")
+    refs = orc.attn_bwd(x["Q"], x["K"], x["V"], x["dO"], ref_idx, geom)
+    for name, got, ref in zip(("dQ", "dK", "dV"), (dQ, dK, dV), refs):
+        assert_close_stored(host(got), ref, wl.dtype, gdt, name + " (training backward)")
+
+
+def test_training_backward_phases_equal_the_single_call_bitwise(sda):
+    wl = RAGGED_D128
+    x = inputs.generate(wl, names=("Q", "K", "V", "dO", "Wq", "Wk"))
+    geom = _geom(wl)
+    ref_idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    p = sda.problem_from_workload(wl)
+    t = {n: dev(x[n], wl.dtype) for n in ("Q", "K", "V", "dO")}
+    ti = torch.from_numpy(ref_idx).cuda()
+    ws = _ws(sda, p, sda.SDA_OP_TRAIN)
+    O = torch.empty_like(t["Q"])
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_attn_fwd_train(p, t["Q"], t["K"], t["V"], ti, O, LSE, ws)
+    a = [torch.empty(O.shape, dtype=torch.float32, device="cuda") for _ in range(3)]
+    b = [torch.empty_like(a[0]) for _ in range(3)]
+    sda.sda_attn_bwd_train(p, LSE, t["dO"], ti, *a, "f32", ws)
+    for ph in (1, 2, 4):
+        sda.sda_attn_bwd_train(p, LSE, t["dO"], ti, *b, "f32", ws, phases=ph)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    # the training forward's O agrees with the inference forward's on the same map
+    O2 = torch.empty_like(O)
+    L2 = torch.empty_like(LSE)
+    sda.sda_attn_fwd(p, t["Q"], t["K"], t["V"], ti, O2, L2)
+    torch.cuda.synchronize()
+    assert float((O.float() - O2.float()).abs().max()) < 2e-2
+    assert float((LSE - L2).abs().max()) < 2e-2
+
+
+@pytest.mark.parametrize("wl", [RAGGED_D64, RAGGED_D128, TILE_1X8X16], ids=lambda w: w.name)
+def test_forward_fp32_output_matches_oracle(sda, wl):
+    """sda_attn_fwd with out_dtype fp32 on a bf16 problem (the partition-state form): O before any rounding,
+    so it must sit well inside the bf16 bound (P enters P V as two bf16 terms; the rest is fp32 accumulation).
+    Also over a key range with inactive query blocks, whose rows keep the caller's contents."""
+    x = inputs.generate(wl, names=("Q", "K", "V", "Wq", "Wk"))
+    geom = _geom(wl)
+    nb = geom.n_blocks
+    ref_idx, _ = orc.predict_blocks(x["Q"], x["K"], x["Wq"], x["Wk"], geom, wl.keep, wl.dtype)
+    p = sda.problem_from_workload(wl)
+    Q, K, V = (dev(x[n], wl.dtype) for n in ("Q", "K", "V"))
+    ti = torch.from_numpy(ref_idx).cuda()
+    O = torch.full(Q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    LSE = torch.full((wl.B, wl.heads, wl.N), float("nan"), dtype=torch.float32, device="cuda")
+    sda.sda_attn_fwd(p, Q, K, V, ti, O, LSE, out_dtype="f32")
+    torch.cuda.synchronize()
+    O_ref, L_ref = orc.attn_fwd(x["Q"], x["K"], x["V"], ref_idx, geom)
+    mx, _ = assert_close(host(O), O_ref, wl.dtype, "O (fp32 output)")
+    assert mx < 1e-3, mx
+    assert_close(host(LSE), L_ref, wl.dtype, "LSE")
+    act = np.arange(nb) % 3 != 1
+    b0, b1 = nb // 3, nb
+    O.fill_(7.0)
+    LSE.fill_(7.0)
+    sda.sda_attn_fwd(p, Q, K, V, ti, O, LSE, kb_begin=b0, kb_end=b1, out_dtype="f32",
+                     qb_active=torch.from_numpy(act.astype(np.uint8)).cuda())
+    torch.cuda.synchronize()
+    O_ref, L_ref = orc.attn_fwd(x["Q"], x["K"], x["V"], ref_idx, geom, kb_begin=b0, kb_end=b1, qb_active=act,
+                                out=(np.full((wl.B, wl.N, wl.heads, wl.d), 7.0), np.full((wl.B, wl.heads, wl.N), 7.0)))
+    mx, _ = assert_close(host(O), O_ref, wl.dtype, "O (fp32 output, key range)")
+    assert mx < 1e-3, mx
+    assert_close(host(LSE), L_ref, wl.dtype, "LSE (key range)")
+    assert sda.sda_get_device_status() == sda.SDA_OK
