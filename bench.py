@@ -54,10 +54,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 #       python profile_step.py --workload train_524k --heads 1 --steps 1 --warmup 1
 # An entry goes back to None whenever its kernel changes, until it is captured again.
 NCU_COUNTERS = {
-    "score_kernel": {"dram_bytes": 0.583e9 + 0.105e9, "tensor_active": 0.429},
-    "fwd_tc_kernel": None,
-    "dqx_kernel": None,
-    "dkdv_kernel": {"dram_bytes": 143.499e9 + 4.275e9, "tensor_active": 0.55},
+    "score_kernel": {"dram_bytes": 8 * (0.0684e9 + 0.0051e9), "tensor_active": 0.527},
+    "fwd_tc_kernel": {"dram_bytes": 8 * (6.807e9 + 0.570e9), "tensor_active": 0.533},
+    "dqx_kernel": {"dram_bytes": 8 * (6.916e9 + 0.263e9), "tensor_active": 0.699},
+    "dkdv_kernel": {"dram_bytes": 8 * (15.158e9 + 0.520e9), "tensor_active": 0.659},
 }
 
 GAP_REL = 1e-3  # selection rows whose k-th / (k+1)-th score gap is below this (relative) are near-ties

@@ -9,8 +9,10 @@ and sda_merge_states_bwd once per step.
 
 A small driver for inspecting the kernels (e.g. under a profiler) on a chosen
 workload: inputs come from the seeded generator, every step runs all the
-calls of the path on the current stream, and the per-call times (CUDA
-events) are printed as one JSON line.  The library must be built.
+calls of the path on the current stream (with a backward, the training pair:
+sda_attn_fwd_train and the three phases of sda_attn_bwd_train), and the
+per-call times (CUDA events) are printed as one JSON line.  The library must
+be built.
 """
 from __future__ import annotations
 
@@ -53,9 +55,9 @@ def main():
     O = torch.empty_like(d["Q"])
     LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
     ws_p = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICT), dtype=torch.uint8, device="cuda")
-    if backward:
+    if backward:  # the training pair, as bench.py runs it
         grads = [torch.empty(d["Q"].shape, dtype=torch.float32, device="cuda") for _ in range(3)]
-        ws_b = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_BWD), dtype=torch.uint8, device="cuda")
+        ws_t = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_TRAIN), dtype=torch.uint8, device="cuda")
     st = torch.cuda.current_stream()
     names_t = ["predict", "fwd"] + (["bwd_prepare", "bwd_dq", "bwd_dkdv"] if backward else [])
 
@@ -63,15 +65,15 @@ def main():
         ev[0].record(st)
         sda.sda_predict_blocks(p, d["Q"], d["K"], d["Wq"], d["Wk"], idx, None, ws_p, st)
         ev[1].record(st)
-        sda.sda_attn_fwd(p, d["Q"], d["K"], d["V"], idx, O, LSE, stream=st)
-        ev[2].record(st)
         if backward:
-            sda.sda_attn_bwd_prepare(p, d["Q"], d["K"], d["V"], O, LSE, d["dO"], idx, ws_b, st)
-            ev[3].record(st)
-            sda.sda_attn_bwd_dq(p, d["Q"], d["K"], d["V"], LSE, d["dO"], idx, grads[0], "f32", ws_b, st)
-            ev[4].record(st)
-            sda.sda_attn_bwd_dkdv(p, d["Q"], d["K"], d["V"], LSE, d["dO"], idx, grads[1], grads[2], "f32", ws_b, st)
-            ev[5].record(st)
+            sda.sda_attn_fwd_train(p, d["Q"], d["K"], d["V"], idx, O, LSE, ws_t, stream=st)
+            ev[2].record(st)
+            for i, ph in enumerate((1, 2, 4)):
+                sda.sda_attn_bwd_train(p, LSE, d["dO"], idx, *grads, "f32", ws_t, phases=ph, stream=st)
+                ev[3 + i].record(st)
+        else:
+            sda.sda_attn_fwd(p, d["Q"], d["K"], d["V"], idx, O, LSE, stream=st)
+            ev[2].record(st)
 
     times = {n: [] for n in names_t}
     for s in range(args.warmup + args.steps):
