@@ -17,32 +17,28 @@
 //
 // One CTA per (query block, head); 12 warps:
 //   warps 0, 2  TMA producers: Q once and the K tiles of each kept block
-//               (warp 0), the V tiles (warp 2), through separate rings so K
-//               can be fetched further ahead (the tile box *is* the
-//               space-time tile, so no token reordering pass exists).  Warp 0
-//               also arrives on P_j's barrier once K_{j+2} has landed.
+//               (warp 0), the V tiles (warp 2), through separate rings (the
+//               tile box *is* the space-time tile, so no token reordering pass
+//               exists).
 //   warp 1      TMEM owner and MMA issuer (converged warp, one elected lane):
-//               S_j = Q K_j^T into one of two TMEM S buffers, then, once P_j
-//               is ready, O_0 += P_j[:, keys 0-63] V_j[0-63] and
-//               O_1 += P_j[:, keys 64-127] V_j[64-127] with P_j read from TMEM
-//               (in bf16 twice, P_hi then P_lo).
+//               S_j = Q K_j^T into one of three TMEM S buffers, up to three
+//               blocks ahead of the softmax; once P_j is ready, O += P_j V_j
+//               with P_j read from TMEM (in bf16 twice, P_hi then P_lo), then
+//               S_{j+3} into the buffer P_j leaves.
 //   warps 4-11  softmax: two warps per query row quarter (thread = row = TMEM
-//               lane); warp half hf owns key columns [64 hf, 64 hf + 64) of
-//               every S tile, with its own running max, its own sums and its
-//               own accumulator O_hf, so the two warps never wait for each
-//               other inside the loop; the two partial states merge once at
-//               the end with log-sum-exp weights.  Online softmax in base 2
-//               with a lazy rescale: O_hf and its sums are rescaled only when
-//               the half-row max grows by more than 2^8, which is exact because
-//               they always share one reference max.  P overwrites S: in fp16,
-//               or in bf16 as P_hi + P_lo (the remainder), both fed to the P V
-//               product, so that O is accurate to fp32 accumulation and not to
-//               bf16's 8 bits; one fp32 sum of P divides O and gives LSE.
-//   warp 3      arrives on P_j's barrier once V_j has landed: with the two
-//               producer arrivals that barrier covers every input of P_j V_j
-//               and of S_{j+2}, so the MMA warp waits once per block.
-// TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,256+D) O_0,
-// [256+D,256+2D) O_1.
+//               lane), each owning 64 of the 128 key columns; the pair swaps
+//               its half-row maxima at a named barrier.  Online softmax in
+//               base 2 with a lazy rescale: O and the sums are rescaled only
+//               when the row max grows by more than 2^15 (fp16 P) or 2^30
+//               (bf16 P), which is exact because they always share one
+//               reference max.  P overwrites S: in fp16, or in bf16 as
+//               P_hi + P_lo (the remainder), both fed to the P V product, so
+//               that O is accurate to fp32 accumulation and not to bf16's 8
+//               bits; one fp32 sum of P divides O and gives LSE.
+//   warp 3      arrives on P_j's barrier once V_j has landed, so that barrier
+//               covers every input of P_j V_j and the MMA warp waits once per
+//               block for it.
+// TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,384) S2/P2, [384,384+D) O.
 #include "internal.h"
 
 namespace sda {
@@ -61,10 +57,18 @@ struct FwdArgs {
   unsigned* status;
 };
 
-constexpr int kThreads = 384;  // warps 0, 2 TMA, warp 1 MMA, warps 4-11 softmax
-// P_j barrier: the 256 softmax threads, the K producer (K_{j+2} landed) and warp 3 (V_j landed).
-constexpr int kPfullCount = 256 + 2;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kThreads = 384;  // warps 0, 2 TMA, warp 1 MMA, warp 3 V arrivals, warps 4-11 softmax
+constexpr int kSBufs = 3;      // S / P buffers in TMEM: S runs up to three blocks ahead of P V
+// P_j barrier: the 256 softmax threads and warp 3 (V_j landed).
+constexpr int kPfullCount = 256 + 1;
+// Lazy rescale: O_hf and its sum are rescaled only when the half-row max grows by more
+// than this many powers of two (P then stays below 2^threshold).  fp16 holds P up to
+// 2^15 (65504 max); bf16 up to about 2^127, and the fp32 accumulators far more, so bf16
+// takes 2^30.  Fewer rescales means fewer waits for the previous P V product.
+template <bool kF16>
+__device__ __forceinline__ float rescale_threshold() {
+  return kF16 ? 15.0f : 30.0f;
+}
 constexpr int kSeenWords = 8192 / 32;       // one bit per key block (n_b <= 8192)
 
 template <int D>
@@ -142,22 +146,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = sK + KST * C::TILE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::SMEM_TILES);
   uint64_t* qfull = bars;
-  uint64_t* kfull = bars + 1;     // KST
-  uint64_t* kempty = kfull + KST; // KST
-  uint64_t* vfull = kempty + KST; // VST
-  uint64_t* vempty = vfull + VST; // VST
-  uint64_t* sfull = vempty + VST; // 2
-  uint64_t* pfull = sfull + 2;    // 2
-  uint64_t* odone = pfull + 2;    // 1
-  uint64_t* drain = odone + 1;    // 1
-  uint64_t* pairbar = drain + 1;  // 4: the two softmax warps of a lane quarter meet here at the end
+  uint64_t* kfull = bars + 1;      // KST
+  uint64_t* kempty = kfull + KST;  // KST
+  uint64_t* vfull = kempty + KST;  // VST
+  uint64_t* vempty = vfull + VST;  // VST
+  uint64_t* sfull = vempty + VST;  // kSBufs
+  uint64_t* pfull = sfull + kSBufs;  // kSBufs
+  uint64_t* odone = pfull + kSBufs;  // 2: P V of blocks of each parity done
+  uint64_t* drain = odone + 2;       // 1
+  uint64_t* pairbar = drain + 1;     // 4: the two softmax warps of a lane quarter meet here at the end
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pairbar + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   int* n_sel_s = abort_flag + 1;
   int* warp_cnt = n_sel_s + 1;  // 16
-  float* half_st = reinterpret_cast<float*>(warp_cnt + 16);  // [2 halves][m, l][128 rows]
-  unsigned* seen = reinterpret_cast<unsigned*>(half_st + 512);  // kSeenWords: blocks met in this row
-  int* sel = reinterpret_cast<int*>(seen + kSeenWords);         // k
+  float* half_max = reinterpret_cast<float*>(warp_cnt + 16);  // [2 block parities][2 halves][128 rows]
+  float* half_l = half_max + 512;                              // [2 halves][128 rows]
+  unsigned* seen = reinterpret_cast<unsigned*>(half_l + 256);  // kSeenWords: blocks met in this row
+  int* sel = reinterpret_cast<int*>(seen + kSeenWords);        // k
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -170,11 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(vfull + s, 1);
       mbar_init(vempty + s, 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSBufs; ++s) {
       mbar_init(sfull + s, 1);
       mbar_init(pfull + s, kPfullCount);
     }
     mbar_init(odone, 1);
+    mbar_init(odone + 1, 1);
     mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) mbar_init(pairbar + q, 2);
     *abort_flag = 0;
@@ -220,13 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------- producers
-    // warp 0: Q once, then the K tiles of the kept blocks (a KST-deep ring, freed as
-    // soon as S_j is computed); warp 2: the V tiles (a VST-deep ring, freed after P_j V_j).
+    // warp 0: Q once, then the K tiles of the kept blocks (a KST-deep ring, a slot freed
+    // once its S is computed); warp 2: the V tiles (a VST-deep ring, freed after P V).
     const bool is_k = warp == 0;
     if (lane == 0 && n_sel > 0) {
       const int RS = is_k ? KST : VST;
       uint8_t* ring = is_k ? sK : sV;
       uint64_t* full = is_k ? kfull : vfull;
+      uint64_t* empty = is_k ? kempty : vempty;
       const CUtensorMap* map = is_k ? &tmK : &tmV;
       prefetch_tmap(map);
       if (is_k) {
@@ -235,37 +242,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) tma_load_5d(sQ + c * 16384, &tmQ, qfull, c * 64, h, w0, h0, t0);
       }
-      auto issue = [&](int i) {
-        const int s = i % RS;
+      int issued = 0;
+      for (; issued < n_sel; ++issued) {
+        const int i = issued, s = i % RS;
+        if (i >= RS && !mbar_wait(empty + s, ((i / RS) - 1) & 1, a.status, abort_flag)) break;
         int jt0, jh0, jw0;
         block_origin(a.g, sel[i], jt0, jh0, jw0);
         mbar_expect_tx(full + s, C::TILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c)
           tma_load_5d(ring + s * C::TILE + c * 16384, map, full + s, c * 64, h, jw0, jh0, jt0);
-      };
-      int issued = 0;
-      for (; issued < RS && issued < n_sel; ++issued) issue(issued);
-      if (is_k) {
-        // Arrive on pfull_j once K_{j+2} has landed (S_{j+2} is issued after the MMA
-        // warp's pfull_j wait, without a wait of its own); then refill the slot of K_j.
-        for (int j = 0; j < n_sel; ++j) {
-          const int t = j + 2;  // issued already: t < j + KST
-          if (t < n_sel && !mbar_wait(kfull + t % KST, (t / KST) & 1, a.status, abort_flag)) break;
-          // phase j - 2 of the same barrier completes before this arrival for phase j
-          if (j >= 2 && !mbar_wait(pfull + (j & 1), ((j >> 1) - 1) & 1, a.status, abort_flag)) break;
-          mbar_arrive(pfull + (j & 1));
-          if (issued < n_sel) {  // issued == j + KST: it reuses the slot of K_j
-            if (!mbar_wait(kempty + j % KST, (j / KST) & 1, a.status, abort_flag)) break;
-            issue(issued++);
-          }
-        }
-      } else {
-        for (; issued < n_sel; ++issued) {
-          const int i = issued;
-          if (!mbar_wait(vempty + i % VST, ((i / VST) - 1) & 1, a.status, abort_flag)) break;
-          issue(i);
-        }
       }
       if (*abort_flag) {  // let copies in flight land before the CTA exits
         if (is_k) wait_plain(qfull, 0);
@@ -279,16 +265,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int j = 0; j < n_sel; ++j) {
         if (!mbar_wait(vfull + j % VST, (j / VST) & 1, a.status, abort_flag)) break;
-        if (j >= 2 && !mbar_wait(pfull + (j & 1), ((j >> 1) - 1) & 1, a.status, abort_flag)) break;
-        mbar_arrive(pfull + (j & 1));
+        // phase j - kSBufs of the same barrier completes before this arrival for phase j
+        if (j >= kSBufs && !mbar_wait(pfull + j % kSBufs, ((j / kSBufs) - 1) & 1, a.status, abort_flag)) break;
+        mbar_arrive(pfull + j % kSBufs);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     // Whole warp, one elected lane issues; descriptors advance by adding to the
-    // start-address field (16-byte units).  One wait per block: pfull_j (softmax of
-    // block j done, V_j and K_{j+2} landed); only K_0 and K_1 are waited on directly.
+    // start-address field (16-byte units).  S runs kSBufs blocks ahead: S_0 .. S_2 as
+    // their K tiles land, then per block j: wait for pfull_j (softmax of block j done,
+    // V_j landed), P_j V_j, then S_{j+3} into the buffer P_j leaves (the tensor pipe runs
+    // its products in order, so P_j is read before S_{j+3} overwrites it) once K_{j+3}
+    // has landed.
     if (n_sel > 0) {
       const uint32_t leader = elect_leader();
       constexpr uint32_t idS = kF16 ? idesc_f16(128, 128, 0, 0) : idesc_bf16(128, 128, 0, 0);
@@ -296,12 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024, 2);
       const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, 2);
       const uint64_t dV = smem_desc(smem_u32(sV), 16384, 1024, 2);
-      const uint32_t tO = tmem + 256;
-      // Every issue_S follows a wait and its tcgen05 fence: kfull for K_0 and K_1,
-      // pfull_{j-2} (K_j landed, P_{j-2} consumed) after that.
-      auto issue_S = [&](int j) {
-        const int s = j % KST;
-        const uint32_t tS = tmem + (j & 1) * 128;
+      const uint32_t tO = tmem + kSBufs * 128;
+      auto issue_S = [&](int t) {
+        const int s = t % KST;
+        const uint32_t tS = tmem + (t % kSBufs) * 128;
         const uint64_t dKs = dK + (uint64_t)((s * C::TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -309,39 +297,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 2;  // 64-column chunk, 16-column step
           mma_ss_by(leader, tS, dQ + off, dKs + off, idS, kk > 0);
         }
-        mma_commit_by(leader, sfull + (j & 1));
-        mma_commit_by(leader, kempty + s);  // K_j is no longer needed once S_j is done
+        mma_commit_by(leader, sfull + t % kSBufs);
+        mma_commit_by(leader, kempty + s);  // K_t is no longer needed once S_t is done
       };
-      bool ok = warp_wait(qfull, 0, a.status, abort_flag) && warp_wait(kfull, 0, a.status, abort_flag);
-      if (ok) {
+      bool ok = warp_wait(qfull, 0, a.status, abort_flag);
+      for (int t = 0; ok && t < kSBufs && t < n_sel; ++t) {
+        if (!(ok = warp_wait(kfull + t % KST, (t / KST) & 1, a.status, abort_flag))) break;
         tc_fence_after();
-        issue_S(0);
+        issue_S(t);
       }
       for (int j = 0; ok && j < n_sel; ++j) {
-        if (j + 1 < n_sel) {
-          // K_{j+1} landed: waited directly for K_1, implied by pfull_{j-1} after that
-          if (j == 0) {
-            if (!(ok = warp_wait(kfull + 1 % KST, (1 / KST) & 1, a.status, abort_flag))) break;
-            tc_fence_after();
-          }
-          issue_S(j + 1);
-        }
-        if (!(ok = warp_wait(pfull + (j & 1), (j >> 1) & 1, a.status, abort_flag))) break;
+        if (!(ok = warp_wait(pfull + j % kSBufs, (j / kSBufs) & 1, a.status, abort_flag))) break;
         tc_fence_after();
         const int s = j % VST;
-        const uint32_t tP = tmem + (j & 1) * 128;
+        const uint32_t tP = tmem + (j % kSBufs) * 128;
         const uint64_t dVs = dV + (uint64_t)((s * C::TILE) >> 4);
-        // keys 16 kk .. 16 kk + 15: kk < 4 feed O_0 (the first softmax warp's keys), kk >= 4 O_1;
-        // in bf16 each step takes P_hi, then P_lo (16 columns further)
+        // keys 16 kk .. 16 kk + 15; in bf16 each step takes P_hi, then P_lo (16 columns further)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t tA = tP + (kk >> 1) * 32 + (kk & 1) * 8;
           const uint64_t bV = dVs + (uint64_t)(kk * (2048 >> 4));
-          mma_ts_by(leader, tO + (kk >> 2) * D, tA, bV, idO, (j > 0 || (kk & 3) > 0));
-          if (!kF16) mma_ts_by(leader, tO + (kk >> 2) * D, tA + 16, bV, idO, 1u);
+          mma_ts_by(leader, tO, tA, bV, idO, (j > 0 || kk > 0));
+          if (!kF16) mma_ts_by(leader, tO, tA + 16, bV, idO, 1u);
         }
         mma_commit_by(leader, vempty + s);
-        mma_commit_by(leader, odone);
+        mma_commit_by(leader, odone + (j & 1));
+        const int t = j + kSBufs;
+        if (t < n_sel) {
+          if (!(ok = warp_wait(kfull + t % KST, (t / KST) & 1, a.status, abort_flag))) break;
+          tc_fence_after();
+          issue_S(t);
+        }
       }
       mma_commit_by(leader, drain);
       wait_plain(drain, 0);
@@ -349,108 +335,118 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------- softmax + epilogue
-    // Two warps per TMEM lane quarter; warp half hf owns S columns [64 hf, 64 hf + 64) of
-    // the quarter's 32 rows and its own accumulator O_hf (all D columns).
+    // Two warps per TMEM lane quarter: warp half hf owns S columns [64 hf, 64 hf + 64) and
+    // O columns [hf D/2, (hf + 1) D/2) of the quarter's 32 rows.  The pair swaps its
+    // half-row maxima through shared memory (double-buffered by block parity) at a named
+    // barrier, so both warps hold the same row maxima and take the same rescale
+    // decisions; a bounded wait's failure is ANDed into the same barrier, so both warps
+    // stop at the same point.
     const int quarter = warp & 3, hf = (warp - 4) >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tOh = tmem + 256 + hf * D + lane_base;
+    const uint32_t tO = tmem + kSBufs * 128 + lane_base;
     auto pair_sync = [&](uint32_t phase) -> bool {
       __syncwarp();
       if (lane == 0) mbar_arrive(pairbar + quarter);
       return mbar_wait(pairbar + quarter, phase & 1, a.status, abort_flag);
     };
-    float m = -INFINITY;  // half-row max, log2 units (scaled)
-    float l = 0.f;        // sum of P (fp32): divides O and gives LSE
+    float m = -INFINITY;  // row max, log2 units (scaled), the same in both warps of the pair
+    float l = 0.f;        // this warp's sum of P (fp32) over its keys
     bool ok = true;
     for (int j = 0; j < n_sel; ++j) {
-      if (!(ok = warp_wait(sfull + (j & 1), (j >> 1) & 1, a.status, abort_flag))) break;
-      tc_fence_after();
-      const uint32_t tS = tmem + (j & 1) * 128 + lane_base + hf * 64;
-      const int J = sel[j];
-      const bool full = a.all_full || block_is_full(a.g, J);
-      uint32_t vm0 = ~0u, vm1 = ~0u;  // key rows of J inside the grid
-      if (!full) {
-        vm0 = block_rows_mask32(a.g, J, hf * 64);
-        vm1 = block_rows_mask32(a.g, J, hf * 64 + 32);
-      }
+      const bool okw = mbar_wait(sfull + j % kSBufs, (j / kSBufs) & 1, a.status, abort_flag);
+      const uint32_t tS = tmem + (j % kSBufs) * 128 + lane_base + hf * 64;
       uint32_t u0[32], u1[32];
-      float c0, c1;
-      tmem_ld32_max(tS, u0, c0);  // values and, from the same load, their maximum
-      tmem_ld32_max(tS + 32, u1, c1);
-      tmem_wait_ld();
+      uint32_t vm0 = ~0u, vm1 = ~0u;  // key rows of J inside the grid
       float mx = -INFINITY;
-      if (full) {
-        mx = fmaxf(c0, c1);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if ((vm0 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u0[e]));
-          if ((vm1 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u1[e]));
+      bool fullj = true;
+      if (okw) {
+        tc_fence_after();
+        const int J = sel[j];
+        fullj = a.all_full || block_is_full(a.g, J);
+        if (!fullj) {
+          vm0 = block_rows_mask32(a.g, J, hf * 64);
+          vm1 = block_rows_mask32(a.g, J, hf * 64 + 32);
         }
+        float c0, c1;
+        tmem_ld32_max(tS, u0, c0);  // values and, from the same load, their maximum
+        tmem_ld32_max(tS + 32, u1, c1);
+        tmem_wait_ld();
+        if (fullj) {
+          mx = fmaxf(c0, c1);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if ((vm0 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u0[e]));
+            if ((vm1 >> e) & 1u) mx = fmaxf(mx, __uint_as_float(u1[e]));
+          }
+        }
+        half_max[((j & 1) * 2 + hf) * 128 + r] = mx;
       }
-      const float m_new = fmaxf(m, mx * a.scale_log2);
+      if (!named_bar_and(2 + quarter, 64, okw)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, half_max[((j & 1) * 2 + (hf ^ 1)) * 128 + r]) * a.scale_log2;  // same in both warps
+      const float m_new = fmaxf(m, mx);
       if (j == 0) {
         m = m_new;
       } else {
-        const bool need = m_new > m + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          // O_hf holds sum_{<j} P V relative to m: wait for the last P V, then rescale it.
-          if (!(ok = warp_wait(odone, (j - 1) & 1, a.status, abort_flag))) break;
+        const bool need = m_new > m + rescale_threshold<kF16>();
+        if (__any_sync(0xffffffffu, need)) {  // both warps of the pair take this branch together
+          // O holds sum_{<j} P V relative to m: wait for P_{j-1} V_{j-1} (odone of block
+          // j - 1; S_j being done implies the products of block j - 3 and before are), then
+          // rescale this warp's half of O.
+          const int jp = j - 1;
+          if (!named_bar_and(2 + quarter, 64, mbar_wait(odone + (jp & 1), (jp >> 1) & 1, a.status, abort_flag))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const float alpha = need ? ex2(m - m_new) : 1.f;
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < D / 64; ++cc) {
             uint32_t u[32];
-            tmem_ld32(tOh + cc * 32, u);
+            const uint32_t tc = tO + hf * (D / 2) + cc * 32;
+            tmem_ld32(tc, u);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            tmem_st32(tOh + cc * 32, u);
+            tmem_st32(tc, u);
           }
           tmem_wait_st();
           l *= alpha;
           if (need) m = m_new;
         }
       }
-      // P in 16-bit pairs: each 32-column chunk of S holds the P of its 32 keys in its
-      // first 16 columns.  Full tiles skip the per-key mask.
-      if (full)
+      // P over S (fp16, or bf16 hi + lo).  Full tiles skip the per-key mask.
+      if (fullj)
         softmax_p<false, kF16>(u0, u1, vm0, vm1, m, a.scale_log2, tS, l);
       else
         softmax_p<true, kF16>(u0, u1, vm0, vm1, m, a.scale_log2, tS, l);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(pfull + (j & 1));
+      mbar_arrive(pfull + j % kSBufs);
     }
-    // Epilogue: merge the two half states, O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1)
-    // with a_h = 2^(m_h - max(m_0, m_1)) -> bf16 (and fp32) -> swizzled staging tiles
-    // (the Q tile, and the K ring for fp32) -> TMA stores.  `drain` completes once every
-    // MMA of the CTA has finished (the MMA warp commits it last).
+    // Epilogue: O / (l_0 + l_1) -> bf16 (and fp32) -> swizzled staging tiles (the Q tile,
+    // and the K ring for fp32) -> TMA stores.  `drain` completes once every MMA of the
+    // CTA has finished (the MMA warp commits it last).
     if (n_sel > 0) ok = mbar_wait(drain, 0, a.status, abort_flag) && ok;
     tc_fence_after();
-    half_st[(hf * 2 + 0) * 128 + r] = m;
-    half_st[(hf * 2 + 1) * 128 + r] = l;
+    half_l[hf * 128 + r] = l;
     ok = pair_sync(0) && ok;
-    const float mo = half_st[((hf ^ 1) * 2 + 0) * 128 + r];
-    const float lo = half_st[((hf ^ 1) * 2 + 1) * 128 + r];
-    const float M = fmaxf(m, mo);
-    const float as = M == -INFINITY ? 0.f : ex2(m - M);
-    const float ao = M == -INFINITY ? 0.f : ex2(mo - M);
-    const float L = as * l + ao * lo;
+    const float L = l + half_l[(hf ^ 1) * 128 + r];
     const float inv = (n_sel > 0 && L > 0.f) ? 1.f / L : 0.f;
-    const float w0c = (hf == 0 ? as : ao) * inv, w1c = (hf == 0 ? ao : as) * inv;  // weights of O_0, O_1
 #pragma unroll
     for (int cc = 0; cc < D / 64; ++cc) {
       const int col = hf * (D / 2) + cc * 32;  // first O column of this 32-column chunk
       float f[32];
       if (n_sel > 0) {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tmem + 256 + lane_base + col, u0);
-        tmem_ld32(tmem + 256 + D + lane_base + col, u1);
+        uint32_t u[32];
+        tmem_ld32(tO + col, u);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) f[e] = w0c * __uint_as_float(u0[e]) + w1c * __uint_as_float(u1[e]);
+        for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(u[e]) * inv;
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) f[e] = 0.f;
@@ -479,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = block_row_token(a.g, I, r);
     if (hf == 0 && n >= 0)
       a.LSE[((long long)a.b * a.Hh + h) * a.N + n] =
-          (n_sel > 0 && L > 0.f) ? (M + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+          (n_sel > 0 && L > 0.f) ? (m + __log2f(L)) * 0.69314718055994531f : -INFINITY;
     fence_async_smem();
     named_bar(1, 256);
     if (warp == 4 && lane == 0) {
@@ -507,8 +503,8 @@ template <int D, bool kF16, bool kO16, bool kO32>
 cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
                        int kb_end, const uint8_t* qb_active, void* O, float* LSE, float* O32, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const size_t smem = 1024 + C::SMEM_TILES + 8 * (1 + 2 * (C::KST + C::VST) + 10) + 4 * (3 + 16) + 4 * 512 +
-                      4 * kSeenWords + 4 * (size_t)p.k + 64;
+  const size_t smem = 1024 + C::SMEM_TILES + 8 * (2 * (C::KST + C::VST) + 2 * kSBufs + 8) + 4 * (3 + 16) +
+                      4 * 768 + 4 * kSeenWords + 4 * (size_t)p.k + 64;
   auto kern = fwd_tc_kernel<D, kF16, kO16, kO32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
