@@ -120,6 +120,9 @@ sda_status sda_workspace_size(const sda_problem* p, int op, size_t* bytes) {
   else if (op == SDA_OP_TRAIN) {
     if (q.dtype != SDA_BF16) return SDA_ERR_UNSUPPORTED;
     *bytes = train_ws_tc(q);
+  } else if (op == SDA_OP_PREDICTOR_GRAD) {
+    if (q.dtype != SDA_BF16) return SDA_ERR_UNSUPPORTED;
+    *bytes = distill_ws_tc(q);
   } else
     return SDA_ERR_INVALID_ARG;
   return SDA_OK;
@@ -143,6 +146,20 @@ sda_status sda_predict_blocks(const sda_problem* p, const void* Q, const void* K
   return from_cuda(predict_f32(q, static_cast<const float*>(Q), static_cast<const float*>(K),
                                static_cast<const float*>(Wq), static_cast<const float*>(Wk), block_idx, block_score,
                                ws, st));
+}
+
+sda_status sda_predictor_grad(const sda_problem* p, const void* Q, const void* K, const void* Wq, const void* Wk,
+                              float* dWq, float* dWk, double* loss, float* s_out, float* t_out, void* ws,
+                              size_t ws_bytes, void* stream) {
+  Prob q;
+  sda_status s = make_prob(p, &q);
+  if (s != SDA_OK) return s;
+  if (!Q || !K || !Wq || !Wk || !dWq || !dWk || !loss || !ws) return SDA_ERR_INVALID_ARG;
+  if ((s = check_supported(q)) != SDA_OK) return s;
+  if (q.dtype != SDA_BF16) return SDA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(Wq) || !aligned16(Wk) || !aligned16(ws)) return SDA_ERR_INVALID_ARG;
+  if (ws_bytes < distill_ws_tc(q)) return SDA_ERR_WORKSPACE;
+  return from_cuda(distill_tc(q, Q, K, Wq, Wk, dWq, dWk, loss, s_out, t_out, ws, static_cast<cudaStream_t>(stream)));
 }
 
 sda_status sda_attn_fwd(const sda_problem* p, const void* Q, const void* K, const void* V, const int32_t* block_idx,

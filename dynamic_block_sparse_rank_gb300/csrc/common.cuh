@@ -403,6 +403,14 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Byte offset of element (row, col) of a 128 x ncols 16-bit tile in the tensor
+// cores' unswizzled K-major operand layout: 8x8 core matrices (8 rows x 16
+// bytes, rows contiguous), K-adjacent core matrices 128 bytes apart (LBO),
+// 8-row groups ncols*16 bytes apart (SBO).
+__host__ __device__ __forceinline__ uint32_t coremat_offset(int row, int col, int ncols) {
+  return (uint32_t)((row >> 3) * (ncols >> 3) * 128 + (col >> 3) * 128 + (row & 7) * 16 + (col & 7) * 2);
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128B-swizzled
 // tile whose rows are 128 bytes (the TMA SWIZZLE_128B pattern).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) {

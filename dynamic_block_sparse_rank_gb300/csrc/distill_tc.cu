@@ -1,0 +1,564 @@
+// Training signal of the low-rank predictor: the gradient of a distillation loss
+// with respect to Wq and Wk.
+//
+// "DSV: Exploiting Dynamic Sparsity to Accelerate Large-Scale Video DiT Training",
+// section 4 ("two-stage training": in the first stage the predictor learns while
+// attention runs dense).  The page gives no loss.  Read: the low-rank block score
+// s(I, J) = max over i in I, j in J of q~_i . k~_j estimates the full-rank block-max
+// logit t(I, J) = max of q_i . k_j over the same pairs, and
+// L = 1/2 sum over (b, h, I, J) of (s - t)^2.  The max passes its gradient to its
+// maximising pair (i*, j*), the first in the tiles' (row, column) order on ties; the
+// bf16 rounding of q~ and k~ passes it unchanged; t, computed from the attention's own
+// Q and K, is a target.  With e = s - t:
+//   dL/dWq[h] = sum e Q_i*^T k~_j*,   dL/dWk[h] = sum e K_j*^T q~_i*.
+//
+// Steps (after the projections of the predictor, which fill the q~ / k~ tiles):
+//   tile_norm_kernel  the largest row norm of every q~ / k~ tile, which bounds the
+//                     fp32 rounding of any low-rank score of a tile pair;
+//   distill_kernel    per (2 query blocks, head): for every key block J and query
+//                     block q, S~ = q~_I k~_J^T (K = r) and S = Q_I K_J^T (K = d) on
+//                     the tensor cores into one of two TMEM buffer pairs; an epilogue
+//                     group of four warps takes t = max S and the first maximum of S~
+//                     exactly — the fp32 entries within the rounding bound of the fp32
+//                     maximum are re-scored in fp64 from the bf16 operands — then adds
+//                     e k~_j* to the query token's r-vector G_q[i*] and e q~_i* to the
+//                     key token's G_k[j*] (fp32 atomics) and e^2 / 2 to the loss;
+//   dw_kernel         dWq[h] = sum_n Q_n^T G_q[n] and dWk[h] = sum_n K_n^T G_k[n].
+#include "internal.h"
+
+namespace sda {
+
+namespace {
+
+constexpr int kDistQB = 2;                     // query blocks per CTA (one per epilogue group)
+constexpr int kDistThreads = 10 * 32;          // warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups
+constexpr double kUnit = 5.9604644775390625e-8;  // 2^-24, fp32's unit roundoff
+
+template <int R, int D>
+struct DistCfg {
+  static constexpr int TB = 128 * R * 2;   // q~ / k~ tile bytes (unswizzled operand layout)
+  static constexpr int TILE = 128 * D * 2;  // Q / K tile bytes (128B-swizzled, D / 64 chunks of 16 KB)
+  static constexpr int CH = D / 64;
+  static constexpr int JS = (R <= 32 || D == 64) ? 3 : 2;  // key-block ring stages
+  static constexpr int TILES_BYTES = kDistQB * (TILE + TB) + JS * (TILE + TB);
+};
+
+struct DistArgs {
+  Geom g;
+  int Hh, b;
+  long long N;
+  const uint8_t* qt;    // [B, Hh, nb] tiles of 128 x r bf16
+  const uint8_t* kt;
+  const float* qnorm;   // [B, Hh, nb]: largest row 2-norm of each q~ tile
+  const float* knorm;
+  float* Gq;            // [B, Hh, N, r]
+  float* Gk;
+  double* loss;
+  float* s_out;         // [B, Hh, nb, nb] or null
+  float* t_out;
+  unsigned* status;
+};
+
+__device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
+  uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > SDA_WAIT_LIMIT_NS) return false;
+  return true;
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t* tile, int row, int col, int ncols) {
+  const uint16_t v = *reinterpret_cast<const uint16_t*>(tile + coremat_offset(row, col, ncols));
+  return __uint_as_float((uint32_t)v << 16);
+}
+
+// One warp per tile: max over its 128 rows of the row's 2-norm (rows outside the grid
+// are zeros).
+template <int R>
+__global__ void tile_norm_kernel(const uint8_t* __restrict__ tiles, long long n_tiles, float* __restrict__ out) {
+  const long long t = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= n_tiles) return;  // whole warps
+  const uint8_t* tile = tiles + t * (128LL * R * 2);
+  float best = 0.f;
+  for (int row = lane; row < 128; row += 32) {
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < R; ++c) {
+      const float v = bf16_at(tile, row, c, R);
+      s = fmaf(v, v, s);
+    }
+    best = fmaxf(best, sqrtf(s));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if (lane == 0) out[t] = best;
+}
+
+// The lexicographic order of candidate maxima: larger exact score, then lower row, then
+// lower column.
+__device__ __forceinline__ bool better(double v, int i, int j, double bv, int bi, int bj) {
+  return v > bv || (v == bv && (i < bi || (i == bi && j < bj)));
+}
+
+template <int R, int D>
+__global__ void __launch_bounds__(kDistThreads, 1)
+    distill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, DistArgs a) {
+  using C = DistCfg<R, D>;
+  constexpr int JS = C::JS;
+  const int nb = a.g.nb;
+  const int h = blockIdx.y;
+  const int I0 = kDistQB * blockIdx.x;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                        // kDistQB x TILE
+  uint8_t* sK = sQ + kDistQB * C::TILE;      // JS x TILE
+  uint8_t* sqt = sK + JS * C::TILE;          // kDistQB x TB
+  uint8_t* skt = sqt + kDistQB * C::TB;      // JS x TB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILES_BYTES);
+  uint64_t* qfull = bars;
+  uint64_t* kfull = qfull + 1;        // JS
+  uint64_t* kempty = kfull + JS;      // JS: the MMAs and both epilogue groups are done with the stage
+  uint64_t* accf = kempty + JS;       // 2: a buffer pair holds a finished (S~, S)
+  uint64_t* accempty = accf + 2;      // 2: its four warps have read it out
+  uint64_t* drain = accempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  float* gmax = reinterpret_cast<float*>(abort_flag + 1);  // [2 groups][4 quarters] max of S~
+  float* gtmax = gmax + 8;                                 // [2][4] max of S
+  double* bestv = reinterpret_cast<double*>((reinterpret_cast<uintptr_t>(gtmax + 8) + 7) & ~uintptr_t(7));  // [2][4]
+  int* besti = reinterpret_cast<int*>(bestv + 8);          // [2][4]
+  int* bestj = besti + 8;                                  // [2][4]
+  uint8_t* fullb = reinterpret_cast<uint8_t*>(bestj + 8);  // nb: key block J lies inside the grid
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(qfull, 1);
+    for (int s = 0; s < JS; ++s) {
+      mbar_init(kfull + s, 1);
+      mbar_init(kempty + s, 1 + kDistQB);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf + b, 1);
+      mbar_init(accempty + b, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int J = tid; J < nb; J += kDistThreads) fullb[J] = block_is_full(a.g, J) ? 1 : 0;
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long long head_tiles = ((long long)a.b * a.Hh + h) * nb;
+  const int n_pairs = nb * kDistQB;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      mbar_expect_tx(qfull, kDistQB * (C::TILE + C::TB));
+      for (int q = 0; q < kDistQB; ++q) {
+        const int I = I0 + q < nb ? I0 + q : nb - 1;
+        int t0, h0, w0;
+        block_origin(a.g, I, t0, h0, w0);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_5d(sQ + q * C::TILE + c * 16384, &tmQ, qfull, c * 64, h, w0, h0, t0);
+        bulk_load(sqt + q * C::TB, a.qt + (head_tiles + I) * C::TB, C::TB, qfull);
+      }
+      int issued = 0;
+      for (int J = 0; J < nb; ++J) {
+        const int s = J % JS;
+        if (J >= JS && !mbar_wait(kempty + s, ((J / JS) - 1) & 1, a.status, abort_flag)) break;
+        int t0, h0, w0;
+        block_origin(a.g, J, t0, h0, w0);
+        mbar_expect_tx(kfull + s, C::TILE + C::TB);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_5d(sK + s * C::TILE + c * 16384, &tmK, kfull + s, c * 64, h, w0, h0, t0);
+        bulk_load(skt + s * C::TB, a.kt + (head_tiles + J) * C::TB, C::TB, kfull + s);
+        issued = J + 1;
+      }
+      if (*abort_flag) {  // let copies in flight land before the CTA exits
+        wait_plain(qfull, 0);
+        for (int J = issued - JS < 0 ? 0 : issued - JS; J < issued; ++J) wait_plain(kfull + J % JS, (J / JS) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // Whole warp, one elected lane issues.  Pair P = 2 J + q goes to buffer pair q:
+    // S~ into columns [256 q, 256 q + 128), S into the next 128.
+    const uint32_t leader = elect_leader();
+    constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
+    constexpr uint32_t SBO = (R / 8) * 128;
+    const uint64_t dA = smem_desc(smem_u32(sqt), 128, SBO, 0), dB = smem_desc(smem_u32(skt), 128, SBO, 0);
+    const uint64_t dQd = smem_desc(smem_u32(sQ), 16, 1024, 2), dKd = smem_desc(smem_u32(sK), 16, 1024, 2);
+    bool ok = warp_wait(qfull, 0, a.status, abort_flag);
+    for (int J = 0; ok && J < nb; ++J) {
+      const int s = J % JS;
+      if (!(ok = warp_wait(kfull + s, (J / JS) & 1, a.status, abort_flag))) break;
+      for (int q = 0; q < kDistQB; ++q) {
+        const int P = J * kDistQB + q, buf = P & 1;
+        if (P >= 2 && !(ok = warp_wait(accempty + buf, ((P >> 1) - 1) & 1, a.status, abort_flag))) break;
+        tc_fence_after();
+        const uint32_t tL = tmem + buf * 256, tF = tL + 128;
+#pragma unroll
+        for (int kk = 0; kk < R / 16; ++kk)
+          mma_ss_by(leader, tL, dA + (uint64_t)((q * C::TB + kk * 256) >> 4),
+                    dB + (uint64_t)((s * C::TB + kk * 256) >> 4), id, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;  // 64-column chunk, 16-column step
+          mma_ss_by(leader, tF, dQd + (uint64_t)((q * C::TILE) >> 4) + off,
+                    dKd + (uint64_t)((s * C::TILE) >> 4) + off, id, kk > 0);
+        }
+        mma_commit_by(leader, accf + buf);
+      }
+      mma_commit_by(leader, kempty + s);
+    }
+    mma_commit_by(leader, drain);
+    wait_plain(drain, 0);
+    __syncwarp();
+  } else {
+    // Epilogue group grp (warps 2 + 4 grp .. 5 + 4 grp, one per TMEM lane quarter) handles
+    // query block I0 + grp against every key block.  Thread = query row.
+    const int grp = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tL = tmem + grp * 256 + lane_base, tF = tL + 128;
+    const int I = I0 + grp;
+    const bool active = I < nb;
+    const bool row_ok = active && block_row_token(a.g, I, row) >= 0;
+    const double qn = active ? (double)a.qnorm[head_tiles + I] : 0.0;
+    const uint8_t* qtile = sqt + grp * C::TB;
+    double loss_acc = 0.0;
+    for (int P = grp; P < n_pairs; P += 2) {
+      const int J = P >> 1;
+      const int s = J % JS;
+      // a failed wait stops all four warps of the group at the same barrier below
+      const bool okw = warp_wait(accf + grp, (P >> 1) & 1, a.status, abort_flag);
+      const bool fj = fullb[J] != 0;
+      // this row's maximum of S~ and of S, over the key rows inside the grid
+      float mi = -INFINITY, ti = -INFINITY;
+      if (okw) tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 4 && okw; ++cc) {
+        uint32_t u[32];
+        tmem_ld32(tL + cc * 32, u);
+        tmem_wait_ld();
+        const uint32_t vm = fj ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float v = __uint_as_float(u[e]);
+          if ((vm >> e) & 1u) mi = fmaxf(mi, v);
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4 && okw; ++cc) {
+        uint32_t u[32];
+        float mx;
+        tmem_ld32_max(tF + cc * 32, u, mx);
+        tmem_wait_ld();
+        if (fj) {
+          ti = fmaxf(ti, mx);
+        } else {
+          const uint32_t vm = block_rows_mask32(a.g, J, cc * 32);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if ((vm >> e) & 1u) ti = fmaxf(ti, __uint_as_float(u[e]));
+        }
+      }
+      if (!row_ok) {
+        mi = -INFINITY;
+        ti = -INFINITY;
+      }
+      float wm = mi, wt = ti;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+        wt = fmaxf(wt, __shfl_xor_sync(0xffffffffu, wt, o));
+      }
+      if (lane == 0) {
+        gmax[grp * 4 + quarter] = wm;
+        gtmax[grp * 4 + quarter] = wt;
+      }
+      if (!named_bar_and(2 + grp, 128, okw)) break;
+      float M = gmax[grp * 4], T = gtmax[grp * 4];
+#pragma unroll
+      for (int qq = 1; qq < 4; ++qq) {
+        M = fmaxf(M, gmax[grp * 4 + qq]);
+        T = fmaxf(T, gtmax[grp * 4 + qq]);
+      }
+      // Every fp32 score within the rounding bound of the fp32 maximum is a candidate
+      // for the exact maximum: |fl(q~.k~) - q~.k~| <= r u ||q~|| ||k~|| / (1 - r u) for
+      // any order of the r fp32 additions, so an entry and the true maximum differ from
+      // their exact values by at most half the bound below each.
+      const double delta = (2.0 * R + 2.0) * kUnit * qn * (double)a.knorm[head_tiles + J];
+      const double floor_v = (double)M - delta;
+      const bool cand = row_ok && (double)mi >= floor_v;
+      double bv = -INFINITY;
+      int bi = 0x7fffffff, bj = 0x7fffffff;
+      if (__any_sync(0xffffffffu, cand)) {
+        const uint8_t* ktile = skt + s * C::TB;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t u[32];
+          tmem_ld32(tL + cc * 32, u);
+          tmem_wait_ld();
+          uint32_t cm = 0;
+          const uint32_t vm = fj ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) cm |= (((vm >> e) & 1u) && (double)__uint_as_float(u[e]) >= floor_v ? 1u : 0u) << e;
+          if (!cand) cm = 0;
+          while (cm) {  // ascending columns: the first of equal exact scores is kept
+            const int e = __ffs(cm) - 1;
+            cm &= cm - 1;
+            const int j = cc * 32 + e;
+            double v = 0.0;
+            for (int c = 0; c < R; ++c) v += (double)bf16_at(qtile, row, c, R) * (double)bf16_at(ktile, j, c, R);
+            if (better(v, row, j, bv, bi, bj)) {
+              bv = v;
+              bi = row;
+              bj = j;
+            }
+          }
+        }
+      }
+      // the TMEM pair is read out: the MMA warp may refill it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty + grp);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o), oj = __shfl_xor_sync(0xffffffffu, bj, o);
+        if (better(ov, oi, oj, bv, bi, bj)) {
+          bv = ov;
+          bi = oi;
+          bj = oj;
+        }
+      }
+      if (lane == 0) {
+        bestv[grp * 4 + quarter] = bv;
+        besti[grp * 4 + quarter] = bi;
+        bestj[grp * 4 + quarter] = bj;
+      }
+      named_bar(2 + grp, 128);
+      if (quarter == 0) {  // one warp of the group adds the gradient terms
+        double v = bestv[grp * 4];
+        int i = besti[grp * 4], j = bestj[grp * 4];
+#pragma unroll
+        for (int qq = 1; qq < 4; ++qq)
+          if (better(bestv[grp * 4 + qq], besti[grp * 4 + qq], bestj[grp * 4 + qq], v, i, j)) {
+            v = bestv[grp * 4 + qq];
+            i = besti[grp * 4 + qq];
+            j = bestj[grp * 4 + qq];
+          }
+        if (active && i < 128 && j < 128) {
+          const double e = v - (double)T;
+          const long long pair = (head_tiles + I) * nb + J;
+          if (lane == 0) {
+            loss_acc += 0.5 * e * e;
+            if (a.s_out) a.s_out[pair] = (float)v;
+            if (a.t_out) a.t_out[pair] = T;
+          }
+          const long long hrow = ((long long)a.b * a.Hh + h) * a.N;
+          float* gq = a.Gq + (hrow + block_row_token(a.g, I, i)) * R;
+          float* gk = a.Gk + (hrow + block_row_token(a.g, J, j)) * R;
+          const uint8_t* ktile = skt + s * C::TB;
+          for (int c = lane; c < R; c += 32) {
+            atomicAdd(gq + c, (float)(e * (double)bf16_at(ktile, j, c, R)));
+            atomicAdd(gk + c, (float)(e * (double)bf16_at(qtile, i, c, R)));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kempty + s);  // this group no longer reads stage s
+      }
+    }
+    if (quarter == 0 && lane == 0 && loss_acc != 0.0) atomicAdd(a.loss, loss_acc);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dW_z[h] = sum over tokens of X_z[token, h, :]^T G_z[h, token, :] with X_0 = Q, G_0 = G_q
+// (dWq) and X_1 = K, G_1 = G_k (dWk), over every batch entry.  A CTA sums a run of
+// tokens for one (head, z) in registers (each thread owns D R / 256 of the d x r
+// outputs) and adds its partial with fp32 atomics.
+template <int D, int R>
+__global__ void __launch_bounds__(256) dw_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K,
+                                                 const float* __restrict__ Gq, const float* __restrict__ Gk, int Hh,
+                                                 long long N, long long total, int per_cta, float* __restrict__ dWq,
+                                                 float* __restrict__ dWk) {
+  constexpr int OUT = D * R / 256;
+  constexpr int TT = 16;  // tokens staged per step
+  __shared__ float xs[TT][D];
+  __shared__ float gs[TT][R];
+  const int h = blockIdx.y, z = blockIdx.z;
+  const __nv_bfloat16* X = z == 0 ? Q : K;
+  const float* G = z == 0 ? Gq : Gk;
+  float* out = z == 0 ? dWq : dWk;
+  float acc[OUT];
+#pragma unroll
+  for (int u = 0; u < OUT; ++u) acc[u] = 0.f;
+  const long long n0 = blockIdx.x * (long long)per_cta;
+  const long long n1 = n0 + per_cta < total ? n0 + per_cta : total;
+  for (long long base = n0; base < n1; base += TT) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < TT * D; e += 256) {
+      const int t = e / D, c = e % D;
+      const long long bn = base + t;  // b * N + n
+      xs[t][c] = bn < n1 ? __bfloat162float(X[(bn * Hh + h) * D + c]) : 0.f;
+    }
+    for (int e = threadIdx.x; e < TT * R; e += 256) {
+      const int t = e / R, c = e % R;
+      const long long bn = base + t;
+      const long long b = bn / N, n = bn % N;
+      gs[t][c] = bn < n1 ? G[((b * Hh + h) * N + n) * R + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int t = 0; t < TT; ++t) {
+#pragma unroll
+      for (int u = 0; u < OUT; ++u) {
+        const int o = threadIdx.x + 256 * u;
+        acc[u] = fmaf(xs[t][o / R], gs[t][o % R], acc[u]);
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < OUT; ++u) {
+    const int o = threadIdx.x + 256 * u;
+    atomicAdd(out + (long long)h * D * R + o, acc[u]);
+  }
+}
+
+struct DistWs {
+  uint8_t* qt;
+  uint8_t* kt;
+  float* qnorm;
+  float* knorm;
+  float* Gq;
+  float* Gk;
+  size_t bytes;
+};
+
+DistWs dist_layout(const Prob& p, void* base) {
+  DistWs w;
+  const size_t tiles = (size_t)p.B * p.Hh * p.g.nb;
+  const size_t tile_bytes = align_up(tiles * 128 * p.r * 2, 256);
+  const size_t g_bytes = align_up((size_t)p.B * p.Hh * p.N * p.r * 4, 256);
+  char* c = static_cast<char*>(base);
+  w.qt = reinterpret_cast<uint8_t*>(c);
+  w.kt = reinterpret_cast<uint8_t*>(c + tile_bytes);
+  size_t off = 2 * tile_bytes;
+  w.qnorm = reinterpret_cast<float*>(c + off);
+  off += align_up(tiles * 4, 256);
+  w.knorm = reinterpret_cast<float*>(c + off);
+  off += align_up(tiles * 4, 256);
+  w.Gq = reinterpret_cast<float*>(c + off);
+  off += g_bytes;
+  w.Gk = reinterpret_cast<float*>(c + off);
+  off += g_bytes;
+  w.bytes = off;
+  return w;
+}
+
+template <int R, int D>
+cudaError_t launch_distill(const Prob& p, const void* Q, const void* K, float* dWq, float* dWk, double* loss,
+                           float* s_out, float* t_out, const DistWs& w, unsigned* status, cudaStream_t st) {
+  using C = DistCfg<R, D>;
+  const size_t tiles = (size_t)p.B * p.Hh * p.g.nb;
+  const int nt_blocks = (int)((tiles * 32 + 255) / 256);
+  tile_norm_kernel<R><<<nt_blocks, 256, 0, st>>>(w.qt, (long long)tiles, w.qnorm);
+  tile_norm_kernel<R><<<nt_blocks, 256, 0, st>>>(w.kt, (long long)tiles, w.knorm);
+  note_launches(2);
+  const size_t smem = 1024 + C::TILES_BYTES + 8 * (1 + 2 * C::JS + 5) + 8 + 16 * 4 + 8 + 8 * 8 + 16 * 4 +
+                      (size_t)p.g.nb + 64;
+  cudaError_t e = cudaFuncSetAttribute(distill_kernel<R, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const size_t per_batch = (size_t)p.N * p.Hh * p.d * 2;
+  const Geom& g = p.g;
+  for (int b = 0; b < p.B; ++b) {
+    CUtensorMap mQ, mK;
+    if (!make_token_map(&mQ, static_cast<const char*>(Q) + b * per_batch, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt,
+                        g.bh, g.bw) ||
+        !make_token_map(&mK, static_cast<const char*>(K) + b * per_batch, kTokBF16, g.T, g.H, g.W, p.Hh, p.d, g.bt,
+                        g.bh, g.bw))
+      return cudaErrorInvalidValue;
+    DistArgs a;
+    a.g = g;
+    a.Hh = p.Hh;
+    a.b = b;
+    a.N = p.N;
+    a.qt = w.qt;
+    a.kt = w.kt;
+    a.qnorm = w.qnorm;
+    a.knorm = w.knorm;
+    a.Gq = w.Gq;
+    a.Gk = w.Gk;
+    a.loss = loss;
+    a.s_out = s_out;
+    a.t_out = t_out;
+    a.status = status;
+    distill_kernel<R, D><<<dim3((g.nb + kDistQB - 1) / kDistQB, p.Hh), kDistThreads, smem, st>>>(mQ, mK, a);
+    note_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const long long total = (long long)p.B * p.N;
+  const int per_cta = 2048;
+  dw_kernel<D, R><<<dim3((unsigned)((total + per_cta - 1) / per_cta), p.Hh, 2), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K), w.Gq, w.Gk, p.Hh, p.N, total, per_cta,
+      dWq, dWk);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+template <int R>
+cudaError_t dispatch_d(const Prob& p, const void* Q, const void* K, float* dWq, float* dWk, double* loss,
+                       float* s_out, float* t_out, const DistWs& w, unsigned* status, cudaStream_t st) {
+  return p.d == 64 ? launch_distill<R, 64>(p, Q, K, dWq, dWk, loss, s_out, t_out, w, status, st)
+                   : launch_distill<R, 128>(p, Q, K, dWq, dWk, loss, s_out, t_out, w, status, st);
+}
+
+}  // namespace
+
+size_t distill_ws_tc(const Prob& p) { return dist_layout(p, nullptr).bytes; }
+
+cudaError_t distill_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, float* dWq,
+                       float* dWk, double* loss, float* s_out, float* t_out, void* ws, cudaStream_t st) {
+  const DistWs w = dist_layout(p, ws);
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  cudaError_t e = project_tc(p, Q, K, Wq, Wk, ws, st);  // q~, k~ tiles at the start of ws
+  if (e != cudaSuccess) return e;
+  const size_t g_bytes = (size_t)p.B * p.Hh * p.N * p.r * 4;
+  const size_t w_bytes = (size_t)p.Hh * p.d * p.r * 4;
+  if ((e = cudaMemsetAsync(w.Gq, 0, g_bytes, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(w.Gk, 0, g_bytes, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dWq, 0, w_bytes, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dWk, 0, w_bytes, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(loss, 0, sizeof(double), st)) != cudaSuccess) return e;
+  switch (p.r) {
+    case 16:
+      return dispatch_d<16>(p, Q, K, dWq, dWk, loss, s_out, t_out, w, status, st);
+    case 32:
+      return dispatch_d<32>(p, Q, K, dWq, dWk, loss, s_out, t_out, w, status, st);
+    case 48:
+      return dispatch_d<48>(p, Q, K, dWq, dWk, loss, s_out, t_out, w, status, st);
+    case 64:
+      return dispatch_d<64>(p, Q, K, dWq, dWk, loss, s_out, t_out, w, status, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sda

@@ -89,6 +89,15 @@ size_t predict_ws_tc(const Prob& p);
 cudaError_t predict_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, int32_t* idx,
                        float* score, void* ws, cudaStream_t st);
 
+// The projections alone (q~, k~ tiles into the predictor workspace, as predict_tc lays them out).
+cudaError_t project_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, void* ws,
+                       cudaStream_t st);
+
+// ---- distill_tc.cu (the predictor's training signal)
+size_t distill_ws_tc(const Prob& p);
+cudaError_t distill_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, float* dWq,
+                       float* dWk, double* loss, float* s_out, float* t_out, void* ws, cudaStream_t st);
+
 // ---- attn_fwd_tc.cu
 // O in bf16, or (out_f32) in fp32.
 cudaError_t fwd_tc(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,

@@ -34,12 +34,7 @@ namespace sda {
 namespace {
 
 // ------------------------------------------------------------------ projection
-// Byte offset of element (row, col) of a 128 x r bf16 tile in the operand layout:
-// 8x8 core matrices (8 rows x 16 bytes, rows contiguous), K-adjacent core
-// matrices 128 bytes apart (LBO), 8-row groups r*16 bytes apart (SBO).
-__device__ __forceinline__ uint32_t op_offset(int row, int col, int r) {
-  return (uint32_t)((row >> 3) * (r >> 3) * 128 + (col >> 3) * 128 + (row & 7) * 16 + (col & 7) * 2);
-}
+__device__ __forceinline__ uint32_t op_offset(int row, int col, int r) { return coremat_offset(row, col, r); }
 
 // One CTA per (128-token tile, head): the tile arrives by TMA (the 5-D box of one
 // space-time tile, 128-byte swizzled, zero outside the grid), W^T is written to shared
@@ -444,6 +439,25 @@ cudaError_t launch_predict(const Prob& p, const void* Q, const void* K, const vo
 }
 
 }  // namespace
+
+cudaError_t project_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, void* ws,
+                       cudaStream_t st) {
+  const size_t tiles = (size_t)p.B * p.Hh * p.g.nb;
+  uint8_t* qt = static_cast<uint8_t*>(ws);
+  uint8_t* kt = qt + align_up(tiles * 128 * p.r * 2, 256);
+  unsigned* status = status_ptr();
+  if (!status) return cudaErrorUnknown;
+  cudaError_t e = cudaErrorInvalidValue;
+#define SDA_PROJ(R)                                                                     \
+  case R:                                                                               \
+    e = p.d == 64 ? launch_proj<R, 64>(p, Q, K, Wq, Wk, qt, kt, status, st)            \
+                  : launch_proj<R, 128>(p, Q, K, Wq, Wk, qt, kt, status, st);          \
+    break;
+  switch (p.r) { SDA_PROJ(16) SDA_PROJ(32) SDA_PROJ(48) SDA_PROJ(64) }
+#undef SDA_PROJ
+  note_launches(2 * p.B);
+  return e;
+}
 
 size_t predict_ws_tc(const Prob& p) {
   return 2 * align_up((size_t)p.B * p.Hh * p.g.nb * 128 * p.r * 2, 256);

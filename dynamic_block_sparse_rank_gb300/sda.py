@@ -16,10 +16,10 @@ LIB_PATH = os.path.join(_HERE, "libsda.so")
 (SDA_OK, SDA_ERR_INVALID_ARG, SDA_ERR_UNSUPPORTED, SDA_ERR_WORKSPACE, SDA_ERR_CUDA, SDA_ERR_DEVICE_TIMEOUT,
  SDA_ERR_DEVICE_BAD_INDEX, SDA_ERR_DEVICE_RANGE) = range(8)
 SDA_F32, SDA_BF16 = 0, 1
-SDA_OP_PREDICT, SDA_OP_BWD, SDA_OP_TRAIN = 0, 1, 2
+SDA_OP_PREDICT, SDA_OP_BWD, SDA_OP_TRAIN, SDA_OP_PREDICTOR_GRAD = 0, 1, 2, 3
 
 EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_attn_fwd", "sda_attn_bwd",
-           "sda_attn_fwd_train", "sda_attn_bwd_train",
+           "sda_attn_fwd_train", "sda_attn_bwd_train", "sda_predictor_grad",
            "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_attn_bwd_partition", "sda_merge_states", "sda_merge_states_bwd",
            "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_selftest_wait_timeout", "sda_status_string")
 
@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
         L.sda_attn_bwd.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]
         L.sda_attn_bwd_prepare.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.sda_attn_fwd_train.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sda_predictor_grad.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.sda_attn_bwd_train.argtypes = [pr, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, vp]
         L.sda_attn_bwd_partition.argtypes = [pr, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, i32, vp, sz,
                                              vp]
@@ -161,6 +162,12 @@ def sda_attn_bwd(p, Q, K, V, O, LSE, dO, block_idx, dQ, dK, dV, grad_dtype, ws, 
     _check(lib().sda_attn_bwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(dO),
                               _ptr(block_idx), _ptr(dQ), _ptr(dK), _ptr(dV), int(gd), _wsptr(ws), _nbytes(ws),
                               _stream(stream)), "sda_attn_bwd")
+
+
+def sda_predictor_grad(p, Q, K, Wq, Wk, dWq, dWk, loss, ws, s_out=None, t_out=None, stream=None):
+    _check(lib().sda_predictor_grad(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(Wq), _ptr(Wk), _ptr(dWq), _ptr(dWk),
+                                    _ptr(loss), _ptr(s_out), _ptr(t_out), _wsptr(ws), _nbytes(ws), _stream(stream)),
+           "sda_predictor_grad")
 
 
 def sda_attn_fwd_train(p, Q, K, V, block_idx, O, LSE, ws, stream=None):

@@ -86,7 +86,7 @@ typedef struct {
 } sda_problem;
 
 /* Workspace queries (op argument of sda_workspace_size). */
-enum { SDA_OP_PREDICT = 0, SDA_OP_BWD = 1, SDA_OP_TRAIN = 2 };
+enum { SDA_OP_PREDICT = 0, SDA_OP_BWD = 1, SDA_OP_TRAIN = 2, SDA_OP_PREDICTOR_GRAD = 3 };
 
 /* Host only.  n_blocks = nT*nH*nW and k = kept key blocks per query block. */
 sda_status sda_num_blocks(const sda_problem* p, int* n_blocks, int* k);
@@ -106,6 +106,27 @@ sda_status sda_workspace_size(const sda_problem* p, int op, size_t* bytes);
 sda_status sda_predict_blocks(const sda_problem* p, const void* Q, const void* K, const void* Wq,
                               const void* Wk, int32_t* block_idx, float* block_score, void* ws,
                               size_t ws_bytes, void* stream);
+
+/* The predictor's training signal (DSV section 4, "two-stage training": the
+ * predictor learns in a stage of its own; the page gives no loss).  For every
+ * (b, head, query block I, key block J): the low-rank block score
+ * s = max over i in I, j in J of q~_i . k~_j (as sda_predict_blocks computes it)
+ * at its maximising pair (i*, j*) — the first in (row, column) order of the two
+ * tiles on ties, found exactly — and the full-rank target t = max of q_i . k_j
+ * over the same pairs.  With e = s - t and L = 1/2 sum e^2:
+ *   dWq[h] = dL/dWq[h] = sum e Q_i*^T k~_j*,   dWk[h] = sum e K_j*^T q~_i*
+ * (the bf16 rounding of q~, k~ passes the gradient unchanged; t is a target).
+ *   Q, K, Wq, Wk  as sda_predict_blocks (tensor-core path only: SDA_BF16)
+ *   dWq, dWk      out [heads, d, r] fp32, summed over the batch
+ *   loss          out, one fp64 value: L over the whole batch
+ *   s_out, t_out  optional out [B, heads, n_b, n_b] fp32 (NULL to skip)
+ *   ws            at least sda_workspace_size(SDA_OP_PREDICTOR_GRAD) bytes.
+ * Its cost is one low-rank and one full-rank (K = d) product per block pair, 1 + d/r
+ * times the predictor's.  The gradient sums use fp32 atomics: results agree
+ * from run to run to fp32 rounding, not bit for bit. */
+sda_status sda_predictor_grad(const sda_problem* p, const void* Q, const void* K, const void* Wq,
+                              const void* Wk, float* dWq, float* dWk, double* loss, float* s_out,
+                              float* t_out, void* ws, size_t ws_bytes, void* stream);
 
 /* Step 2a: block-sparse attention forward over the kept blocks J of each query
  * block I that satisfy kb_begin <= J < kb_end (0, n_b = all keys).

@@ -177,6 +177,19 @@ def test_training_pair_validates_on_the_host(L):
     assert e.value.status == sda.SDA_ERR_UNSUPPORTED
 
 
+def test_predictor_training_signal_validates_on_the_host(L):
+    p = _bad({})
+    need = sda.sda_workspace_size(p, sda.SDA_OP_PREDICTOR_GRAD)
+    assert need > sda.sda_workspace_size(p, sda.SDA_OP_PREDICT)  # q~, k~ tiles + norms + per-token sums
+    g = L.sda_predictor_grad
+    assert g(ctypes.byref(p), None, 16, 16, 16, 16, 16, 16, None, None, 16, need, None) == sda.SDA_ERR_INVALID_ARG
+    assert g(ctypes.byref(p), 16, 16, 16, 16, 16, 16, None, None, None, 16, need, None) == sda.SDA_ERR_INVALID_ARG
+    assert g(ctypes.byref(p), 18, 16, 16, 16, 16, 16, 16, None, None, 16, need, None) == sda.SDA_ERR_INVALID_ARG
+    assert g(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, None, None, 16, need - 1, None) == sda.SDA_ERR_WORKSPACE
+    f32 = _bad({"dtype": "f32"})
+    assert g(ctypes.byref(f32), 16, 16, 16, 16, 16, 16, 16, None, None, 16, 1 << 40, None) == sda.SDA_ERR_UNSUPPORTED
+
+
 def test_status_strings(L):
     for s in range(8):
         assert sda.status_string(s) and "unknown" not in sda.status_string(s)

@@ -348,3 +348,28 @@ def test_merge_131k_partition_states_and_reuse_every_head(sda, parity_report):
         deviation.append(errors(Ro, Eo))
     # the reuse approximation's deviation from the exact merge is reported, not graded
     rec.e["reuse_vs_exact_merge_max_abs_rel_frob"] = [max(d[0] for d in deviation), max(d[1] for d in deviation)]
+
+
+def test_fwd_8k_predictor_training_signal_full_oracle(sda, parity_report):
+    """The predictor's training signal on the 8,192-token workload in full (all 12 heads, all 4,096 block pairs
+    each): per-pair s and t, the loss and dWq, dWk against the oracle's distillation gradient."""
+    from tests.test_gpu_parity import _gpu_predictor_grad, check_predictor_grad
+
+    wl = inputs.WORKLOADS["fwd_8k"]
+    rec = _Record(parity_report, wl.name + " predictor training signal", "all 12 heads x all 4,096 block pairs")
+    x = _inputs(wl, ("Q", "K", "Wq", "Wk"))
+    geom = _geom(wl)
+    dWq, dWk, L, s, t = _gpu_predictor_grad(sda, wl, x)
+    L_ref, dWq_ref, dWk_ref, s_ref, t_ref = rec.oracle(orc.predictor_distill_grad, x["Q"], x["K"], x["Wq"], x["Wk"],
+                                                       geom, wl.dtype)
+    check_scores(s, s_ref)
+    terr = float(np.abs(t - t_ref).max() / np.abs(t_ref).max())
+    assert terr < 1e-5, terr
+    assert abs(L - L_ref) <= 1e-4 * abs(L_ref), (L, L_ref)
+    rq = check_predictor_grad(dWq, dWq_ref, "dWq")
+    rk = check_predictor_grad(dWk, dWk_ref, "dWk")
+    rec.e["outputs"]["dWq (max-abs / scale, rel-frob)"] = list(rq)
+    rec.e["outputs"]["dWk (max-abs / scale, rel-frob)"] = list(rk)
+    rec.e["outputs"]["loss (relative error)"] = abs(L - L_ref) / abs(L_ref)
+    rec.e["outputs"]["t (max error / max |t|)"] = terr
+    assert sda.sda_get_device_status() == sda.SDA_OK

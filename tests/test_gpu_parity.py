@@ -542,3 +542,48 @@ def test_forward_fp32_output_matches_oracle(sda, wl):
     assert mx < 1e-3, mx
     assert_close(host(LSE), L_ref, wl.dtype, "LSE (key range)")
     assert sda.sda_get_device_status() == sda.SDA_OK
+
+
+def _gpu_predictor_grad(sda, wl, x):
+    p = sda.problem_from_workload(wl)
+    nb, _ = sda.sda_num_blocks(p)
+    dWq = torch.full((wl.heads, wl.d, wl.rank), float("nan"), dtype=torch.float32, device="cuda")
+    dWk = torch.full_like(dWq, float("nan"))
+    loss = torch.full((1,), float("nan"), dtype=torch.float64, device="cuda")
+    s = torch.full((wl.B, wl.heads, nb, nb), float("nan"), dtype=torch.float32, device="cuda")
+    t = torch.full_like(s, float("nan"))
+    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICTOR_GRAD), dtype=torch.uint8, device="cuda")
+    sda.sda_predictor_grad(p, dev(x["Q"], wl.dtype), dev(x["K"], wl.dtype), dev(x["Wq"], wl.dtype),
+                           dev(x["Wk"], wl.dtype), dWq, dWk, loss, ws, s_out=s, t_out=t)
+    torch.cuda.synchronize()
+    return host(dWq), host(dWk), float(loss.item()), host(s), host(t)
+
+
+def check_predictor_grad(got, ref, what):
+    """Reading 16: the predictor's weight gradient sums e Q (x) k~ over every block pair, entries of order
+    1e3-1e5 at these inputs, so it is held to rel-Frobenius <= 1e-2 and max-abs <= 2e-2 of its own largest
+    entry (an absolute 2e-2 would ask 1e-7 relative, below fp32's rounding of the sum)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    mx, rel = errors(got, ref)
+    scale = np.abs(ref).max()
+    assert rel <= 1e-2 and mx <= 2e-2 * scale, f"{what}: max-abs {mx:.3e} (scale {scale:.3e}), rel-frob {rel:.3e}"
+    return mx / scale, rel
+
+
+@pytest.mark.parametrize("wl", [RAGGED_D64, RAGGED_D128, TILE_4X4X8, TWO_BATCH, TILE_1X1X128], ids=lambda w: w.name)
+def test_predictor_training_signal_matches_oracle(sda, wl):
+    """sda_predictor_grad against the oracle's distillation gradient: per (I, J) the low-rank block score s at
+    its exact first maximum and the full-rank block max t, the loss, and dWq, dWk."""
+    x = inputs.generate(wl, names=("Q", "K", "Wq", "Wk"))
+    geom = _geom(wl)
+    dWq, dWk, L, s, t = _gpu_predictor_grad(sda, wl, x)
+    L_ref, dWq_ref, dWk_ref, s_ref, t_ref = orc.predictor_distill_grad(x["Q"], x["K"], x["Wq"], x["Wk"], geom,
+                                                                        wl.dtype)
+    check_scores(s, s_ref)  # the low-rank scores, as the predictor's
+    terr = np.abs(t - t_ref).max() / np.abs(t_ref).max()
+    assert terr < 1e-5, terr  # fp32 accumulation of exact bf16 products
+    assert abs(L - L_ref) <= 1e-4 * abs(L_ref), (L, L_ref)
+    check_predictor_grad(dWq, dWq_ref, "dWq")
+    check_predictor_grad(dWk, dWk_ref, "dWk")
+    assert sda.sda_get_device_status() == sda.SDA_OK
