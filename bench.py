@@ -478,6 +478,32 @@ def main():
         merge["bwd"] = {"ms": bms, "bytes": bbytes, "gbs": bbytes / (bms / 1e3) / 1e9}
         del Os, Ls, dO, dL, gO, gL
 
+    # ---- the predictor's training signal on the 61K-token shapes (distillation gradient of Wq, Wk)
+    pgrad = None
+    if rank == 0:
+        pw = inputs.WORKLOADS["fwd_61k"]
+        xp = inputs.generate(pw, names=("Q", "K", "Wq", "Wk"))
+        tp = {n: torch.from_numpy(xp[n]).to(torch.bfloat16).to(dev) for n in ("Q", "K", "Wq", "Wk")}
+        del xp
+        pp = sda.problem_from_workload(pw)
+        gq = torch.empty((pw.heads, pw.d, pw.rank), dtype=torch.float32, device=dev)
+        gk = torch.empty_like(gq)
+        gl = torch.empty((1,), dtype=torch.float64, device=dev)
+        gws = torch.empty(sda.sda_workspace_size(pp, sda.SDA_OP_PREDICTOR_GRAD), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            sda.sda_predictor_grad(pp, tp["Q"], tp["K"], tp["Wq"], tp["Wk"], gq, gk, gl, gws, stream=stream)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        g0.record(stream)
+        for _ in range(reps):
+            sda.sda_predictor_grad(pp, tp["Q"], tp["K"], tp["Wq"], tp["Wk"], gq, gk, gl, gws, stream=stream)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        gms = g0.elapsed_time(g1) / reps
+        gflops = 2.0 * (pw.rank + pw.d) * pw.B * pw.heads * float(pw.N) ** 2  # both products, every token pair
+        pgrad = {"workload": pw.name, "ms": gms, "flops": gflops, "tflops": gflops / (gms / 1e3) / 1e12}
+        del tp, gws
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -551,6 +577,7 @@ def main():
         "kernels": {n: {"ms": t, "tflops": f / (t / 1e3) / 1e12, "frac": f / (t / 1e3) / 1e12 / tc_peak}
                     for n, (t, f) in kern.items()},
         "merge": merge,
+        "predictor_grad": dict(pgrad, frac_of_peak=pgrad["tflops"] / tc_peak) if pgrad else None,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,

@@ -2,8 +2,9 @@
 
 A 2-head bf16 problem on a ragged 3 x 10 x 12 grid (2x8x8 tiles, 8 blocks,
 d = 64, r = 16, 4 of 8 key blocks kept): predictor + top-k, forward, backward,
-two key-partition states and their merge, and the gradient through that merge
-(merge backward, then each partition state's backward, summed).
+two key-partition states and their merge, the gradient through that merge
+(merge backward, then each partition state's backward, summed), and the
+predictor's training signal (distillation gradient of Wq, Wk).
 """
 from __future__ import annotations
 
@@ -82,6 +83,17 @@ def run(device: int = 0) -> dict:
     mref = orc.reuse_bwd(x["Q"], x["K"], x["V"], x["dO"], ref_idx, geom, 2, 0, None, state_dtype="bf16")
     for name, got, ref in zip(("dQ", "dK", "dV"), total, mref):
         assert_close(host(got), ref, "bf16", "smoke merged-partition " + name)
+    # 6. the predictor's training signal (distillation gradient of Wq, Wk)
+    dWq = torch.empty((wl.heads, wl.d, wl.rank), dtype=torch.float32, device="cuda")
+    dWk = torch.empty_like(dWq)
+    loss = torch.empty((1,), dtype=torch.float64, device="cuda")
+    wsg = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICTOR_GRAD), dtype=torch.uint8, device="cuda")
+    sda.sda_predictor_grad(p, Q, K, Wq, Wk, dWq, dWk, loss, wsg)
+    loss_ref, dWq_ref, dWk_ref, _, _ = orc.predictor_distill_grad(x["Q"], x["K"], x["Wq"], x["Wk"], geom, "bf16")
+    for name, got, ref in (("dWq", dWq, dWq_ref), ("dWk", dWk, dWk_ref)):
+        err = np.linalg.norm(host(got) - ref) / np.linalg.norm(ref)
+        assert err < 1e-2, (name, err)
+    assert abs(float(loss.item()) - loss_ref) <= 1e-4 * abs(loss_ref)
     st = sda.sda_get_device_status()
     assert st == sda.SDA_OK, sda.status_string(st)
     return {"selection": sel, "score_rel_err": float(s_err)}
