@@ -19,10 +19,13 @@
 //                     block q, S~ = q~_I k~_J^T (K = r) and S = Q_I K_J^T (K = d) on
 //                     the tensor cores into one of two TMEM buffer pairs; an epilogue
 //                     group of four warps takes t = max S and the first maximum of S~
-//                     exactly — the fp32 entries within the rounding bound of the fp32
-//                     maximum are re-scored in fp64 from the bf16 operands — then adds
-//                     e k~_j* to the query token's r-vector G_q[i*] and e q~_i* to the
-//                     key token's G_k[j*] (fp32 atomics) and e^2 / 2 to the loss;
+//                     (the fp32 entries within twice the rounding bound of the fp32
+//                     maximum re-scored from the bf16 operands, a compensated fp32 sum
+//                     of exact products good to about 2^-44; equal operands tie
+//                     exactly and go to the first row, then column), then adds
+//                     e k~_j* to the query token's r-vector G_q[i*] and
+//                     e q~_i* to the key token's G_k[j*] (fp32 atomics) and e^2 / 2
+//                     to the loss;
 //   dw_kernel         dWq[h] = sum_n Q_n^T G_q[n] and dWk[h] = sum_n K_n^T G_k[n].
 #include "internal.h"
 
@@ -32,7 +35,7 @@ namespace {
 
 constexpr int kDistQB = 2;                     // query blocks per CTA (one per epilogue group)
 constexpr int kDistThreads = 10 * 32;          // warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups
-constexpr double kUnit = 5.9604644775390625e-8;  // 2^-24, fp32's unit roundoff
+constexpr float kUnitF = 5.9604644775390625e-8f;  // 2^-24, fp32's unit roundoff
 
 template <int R, int D>
 struct DistCfg {
@@ -94,10 +97,48 @@ __global__ void tile_norm_kernel(const uint8_t* __restrict__ tiles, long long n_
   if (lane == 0) out[t] = best;
 }
 
-// The lexicographic order of candidate maxima: larger exact score, then lower row, then
-// lower column.
-__device__ __forceinline__ bool better(double v, int i, int j, double bv, int bi, int bj) {
-  return v > bv || (v == bv && (i < bi || (i == bi && j < bj)));
+// A candidate's low-rank score as an unevaluated sum hi + lo of two fp32 numbers,
+// normalised so that hi = fl(hi + lo).  FP64 issues at a small fraction of the FP32 rate
+// on this part, so the re-scoring of candidates stays in fp32.
+struct Score2 {
+  float hi, lo;
+};
+
+// The lexicographic order of candidate maxima: larger score, then lower row, then lower
+// column.  On normalised pairs, (hi, lo) order is the order of hi + lo.
+__device__ __forceinline__ bool better(Score2 v, int i, int j, Score2 bv, int bi, int bj) {
+  if (v.hi != bv.hi) return v.hi > bv.hi;
+  if (v.lo != bv.lo) return v.lo > bv.lo;
+  return i < bi || (i == bi && j < bj);
+}
+
+// q~_row . k~_j from the bf16 tiles: every bf16 x bf16 product is exact in fp32, each
+// addition's rounding error is recovered exactly (two-sum) and summed in lo, so hi + lo is
+// the exact sum up to about r^2 2^-48 of sum |q~_c k~_c|; equal operands give equal results.
+// A row of a tile is r / 8 runs of 16 bytes, 128 bytes apart (the core-matrix layout).
+template <int R>
+__device__ __forceinline__ Score2 exact_score(const uint8_t* qtile, int row, const uint8_t* ktile, int j) {
+  const uint8_t* qb = qtile + coremat_offset(row, 0, R);
+  const uint8_t* kb = ktile + coremat_offset(j, 0, R);
+  float hi = 0.f, lo = 0.f;
+#pragma unroll
+  for (int g = 0; g < R / 8; ++g) {
+    const uint4 qv = *reinterpret_cast<const uint4*>(qb + g * 128);
+    const uint4 kv = *reinterpret_cast<const uint4*>(kb + g * 128);
+    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t qe = (e & 1) ? (qw[e >> 1] & 0xffff0000u) : (qw[e >> 1] << 16);
+      const uint32_t ke = (e & 1) ? (kw[e >> 1] & 0xffff0000u) : (kw[e >> 1] << 16);
+      const float p = __uint_as_float(qe) * __uint_as_float(ke);
+      const float t = hi + p;
+      const float bb = t - hi;
+      lo += (hi - (t - bb)) + (p - bb);
+      hi = t;
+    }
+  }
+  const float t = hi + lo;  // |lo| <= |hi| here: fast two-sum
+  return {t, lo - (t - hi)};
 }
 
 template <int R, int D>
@@ -105,9 +146,19 @@ __global__ void __launch_bounds__(kDistThreads, 1)
     distill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, DistArgs a) {
   using C = DistCfg<R, D>;
   constexpr int JS = C::JS;
+  // twice the rounding bound of one low-rank score per unit of ||q~|| ||k~||: (4 r + 4) u
+  constexpr float kBoundCoef = (4.0f * R + 4.0f) * kUnitF;
   const int nb = a.g.nb;
   const int h = blockIdx.y;
   const int I0 = kDistQB * blockIdx.x;
+  // Key blocks are visited from a per-CTA offset within a window of 64: CTAs running side by
+  // side add their G_k terms to different key tokens (the same few rows of one key block
+  // would otherwise take every CTA's atomics at once) while their key tiles stay close in L2.
+  const int rot = (int)(blockIdx.x % 64u) % nb;
+  auto key_block = [&](int it) {
+    const int J = it + rot;
+    return J >= nb ? J - nb : J;
+  };
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,7 +177,7 @@ __global__ void __launch_bounds__(kDistThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* gmax = reinterpret_cast<float*>(abort_flag + 1);  // [2 groups][4 quarters] max of S~
   float* gtmax = gmax + 8;                                 // [2][4] max of S
-  double* bestv = reinterpret_cast<double*>((reinterpret_cast<uintptr_t>(gtmax + 8) + 7) & ~uintptr_t(7));  // [2][4]
+  Score2* bestv = reinterpret_cast<Score2*>(gtmax + 8);  // [2][4]
   int* besti = reinterpret_cast<int*>(bestv + 8);          // [2][4]
   int* bestj = besti + 8;                                  // [2][4]
   uint8_t* fullb = reinterpret_cast<uint8_t*>(bestj + 8);  // nb: key block J lies inside the grid
@@ -172,9 +223,9 @@ __global__ void __launch_bounds__(kDistThreads, 1)
         bulk_load(sqt + q * C::TB, a.qt + (head_tiles + I) * C::TB, C::TB, qfull);
       }
       int issued = 0;
-      for (int J = 0; J < nb; ++J) {
-        const int s = J % JS;
-        if (J >= JS && !mbar_wait(kempty + s, ((J / JS) - 1) & 1, a.status, abort_flag)) break;
+      for (int it = 0; it < nb; ++it) {
+        const int s = it % JS, J = key_block(it);
+        if (it >= JS && !mbar_wait(kempty + s, ((it / JS) - 1) & 1, a.status, abort_flag)) break;
         int t0, h0, w0;
         block_origin(a.g, J, t0, h0, w0);
         mbar_expect_tx(kfull + s, C::TILE + C::TB);
@@ -182,11 +233,11 @@ __global__ void __launch_bounds__(kDistThreads, 1)
         for (int c = 0; c < C::CH; ++c)
           tma_load_5d(sK + s * C::TILE + c * 16384, &tmK, kfull + s, c * 64, h, w0, h0, t0);
         bulk_load(skt + s * C::TB, a.kt + (head_tiles + J) * C::TB, C::TB, kfull + s);
-        issued = J + 1;
+        issued = it + 1;
       }
       if (*abort_flag) {  // let copies in flight land before the CTA exits
         wait_plain(qfull, 0);
-        for (int J = issued - JS < 0 ? 0 : issued - JS; J < issued; ++J) wait_plain(kfull + J % JS, (J / JS) & 1);
+        for (int it = issued - JS < 0 ? 0 : issued - JS; it < issued; ++it) wait_plain(kfull + it % JS, (it / JS) & 1);
       }
     }
     __syncwarp();
@@ -199,11 +250,11 @@ __global__ void __launch_bounds__(kDistThreads, 1)
     const uint64_t dA = smem_desc(smem_u32(sqt), 128, SBO, 0), dB = smem_desc(smem_u32(skt), 128, SBO, 0);
     const uint64_t dQd = smem_desc(smem_u32(sQ), 16, 1024, 2), dKd = smem_desc(smem_u32(sK), 16, 1024, 2);
     bool ok = warp_wait(qfull, 0, a.status, abort_flag);
-    for (int J = 0; ok && J < nb; ++J) {
-      const int s = J % JS;
-      if (!(ok = warp_wait(kfull + s, (J / JS) & 1, a.status, abort_flag))) break;
+    for (int it = 0; ok && it < nb; ++it) {
+      const int s = it % JS;
+      if (!(ok = warp_wait(kfull + s, (it / JS) & 1, a.status, abort_flag))) break;
       for (int q = 0; q < kDistQB; ++q) {
-        const int P = J * kDistQB + q, buf = P & 1;
+        const int P = it * kDistQB + q, buf = P & 1;
         if (P >= 2 && !(ok = warp_wait(accempty + buf, ((P >> 1) - 1) & 1, a.status, abort_flag))) break;
         tc_fence_after();
         const uint32_t tL = tmem + buf * 256, tF = tL + 128;
@@ -235,43 +286,38 @@ __global__ void __launch_bounds__(kDistThreads, 1)
     const int I = I0 + grp;
     const bool active = I < nb;
     const bool row_ok = active && block_row_token(a.g, I, row) >= 0;
-    const double qn = active ? (double)a.qnorm[head_tiles + I] : 0.0;
+    const float qn = active ? a.qnorm[head_tiles + I] : 0.f;
     const uint8_t* qtile = sqt + grp * C::TB;
-    double loss_acc = 0.0;
+    float loss_acc = 0.f, loss_comp = 0.f;  // compensated sum of this group's e^2 / 2
     for (int P = grp; P < n_pairs; P += 2) {
-      const int J = P >> 1;
-      const int s = J % JS;
+      const int s = (P >> 1) % JS, J = key_block(P >> 1);
       // a failed wait stops all four warps of the group at the same barrier below
       const bool okw = warp_wait(accf + grp, (P >> 1) & 1, a.status, abort_flag);
       const bool fj = fullb[J] != 0;
-      // this row's maximum of S~ and of S, over the key rows inside the grid
+      // The row maxima of S~ (mi) and S (ti), over the key rows inside the grid; the
+      // reducing TMEM load gives them for full key blocks.
       float mi = -INFINITY, ti = -INFINITY;
-      if (okw) tc_fence_after();
+      if (okw) {
+        tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 4 && okw; ++cc) {
-        uint32_t u[32];
-        tmem_ld32(tL + cc * 32, u);
-        tmem_wait_ld();
-        const uint32_t vm = fj ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float v = __uint_as_float(u[e]);
-          if ((vm >> e) & 1u) mi = fmaxf(mi, v);
-        }
-      }
-#pragma unroll
-      for (int cc = 0; cc < 4 && okw; ++cc) {
-        uint32_t u[32];
-        float mx;
-        tmem_ld32_max(tF + cc * 32, u, mx);
-        tmem_wait_ld();
-        if (fj) {
-          ti = fmaxf(ti, mx);
-        } else {
-          const uint32_t vm = block_rows_mask32(a.g, J, cc * 32);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if ((vm >> e) & 1u) ti = fmaxf(ti, __uint_as_float(u[e]));
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t tb = half ? tF : tL;
+          float m = -INFINITY;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; cc += 2) {
+            uint32_t w0[32], w1[32];
+            float x0, x1;
+            tmem_ld32_max(tb + cc * 32, w0, x0);
+            tmem_ld32_max(tb + cc * 32 + 32, w1, x1);
+            tmem_wait_ld();
+            if (fj) {
+              m = fmaxf(m, fmaxf(x0, x1));
+            } else {
+              m = fmaxf(m, masked_max64(block_rows_mask32(a.g, J, cc * 32), block_rows_mask32(a.g, J, cc * 32 + 32),
+                                        w0, w1));
+            }
+          }
+          if (half) ti = m; else mi = m;
         }
       }
       if (!row_ok) {
@@ -295,33 +341,38 @@ __global__ void __launch_bounds__(kDistThreads, 1)
         M = fmaxf(M, gmax[grp * 4 + qq]);
         T = fmaxf(T, gtmax[grp * 4 + qq]);
       }
-      // Every fp32 score within the rounding bound of the fp32 maximum is a candidate
-      // for the exact maximum: |fl(q~.k~) - q~.k~| <= r u ||q~|| ||k~|| / (1 - r u) for
-      // any order of the r fp32 additions, so an entry and the true maximum differ from
-      // their exact values by at most half the bound below each.
-      const double delta = (2.0 * R + 2.0) * kUnit * qn * (double)a.knorm[head_tiles + J];
-      const double floor_v = (double)M - delta;
-      const bool cand = row_ok && (double)mi >= floor_v;
-      double bv = -INFINITY;
+      // Every fp32 score within twice the rounding bound of the fp32 maximum M is a
+      // candidate for the exact maximum.  An r-term dot product accumulated in fp32, with
+      // each of at most r additions rounded to nearest or truncated, is off by at most
+      // 2 r u ||q~|| ||k~|| (1 + O(u)), u = 2^-24; delta_f rounds (4 r + 4) u ||q~|| ||k~||
+      // up and floor_f rounds M - delta_f down, so the entries >= floor_f of the candidate
+      // rows (mi >= floor_f) hold every entry that can be the exact maximum.  The tests
+      // stay in fp32 (FP64 is slow on this part); only candidates are re-scored.
+      const float delta_f = __fmul_ru(__fmul_ru(kBoundCoef, qn), a.knorm[head_tiles + J]);
+      const float floor_f = __fsub_rd(M, delta_f);
+      const bool cand = row_ok && mi >= floor_f;
+      Score2 bv = {-INFINITY, 0.f};
       int bi = 0x7fffffff, bj = 0x7fffffff;
-      if (__any_sync(0xffffffffu, cand)) {
+      const bool wcand = __any_sync(0xffffffffu, cand);
+      if (wcand) {  // usually one warp of the four: its candidate row's columns, again from TMEM
         const uint8_t* ktile = skt + s * C::TB;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
-          uint32_t u[32];
-          tmem_ld32(tL + cc * 32, u);
+          uint32_t w[32];
+          tmem_ld32(tL + cc * 32, w);
           tmem_wait_ld();
           uint32_t cm = 0;
-          const uint32_t vm = fj ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32);
+          if (cand) {
+            const uint32_t vm = fj ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) cm |= (((vm >> e) & 1u) && (double)__uint_as_float(u[e]) >= floor_v ? 1u : 0u) << e;
-          if (!cand) cm = 0;
+            for (int e = 0; e < 32; ++e) cm |= (__uint_as_float(w[e]) >= floor_f ? 1u : 0u) << e;
+            cm &= vm;
+          }
           while (cm) {  // ascending columns: the first of equal exact scores is kept
             const int e = __ffs(cm) - 1;
             cm &= cm - 1;
             const int j = cc * 32 + e;
-            double v = 0.0;
-            for (int c = 0; c < R; ++c) v += (double)bf16_at(qtile, row, c, R) * (double)bf16_at(ktile, j, c, R);
+            const Score2 v = exact_score<R>(qtile, row, ktile, j);
             if (better(v, row, j, bv, bi, bj)) {
               bv = v;
               bi = row;
@@ -334,14 +385,16 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(accempty + grp);
+      if (wcand) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o), oj = __shfl_xor_sync(0xffffffffu, bj, o);
-        if (better(ov, oi, oj, bv, bi, bj)) {
-          bv = ov;
-          bi = oi;
-          bj = oj;
+        for (int o = 16; o > 0; o >>= 1) {
+          const Score2 ov = {__shfl_xor_sync(0xffffffffu, bv.hi, o), __shfl_xor_sync(0xffffffffu, bv.lo, o)};
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o), oj = __shfl_xor_sync(0xffffffffu, bj, o);
+          if (better(ov, oi, oj, bv, bi, bj)) {
+            bv = ov;
+            bi = oi;
+            bj = oj;
+          }
         }
       }
       if (lane == 0) {
@@ -351,7 +404,7 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       }
       named_bar(2 + grp, 128);
       if (quarter == 0) {  // one warp of the group adds the gradient terms
-        double v = bestv[grp * 4];
+        Score2 v = bestv[grp * 4];
         int i = besti[grp * 4], j = bestj[grp * 4];
 #pragma unroll
         for (int qq = 1; qq < 4; ++qq)
@@ -361,11 +414,14 @@ __global__ void __launch_bounds__(kDistThreads, 1)
             j = bestj[grp * 4 + qq];
           }
         if (active && i < 128 && j < 128) {
-          const double e = v - (double)T;
+          const float e = (v.hi - T) + v.lo;
           const long long pair = (head_tiles + I) * nb + J;
           if (lane == 0) {
-            loss_acc += 0.5 * e * e;
-            if (a.s_out) a.s_out[pair] = (float)v;
+            const float y = 0.5f * e * e - loss_comp;
+            const float t1 = loss_acc + y;
+            loss_comp = (t1 - loss_acc) - y;
+            loss_acc = t1;
+            if (a.s_out) a.s_out[pair] = v.hi;
             if (a.t_out) a.t_out[pair] = T;
           }
           const long long hrow = ((long long)a.b * a.Hh + h) * a.N;
@@ -373,15 +429,15 @@ __global__ void __launch_bounds__(kDistThreads, 1)
           float* gk = a.Gk + (hrow + block_row_token(a.g, J, j)) * R;
           const uint8_t* ktile = skt + s * C::TB;
           for (int c = lane; c < R; c += 32) {
-            atomicAdd(gq + c, (float)(e * (double)bf16_at(ktile, j, c, R)));
-            atomicAdd(gk + c, (float)(e * (double)bf16_at(qtile, i, c, R)));
+            atomicAdd(gq + c, e * bf16_at(ktile, j, c, R));
+            atomicAdd(gk + c, e * bf16_at(qtile, i, c, R));
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(kempty + s);  // this group no longer reads stage s
       }
     }
-    if (quarter == 0 && lane == 0 && loss_acc != 0.0) atomicAdd(a.loss, loss_acc);
+    if (quarter == 0 && lane == 0 && loss_acc != 0.f) atomicAdd(a.loss, (double)loss_acc - (double)loss_comp);
   }
   __syncthreads();
   if (warp == 1) {

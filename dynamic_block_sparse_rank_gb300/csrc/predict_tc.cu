@@ -175,18 +175,6 @@ __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-// Max of the loaded values whose column bit is set in v0 (u0) or v1 (u1).
-__device__ __forceinline__ float masked_max64(uint32_t v0, uint32_t v1, const uint32_t (&u0)[32],
-                                              const uint32_t (&u1)[32]) {
-  float m = -INFINITY;
-#pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    if ((v0 >> c) & 1u) m = fmaxf(m, __uint_as_float(u0[c]));
-    if ((v1 >> c) & 1u) m = fmaxf(m, __uint_as_float(u1[c]));
-  }
-  return m;
-}
-
 // One CTA per (QB consecutive query blocks, head).  For every key block J and
 // query block q the pair P = J QB + q is accumulated (M=128 query rows, N=128
 // key rows, K=r) in TMEM buffer P mod 4 and reduced to its max by group P mod 4.

@@ -587,3 +587,60 @@ def test_predictor_training_signal_matches_oracle(sda, wl):
     check_predictor_grad(dWq, dWq_ref, "dWq")
     check_predictor_grad(dWk, dWk_ref, "dWk")
     assert sda.sda_get_device_status() == sda.SDA_OK
+
+
+def _tied_selection_inputs(wl, seed=7):
+    """Inputs whose low-rank operands are exact on both sides, with planted exact ties.
+
+    Wq[h] and Wk[h] are selection matrices (one 1 per column), so q~ and k~ are copies of r columns of Q and K:
+    bf16 values that neither projection rounds.  In every block two query rows (a before c in tile order) carry
+    the same vector z_h in the selected columns of Q, and two key rows (ka before kc) carry z_h in those of K; z_h
+    is 8 times a drawn row, so z_h . z_h beats every other pair and each (I, J) has a four-way exact tie whose
+    first pair is (a, ka).  The rest of those Q and K rows stay as drawn, so which tied token the gradient takes
+    shows in dWq and dWk."""
+    x = inputs.generate(wl, names=("Q", "K", "Wq", "Wk"))
+    geom = _geom(wl)
+    rng = np.random.default_rng(seed)
+    Q, K = x["Q"].copy(), x["K"].copy()
+    Wq, Wk = np.zeros_like(x["Wq"]), np.zeros_like(x["Wk"])
+    for h in range(wl.heads):
+        sq = rng.choice(wl.d, wl.rank, replace=False)
+        sk = rng.choice(wl.d, wl.rank, replace=False)
+        Wq[h, sq, np.arange(wl.rank)] = 1.0
+        Wk[h, sk, np.arange(wl.rank)] = 1.0
+        for b in range(wl.B):
+            z = 8.0 * Q[b, int(geom.tokens(0)[0]), h, sq]  # bf16 values times a power of two: still bf16
+            for I in range(geom.n_blocks):
+                toks = geom.tokens(I)
+                assert len(toks) >= 4
+                for t in (toks[1], toks[-2]):
+                    Q[b, t, h, sq] = z
+                for t in (toks[2], toks[-1]):
+                    K[b, t, h, sk] = z
+    return {"Q": Q, "K": K, "Wq": Wq, "Wk": Wk}, geom
+
+
+@pytest.mark.parametrize("wl", [RAGGED_D64, TILE_4X4X8], ids=lambda w: w.name)
+def test_predictor_training_signal_takes_the_first_exact_maximum(sda, wl):
+    """Reading 14's tie rule, pinned on the GPU: with exact low-rank operands the GPU's s must be the oracle's
+    exact maximum rounded once to fp32 (no tolerance), and the planted four-way ties must go to the first query
+    row and key column in tile order; dWq and dWk then match to fp32 accumulation (a wrong pick in a single
+    block moves them by about 1e-2, relative)."""
+    x, geom = _tied_selection_inputs(wl)
+    dWq, dWk, L, s, t = _gpu_predictor_grad(sda, wl, x)
+    L_ref, dWq_ref, dWk_ref, s_ref, t_ref = orc.predictor_distill_grad(x["Q"], x["K"], x["Wq"], x["Wk"], geom,
+                                                                        wl.dtype)
+    # the construction: every block pair's maximum is z . z
+    for b in range(wl.B):
+        for h in range(wl.heads):
+            q = np.asarray(x["Q"][b, geom.tokens(0)[1], h], dtype=np.float64)
+            zz = float(np.sum(q ** 2 * (x["Wq"][h].sum(axis=1) > 0)))
+            assert np.all(s_ref[b, h] == zz)
+    np.testing.assert_array_equal(s, s_ref.astype(np.float32))
+    assert np.abs(t - t_ref).max() / np.abs(t_ref).max() < 1e-5
+    assert abs(L - L_ref) <= 1e-4 * abs(L_ref), (L, L_ref)
+    # e = s - t carries t's fp32 accumulation (~1e-6 relative); one wrong tie pick moves dW by ~1e-2
+    for name, got, ref in (("dWq", dWq, dWq_ref), ("dWk", dWk, dWk_ref)):
+        mx, rel = errors(got, ref)
+        assert rel <= 1e-4 and mx <= 1e-4 * np.abs(ref).max(), f"{name}: max-abs {mx:.3e}, rel-frob {rel:.3e}"
+    assert sda.sda_get_device_status() == sda.SDA_OK
