@@ -120,7 +120,7 @@ template <int R>
 __device__ __forceinline__ Score2 exact_score(const uint8_t* qtile, int row, const uint8_t* ktile, int j) {
   const uint8_t* qb = qtile + coremat_offset(row, 0, R);
   const uint8_t* kb = ktile + coremat_offset(j, 0, R);
-  float hi = 0.f, lo = 0.f;
+  float hi[2] = {0.f, 0.f}, lo[2] = {0.f, 0.f};  // even and odd terms: two shorter dependence chains
 #pragma unroll
   for (int g = 0; g < R / 8; ++g) {
     const uint4 qv = *reinterpret_cast<const uint4*>(qb + g * 128);
@@ -131,14 +131,17 @@ __device__ __forceinline__ Score2 exact_score(const uint8_t* qtile, int row, con
       const uint32_t qe = (e & 1) ? (qw[e >> 1] & 0xffff0000u) : (qw[e >> 1] << 16);
       const uint32_t ke = (e & 1) ? (kw[e >> 1] & 0xffff0000u) : (kw[e >> 1] << 16);
       const float p = __uint_as_float(qe) * __uint_as_float(ke);
-      const float t = hi + p;
-      const float bb = t - hi;
-      lo += (hi - (t - bb)) + (p - bb);
-      hi = t;
+      const float t = hi[e & 1] + p;
+      const float bb = t - hi[e & 1];
+      lo[e & 1] += (hi[e & 1] - (t - bb)) + (p - bb);
+      hi[e & 1] = t;
     }
   }
-  const float t = hi + lo;  // |lo| <= |hi| here: fast two-sum
-  return {t, lo - (t - hi)};
+  const float t = hi[0] + hi[1];  // two-sum of the two partial sums
+  const float bb = t - hi[0];
+  const float l = (lo[0] + lo[1]) + ((hi[0] - (t - bb)) + (hi[1] - bb));
+  const float u = t + l;  // |l| <= |t| here: fast two-sum
+  return {u, l - (u - t)};
 }
 
 template <int R, int D>
@@ -291,33 +294,44 @@ __global__ void __launch_bounds__(kDistThreads, 1)
     float loss_acc = 0.f, loss_comp = 0.f;  // compensated sum of this group's e^2 / 2
     for (int P = grp; P < n_pairs; P += 2) {
       const int s = (P >> 1) % JS, J = key_block(P >> 1);
+      const float kn = a.knorm[head_tiles + J];  // issued before the wait: its latency overlaps it
       // a failed wait stops all four warps of the group at the same barrier below
       const bool okw = warp_wait(accf + grp, (P >> 1) & 1, a.status, abort_flag);
       const bool fj = fullb[J] != 0;
       // The row maxima of S~ (mi) and S (ti), over the key rows inside the grid; the
       // reducing TMEM load gives them for full key blocks.
       float mi = -INFINITY, ti = -INFINITY;
+      float cmx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // per 32 columns of S~
       if (okw) {
         tc_fence_after();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t tb = half ? tF : tL;
-          float m = -INFINITY;
-#pragma unroll 1
-          for (int cc = 0; cc < 4; cc += 2) {
-            uint32_t w0[32], w1[32];
-            float x0, x1;
-            tmem_ld32_max(tb + cc * 32, w0, x0);
-            tmem_ld32_max(tb + cc * 32 + 32, w1, x1);
-            tmem_wait_ld();
-            if (fj) {
-              m = fmaxf(m, fmaxf(x0, x1));
-            } else {
-              m = fmaxf(m, masked_max64(block_rows_mask32(a.g, J, cc * 32), block_rows_mask32(a.g, J, cc * 32 + 32),
-                                        w0, w1));
-            }
+        for (int cc = 0; cc < 4; cc += 2) {
+          uint32_t w0[32], w1[32];
+          float x0, x1;
+          tmem_ld32_max(tL + cc * 32, w0, x0);
+          tmem_ld32_max(tL + cc * 32 + 32, w1, x1);
+          tmem_wait_ld();
+          if (!fj) {
+            x0 = masked_max64(block_rows_mask32(a.g, J, cc * 32), 0u, w0, w1);
+            x1 = masked_max64(0u, block_rows_mask32(a.g, J, cc * 32 + 32), w0, w1);
           }
-          if (half) ti = m; else mi = m;
+          cmx[cc] = x0;
+          cmx[cc + 1] = x1;
+        }
+        mi = fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3]));
+#pragma unroll 1
+        for (int cc = 0; cc < 4; cc += 2) {
+          uint32_t w0[32], w1[32];
+          float x0, x1;
+          tmem_ld32_max(tF + cc * 32, w0, x0);
+          tmem_ld32_max(tF + cc * 32 + 32, w1, x1);
+          tmem_wait_ld();
+          if (fj) {
+            ti = fmaxf(ti, fmaxf(x0, x1));
+          } else {
+            ti = fmaxf(ti, masked_max64(block_rows_mask32(a.g, J, cc * 32), block_rows_mask32(a.g, J, cc * 32 + 32),
+                                        w0, w1));
+          }
         }
       }
       if (!row_ok) {
@@ -348,7 +362,7 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       // up and floor_f rounds M - delta_f down, so the entries >= floor_f of the candidate
       // rows (mi >= floor_f) hold every entry that can be the exact maximum.  The tests
       // stay in fp32 (FP64 is slow on this part); only candidates are re-scored.
-      const float delta_f = __fmul_ru(__fmul_ru(kBoundCoef, qn), a.knorm[head_tiles + J]);
+      const float delta_f = __fmul_ru(__fmul_ru(kBoundCoef, qn), kn);
       const float floor_f = __fsub_rd(M, delta_f);
       const bool cand = row_ok && mi >= floor_f;
       Score2 bv = {-INFINITY, 0.f};
@@ -356,13 +370,15 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       const bool wcand = __any_sync(0xffffffffu, cand);
       if (wcand) {  // usually one warp of the four: its candidate row's columns, again from TMEM
         const uint8_t* ktile = skt + s * C::TB;
-#pragma unroll 1
+#pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
+          const bool need = cand && cmx[cc] >= floor_f;  // the 32 columns can hold a candidate
+          if (!__any_sync(0xffffffffu, need)) continue;
           uint32_t w[32];
           tmem_ld32(tL + cc * 32, w);
           tmem_wait_ld();
           uint32_t cm = 0;
-          if (cand) {
+          if (need) {
             const uint32_t vm = fj ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32);
 #pragma unroll
             for (int e = 0; e < 32; ++e) cm |= (__uint_as_float(w[e]) >= floor_f ? 1u : 0u) << e;
@@ -385,7 +401,14 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(accempty + grp);
-      if (wcand) {
+      const unsigned found = __ballot_sync(0xffffffffu, bi != 0x7fffffff);
+      if (found != 0u && (found & (found - 1u)) == 0u) {  // one lane holds the warp's best
+        const int src = __ffs(found) - 1;
+        bv.hi = __shfl_sync(0xffffffffu, bv.hi, src);
+        bv.lo = __shfl_sync(0xffffffffu, bv.lo, src);
+        bi = __shfl_sync(0xffffffffu, bi, src);
+        bj = __shfl_sync(0xffffffffu, bj, src);
+      } else if (found != 0u) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
           const Score2 ov = {__shfl_xor_sync(0xffffffffu, bv.hi, o), __shfl_xor_sync(0xffffffffu, bv.lo, o)};
@@ -424,17 +447,34 @@ __global__ void __launch_bounds__(kDistThreads, 1)
             if (a.s_out) a.s_out[pair] = v.hi;
             if (a.t_out) a.t_out[pair] = T;
           }
+          // the operand values leave the stage before it is released; the atomics follow
+          // the release (an arrive orders the thread's earlier memory operations before it,
+          // and would otherwise wait for these atomics to reach L2)
+          const uint8_t* ktile = skt + s * C::TB;
+          float kv[(R + 31) / 32], qv[(R + 31) / 32];
+#pragma unroll
+          for (int u = 0; u < (R + 31) / 32; ++u) {
+            const int c = lane + 32 * u;
+            kv[u] = c < R ? bf16_at(ktile, j, c, R) : 0.f;
+            qv[u] = c < R ? bf16_at(qtile, i, c, R) : 0.f;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(kempty + s);  // this group no longer reads stage s
           const long long hrow = ((long long)a.b * a.Hh + h) * a.N;
           float* gq = a.Gq + (hrow + block_row_token(a.g, I, i)) * R;
           float* gk = a.Gk + (hrow + block_row_token(a.g, J, j)) * R;
-          const uint8_t* ktile = skt + s * C::TB;
-          for (int c = lane; c < R; c += 32) {
-            atomicAdd(gq + c, e * bf16_at(ktile, j, c, R));
-            atomicAdd(gk + c, e * bf16_at(qtile, i, c, R));
+#pragma unroll
+          for (int u = 0; u < (R + 31) / 32; ++u) {
+            const int c = lane + 32 * u;
+            if (c < R) {
+              atomicAdd(gq + c, e * kv[u]);
+              atomicAdd(gk + c, e * qv[u]);
+            }
           }
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(kempty + s);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(kempty + s);  // this group no longer reads stage s
       }
     }
     if (quarter == 0 && lane == 0 && loss_acc != 0.f) atomicAdd(a.loss, (double)loss_acc - (double)loss_comp);
