@@ -1,0 +1,145 @@
+"""Oracle for 3D deformable sliding attention: a plain, slow, fp64 CPU statement.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this module; only the
+tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+call it.  It shares no code with the CUDA path.
+
+What it follows: "MegaSlide-DiT" (gist.science explainer), section 2 "3D
+deformable sliding attention (3D-DSA)": each token attends to keys and values
+sampled in a local kt x kh x kw space-time neighbourhood rather than to the
+whole sequence; the sampling points are moved by offsets that a light 3D
+convolution followed by a linear layer predicts from the input; the samples
+are taken by trilinear interpolation; the cost is linear in the number of
+tokens for a fixed window.
+
+Readings taken where the page is silent (each is restated in the design notes):
+
+D1. The window sizes kt, kh, kw are odd; the S = kt kh kw base points of token
+    (t, h, w) are (t + a, h + b, w + c) for a in -(kt-1)/2 .. (kt-1)/2 (and so
+    on), in (a, b, c) raster order.
+D2. The offsets are predicted per head from that head's queries: a depthwise
+    3 x 3 x 3 convolution over the token grid (zero padding, per-channel bias),
+    then a linear layer from d channels to 3 S outputs (with bias), giving one
+    (dt, dh, dw) offset per sampling point, in token units.
+D3. Sampling point s of token n is p_n + g_s + offset_{n,s}.  Keys and values
+    there are the trilinear interpolation of the grid's K and V rows; grid
+    points outside the T x H x W raster count as zero vectors (zero padding),
+    so a sample wholly outside the grid has k = v = 0 and still takes part in
+    the softmax with logit 0.
+D4. Attention over the S samples of a token: logits scale * q . k_s (scale
+    1/sqrt(d) unless given), softmax over s, O = sum_s softmax_s v_s, and the
+    natural-log log-sum-exp of the logits, per (batch, head, token).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+def window_points(kt, kh, kw):
+    """Base offsets g_s of the window (reading D1), shape [S, 3] in (t, h, w) order."""
+    for k in (kt, kh, kw):
+        if k < 1 or k % 2 == 0:
+            raise ValueError("window sizes must be odd and positive")
+    pts = []
+    for a in range(kt):
+        for b in range(kh):
+            for c in range(kw):
+                pts.append((a - (kt - 1) // 2, b - (kh - 1) // 2, c - (kw - 1) // 2))
+    return np.asarray(pts, dtype=np.float64)
+
+
+def token_coords(T, H, W):
+    """(t, h, w) of every raster token n = (t H + h) W + w, shape [N, 3]."""
+    t, h, w = np.meshgrid(np.arange(T), np.arange(H), np.arange(W), indexing="ij")
+    return np.stack([t.ravel(), h.ravel(), w.ravel()], axis=1).astype(np.float64)
+
+
+def dsa3d_offsets(Q, Wc, bc, Wl, bl, T, H, W):
+    """Offsets of every sampling point (reading D2).
+
+    Q: [B, N, Hh, d] with N = T H W in raster order; Wc: [Hh, d, 3, 3, 3]
+    (depthwise kernel, taps in (dt, dh, dw) order, centre at [1, 1, 1]);
+    bc: [Hh, d]; Wl: [Hh, d, 3 S]; bl: [Hh, 3 S].
+    Returns [B, N, Hh, S, 3] fp64: Y = conv(Q_h) + bc, offsets = Y Wl[h] + bl[h].
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    B, N, Hh, d = Q.shape
+    assert N == T * H * W
+    S3 = Wl.shape[2]
+    X = Q.reshape(B, T, H, W, Hh, d)
+    Xp = np.zeros((B, T + 2, H + 2, W + 2, Hh, d))
+    Xp[:, 1:-1, 1:-1, 1:-1] = X
+    out = np.empty((B, N, Hh, S3 // 3, 3))
+    for h in range(Hh):
+        Y = np.broadcast_to(np.asarray(bc[h], dtype=np.float64), (B, T, H, W, d)).copy()
+        for a in range(3):
+            for b in range(3):
+                for c in range(3):
+                    Y += Xp[:, a:a + T, b:b + H, c:c + W, h, :] * np.asarray(Wc[h, :, a, b, c], dtype=np.float64)
+        off = Y.reshape(B, N, d) @ np.asarray(Wl[h], dtype=np.float64) + np.asarray(bl[h], dtype=np.float64)
+        out[:, :, h] = off.reshape(B, N, S3 // 3, 3)
+    return out
+
+
+def trilinear(X, pos, T, H, W):
+    """Trilinear interpolation of grid rows (reading D3).
+
+    X: [N, d] rows of one (batch, head) in raster order; pos: [..., 3] fractional
+    (t, h, w) positions.  Each of the 8 surrounding grid points weighs the product
+    of (1 - |distance|) along the three axes; points outside the raster are zero
+    rows.  Returns [..., d].
+    """
+    pos = np.asarray(pos, dtype=np.float64)
+    base = np.floor(pos)
+    frac = pos - base
+    out = np.zeros(pos.shape[:-1] + (X.shape[1],))
+    for ct in (0, 1):
+        for ch in (0, 1):
+            for cw in (0, 1):
+                t = base[..., 0] + ct
+                h = base[..., 1] + ch
+                w = base[..., 2] + cw
+                wt = np.where(ct, frac[..., 0], 1.0 - frac[..., 0])
+                wh = np.where(ch, frac[..., 1], 1.0 - frac[..., 1])
+                ww = np.where(cw, frac[..., 2], 1.0 - frac[..., 2])
+                inside = (t >= 0) & (t < T) & (h >= 0) & (h < H) & (w >= 0) & (w < W)
+                n = np.where(inside, (t * H + h) * W + w, 0).astype(np.int64)
+                out += (np.where(inside, wt * wh * ww, 0.0))[..., None] * X[n]
+    return out
+
+
+def dsa3d_fwd(Q, K, V, offsets, T, H, W, kt, kh, kw, scale=None, tokens=None):
+    """3D deformable sliding attention forward (readings D1, D3, D4).
+
+    Q, K, V: [B, N, Hh, d]; offsets: [B, N, Hh, S, 3].  Returns (O [B, Nq, Hh, d],
+    LSE [B, Hh, Nq]) fp64, Nq = N, or the number of `tokens` when only those
+    query tokens (raster indices) are wanted.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    offsets = np.asarray(offsets, dtype=np.float64)
+    B, N, Hh, d = Q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    g = window_points(kt, kh, kw)
+    toks = np.arange(N) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    p = token_coords(T, H, W)[toks]
+    O = np.zeros((B, len(toks), Hh, d))
+    L = np.zeros((B, Hh, len(toks)))
+    chunk = 256
+    for b in range(B):
+        for h in range(Hh):
+            for c0 in range(0, len(toks), chunk):
+                sl = slice(c0, c0 + chunk)
+                pos = p[sl, None, :] + g[None, :, :] + offsets[b, toks[sl], h]  # [n, S, 3]
+                ks = trilinear(K[b, :, h, :], pos, T, H, W)
+                vs = trilinear(V[b, :, h, :], pos, T, H, W)
+                logit = scale * np.einsum("nd,nsd->ns", Q[b, toks[sl], h, :], ks)
+                m = logit.max(axis=1, keepdims=True)
+                e = np.exp(logit - m)
+                z = e.sum(axis=1, keepdims=True)
+                O[b, sl, h, :] = np.einsum("ns,nsd->nd", e / z, vs)
+                L[b, h, sl] = (m + np.log(z))[:, 0]
+    return O, L
