@@ -76,6 +76,17 @@ def parse():
     return ap.parse_args()
 
 
+def dsa3d_fractions(dsa, hbm_peak, sm_mhz):
+    """Fractions for the 3D-DSA kernels: of the measured HBM peak, and of the FP32 peak derived from the unit
+    counts (152 SMs x 128 FP32 lanes x 2 FLOP per FMA) at the clock sampled during the run."""
+    fp32_peak = 152 * 128 * 2 * (sm_mhz or 1900.0) * 1e6 / 1e12
+    for k in ("offsets", "attention"):
+        dsa[k]["frac_of_hbm_peak"] = dsa[k]["gbs"] / hbm_peak
+        dsa[k]["frac_of_fp32_peak"] = dsa[k]["tflops"] / fp32_peak
+    dsa["fp32_peak_tflops"] = fp32_peak
+    return dsa
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -504,6 +515,50 @@ def main():
         pgrad = {"workload": pw.name, "ms": gms, "flops": gflops, "tflops": gflops / (gms / 1e3) / 1e12}
         del tp, gws
 
+    # ---- 3D deformable sliding attention on the same 524K-token grid: offsets, then the window attention
+    dsa = None
+    if rank == 0:
+        dw = inputs.DSA3D_WORKLOADS["dsa3d_524k"]
+        xd = inputs.generate_dsa3d(dw, names=("Wc", "bc", "Wl", "bl"))
+        td = {n: torch.from_numpy(xd[n]).to(dev) for n in xd}
+        g = torch.Generator(device=dev).manual_seed(1)
+        dshape = (dw.B, dw.N, dw.heads, dw.d)
+        # seeded device draws of the activations (N(0,1), bf16): the offsets come from the network
+        aQ, aK, aV = (torch.randn(dshape, device=dev, generator=g).to(torch.bfloat16) for _ in range(3))
+        doff = torch.empty((dw.B, dw.N, dw.heads, dw.S, 3), dtype=torch.float32, device=dev)
+        aO = torch.empty_like(aQ)
+        aL = torch.empty((dw.B, dw.heads, dw.N), dtype=torch.float32, device=dev)
+        dp = sda.dsa3d_problem(dw.B, dw.T, dw.H, dw.W, dw.heads, dw.d, dw.kt, dw.kh, dw.kw)
+        for _ in range(2):
+            sda.sda_dsa3d_offsets(dp, aQ, td["Wc"], td["bc"], td["Wl"], td["bl"], doff, stream=stream)
+            sda.sda_dsa3d_fwd(dp, aQ, aK, aV, doff, aO, aL, stream=stream)
+        de = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        reps = 3
+        t_off = t_att = 0.0
+        for _ in range(reps):
+            de[0].record(stream)
+            sda.sda_dsa3d_offsets(dp, aQ, td["Wc"], td["bc"], td["Wl"], td["bl"], doff, stream=stream)
+            de[1].record(stream)
+            sda.sda_dsa3d_fwd(dp, aQ, aK, aV, doff, aO, aL, stream=stream)
+            de[2].record(stream)
+            torch.cuda.synchronize()
+            t_off += de[0].elapsed_time(de[1]) / reps
+            t_att += de[1].elapsed_time(de[2]) / reps
+        th = float(dw.B * dw.N * dw.heads)  # (token, head) units
+        row = 2.0 * dw.d  # bytes of one bf16 row
+        # algorithmic work per (token, head): offsets 2 * 27 d + 2 d 3S FLOP, reading the Q row and writing
+        # 3S fp32; attention 8 corners x (q.k and the weighted v) = 32 d FLOP per window point, reading the
+        # Q, K, V rows once (ideal reuse) and the offsets, writing the O row and the LSE
+        f_off, b_off = th * (2.0 * 27 * dw.d + 2.0 * dw.d * 3 * dw.S), th * (row + 12.0 * dw.S)
+        f_att, b_att = th * 32.0 * dw.d * dw.S, th * (3 * row + 12.0 * dw.S + row + 4.0)
+        dsa = {"workload": dw.name, "tokens": dw.N, "heads": dw.heads, "window": [dw.kt, dw.kh, dw.kw],
+               "ms": {"offsets": t_off, "attention": t_att, "total": t_off + t_att},
+               "tokens_per_s": dw.B * dw.N / ((t_off + t_att) / 1e3),
+               "offsets": {"tflops": f_off / (t_off / 1e3) / 1e12, "gbs": b_off / (t_off / 1e3) / 1e9},
+               "attention": {"tflops": f_att / (t_att / 1e3) / 1e12, "gbs": b_att / (t_att / 1e3) / 1e9},
+               "status": sda.status_string(sda.sda_get_device_status(stream))}
+        del aQ, aK, aV, doff, aO, aL, td
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -578,6 +633,7 @@ def main():
                     for n, (t, f) in kern.items()},
         "merge": merge,
         "predictor_grad": dict(pgrad, frac_of_peak=pgrad["tflops"] / tc_peak) if pgrad else None,
+        "dsa3d": dsa3d_fractions(dsa, hbm_peak, clocks.get("sm_mhz")) if dsa else None,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,

@@ -374,3 +374,48 @@ sda_status sda_merge_states_bwd(int n_states, const void* const* O_parts, const 
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ 3D deformable sliding attention
+static sda_status dsa3d_args(const sda_dsa3d_problem* p, sda::Dsa3dArgs& a) {
+  if (!p) return SDA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->T < 1 || p->H < 1 || p->W < 1 || p->heads < 1 || p->d < 1) return SDA_ERR_INVALID_ARG;
+  if (p->kt < 1 || p->kh < 1 || p->kw < 1 || p->kt % 2 == 0 || p->kh % 2 == 0 || p->kw % 2 == 0)
+    return SDA_ERR_INVALID_ARG;
+  const long long N = (long long)p->T * p->H * p->W;
+  if (N > 0x7fffffffLL || N * p->heads * (long long)p->d * p->B > (1LL << 40)) return SDA_ERR_INVALID_ARG;
+  const long long S = (long long)p->kt * p->kh * p->kw;
+  if (p->d != 64 && p->d != 128) return SDA_ERR_UNSUPPORTED;
+  if (S > 125) return SDA_ERR_UNSUPPORTED;
+  if (p->heads > 65535 || p->B > 65535) return SDA_ERR_UNSUPPORTED;
+  a.B = p->B;
+  a.T = p->T;
+  a.H = p->H;
+  a.W = p->W;
+  a.heads = p->heads;
+  a.d = p->d;
+  a.kt = p->kt;
+  a.kh = p->kh;
+  a.kw = p->kw;
+  a.S = (int)S;
+  a.scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)p->d));
+  return SDA_OK;
+}
+
+sda_status sda_dsa3d_offsets(const sda_dsa3d_problem* p, const void* Q, const float* Wc, const float* bc,
+                             const float* Wl, const float* bl, float* offsets, void* stream) {
+  sda::Dsa3dArgs a;
+  const sda_status st = dsa3d_args(p, a);
+  if (st != SDA_OK) return st;
+  if (!Q || !Wc || !bc || !Wl || !bl || !offsets || !aligned16(Q)) return SDA_ERR_INVALID_ARG;
+  return from_cuda(sda::dsa3d_offsets(a, Q, Wc, bc, Wl, bl, offsets, static_cast<cudaStream_t>(stream)));
+}
+
+sda_status sda_dsa3d_fwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
+                         const float* offsets, void* O, float* LSE, void* stream) {
+  sda::Dsa3dArgs a;
+  const sda_status st = dsa3d_args(p, a);
+  if (st != SDA_OK) return st;
+  if (!Q || !K || !V || !offsets || !O || !LSE) return SDA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SDA_ERR_INVALID_ARG;
+  return from_cuda(sda::dsa3d_fwd(a, Q, K, V, offsets, O, LSE, static_cast<cudaStream_t>(stream)));
+}

@@ -1,0 +1,343 @@
+// 3D deformable sliding attention: the offset network and the sampled-window
+// attention ("MegaSlide-DiT", gist.science explainer, section 2 "3D deformable
+// sliding attention (3D-DSA)": keys and values sampled by trilinear
+// interpolation in a kt x kh x kw neighbourhood moved by offsets that a light
+// 3D convolution and a linear layer predict; linear cost in N).
+//
+// Neither step is a dense contraction worth the tensor cores: the offset
+// network is a 27-tap depthwise convolution and a d x 3S matrix per token
+// (3S = 81 outputs for a 3x3x3 window), and the attention is a batch of
+// per-token gathers of 8 S key and value rows with no operand shared between
+// tokens.  Both are SIMT kernels whose bound is the gather traffic through L1
+// (the rows of a token's neighbourhood are re-read by its neighbours) and the
+// FP32 pipe; HBM sees each input row about once.
+//
+//   dsa3d_offsets_kernel  64 raster tokens x one head per CTA.  Stage 1: a
+//                         thread owns a channel pair and runs the 27-tap
+//                         depthwise convolution for 16 or 8 tokens (zero
+//                         padding), into shared memory as [channel][token].
+//                         Stage 2: the d x 3S matrix, staged in shared memory
+//                         96 columns at a time, is applied as a register-tiled
+//                         product (4 tokens x 6 outputs per thread, packed
+//                         fp32x2 FMAs).
+//   dsa3d_fwd_kernel      a warp serves 256/d tokens of one head, a token's
+//                         row split over d/8 lanes (16 bytes each); per
+//                         window point the 8 trilinear corners
+//                         inside the raster are gathered (K and V rows, one
+//                         contiguous 128- or 256-byte row per corner), the logit
+//                         is the corner-weighted q.k reduced across the
+//                         token's lanes, and an online softmax (base 2)
+//                         accumulates the corner-weighted v (packed fp32x2
+//                         FMAs).  Positions are tested against the
+//                         raster in float before any index is formed, so a
+//                         non-finite offset only moves its sample outside.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace sda {
+
+namespace {
+
+constexpr int kDsaTok = 32;     // tokens per CTA, both kernels
+constexpr int kDsaThreads = 256;
+
+__device__ __forceinline__ void raster_coords(int n, int H, int W, int& t, int& y, int& x) {
+  x = n % W;
+  const int r = n / W;
+  y = r % H;
+  t = r / H;
+}
+
+// d = fma(a, b, c) on two fp32 lanes at once (the packed FP32 FMA of sm_100 and later).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d, ua, ub, uc;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(ua), "l"(ub), "l"(uc));
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+  return r;
+}
+
+// The two bf16 of a 32-bit word as fp32 (low half first).
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+constexpr int kOffTok = 64;     // tokens per CTA of the offset network
+constexpr int kOffJ = 96;       // outputs per pass: 16 groups of 6
+constexpr int kOffYStride = kOffTok + 4;  // floats per channel row of Y (float4-aligned)
+
+__host__ __device__ constexpr size_t offsets_smem_bytes(int D) {
+  return (size_t)D * kOffYStride * 4 + (size_t)D * kOffJ * 4;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDsaThreads) dsa3d_offsets_kernel(const __nv_bfloat16* __restrict__ Q,
+                                                                   const float* __restrict__ Wc,
+                                                                   const float* __restrict__ bc,
+                                                                   const float* __restrict__ Wl,
+                                                                   const float* __restrict__ bl,
+                                                                   float* __restrict__ off, Dsa3dArgs a) {
+  extern __shared__ __align__(16) float dsmem[];
+  float* Ys = dsmem;                      // [D][kOffYStride]
+  float* Ws = dsmem + D * kOffYStride;   // [D][kOffJ]: one pass's columns of Wl[h]
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int N = a.T * a.H * a.W;
+  const int n0 = blockIdx.x * kOffTok;
+  const int tid = threadIdx.x;
+
+  // Stage 1: Y[c][tok] = bc + sum over the 27 taps of Wc * Q (zero outside the raster).  A
+  // thread owns a channel pair: its 54 taps stay in registers, its loads are 4-byte pieces of
+  // one 128- or 256-byte row per warp.
+  {
+    constexpr int kPairs = D / 2;
+    constexpr int kGroups = kDsaThreads / kPairs;
+    const int cp = tid % kPairs, tg = tid / kPairs;
+    const int c0 = 2 * cp;
+    float w0[27], w1[27];
+    const float* wc0 = Wc + ((long long)h * D + c0) * 27;
+#pragma unroll
+    for (int k = 0; k < 27; ++k) {
+      w0[k] = wc0[k];
+      w1[k] = wc0[27 + k];
+    }
+    const float b0 = bc[h * D + c0], b1 = bc[h * D + c0 + 1];
+    const __nv_bfloat16* Qh = Q + (long long)b * N * a.heads * D + (long long)h * D + c0;
+    // two tokens per iteration: their 54 loads are in flight together
+    static_assert((kOffTok / kGroups) % 2 == 0, "tokens per thread must be even");
+    for (int tok = tg; tok < kOffTok; tok += 2 * kGroups) {
+      uint32_t v[2][27];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int n = n0 + tok + e * kGroups;
+        int t = 0, y = 0, x = 0;
+        if (n < N) raster_coords(n, a.H, a.W, t, y, x);
+#pragma unroll
+        for (int k = 0; k < 27; ++k) {
+          const int tt = t + k / 9 - 1, yy = y + (k / 3) % 3 - 1, xx = x + k % 3 - 1;
+          const bool in = n < N && tt >= 0 && tt < a.T && yy >= 0 && yy < a.H && xx >= 0 && xx < a.W;
+          const int m = (tt * a.H + yy) * a.W + xx;
+          v[e][k] = in ? __ldg(reinterpret_cast<const unsigned*>(Qh + (long long)m * a.heads * D)) : 0u;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float y0 = b0, y1 = b1;
+#pragma unroll
+        for (int k = 0; k < 27; ++k) {
+          const float2 f = bf16x2_to_f2(v[e][k]);  // zero bits outside the raster: zero padding
+          y0 = fmaf(w0[k], f.x, y0);
+          y1 = fmaf(w1[k], f.y, y1);
+        }
+        Ys[c0 * kOffYStride + tok + e * kGroups] = y0;
+        Ys[(c0 + 1) * kOffYStride + tok + e * kGroups] = y1;
+      }
+    }
+  }
+
+  // Stage 2: off[tok][j] = bl[j] + sum_c Y[c][tok] Wl[h][c][j].  Register tiles of 4 tokens x 6
+  // outputs per thread (16 x 16 threads cover 64 tokens x 96 outputs per pass).
+  const int S3 = 3 * a.S;
+  const int tg = tid / 16, jg = tid % 16;
+  const float* wl = Wl + (long long)h * D * S3;
+  for (int j0 = 0; j0 < S3; j0 += kOffJ) {
+    __syncthreads();  // Y written (first pass) / the previous pass's Ws read
+    for (int e = tid; e < D * kOffJ; e += kDsaThreads) {
+      const int c = e / kOffJ, jj = e % kOffJ;
+      Ws[e] = j0 + jj < S3 ? wl[(long long)c * S3 + j0 + jj] : 0.f;
+    }
+    __syncthreads();
+    float2 acc[4][3];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int j = j0 + jg * 6 + 2 * q;
+        acc[i][q] = make_float2(j < S3 ? bl[h * S3 + j] : 0.f, j + 1 < S3 ? bl[h * S3 + j + 1] : 0.f);
+      }
+#pragma unroll 4
+    for (int c = 0; c < D; ++c) {
+      const float4 y4 = *reinterpret_cast<const float4*>(Ys + c * kOffYStride + tg * 4);
+      const float2* wr = reinterpret_cast<const float2*>(Ws + c * kOffJ + jg * 6);
+      const float2 wv[3] = {wr[0], wr[1], wr[2]};
+      const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int q = 0; q < 3; ++q) acc[i][q] = ffma2(make_float2(yv[i], yv[i]), wv[q], acc[i][q]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int n = n0 + tg * 4 + i;
+      if (n >= N) continue;
+      float* orow = off + (((long long)b * N + n) * a.heads + h) * S3;
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const int j = j0 + jg * 6 + 2 * q;
+        if (j < S3) orow[j] = acc[i][q].x;
+        if (j + 1 < S3) orow[j + 1] = acc[i][q].y;
+      }
+    }
+  }
+}
+
+// A warp serves 256 / D tokens of one head: a token's row is split over D / 8 lanes, 8
+// channels (16 bytes) each.  Per window point the three axes give the two candidate grid
+// coordinates, their weights (1 - f, f) and whether each lies inside the raster; the 8
+// corners combine them, and only corners inside with a non-zero weight are gathered.
+template <int D>
+__global__ void __launch_bounds__(kDsaThreads) dsa3d_fwd_kernel(const __nv_bfloat16* __restrict__ Q,
+                                                               const __nv_bfloat16* __restrict__ K,
+                                                               const __nv_bfloat16* __restrict__ V,
+                                                               const float* __restrict__ off,
+                                                               __nv_bfloat16* __restrict__ O, float* __restrict__ LSE,
+                                                               Dsa3dArgs a) {
+  constexpr int LPT = D / 8;       // lanes per token
+  constexpr int TPW = 32 / LPT;    // tokens per warp at a time
+  constexpr int kWarps = kDsaThreads / 32;
+  constexpr int kPerWarp = kDsaTok / kWarps;  // tokens per warp
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = lane / LPT, sl = lane % LPT;
+  const int N = a.T * a.H * a.W;
+  const long long rs = (long long)a.heads * D;  // elements between consecutive tokens' rows
+  const __nv_bfloat16* Kb = K + (long long)b * N * rs + (long long)h * D + sl * 8;
+  const __nv_bfloat16* Vb = V + (long long)b * N * rs + (long long)h * D + sl * 8;
+  const int rt = (a.kt - 1) / 2, rh = (a.kh - 1) / 2, rw = (a.kw - 1) / 2;
+  const float Tm = (float)(a.T - 1), Hm = (float)(a.H - 1), Wm = (float)(a.W - 1);
+  const int HW = a.H * a.W;
+  for (int u = 0; u < kPerWarp; u += TPW) {
+    const int n_raw = blockIdx.x * kDsaTok + warp * kPerWarp + u + slot;
+    const bool valid = n_raw < N;
+    const int n = valid ? n_raw : N - 1;  // lanes of a missing token compute a copy and store nothing
+    int t, y, x;
+    raster_coords(n, a.H, a.W, t, y, x);
+    const long long row = ((long long)b * N + n) * rs + (long long)h * D + sl * 8;
+    float2 q[4];
+    {
+      const uint4 qv = __ldg(reinterpret_cast<const uint4*>(Q + row));
+      const float qs = a.scale * kLog2e;  // logits in base 2
+      const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = bf16x2_to_f2(w4[i]);
+        q[i] = make_float2(f.x * qs, f.y * qs);
+      }
+    }
+    const float* offn = off + (((long long)b * N + n) * a.heads + h) * (3LL * a.S);
+    float m = -INFINITY, l = 0.f;
+    float2 o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = make_float2(0.f, 0.f);
+    int s = 0;
+    for (int wa = 0; wa < a.kt; ++wa)
+      for (int wb = 0; wb < a.kh; ++wb)
+        for (int wc = 0; wc < a.kw; ++wc, ++s) {
+          const float pt = (float)(t + wa - rt) + __ldg(offn + 3 * s);
+          const float ph = (float)(y + wb - rh) + __ldg(offn + 3 * s + 1);
+          const float pw = (float)(x + wc - rw) + __ldg(offn + 3 * s + 2);
+          const float bt = floorf(pt), bh = floorf(ph), bw = floorf(pw);
+          const float ft = pt - bt, fh = ph - bh, fw = pw - bw;
+          // per axis: is coordinate base (+1) inside the raster; tested in float, so NaN or
+          // far-out positions fail here and form no index
+          const bool t0 = bt >= 0.f && bt <= Tm, t1 = bt >= -1.f && bt <= Tm - 1.f;
+          const bool h0 = bh >= 0.f && bh <= Hm, h1 = bh >= -1.f && bh <= Hm - 1.f;
+          const bool w0 = bw >= 0.f && bw <= Wm, w1 = bw >= -1.f && bw <= Wm - 1.f;
+          const float wt[2] = {1.f - ft, ft}, wh[2] = {1.f - fh, fh}, ww[2] = {1.f - fw, fw};
+          const bool vt[2] = {t0, t1}, vh[2] = {h0, h1}, vw[2] = {w0, w1};
+          // base index from coordinates clamped to [-1, max]: only corners found inside use it
+          const int it = (int)fminf(fmaxf(bt, -1.f), Tm), ih = (int)fminf(fmaxf(bh, -1.f), Hm),
+                    iw = (int)fminf(fmaxf(bw, -1.f), Wm);
+          const int m000 = (it * a.H + ih) * a.W + iw;
+          float dot = 0.f;
+          float2 vs[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) vs[i] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int corner = 0; corner < 8; ++corner) {
+            const int ct = corner >> 2, ch = (corner >> 1) & 1, cw = corner & 1;
+            const float wgt = wt[ct] * wh[ch] * ww[cw];
+            if (!(vt[ct] && vh[ch] && vw[cw]) || wgt == 0.f) continue;
+            const long long mrow = (long long)(m000 + ct * HW + ch * a.W + cw) * rs;
+            const uint4 kv = __ldg(reinterpret_cast<const uint4*>(Kb + mrow));
+            const uint4 vv = __ldg(reinterpret_cast<const uint4*>(Vb + mrow));
+            const uint32_t kw4[4] = {kv.x, kv.y, kv.z, kv.w}, vw4[4] = {vv.x, vv.y, vv.z, vv.w};
+            float2 pd = make_float2(0.f, 0.f);
+            const float2 w2 = make_float2(wgt, wgt);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              pd = ffma2(q[i], bf16x2_to_f2(kw4[i]), pd);
+              vs[i] = ffma2(w2, bf16x2_to_f2(vw4[i]), vs[i]);
+            }
+            dot = fmaf(wgt, pd.x + pd.y, dot);
+          }
+#pragma unroll
+          for (int sh = LPT / 2; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+          const float mn = fmaxf(m, dot);
+          const float corr = exp2f(m - mn), p = exp2f(dot - mn);
+          l = fmaf(l, corr, p);
+          const float2 c2 = make_float2(corr, corr), p2 = make_float2(p, p);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = ffma2(o[i], c2, make_float2(p2.x * vs[i].x, p2.y * vs[i].y));
+          m = mn;
+        }
+    if (valid) {
+      const float inv = 1.f / l;
+      uint32_t w4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 r = __floats2bfloat162_rn(o[i].x * inv, o[i].y * inv);
+        w4[i] = *reinterpret_cast<uint32_t*>(&r);
+      }
+      *reinterpret_cast<uint4*>(O + row) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      if (sl == 0) LSE[((long long)b * a.heads + h) * N + n] = (m + log2f(l)) * 0.6931471805599453f;
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_dsa3d(const Dsa3dArgs& a, const __nv_bfloat16* Q, const __nv_bfloat16* K, const __nv_bfloat16* V,
+                         const float* Wc, const float* bc, const float* Wl, const float* bl, float* off,
+                         __nv_bfloat16* O, float* LSE, bool offsets, cudaStream_t st) {
+  const long long N = (long long)a.T * a.H * a.W;
+  if (offsets) {
+    const size_t smem = offsets_smem_bytes(D);
+    cudaError_t e =
+        cudaFuncSetAttribute(dsa3d_offsets_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((N + kOffTok - 1) / kOffTok), a.heads, a.B);
+    dsa3d_offsets_kernel<D><<<grid, kDsaThreads, smem, st>>>(Q, Wc, bc, Wl, bl, off, a);
+  } else {
+    const dim3 grid((unsigned)((N + kDsaTok - 1) / kDsaTok), a.heads, a.B);
+    dsa3d_fwd_kernel<D><<<grid, kDsaThreads, 0, st>>>(Q, K, V, off, O, LSE, a);
+  }
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t dsa3d_offsets(const Dsa3dArgs& a, const void* Q, const float* Wc, const float* bc, const float* Wl,
+                          const float* bl, float* off, cudaStream_t st) {
+  const auto* q = static_cast<const __nv_bfloat16*>(Q);
+  return a.d == 64 ? launch_dsa3d<64>(a, q, nullptr, nullptr, Wc, bc, Wl, bl, off, nullptr, nullptr, true, st)
+                   : launch_dsa3d<128>(a, q, nullptr, nullptr, Wc, bc, Wl, bl, off, nullptr, nullptr, true, st);
+}
+
+cudaError_t dsa3d_fwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off, void* O,
+                      float* LSE, cudaStream_t st) {
+  const auto* q = static_cast<const __nv_bfloat16*>(Q);
+  const auto* k = static_cast<const __nv_bfloat16*>(K);
+  const auto* v = static_cast<const __nv_bfloat16*>(V);
+  auto* o = static_cast<__nv_bfloat16*>(O);
+  return a.d == 64
+             ? launch_dsa3d<64>(a, q, k, v, nullptr, nullptr, nullptr, nullptr, const_cast<float*>(off), o, LSE, false, st)
+             : launch_dsa3d<128>(a, q, k, v, nullptr, nullptr, nullptr, nullptr, const_cast<float*>(off), o, LSE, false,
+                                 st);
+}
+
+}  // namespace sda

@@ -85,6 +85,16 @@ bool make_token_map(CUtensorMap* m, const void* base, TokType t, int T, int H, i
                     int bw);
 
 // ---- predict_tc.cu (bf16 problems)
+// 3D deformable sliding attention (dsa3d.cu)
+struct Dsa3dArgs {
+  int B, T, H, W, heads, d, kt, kh, kw, S;
+  float scale;
+};
+cudaError_t dsa3d_offsets(const Dsa3dArgs& a, const void* Q, const float* Wc, const float* bc, const float* Wl,
+                          const float* bl, float* off, cudaStream_t st);
+cudaError_t dsa3d_fwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off, void* O,
+                      float* LSE, cudaStream_t st);
+
 size_t predict_ws_tc(const Prob& p);
 cudaError_t predict_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, int32_t* idx,
                        float* score, void* ws, cudaStream_t st);

@@ -252,3 +252,85 @@ def digest(arrays: dict[str, np.ndarray]) -> str:
         hsh.update(k.encode())
         hsh.update(np.ascontiguousarray(arrays[k]).tobytes())
     return hsh.hexdigest()
+
+
+# --------------------------------------------------------------------------- 3D deformable sliding attention
+# Workloads of "MegaSlide-DiT" (gist.science explainer, section 2 "3D deformable sliding attention"): the
+# same T x H x W latent grids, a kt x kh x kw window per token.  Recipe: Q, K as above (shared Fourier field
+# plus noise, so attention is local in space-time), V ~ N(0,1), all rounded to bf16; offsets ~ N(0, off_std^2)
+# in token units (fp32, drawn directly for the attention alone); offset-network weights in fp32:
+# Wc ~ N(0, 1/27), bc ~ N(0, 0.1^2), Wl ~ N(0, off_std^2 / (d (amp^2 + 1))), bl ~ N(0, 0.1^2), which gives
+# predicted offsets of about off_std tokens.
+_DSA_OFF, _DSA_WC, _DSA_BC, _DSA_WL, _DSA_BL = range(20, 25)
+
+
+@dataclasses.dataclass(frozen=True)
+class Dsa3dWorkload:
+    """Shape and generator parameters of one 3D-DSA problem (bf16 activations)."""
+
+    name: str
+    B: int
+    heads: int
+    T: int
+    H: int
+    W: int
+    d: int
+    kt: int
+    kh: int
+    kw: int
+    off_std: float
+    amp: float = 3.0
+    n_terms: int = 16
+    dtype: str = "bf16"
+
+    @property
+    def N(self) -> int:
+        return self.T * self.H * self.W
+
+    @property
+    def S(self) -> int:
+        return self.kt * self.kh * self.kw
+
+    def with_(self, **kw) -> "Dsa3dWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+DSA3D_WORKLOADS = {
+    # ragged grid, d = 64, 3 x 3 x 3 window
+    "dsa3d_ragged_d64": Dsa3dWorkload("dsa3d_ragged_d64", 1, 3, 5, 12, 20, 64, 3, 3, 3, 1.0),
+    # two batch entries, d = 128, a flat 1 x 5 x 5 window, larger offsets
+    "dsa3d_d128_1x5x5": Dsa3dWorkload("dsa3d_d128_1x5x5", 2, 2, 4, 9, 11, 128, 1, 5, 5, 1.5, 4.0),
+    # offsets of several tokens: many samples leave the raster
+    "dsa3d_far": Dsa3dWorkload("dsa3d_far", 1, 2, 3, 8, 10, 128, 3, 3, 3, 6.0),
+    # the 524,288-token grid of the block-sparse workloads, 8 heads, d = 128, 3 x 3 x 3
+    "dsa3d_524k": Dsa3dWorkload("dsa3d_524k", 1, 8, 32, 128, 128, 128, 3, 3, 3, 1.0, 4.0, 32),
+}
+
+
+def generate_dsa3d(wl: Dsa3dWorkload, seed: int = 0, names=("Q", "K", "V", "offsets"), heads=None,
+                   threads: int | None = None) -> dict[str, np.ndarray]:
+    """Draw the seeded inputs of a 3D-DSA workload.
+
+    names: Q, K, V ([B, N, heads_sel, d] float32 holding bf16 values), offsets ([B, N, heads_sel, S, 3]
+    float32), Wc ([heads_sel, d, 3, 3, 3]), bc ([heads_sel, d]), Wl ([heads_sel, d, 3 S]), bl
+    ([heads_sel, 3 S]).  As for `generate`, a head's values do not depend on which heads are asked for.
+    """
+    heads = list(range(wl.heads)) if heads is None else list(heads)
+    want = frozenset(names)
+    out = generate(wl, seed, names=tuple(n for n in ("Q", "K", "V") if n in want), heads=heads,
+                   threads=threads) if want & {"Q", "K", "V"} else {}
+    S, d = wl.S, wl.d
+    if "offsets" in want:
+        off = np.empty((wl.B, wl.N, len(heads), S, 3), dtype=np.float32)
+        for b in range(wl.B):
+            for hi, h in enumerate(heads):
+                off[b, :, hi] = wl.off_std * _rng(seed, _DSA_OFF, b, h).standard_normal((wl.N, S, 3))
+        out["offsets"] = off
+    wscale = wl.off_std / math.sqrt(d * (wl.amp ** 2 + 1.0))
+    for name, stream, shape, sd in (("Wc", _DSA_WC, (d, 3, 3, 3), 1.0 / math.sqrt(27.0)),
+                                    ("bc", _DSA_BC, (d,), 0.1),
+                                    ("Wl", _DSA_WL, (d, 3 * S), wscale),
+                                    ("bl", _DSA_BL, (3 * S,), 0.1)):
+        if name in want:
+            out[name] = np.stack([sd * _rng(seed, stream, h).standard_normal(shape) for h in heads]).astype(np.float32)
+    return out

@@ -21,7 +21,8 @@ SDA_OP_PREDICT, SDA_OP_BWD, SDA_OP_TRAIN, SDA_OP_PREDICTOR_GRAD = 0, 1, 2, 3
 EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_attn_fwd", "sda_attn_bwd",
            "sda_attn_fwd_train", "sda_attn_bwd_train", "sda_predictor_grad",
            "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_attn_bwd_partition", "sda_merge_states", "sda_merge_states_bwd",
-           "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_selftest_wait_timeout", "sda_status_string")
+           "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_selftest_wait_timeout", "sda_status_string",
+           "sda_dsa3d_offsets", "sda_dsa3d_fwd")
 
 
 class SdaError(RuntimeError):
@@ -35,6 +36,12 @@ class Problem(ctypes.Structure):
                 ("W", ctypes.c_int), ("head_dim", ctypes.c_int), ("bt", ctypes.c_int), ("bh", ctypes.c_int),
                 ("bw", ctypes.c_int), ("rank", ctypes.c_int), ("keep_ratio", ctypes.c_double),
                 ("dtype", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+
+
+class Dsa3dProblem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
+                ("heads", ctypes.c_int), ("d", ctypes.c_int), ("kt", ctypes.c_int), ("kh", ctypes.c_int),
+                ("kw", ctypes.c_int), ("scale", ctypes.c_float)]
 
 
 _lib = None
@@ -69,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.sda_merge_states.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), i32, i32, i32, i32, i32, vp, vp, vp]
         L.sda_merge_states_bwd.argtypes = [i32, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp, i32, i32, i32, i32,
                                            i32, ctypes.POINTER(vp), ctypes.POINTER(vp), vp]
+        dp = ctypes.POINTER(Dsa3dProblem)
+        L.sda_dsa3d_offsets.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
+        L.sda_dsa3d_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
         L.sda_get_device_status.argtypes = [vp]
         L.sda_status_string.argtypes = [i32]
         L.sda_status_string.restype = ctypes.c_char_p
@@ -248,3 +258,17 @@ def sda_merge_states_bwd(O_parts, LSE_parts, dO, dLSE, B, N, heads, head_dim, dt
 
 def sda_get_device_status(stream=None) -> int:
     return lib().sda_get_device_status(_stream(stream))
+
+
+def dsa3d_problem(B, T, H, W, heads, d, kt, kh, kw, scale=0.0) -> Dsa3dProblem:
+    return Dsa3dProblem(B, T, H, W, heads, d, kt, kh, kw, float(scale))
+
+
+def sda_dsa3d_offsets(p: Dsa3dProblem, Q, Wc, bc, Wl, bl, offsets, stream=None):
+    _check(lib().sda_dsa3d_offsets(ctypes.byref(p), _ptr(Q), _ptr(Wc), _ptr(bc), _ptr(Wl), _ptr(bl), _ptr(offsets),
+                                   _stream(stream)), "sda_dsa3d_offsets")
+
+
+def sda_dsa3d_fwd(p: Dsa3dProblem, Q, K, V, offsets, O, LSE, stream=None):
+    _check(lib().sda_dsa3d_fwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(offsets), _ptr(O), _ptr(LSE),
+                               _stream(stream)), "sda_dsa3d_fwd")

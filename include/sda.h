@@ -319,6 +319,53 @@ sda_status sda_predict_blocks_noalloc(const sda_problem* p, const void* Q, const
  * (and clears it).  Nothing faults or hangs; the context stays usable. */
 sda_status sda_selftest_wait_timeout(unsigned limit_us, int* completed, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * 3D deformable sliding attention ("MegaSlide-DiT", gist.science explainer,
+ * section 2 "3D deformable sliding attention (3D-DSA)"): every token attends
+ * to S = kt*kh*kw keys and values sampled by trilinear interpolation around
+ * it, at window points moved by offsets that a depthwise 3x3x3 convolution and
+ * a linear layer predict from the token's query.  Cost linear in N.
+ *
+ * Tokens of one batch entry are the T x H x W raster (n = (t*H + h)*W + w).
+ * Window point s = (a*kh + b)*kw + c of token (t, h, w) sits at
+ * (t + a - (kt-1)/2, h + b - (kh-1)/2, w + c - (kw-1)/2) plus its offset
+ * (dt, dh, dw) in token units.  K and V there are the trilinear interpolation
+ * of the grid's rows, grid points outside the raster counting as zero rows (a
+ * sample wholly outside gives k = v = 0 and logit 0; so does a non-finite
+ * offset).  Logits scale * q.k, softmax over the S samples, O the weighted sum
+ * of the sampled v, LSE the natural-log log-sum-exp of the logits.
+ *
+ * Layouts (row-major, device pointers, caller-owned, no aliasing between
+ * inputs and outputs):
+ *   Q, K, V, O  bf16 [B, N, heads, d], d in {64, 128}, 16-byte aligned
+ *   offsets     fp32 [B, N, heads, S, 3]  (dt, dh, dw) per window point
+ *   LSE         fp32 [B, heads, N]
+ *   Wc          fp32 [heads, d, 3, 3, 3]  depthwise kernel, taps (dt, dh, dw)
+ *                                         with the centre at [1, 1, 1]
+ *   bc          fp32 [heads, d]
+ *   Wl          fp32 [heads, d, 3*S]      output j = 3*s + axis
+ *   bl          fp32 [heads, 3*S]
+ * Both calls are asynchronous on `stream` (a cudaStream_t, or NULL), allocate
+ * nothing and keep no state.  SDA_ERR_INVALID_ARG for a null pointer,
+ * non-positive sizes, even window sizes or a misaligned tensor;
+ * SDA_ERR_UNSUPPORTED for d outside {64, 128} or S > 125.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int B, T, H, W; /* batch entries and the token grid, N = T*H*W */
+  int heads, d;   /* heads, head dimension */
+  int kt, kh, kw; /* odd window sizes, S = kt*kh*kw */
+  float scale;    /* softmax scale; <= 0 selects 1/sqrt(d) */
+} sda_dsa3d_problem;
+
+/* Offsets of every window point: Y = depthwise conv3d(Q of the head, Wc) + bc
+ * (zero padding), offsets = Y Wl[h] + bl[h], all in fp32 from the bf16 Q. */
+sda_status sda_dsa3d_offsets(const sda_dsa3d_problem* p, const void* Q, const float* Wc, const float* bc,
+                             const float* Wl, const float* bl, float* offsets, void* stream);
+
+/* Attention over the sampled window points (O bf16, LSE fp32), fp32 inside. */
+sda_status sda_dsa3d_fwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
+                         const float* offsets, void* O, float* LSE, void* stream);
+
 /* Host only.  Number of CUDA kernels the library has launched in this process
  * (all devices, all calls); a caller can difference it around a region. */
 unsigned long long sda_kernel_launch_count(void);

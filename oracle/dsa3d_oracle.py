@@ -25,7 +25,8 @@ D3. Sampling point s of token n is p_n + g_s + offset_{n,s}.  Keys and values
     there are the trilinear interpolation of the grid's K and V rows; grid
     points outside the T x H x W raster count as zero vectors (zero padding),
     so a sample wholly outside the grid has k = v = 0 and still takes part in
-    the softmax with logit 0.
+    the softmax with logit 0.  A sampling point with a non-finite coordinate
+    counts as wholly outside.
 D4. Attention over the S samples of a token: logits scale * q . k_s (scale
     1/sqrt(d) unless given), softmax over s, O = sum_s softmax_s v_s, and the
     natural-log log-sum-exp of the logits, per (batch, head, token).
@@ -56,30 +57,34 @@ def token_coords(T, H, W):
     return np.stack([t.ravel(), h.ravel(), w.ravel()], axis=1).astype(np.float64)
 
 
-def dsa3d_offsets(Q, Wc, bc, Wl, bl, T, H, W):
+def dsa3d_offsets(Q, Wc, bc, Wl, bl, T, H, W, tokens=None):
     """Offsets of every sampling point (reading D2).
 
     Q: [B, N, Hh, d] with N = T H W in raster order; Wc: [Hh, d, 3, 3, 3]
     (depthwise kernel, taps in (dt, dh, dw) order, centre at [1, 1, 1]);
     bc: [Hh, d]; Wl: [Hh, d, 3 S]; bl: [Hh, 3 S].
-    Returns [B, N, Hh, S, 3] fp64: Y = conv(Q_h) + bc, offsets = Y Wl[h] + bl[h].
+    Returns [B, Nq, Hh, S, 3] fp64: Y = conv(Q_h) + bc, offsets = Y Wl[h] + bl[h],
+    for every token or, when given, only the raster indices `tokens`.
     """
     Q = np.asarray(Q, dtype=np.float64)
     B, N, Hh, d = Q.shape
     assert N == T * H * W
     S3 = Wl.shape[2]
-    X = Q.reshape(B, T, H, W, Hh, d)
-    Xp = np.zeros((B, T + 2, H + 2, W + 2, Hh, d))
-    Xp[:, 1:-1, 1:-1, 1:-1] = X
-    out = np.empty((B, N, Hh, S3 // 3, 3))
+    toks = np.arange(N) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    p = token_coords(T, H, W)[toks].astype(np.int64)
+    out = np.empty((B, len(toks), Hh, S3 // 3, 3))
     for h in range(Hh):
-        Y = np.broadcast_to(np.asarray(bc[h], dtype=np.float64), (B, T, H, W, d)).copy()
+        Y = np.broadcast_to(np.asarray(bc[h], dtype=np.float64), (B, len(toks), d)).copy()
         for a in range(3):
             for b in range(3):
                 for c in range(3):
-                    Y += Xp[:, a:a + T, b:b + H, c:c + W, h, :] * np.asarray(Wc[h, :, a, b, c], dtype=np.float64)
-        off = Y.reshape(B, N, d) @ np.asarray(Wl[h], dtype=np.float64) + np.asarray(bl[h], dtype=np.float64)
-        out[:, :, h] = off.reshape(B, N, S3 // 3, 3)
+                    t, y, x = p[:, 0] + a - 1, p[:, 1] + b - 1, p[:, 2] + c - 1
+                    inside = (t >= 0) & (t < T) & (y >= 0) & (y < H) & (x >= 0) & (x < W)
+                    m = np.where(inside, (t * H + y) * W + x, 0)
+                    Y += np.where(inside[None, :, None], Q[:, m, h, :], 0.0) * np.asarray(Wc[h, :, a, b, c],
+                                                                                          dtype=np.float64)
+        off = Y @ np.asarray(Wl[h], dtype=np.float64) + np.asarray(bl[h], dtype=np.float64)
+        out[:, :, h] = off.reshape(B, len(toks), S3 // 3, 3)
     return out
 
 
@@ -92,6 +97,8 @@ def trilinear(X, pos, T, H, W):
     rows.  Returns [..., d].
     """
     pos = np.asarray(pos, dtype=np.float64)
+    # a position with a non-finite coordinate lies outside the raster (reading D3)
+    pos = np.where(np.isfinite(pos).all(axis=-1, keepdims=True), pos, -2.0)
     base = np.floor(pos)
     frac = pos - base
     out = np.zeros(pos.shape[:-1] + (X.shape[1],))
@@ -110,10 +117,11 @@ def trilinear(X, pos, T, H, W):
     return out
 
 
-def dsa3d_fwd(Q, K, V, offsets, T, H, W, kt, kh, kw, scale=None, tokens=None):
+def dsa3d_fwd(Q, K, V, offsets, T, H, W, kt, kh, kw, scale=None, tokens=None, offsets_of_tokens=False):
     """3D deformable sliding attention forward (readings D1, D3, D4).
 
-    Q, K, V: [B, N, Hh, d]; offsets: [B, N, Hh, S, 3].  Returns (O [B, Nq, Hh, d],
+    Q, K, V: [B, N, Hh, d]; offsets: [B, N, Hh, S, 3] (or [B, Nq, Hh, S, 3], the
+    selected tokens' rows only, with offsets_of_tokens).  Returns (O [B, Nq, Hh, d],
     LSE [B, Hh, Nq]) fp64, Nq = N, or the number of `tokens` when only those
     query tokens (raster indices) are wanted.
     """
@@ -133,7 +141,8 @@ def dsa3d_fwd(Q, K, V, offsets, T, H, W, kt, kh, kw, scale=None, tokens=None):
         for h in range(Hh):
             for c0 in range(0, len(toks), chunk):
                 sl = slice(c0, c0 + chunk)
-                pos = p[sl, None, :] + g[None, :, :] + offsets[b, toks[sl], h]  # [n, S, 3]
+                orow = offsets[b, sl, h] if offsets_of_tokens else offsets[b, toks[sl], h]
+                pos = p[sl, None, :] + g[None, :, :] + orow  # [n, S, 3]
                 ks = trilinear(K[b, :, h, :], pos, T, H, W)
                 vs = trilinear(V[b, :, h, :], pos, T, H, W)
                 logit = scale * np.einsum("nd,nsd->ns", Q[b, toks[sl], h, :], ks)

@@ -201,3 +201,28 @@ def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sda, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         sda.lib()
+
+
+def test_dsa3d_host_validation(L):
+    """Argument checks of the 3D-DSA calls happen before any launch (no GPU needed)."""
+    import ctypes
+
+    from dynamic_block_sparse_rank_gb300 import sda
+
+    fake = 1 << 20  # 16-byte aligned, never dereferenced: every call below fails validation first
+    f = lambda p: sda.lib().sda_dsa3d_fwd(ctypes.byref(p), fake, fake, fake, fake, fake, fake, None)
+    g = lambda p: sda.lib().sda_dsa3d_offsets(ctypes.byref(p), fake, fake, fake, fake, fake, fake, None)
+    good = dict(B=1, T=4, H=5, W=6, heads=2, d=64, kt=3, kh=3, kw=3)
+    bad = [(dict(kt=2), sda.SDA_ERR_INVALID_ARG), (dict(T=0), sda.SDA_ERR_INVALID_ARG),
+           (dict(heads=0), sda.SDA_ERR_INVALID_ARG), (dict(d=96), sda.SDA_ERR_UNSUPPORTED),
+           (dict(kt=7, kh=7, kw=3), sda.SDA_ERR_UNSUPPORTED), (dict(kw=-1), sda.SDA_ERR_INVALID_ARG)]
+    for change, want in bad:
+        p = sda.dsa3d_problem(**{**good, **change})
+        assert f(p) == want and g(p) == want, change
+    p = sda.dsa3d_problem(**good)
+    assert sda.lib().sda_dsa3d_fwd(ctypes.byref(p), fake, None, fake, fake, fake, fake, None) == sda.SDA_ERR_INVALID_ARG
+    assert sda.lib().sda_dsa3d_fwd(ctypes.byref(p), fake + 8, fake, fake, fake, fake, fake, None) == \
+        sda.SDA_ERR_INVALID_ARG  # misaligned Q
+    assert sda.lib().sda_dsa3d_offsets(ctypes.byref(p), fake, fake, None, fake, fake, fake, None) == \
+        sda.SDA_ERR_INVALID_ARG
+    assert sda.lib().sda_dsa3d_fwd(None, fake, fake, fake, fake, fake, fake, None) == sda.SDA_ERR_INVALID_ARG

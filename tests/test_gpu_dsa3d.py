@@ -1,0 +1,128 @@
+"""GPU parity of 3D deformable sliding attention against the fp64 oracle (through the C ABI).
+
+"MegaSlide-DiT" (gist.science explainer), section 2 "3D deformable sliding attention": offsets from a
+depthwise 3x3x3 convolution and a linear layer, trilinear sampling of K and V around every token, softmax
+over the window.  Tolerances: O is stored in bf16, so the bf16 bound (max-abs 2e-2, rel-Frobenius 1e-2);
+LSE and the offsets are fp32 results of exact bf16 inputs, held to 1e-4 of their scale (fp32 accumulation
+over at most 27 + d terms).
+"""
+import math
+
+import numpy as np
+import pytest
+
+from dynamic_block_sparse_rank_gb300 import inputs
+from oracle import dsa3d_oracle as D
+from tests.parity_util import assert_close, dev, errors, host
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dynamic_block_sparse_rank_gb300 import sda as s
+
+    s.lib()
+    return s
+
+WLS = inputs.DSA3D_WORKLOADS
+SMALL = [WLS["dsa3d_ragged_d64"], WLS["dsa3d_d128_1x5x5"], WLS["dsa3d_far"]]
+
+
+def _problem(sda, wl, scale=0.0):
+    return sda.dsa3d_problem(wl.B, wl.T, wl.H, wl.W, wl.heads, wl.d, wl.kt, wl.kh, wl.kw, scale)
+
+
+def _gpu_fwd(sda, wl, x, offsets, scale=0.0):
+    O = torch.full((wl.B, wl.N, wl.heads, wl.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L = torch.full((wl.B, wl.heads, wl.N), float("nan"), dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_fwd(_problem(sda, wl, scale), dev(x["Q"], "bf16"), dev(x["K"], "bf16"), dev(x["V"], "bf16"),
+                      torch.from_numpy(np.ascontiguousarray(offsets, dtype=np.float32)).cuda(), O, L)
+    torch.cuda.synchronize()
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    return host(O), host(L)
+
+
+def _gpu_offsets(sda, wl, x):
+    off = torch.full((wl.B, wl.N, wl.heads, wl.S, 3), float("nan"), dtype=torch.float32, device="cuda")
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    sda.sda_dsa3d_offsets(_problem(sda, wl), dev(x["Q"], "bf16"), f(x["Wc"]), f(x["bc"]), f(x["Wl"]), f(x["bl"]),
+                          off)
+    torch.cuda.synchronize()
+    return host(off)
+
+
+def check_fp32(got, ref, what, rel=1e-4):
+    mx, rf = errors(got, ref)
+    scale = max(1.0, float(np.abs(ref).max()))
+    assert mx <= rel * scale and rf <= rel, f"{what}: max-abs {mx:.3e} (scale {scale:.3e}), rel-frob {rf:.3e}"
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_dsa3d_forward_matches_oracle(sda, wl):
+    x = inputs.generate_dsa3d(wl)
+    O, L = _gpu_fwd(sda, wl, x, x["offsets"])
+    Or, Lr = D.dsa3d_fwd(x["Q"], x["K"], x["V"], x["offsets"], wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    assert_close(O, Or, "bf16", "O")
+    check_fp32(L, Lr, "LSE")
+
+
+@pytest.mark.parametrize("wl", SMALL[:2], ids=lambda w: w.name)
+def test_dsa3d_offsets_match_oracle(sda, wl):
+    x = inputs.generate_dsa3d(wl, names=("Q", "Wc", "bc", "Wl", "bl"))
+    got = _gpu_offsets(sda, wl, x)
+    ref = D.dsa3d_offsets(x["Q"], x["Wc"], x["bc"], x["Wl"], x["bl"], wl.T, wl.H, wl.W)
+    check_fp32(got, ref, "offsets")
+
+
+def test_dsa3d_predicted_offsets_then_attention(sda):
+    """The whole path: the GPU's offsets feed the GPU's attention; the oracle's own offsets feed its own."""
+    wl = WLS["dsa3d_ragged_d64"]
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V", "Wc", "bc", "Wl", "bl"))
+    off = _gpu_offsets(sda, wl, x)
+    O, L = _gpu_fwd(sda, wl, x, off)
+    ref_off = D.dsa3d_offsets(x["Q"], x["Wc"], x["bc"], x["Wl"], x["bl"], wl.T, wl.H, wl.W)
+    Or, Lr = D.dsa3d_fwd(x["Q"], x["K"], x["V"], ref_off, wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    assert_close(O, Or, "bf16", "O")
+    check_fp32(L, Lr, "LSE")
+
+
+def test_dsa3d_samples_outside_or_not_finite(sda):
+    """Samples wholly outside the raster, and non-finite offsets, give k = v = 0 and logit 0 on both sides;
+    with every sample out, O = 0 and LSE = log S exactly."""
+    wl = WLS["dsa3d_ragged_d64"]
+    x = inputs.generate_dsa3d(wl)
+    off = x["offsets"].copy()
+    rng = np.random.default_rng(3)
+    pick = rng.random(off.shape[:4]) < 0.2
+    off[pick, 0] = np.where(rng.random(pick.sum()) < 0.5, np.nan, np.inf)
+    O, L = _gpu_fwd(sda, wl, x, off)
+    Or, Lr = D.dsa3d_fwd(x["Q"], x["K"], x["V"], off, wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    assert_close(O, Or, "bf16", "O (non-finite offsets)")
+    check_fp32(L, Lr, "LSE (non-finite offsets)")
+    O2, L2 = _gpu_fwd(sda, wl, x, np.full_like(off, 1.0e6))
+    assert np.all(O2 == 0.0)
+    np.testing.assert_allclose(L2, math.log(wl.S), rtol=0, atol=2e-6)
+
+
+def test_dsa3d_one_point_window_returns_v(sda):
+    wl = WLS["dsa3d_d128_1x5x5"].with_(kt=1, kh=1, kw=1)
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V"))
+    O, L = _gpu_fwd(sda, wl, x, np.zeros((wl.B, wl.N, wl.heads, 1, 3), np.float32), scale=0.25)
+    np.testing.assert_array_equal(O, x["V"])  # softmax over one sample, stored exactly
+    ref = 0.25 * np.einsum("bnhd,bnhd->bhn", x["Q"].astype(np.float64), x["K"].astype(np.float64))
+    check_fp32(L, ref, "LSE")
+
+
+def test_dsa3d_integer_offsets_gather_rows(sda):
+    wl = WLS["dsa3d_far"]
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V", "offsets"))
+    off = np.rint(x["offsets"])
+    O, L = _gpu_fwd(sda, wl, x, off)
+    Or, Lr = D.dsa3d_fwd(x["Q"], x["K"], x["V"], off, wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    assert_close(O, Or, "bf16", "O (integer offsets)")
+    check_fp32(L, Lr, "LSE (integer offsets)")

@@ -373,3 +373,48 @@ def test_fwd_8k_predictor_training_signal_full_oracle(sda, parity_report):
     rec.e["outputs"]["loss (relative error)"] = abs(L - L_ref) / abs(L_ref)
     rec.e["outputs"]["t (max error / max |t|)"] = terr
     assert sda.sda_get_device_status() == sda.SDA_OK
+
+
+def test_dsa3d_524k_sampled_tokens_every_head(sda, parity_report):
+    """3D deformable sliding attention on the 524,288-token grid, 8 heads, d = 128, 3 x 3 x 3 window: the GPU
+    runs the whole path (predicted offsets, then the attention) on every token; the oracle recomputes the
+    offsets and the attention of 1,024 seeded tokens per head plus the grid's 8 corners ("MegaSlide-DiT",
+    section 2 "3D-DSA")."""
+    from oracle import dsa3d_oracle as D
+
+    wl = inputs.DSA3D_WORKLOADS["dsa3d_524k"]
+    rng = np.random.default_rng(11)
+    corners = [((t * wl.H + h) * wl.W + w) for t in (0, wl.T - 1) for h in (0, wl.H - 1) for w in (0, wl.W - 1)]
+    toks = np.unique(np.concatenate([rng.choice(wl.N, 1024, replace=False), corners]))
+    rec = _Record(parity_report, wl.name, f"all 8 heads x {len(toks)} of {wl.N} tokens (fraction "
+                                          f"{len(toks) / wl.N:.4f}), whole path: offsets then attention")
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V", "Wc", "bc", "Wl", "bl"))
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    p = sda.dsa3d_problem(wl.B, wl.T, wl.H, wl.W, wl.heads, wl.d, wl.kt, wl.kh, wl.kw)
+    Q, K, V = (dev(x[n], "bf16") for n in ("Q", "K", "V"))
+    off = torch.empty((wl.B, wl.N, wl.heads, wl.S, 3), dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_offsets(p, Q, f(x["Wc"]), f(x["bc"]), f(x["Wl"]), f(x["bl"]), off)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_fwd(p, Q, K, V, off, O, LSE)
+    torch.cuda.synchronize()
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    tt = torch.from_numpy(toks).cuda()
+    off_s = host(off[:, tt])
+    O_s, L_s = host(O[:, tt]), host(LSE[:, :, tt])
+    del off, O, LSE, Q, K, V
+    ref_off = rec.oracle(D.dsa3d_offsets, x["Q"], x["Wc"], x["bc"], x["Wl"], x["bl"], wl.T, wl.H, wl.W, tokens=toks)
+    mx, rel = errors(off_s, ref_off)
+    scale = float(np.abs(ref_off).max())
+    assert mx <= 1e-4 * scale and rel <= 1e-4, (mx, scale, rel)
+    # the attention of the sampled tokens from the oracle's own offsets
+    Or, Lr = rec.oracle(D.dsa3d_fwd, x["Q"], x["K"], x["V"], ref_off, wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw,
+                        tokens=toks, offsets_of_tokens=True)
+    rec.close(O_s, Or, "bf16", "O", "O")
+    mx, rel = errors(L_s, Lr)
+    assert mx <= 1e-4 * max(1.0, float(np.abs(Lr).max())) and rel <= 1e-4, (mx, rel)
+    o = rec.e["outputs"].setdefault("offsets", {"max_abs": 0.0, "rel_frob_max": 0.0, "values": 0})
+    o.update(max_abs=max(o["max_abs"], float(errors(off_s, ref_off)[0])), values=o["values"] + int(ref_off.size))
+    o["rel_frob_max"] = max(o["rel_frob_max"], float(errors(off_s, ref_off)[1]))
+    lo = rec.e["outputs"].setdefault("LSE", {"max_abs": 0.0, "rel_frob_max": 0.0, "values": 0})
+    lo.update(max_abs=max(lo["max_abs"], mx), rel_frob_max=max(lo["rel_frob_max"], rel), values=lo["values"] + Lr.size)

@@ -95,8 +95,8 @@ def test_trilinear_reproduces_affine_rows_and_grid_points():
     pos = rng.uniform([0, 0, 0], [T - 1, H - 1, W - 1], size=(50, 3))  # inside the raster: no zero padding
     np.testing.assert_allclose(D.trilinear(X, pos, T, H, W), pos @ A + b0, rtol=0, atol=1e-12)
     np.testing.assert_array_equal(D.trilinear(X, c, T, H, W), X)  # grid points: the rows themselves
-    far = np.array([[-2.0, 0, 0], [0, H + 0.5, 0], [0, 0, -1.0]])
-    assert np.all(D.trilinear(X, far, T, H, W) == 0.0)  # wholly outside: zero rows
+    far = np.array([[-2.0, 0, 0], [0, H + 0.5, 0], [0, 0, -1.0], [np.nan, 1, 1], [1, np.inf, 1], [1, 1, -np.inf]])
+    assert np.all(D.trilinear(X, far, T, H, W) == 0.0)  # wholly outside or not finite: zero rows
 
 
 def test_trilinear_matches_scipy_linear_interpolation_with_zero_padding():
@@ -150,6 +150,9 @@ def test_query_subset_matches_the_full_forward():
     Os, Ls = D.dsa3d_fwd(Q, K, V, off, T, H, W, 3, 3, 3, tokens=toks)
     np.testing.assert_array_equal(Os, O[:, toks])
     np.testing.assert_array_equal(Ls, L[:, :, toks])
+    Ot, Lt = D.dsa3d_fwd(Q, K, V, off[:, toks], T, H, W, 3, 3, 3, tokens=toks, offsets_of_tokens=True)
+    np.testing.assert_array_equal(Ot, Os)
+    np.testing.assert_array_equal(Lt, Ls)
 
 
 def test_offsets_network_matches_scipy_correlation_and_a_matmul():
@@ -176,3 +179,16 @@ def test_offsets_network_matches_scipy_correlation_and_a_matmul():
     got2 = D.dsa3d_offsets(Q, Wc2, np.zeros((Hh, d)), Wl2, np.zeros((Hh, 3 * S)), T, H, W)
     np.testing.assert_array_equal(got2[0, :, :, 0, 0], Q[0, :, :, 0])
     assert np.all(got2[0, :, :, 1:] == 0.0) and np.all(got2[0, :, :, 0, 1:] == 0.0)
+
+
+def test_offsets_of_a_token_subset_match_all_tokens():
+    rng = np.random.default_rng(9)
+    T, H, W, Hh, d, S = 2, 3, 4, 2, 3, 9
+    N = T * H * W
+    Q = rng.standard_normal((2, N, Hh, d))
+    Wc, bc = rng.standard_normal((Hh, d, 3, 3, 3)), rng.standard_normal((Hh, d))
+    Wl, bl = rng.standard_normal((Hh, d, 3 * S)), rng.standard_normal((Hh, 3 * S))
+    full = D.dsa3d_offsets(Q, Wc, bc, Wl, bl, T, H, W)
+    toks = [23, 0, 7, 12]
+    np.testing.assert_allclose(D.dsa3d_offsets(Q, Wc, bc, Wl, bl, T, H, W, tokens=toks), full[:, toks],
+                               rtol=0, atol=1e-12)
