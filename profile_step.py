@@ -2,10 +2,14 @@
 
     python profile_step.py --workload fwd_61k [--heads 10] [--backward] [--steps 1]
     python profile_step.py --workload merge_131k --merge [--heads 4]
+    python profile_step.py --workload dsa3d_524k --dsa3d [--heads 1]
 
 With --merge it runs the state merge and its gradient instead: the workload's
 partition count of random (O, LSE) states of its shapes, then sda_merge_states
-and sda_merge_states_bwd once per step.
+and sda_merge_states_bwd once per step.  With --dsa3d it runs 3D deformable
+sliding attention on a workload of DSA3D_WORKLOADS: sda_dsa3d_offsets from the
+seeded offset-network weights, then sda_dsa3d_fwd on those offsets (Q, K, V
+drawn N(0,1) on the device).
 
 A small driver for inspecting the kernels (e.g. under a profiler) on a chosen
 workload: inputs come from the seeded generator, every step runs all the
@@ -33,12 +37,15 @@ def main():
     ap.add_argument("--steps", type=int, default=1)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--merge", action="store_true", help="run the state merge and its gradient instead")
+    ap.add_argument("--dsa3d", action="store_true", help="run 3D deformable sliding attention instead")
     args = ap.parse_args()
 
     import torch
 
     from dynamic_block_sparse_rank_gb300 import inputs, sda
 
+    if args.dsa3d:
+        return dsa3d_steps(args)
     wl = inputs.WORKLOADS[args.workload]
     if args.heads:
         wl = wl.with_(heads=args.heads)
@@ -124,6 +131,44 @@ def merge_steps(wl, args):
     print(json.dumps({"workload": wl.name, "heads": wl.heads, "tokens": wl.N, "states": n,
                       "ms": {k: statistics.median(v) for k, v in times.items()},
                       "bytes": {"merge": (n + 1) * rows * (2 * wl.d + 4), "merge_bwd": (2 * n + 1) * rows * (2 * wl.d + 4)},
+                      "status": sda.status_string(status)}))
+    if status != sda.SDA_OK:
+        raise SystemExit(1)
+
+
+def dsa3d_steps(args):
+    import torch
+
+    from dynamic_block_sparse_rank_gb300 import inputs, sda
+
+    wl = inputs.DSA3D_WORKLOADS[args.workload]
+    if args.heads:
+        wl = wl.with_(heads=args.heads)
+    x = inputs.generate_dsa3d(wl, names=("Wc", "bc", "Wl", "bl"))
+    w = {n: torch.from_numpy(a).cuda() for n, a in x.items()}
+    g = torch.Generator(device="cuda").manual_seed(0)
+    shape = (wl.B, wl.N, wl.heads, wl.d)
+    Q, K, V = (torch.randn(shape, device="cuda", generator=g).to(torch.bfloat16) for _ in range(3))
+    off = torch.empty((wl.B, wl.N, wl.heads, wl.S, 3), dtype=torch.float32, device="cuda")
+    O = torch.empty_like(Q)
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    p = sda.dsa3d_problem(wl.B, wl.T, wl.H, wl.W, wl.heads, wl.d, wl.kt, wl.kh, wl.kw)
+    st = torch.cuda.current_stream()
+    times = {"offsets": [], "attention": []}
+    for s in range(args.warmup + args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(st)
+        sda.sda_dsa3d_offsets(p, Q, w["Wc"], w["bc"], w["Wl"], w["bl"], off, st)
+        ev[1].record(st)
+        sda.sda_dsa3d_fwd(p, Q, K, V, off, O, LSE, st)
+        ev[2].record(st)
+        torch.cuda.synchronize()
+        if s >= args.warmup:
+            times["offsets"].append(ev[0].elapsed_time(ev[1]))
+            times["attention"].append(ev[1].elapsed_time(ev[2]))
+    status = sda.sda_get_device_status()
+    print(json.dumps({"workload": wl.name, "heads": wl.heads, "tokens": wl.N, "window": [wl.kt, wl.kh, wl.kw],
+                      "ms": {k: statistics.median(v) for k, v in times.items()},
                       "status": sda.status_string(status)}))
     if status != sda.SDA_OK:
         raise SystemExit(1)

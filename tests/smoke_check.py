@@ -3,8 +3,9 @@
 A 2-head bf16 problem on a ragged 3 x 10 x 12 grid (2x8x8 tiles, 8 blocks,
 d = 64, r = 16, 4 of 8 key blocks kept): predictor + top-k, forward, backward,
 two key-partition states and their merge, the gradient through that merge
-(merge backward, then each partition state's backward, summed), and the
-predictor's training signal (distillation gradient of Wq, Wk).
+(merge backward, then each partition state's backward, summed), the
+predictor's training signal (distillation gradient of Wq, Wk), and 3D deformable
+sliding attention (predicted offsets, then the sampled-window attention).
 """
 from __future__ import annotations
 
@@ -94,6 +95,24 @@ def run(device: int = 0) -> dict:
         err = np.linalg.norm(host(got) - ref) / np.linalg.norm(ref)
         assert err < 1e-2, (name, err)
     assert abs(float(loss.item()) - loss_ref) <= 1e-4 * abs(loss_ref)
+    # 7. 3D deformable sliding attention: predicted offsets, then the sampled-window attention
+    from oracle import dsa3d_oracle as D
+
+    dw = inputs.Dsa3dWorkload("smoke_dsa3d", 1, 2, 3, 8, 10, 64, 3, 3, 3, 1.0)
+    xd = inputs.generate_dsa3d(dw, names=("Q", "K", "V", "Wc", "bc", "Wl", "bl"))
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    dp = sda.dsa3d_problem(dw.B, dw.T, dw.H, dw.W, dw.heads, dw.d, dw.kt, dw.kh, dw.kw)
+    dQ, dK, dV = (dev(xd[n], "bf16") for n in ("Q", "K", "V"))
+    doff = torch.empty((dw.B, dw.N, dw.heads, dw.S, 3), dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_offsets(dp, dQ, f32(xd["Wc"]), f32(xd["bc"]), f32(xd["Wl"]), f32(xd["bl"]), doff)
+    dO_ = torch.empty_like(dQ)
+    dL = torch.empty((dw.B, dw.heads, dw.N), dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_fwd(dp, dQ, dK, dV, doff, dO_, dL)
+    roff = D.dsa3d_offsets(xd["Q"], xd["Wc"], xd["bc"], xd["Wl"], xd["bl"], dw.T, dw.H, dw.W)
+    assert np.abs(host(doff) - roff).max() <= 1e-4 * max(1.0, np.abs(roff).max())
+    rO, rL = D.dsa3d_fwd(xd["Q"], xd["K"], xd["V"], roff, dw.T, dw.H, dw.W, dw.kt, dw.kh, dw.kw)
+    assert_close(host(dO_), rO, "bf16", "smoke 3D-DSA O")
+    assert np.abs(host(dL) - rL).max() <= 1e-4 * max(1.0, np.abs(rL).max())
     st = sda.sda_get_device_status()
     assert st == sda.SDA_OK, sda.status_string(st)
     return {"selection": sel, "score_rel_err": float(s_err)}
