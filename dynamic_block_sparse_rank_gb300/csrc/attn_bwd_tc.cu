@@ -782,13 +782,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         uint32_t pds[16];
         const uint32_t vm = full ? 0xffffffffu : block_rows_mask32(a.g, J, col0);
+        // column pairs through the packed fp32x2 forms: the same roundings as the scalar ones
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nl2 = make_float2(-l2, -l2);
+        const float2 nD2 = make_float2(-Dx, -Dx);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), a.scale_log2, -l2));
-          float p1 = ex2(fmaf(__uint_as_float(us[2 * e + 1]), a.scale_log2, -l2));
+          const float2 x2 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl2);
+          float p0 = ex2(x2.x), p1 = ex2(x2.y);
           if (!((vm >> (2 * e)) & 1u)) p0 = 0.f;
           if (!((vm >> (2 * e + 1)) & 1u)) p1 = 0.f;
-          pds[e] = pack_f16(p0 * (__uint_as_float(up[2 * e]) - Dx), p1 * (__uint_as_float(up[2 * e + 1]) - Dx));
+          const float2 d2 = fadd2(make_float2(__uint_as_float(up[2 * e]), __uint_as_float(up[2 * e + 1])), nD2);
+          const float2 r2 = fmul2(make_float2(p0, p1), d2);
+          pds[e] = pack_f16(r2.x, r2.y);
         }
         tmem_st16(tS + lane_base + grp * 64 + cc * 16, pds);
       }
@@ -1008,14 +1013,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tdP + lane_base + col0, up);
         tmem_wait_ld();
         uint32_t pp[16], pd[16];
+        // column pairs through the packed fp32x2 forms: the same roundings as the scalar ones
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c = col0 + 2 * e;
-          float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), a.scale_log2, -l2[c]));
-          float p1 = ex2(fmaf(__uint_as_float(us[2 * e + 1]), a.scale_log2, -l2[c + 1]));
+          const float2 x2 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2,
+                                  make_float2(-l2[c], -l2[c + 1]));
+          float p0 = ex2(x2.x), p1 = ex2(x2.y);
           if (!row_ok) p0 = p1 = 0.f;
           pp[e] = pack_f16(p0, p1);
-          pd[e] = pack_f16(p0 * (__uint_as_float(up[2 * e]) - dv[c]), p1 * (__uint_as_float(up[2 * e + 1]) - dv[c + 1]));
+          const float2 d2 = fadd2(make_float2(__uint_as_float(up[2 * e]), __uint_as_float(up[2 * e + 1])),
+                                  make_float2(-dv[c], -dv[c + 1]));
+          const float2 r2 = fmul2(make_float2(p0, p1), d2);
+          pd[e] = pack_f16(r2.x, r2.y);
         }
         tmem_st16(tS + lane_base + grp * 64 + cc * 16, pp);
         tmem_st16(tdP + lane_base + grp * 64 + cc * 16, pd);

@@ -96,7 +96,9 @@ __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
 template <bool kMask, bool kF16>
 __device__ __forceinline__ void softmax_p(const uint32_t (&u0)[32], const uint32_t (&u1)[32], uint32_t vm0,
                                           uint32_t vm1, float m, float scale_log2, uint32_t tS, float& l) {
-  float sa = 0.f, sb = 0.f;
+  // pairs of columns through the packed fp32x2 FMA: the same roundings as two scalar FMAs
+  float2 sab = make_float2(0.f, 0.f);
+  const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m, -m);
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     const uint32_t(&u)[32] = cc ? u1 : u0;
@@ -104,15 +106,14 @@ __device__ __forceinline__ void softmax_p(const uint32_t (&u0)[32], const uint32
     uint32_t ph[16], pl[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      float s0 = fmaf(__uint_as_float(u[2 * e]), scale_log2, -m);
-      float s1 = fmaf(__uint_as_float(u[2 * e + 1]), scale_log2, -m);
+      const float2 s2 = ffma2(make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1])), sc2, nm2);
+      float s0 = s2.x, s1 = s2.y;
       if (kMask) {
         if (!((vm >> (2 * e)) & 1u)) s0 = -INFINITY;
         if (!((vm >> (2 * e + 1)) & 1u)) s1 = -INFINITY;
       }
       const float p0 = ex2(s0), p1 = ex2(s1);
-      sa += p0;
-      sb += p1;
+      sab = fadd2(sab, make_float2(p0, p1));
       if (kF16) {
         ph[e] = pack_f16(p0, p1);
       } else {
@@ -123,7 +124,7 @@ __device__ __forceinline__ void softmax_p(const uint32_t (&u0)[32], const uint32
     tmem_st16(tS + cc * 32, ph);
     if (!kF16) tmem_st16(tS + cc * 32 + 16, pl);
   }
-  l += sa + sb;
+  l += sab.x + sab.y;
 }
 
 // kF16: operands and P in fp16 (training), otherwise bf16.  kO16: O is written in bf16

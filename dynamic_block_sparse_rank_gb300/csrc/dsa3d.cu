@@ -49,23 +49,6 @@ __device__ __forceinline__ void raster_coords(int n, int H, int W, int& t, int& 
   t = r / H;
 }
 
-// d = fma(a, b, c) on two fp32 lanes at once (the packed FP32 FMA of sm_100 and later).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t d, ua, ub, uc;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(ua), "l"(ub), "l"(uc));
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
-  return r;
-}
-
-// The two bf16 of a 32-bit word as fp32 (low half first).
-__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
-  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-}
-
 constexpr int kOffTok = 64;     // tokens per CTA of the offset network
 constexpr int kOffJ = 96;       // outputs per pass: 16 groups of 6
 constexpr int kOffYStride = kOffTok + 4;  // floats per channel row of Y (float4-aligned)
