@@ -21,12 +21,13 @@
 //               tile box *is* the space-time tile, so no token reordering pass
 //               exists).
 //   warp 1      TMEM owner and MMA issuer (converged warp, one elected lane):
-//               S_j = Q K_j^T into one of three TMEM S buffers, up to three
-//               blocks ahead of the softmax; once P_j is ready, O += P_j V_j
-//               with P_j read from TMEM (in bf16 twice, P_hi then P_lo), then
-//               S_{j+3} into the buffer P_j leaves.
-//   warps 4-11  softmax: two warps per query row quarter (thread = row = TMEM
-//               lane), each owning 64 of the 128 key columns; the pair swaps
+//               S_j = Q K_j^T (Q from TMEM) into one of two TMEM S buffers, up
+//               to two blocks ahead of the softmax; once P_j is ready, O += P_j
+//               V_j with P_j read from TMEM (in bf16 twice, P_hi then P_lo),
+//               then S_{j+2} into the buffer P_j leaves.
+//   warps 4-11  copy Q from its tile into TMEM once, then softmax: two warps
+//               per query row quarter (thread = row = TMEM lane), each owning
+//               64 of the 128 key columns; the pair swaps
 //               its half-row maxima at a named barrier.  Online softmax in
 //               base 2 with a lazy rescale: O and the sums are rescaled only
 //               when the row max grows by more than 2^15 (fp16 P) or 2^30
@@ -38,7 +39,9 @@
 //   warp 3      arrives on P_j's barrier once V_j has landed, so that barrier
 //               covers every input of P_j V_j and the MMA warp waits once per
 //               block for it.
-// TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,384) S2/P2, [384,384+D) O.
+// TMEM columns: [0,128) S0/P0, [128,256) S1/P1, [256,256+D) O, [384,384+D/2) Q (packed
+// 16-bit pairs: the S products take Q from TMEM and only K from shared memory, which
+// keeps their operand traffic, with the K and V tile loads, under shared memory's rate).
 #include "internal.h"
 
 namespace sda {
@@ -58,7 +61,8 @@ struct FwdArgs {
 };
 
 constexpr int kThreads = 384;  // warps 0, 2 TMA, warp 1 MMA, warp 3 V arrivals, warps 4-11 softmax
-constexpr int kSBufs = 3;      // S / P buffers in TMEM: S runs up to three blocks ahead of P V
+constexpr int kSBufs = 2;      // S / P buffers in TMEM: S runs up to two blocks ahead of P V
+constexpr int kTQ = 384;       // TMEM column of Q (the S products' A operand, d / 2 packed columns)
 // P_j barrier: the 256 softmax threads and warp 3 (V_j landed).
 constexpr int kPfullCount = 256 + 1;
 // Lazy rescale: O_hf and its sum are rescaled only when the half-row max grows by more
@@ -154,7 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sfull = vempty + VST;  // kSBufs
   uint64_t* pfull = sfull + kSBufs;  // kSBufs
   uint64_t* odone = pfull + kSBufs;  // 2: P V of blocks of each parity done
-  uint64_t* drain = odone + 2;       // 1
+  uint64_t* qtmem = odone + 2;       // 1: Q is in TMEM (the 256 softmax threads)
+  uint64_t* drain = qtmem + 1;       // 1
   uint64_t* pairbar = drain + 1;     // 4: the two softmax warps of a lane quarter meet here at the end
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pairbar + 4);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
@@ -182,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(odone, 1);
     mbar_init(odone + 1, 1);
+    mbar_init(qtmem, 256);
     mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) mbar_init(pairbar + q, 2);
     *abort_flag = 0;
@@ -275,16 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     // Whole warp, one elected lane issues; descriptors advance by adding to the
-    // start-address field (16-byte units).  S runs kSBufs blocks ahead: S_0 .. S_2 as
-    // their K tiles land, then per block j: wait for pfull_j (softmax of block j done,
-    // V_j landed), P_j V_j, then S_{j+3} into the buffer P_j leaves (the tensor pipe runs
-    // its products in order, so P_j is read before S_{j+3} overwrites it) once K_{j+3}
-    // has landed.
+    // start-address field (16-byte units).  S runs kSBufs blocks ahead: S_0 and S_1 as
+    // their K tiles land (and Q is in TMEM), then per block j: wait for pfull_j (softmax of
+    // block j done, V_j landed), P_j V_j, then S_{j+2} into the buffer P_j leaves (the
+    // tensor pipe runs its products in order, so P_j is read before S_{j+2} overwrites it)
+    // once K_{j+2} has landed.
     if (n_sel > 0) {
       const uint32_t leader = elect_leader();
       constexpr uint32_t idS = kF16 ? idesc_f16(128, 128, 0, 0) : idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idO = kF16 ? idesc_f16(128, D, 0, 1) : idesc_bf16(128, D, 0, 1);
-      const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024, 2);
       const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, 2);
       const uint64_t dV = smem_desc(smem_u32(sV), 16384, 1024, 2);
       const uint32_t tO = tmem + kSBufs * 128;
@@ -296,12 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           constexpr int kChunk = 16384 >> 4;
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 2;  // 64-column chunk, 16-column step
-          mma_ss_by(leader, tS, dQ + off, dKs + off, idS, kk > 0);
+          mma_ts_by(leader, tS, tmem + kTQ + kk * 8, dKs + off, idS, kk > 0);
         }
         mma_commit_by(leader, sfull + t % kSBufs);
         mma_commit_by(leader, kempty + s);  // K_t is no longer needed once S_t is done
       };
-      bool ok = warp_wait(qfull, 0, a.status, abort_flag);
+      bool ok = warp_wait(qtmem, 0, a.status, abort_flag);
       for (int t = 0; ok && t < kSBufs && t < n_sel; ++t) {
         if (!(ok = warp_wait(kfull + t % KST, (t / KST) & 1, a.status, abort_flag))) break;
         tc_fence_after();
@@ -354,6 +359,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY;  // row max, log2 units (scaled), the same in both warps of the pair
     float l = 0.f;        // this warp's sum of P (fp32) over its keys
     bool ok = true;
+    // Q into TMEM, the A operand of every S product (so S reads only K from shared
+    // memory): this thread's row, elements [hf d/2, (hf + 1) d/2), 16-byte vectors of the
+    // swizzled tile, 8 values = 4 packed columns each.
+    if (n_sel > 0 && mbar_wait(qfull, 0, a.status, abort_flag)) {
+      constexpr int kV = D / 16;  // vectors of this half row
+      uint32_t u[kV * 4];
+#pragma unroll
+      for (int v = 0; v < kV; ++v) {
+        const int qq = hf * kV + v;  // 16-byte vector of the row
+        const uint4 x = *reinterpret_cast<const uint4*>(sQ + (qq >> 3) * 16384 + sw128_offset(r, qq & 7));
+        u[4 * v] = x.x;
+        u[4 * v + 1] = x.y;
+        u[4 * v + 2] = x.z;
+        u[4 * v + 3] = x.w;
+      }
+      if constexpr (D == 128)
+        tmem_st32(tmem + kTQ + lane_base + hf * 32, u);
+      else
+        tmem_st16(tmem + kTQ + lane_base + hf * 16, u);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(qtmem);
+    }
     for (int j = 0; j < n_sel; ++j) {
       const bool okw = mbar_wait(sfull + j % kSBufs, (j / kSBufs) & 1, a.status, abort_flag);
       const uint32_t tS = tmem + (j % kSBufs) * 128 + lane_base + hf * 64;
@@ -504,7 +532,7 @@ template <int D, bool kF16, bool kO16, bool kO32>
 cudaError_t launch_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* idx, int kb_begin,
                        int kb_end, const uint8_t* qb_active, void* O, float* LSE, float* O32, cudaStream_t st) {
   using C = FwdCfg<D>;
-  const size_t smem = 1024 + C::SMEM_TILES + 8 * (2 * (C::KST + C::VST) + 2 * kSBufs + 8) + 4 * (3 + 16) +
+  const size_t smem = 1024 + C::SMEM_TILES + 8 * (2 * (C::KST + C::VST) + 2 * kSBufs + 9) + 4 * (3 + 16) +
                       4 * 768 + 4 * kSeenWords + 4 * (size_t)p.k + 64;
   auto kern = fwd_tc_kernel<D, kF16, kO16, kO32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
