@@ -49,15 +49,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # 134 MB, larger than L2), scaled to the eight-head launch by the units processed (DRAM bytes grow in
 # proportion to the heads), and the tensor pipe's active fraction as ncu reports it:
 #   python profile_step.py --workload train_524k --heads 1 --steps 1 --warmup 1 &&
-#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed \
-#       --clock-control none -k regex:<kernel> -s <launches before it> -c 1 \
+#   ncu --set full --clock-control none -k regex:<kernel> -s 1 -c 1 -o prof_<kernel> \
 #       python profile_step.py --workload train_524k --heads 1 --steps 1 --warmup 1
+# (dram__bytes_read.sum + dram__bytes_write.sum; sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active)
 # An entry goes back to None whenever its kernel changes, until it is captured again.
 NCU_COUNTERS = {
-    "score_kernel": {"dram_bytes": 8 * (0.0684e9 + 0.0051e9), "tensor_active": 0.527},
-    "fwd_tc_kernel": {"dram_bytes": 8 * (6.807e9 + 0.570e9), "tensor_active": 0.533},
-    "dqx_kernel": {"dram_bytes": 8 * (6.916e9 + 0.263e9), "tensor_active": 0.699},
-    "dkdv_kernel": {"dram_bytes": 8 * (15.158e9 + 0.520e9), "tensor_active": 0.659},
+    "score_kernel": {"dram_bytes": 8 * (0.0683e9 + 0.0052e9), "tensor_active": 0.555},
+    "fwd_tc_kernel": {"dram_bytes": 8 * (7.670e9 + 0.570e9), "tensor_active": 0.635},
+    "dqx_kernel": {"dram_bytes": 8 * (6.908e9 + 0.263e9), "tensor_active": 0.759},
+    "dkdv_kernel": {"dram_bytes": 8 * (15.113e9 + 0.520e9), "tensor_active": 0.681},
 }
 
 GAP_REL = 1e-3  # selection rows whose k-th / (k+1)-th score gap is below this (relative) are near-ties
