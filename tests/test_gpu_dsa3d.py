@@ -126,3 +126,21 @@ def test_dsa3d_integer_offsets_gather_rows(sda):
     Or, Lr = D.dsa3d_fwd(x["Q"], x["K"], x["V"], off, wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
     assert_close(O, Or, "bf16", "O (integer offsets)")
     check_fp32(L, Lr, "LSE (integer offsets)")
+
+
+@pytest.mark.parametrize("wl", [inputs.Dsa3dWorkload("dsa3d_5x5x5_d64", 1, 2, 6, 7, 9, 64, 5, 5, 5, 1.5),
+                                inputs.Dsa3dWorkload("dsa3d_one_token_d128", 2, 3, 1, 1, 1, 128, 3, 3, 3, 0.5),
+                                inputs.Dsa3dWorkload("dsa3d_line_d128", 1, 1, 1, 1, 37, 128, 1, 1, 7, 2.0)],
+                         ids=lambda w: w.name)
+def test_dsa3d_edge_shapes(sda, wl):
+    """The largest window (5 x 5 x 5 = 125 points: 375 offset outputs, four passes of the offset network's
+    output tiles), a single-token grid (every sample but the centre's corners outside), and a 1 x 1 x 37 line
+    with a 1 x 1 x 7 window; both steps against the oracle."""
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V", "offsets", "Wc", "bc", "Wl", "bl"))
+    O, L = _gpu_fwd(sda, wl, x, x["offsets"])
+    Or, Lr = D.dsa3d_fwd(x["Q"], x["K"], x["V"], x["offsets"], wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    assert_close(O, Or, "bf16", "O")
+    check_fp32(L, Lr, "LSE")
+    got = _gpu_offsets(sda, wl, x)
+    ref = D.dsa3d_offsets(x["Q"], x["Wc"], x["bc"], x["Wl"], x["bl"], wl.T, wl.H, wl.W)
+    check_fp32(got, ref, "offsets")
