@@ -152,3 +152,123 @@ def dsa3d_fwd(Q, K, V, offsets, T, H, W, kt, kh, kw, scale=None, tokens=None, of
                 O[b, sl, h, :] = np.einsum("ns,nsd->nd", e / z, vs)
                 L[b, h, sl] = (m + np.log(z))[:, 0]
     return O, L
+
+
+# --------------------------------------------------------------------------- backward
+# D5. The backward differentiates readings D1-D4 as written, with dLSE = 0 (the loss reaches the
+#     attention through O): for every token n and window point s, with k~_s, v~_s the sampled rows,
+#     a_s = scale q.k~_s, P = softmax(a), dP_s = dO.v~_s and da_s = P_s (dP_s - sum_u P_u dP_u):
+#       dq_n = scale sum_s da_s k~_s,
+#       dK[m] += w_c scale da_s q_n and dV[m] += w_c P_s dO_n for every corner c (row m, weight w_c) of
+#       every sample inside the raster,
+#       d offset_s = sum_c (d w_c / d pos) (scale da_s q.K[m_c] + P_s dO.V[m_c]),
+#     where d w_c / d pos along an axis is -1 or +1 (lower or upper neighbour on that axis) times the
+#     other two axes' weights: the derivative of the interpolation at a position off the integer grid
+#     (on the grid, the one-sided derivative from above, as floor() sees it).  The offset network's
+#     backward follows from D2: dY = d offsets Wl^T, dWl = Y^T d offsets, dbl = sum d offsets,
+#     dWc[c, tap] = sum_n dY[n, c] Q[n + tap, c], dbc = sum_n dY, and dQ += the transposed convolution
+#     of dY (zero padding).
+
+
+def _corners(pos, T, H, W):
+    """The 8 trilinear corners of every position: (row index, inside, weight, d weight / d (t, h, w))."""
+    pos = np.where(np.isfinite(pos).all(axis=-1, keepdims=True), pos, -2.0)
+    base = np.floor(pos)
+    f = pos - base
+    out = []
+    for ct in (0, 1):
+        for ch in (0, 1):
+            for cw in (0, 1):
+                t = base[..., 0] + ct
+                h = base[..., 1] + ch
+                w = base[..., 2] + cw
+                wt = np.where(ct, f[..., 0], 1.0 - f[..., 0])
+                wh = np.where(ch, f[..., 1], 1.0 - f[..., 1])
+                ww = np.where(cw, f[..., 2], 1.0 - f[..., 2])
+                st, sh, sw = (1.0 if ct else -1.0), (1.0 if ch else -1.0), (1.0 if cw else -1.0)
+                inside = (t >= 0) & (t < T) & (h >= 0) & (h < H) & (w >= 0) & (w < W)
+                n = np.where(inside, (t * H + h) * W + w, 0).astype(np.int64)
+                m = inside.astype(np.float64)
+                dw = np.stack([st * wh * ww, sh * wt * ww, sw * wt * wh], axis=-1) * m[..., None]
+                out.append((n, inside, wt * wh * ww * m, dw))
+    return out
+
+
+def dsa3d_bwd(Q, K, V, offsets, dO, T, H, W, kt, kh, kw, scale=None):
+    """Gradients of 3D deformable sliding attention (reading D5).
+
+    Q, K, V, dO: [B, N, Hh, d]; offsets: [B, N, Hh, S, 3].  Returns (dQ, dK, dV [B, N, Hh, d],
+    d_offsets [B, N, Hh, S, 3]) fp64; dQ is the attention's part only.
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    dO = np.asarray(dO, dtype=np.float64)
+    offsets = np.asarray(offsets, dtype=np.float64)
+    B, N, Hh, d = Q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    g = window_points(kt, kh, kw)
+    p = token_coords(T, H, W)
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    doff = np.zeros_like(offsets)
+    chunk = 256
+    for b in range(B):
+        for h in range(Hh):
+            Kh, Vh = K[b, :, h, :], V[b, :, h, :]
+            for c0 in range(0, N, chunk):
+                sl = slice(c0, min(N, c0 + chunk))
+                q, do = Q[b, sl, h, :], dO[b, sl, h, :]
+                pos = p[sl, None, :] + g[None, :, :] + offsets[b, sl, h]  # [n, S, 3]
+                cs = _corners(pos, T, H, W)
+                ks = sum(w[..., None] * Kh[n] for n, _, w, _ in cs)  # [n, S, d]
+                vs = sum(w[..., None] * Vh[n] for n, _, w, _ in cs)
+                a = scale * np.einsum("nd,nsd->ns", q, ks)
+                P = np.exp(a - a.max(axis=1, keepdims=True))
+                P /= P.sum(axis=1, keepdims=True)
+                dP = np.einsum("nd,nsd->ns", do, vs)
+                da = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+                dQ[b, sl, h, :] = scale * np.einsum("ns,nsd->nd", da, ks)
+                for n, inside, w, dw in cs:
+                    gk = (w * scale * da)[..., None] * q[:, None, :]  # [n, S, d]
+                    gv = (w * P)[..., None] * do[:, None, :]
+                    np.add.at(dK[b, :, h, :], n[inside], gk[inside])
+                    np.add.at(dV[b, :, h, :], n[inside], gv[inside])
+                    qk = np.einsum("nd,nsd->ns", q, Kh[n])
+                    dv = np.einsum("nd,nsd->ns", do, Vh[n])
+                    doff[b, sl, h] += dw * (scale * da * qk + P * dv)[..., None]
+    return dQ, dK, dV, doff
+
+
+def dsa3d_offsets_bwd(Q, Wc, bc, Wl, bl, d_offsets, T, H, W):
+    """Gradients of the offset network (reading D5): (dQ_net [B, N, Hh, d], dWc, dbc, dWl, dbl) fp64."""
+    Q = np.asarray(Q, dtype=np.float64)
+    B, N, Hh, d = Q.shape
+    S3 = Wl.shape[2]
+    X = Q.reshape(B, T, H, W, Hh, d)
+    Xp = np.zeros((B, T + 2, H + 2, W + 2, Hh, d))
+    Xp[:, 1:-1, 1:-1, 1:-1] = X
+    dQ = np.zeros((B, T + 2, H + 2, W + 2, Hh, d))
+    dWc = np.zeros((Hh, d, 3, 3, 3))
+    dbc = np.zeros((Hh, d))
+    dWl = np.zeros((Hh, d, S3))
+    dbl = np.zeros((Hh, S3))
+    for h in range(Hh):
+        Y = np.broadcast_to(np.asarray(bc[h], dtype=np.float64), (B, T, H, W, d)).copy()
+        for a in range(3):
+            for b_ in range(3):
+                for c in range(3):
+                    Y += Xp[:, a:a + T, b_:b_ + H, c:c + W, h, :] * np.asarray(Wc[h, :, a, b_, c], dtype=np.float64)
+        G = np.asarray(d_offsets[:, :, h], dtype=np.float64).reshape(B, N, S3)
+        Yf = Y.reshape(B, N, d)
+        dWl[h] = np.einsum("bnd,bnj->dj", Yf, G)
+        dbl[h] = G.sum(axis=(0, 1))
+        dY = (G @ np.asarray(Wl[h], dtype=np.float64).T).reshape(B, T, H, W, d)
+        dbc[h] = dY.sum(axis=(0, 1, 2, 3))
+        for a in range(3):
+            for b_ in range(3):
+                for c in range(3):
+                    dWc[h, :, a, b_, c] = (dY * Xp[:, a:a + T, b_:b_ + H, c:c + W, h, :]).sum(axis=(0, 1, 2, 3))
+                    dQ[:, a:a + T, b_:b_ + H, c:c + W, h, :] += dY * np.asarray(Wc[h, :, a, b_, c], dtype=np.float64)
+    return dQ[:, 1:-1, 1:-1, 1:-1].reshape(B, N, Hh, d), dWc, dbc, dWl, dbl

@@ -192,3 +192,87 @@ def test_offsets_of_a_token_subset_match_all_tokens():
     toks = [23, 0, 7, 12]
     np.testing.assert_allclose(D.dsa3d_offsets(Q, Wc, bc, Wl, bl, T, H, W, tokens=toks), full[:, toks],
                                rtol=0, atol=1e-12)
+
+
+def _torch_dsa3d(Q, K, V, off, T, H, W, kt, kh, kw, scale):
+    """The forward written with torch's grid_sample (trilinear, zero padding, corner-aligned grid): an
+    independent statement of readings D1-D4 whose autograd gives the gradients."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    B, N, Hh, d = Q.shape
+    g = torch.as_tensor(D.window_points(kt, kh, kw))
+    p = torch.as_tensor(D.token_coords(T, H, W))
+    O = torch.zeros(B, N, Hh, d, dtype=torch.float64)
+    outs = []
+    for b in range(B):
+        for h in range(Hh):
+            pos = p[:, None, :] + g[None] + off[b, :, h]  # [N, S, 3] as (t, h, w)
+            grid = torch.stack([2 * pos[..., 2] / (W - 1) - 1, 2 * pos[..., 1] / (H - 1) - 1,
+                                2 * pos[..., 0] / (T - 1) - 1], dim=-1)[None, :, :, None, :]
+            vol = lambda X: X[b, :, h, :].reshape(T, H, W, d).permute(3, 0, 1, 2)[None]
+            ks = F.grid_sample(vol(K), grid, mode="bilinear", padding_mode="zeros", align_corners=True)
+            vs = F.grid_sample(vol(V), grid, mode="bilinear", padding_mode="zeros", align_corners=True)
+            ks, vs = ks[0, :, :, :, 0].permute(1, 2, 0), vs[0, :, :, :, 0].permute(1, 2, 0)  # [N, S, d]
+            a = scale * torch.einsum("nd,nsd->ns", Q[b, :, h, :], ks)
+            outs.append(((b, h), torch.einsum("ns,nsd->nd", torch.softmax(a, dim=1), vs)))
+    for (b, h), o in outs:
+        O = O.index_put((torch.tensor(b), torch.arange(N), torch.tensor(h)), o)
+    return O
+
+
+def test_backward_matches_torch_autograd_through_grid_sample():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(10)
+    T, H, W, Hh, d = 3, 4, 5, 2, 6
+    N = T * H * W
+    Q, K, V, dO = (rng.standard_normal((1, N, Hh, d)) for _ in range(4))
+    off = rng.normal(0, 0.8, size=(1, N, Hh, 27, 3))
+    scale = 0.45
+    dQ, dK, dV, doff = D.dsa3d_bwd(Q, K, V, off, dO, T, H, W, 3, 3, 3, scale=scale)
+    tQ, tK, tV, toff = (torch.tensor(x, requires_grad=True) for x in (Q, K, V, off))
+    O = _torch_dsa3d(tQ, tK, tV, toff, T, H, W, 3, 3, 3, scale)
+    Or, _ = D.dsa3d_fwd(Q, K, V, off, T, H, W, 3, 3, 3, scale=scale)
+    np.testing.assert_allclose(O.detach().numpy(), Or, rtol=0, atol=1e-12)  # the same forward
+    (O * torch.tensor(dO)).sum().backward()
+    for name, got, ref in (("dQ", dQ, tQ.grad), ("dK", dK, tK.grad), ("dV", dV, tV.grad), ("doff", doff, toff.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-10, err_msg=name)
+
+
+def test_offset_gradient_matches_finite_differences():
+    rng = np.random.default_rng(11)
+    T, H, W, Hh, d = 2, 3, 4, 1, 4
+    N = T * H * W
+    Q, K, V, dO = (rng.standard_normal((1, N, Hh, d)) for _ in range(4))
+    off = rng.normal(0, 0.6, size=(1, N, Hh, 9, 3))
+    _, _, _, doff = D.dsa3d_bwd(Q, K, V, off, dO, T, H, W, 1, 3, 3)
+    eps = 1e-6
+    for (n, s, ax) in [(0, 0, 0), (5, 4, 1), (11, 8, 2), (23, 3, 2), (17, 6, 0)]:
+        e = np.zeros_like(off)
+        e[0, n, 0, s, ax] = eps
+        Op, _ = D.dsa3d_fwd(Q, K, V, off + e, T, H, W, 1, 3, 3)
+        Om, _ = D.dsa3d_fwd(Q, K, V, off - e, T, H, W, 1, 3, 3)
+        fd = float(((Op - Om) * dO).sum() / (2 * eps))
+        assert abs(fd - doff[0, n, 0, s, ax]) <= 1e-6 * max(1.0, abs(fd)), (n, s, ax, fd, doff[0, n, 0, s, ax])
+
+
+def test_offset_network_backward_matches_torch_autograd():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(12)
+    T, H, W, Hh, d, S = 3, 4, 5, 2, 3, 9
+    N = T * H * W
+    Q = rng.standard_normal((2, N, Hh, d))
+    Wc, bc = rng.standard_normal((Hh, d, 3, 3, 3)), rng.standard_normal((Hh, d))
+    Wl, bl = rng.standard_normal((Hh, d, 3 * S)), rng.standard_normal((Hh, 3 * S))
+    G = rng.standard_normal((2, N, Hh, S, 3))
+    dQ, dWc, dbc, dWl, dbl = D.dsa3d_offsets_bwd(Q, Wc, bc, Wl, bl, G, T, H, W)
+    tQ, tWc, tbc, tWl, tbl = (torch.tensor(x, requires_grad=True) for x in (Q, Wc, bc, Wl, bl))
+    loss = 0
+    for h in range(Hh):
+        X = tQ[:, :, h, :].reshape(2, T, H, W, d).permute(0, 4, 1, 2, 3)  # [B, d, T, H, W]
+        Y = torch.nn.functional.conv3d(X, tWc[h][:, None], tbc[h], padding=1, groups=d)
+        off = Y.permute(0, 2, 3, 4, 1).reshape(2, N, d) @ tWl[h] + tbl[h]
+        loss = loss + (off * torch.tensor(G[:, :, h].reshape(2, N, 3 * S))).sum()
+    loss.backward()
+    for name, got, ref in (("dQ", dQ, tQ.grad), ("dWc", dWc, tWc.grad), ("dbc", dbc, tbc.grad),
+                           ("dWl", dWl, tWl.grad), ("dbl", dbl, tbl.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-9, err_msg=name)
