@@ -419,3 +419,17 @@ sda_status sda_dsa3d_fwd(const sda_dsa3d_problem* p, const void* Q, const void* 
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SDA_ERR_INVALID_ARG;
   return from_cuda(sda::dsa3d_fwd(a, Q, K, V, offsets, O, LSE, static_cast<cudaStream_t>(stream)));
 }
+
+sda_status sda_dsa3d_bwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
+                         const float* offsets, const float* LSE, const void* dO, float* dQ, float* dK, float* dV,
+                         float* d_offsets, void* stream) {
+  sda::Dsa3dArgs a;
+  const sda_status st = dsa3d_args(p, a);
+  if (st != SDA_OK) return st;
+  if (!Q || !K || !V || !offsets || !LSE || !dO || !dQ || !dK || !dV || !d_offsets) return SDA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
+      !aligned16(dV))
+    return SDA_ERR_INVALID_ARG;
+  return from_cuda(sda::dsa3d_bwd(a, Q, K, V, offsets, LSE, dO, dQ, dK, dV, d_offsets,
+                                  static_cast<cudaStream_t>(stream)));
+}

@@ -282,6 +282,194 @@ __global__ void __launch_bounds__(kDsaThreads) dsa3d_fwd_kernel(const __nv_bfloa
   }
 }
 
+// Backward of the window attention (dLSE = 0).  The same warp layout as the forward.  Pass 1
+// recomputes every window point's logit and P_s = exp(a_s - LSE) (the forward's LSE) and
+// dP_s = dO . v~_s, keeping both in shared memory, and sums D = sum_s P_s dP_s; pass 2 gathers
+// the corners again and, with da_s = P_s (dP_s - D), accumulates dq = scale sum_s da_s k~_s,
+// adds w_c scale da_s q to dK and w_c P_s dO to dV at every corner row (fp32 vector atomics:
+// the corner rows of neighbouring tokens overlap), and forms the offset gradient from the
+// weights' derivatives, sum_c dw_c (scale da_s q.K_c + P_s dO.V_c).
+constexpr int kMaxS = 125;
+
+template <int D>
+__global__ void __launch_bounds__(kDsaThreads, 2) dsa3d_bwd_kernel(const __nv_bfloat16* __restrict__ Q,
+                                                               const __nv_bfloat16* __restrict__ K,
+                                                               const __nv_bfloat16* __restrict__ V,
+                                                               const float* __restrict__ off,
+                                                               const float* __restrict__ LSE,
+                                                               const __nv_bfloat16* __restrict__ dO,
+                                                               float* __restrict__ dQ, float* __restrict__ dK,
+                                                               float* __restrict__ dV, float* __restrict__ doff,
+                                                               Dsa3dArgs a) {
+  constexpr int LPT = D / 8;
+  constexpr int TPW = 32 / LPT;
+  constexpr int kWarps = kDsaThreads / 32;
+  constexpr int kPerWarp = kDsaTok / kWarps;
+  constexpr float kLog2e = 1.4426950408889634f;
+  __shared__ float2 pdp[kWarps][TPW][kMaxS];  // (P_s, dP_s) per token slot
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = lane / LPT, sl = lane % LPT;
+  const int N = a.T * a.H * a.W;
+  const long long rs = (long long)a.heads * D;
+  const long long hb = (long long)b * N * rs + (long long)h * D + sl * 8;  // this head's lane offset, batch b
+  const int rt = (a.kt - 1) / 2, rh = (a.kh - 1) / 2, rw = (a.kw - 1) / 2;
+  const float Tm = (float)(a.T - 1), Hm = (float)(a.H - 1), Wm = (float)(a.W - 1);
+  const int HW = a.H * a.W;
+  auto load8 = [&](const __nv_bfloat16* p, float2 (&v)[4]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    v[0] = bf16x2_to_f2(u.x);
+    v[1] = bf16x2_to_f2(u.y);
+    v[2] = bf16x2_to_f2(u.z);
+    v[3] = bf16x2_to_f2(u.w);
+  };
+  auto group_sum = [&](float x) {
+#pragma unroll
+    for (int sh = LPT / 2; sh > 0; sh >>= 1) x += __shfl_xor_sync(0xffffffffu, x, sh);
+    return x;
+  };
+  for (int u = 0; u < kPerWarp; u += TPW) {
+    const int n_raw = blockIdx.x * kDsaTok + warp * kPerWarp + u + slot;
+    const bool valid = n_raw < N;
+    const int n = valid ? n_raw : N - 1;  // lanes of a missing token compute a copy and write nothing
+    int t, y, x;
+    raster_coords(n, a.H, a.W, t, y, x);
+    float2 q[4], g[4];
+    load8(Q + hb + (long long)n * rs, q);
+    load8(dO + hb + (long long)n * rs, g);
+    const float lse2 = LSE[((long long)b * a.heads + h) * N + n] * kLog2e;
+    const float sl2 = a.scale * kLog2e;
+    const float* offn = off + (((long long)b * N + n) * a.heads + h) * (3LL * a.S);
+    // corners of window point s: base index, per-axis weights and inside flags
+    struct Pt {
+      int m000;
+      float f[3];
+      bool v0[3], v1[3];
+    };
+    auto point = [&](int s, int wa, int wb, int wc) {
+      Pt P;
+      const float pc[3] = {(float)(t + wa - rt) + __ldg(offn + 3 * s), (float)(y + wb - rh) + __ldg(offn + 3 * s + 1),
+                           (float)(x + wc - rw) + __ldg(offn + 3 * s + 2)};
+      const float mx[3] = {Tm, Hm, Wm};
+      int ib[3];
+#pragma unroll
+      for (int ax = 0; ax < 3; ++ax) {
+        const float bse = floorf(pc[ax]);
+        P.f[ax] = pc[ax] - bse;
+        P.v0[ax] = bse >= 0.f && bse <= mx[ax];  // tested in float: NaN fails, no index is formed
+        P.v1[ax] = bse >= -1.f && bse <= mx[ax] - 1.f;
+        ib[ax] = (int)fminf(fmaxf(bse, -1.f), mx[ax]);
+      }
+      P.m000 = (ib[0] * a.H + ib[1]) * a.W + ib[2];
+      return P;
+    };
+    // pass 1: P_s, dP_s and D
+    float Dsum = 0.f;
+    {
+      int s = 0;
+      for (int wa = 0; wa < a.kt; ++wa)
+        for (int wb = 0; wb < a.kh; ++wb)
+          for (int wc = 0; wc < a.kw; ++wc, ++s) {
+            const Pt P = point(s, wa, wb, wc);
+            float dq = 0.f, dv = 0.f;
+#pragma unroll
+            for (int corner = 0; corner < 8; ++corner) {
+              const int ct = corner >> 2, ch = (corner >> 1) & 1, cw = corner & 1;
+              const bool in = (ct ? P.v1[0] : P.v0[0]) && (ch ? P.v1[1] : P.v0[1]) && (cw ? P.v1[2] : P.v0[2]);
+              const float w = (ct ? P.f[0] : 1.f - P.f[0]) * (ch ? P.f[1] : 1.f - P.f[1]) * (cw ? P.f[2] : 1.f - P.f[2]);
+              if (!in || w == 0.f) continue;
+              const long long row = (long long)(P.m000 + ct * HW + ch * a.W + cw) * rs;
+              float2 kv[4], vv[4];
+              load8(K + hb + row, kv);
+              load8(V + hb + row, vv);
+              float2 pq = make_float2(0.f, 0.f), pv = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                pq = ffma2(q[i], kv[i], pq);
+                pv = ffma2(g[i], vv[i], pv);
+              }
+              dq = fmaf(w, pq.x + pq.y, dq);
+              dv = fmaf(w, pv.x + pv.y, dv);
+            }
+            dq = group_sum(dq);
+            dv = group_sum(dv);
+            const float Ps = exp2f(fmaf(dq, sl2, -lse2));
+            if (sl == 0) pdp[warp][slot][s] = make_float2(Ps, dv);
+            Dsum = fmaf(Ps, dv, Dsum);
+          }
+    }
+    __syncwarp();
+    // pass 2: gradients
+    float2 dqa[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dqa[i] = make_float2(0.f, 0.f);
+    int s = 0;
+    for (int wa = 0; wa < a.kt; ++wa)
+      for (int wb = 0; wb < a.kh; ++wb)
+        for (int wc = 0; wc < a.kw; ++wc, ++s) {
+          const float2 pd = pdp[warp][slot][s];
+          const float Ps = pd.x, da = Ps * (pd.y - Dsum);
+          const float sda = a.scale * da;
+          const Pt P = point(s, wa, wb, wc);
+          float go[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+          for (int corner = 0; corner < 8; ++corner) {
+            const int ct = corner >> 2, ch = (corner >> 1) & 1, cw = corner & 1;
+            const bool in = (ct ? P.v1[0] : P.v0[0]) && (ch ? P.v1[1] : P.v0[1]) && (cw ? P.v1[2] : P.v0[2]);
+            if (!in) continue;
+            const float wt = ct ? P.f[0] : 1.f - P.f[0], wh = ch ? P.f[1] : 1.f - P.f[1],
+                        ww = cw ? P.f[2] : 1.f - P.f[2];
+            const long long row = (long long)(P.m000 + ct * HW + ch * a.W + cw) * rs;
+            float2 kv[4], vv[4];
+            load8(K + hb + row, kv);
+            load8(V + hb + row, vv);
+            float2 pq = make_float2(0.f, 0.f), pv = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              pq = ffma2(q[i], kv[i], pq);
+              pv = ffma2(g[i], vv[i], pv);
+            }
+            // derivative of this corner's weight along t, h, w times its share of the loss
+            const float c = fmaf(sda, pq.x + pq.y, Ps * (pv.x + pv.y));
+            go[0] = fmaf((ct ? 1.f : -1.f) * wh * ww, c, go[0]);
+            go[1] = fmaf((ch ? 1.f : -1.f) * wt * ww, c, go[1]);
+            go[2] = fmaf((cw ? 1.f : -1.f) * wt * wh, c, go[2]);
+            const float w = wt * wh * ww;
+            if (w == 0.f) continue;
+            const float2 wk = make_float2(w * sda, w * sda), wv = make_float2(w * Ps, w * Ps);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dqa[i] = ffma2(wk, kv[i], dqa[i]);
+            if (valid) {
+              float* dkr = dK + hb + row;
+              float* dvr = dV + hb + row;
+              atomicAdd(reinterpret_cast<float4*>(dkr),
+                        make_float4(wk.x * q[0].x, wk.x * q[0].y, wk.x * q[1].x, wk.x * q[1].y));
+              atomicAdd(reinterpret_cast<float4*>(dkr + 4),
+                        make_float4(wk.x * q[2].x, wk.x * q[2].y, wk.x * q[3].x, wk.x * q[3].y));
+              atomicAdd(reinterpret_cast<float4*>(dvr),
+                        make_float4(wv.x * g[0].x, wv.x * g[0].y, wv.x * g[1].x, wv.x * g[1].y));
+              atomicAdd(reinterpret_cast<float4*>(dvr + 4),
+                        make_float4(wv.x * g[2].x, wv.x * g[2].y, wv.x * g[3].x, wv.x * g[3].y));
+            }
+          }
+#pragma unroll
+          for (int ax = 0; ax < 3; ++ax) go[ax] = group_sum(go[ax]);
+          if (valid && sl == 0) {
+            float* o = doff + (((long long)b * N + n) * a.heads + h) * (3LL * a.S) + 3 * s;
+            o[0] = go[0];
+            o[1] = go[1];
+            o[2] = go[2];
+          }
+        }
+    if (valid) {
+      float* dqr = dQ + hb + (long long)n * rs;
+      reinterpret_cast<float4*>(dqr)[0] = make_float4(dqa[0].x, dqa[0].y, dqa[1].x, dqa[1].y);
+      reinterpret_cast<float4*>(dqr)[1] = make_float4(dqa[2].x, dqa[2].y, dqa[3].x, dqa[3].y);
+    }
+    __syncwarp();
+  }
+}
+
 template <int D>
 cudaError_t launch_dsa3d(const Dsa3dArgs& a, const __nv_bfloat16* Q, const __nv_bfloat16* K, const __nv_bfloat16* V,
                          const float* Wc, const float* bc, const float* Wl, const float* bl, float* off,
@@ -302,7 +490,33 @@ cudaError_t launch_dsa3d(const Dsa3dArgs& a, const __nv_bfloat16* Q, const __nv_
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_dsa3d_bwd(const Dsa3dArgs& a, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                             const __nv_bfloat16* V, const float* off, const float* LSE, const __nv_bfloat16* dO,
+                             float* dQ, float* dK, float* dV, float* doff, cudaStream_t st) {
+  const long long N = (long long)a.T * a.H * a.W;
+  const size_t bytes = (size_t)a.B * N * a.heads * D * sizeof(float);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(dK, 0, bytes, st)) != cudaSuccess) return e;  // accumulated by atomics
+  if ((e = cudaMemsetAsync(dV, 0, bytes, st)) != cudaSuccess) return e;
+  const dim3 grid((unsigned)((N + kDsaTok - 1) / kDsaTok), a.heads, a.B);
+  dsa3d_bwd_kernel<D><<<grid, kDsaThreads, 0, st>>>(Q, K, V, off, LSE, dO, dQ, dK, dV, doff, a);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t dsa3d_bwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off,
+                      const float* LSE, const void* dO, float* dQ, float* dK, float* dV, float* doff,
+                      cudaStream_t st) {
+  const auto* q = static_cast<const __nv_bfloat16*>(Q);
+  const auto* k = static_cast<const __nv_bfloat16*>(K);
+  const auto* v = static_cast<const __nv_bfloat16*>(V);
+  const auto* g = static_cast<const __nv_bfloat16*>(dO);
+  return a.d == 64 ? launch_dsa3d_bwd<64>(a, q, k, v, off, LSE, g, dQ, dK, dV, doff, st)
+                   : launch_dsa3d_bwd<128>(a, q, k, v, off, LSE, g, dQ, dK, dV, doff, st);
+}
 
 cudaError_t dsa3d_offsets(const Dsa3dArgs& a, const void* Q, const float* Wc, const float* bc, const float* Wl,
                           const float* bl, float* off, cudaStream_t st) {

@@ -94,6 +94,9 @@ cudaError_t dsa3d_offsets(const Dsa3dArgs& a, const void* Q, const float* Wc, co
                           const float* bl, float* off, cudaStream_t st);
 cudaError_t dsa3d_fwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off, void* O,
                       float* LSE, cudaStream_t st);
+cudaError_t dsa3d_bwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off,
+                      const float* LSE, const void* dO, float* dQ, float* dK, float* dV, float* doff,
+                      cudaStream_t st);
 
 size_t predict_ws_tc(const Prob& p);
 cudaError_t predict_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, int32_t* idx,

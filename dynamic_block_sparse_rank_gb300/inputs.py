@@ -311,14 +311,14 @@ def generate_dsa3d(wl: Dsa3dWorkload, seed: int = 0, names=("Q", "K", "V", "offs
                    threads: int | None = None) -> dict[str, np.ndarray]:
     """Draw the seeded inputs of a 3D-DSA workload.
 
-    names: Q, K, V ([B, N, heads_sel, d] float32 holding bf16 values), offsets ([B, N, heads_sel, S, 3]
+    names: Q, K, V, dO ([B, N, heads_sel, d] float32 holding bf16 values), offsets ([B, N, heads_sel, S, 3]
     float32), Wc ([heads_sel, d, 3, 3, 3]), bc ([heads_sel, d]), Wl ([heads_sel, d, 3 S]), bl
     ([heads_sel, 3 S]).  As for `generate`, a head's values do not depend on which heads are asked for.
     """
     heads = list(range(wl.heads)) if heads is None else list(heads)
     want = frozenset(names)
-    out = generate(wl, seed, names=tuple(n for n in ("Q", "K", "V") if n in want), heads=heads,
-                   threads=threads) if want & {"Q", "K", "V"} else {}
+    out = generate(wl, seed, names=tuple(n for n in ("Q", "K", "V", "dO") if n in want), heads=heads,
+                   threads=threads) if want & {"Q", "K", "V", "dO"} else {}
     S, d = wl.S, wl.d
     if "offsets" in want:
         off = np.empty((wl.B, wl.N, len(heads), S, 3), dtype=np.float32)

@@ -22,6 +22,9 @@
  *      Attention State Reuse" (near partitions recomputed, far ones reused),
  *      and sda_merge_states_bwd, its gradient for training through the reuse.
  *
+ * A second sparse-attention family, 3D deformable sliding attention
+ * ("MegaSlide-DiT"), has its own calls (sda_dsa3d_*) and problem struct below.
+ *
  * Conventions shared by every call
  *   - Tokens of a T x H x W latent grid are in raster order n = (t*H + h)*W + w.
  *     Q, K, V, O, dO, dQ, dK, dV are contiguous row-major [B, N, heads, d].
@@ -112,7 +115,9 @@ sda_status sda_predict_blocks(const sda_problem* p, const void* Q, const void* K
  * (b, head, query block I, key block J): the low-rank block score
  * s = max over i in I, j in J of q~_i . k~_j (as sda_predict_blocks computes it)
  * at its maximising pair (i*, j*) — the first in (row, column) order of the two
- * tiles on ties, found exactly — and the full-rank target t = max of q_i . k_j
+ * tiles on ties; fp32 candidates within twice their rounding bound are
+ * re-scored to about 2^-44, so equal scores tie exactly — and the full-rank
+ * target t = max of q_i . k_j
  * over the same pairs.  With e = s - t and L = 1/2 sum e^2:
  *   dWq[h] = dL/dWq[h] = sum e Q_i*^T k~_j*,   dWk[h] = sum e K_j*^T q~_i*
  * (the bf16 rounding of q~, k~ passes the gradient unchanged; t is a target).
@@ -365,6 +370,24 @@ sda_status sda_dsa3d_offsets(const sda_dsa3d_problem* p, const void* Q, const fl
 /* Attention over the sampled window points (O bf16, LSE fp32), fp32 inside. */
 sda_status sda_dsa3d_fwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
                          const float* offsets, void* O, float* LSE, void* stream);
+
+/* Gradients of sda_dsa3d_fwd for a loss that reaches it through O (no LSE
+ * gradient): with P the window softmax, dP_s = dO.v~_s and
+ * da_s = P_s (dP_s - sum_u P_u dP_u),
+ *   dQ        = scale sum_s da_s k~_s (the attention's part: the offset
+ *               network's contribution to dQ is not included),
+ *   dK, dV    at every trilinear corner row m of every sample: w_m scale da_s q
+ *               and w_m P_s dO, summed over all tokens and samples,
+ *   d_offsets = the derivative through the interpolation weights (one-sided
+ *               from above on the integer grid, as floor() sees it).
+ * Inputs as sda_dsa3d_fwd plus LSE (the forward's, fp32 [B, heads, N]) and dO
+ * (bf16 [B, N, heads, d]); outputs fp32: dQ, dK, dV [B, N, heads, d] (16-byte
+ * aligned), d_offsets [B, N, heads, S, 3].  dK and dV are cleared by the call
+ * and then accumulated with atomics (their last bits depend on the order of
+ * the additions); dQ and d_offsets are written.  Errors as sda_dsa3d_fwd. */
+sda_status sda_dsa3d_bwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
+                         const float* offsets, const float* LSE, const void* dO, float* dQ, float* dK, float* dV,
+                         float* d_offsets, void* stream);
 
 /* Host only.  Number of CUDA kernels the library has launched in this process
  * (all devices, all calls); a caller can difference it around a region. */

@@ -29,6 +29,7 @@ def sda():
     s.lib()
     return s
 
+
 WLS = inputs.DSA3D_WORKLOADS
 SMALL = [WLS["dsa3d_ragged_d64"], WLS["dsa3d_d128_1x5x5"], WLS["dsa3d_far"]]
 
@@ -59,6 +60,7 @@ def _gpu_offsets(sda, wl, x):
 def check_fp32(got, ref, what, rel=1e-4):
     mx, rf = errors(got, ref)
     scale = max(1.0, float(np.abs(ref).max()))
+    print(f"{what}: max-abs/scale {mx / scale:.2e}, rel-frob {rf:.2e}")
     assert mx <= rel * scale and rf <= rel, f"{what}: max-abs {mx:.3e} (scale {scale:.3e}), rel-frob {rf:.3e}"
 
 
@@ -144,3 +146,56 @@ def test_dsa3d_edge_shapes(sda, wl):
     got = _gpu_offsets(sda, wl, x)
     ref = D.dsa3d_offsets(x["Q"], x["Wc"], x["bc"], x["Wl"], x["bl"], wl.T, wl.H, wl.W)
     check_fp32(got, ref, "offsets")
+
+
+BWD_REL = 5e-4  # backward results, relative to their scale (see test_dsa3d_backward_matches_oracle)
+
+
+def _gpu_bwd(sda, wl, x, offsets):
+    O, L = None, None
+    p = _problem(sda, wl)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    Q, K, V, dO = (dev(x[n], "bf16") for n in ("Q", "K", "V", "dO"))
+    off = f32(offsets)
+    Ot = torch.empty_like(Q)
+    Lt = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_fwd(p, Q, K, V, off, Ot, Lt)
+    shape = (wl.B, wl.N, wl.heads, wl.d)
+    dQ, dK, dV = (torch.full(shape, float("nan"), dtype=torch.float32, device="cuda") for _ in range(3))
+    doff = torch.full(off.shape, float("nan"), dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_bwd(p, Q, K, V, off, Lt, dO, dQ, dK, dV, doff)
+    torch.cuda.synchronize()
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    del O, L
+    return host(dQ), host(dK), host(dV), host(doff)
+
+
+@pytest.mark.parametrize("wl", SMALL + [inputs.Dsa3dWorkload("dsa3d_5x5x5_d64", 1, 2, 6, 7, 9, 64, 5, 5, 5, 1.5)],
+                         ids=lambda w: w.name)
+def test_dsa3d_backward_matches_oracle(sda, wl):
+    """dQ (the attention's part), dK, dV and the offsets' gradient against the oracle's reading D5 (pinned by
+    torch autograd through grid_sample and by finite differences).  fp32 results of bf16 inputs, held to
+    BWD_REL of their scale: with the correlated Q, K of these inputs the logits' dot products reach a few
+    hundred, whose fp32 accumulation moves each logit, and so each P, by ~1e-5 relative; dP - D then cancels,
+    and dK, dV sum up to 8 S contributions per row by atomics."""
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V", "dO", "offsets"))
+    dQ, dK, dV, doff = _gpu_bwd(sda, wl, x, x["offsets"])
+    rQ, rK, rV, roff = D.dsa3d_bwd(x["Q"], x["K"], x["V"], x["offsets"], x["dO"], wl.T, wl.H, wl.W, wl.kt, wl.kh,
+                                   wl.kw)
+    for name, got, ref in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV), ("d_offsets", doff, roff)):
+        check_fp32(got, ref, name, rel=BWD_REL)
+
+
+def test_dsa3d_backward_outside_and_integer_samples(sda):
+    """Non-finite offsets give no gradient through their samples; integer offsets take the derivative from
+    above (floor's side), as the oracle does."""
+    wl = WLS["dsa3d_ragged_d64"]
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V", "dO", "offsets"))
+    off = np.rint(x["offsets"]).astype(np.float32)
+    rng = np.random.default_rng(5)
+    pick = rng.random(off.shape[:4]) < 0.15
+    off[pick, 1] = np.nan
+    dQ, dK, dV, doff = _gpu_bwd(sda, wl, x, off)
+    rQ, rK, rV, roff = D.dsa3d_bwd(x["Q"], x["K"], x["V"], off, x["dO"], wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    for name, got, ref in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV), ("d_offsets", doff, roff)):
+        check_fp32(got, ref, name, rel=BWD_REL)
