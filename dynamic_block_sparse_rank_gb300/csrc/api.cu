@@ -433,3 +433,26 @@ sda_status sda_dsa3d_bwd(const sda_dsa3d_problem* p, const void* Q, const void* 
   return from_cuda(sda::dsa3d_bwd(a, Q, K, V, offsets, LSE, dO, dQ, dK, dV, d_offsets,
                                   static_cast<cudaStream_t>(stream)));
 }
+
+sda_status sda_dsa3d_offsets_bwd_workspace_size(const sda_dsa3d_problem* p, size_t* bytes) {
+  sda::Dsa3dArgs a;
+  const sda_status st = dsa3d_args(p, a);
+  if (st != SDA_OK) return st;
+  if (!bytes) return SDA_ERR_INVALID_ARG;
+  *bytes = sda::dsa3d_offsets_bwd_ws_bytes(a);
+  return SDA_OK;
+}
+
+sda_status sda_dsa3d_offsets_bwd(const sda_dsa3d_problem* p, const void* Q, const float* Wc, const float* bc,
+                                 const float* Wl, const float* d_offsets, float* dQ, float* dWc, float* dbc,
+                                 float* dWl, float* dbl, void* ws, size_t ws_bytes, void* stream) {
+  sda::Dsa3dArgs a;
+  const sda_status st = dsa3d_args(p, a);
+  if (st != SDA_OK) return st;
+  if (!Q || !Wc || !bc || !Wl || !d_offsets || !dQ || !dWc || !dbc || !dWl || !dbl || !ws)
+    return SDA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(ws)) return SDA_ERR_INVALID_ARG;
+  if (ws_bytes < sda::dsa3d_offsets_bwd_ws_bytes(a)) return SDA_ERR_WORKSPACE;
+  return from_cuda(sda::dsa3d_offsets_bwd(a, Q, Wc, bc, Wl, d_offsets, dQ, dWc, dbc, dWl, dbl, ws,
+                                          static_cast<cudaStream_t>(stream)));
+}

@@ -57,6 +57,60 @@ __host__ __device__ constexpr size_t offsets_smem_bytes(int D) {
   return (size_t)D * kOffYStride * 4 + (size_t)D * kOffJ * 4;
 }
 
+// Y[c][tok] = bc + sum over the 27 taps of Wc * Q (zero outside the raster) for the kOffTok
+// raster tokens from n0 of head h, into Ys ([D][kOffYStride], all 256 threads).  A thread owns a
+// channel pair: its 54 taps stay in registers, its loads are 4-byte pieces of one 128- or
+// 256-byte row per warp, kPer tokens' loads in flight together.  Tokens at or past N get bc.
+template <int D, int kPer>
+__device__ __forceinline__ void conv_tile(const __nv_bfloat16* __restrict__ Q, const float* __restrict__ Wc,
+                                          const float* __restrict__ bc, const Dsa3dArgs& a, int b, int h, int n0,
+                                          float* Ys) {
+  constexpr int kPairs = D / 2;
+  constexpr int kGroups = kDsaThreads / kPairs;
+  static_assert((kOffTok / kGroups) % kPer == 0, "tokens per thread must divide by kPer");
+  const int N = a.T * a.H * a.W;
+  const int tid = threadIdx.x;
+  const int cp = tid % kPairs, tg = tid / kPairs;
+  const int c0 = 2 * cp;
+  float w0[27], w1[27];
+  const float* wc0 = Wc + ((long long)h * D + c0) * 27;
+#pragma unroll
+  for (int k = 0; k < 27; ++k) {
+    w0[k] = wc0[k];
+    w1[k] = wc0[27 + k];
+  }
+  const float b0 = bc[h * D + c0], b1 = bc[h * D + c0 + 1];
+  const __nv_bfloat16* Qh = Q + (long long)b * N * a.heads * D + (long long)h * D + c0;
+  for (int tok = tg; tok < kOffTok; tok += kPer * kGroups) {
+    uint32_t v[kPer][27];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int n = n0 + tok + e * kGroups;
+      int t = 0, y = 0, x = 0;
+      if (n < N) raster_coords(n, a.H, a.W, t, y, x);
+#pragma unroll
+      for (int k = 0; k < 27; ++k) {
+        const int tt = t + k / 9 - 1, yy = y + (k / 3) % 3 - 1, xx = x + k % 3 - 1;
+        const bool in = n < N && tt >= 0 && tt < a.T && yy >= 0 && yy < a.H && xx >= 0 && xx < a.W;
+        const int m = (tt * a.H + yy) * a.W + xx;
+        v[e][k] = in ? __ldg(reinterpret_cast<const unsigned*>(Qh + (long long)m * a.heads * D)) : 0u;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      float y0 = b0, y1 = b1;
+#pragma unroll
+      for (int k = 0; k < 27; ++k) {
+        const float2 f = bf16x2_to_f2(v[e][k]);  // zero bits outside the raster: zero padding
+        y0 = fmaf(w0[k], f.x, y0);
+        y1 = fmaf(w1[k], f.y, y1);
+      }
+      Ys[c0 * kOffYStride + tok + e * kGroups] = y0;
+      Ys[(c0 + 1) * kOffYStride + tok + e * kGroups] = y1;
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kDsaThreads) dsa3d_offsets_kernel(const __nv_bfloat16* __restrict__ Q,
                                                                    const float* __restrict__ Wc,
@@ -72,54 +126,8 @@ __global__ void __launch_bounds__(kDsaThreads) dsa3d_offsets_kernel(const __nv_b
   const int n0 = blockIdx.x * kOffTok;
   const int tid = threadIdx.x;
 
-  // Stage 1: Y[c][tok] = bc + sum over the 27 taps of Wc * Q (zero outside the raster).  A
-  // thread owns a channel pair: its 54 taps stay in registers, its loads are 4-byte pieces of
-  // one 128- or 256-byte row per warp.
-  {
-    constexpr int kPairs = D / 2;
-    constexpr int kGroups = kDsaThreads / kPairs;
-    const int cp = tid % kPairs, tg = tid / kPairs;
-    const int c0 = 2 * cp;
-    float w0[27], w1[27];
-    const float* wc0 = Wc + ((long long)h * D + c0) * 27;
-#pragma unroll
-    for (int k = 0; k < 27; ++k) {
-      w0[k] = wc0[k];
-      w1[k] = wc0[27 + k];
-    }
-    const float b0 = bc[h * D + c0], b1 = bc[h * D + c0 + 1];
-    const __nv_bfloat16* Qh = Q + (long long)b * N * a.heads * D + (long long)h * D + c0;
-    // two tokens per iteration: their 54 loads are in flight together
-    static_assert((kOffTok / kGroups) % 2 == 0, "tokens per thread must be even");
-    for (int tok = tg; tok < kOffTok; tok += 2 * kGroups) {
-      uint32_t v[2][27];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int n = n0 + tok + e * kGroups;
-        int t = 0, y = 0, x = 0;
-        if (n < N) raster_coords(n, a.H, a.W, t, y, x);
-#pragma unroll
-        for (int k = 0; k < 27; ++k) {
-          const int tt = t + k / 9 - 1, yy = y + (k / 3) % 3 - 1, xx = x + k % 3 - 1;
-          const bool in = n < N && tt >= 0 && tt < a.T && yy >= 0 && yy < a.H && xx >= 0 && xx < a.W;
-          const int m = (tt * a.H + yy) * a.W + xx;
-          v[e][k] = in ? __ldg(reinterpret_cast<const unsigned*>(Qh + (long long)m * a.heads * D)) : 0u;
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float y0 = b0, y1 = b1;
-#pragma unroll
-        for (int k = 0; k < 27; ++k) {
-          const float2 f = bf16x2_to_f2(v[e][k]);  // zero bits outside the raster: zero padding
-          y0 = fmaf(w0[k], f.x, y0);
-          y1 = fmaf(w1[k], f.y, y1);
-        }
-        Ys[c0 * kOffYStride + tok + e * kGroups] = y0;
-        Ys[(c0 + 1) * kOffYStride + tok + e * kGroups] = y1;
-      }
-    }
-  }
+  // Stage 1: Y[c][tok] = bc + sum over the 27 taps of Wc * Q (zero outside the raster).
+  conv_tile<D, 2>(Q, Wc, bc, a, b, h, n0, Ys);
 
   // Stage 2: off[tok][j] = bl[j] + sum_c Y[c][tok] Wl[h][c][j].  Register tiles of 4 tokens x 6
   // outputs per thread (16 x 16 threads cover 64 tokens x 96 outputs per pass).
@@ -470,6 +478,222 @@ __global__ void __launch_bounds__(kDsaThreads, 2) dsa3d_bwd_kernel(const __nv_bf
   }
 }
 
+// Offset network backward, part 1 (gradients of the linear layer): for 64-token tiles of one
+// (batch entry, head), with G = the tile's d_offsets, dY = G Wl[h]^T goes to the workspace
+// ([B, N, heads, D] fp32), dWl[h] += Y^T G and dbl[h] += the column sums of G, Y recomputed
+// by conv_tile.  The 3S outputs go in passes of 96 columns; a pass walks all of the CTA's
+// tiles (every gridDim.x-th), adds its share of dY into the workspace (the first pass writes
+// it; one thread owns an element in every pass) and keeps its dWl / dbl columns in registers
+// until the pass ends, then adds them into dWl / dbl with atomics.  A 3 x 3 x 3 window takes
+// one pass; each further pass recomputes Y.
+constexpr int kGStride = kOffJ + 4;  // floats per token row of the staged d_offsets columns
+
+__host__ __device__ constexpr int wlt_stride(int D) { return D + 4; }
+
+__host__ __device__ constexpr size_t offsets_bwd_smem_bytes(int D) {
+  return ((size_t)D * kOffYStride + (size_t)kOffTok * kGStride + (size_t)kOffJ * wlt_stride(D)) * 4;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDsaThreads, 1)
+    dsa3d_offsets_bwd_kernel(const __nv_bfloat16* __restrict__ Q, const float* __restrict__ Wc,
+                             const float* __restrict__ bc, const float* __restrict__ Wl,
+                             const float* __restrict__ doff, float* __restrict__ dY, float* __restrict__ dWl,
+                             float* __restrict__ dbl, Dsa3dArgs a) {
+  constexpr int CPT = D / 16;  // channels per thread in both register tiles
+  extern __shared__ __align__(16) float dsmem[];
+  float* Ys = dsmem;                     // [D][kOffYStride]
+  float* Gs = Ys + D * kOffYStride;      // [kOffTok][kGStride]: one pass's d_offsets columns
+  float* WlT = Gs + kOffTok * kGStride;  // [kOffJ][D + 4]: the same columns of Wl[h], transposed
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int N = a.T * a.H * a.W;
+  const int S3 = 3 * a.S;
+  const int ntiles = (N + kOffTok - 1) / kOffTok;
+  const int tid = threadIdx.x;
+  const float* wl = Wl + (long long)h * D * S3;
+  // dY tile: channels c1 .. c1 + CPT - 1 x tokens 4 tg1 .. 4 tg1 + 3
+  const int c1 = (tid % 16) * CPT, tg1 = tid / 16;
+  // dWl tile: channels cg2 + 16 k (k < CPT; interleaved, so the two channel groups of a warp
+  // read different banks of Ys) x columns 6 jg2 .. 6 jg2 + 5 of the pass
+  const int jg2 = tid % 16, cg2 = tid / 16;
+
+  for (int j0 = 0; j0 < S3; j0 += kOffJ) {
+    const int jn = min(kOffJ, S3 - j0);
+    __syncthreads();  // the previous pass's WlT reads are done
+    for (int e = tid; e < D * kOffJ; e += kDsaThreads) {
+      const int c = e / kOffJ, jj = e % kOffJ;
+      WlT[jj * wlt_stride(D) + c] = jj < jn ? wl[(long long)c * S3 + j0 + jj] : 0.f;
+    }
+    float2 gw[CPT][3];  // dWl[h][cg2 + 16 k][j0 + 6 jg2 + 2 q, + 1]
+    float2 gb[3];       // dbl[h][the same columns]
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      gb[q] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) gw[k][q] = make_float2(0.f, 0.f);
+    }
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const int n0 = tile * kOffTok;
+      __syncthreads();  // the previous tile's Ys / Gs reads are done
+      conv_tile<D, 1>(Q, Wc, bc, a, b, h, n0, Ys);
+      static_assert((kOffTok * kOffJ) % kDsaThreads == 0, "G staging must tile evenly");
+#pragma unroll 8
+      for (int e = tid; e < kOffTok * kOffJ; e += kDsaThreads) {
+        const int tok = e / kOffJ, jj = e % kOffJ;
+        const int n = n0 + tok;
+        // rows past N and columns past 3S stay zero: they add nothing to dY, dWl or dbl
+        Gs[tok * kGStride + jj] =
+            n < N && jj < jn ? __ldg(doff + (((long long)b * N + n) * a.heads + h) * S3 + j0 + jj) : 0.f;
+      }
+      __syncthreads();
+
+      // dY[tok][c] (+)= sum_j G[tok][j] Wl[h][c][j] over this pass's columns
+      float2 acc[CPT][2];  // tokens (4 tg1, 4 tg1 + 1) and (4 tg1 + 2, 4 tg1 + 3)
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) acc[k][0] = acc[k][1] = make_float2(0.f, 0.f);
+#pragma unroll 4
+      for (int jj = 0; jj < jn; ++jj) {
+        const float* gcol = Gs + (4 * tg1) * kGStride + jj;
+        const float2 g01 = make_float2(gcol[0], gcol[kGStride]);
+        const float2 g23 = make_float2(gcol[2 * kGStride], gcol[3 * kGStride]);
+        float w[CPT];
+#pragma unroll
+        for (int k = 0; k < CPT; k += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(WlT + jj * wlt_stride(D) + c1 + k);
+          w[k] = w4.x;
+          w[k + 1] = w4.y;
+          w[k + 2] = w4.z;
+          w[k + 3] = w4.w;
+        }
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+          acc[k][0] = ffma2(make_float2(w[k], w[k]), g01, acc[k][0]);
+          acc[k][1] = ffma2(make_float2(w[k], w[k]), g23, acc[k][1]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = n0 + 4 * tg1 + i;
+        if (n >= N) continue;
+        float* row = dY + (((long long)b * N + n) * a.heads + h) * D + c1;
+#pragma unroll
+        for (int k = 0; k < CPT; k += 4) {
+          float4 v;
+          v.x = (i & 1) ? acc[k][i >> 1].y : acc[k][i >> 1].x;
+          v.y = (i & 1) ? acc[k + 1][i >> 1].y : acc[k + 1][i >> 1].x;
+          v.z = (i & 1) ? acc[k + 2][i >> 1].y : acc[k + 2][i >> 1].x;
+          v.w = (i & 1) ? acc[k + 3][i >> 1].y : acc[k + 3][i >> 1].x;
+          float4* p = reinterpret_cast<float4*>(row + k);
+          if (j0 > 0) {
+            const float4 o = *p;
+            v.x += o.x;
+            v.y += o.y;
+            v.z += o.z;
+            v.w += o.w;
+          }
+          *p = v;
+        }
+      }
+
+      // dWl[h][c][j] += sum_tok Y[c][tok] G[tok][j]; dbl[h][j] += sum_tok G[tok][j]
+#pragma unroll 2
+      for (int tok = 0; tok < kOffTok; ++tok) {
+        const float2* grow = reinterpret_cast<const float2*>(Gs + tok * kGStride + 6 * jg2);
+        const float2 g[3] = {grow[0], grow[1], grow[2]};
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+          const float y = Ys[(cg2 + 16 * k) * kOffYStride + tok];
+#pragma unroll
+          for (int q = 0; q < 3; ++q) gw[k][q] = ffma2(make_float2(y, y), g[q], gw[k][q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) gb[q] = fadd2(gb[q], g[q]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int j = j0 + 6 * jg2 + 2 * q;
+#pragma unroll
+      for (int k = 0; k < CPT; ++k) {
+        float* p = dWl + ((long long)h * D + cg2 + 16 * k) * S3 + j;
+        if (j < S3) atomicAdd(p, gw[k][q].x);
+        if (j + 1 < S3) atomicAdd(p + 1, gw[k][q].y);
+      }
+      if (cg2 == 0) {
+        if (j < S3) atomicAdd(dbl + (long long)h * S3 + j, gb[q].x);
+        if (j + 1 < S3) atomicAdd(dbl + (long long)h * S3 + j + 1, gb[q].y);
+      }
+    }
+  }
+}
+
+// Offset network backward, part 2 (gradients of the depthwise convolution): with dY from part
+// 1, dQ[m][c] += sum over taps of Wc[h][c][tap] dY[m - tap][c] (the transposed convolution,
+// zero padding), dWc[h][c][tap] += sum_m dY[m - tap][c] Q[m][c] and dbc[h][c] += sum_m dY[m][c].
+// A thread owns one channel (the warp reads one 128-byte piece of a row per tap) and 256 / D
+// tokens run side by side, two per thread at a time; the CTA walks 32-token tiles with the
+// grid's x stride, keeps its 27 + 1 weight-gradient sums in registers and adds them with
+// atomics at the end.
+constexpr int kConvTok = 32;
+
+template <int D>
+__global__ void __launch_bounds__(kDsaThreads, 2)
+    dsa3d_offsets_bwd_conv_kernel(const __nv_bfloat16* __restrict__ Q, const float* __restrict__ Wc,
+                                  const float* __restrict__ dY, float* __restrict__ dQ, float* __restrict__ dWc,
+                                  float* __restrict__ dbc, Dsa3dArgs a) {
+  constexpr int kLanes = kDsaThreads / D;
+  static_assert(kConvTok % (2 * kLanes) == 0, "two tokens per thread per step");
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int N = a.T * a.H * a.W;
+  const int ntiles = (N + kConvTok - 1) / kConvTok;
+  const int c = threadIdx.x % D, lane = threadIdx.x / D;
+  const long long rs = (long long)a.heads * D;  // elements between consecutive tokens' rows
+  const long long base = (long long)b * N * rs + (long long)h * D + c;
+  float w[27], gw[27];
+#pragma unroll
+  for (int k = 0; k < 27; ++k) {
+    w[k] = Wc[((long long)h * D + c) * 27 + k];
+    gw[k] = 0.f;
+  }
+  float gb = 0.f;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int tok = lane; tok < kConvTok; tok += 2 * kLanes) {
+      float v[2][27];
+      float q[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int m = tile * kConvTok + tok + e * kLanes;
+        int t = 0, y = 0, x = 0;
+        if (m < N) raster_coords(m, a.H, a.W, t, y, x);
+        q[e] = m < N ? __bfloat162float(Q[base + (long long)m * rs]) : 0.f;
+#pragma unroll
+        for (int k = 0; k < 27; ++k) {
+          // tap k reads X at (t, y, x) + (k / 9, k / 3 % 3, k % 3) - 1 for the output at n = m - that
+          const int tt = t - k / 9 + 1, yy = y - (k / 3) % 3 + 1, xx = x - k % 3 + 1;
+          const bool in = m < N && tt >= 0 && tt < a.T && yy >= 0 && yy < a.H && xx >= 0 && xx < a.W;
+          const int n = (tt * a.H + yy) * a.W + xx;
+          v[e][k] = in ? __ldg(dY + base + (long long)n * rs) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int m = tile * kConvTok + tok + e * kLanes;
+        float dq = 0.f;
+#pragma unroll
+        for (int k = 0; k < 27; ++k) {
+          dq = fmaf(w[k], v[e][k], dq);
+          gw[k] = fmaf(v[e][k], q[e], gw[k]);
+        }
+        gb += v[e][13];  // the centre tap: dY of the token itself
+        if (m < N) dQ[base + (long long)m * rs] += dq;
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 27; ++k) atomicAdd(dWc + ((long long)h * D + c) * 27 + k, gw[k]);
+  atomicAdd(dbc + (long long)h * D + c, gb);
+}
+
 template <int D>
 cudaError_t launch_dsa3d(const Dsa3dArgs& a, const __nv_bfloat16* Q, const __nv_bfloat16* K, const __nv_bfloat16* V,
                          const float* Wc, const float* bc, const float* Wl, const float* bl, float* off,
@@ -505,6 +729,48 @@ cudaError_t launch_dsa3d_bwd(const Dsa3dArgs& a, const __nv_bfloat16* Q, const _
   return cudaGetLastError();
 }
 
+// Persistent grid of part 1 / part 2 of the offset network backward: per (batch entry, head)
+// as many CTAs as the device holds at once (capped by the tiles), so that the CTAs of one head
+// run together and its rows' neighbours meet in L2.
+template <typename K>
+cudaError_t resident_ctas(K kernel, size_t smem, int tiles, int& ctas) {
+  int dev = 0, sms = 0, occ = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kDsaThreads, smem)) != cudaSuccess) return e;
+  ctas = max(1, min(tiles, max(1, occ) * sms));
+  return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_dsa3d_offsets_bwd(const Dsa3dArgs& a, const __nv_bfloat16* Q, const float* Wc, const float* bc,
+                                     const float* Wl, const float* doff, float* dQ, float* dWc, float* dbc,
+                                     float* dWl, float* dbl, float* dY, cudaStream_t st) {
+  const int N = a.T * a.H * a.W;
+  const int S3 = 3 * a.S;
+  cudaError_t e;
+  // weight gradients are accumulated by atomics
+  if ((e = cudaMemsetAsync(dWc, 0, (size_t)a.heads * D * 27 * sizeof(float), st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dbc, 0, (size_t)a.heads * D * sizeof(float), st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dWl, 0, (size_t)a.heads * D * S3 * sizeof(float), st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dbl, 0, (size_t)a.heads * S3 * sizeof(float), st)) != cudaSuccess) return e;
+  const size_t smem = offsets_bwd_smem_bytes(D);
+  if ((e = cudaFuncSetAttribute(dsa3d_offsets_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem)) != cudaSuccess)
+    return e;
+  int c1 = 0, c2 = 0;
+  if ((e = resident_ctas(dsa3d_offsets_bwd_kernel<D>, smem, (N + kOffTok - 1) / kOffTok, c1)) != cudaSuccess)
+    return e;
+  if ((e = resident_ctas(dsa3d_offsets_bwd_conv_kernel<D>, 0, (N + kConvTok - 1) / kConvTok, c2)) != cudaSuccess)
+    return e;
+  dsa3d_offsets_bwd_kernel<D><<<dim3(c1, a.heads, a.B), kDsaThreads, smem, st>>>(Q, Wc, bc, Wl, doff, dY, dWl,
+                                                                                  dbl, a);
+  dsa3d_offsets_bwd_conv_kernel<D><<<dim3(c2, a.heads, a.B), kDsaThreads, 0, st>>>(Q, Wc, dY, dQ, dWc, dbc, a);
+  note_launches(2);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t dsa3d_bwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off,
@@ -535,6 +801,19 @@ cudaError_t dsa3d_fwd(const Dsa3dArgs& a, const void* Q, const void* K, const vo
              ? launch_dsa3d<64>(a, q, k, v, nullptr, nullptr, nullptr, nullptr, const_cast<float*>(off), o, LSE, false, st)
              : launch_dsa3d<128>(a, q, k, v, nullptr, nullptr, nullptr, nullptr, const_cast<float*>(off), o, LSE, false,
                                  st);
+}
+
+cudaError_t dsa3d_offsets_bwd(const Dsa3dArgs& a, const void* Q, const float* Wc, const float* bc, const float* Wl,
+                              const float* doff, float* dQ, float* dWc, float* dbc, float* dWl, float* dbl,
+                              void* ws, cudaStream_t st) {
+  const auto* q = static_cast<const __nv_bfloat16*>(Q);
+  auto* dY = static_cast<float*>(ws);
+  return a.d == 64 ? launch_dsa3d_offsets_bwd<64>(a, q, Wc, bc, Wl, doff, dQ, dWc, dbc, dWl, dbl, dY, st)
+                   : launch_dsa3d_offsets_bwd<128>(a, q, Wc, bc, Wl, doff, dQ, dWc, dbc, dWl, dbl, dY, st);
+}
+
+size_t dsa3d_offsets_bwd_ws_bytes(const Dsa3dArgs& a) {
+  return (size_t)a.B * a.T * a.H * a.W * a.heads * a.d * sizeof(float);
 }
 
 }  // namespace sda

@@ -97,6 +97,10 @@ cudaError_t dsa3d_fwd(const Dsa3dArgs& a, const void* Q, const void* K, const vo
 cudaError_t dsa3d_bwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off,
                       const float* LSE, const void* dO, float* dQ, float* dK, float* dV, float* doff,
                       cudaStream_t st);
+cudaError_t dsa3d_offsets_bwd(const Dsa3dArgs& a, const void* Q, const float* Wc, const float* bc, const float* Wl,
+                              const float* doff, float* dQ, float* dWc, float* dbc, float* dWl, float* dbl,
+                              void* ws, cudaStream_t st);
+size_t dsa3d_offsets_bwd_ws_bytes(const Dsa3dArgs& a);
 
 size_t predict_ws_tc(const Prob& p);
 cudaError_t predict_tc(const Prob& p, const void* Q, const void* K, const void* Wq, const void* Wk, int32_t* idx,

@@ -261,7 +261,7 @@ def digest(arrays: dict[str, np.ndarray]) -> str:
 # in token units (fp32, drawn directly for the attention alone); offset-network weights in fp32:
 # Wc ~ N(0, 1/27), bc ~ N(0, 0.1^2), Wl ~ N(0, off_std^2 / (d (amp^2 + 1))), bl ~ N(0, 0.1^2), which gives
 # predicted offsets of about off_std tokens.
-_DSA_OFF, _DSA_WC, _DSA_BC, _DSA_WL, _DSA_BL = range(20, 25)
+_DSA_OFF, _DSA_WC, _DSA_BC, _DSA_WL, _DSA_BL, _DSA_DOFF = range(20, 26)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -311,8 +311,8 @@ def generate_dsa3d(wl: Dsa3dWorkload, seed: int = 0, names=("Q", "K", "V", "offs
                    threads: int | None = None) -> dict[str, np.ndarray]:
     """Draw the seeded inputs of a 3D-DSA workload.
 
-    names: Q, K, V, dO ([B, N, heads_sel, d] float32 holding bf16 values), offsets ([B, N, heads_sel, S, 3]
-    float32), Wc ([heads_sel, d, 3, 3, 3]), bc ([heads_sel, d]), Wl ([heads_sel, d, 3 S]), bl
+    names: Q, K, V, dO ([B, N, heads_sel, d] float32 holding bf16 values), offsets and d_offsets (an upstream
+    gradient of the offsets, unit normal) ([B, N, heads_sel, S, 3] float32), Wc ([heads_sel, d, 3, 3, 3]), bc ([heads_sel, d]), Wl ([heads_sel, d, 3 S]), bl
     ([heads_sel, 3 S]).  As for `generate`, a head's values do not depend on which heads are asked for.
     """
     heads = list(range(wl.heads)) if heads is None else list(heads)
@@ -326,6 +326,12 @@ def generate_dsa3d(wl: Dsa3dWorkload, seed: int = 0, names=("Q", "K", "V", "offs
             for hi, h in enumerate(heads):
                 off[b, :, hi] = wl.off_std * _rng(seed, _DSA_OFF, b, h).standard_normal((wl.N, S, 3))
         out["offsets"] = off
+    if "d_offsets" in want:
+        g = np.empty((wl.B, wl.N, len(heads), S, 3), dtype=np.float32)
+        for b in range(wl.B):
+            for hi, h in enumerate(heads):
+                g[b, :, hi] = _rng(seed, _DSA_DOFF, b, h).standard_normal((wl.N, S, 3))
+        out["d_offsets"] = g
     wscale = wl.off_std / math.sqrt(d * (wl.amp ** 2 + 1.0))
     for name, stream, shape, sd in (("Wc", _DSA_WC, (d, 3, 3, 3), 1.0 / math.sqrt(27.0)),
                                     ("bc", _DSA_BC, (d,), 0.1),

@@ -389,6 +389,29 @@ sda_status sda_dsa3d_bwd(const sda_dsa3d_problem* p, const void* Q, const void* 
                          const float* offsets, const float* LSE, const void* dO, float* dQ, float* dK, float* dV,
                          float* d_offsets, void* stream);
 
+/* Host only.  Bytes of device workspace that sda_dsa3d_offsets_bwd needs:
+ * B*N*heads*d*4 (the fp32 gradient of the convolution output Y). */
+sda_status sda_dsa3d_offsets_bwd_workspace_size(const sda_dsa3d_problem* p, size_t* bytes);
+
+/* Gradients of sda_dsa3d_offsets (the offset network) for the offsets'
+ * gradient d_offsets (fp32 [B, N, heads, S, 3], e.g. from sda_dsa3d_bwd).
+ * With Y the convolution output and G = d_offsets of a head:
+ *   dY  = G Wl[h]^T,   dWl[h] = Y^T G,   dbl[h] = sum over tokens of G,
+ *   dWc[h][c][tap] = sum_n dY[n][c] Q[n + tap][c] (zero outside the raster),
+ *   dbc[h][c] = sum_n dY[n][c],
+ *   dQ += the transposed convolution of dY with Wc[h] (zero padding).
+ * dQ (fp32 [B, N, heads, d]) is ADDED to, so that a caller passes the dQ of
+ * sda_dsa3d_bwd and receives the total; dWc, dbc, dWl, dbl (fp32, shaped as
+ * Wc, bc, Wl, bl) are cleared by the call and then accumulated with atomics
+ * (their last bits depend on the order of the additions).  bl does not enter.
+ *   ws  device workspace of at least
+ *       sda_dsa3d_offsets_bwd_workspace_size bytes, 16-byte aligned.
+ * Asynchronous on `stream`; allocates nothing.  Errors as sda_dsa3d_fwd, plus
+ * SDA_ERR_WORKSPACE for a workspace smaller than that size. */
+sda_status sda_dsa3d_offsets_bwd(const sda_dsa3d_problem* p, const void* Q, const float* Wc, const float* bc,
+                                 const float* Wl, const float* d_offsets, float* dQ, float* dWc, float* dbc,
+                                 float* dWl, float* dbl, void* ws, size_t ws_bytes, void* stream);
+
 /* Host only.  Number of CUDA kernels the library has launched in this process
  * (all devices, all calls); a caller can difference it around a region. */
 unsigned long long sda_kernel_launch_count(void);

@@ -194,11 +194,16 @@ def _corners(pos, T, H, W):
     return out
 
 
-def dsa3d_bwd(Q, K, V, offsets, dO, T, H, W, kt, kh, kw, scale=None):
+def dsa3d_bwd(Q, K, V, offsets, dO, T, H, W, kt, kh, kw, scale=None, tokens=None, rows=None):
     """Gradients of 3D deformable sliding attention (reading D5).
 
     Q, K, V, dO: [B, N, Hh, d]; offsets: [B, N, Hh, S, 3].  Returns (dQ, dK, dV [B, N, Hh, d],
     d_offsets [B, N, Hh, S, 3]) fp64; dQ is the attention's part only.
+
+    tokens (sorted raster indices) restricts the work to those tokens: dQ and d_offsets then hold their rows
+    only, and dK, dV hold, for the raster rows `rows` (sorted; default: tokens), the sum over the selected
+    tokens' samples alone.  A row's dK, dV are its full value when every token whose samples touch it is
+    selected.
     """
     Q = np.asarray(Q, dtype=np.float64)
     K = np.asarray(K, dtype=np.float64)
@@ -209,18 +214,21 @@ def dsa3d_bwd(Q, K, V, offsets, dO, T, H, W, kt, kh, kw, scale=None):
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     g = window_points(kt, kh, kw)
     p = token_coords(T, H, W)
-    dQ = np.zeros_like(Q)
-    dK = np.zeros_like(K)
-    dV = np.zeros_like(V)
-    doff = np.zeros_like(offsets)
+    toks = np.arange(N) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    rows = toks if rows is None else np.asarray(rows, dtype=np.int64)
+    dQ = np.zeros((B, len(toks), Hh, d))
+    dK = np.zeros((B, len(rows), Hh, d))
+    dV = np.zeros((B, len(rows), Hh, d))
+    doff = np.zeros((B, len(toks)) + offsets.shape[2:])
     chunk = 256
     for b in range(B):
         for h in range(Hh):
             Kh, Vh = K[b, :, h, :], V[b, :, h, :]
-            for c0 in range(0, N, chunk):
-                sl = slice(c0, min(N, c0 + chunk))
-                q, do = Q[b, sl, h, :], dO[b, sl, h, :]
-                pos = p[sl, None, :] + g[None, :, :] + offsets[b, sl, h]  # [n, S, 3]
+            for c0 in range(0, len(toks), chunk):
+                sl = slice(c0, min(len(toks), c0 + chunk))
+                tk = toks[sl]
+                q, do = Q[b, tk, h, :], dO[b, tk, h, :]
+                pos = p[tk, None, :] + g[None, :, :] + offsets[b, tk, h]  # [n, S, 3]
                 cs = _corners(pos, T, H, W)
                 ks = sum(w[..., None] * Kh[n] for n, _, w, _ in cs)  # [n, S, d]
                 vs = sum(w[..., None] * Vh[n] for n, _, w, _ in cs)
@@ -233,8 +241,10 @@ def dsa3d_bwd(Q, K, V, offsets, dO, T, H, W, kt, kh, kw, scale=None):
                 for n, inside, w, dw in cs:
                     gk = (w * scale * da)[..., None] * q[:, None, :]  # [n, S, d]
                     gv = (w * P)[..., None] * do[:, None, :]
-                    np.add.at(dK[b, :, h, :], n[inside], gk[inside])
-                    np.add.at(dV[b, :, h, :], n[inside], gv[inside])
+                    r = np.minimum(np.searchsorted(rows, n), len(rows) - 1)  # the corner row's place in rows
+                    hit = inside & (rows[r] == n)
+                    np.add.at(dK[b, :, h, :], r[hit], gk[hit])
+                    np.add.at(dV[b, :, h, :], r[hit], gv[hit])
                     qk = np.einsum("nd,nsd->ns", q, Kh[n])
                     dv = np.einsum("nd,nsd->ns", do, Vh[n])
                     doff[b, sl, h] += dw * (scale * da * qk + P * dv)[..., None]

@@ -104,3 +104,18 @@ def check_selection(gpu_idx: np.ndarray, scores: np.ndarray, k: int) -> dict:
         elif not np.array_equal(got, want):
             stats["near_tie_differs"] += 1
     return stats
+
+
+def reaching_tokens(rows, offsets, T, H, W, kt, kh, kw):
+    """Every token one of whose samples can have a trilinear corner on one of `rows`: the tokens within the
+    window's half-size plus the largest |offset| plus one of a row, per axis."""
+    r = np.ceil(np.nanmax(np.abs(offsets), axis=(0, 1, 2, 3))).astype(int) + 1 + np.array([kt, kh, kw]) // 2
+    out = set()
+    for m in np.asarray(rows):
+        t, y, x = m // (H * W), (m // W) % H, m % W
+        for tt in range(max(0, t - r[0]), min(T, t + r[0] + 1)):
+            for yy in range(max(0, y - r[1]), min(H, y + r[1] + 1)):
+                for xx in range(max(0, x - r[2]), min(W, x + r[2] + 1)):
+                    out.add((tt * H + yy) * W + xx)
+    return np.array(sorted(out), dtype=np.int64)
+

@@ -226,3 +226,29 @@ def test_dsa3d_host_validation(L):
     assert sda.lib().sda_dsa3d_offsets(ctypes.byref(p), fake, fake, None, fake, fake, fake, None) == \
         sda.SDA_ERR_INVALID_ARG
     assert sda.lib().sda_dsa3d_fwd(None, fake, fake, fake, fake, fake, fake, None) == sda.SDA_ERR_INVALID_ARG
+
+
+def test_dsa3d_backward_host_validation(L):
+    """The 3D-DSA backward calls check their arguments and workspace before any launch."""
+    import ctypes
+
+    from dynamic_block_sparse_rank_gb300 import sda
+
+    fake = 1 << 20
+    good = dict(B=2, T=4, H=5, W=6, heads=3, d=128, kt=3, kh=3, kw=3)
+    p = sda.dsa3d_problem(**good)
+    assert sda.sda_dsa3d_offsets_bwd_workspace_size(p) == 2 * 4 * 5 * 6 * 3 * 128 * 4
+    need = sda.sda_dsa3d_offsets_bwd_workspace_size(p)
+    ob = lambda p, ws_bytes, *ptrs: sda.lib().sda_dsa3d_offsets_bwd(
+        ctypes.byref(p), *(ptrs or (fake,) * 10), fake, ws_bytes, None)
+    assert ob(p, need - 4) == sda.SDA_ERR_WORKSPACE
+    assert ob(sda.dsa3d_problem(**{**good, "d": 96}), need) == sda.SDA_ERR_UNSUPPORTED
+    assert ob(sda.dsa3d_problem(**{**good, "kh": 4}), need) == sda.SDA_ERR_INVALID_ARG
+    assert ob(p, need, fake + 8, *(fake,) * 9) == sda.SDA_ERR_INVALID_ARG  # misaligned Q
+    assert ob(p, need, fake, fake, None, *(fake,) * 7) == sda.SDA_ERR_INVALID_ARG  # no bc
+    assert sda.lib().sda_dsa3d_offsets_bwd(ctypes.byref(p), *(fake,) * 10, fake + 4, need, None) == \
+        sda.SDA_ERR_INVALID_ARG  # misaligned workspace
+    assert sda.lib().sda_dsa3d_offsets_bwd_workspace_size(ctypes.byref(p), None) == sda.SDA_ERR_INVALID_ARG
+    bw = lambda *ptrs: sda.lib().sda_dsa3d_bwd(ctypes.byref(p), *ptrs, None)
+    assert bw(*(fake,) * 6, fake + 4, *(fake,) * 4) == sda.SDA_ERR_INVALID_ARG  # misaligned dQ
+    assert bw(*(fake,) * 9, None, fake) == sda.SDA_ERR_INVALID_ARG  # no dV

@@ -149,6 +149,7 @@ def test_dsa3d_edge_shapes(sda, wl):
 
 
 BWD_REL = 5e-4  # backward results, relative to their scale (see test_dsa3d_backward_matches_oracle)
+OFFB_REL = 1e-5  # the offset network's backward: fp32 sums of exact inputs (see its test)
 
 
 def _gpu_bwd(sda, wl, x, offsets):
@@ -199,3 +200,51 @@ def test_dsa3d_backward_outside_and_integer_samples(sda):
     rQ, rK, rV, roff = D.dsa3d_bwd(x["Q"], x["K"], x["V"], off, x["dO"], wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
     for name, got, ref in (("dQ", dQ, rQ), ("dK", dK, rK), ("dV", dV, rV), ("d_offsets", doff, roff)):
         check_fp32(got, ref, name, rel=BWD_REL)
+
+
+def _gpu_offsets_bwd(sda, wl, x, dQ0):
+    p = _problem(sda, wl)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    dQ = f32(dQ0)
+    outs = [torch.full(x[n].shape, float("nan"), dtype=torch.float32, device="cuda") for n in ("Wc", "bc", "Wl", "bl")]
+    ws = torch.empty(sda.sda_dsa3d_offsets_bwd_workspace_size(p) // 4, dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_offsets_bwd(p, dev(x["Q"], "bf16"), f32(x["Wc"]), f32(x["bc"]), f32(x["Wl"]), f32(x["d_offsets"]),
+                              dQ, *outs, ws)
+    torch.cuda.synchronize()
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    return [host(dQ)] + [host(t) for t in outs]
+
+
+@pytest.mark.parametrize("wl", SMALL + [inputs.Dsa3dWorkload("dsa3d_5x5x5_d64", 1, 2, 6, 7, 9, 64, 5, 5, 5, 1.5),
+                                        inputs.Dsa3dWorkload("dsa3d_3x5x5_d128", 2, 1, 5, 6, 70, 128, 3, 5, 5, 1.0)],
+                         ids=lambda w: w.name)
+def test_dsa3d_offsets_backward_matches_oracle(sda, wl):
+    """The offset network's gradients (reading D5: dY = G Wl^T, dWl = Y^T G, dbl, dWc, dbc and the transposed
+    convolution added into dQ) against the oracle, which torch autograd through conv3d pins.  dQ starts from a
+    given value, so the call's addition is checked too.  The inputs are exact in fp32 and every result is an
+    fp32 sum of at most a few thousand products (weight gradients over every token, by atomics), whose
+    rounding stays near 1e-7 of the scale: held to OFFB_REL.  The 5 x 5 x 5 and 3 x 5 x 5 windows take 4 and
+    3 column passes."""
+    x = inputs.generate_dsa3d(wl, names=("Q", "Wc", "bc", "Wl", "bl", "d_offsets"))
+    dQ0 = inputs.generate_dsa3d(wl, seed=3, names=("dO",))["dO"]
+    got = _gpu_offsets_bwd(sda, wl, x, dQ0)
+    ref = D.dsa3d_offsets_bwd(x["Q"], x["Wc"], x["bc"], x["Wl"], x["bl"], x["d_offsets"], wl.T, wl.H, wl.W)
+    ref = [ref[0] + dQ0.astype(np.float64)] + list(ref[1:])
+    for name, g, r in zip(("dQ", "dWc", "dbc", "dWl", "dbl"), got, ref):
+        check_fp32(g, r, name, rel=OFFB_REL)
+
+
+def test_dsa3d_full_backward_chain(sda):
+    """Attention backward, then the offset network's: the total dQ and the weight gradients match the oracle's
+    chain (dsa3d_bwd's d_offsets fed to dsa3d_offsets_bwd), with the offsets the network predicts."""
+    wl = WLS["dsa3d_ragged_d64"]
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V", "dO", "Wc", "bc", "Wl", "bl"))
+    off = D.dsa3d_offsets(x["Q"], x["Wc"], x["bc"], x["Wl"], x["bl"], wl.T, wl.H, wl.W)
+    dQa, dK, dV, doff = _gpu_bwd(sda, wl, x, off)
+    rQ, rK, rV, roff = D.dsa3d_bwd(x["Q"], x["K"], x["V"], off, x["dO"], wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+    y = dict(x, d_offsets=doff)
+    got = _gpu_offsets_bwd(sda, wl, y, dQa)
+    ref = D.dsa3d_offsets_bwd(x["Q"], x["Wc"], x["bc"], x["Wl"], x["bl"], roff, wl.T, wl.H, wl.W)
+    ref = [ref[0] + rQ] + list(ref[1:])
+    for name, g, r in zip(("dQ total", "dWc", "dbc", "dWl", "dbl"), got, ref):
+        check_fp32(g, r, name, rel=BWD_REL)

@@ -418,3 +418,75 @@ def test_dsa3d_524k_sampled_tokens_every_head(sda, parity_report):
     o["rel_frob_max"] = max(o["rel_frob_max"], float(errors(off_s, ref_off)[1]))
     lo = rec.e["outputs"].setdefault("LSE", {"max_abs": 0.0, "rel_frob_max": 0.0, "values": 0})
     lo.update(max_abs=max(lo["max_abs"], mx), rel_frob_max=max(lo["rel_frob_max"], rel), values=lo["values"] + Lr.size)
+
+
+def _fp32_record(rec, key, got, ref, rel):
+    mx, rf = errors(got, ref)
+    scale = max(1.0, float(np.abs(ref).max()))
+    assert mx <= rel * scale and rf <= rel, f"{key}: max-abs {mx:.3e} (scale {scale:.3e}), rel-frob {rf:.3e}"
+    o = rec.e["outputs"].setdefault(key, {"max_abs": 0.0, "rel_frob_max": 0.0, "values": 0})
+    o["max_abs"] = max(o["max_abs"], float(mx))
+    o["rel_frob_max"] = max(o["rel_frob_max"], float(rf))
+    o["values"] += int(np.size(ref))
+
+
+def test_dsa3d_524k_backward_sampled(sda, parity_report):
+    """Both 3D-DSA backward calls on the 524,288-token grid, 8 heads, d = 128, 3 x 3 x 3 window, every token on
+    the GPU.  The oracle recomputes: dQ and d_offsets of 512 seeded tokens (plus the grid's corners) on every
+    head; dK and dV of 6 seeded rows (plus the first and last) on heads 0 and 7, from every token that can
+    reach them; and the offset network's gradients of head 0 in full (dWc, dbc, dWl, dbl sum over all
+    524,288 tokens) with its dQ at the sampled tokens.  Tolerance 5e-4 of scale, as at the small sizes."""
+    from oracle import dsa3d_oracle as D
+    from tests.parity_util import reaching_tokens
+
+    wl = inputs.DSA3D_WORKLOADS["dsa3d_524k"]
+    rng = np.random.default_rng(12)
+    corners = [((t * wl.H + h) * wl.W + w) for t in (0, wl.T - 1) for h in (0, wl.H - 1) for w in (0, wl.W - 1)]
+    toks = np.unique(np.concatenate([rng.choice(wl.N, 512, replace=False), corners]))
+    rows = np.unique(np.concatenate([rng.choice(wl.N, 6, replace=False), [0, wl.N - 1]]))
+    rec = _Record(parity_report, wl.name + "_backward",
+                  f"dQ, d_offsets: 8 heads x {len(toks)} tokens; dK, dV: 2 heads x {len(rows)} rows; offset "
+                  f"network: head 0 in full")
+    x = inputs.generate_dsa3d(wl, names=("Q", "K", "V", "dO", "offsets", "Wc", "bc", "Wl", "d_offsets"))
+    f = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    p = sda.dsa3d_problem(wl.B, wl.T, wl.H, wl.W, wl.heads, wl.d, wl.kt, wl.kh, wl.kw)
+    Q, K, V, dO = (dev(x[n], "bf16") for n in ("Q", "K", "V", "dO"))
+    off = f(x["offsets"])
+    O = torch.empty_like(Q)
+    LSE = torch.empty((wl.B, wl.heads, wl.N), dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_fwd(p, Q, K, V, off, O, LSE)
+    shape = (wl.B, wl.N, wl.heads, wl.d)
+    dQ, dK, dV = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(3))
+    doff = torch.empty_like(off)
+    sda.sda_dsa3d_bwd(p, Q, K, V, off, LSE, dO, dQ, dK, dV, doff)
+    dQn = torch.zeros(shape, dtype=torch.float32, device="cuda")
+    gW = [torch.empty(x[n].shape, dtype=torch.float32, device="cuda") for n in ("Wc", "bc", "Wl")]
+    gW.append(torch.empty((wl.heads, 3 * wl.S), dtype=torch.float32, device="cuda"))
+    ws = torch.empty(sda.sda_dsa3d_offsets_bwd_workspace_size(p) // 4, dtype=torch.float32, device="cuda")
+    sda.sda_dsa3d_offsets_bwd(p, Q, f(x["Wc"]), f(x["bc"]), f(x["Wl"]), f(x["d_offsets"]), dQn, *gW, ws)
+    torch.cuda.synchronize()
+    assert sda.sda_get_device_status() == sda.SDA_OK
+    tt, rr = torch.from_numpy(toks).cuda(), torch.from_numpy(rows).cuda()
+    dQ_s, doff_s = host(dQ[:, tt]), host(doff[:, tt])
+    dK_r, dV_r = host(dK[:, rr]), host(dV[:, rr])
+    dQn_s = host(dQn[:, tt, :1])
+    gW = [host(g[:1]) for g in gW]
+    del Q, K, V, dO, off, O, LSE, dQ, dK, dV, doff, dQn, ws
+    torch.cuda.empty_cache()
+    rel = 5e-4
+    ref = rec.oracle(D.dsa3d_bwd, x["Q"], x["K"], x["V"], x["offsets"], x["dO"], wl.T, wl.H, wl.W, wl.kt, wl.kh,
+                     wl.kw, tokens=toks)
+    _fp32_record(rec, "dQ", dQ_s, ref[0], rel)
+    _fp32_record(rec, "d_offsets", doff_s, ref[3], rel)
+    for hi, h in enumerate((0, wl.heads - 1)):
+        xs = {n: x[n][:, :, h:h + 1] for n in ("Q", "K", "V", "dO", "offsets")}
+        near = reaching_tokens(rows, xs["offsets"], wl.T, wl.H, wl.W, wl.kt, wl.kh, wl.kw)
+        rk = rec.oracle(D.dsa3d_bwd, xs["Q"], xs["K"], xs["V"], xs["offsets"], xs["dO"], wl.T, wl.H, wl.W, wl.kt,
+                        wl.kh, wl.kw, tokens=near, rows=rows)
+        _fp32_record(rec, "dK", dK_r[:, :, h:h + 1], rk[1], rel)
+        _fp32_record(rec, "dV", dV_r[:, :, h:h + 1], rk[2], rel)
+    rn = rec.oracle(D.dsa3d_offsets_bwd, x["Q"][:, :, :1], x["Wc"][:1], x["bc"][:1], x["Wl"][:1], None,
+                    x["d_offsets"][:, :, :1], wl.T, wl.H, wl.W)
+    _fp32_record(rec, "offset network dQ", dQn_s, rn[0][:, toks], rel)
+    for name, g, r in zip(("dWc", "dbc", "dWl", "dbl"), gW, rn[1:]):
+        _fp32_record(rec, name, g, r, rel)

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 from oracle import dsa3d_oracle as D
+from tests.parity_util import reaching_tokens
 
 pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
 
@@ -276,3 +277,26 @@ def test_offset_network_backward_matches_torch_autograd():
     for name, got, ref in (("dQ", dQ, tQ.grad), ("dWc", dWc, tWc.grad), ("dbc", dbc, tbc.grad),
                            ("dWl", dWl, tWl.grad), ("dbl", dbl, tbl.grad)):
         np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-9, err_msg=name)
+
+
+def test_backward_of_a_token_subset_matches_all_tokens():
+    """The subset mode only selects: dQ and d_offsets of the chosen tokens are the full call's rows, and dK, dV
+    of chosen rows are the full call's when every token that reaches them is selected, and less when not."""
+    rng = np.random.default_rng(14)
+    T, H, W, Hh, d = 6, 9, 14, 2, 4
+    N = T * H * W
+    Q, K, V, dO = (rng.standard_normal((2, N, Hh, d)) for _ in range(4))
+    off = rng.normal(0, 0.4, size=(2, N, Hh, 27, 3))
+    full = D.dsa3d_bwd(Q, K, V, off, dO, T, H, W, 3, 3, 3)
+    toks = np.sort(rng.choice(N, 37, replace=False))
+    sub = D.dsa3d_bwd(Q, K, V, off, dO, T, H, W, 3, 3, 3, tokens=toks)
+    np.testing.assert_allclose(sub[0], full[0][:, toks], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(sub[3], full[3][:, toks], rtol=0, atol=1e-12)
+    rows = np.array([0, 417, N - 1])
+    near = reaching_tokens(rows, off, T, H, W, 3, 3, 3)
+    assert len(near) < N
+    part = D.dsa3d_bwd(Q, K, V, off, dO, T, H, W, 3, 3, 3, tokens=near, rows=rows)
+    np.testing.assert_allclose(part[1], full[1][:, rows], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(part[2], full[2][:, rows], rtol=0, atol=1e-12)
+    few = D.dsa3d_bwd(Q, K, V, off, dO, T, H, W, 3, 3, 3, tokens=near[::2], rows=rows)
+    assert np.abs(few[2] - full[2][:, rows]).max() > 1e-3  # half the reaching tokens miss part of dV
