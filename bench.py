@@ -80,7 +80,7 @@ def dsa3d_fractions(dsa, hbm_peak, sm_mhz):
     """Fractions for the 3D-DSA kernels: of the measured HBM peak, and of the FP32 peak derived from the unit
     counts (152 SMs x 128 FP32 lanes x 2 FLOP per FMA) at the clock sampled during the run."""
     fp32_peak = 152 * 128 * 2 * (sm_mhz or 1900.0) * 1e6 / 1e12
-    for k in ("offsets", "attention"):
+    for k in ("offsets", "attention", "attention_bwd", "offsets_bwd"):
         dsa[k]["frac_of_hbm_peak"] = dsa[k]["gbs"] / hbm_peak
         dsa[k]["frac_of_fp32_peak"] = dsa[k]["tflops"] / fp32_peak
     dsa["fp32_peak_tflops"] = fp32_peak
@@ -544,6 +544,27 @@ def main():
             torch.cuda.synchronize()
             t_off += de[0].elapsed_time(de[1]) / reps
             t_att += de[1].elapsed_time(de[2]) / reps
+        # the backward of both: attention (dQ, dK, dV, d_offsets), then the offset network (dQ added to, the
+        # weight gradients)
+        adO = torch.randn(dshape, device=dev, generator=g).to(torch.bfloat16)
+        gQ, gK, gV = (torch.empty(dshape, dtype=torch.float32, device=dev) for _ in range(3))
+        goff = torch.empty_like(doff)
+        gw = [torch.empty_like(td[n]) for n in ("Wc", "bc", "Wl", "bl")]
+        gws = torch.empty(sda.sda_dsa3d_offsets_bwd_workspace_size(dp), dtype=torch.uint8, device=dev)
+        bws = torch.empty(sda.sda_dsa3d_bwd_workspace_size(dp), dtype=torch.uint8, device=dev)
+        for _ in range(2):
+            sda.sda_dsa3d_bwd(dp, aQ, aK, aV, doff, aL, adO, gQ, gK, gV, goff, bws, stream=stream)
+            sda.sda_dsa3d_offsets_bwd(dp, aQ, td["Wc"], td["bc"], td["Wl"], goff, gQ, *gw, gws, stream=stream)
+        t_abwd = t_obwd = 0.0
+        for _ in range(reps):
+            de[0].record(stream)
+            sda.sda_dsa3d_bwd(dp, aQ, aK, aV, doff, aL, adO, gQ, gK, gV, goff, bws, stream=stream)
+            de[1].record(stream)
+            sda.sda_dsa3d_offsets_bwd(dp, aQ, td["Wc"], td["bc"], td["Wl"], goff, gQ, *gw, gws, stream=stream)
+            de[2].record(stream)
+            torch.cuda.synchronize()
+            t_abwd += de[0].elapsed_time(de[1]) / reps
+            t_obwd += de[1].elapsed_time(de[2]) / reps
         th = float(dw.B * dw.N * dw.heads)  # (token, head) units
         row = 2.0 * dw.d  # bytes of one bf16 row
         # algorithmic work per (token, head): offsets 2 * 27 d + 2 d 3S FLOP, reading the Q row and writing
@@ -551,13 +572,27 @@ def main():
         # Q, K, V rows once (ideal reuse) and the offsets, writing the O row and the LSE
         f_off, b_off = th * (2.0 * 27 * dw.d + 2.0 * dw.d * 3 * dw.S), th * (row + 12.0 * dw.S)
         f_att, b_att = th * 32.0 * dw.d * dw.S, th * (3 * row + 12.0 * dw.S + row + 4.0)
+        # attention backward per window point: 8 corners x (q.K[m], dO.V[m], the dq term, the dK and dV rows)
+        # = 80 d FLOP, reading the Q, K, V, dO rows, the offsets and LSE, writing dQ, dK, dV (fp32) and the
+        # offsets' gradient; offset network backward: the convolution twice forward-sized (Y recomputed, the
+        # transposed one) plus dWc, and the two d x 3S products (dY, dWl), reading the Q row and the offsets'
+        # gradient, updating the fp32 dQ row
+        f_abwd = th * 80.0 * dw.d * dw.S
+        b_abwd = th * (4 * row + 24.0 * dw.S + 4.0 + 12.0 * dw.d)
+        f_obwd = th * (3 * 2.0 * 27 * dw.d + 2 * 2.0 * dw.d * 3 * dw.S)
+        b_obwd = th * (row + 12.0 * dw.S + 8.0 * dw.d)
+        t_all = t_off + t_att + t_abwd + t_obwd
         dsa = {"workload": dw.name, "tokens": dw.N, "heads": dw.heads, "window": [dw.kt, dw.kh, dw.kw],
-               "ms": {"offsets": t_off, "attention": t_att, "total": t_off + t_att},
+               "ms": {"offsets": t_off, "attention": t_att, "total": t_off + t_att, "attention_bwd": t_abwd,
+                      "offsets_bwd": t_obwd, "fwd_bwd_total": t_all},
                "tokens_per_s": dw.B * dw.N / ((t_off + t_att) / 1e3),
+               "tokens_per_s_fwd_bwd": dw.B * dw.N / (t_all / 1e3),
                "offsets": {"tflops": f_off / (t_off / 1e3) / 1e12, "gbs": b_off / (t_off / 1e3) / 1e9},
                "attention": {"tflops": f_att / (t_att / 1e3) / 1e12, "gbs": b_att / (t_att / 1e3) / 1e9},
+               "attention_bwd": {"tflops": f_abwd / (t_abwd / 1e3) / 1e12, "gbs": b_abwd / (t_abwd / 1e3) / 1e9},
+               "offsets_bwd": {"tflops": f_obwd / (t_obwd / 1e3) / 1e12, "gbs": b_obwd / (t_obwd / 1e3) / 1e9},
                "status": sda.status_string(sda.sda_get_device_status(stream))}
-        del aQ, aK, aV, doff, aO, aL, td
+        del aQ, aK, aV, doff, aO, aL, td, adO, gQ, gK, gV, goff, gw, gws, bws
 
     if rank != 0:
         if dist is not None:

@@ -420,17 +420,38 @@ sda_status sda_dsa3d_fwd(const sda_dsa3d_problem* p, const void* Q, const void* 
   return from_cuda(sda::dsa3d_fwd(a, Q, K, V, offsets, O, LSE, static_cast<cudaStream_t>(stream)));
 }
 
-sda_status sda_dsa3d_bwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
-                         const float* offsets, const float* LSE, const void* dO, float* dQ, float* dK, float* dV,
-                         float* d_offsets, void* stream) {
-  sda::Dsa3dArgs a;
+// The window attention's backward buckets its samples with 32-bit indices.
+static sda_status dsa3d_bwd_args(const sda_dsa3d_problem* p, sda::Dsa3dArgs& a) {
   const sda_status st = dsa3d_args(p, a);
   if (st != SDA_OK) return st;
-  if (!Q || !K || !V || !offsets || !LSE || !dO || !dQ || !dK || !dV || !d_offsets) return SDA_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
-      !aligned16(dV))
+  const long long N = (long long)a.T * a.H * a.W;
+  if (N * a.S > 0x7fffffffLL || (long long)(a.T + 1) * (a.H + 1) * (a.W + 1) >= 0x7fffffffLL)
+    return SDA_ERR_UNSUPPORTED;
+  return SDA_OK;
+}
+
+sda_status sda_dsa3d_bwd_workspace_size(const sda_dsa3d_problem* p, size_t* bytes) {
+  sda::Dsa3dArgs a;
+  const sda_status st = dsa3d_bwd_args(p, a);
+  if (st != SDA_OK) return st;
+  if (!bytes) return SDA_ERR_INVALID_ARG;
+  *bytes = sda::dsa3d_bwd_ws_bytes(a);
+  return SDA_OK;
+}
+
+sda_status sda_dsa3d_bwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
+                         const float* offsets, const float* LSE, const void* dO, float* dQ, float* dK, float* dV,
+                         float* d_offsets, void* ws, size_t ws_bytes, void* stream) {
+  sda::Dsa3dArgs a;
+  const sda_status st = dsa3d_bwd_args(p, a);
+  if (st != SDA_OK) return st;
+  if (!Q || !K || !V || !offsets || !LSE || !dO || !dQ || !dK || !dV || !d_offsets || !ws)
     return SDA_ERR_INVALID_ARG;
-  return from_cuda(sda::dsa3d_bwd(a, Q, K, V, offsets, LSE, dO, dQ, dK, dV, d_offsets,
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
+      !aligned16(dV) || !aligned16(ws))
+    return SDA_ERR_INVALID_ARG;
+  if (ws_bytes < sda::dsa3d_bwd_ws_bytes(a)) return SDA_ERR_WORKSPACE;
+  return from_cuda(sda::dsa3d_bwd(a, Q, K, V, offsets, LSE, dO, dQ, dK, dV, d_offsets, ws,
                                   static_cast<cudaStream_t>(stream)));
 }
 

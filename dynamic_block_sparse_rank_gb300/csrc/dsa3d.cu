@@ -290,14 +290,78 @@ __global__ void __launch_bounds__(kDsaThreads) dsa3d_fwd_kernel(const __nv_bfloa
   }
 }
 
-// Backward of the window attention (dLSE = 0).  The same warp layout as the forward.  Pass 1
-// recomputes every window point's logit and P_s = exp(a_s - LSE) (the forward's LSE) and
-// dP_s = dO . v~_s, keeping both in shared memory, and sums D = sum_s P_s dP_s; pass 2 gathers
-// the corners again and, with da_s = P_s (dP_s - D), accumulates dq = scale sum_s da_s k~_s,
-// adds w_c scale da_s q to dK and w_c P_s dO to dV at every corner row (fp32 vector atomics:
-// the corner rows of neighbouring tokens overlap), and forms the offset gradient from the
-// weights' derivatives, sum_c dw_c (scale da_s q.K_c + P_s dO.V_c).
-constexpr int kMaxS = 125;
+// Floor cell, fractional position and per-axis inside flags of a sample position (token units).
+// Every test is in float: a NaN position fails them all, and no index is formed from it.
+struct SampleCell {
+  float f[3];
+  bool v0[3], v1[3];  // the lower / upper corner on that axis is inside the raster
+  int ib[3];          // the floor, clamped to -1 .. size - 1
+  int cell;           // index among cell_entries(), -1 when no corner is inside
+};
+
+// Cells of one (batch entry, head): the (T+1) x (H+1) x (W+1) floor positions -1 .. T-1 etc.,
+// plus one entry for the total.
+__host__ __device__ inline long long cell_entries(const Dsa3dArgs& a) {
+  return (long long)(a.T + 1) * (a.H + 1) * (a.W + 1) + 1;
+}
+
+__device__ __forceinline__ SampleCell sample_cell(const float (&pc)[3], const Dsa3dArgs& a) {
+  SampleCell c;
+  const float mx[3] = {(float)(a.T - 1), (float)(a.H - 1), (float)(a.W - 1)};
+#pragma unroll
+  for (int ax = 0; ax < 3; ++ax) {
+    const float bse = floorf(pc[ax]);
+    c.f[ax] = pc[ax] - bse;
+    c.v0[ax] = bse >= 0.f && bse <= mx[ax];
+    c.v1[ax] = bse >= -1.f && bse <= mx[ax] - 1.f;
+    c.ib[ax] = (int)fminf(fmaxf(bse, -1.f), mx[ax]);
+  }
+  const bool any = (c.v0[0] || c.v1[0]) && (c.v0[1] || c.v1[1]) && (c.v0[2] || c.v1[2]);
+  c.cell = any ? ((c.ib[0] + 1) * (a.H + 1) + c.ib[1] + 1) * (a.W + 1) + c.ib[2] + 1 : -1;
+  return c;
+}
+
+// Backward of the window attention (dLSE = 0), per token, in one gather of the corners.  The
+// same warp layout as the forward.  For every window point the corners' K and V rows give the
+// logit q.k~_s (so P_s = exp(a_s - LSE), the forward's LSE), dP_s = dO.v~_s, k~_s itself, and
+// the weights' derivatives applied to q.K_c and dO.V_c per axis (GK_s, GV_s).  Everything that
+// needs D = sum_s P_s dP_s is linear in it: with da_s = P_s (dP_s - D),
+//   dq = scale sum_s da_s k~_s = scale (sum_s P_s dP_s k~_s - D sum_s P_s k~_s)
+// (two register accumulators), and the offset gradient scale da_s GK_s + P_s GV_s is formed
+// after the loop from (P_s, dP_s, GK_s, GV_s) kept in shared memory, one sample per lane.  dK
+// and dV are not scattered from here: every sample's coefficients (scale da_s, P_s) go to
+// `coef`, and the sample is counted in the cell of the grid that holds its floor position
+// (cells -1 .. T-1 per axis, so that every cell with a corner inside the raster has one), for
+// dsa3d_dkdv_kernel to gather.
+constexpr int kSampleWords = 9;  // P, dP, GK[3], GV[3], cell
+
+// token slots of a CTA (8 warps x 256 / D tokens side by side) x S samples x kSampleWords
+__host__ __device__ constexpr size_t bwd_smem_bytes(int D, int S) {
+  return (size_t)(kDsaThreads / 32) * (256 / D) * S * kSampleWords * 4;
+}
+
+// Sums 8 values over the LPT lanes of a token group by halving: after it lane sl holds the
+// total of value sl / (LPT / 8) (8 shuffles for LPT = 16, 7 for LPT = 8, instead of 8 full
+// reductions).
+template <int LPT>
+__device__ __forceinline__ float reduce8(const float (&v)[8], int sl) {
+  const bool hA = sl & (LPT / 2), hB = sl & (LPT / 4), hC = sl & (LPT / 8);
+  float a[4], b2[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = hA ? v[i] : v[i + 4], keep = hA ? v[i + 4] : v[i];
+    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, LPT / 2);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = hB ? a[i] : a[i + 2], keep = hB ? a[i + 2] : a[i];
+    b2[i] = keep + __shfl_xor_sync(0xffffffffu, send, LPT / 4);
+  }
+  float c = (hC ? b2[1] : b2[0]) + __shfl_xor_sync(0xffffffffu, hC ? b2[0] : b2[1], LPT / 8);
+#pragma unroll
+  for (int o = LPT / 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  return c;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kDsaThreads, 2) dsa3d_bwd_kernel(const __nv_bfloat16* __restrict__ Q,
@@ -306,15 +370,16 @@ __global__ void __launch_bounds__(kDsaThreads, 2) dsa3d_bwd_kernel(const __nv_bf
                                                                const float* __restrict__ off,
                                                                const float* __restrict__ LSE,
                                                                const __nv_bfloat16* __restrict__ dO,
-                                                               float* __restrict__ dQ, float* __restrict__ dK,
-                                                               float* __restrict__ dV, float* __restrict__ doff,
+                                                               float* __restrict__ dQ, float2* __restrict__ coef,
+                                                               int* __restrict__ count, float* __restrict__ doff,
                                                                Dsa3dArgs a) {
   constexpr int LPT = D / 8;
   constexpr int TPW = 32 / LPT;
   constexpr int kWarps = kDsaThreads / 32;
   constexpr int kPerWarp = kDsaTok / kWarps;
+  constexpr int kSub = LPT / 8;  // lanes holding the same reduced value
   constexpr float kLog2e = 1.4426950408889634f;
-  __shared__ float2 pdp[kWarps][TPW][kMaxS];  // (P_s, dP_s) per token slot
+  extern __shared__ float bsm[];  // [kWarps * TPW token slots][S][kSampleWords]
   const int h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int slot = lane / LPT, sl = lane % LPT;
@@ -322,19 +387,14 @@ __global__ void __launch_bounds__(kDsaThreads, 2) dsa3d_bwd_kernel(const __nv_bf
   const long long rs = (long long)a.heads * D;
   const long long hb = (long long)b * N * rs + (long long)h * D + sl * 8;  // this head's lane offset, batch b
   const int rt = (a.kt - 1) / 2, rh = (a.kh - 1) / 2, rw = (a.kw - 1) / 2;
-  const float Tm = (float)(a.T - 1), Hm = (float)(a.H - 1), Wm = (float)(a.W - 1);
   const int HW = a.H * a.W;
+  float* rec = bsm + (size_t)(warp * TPW + slot) * a.S * kSampleWords;
   auto load8 = [&](const __nv_bfloat16* p, float2 (&v)[4]) {
     const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
     v[0] = bf16x2_to_f2(u.x);
     v[1] = bf16x2_to_f2(u.y);
     v[2] = bf16x2_to_f2(u.z);
     v[3] = bf16x2_to_f2(u.w);
-  };
-  auto group_sum = [&](float x) {
-#pragma unroll
-    for (int sh = LPT / 2; sh > 0; sh >>= 1) x += __shfl_xor_sync(0xffffffffu, x, sh);
-    return x;
   };
   for (int u = 0; u < kPerWarp; u += TPW) {
     const int n_raw = blockIdx.x * kDsaTok + warp * kPerWarp + u + slot;
@@ -347,134 +407,251 @@ __global__ void __launch_bounds__(kDsaThreads, 2) dsa3d_bwd_kernel(const __nv_bf
     load8(dO + hb + (long long)n * rs, g);
     const float lse2 = LSE[((long long)b * a.heads + h) * N + n] * kLog2e;
     const float sl2 = a.scale * kLog2e;
-    const float* offn = off + (((long long)b * N + n) * a.heads + h) * (3LL * a.S);
-    // corners of window point s: base index, per-axis weights and inside flags
-    struct Pt {
-      int m000;
-      float f[3];
-      bool v0[3], v1[3];
-    };
-    auto point = [&](int s, int wa, int wb, int wc) {
-      Pt P;
-      const float pc[3] = {(float)(t + wa - rt) + __ldg(offn + 3 * s), (float)(y + wb - rh) + __ldg(offn + 3 * s + 1),
-                           (float)(x + wc - rw) + __ldg(offn + 3 * s + 2)};
-      const float mx[3] = {Tm, Hm, Wm};
-      int ib[3];
+    const long long ns = ((long long)b * N + n) * a.heads + h;
+    const float* offn = off + ns * (3LL * a.S);
+    float2 acc_pd[4], acc_p[4];  // sum_s P_s dP_s k~_s, sum_s P_s k~_s (this lane's 8 channels)
 #pragma unroll
-      for (int ax = 0; ax < 3; ++ax) {
-        const float bse = floorf(pc[ax]);
-        P.f[ax] = pc[ax] - bse;
-        P.v0[ax] = bse >= 0.f && bse <= mx[ax];  // tested in float: NaN fails, no index is formed
-        P.v1[ax] = bse >= -1.f && bse <= mx[ax] - 1.f;
-        ib[ax] = (int)fminf(fmaxf(bse, -1.f), mx[ax]);
-      }
-      P.m000 = (ib[0] * a.H + ib[1]) * a.W + ib[2];
-      return P;
-    };
-    // pass 1: P_s, dP_s and D
+    for (int i = 0; i < 4; ++i) acc_pd[i] = acc_p[i] = make_float2(0.f, 0.f);
     float Dsum = 0.f;
-    {
-      int s = 0;
-      for (int wa = 0; wa < a.kt; ++wa)
-        for (int wb = 0; wb < a.kh; ++wb)
-          for (int wc = 0; wc < a.kw; ++wc, ++s) {
-            const Pt P = point(s, wa, wb, wc);
-            float dq = 0.f, dv = 0.f;
-#pragma unroll
-            for (int corner = 0; corner < 8; ++corner) {
-              const int ct = corner >> 2, ch = (corner >> 1) & 1, cw = corner & 1;
-              const bool in = (ct ? P.v1[0] : P.v0[0]) && (ch ? P.v1[1] : P.v0[1]) && (cw ? P.v1[2] : P.v0[2]);
-              const float w = (ct ? P.f[0] : 1.f - P.f[0]) * (ch ? P.f[1] : 1.f - P.f[1]) * (cw ? P.f[2] : 1.f - P.f[2]);
-              if (!in || w == 0.f) continue;
-              const long long row = (long long)(P.m000 + ct * HW + ch * a.W + cw) * rs;
-              float2 kv[4], vv[4];
-              load8(K + hb + row, kv);
-              load8(V + hb + row, vv);
-              float2 pq = make_float2(0.f, 0.f), pv = make_float2(0.f, 0.f);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                pq = ffma2(q[i], kv[i], pq);
-                pv = ffma2(g[i], vv[i], pv);
-              }
-              dq = fmaf(w, pq.x + pq.y, dq);
-              dv = fmaf(w, pv.x + pv.y, dv);
-            }
-            dq = group_sum(dq);
-            dv = group_sum(dv);
-            const float Ps = exp2f(fmaf(dq, sl2, -lse2));
-            if (sl == 0) pdp[warp][slot][s] = make_float2(Ps, dv);
-            Dsum = fmaf(Ps, dv, Dsum);
-          }
-    }
-    __syncwarp();
-    // pass 2: gradients
-    float2 dqa[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dqa[i] = make_float2(0.f, 0.f);
     int s = 0;
     for (int wa = 0; wa < a.kt; ++wa)
       for (int wb = 0; wb < a.kh; ++wb)
         for (int wc = 0; wc < a.kw; ++wc, ++s) {
-          const float2 pd = pdp[warp][slot][s];
-          const float Ps = pd.x, da = Ps * (pd.y - Dsum);
-          const float sda = a.scale * da;
-          const Pt P = point(s, wa, wb, wc);
-          float go[3] = {0.f, 0.f, 0.f};
+          const float pc[3] = {(float)(t + wa - rt) + __ldg(offn + 3 * s),
+                               (float)(y + wb - rh) + __ldg(offn + 3 * s + 1),
+                               (float)(x + wc - rw) + __ldg(offn + 3 * s + 2)};
+          const SampleCell c = sample_cell(pc, a);
+          const int m000 = (c.ib[0] * a.H + c.ib[1]) * a.W + c.ib[2];
+          float2 ks[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ks[i] = make_float2(0.f, 0.f);
+          // partial sums over this lane's channels: w q.K, w dO.V, then dw/dpos q.K and dw/dpos dO.V per axis
+          float v8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int corner = 0; corner < 8; ++corner) {
             const int ct = corner >> 2, ch = (corner >> 1) & 1, cw = corner & 1;
-            const bool in = (ct ? P.v1[0] : P.v0[0]) && (ch ? P.v1[1] : P.v0[1]) && (cw ? P.v1[2] : P.v0[2]);
+            const bool in = (ct ? c.v1[0] : c.v0[0]) && (ch ? c.v1[1] : c.v0[1]) && (cw ? c.v1[2] : c.v0[2]);
             if (!in) continue;
-            const float wt = ct ? P.f[0] : 1.f - P.f[0], wh = ch ? P.f[1] : 1.f - P.f[1],
-                        ww = cw ? P.f[2] : 1.f - P.f[2];
-            const long long row = (long long)(P.m000 + ct * HW + ch * a.W + cw) * rs;
+            const float wt = ct ? c.f[0] : 1.f - c.f[0], wh = ch ? c.f[1] : 1.f - c.f[1],
+                        ww = cw ? c.f[2] : 1.f - c.f[2];
+            const float w = wt * wh * ww;
+            const long long row = (long long)(m000 + ct * HW + ch * a.W + cw) * rs;
             float2 kv[4], vv[4];
             load8(K + hb + row, kv);
             load8(V + hb + row, vv);
             float2 pq = make_float2(0.f, 0.f), pv = make_float2(0.f, 0.f);
+            const float2 w2 = make_float2(w, w);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               pq = ffma2(q[i], kv[i], pq);
               pv = ffma2(g[i], vv[i], pv);
+              ks[i] = ffma2(w2, kv[i], ks[i]);
             }
-            // derivative of this corner's weight along t, h, w times its share of the loss
-            const float c = fmaf(sda, pq.x + pq.y, Ps * (pv.x + pv.y));
-            go[0] = fmaf((ct ? 1.f : -1.f) * wh * ww, c, go[0]);
-            go[1] = fmaf((ch ? 1.f : -1.f) * wt * ww, c, go[1]);
-            go[2] = fmaf((cw ? 1.f : -1.f) * wt * wh, c, go[2]);
-            const float w = wt * wh * ww;
-            if (w == 0.f) continue;
-            const float2 wk = make_float2(w * sda, w * sda), wv = make_float2(w * Ps, w * Ps);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dqa[i] = ffma2(wk, kv[i], dqa[i]);
-            if (valid) {
-              float* dkr = dK + hb + row;
-              float* dvr = dV + hb + row;
-              atomicAdd(reinterpret_cast<float4*>(dkr),
-                        make_float4(wk.x * q[0].x, wk.x * q[0].y, wk.x * q[1].x, wk.x * q[1].y));
-              atomicAdd(reinterpret_cast<float4*>(dkr + 4),
-                        make_float4(wk.x * q[2].x, wk.x * q[2].y, wk.x * q[3].x, wk.x * q[3].y));
-              atomicAdd(reinterpret_cast<float4*>(dvr),
-                        make_float4(wv.x * g[0].x, wv.x * g[0].y, wv.x * g[1].x, wv.x * g[1].y));
-              atomicAdd(reinterpret_cast<float4*>(dvr + 4),
-                        make_float4(wv.x * g[2].x, wv.x * g[2].y, wv.x * g[3].x, wv.x * g[3].y));
-            }
+            const float pqs = pq.x + pq.y, pvs = pv.x + pv.y;
+            const float dt = (ct ? 1.f : -1.f) * wh * ww, dh = (ch ? 1.f : -1.f) * wt * ww,
+                        dw = (cw ? 1.f : -1.f) * wt * wh;
+            v8[0] = fmaf(w, pqs, v8[0]);
+            v8[1] = fmaf(w, pvs, v8[1]);
+            v8[2] = fmaf(dt, pqs, v8[2]);
+            v8[3] = fmaf(dh, pqs, v8[3]);
+            v8[4] = fmaf(dw, pqs, v8[4]);
+            v8[5] = fmaf(dt, pvs, v8[5]);
+            v8[6] = fmaf(dh, pvs, v8[6]);
+            v8[7] = fmaf(dw, pvs, v8[7]);
           }
+          const float r = reduce8<LPT>(v8, sl);  // total of value sl / kSub
+          const float logit = __shfl_sync(0xffffffffu, r, slot * LPT);
+          const float dP = __shfl_sync(0xffffffffu, r, slot * LPT + kSub);
+          const float Ps = exp2f(fmaf(logit, sl2, -lse2));
+          const float pd = Ps * dP;
+          Dsum += pd;
+          const float2 pd2 = make_float2(pd, pd), p2 = make_float2(Ps, Ps);
 #pragma unroll
-          for (int ax = 0; ax < 3; ++ax) go[ax] = group_sum(go[ax]);
-          if (valid && sl == 0) {
-            float* o = doff + (((long long)b * N + n) * a.heads + h) * (3LL * a.S) + 3 * s;
-            o[0] = go[0];
-            o[1] = go[1];
-            o[2] = go[2];
+          for (int i = 0; i < 4; ++i) {
+            acc_pd[i] = ffma2(pd2, ks[i], acc_pd[i]);
+            acc_p[i] = ffma2(p2, ks[i], acc_p[i]);
+          }
+          if (sl % kSub == 0) {
+            const int k = sl / kSub;
+            float* rs9 = rec + s * kSampleWords;
+            rs9[k] = k == 0 ? Ps : r;  // P, dP, GK[3], GV[3]
+            if (k == 0) rs9[8] = __int_as_float(c.cell);
           }
         }
-    if (valid) {
-      float* dqr = dQ + hb + (long long)n * rs;
-      reinterpret_cast<float4*>(dqr)[0] = make_float4(dqa[0].x, dqa[0].y, dqa[1].x, dqa[1].y);
-      reinterpret_cast<float4*>(dqr)[1] = make_float4(dqa[2].x, dqa[2].y, dqa[3].x, dqa[3].y);
-    }
     __syncwarp();
+    if (valid) {
+      float4 o[2];
+      float* of = reinterpret_cast<float*>(o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        of[2 * i] = a.scale * fmaf(-Dsum, acc_p[i].x, acc_pd[i].x);
+        of[2 * i + 1] = a.scale * fmaf(-Dsum, acc_p[i].y, acc_pd[i].y);
+      }
+      float4* dqr = reinterpret_cast<float4*>(dQ + hb + (long long)n * rs);
+      dqr[0] = o[0];
+      dqr[1] = o[1];
+      // per sample, one lane each: the offset gradient, the coefficients, the cell count
+      for (int s2 = sl; s2 < a.S; s2 += LPT) {
+        const float* rs9 = rec + s2 * kSampleWords;
+        const float Ps = rs9[0], sda = a.scale * Ps * (rs9[1] - Dsum);
+        float* od = doff + ns * (3LL * a.S) + 3 * s2;
+        od[0] = fmaf(sda, rs9[2], Ps * rs9[5]);
+        od[1] = fmaf(sda, rs9[3], Ps * rs9[6]);
+        od[2] = fmaf(sda, rs9[4], Ps * rs9[7]);
+        coef[ns * a.S + s2] = make_float2(sda, Ps);
+        const int cell = __float_as_int(rs9[8]);
+        if (cell >= 0) atomicAdd(count + ((long long)b * a.heads + h) * cell_entries(a) + cell, 1);
+      }
+    }
+    __syncwarp();  // the records are rewritten by the next token
+  }
+}
+
+// ---- dK and dV of the window attention, gathered per row: the samples counted per cell by
+// dsa3d_bwd_kernel are bucketed by cell (an exclusive scan of the counts, then a fill), and a
+// row m = (t, y, x) sums the contributions of the samples in the 8 cells (t, y, x) - {0, 1}^3,
+// whose corner it is: dK[m] = sum w scale da q_n, dV[m] = sum w P dO_n, w the sample's
+// trilinear weight at m.  Every row is written once, by one thread group: no atomics on rows.
+
+// Exclusive prefix sum of one (batch entry, head)'s cell counts, in place: count[e] becomes the
+// first record of cell e (count[E] the total), copied to cursor for the fill.  One CTA per
+// (batch entry, head), 4,096 entries a round.
+__global__ void __launch_bounds__(1024) dsa3d_cell_scan_kernel(int* __restrict__ count, int* __restrict__ cursor,
+                                                               long long ncell) {
+  __shared__ int wsum[32];
+  int* c = count + blockIdx.x * ncell;
+  int* cur = cursor + blockIdx.x * ncell;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int carry = 0;
+  for (long long base = 0; base < ncell; base += 4096) {
+    const long long i0 = base + 4LL * tid;
+    int v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = i0 + k < ncell ? c[i0 + k] : 0;
+    const int tsum = v[0] + v[1] + v[2] + v[3];
+    int x = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = wsum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      wsum[lane] = w;
+    }
+    __syncthreads();
+    int e = carry + (warp ? wsum[warp - 1] : 0) + x - tsum;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (i0 + k < ncell) {
+        c[i0 + k] = e;
+        cur[i0 + k] = e;
+      }
+      e += v[k];
+    }
+    carry += wsum[31];
+    __syncthreads();  // wsum is rewritten next round
+  }
+}
+
+// One thread per (token, window point): the sample's floor cell and fractional position,
+// computed as dsa3d_bwd_kernel computes them (sample_cell), and its record written at the next
+// free place of its cell: (token, f_t, f_h, f_w) and (scale da, P).
+__global__ void __launch_bounds__(kDsaThreads) dsa3d_cell_fill_kernel(const float* __restrict__ off,
+                                                                     const float2* __restrict__ coef,
+                                                                     int* __restrict__ cursor,
+                                                                     int4* __restrict__ rec,
+                                                                     float2* __restrict__ rcoef, Dsa3dArgs a) {
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int N = a.T * a.H * a.W;
+  const long long NS = (long long)N * a.S;
+  const long long idx = (long long)blockIdx.x * kDsaThreads + threadIdx.x;
+  if (idx >= NS) return;
+  const int n = (int)(idx / a.S), s = (int)(idx % a.S);
+  int t, y, x;
+  raster_coords(n, a.H, a.W, t, y, x);
+  const int wa = s / (a.kh * a.kw), wb = (s / a.kw) % a.kh, wc = s % a.kw;
+  const long long ns = ((long long)b * N + n) * a.heads + h;
+  const float* o = off + ns * (3LL * a.S) + 3 * s;
+  const float pc[3] = {(float)(t + wa - (a.kt - 1) / 2) + __ldg(o), (float)(y + wb - (a.kh - 1) / 2) + __ldg(o + 1),
+                       (float)(x + wc - (a.kw - 1) / 2) + __ldg(o + 2)};
+  const SampleCell c = sample_cell(pc, a);
+  if (c.cell < 0) return;
+  const long long bh = (long long)b * a.heads + h;
+  const int slot = atomicAdd(cursor + bh * cell_entries(a) + c.cell, 1);
+  if (slot >= NS) return;  // only if this count disagreed with dsa3d_bwd_kernel's: never write past the records
+  rec[bh * NS + slot] = make_int4(n, __float_as_int(c.f[0]), __float_as_int(c.f[1]), __float_as_int(c.f[2]));
+  rcoef[bh * NS + slot] = __ldg(coef + ns * a.S + s);
+}
+
+// dK, dV rows gathered from the bucketed records, in the forward's warp layout (a row split
+// over D / 8 lanes of 16 bytes, 256 / D rows per warp side by side).
+template <int D>
+__global__ void __launch_bounds__(kDsaThreads) dsa3d_dkdv_kernel(const __nv_bfloat16* __restrict__ Q,
+                                                                const __nv_bfloat16* __restrict__ dO,
+                                                                const int* __restrict__ start,
+                                                                const int4* __restrict__ rec,
+                                                                const float2* __restrict__ rcoef,
+                                                                float* __restrict__ dK, float* __restrict__ dV,
+                                                                Dsa3dArgs a) {
+  constexpr int LPT = D / 8;
+  constexpr int TPW = 32 / LPT;
+  constexpr int kWarps = kDsaThreads / 32;
+  constexpr int kPerWarp = kDsaTok / kWarps;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slot = lane / LPT, sl = lane % LPT;
+  const int N = a.T * a.H * a.W;
+  const long long rs = (long long)a.heads * D;
+  const long long hb = (long long)b * N * rs + (long long)h * D + sl * 8;
+  const long long bh = (long long)b * a.heads + h;
+  const int* st = start + bh * cell_entries(a);
+  const int4* rc = rec + bh * ((long long)N * a.S);
+  const float2* cf = rcoef + bh * ((long long)N * a.S);
+  for (int u = 0; u < kPerWarp; u += TPW) {
+    const int m = blockIdx.x * kDsaTok + warp * kPerWarp + u + slot;
+    if (m >= N) continue;  // no shuffles below: a group may leave alone
+    int t, y, x;
+    raster_coords(m, a.H, a.W, t, y, x);
+    float2 ak[4], av[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ak[i] = av[i] = make_float2(0.f, 0.f);
+#pragma unroll 1
+    for (int corner = 0; corner < 8; ++corner) {
+      const int ct = corner >> 2, ch = (corner >> 1) & 1, cw = corner & 1;
+      const int cell = ((t - ct + 1) * (a.H + 1) + y - ch + 1) * (a.W + 1) + x - cw + 1;
+      const int i1 = __ldg(st + cell + 1);
+      for (int i = __ldg(st + cell); i < i1; ++i) {
+        const int4 r = __ldg(rc + i);
+        const float2 c = __ldg(cf + i);
+        const float f0 = __int_as_float(r.y), f1 = __int_as_float(r.z), f2 = __int_as_float(r.w);
+        const float w = (ct ? f0 : 1.f - f0) * (ch ? f1 : 1.f - f1) * (cw ? f2 : 1.f - f2);
+        const uint4 qu = __ldg(reinterpret_cast<const uint4*>(Q + hb + (long long)r.x * rs));
+        const uint4 gu = __ldg(reinterpret_cast<const uint4*>(dO + hb + (long long)r.x * rs));
+        const float2 wk = make_float2(w * c.x, w * c.x), wv = make_float2(w * c.y, w * c.y);
+        ak[0] = ffma2(wk, bf16x2_to_f2(qu.x), ak[0]);
+        ak[1] = ffma2(wk, bf16x2_to_f2(qu.y), ak[1]);
+        ak[2] = ffma2(wk, bf16x2_to_f2(qu.z), ak[2]);
+        ak[3] = ffma2(wk, bf16x2_to_f2(qu.w), ak[3]);
+        av[0] = ffma2(wv, bf16x2_to_f2(gu.x), av[0]);
+        av[1] = ffma2(wv, bf16x2_to_f2(gu.y), av[1]);
+        av[2] = ffma2(wv, bf16x2_to_f2(gu.z), av[2]);
+        av[3] = ffma2(wv, bf16x2_to_f2(gu.w), av[3]);
+      }
+    }
+    float* dkr = dK + hb + (long long)m * rs;
+    float* dvr = dV + hb + (long long)m * rs;
+    reinterpret_cast<float4*>(dkr)[0] = make_float4(ak[0].x, ak[0].y, ak[1].x, ak[1].y);
+    reinterpret_cast<float4*>(dkr)[1] = make_float4(ak[2].x, ak[2].y, ak[3].x, ak[3].y);
+    reinterpret_cast<float4*>(dvr)[0] = make_float4(av[0].x, av[0].y, av[1].x, av[1].y);
+    reinterpret_cast<float4*>(dvr)[1] = make_float4(av[2].x, av[2].y, av[3].x, av[3].y);
   }
 }
 
@@ -714,18 +891,62 @@ cudaError_t launch_dsa3d(const Dsa3dArgs& a, const __nv_bfloat16* Q, const __nv_
   return cudaGetLastError();
 }
 
+// Workspace of the window attention's backward: per (batch entry, head) the samples'
+// coefficients in token order, their records and coefficients in cell order, the cell starts
+// and the fill cursors; 256-byte aligned pieces.
+struct BwdWs {
+  float2* coef;
+  int4* rec;
+  float2* rcoef;
+  int* count;
+  int* cursor;
+  size_t count_bytes, bytes;
+};
+
+BwdWs bwd_ws_layout(const Dsa3dArgs& a, void* base) {
+  const size_t samples = (size_t)a.B * a.heads * a.T * a.H * a.W * a.S;
+  const size_t cells = (size_t)a.B * a.heads * cell_entries(a);
+  size_t at = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = at;
+    at = (at + bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  const size_t o_coef = take(samples * sizeof(float2)), o_rec = take(samples * sizeof(int4)),
+               o_rcoef = take(samples * sizeof(float2)), o_count = take(cells * sizeof(int)),
+               o_cursor = take(cells * sizeof(int));
+  BwdWs w{};
+  if (char* p = static_cast<char*>(base)) {
+    w.coef = reinterpret_cast<float2*>(p + o_coef);
+    w.rec = reinterpret_cast<int4*>(p + o_rec);
+    w.rcoef = reinterpret_cast<float2*>(p + o_rcoef);
+    w.count = reinterpret_cast<int*>(p + o_count);
+    w.cursor = reinterpret_cast<int*>(p + o_cursor);
+  }
+  w.count_bytes = cells * sizeof(int);
+  w.bytes = at;
+  return w;
+}
+
 template <int D>
 cudaError_t launch_dsa3d_bwd(const Dsa3dArgs& a, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                              const __nv_bfloat16* V, const float* off, const float* LSE, const __nv_bfloat16* dO,
-                             float* dQ, float* dK, float* dV, float* doff, cudaStream_t st) {
+                             float* dQ, float* dK, float* dV, float* doff, void* ws, cudaStream_t st) {
   const long long N = (long long)a.T * a.H * a.W;
-  const size_t bytes = (size_t)a.B * N * a.heads * D * sizeof(float);
+  const BwdWs w = bwd_ws_layout(a, ws);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(dK, 0, bytes, st)) != cudaSuccess) return e;  // accumulated by atomics
-  if ((e = cudaMemsetAsync(dV, 0, bytes, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(w.count, 0, w.count_bytes, st)) != cudaSuccess) return e;
   const dim3 grid((unsigned)((N + kDsaTok - 1) / kDsaTok), a.heads, a.B);
-  dsa3d_bwd_kernel<D><<<grid, kDsaThreads, 0, st>>>(Q, K, V, off, LSE, dO, dQ, dK, dV, doff, a);
-  note_launches(1);
+  const size_t smem = bwd_smem_bytes(D, a.S);
+  if ((e = cudaFuncSetAttribute(dsa3d_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  dsa3d_bwd_kernel<D><<<grid, kDsaThreads, smem, st>>>(Q, K, V, off, LSE, dO, dQ, w.coef, w.count, doff, a);
+  dsa3d_cell_scan_kernel<<<a.B * a.heads, 1024, 0, st>>>(w.count, w.cursor, cell_entries(a));
+  const dim3 fgrid((unsigned)((N * a.S + kDsaThreads - 1) / kDsaThreads), a.heads, a.B);
+  dsa3d_cell_fill_kernel<<<fgrid, kDsaThreads, 0, st>>>(off, w.coef, w.cursor, w.rec, w.rcoef, a);
+  dsa3d_dkdv_kernel<D><<<grid, kDsaThreads, 0, st>>>(Q, dO, w.count, w.rec, w.rcoef, dK, dV, a);
+  note_launches(4);
   return cudaGetLastError();
 }
 
@@ -774,15 +995,17 @@ cudaError_t launch_dsa3d_offsets_bwd(const Dsa3dArgs& a, const __nv_bfloat16* Q,
 }  // namespace
 
 cudaError_t dsa3d_bwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off,
-                      const float* LSE, const void* dO, float* dQ, float* dK, float* dV, float* doff,
+                      const float* LSE, const void* dO, float* dQ, float* dK, float* dV, float* doff, void* ws,
                       cudaStream_t st) {
   const auto* q = static_cast<const __nv_bfloat16*>(Q);
   const auto* k = static_cast<const __nv_bfloat16*>(K);
   const auto* v = static_cast<const __nv_bfloat16*>(V);
   const auto* g = static_cast<const __nv_bfloat16*>(dO);
-  return a.d == 64 ? launch_dsa3d_bwd<64>(a, q, k, v, off, LSE, g, dQ, dK, dV, doff, st)
-                   : launch_dsa3d_bwd<128>(a, q, k, v, off, LSE, g, dQ, dK, dV, doff, st);
+  return a.d == 64 ? launch_dsa3d_bwd<64>(a, q, k, v, off, LSE, g, dQ, dK, dV, doff, ws, st)
+                   : launch_dsa3d_bwd<128>(a, q, k, v, off, LSE, g, dQ, dK, dV, doff, ws, st);
 }
+
+size_t dsa3d_bwd_ws_bytes(const Dsa3dArgs& a) { return bwd_ws_layout(a, nullptr).bytes; }
 
 cudaError_t dsa3d_offsets(const Dsa3dArgs& a, const void* Q, const float* Wc, const float* bc, const float* Wl,
                           const float* bl, float* off, cudaStream_t st) {

@@ -95,8 +95,9 @@ cudaError_t dsa3d_offsets(const Dsa3dArgs& a, const void* Q, const float* Wc, co
 cudaError_t dsa3d_fwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off, void* O,
                       float* LSE, cudaStream_t st);
 cudaError_t dsa3d_bwd(const Dsa3dArgs& a, const void* Q, const void* K, const void* V, const float* off,
-                      const float* LSE, const void* dO, float* dQ, float* dK, float* dV, float* doff,
+                      const float* LSE, const void* dO, float* dQ, float* dK, float* dV, float* doff, void* ws,
                       cudaStream_t st);
+size_t dsa3d_bwd_ws_bytes(const Dsa3dArgs& a);
 cudaError_t dsa3d_offsets_bwd(const Dsa3dArgs& a, const void* Q, const float* Wc, const float* bc, const float* Wl,
                               const float* doff, float* dQ, float* dWc, float* dbc, float* dWl, float* dbl,
                               void* ws, cudaStream_t st);

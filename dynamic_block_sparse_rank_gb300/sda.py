@@ -22,7 +22,7 @@ EXPORTS = ("sda_num_blocks", "sda_workspace_size", "sda_predict_blocks", "sda_at
            "sda_attn_fwd_train", "sda_attn_bwd_train", "sda_predictor_grad",
            "sda_attn_bwd_prepare", "sda_attn_bwd_dq", "sda_attn_bwd_dkdv", "sda_attn_bwd_partition", "sda_merge_states", "sda_merge_states_bwd",
            "sda_get_device_status", "sda_kernel_launch_count", "sda_predict_blocks_noalloc", "sda_selftest_wait_timeout", "sda_status_string",
-           "sda_dsa3d_offsets", "sda_dsa3d_fwd", "sda_dsa3d_bwd", "sda_dsa3d_offsets_bwd_workspace_size",
+           "sda_dsa3d_offsets", "sda_dsa3d_fwd", "sda_dsa3d_bwd", "sda_dsa3d_bwd_workspace_size", "sda_dsa3d_offsets_bwd_workspace_size",
            "sda_dsa3d_offsets_bwd")
 
 
@@ -80,7 +80,8 @@ def lib() -> ctypes.CDLL:
         dp = ctypes.POINTER(Dsa3dProblem)
         L.sda_dsa3d_offsets.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
         L.sda_dsa3d_fwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp]
-        L.sda_dsa3d_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.sda_dsa3d_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.sda_dsa3d_bwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         L.sda_dsa3d_offsets_bwd_workspace_size.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         L.sda_dsa3d_offsets_bwd.argtypes = [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.sda_get_device_status.argtypes = [vp]
@@ -278,9 +279,16 @@ def sda_dsa3d_fwd(p: Dsa3dProblem, Q, K, V, offsets, O, LSE, stream=None):
                                _stream(stream)), "sda_dsa3d_fwd")
 
 
-def sda_dsa3d_bwd(p: Dsa3dProblem, Q, K, V, offsets, LSE, dO, dQ, dK, dV, d_offsets, stream=None):
+def sda_dsa3d_bwd_workspace_size(p: Dsa3dProblem) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().sda_dsa3d_bwd_workspace_size(ctypes.byref(p), ctypes.byref(b)), "sda_dsa3d_bwd_workspace_size")
+    return b.value
+
+
+def sda_dsa3d_bwd(p: Dsa3dProblem, Q, K, V, offsets, LSE, dO, dQ, dK, dV, d_offsets, ws, stream=None):
     _check(lib().sda_dsa3d_bwd(ctypes.byref(p), _ptr(Q), _ptr(K), _ptr(V), _ptr(offsets), _ptr(LSE), _ptr(dO),
-                               _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(d_offsets), _stream(stream)), "sda_dsa3d_bwd")
+                               _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(d_offsets), _ptr(ws), _nbytes(ws),
+                               _stream(stream)), "sda_dsa3d_bwd")
 
 
 def sda_dsa3d_offsets_bwd_workspace_size(p: Dsa3dProblem) -> int:

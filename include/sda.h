@@ -371,6 +371,14 @@ sda_status sda_dsa3d_offsets(const sda_dsa3d_problem* p, const void* Q, const fl
 sda_status sda_dsa3d_fwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
                          const float* offsets, void* O, float* LSE, void* stream);
 
+/* Host only.  Bytes of device workspace that sda_dsa3d_bwd needs: 32 per
+ * sample (B*N*heads*S of them: its two coefficients, in token order and again
+ * in cell order, and a 16-byte record), plus two 4-byte counters per cell of
+ * the (T+1) x (H+1) x (W+1) grid of floor positions and one more, per batch
+ * entry and head.  SDA_ERR_UNSUPPORTED when N*S or the cell count reaches
+ * 2^31. */
+sda_status sda_dsa3d_bwd_workspace_size(const sda_dsa3d_problem* p, size_t* bytes);
+
 /* Gradients of sda_dsa3d_fwd for a loss that reaches it through O (no LSE
  * gradient): with P the window softmax, dP_s = dO.v~_s and
  * da_s = P_s (dP_s - sum_u P_u dP_u),
@@ -382,12 +390,18 @@ sda_status sda_dsa3d_fwd(const sda_dsa3d_problem* p, const void* Q, const void* 
  *               from above on the integer grid, as floor() sees it).
  * Inputs as sda_dsa3d_fwd plus LSE (the forward's, fp32 [B, heads, N]) and dO
  * (bf16 [B, N, heads, d]); outputs fp32: dQ, dK, dV [B, N, heads, d] (16-byte
- * aligned), d_offsets [B, N, heads, S, 3].  dK and dV are cleared by the call
- * and then accumulated with atomics (their last bits depend on the order of
- * the additions); dQ and d_offsets are written.  Errors as sda_dsa3d_fwd. */
+ * aligned), d_offsets [B, N, heads, S, 3]; all are written (not added to).
+ * dK and dV rows are gathered: the samples are bucketed by the cell of their
+ * floor position and each row sums the samples of the 8 cells it is a corner
+ * of, in an order that the bucketing's atomics set (their last bits can vary
+ * between runs).
+ *   ws  device workspace of at least sda_dsa3d_bwd_workspace_size bytes,
+ *       16-byte aligned.
+ * Errors as sda_dsa3d_fwd, plus SDA_ERR_WORKSPACE for a smaller workspace and
+ * the limits of sda_dsa3d_bwd_workspace_size. */
 sda_status sda_dsa3d_bwd(const sda_dsa3d_problem* p, const void* Q, const void* K, const void* V,
                          const float* offsets, const float* LSE, const void* dO, float* dQ, float* dK, float* dV,
-                         float* d_offsets, void* stream);
+                         float* d_offsets, void* ws, size_t ws_bytes, void* stream);
 
 /* Host only.  Bytes of device workspace that sda_dsa3d_offsets_bwd needs:
  * B*N*heads*d*4 (the fp32 gradient of the convolution output Y). */

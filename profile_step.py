@@ -2,14 +2,15 @@
 
     python profile_step.py --workload fwd_61k [--heads 10] [--backward] [--steps 1]
     python profile_step.py --workload merge_131k --merge [--heads 4]
-    python profile_step.py --workload dsa3d_524k --dsa3d [--heads 1]
+    python profile_step.py --workload dsa3d_524k --dsa3d [--heads 1] [--backward]
 
 With --merge it runs the state merge and its gradient instead: the workload's
 partition count of random (O, LSE) states of its shapes, then sda_merge_states
 and sda_merge_states_bwd once per step.  With --dsa3d it runs 3D deformable
 sliding attention on a workload of DSA3D_WORKLOADS: sda_dsa3d_offsets from the
 seeded offset-network weights, then sda_dsa3d_fwd on those offsets (Q, K, V
-drawn N(0,1) on the device).
+drawn N(0,1) on the device); with --backward also sda_dsa3d_bwd (dO drawn
+N(0,1)) and sda_dsa3d_offsets_bwd on the offsets' gradient it returns.
 
 A small driver for inspecting the kernels (e.g. under a profiler) on a chosen
 workload: inputs come from the seeded generator, every step runs all the
@@ -155,17 +156,33 @@ def dsa3d_steps(args):
     p = sda.dsa3d_problem(wl.B, wl.T, wl.H, wl.W, wl.heads, wl.d, wl.kt, wl.kh, wl.kw)
     st = torch.cuda.current_stream()
     times = {"offsets": [], "attention": []}
+    if args.backward:
+        dO = torch.randn(shape, device="cuda", generator=g).to(torch.bfloat16)
+        dQ, dK, dV = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(3))
+        doff = torch.empty_like(off)
+        gw = [torch.empty_like(w[n]) for n in ("Wc", "bc", "Wl", "bl")]
+        ws = torch.empty(sda.sda_dsa3d_offsets_bwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+        bws = torch.empty(sda.sda_dsa3d_bwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+        times.update(attention_bwd=[], offsets_bwd=[])
     for s in range(args.warmup + args.steps):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         ev[0].record(st)
         sda.sda_dsa3d_offsets(p, Q, w["Wc"], w["bc"], w["Wl"], w["bl"], off, st)
         ev[1].record(st)
         sda.sda_dsa3d_fwd(p, Q, K, V, off, O, LSE, st)
         ev[2].record(st)
+        if args.backward:
+            sda.sda_dsa3d_bwd(p, Q, K, V, off, LSE, dO, dQ, dK, dV, doff, bws, st)
+            ev[3].record(st)
+            sda.sda_dsa3d_offsets_bwd(p, Q, w["Wc"], w["bc"], w["Wl"], doff, dQ, *gw, ws, st)
+            ev[4].record(st)
         torch.cuda.synchronize()
         if s >= args.warmup:
             times["offsets"].append(ev[0].elapsed_time(ev[1]))
             times["attention"].append(ev[1].elapsed_time(ev[2]))
+            if args.backward:
+                times["attention_bwd"].append(ev[2].elapsed_time(ev[3]))
+                times["offsets_bwd"].append(ev[3].elapsed_time(ev[4]))
     status = sda.sda_get_device_status()
     print(json.dumps({"workload": wl.name, "heads": wl.heads, "tokens": wl.N, "window": [wl.kt, wl.kh, wl.kw],
                       "ms": {k: statistics.median(v) for k, v in times.items()},

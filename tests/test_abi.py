@@ -249,6 +249,20 @@ def test_dsa3d_backward_host_validation(L):
     assert sda.lib().sda_dsa3d_offsets_bwd(ctypes.byref(p), *(fake,) * 10, fake + 4, need, None) == \
         sda.SDA_ERR_INVALID_ARG  # misaligned workspace
     assert sda.lib().sda_dsa3d_offsets_bwd_workspace_size(ctypes.byref(p), None) == sda.SDA_ERR_INVALID_ARG
-    bw = lambda *ptrs: sda.lib().sda_dsa3d_bwd(ctypes.byref(p), *ptrs, None)
-    assert bw(*(fake,) * 6, fake + 4, *(fake,) * 4) == sda.SDA_ERR_INVALID_ARG  # misaligned dQ
-    assert bw(*(fake,) * 9, None, fake) == sda.SDA_ERR_INVALID_ARG  # no dV
+    samples, cells = 2 * 3 * 120 * 27, 2 * 3 * (5 * 6 * 7 + 1)
+    bneed = sda.sda_dsa3d_bwd_workspace_size(p)
+    assert 32 * samples + 8 * cells <= bneed <= 32 * samples + 8 * cells + 5 * 256
+    def bw(*ptrs, ws=fake, n=bneed):  # Q, K, V, offsets, LSE, dO, dQ, dK, dV, d_offsets; every case fails its checks
+        assert len(ptrs) == 10
+        return sda.lib().sda_dsa3d_bwd(ctypes.byref(p), *ptrs, ws, n, None)
+
+    assert bw(*(fake,) * 6, fake + 4, *(fake,) * 3) == sda.SDA_ERR_INVALID_ARG  # misaligned dQ
+    assert bw(*(fake,) * 8, None, fake) == sda.SDA_ERR_INVALID_ARG  # no dV
+    assert bw(*(fake,) * 10, n=bneed - 1) == sda.SDA_ERR_WORKSPACE
+    assert bw(*(fake,) * 10, ws=fake + 8) == sda.SDA_ERR_INVALID_ARG  # misaligned workspace
+    assert bw(*(fake,) * 10, ws=None) == sda.SDA_ERR_INVALID_ARG
+    big = sda.dsa3d_problem(**{**good, "B": 1, "heads": 1, "d": 64, "T": 100, "H": 1000, "W": 1000})
+    size = ctypes.c_size_t()
+    assert sda.lib().sda_dsa3d_bwd_workspace_size(ctypes.byref(big), ctypes.byref(size)) == \
+        sda.SDA_ERR_UNSUPPORTED  # N S = 2.7e9 samples: past the 32-bit bucket indices
+    assert sda.lib().sda_dsa3d_offsets_bwd_workspace_size(ctypes.byref(big), ctypes.byref(size)) == sda.SDA_OK

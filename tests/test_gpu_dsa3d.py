@@ -164,7 +164,8 @@ def _gpu_bwd(sda, wl, x, offsets):
     shape = (wl.B, wl.N, wl.heads, wl.d)
     dQ, dK, dV = (torch.full(shape, float("nan"), dtype=torch.float32, device="cuda") for _ in range(3))
     doff = torch.full(off.shape, float("nan"), dtype=torch.float32, device="cuda")
-    sda.sda_dsa3d_bwd(p, Q, K, V, off, Lt, dO, dQ, dK, dV, doff)
+    ws = torch.full((sda.sda_dsa3d_bwd_workspace_size(p),), 0xA5, dtype=torch.uint8, device="cuda")  # not zeroed
+    sda.sda_dsa3d_bwd(p, Q, K, V, off, Lt, dO, dQ, dK, dV, doff, ws)
     torch.cuda.synchronize()
     assert sda.sda_get_device_status() == sda.SDA_OK
     del O, L

@@ -458,7 +458,9 @@ def test_dsa3d_524k_backward_sampled(sda, parity_report):
     shape = (wl.B, wl.N, wl.heads, wl.d)
     dQ, dK, dV = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(3))
     doff = torch.empty_like(off)
-    sda.sda_dsa3d_bwd(p, Q, K, V, off, LSE, dO, dQ, dK, dV, doff)
+    bws = torch.empty(sda.sda_dsa3d_bwd_workspace_size(p), dtype=torch.uint8, device="cuda")
+    sda.sda_dsa3d_bwd(p, Q, K, V, off, LSE, dO, dQ, dK, dV, doff, bws)
+    del bws
     dQn = torch.zeros(shape, dtype=torch.float32, device="cuda")
     gW = [torch.empty(x[n].shape, dtype=torch.float32, device="cuda") for n in ("Wc", "bc", "Wl")]
     gW.append(torch.empty((wl.heads, 3 * wl.S), dtype=torch.float32, device="cuda"))
