@@ -364,7 +364,7 @@ __device__ __forceinline__ float reduce8(const float (&v)[8], int sl) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kDsaThreads, 2) dsa3d_bwd_kernel(const __nv_bfloat16* __restrict__ Q,
+__global__ void __launch_bounds__(kDsaThreads, 3) dsa3d_bwd_kernel(const __nv_bfloat16* __restrict__ Q,
                                                                const __nv_bfloat16* __restrict__ K,
                                                                const __nv_bfloat16* __restrict__ V,
                                                                const float* __restrict__ off,
@@ -515,20 +515,36 @@ __global__ void __launch_bounds__(kDsaThreads, 2) dsa3d_bwd_kernel(const __nv_bf
 
 // Exclusive prefix sum of one (batch entry, head)'s cell counts, in place: count[e] becomes the
 // first record of cell e (count[E] the total), copied to cursor for the fill.  One CTA per
-// (batch entry, head), 4,096 entries a round.
+// (batch entry, head); a round stages 8,192 entries in shared memory with coalesced loads,
+// each thread scans 8 consecutive ones (skewed rows: no bank conflicts), and the round is
+// stored back coalesced.
+constexpr int kScanPer = 8;
+constexpr int kScanRound = 1024 * kScanPer;
+
+__device__ __forceinline__ int scan_skew(int i) { return i + (i >> 5); }
+
 __global__ void __launch_bounds__(1024) dsa3d_cell_scan_kernel(int* __restrict__ count, int* __restrict__ cursor,
                                                                long long ncell) {
+  __shared__ int buf[kScanRound + kScanRound / 32];
   __shared__ int wsum[32];
   int* c = count + blockIdx.x * ncell;
   int* cur = cursor + blockIdx.x * ncell;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int carry = 0;
-  for (long long base = 0; base < ncell; base += 4096) {
-    const long long i0 = base + 4LL * tid;
-    int v[4];
+  for (long long base = 0; base < ncell; base += kScanRound) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = i0 + k < ncell ? c[i0 + k] : 0;
-    const int tsum = v[0] + v[1] + v[2] + v[3];
+    for (int k = 0; k < kScanPer; ++k) {
+      const int i = k * 1024 + tid;
+      buf[scan_skew(i)] = base + i < ncell ? c[base + i] : 0;
+    }
+    __syncthreads();
+    int v[kScanPer];
+    int tsum = 0;
+#pragma unroll
+    for (int k = 0; k < kScanPer; ++k) {
+      v[k] = buf[scan_skew(kScanPer * tid + k)];
+      tsum += v[k];
+    }
     int x = tsum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -549,15 +565,22 @@ __global__ void __launch_bounds__(1024) dsa3d_cell_scan_kernel(int* __restrict__
     __syncthreads();
     int e = carry + (warp ? wsum[warp - 1] : 0) + x - tsum;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (i0 + k < ncell) {
-        c[i0 + k] = e;
-        cur[i0 + k] = e;
-      }
+    for (int k = 0; k < kScanPer; ++k) {
+      buf[scan_skew(kScanPer * tid + k)] = e;
       e += v[k];
     }
     carry += wsum[31];
-    __syncthreads();  // wsum is rewritten next round
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kScanPer; ++k) {
+      const int i = k * 1024 + tid;
+      if (base + i < ncell) {
+        const int o = buf[scan_skew(i)];
+        c[base + i] = o;
+        cur[base + i] = o;
+      }
+    }
+    __syncthreads();  // buf and wsum are rewritten next round
   }
 }
 
