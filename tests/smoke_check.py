@@ -5,7 +5,8 @@ d = 64, r = 16, 4 of 8 key blocks kept): predictor + top-k, forward, backward,
 two key-partition states and their merge, the gradient through that merge
 (merge backward, then each partition state's backward, summed), the
 predictor's training signal (distillation gradient of Wq, Wk), and 3D deformable
-sliding attention (predicted offsets, then the sampled-window attention).
+sliding attention (predicted offsets, the sampled-window attention, and the
+backward of both).
 """
 from __future__ import annotations
 
@@ -95,11 +96,12 @@ def run(device: int = 0) -> dict:
         err = np.linalg.norm(host(got) - ref) / np.linalg.norm(ref)
         assert err < 1e-2, (name, err)
     assert abs(float(loss.item()) - loss_ref) <= 1e-4 * abs(loss_ref)
-    # 7. 3D deformable sliding attention: predicted offsets, then the sampled-window attention
+    # 7. 3D deformable sliding attention: predicted offsets, the sampled-window attention, then the backward
+    # of both (attention, then the offset network)
     from oracle import dsa3d_oracle as D
 
     dw = inputs.Dsa3dWorkload("smoke_dsa3d", 1, 2, 3, 8, 10, 64, 3, 3, 3, 1.0)
-    xd = inputs.generate_dsa3d(dw, names=("Q", "K", "V", "Wc", "bc", "Wl", "bl"))
+    xd = inputs.generate_dsa3d(dw, names=("Q", "K", "V", "dO", "Wc", "bc", "Wl", "bl"))
     f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
     dp = sda.dsa3d_problem(dw.B, dw.T, dw.H, dw.W, dw.heads, dw.d, dw.kt, dw.kh, dw.kw)
     dQ, dK, dV = (dev(xd[n], "bf16") for n in ("Q", "K", "V"))
@@ -113,6 +115,20 @@ def run(device: int = 0) -> dict:
     rO, rL = D.dsa3d_fwd(xd["Q"], xd["K"], xd["V"], roff, dw.T, dw.H, dw.W, dw.kt, dw.kh, dw.kw)
     assert_close(host(dO_), rO, "bf16", "smoke 3D-DSA O")
     assert np.abs(host(dL) - rL).max() <= 1e-4 * max(1.0, np.abs(rL).max())
+    shape = (dw.B, dw.N, dw.heads, dw.d)
+    gQ, gK, gV = (torch.empty(shape, dtype=torch.float32, device="cuda") for _ in range(3))
+    goff = torch.empty_like(doff)
+    ws = torch.empty(sda.sda_dsa3d_bwd_workspace_size(dp), dtype=torch.uint8, device="cuda")
+    sda.sda_dsa3d_bwd(dp, dQ, dK, dV, doff, dL, dev(xd["dO"], "bf16"), gQ, gK, gV, goff, ws)
+    gw = [torch.empty(xd[n].shape, dtype=torch.float32, device="cuda") for n in ("Wc", "bc", "Wl", "bl")]
+    ws2 = torch.empty(sda.sda_dsa3d_offsets_bwd_workspace_size(dp), dtype=torch.uint8, device="cuda")
+    sda.sda_dsa3d_offsets_bwd(dp, dQ, f32(xd["Wc"]), f32(xd["bc"]), f32(xd["Wl"]), goff, gQ, *gw, ws2)
+    rQ, rK, rV, rdo = D.dsa3d_bwd(xd["Q"], xd["K"], xd["V"], roff, xd["dO"], dw.T, dw.H, dw.W, dw.kt, dw.kh, dw.kw)
+    rn = D.dsa3d_offsets_bwd(xd["Q"], xd["Wc"], xd["bc"], xd["Wl"], xd["bl"], rdo, dw.T, dw.H, dw.W)
+    for name, got, ref in (("dQ", gQ, rQ + rn[0]), ("dK", gK, rK), ("dV", gV, rV), ("dWc", gw[0], rn[1]),
+                           ("dWl", gw[2], rn[3])):
+        err = np.abs(host(got) - ref).max()
+        assert err <= 5e-4 * max(1.0, np.abs(ref).max()), f"smoke 3D-DSA {name}: {err}"
     st = sda.sda_get_device_status()
     assert st == sda.SDA_OK, sda.status_string(st)
     return {"selection": sel, "score_rel_err": float(s_err)}
