@@ -10,7 +10,9 @@ and sda_merge_states_bwd once per step.  With --dsa3d it runs 3D deformable
 sliding attention on a workload of DSA3D_WORKLOADS: sda_dsa3d_offsets from the
 seeded offset-network weights, then sda_dsa3d_fwd on those offsets (Q, K, V
 drawn N(0,1) on the device); with --backward also sda_dsa3d_bwd (dO drawn
-N(0,1)) and sda_dsa3d_offsets_bwd on the offsets' gradient it returns.
+N(0,1)) and sda_dsa3d_offsets_bwd on the offsets' gradient it returns.  With
+--distill it runs sda_predictor_grad (the predictor's training signal) on the
+workload's seeded Q, K, Wq, Wk.
 
 A small driver for inspecting the kernels (e.g. under a profiler) on a chosen
 workload: inputs come from the seeded generator, every step runs all the
@@ -39,6 +41,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--merge", action="store_true", help="run the state merge and its gradient instead")
     ap.add_argument("--dsa3d", action="store_true", help="run 3D deformable sliding attention instead")
+    ap.add_argument("--distill", action="store_true", help="run the predictor's training signal instead")
     args = ap.parse_args()
 
     import torch
@@ -52,6 +55,8 @@ def main():
         wl = wl.with_(heads=args.heads)
     if args.merge:
         return merge_steps(wl, args)
+    if args.distill:
+        return distill_steps(wl, args)
     backward = args.backward or wl.backward
     names = ("Q", "K", "V", "Wq", "Wk") + (("dO",) if backward else ())
     x = inputs.generate(wl, names=names)
@@ -132,6 +137,35 @@ def merge_steps(wl, args):
     print(json.dumps({"workload": wl.name, "heads": wl.heads, "tokens": wl.N, "states": n,
                       "ms": {k: statistics.median(v) for k, v in times.items()},
                       "bytes": {"merge": (n + 1) * rows * (2 * wl.d + 4), "merge_bwd": (2 * n + 1) * rows * (2 * wl.d + 4)},
+                      "status": sda.status_string(status)}))
+    if status != sda.SDA_OK:
+        raise SystemExit(1)
+
+
+def distill_steps(wl, args):
+    import torch
+
+    from dynamic_block_sparse_rank_gb300 import inputs, sda
+
+    x = inputs.generate(wl, names=("Q", "K", "Wq", "Wk"))
+    d = {n: torch.from_numpy(a).to(torch.bfloat16).cuda() for n, a in x.items()}
+    p = sda.problem_from_workload(wl)
+    gq = torch.empty((wl.heads, wl.d, wl.rank), dtype=torch.float32, device="cuda")
+    gk = torch.empty_like(gq)
+    loss = torch.empty((1,), dtype=torch.float64, device="cuda")
+    ws = torch.empty(sda.sda_workspace_size(p, sda.SDA_OP_PREDICTOR_GRAD), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    times = []
+    for s in range(args.warmup + args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(st)
+        sda.sda_predictor_grad(p, d["Q"], d["K"], d["Wq"], d["Wk"], gq, gk, loss, ws, stream=st)
+        ev[1].record(st)
+        torch.cuda.synchronize()
+        if s >= args.warmup:
+            times.append(ev[0].elapsed_time(ev[1]))
+    status = sda.sda_get_device_status()
+    print(json.dumps({"workload": wl.name, "heads": wl.heads, "tokens": wl.N, "ms": statistics.median(times),
                       "status": sda.status_string(status)}))
     if status != sda.SDA_OK:
         raise SystemExit(1)
