@@ -34,7 +34,10 @@ namespace sda {
 namespace {
 
 constexpr int kDistQB = 2;                     // query blocks per CTA (one per epilogue group)
-constexpr int kDistThreads = 10 * 32;          // warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups
+// warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups, warps 10-13 two scorers per group
+// (one per slot: alternate pairs)
+constexpr int kDistThreads = (2 + 6 * kDistQB) * 32;
+constexpr int kCandWords = 2 * kDistQB * 4 * 4 * 32;  // candidate masks: [slot][group][quarter][chunk][lane]
 constexpr float kUnitF = 5.9604644775390625e-8f;  // 2^-24, fp32's unit roundoff
 
 template <int R, int D>
@@ -178,14 +181,17 @@ __global__ void __launch_bounds__(kDistThreads, 1)
   uint64_t* accf = kempty + JS;       // 2: a buffer pair holds a finished (S~, S)
   uint64_t* accempty = accf + 2;      // 2: its four warps have read it out
   uint64_t* drain = accempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  // per [slot][group]: lready — the group's four warps published a pair's maxima and candidate
+  // masks in the slot; lfree — the group's scorer has read them (the slot may be rewritten)
+  uint64_t* lready = drain + 1;            // 2 * kDistQB
+  uint64_t* lfree = lready + 2 * kDistQB;  // 2 * kDistQB
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lfree + 2 * kDistQB);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  float* gmax = reinterpret_cast<float*>(abort_flag + 1);  // [2 groups][4 quarters] max of S~
-  float* gtmax = gmax + 8;                                 // [2][4] max of S
-  Score2* bestv = reinterpret_cast<Score2*>(gtmax + 8);  // [2][4]
-  int* besti = reinterpret_cast<int*>(bestv + 8);          // [2][4]
-  int* bestj = besti + 8;                                  // [2][4]
-  uint8_t* fullb = reinterpret_cast<uint8_t*>(bestj + 8);  // nb: key block J lies inside the grid
+  float* gmax = reinterpret_cast<float*>(abort_flag + 1);  // [slot][group][quarter] max of S~
+  float* gtmax = gmax + 2 * kDistQB * 4;                   // [slot][group][quarter] max of S
+  uint32_t* cflag = reinterpret_cast<uint32_t*>(gtmax + 2 * kDistQB * 4);  // [slot][group][quarter]: chunks
+  uint32_t* cmask = cflag + 2 * kDistQB * 4;                                 // kCandWords
+  uint8_t* fullb = reinterpret_cast<uint8_t*>(cmask + kCandWords);  // nb: key block J lies inside the grid
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -199,6 +205,10 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       mbar_init(accempty + b, 4);
     }
     mbar_init(drain, 1);
+    for (int b = 0; b < 2 * kDistQB; ++b) {
+      mbar_init(lready + b, 4);
+      mbar_init(lfree + b, 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -280,9 +290,11 @@ __global__ void __launch_bounds__(kDistThreads, 1)
     mma_commit_by(leader, drain);
     wait_plain(drain, 0);
     __syncwarp();
-  } else {
+  } else if (warp < 2 + 4 * kDistQB) {
     // Epilogue group grp (warps 2 + 4 grp .. 5 + 4 grp, one per TMEM lane quarter) handles
-    // query block I0 + grp against every key block.  Thread = query row.
+    // query block I0 + grp against every key block.  Thread = query row.  Per pair it reads
+    // S~ and S out of TMEM, finds the maxima and marks the candidates for the exact maximum,
+    // publishes them in slot u & 1 to the group's scorer warp and releases the TMEM pair.
     const int grp = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -292,13 +304,14 @@ __global__ void __launch_bounds__(kDistThreads, 1)
     const bool active = I < nb;
     const bool row_ok = active && block_row_token(a.g, I, row) >= 0;
     const float qn = active ? a.qnorm[head_tiles + I] : 0.f;
-    const uint8_t* qtile = sqt + grp * C::TB;
-    float loss_acc = 0.f, loss_comp = 0.f;  // compensated sum of this group's e^2 / 2
     for (int P = grp; P < n_pairs; P += 2) {
-      const int s = (P >> 1) % JS, J = key_block(P >> 1);
-      const float kn = a.knorm[head_tiles + J];  // issued before the wait: its latency overlaps it
+      const int u = P >> 1, slot = u & 1, J = key_block(u);
+      const int sg = slot * kDistQB + grp;  // this pair's slot of the group
+      const float kn = a.knorm[head_tiles + J];  // issued before the waits: its latency overlaps them
       // a failed wait stops all four warps of the group at the same barrier below
-      const bool okw = warp_wait(accf + grp, (P >> 1) & 1, a.status, abort_flag);
+      bool okw = warp_wait(accf + grp, u & 1, a.status, abort_flag);
+      // the slot's previous pair (u - 2) has been read by the scorer before any of it is rewritten
+      if (okw && u >= 2) okw = warp_wait(lfree + sg, ((u >> 1) - 1) & 1, a.status, abort_flag);
       const bool fj = fullb[J] != 0;
       // The row maxima of S~ (mi) and S (ti), over the key rows inside the grid; the
       // reducing TMEM load gives them for full key blocks.
@@ -347,16 +360,11 @@ __global__ void __launch_bounds__(kDistThreads, 1)
         wt = fmaxf(wt, __shfl_xor_sync(0xffffffffu, wt, o));
       }
       if (lane == 0) {
-        gmax[grp * 4 + quarter] = wm;
-        gtmax[grp * 4 + quarter] = wt;
+        gmax[sg * 4 + quarter] = wm;
+        gtmax[sg * 4 + quarter] = wt;
       }
       if (!named_bar_and(2 + grp, 128, okw)) break;
-      float M = gmax[grp * 4], T = gtmax[grp * 4];
-#pragma unroll
-      for (int qq = 1; qq < 4; ++qq) {
-        M = fmaxf(M, gmax[grp * 4 + qq]);
-        T = fmaxf(T, gtmax[grp * 4 + qq]);
-      }
+      const float M = fmaxf(fmaxf(gmax[sg * 4], gmax[sg * 4 + 1]), fmaxf(gmax[sg * 4 + 2], gmax[sg * 4 + 3]));
       // Every fp32 score within twice the rounding bound of the fp32 maximum M is a
       // candidate for the exact maximum.  An r-term dot product accumulated in fp32, with
       // each of at most r additions rounded to nearest or truncated, is off by at most
@@ -367,12 +375,9 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       const float delta_f = __fmul_ru(__fmul_ru(kBoundCoef, qn), kn);
       const float floor_f = __fsub_rd(M, delta_f);
       const bool cand = row_ok && mi >= floor_f;
-      Score2 bv = {-INFINITY, 0.f};
-      int bi = 0x7fffffff, bj = 0x7fffffff;
-      const bool wcand = __any_sync(0xffffffffu, cand);
-      if (wcand) {  // usually one warp of the four: its candidate row's columns, again from TMEM
-        const uint8_t* ktile = skt + s * C::TB;
-        uint32_t needm = 0;  // the 32-column chunks that can hold a candidate of this row
+      uint32_t chunks = 0;  // the 32-column chunks in which some row of this warp has a candidate
+      if (__any_sync(0xffffffffu, cand)) {  // usually one warp of the four: its candidate row's columns, again from TMEM
+        uint32_t needm = 0;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) needm |= (cand && cmx[cc] >= floor_f ? 1u : 0u) << cc;
 #pragma unroll 1
@@ -389,105 +394,100 @@ __global__ void __launch_bounds__(kDistThreads, 1)
             for (int e = 0; e < 32; ++e) m4[e & 3] |= (__uint_as_float(w[e]) >= floor_f ? 1u : 0u) << e;
             cm = ((m4[0] | m4[1]) | (m4[2] | m4[3])) & (fj ? 0xffffffffu : block_rows_mask32(a.g, J, cc * 32));
           }
-          // every candidate of the warp, each scored by the whole warp (lowest lane, then lowest
-          // column first; the order does not matter: better() is a total order)
-          for (;;) {
-            const unsigned who = __ballot_sync(0xffffffffu, cm != 0u);
-            if (who == 0u) break;
-            const int src = __ffs(who) - 1;
-            const int e = __ffs(__shfl_sync(0xffffffffu, cm, src)) - 1;
-            if (lane == src) cm &= cm - 1u;
-            const int crow = quarter * 32 + src, j = cc * 32 + e;
-            const Score2 v = exact_score_warp<R>(qtile, crow, ktile, j, lane);
-            if (lane == src && better(v, crow, j, bv, bi, bj)) {
-              bv = v;
-              bi = crow;
-              bj = j;
-            }
-          }
+          cmask[((sg * 4 + quarter) * 4 + cc) * 32 + lane] = cm;
+          if (__any_sync(0xffffffffu, cm != 0u)) chunks |= 1u << cc;
         }
       }
-      // the TMEM pair is read out: the MMA warp may refill it
+      if (lane == 0) cflag[sg * 4 + quarter] = chunks;
+      // the TMEM pair is read out: the MMA warp may refill it; the slot goes to the scorer
       tc_fence_before();
+      __threadfence_block();  // this lane's masks before the arrive that publishes them
       __syncwarp();
-      if (lane == 0) mbar_arrive(accempty + grp);
-      const unsigned found = __ballot_sync(0xffffffffu, bi != 0x7fffffff);
-      if (found != 0u && (found & (found - 1u)) == 0u) {  // one lane holds the warp's best
-        const int src = __ffs(found) - 1;
-        bv.hi = __shfl_sync(0xffffffffu, bv.hi, src);
-        bv.lo = __shfl_sync(0xffffffffu, bv.lo, src);
-        bi = __shfl_sync(0xffffffffu, bi, src);
-        bj = __shfl_sync(0xffffffffu, bj, src);
-      } else if (found != 0u) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const Score2 ov = {__shfl_xor_sync(0xffffffffu, bv.hi, o), __shfl_xor_sync(0xffffffffu, bv.lo, o)};
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o), oj = __shfl_xor_sync(0xffffffffu, bj, o);
-          if (better(ov, oi, oj, bv, bi, bj)) {
-            bv = ov;
-            bi = oi;
-            bj = oj;
-          }
-        }
-      }
       if (lane == 0) {
-        bestv[grp * 4 + quarter] = bv;
-        besti[grp * 4 + quarter] = bi;
-        bestj[grp * 4 + quarter] = bj;
-      }
-      named_bar(2 + grp, 128);
-      if (quarter == 0) {  // one warp of the group adds the gradient terms
-        Score2 v = bestv[grp * 4];
-        int i = besti[grp * 4], j = bestj[grp * 4];
-#pragma unroll
-        for (int qq = 1; qq < 4; ++qq)
-          if (better(bestv[grp * 4 + qq], besti[grp * 4 + qq], bestj[grp * 4 + qq], v, i, j)) {
-            v = bestv[grp * 4 + qq];
-            i = besti[grp * 4 + qq];
-            j = bestj[grp * 4 + qq];
-          }
-        if (active && i < 128 && j < 128) {
-          const float e = (v.hi - T) + v.lo;
-          const long long pair = (head_tiles + I) * nb + J;
-          if (lane == 0) {
-            const float y = 0.5f * e * e - loss_comp;
-            const float t1 = loss_acc + y;
-            loss_comp = (t1 - loss_acc) - y;
-            loss_acc = t1;
-            if (a.s_out) a.s_out[pair] = v.hi;
-            if (a.t_out) a.t_out[pair] = T;
-          }
-          // the operand values leave the stage before it is released; the atomics follow
-          // the release (an arrive orders the thread's earlier memory operations before it,
-          // and would otherwise wait for these atomics to reach L2)
-          const uint8_t* ktile = skt + s * C::TB;
-          float kv[(R + 31) / 32], qv[(R + 31) / 32];
-#pragma unroll
-          for (int u = 0; u < (R + 31) / 32; ++u) {
-            const int c = lane + 32 * u;
-            kv[u] = c < R ? bf16_at(ktile, j, c, R) : 0.f;
-            qv[u] = c < R ? bf16_at(qtile, i, c, R) : 0.f;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(kempty + s);  // this group no longer reads stage s
-          const long long hrow = ((long long)a.b * a.Hh + h) * a.N;
-          float* gq = a.Gq + (hrow + block_row_token(a.g, I, i)) * R;
-          float* gk = a.Gk + (hrow + block_row_token(a.g, J, j)) * R;
-#pragma unroll
-          for (int u = 0; u < (R + 31) / 32; ++u) {
-            const int c = lane + 32 * u;
-            if (c < R) {
-              atomicAdd(gq + c, e * kv[u]);
-              atomicAdd(gk + c, e * qv[u]);
-            }
-          }
-        } else {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(kempty + s);
-        }
+        mbar_arrive(accempty + grp);
+        mbar_arrive(lready + sg);
       }
     }
-    if (quarter == 0 && lane == 0 && loss_acc != 0.f) atomicAdd(a.loss, (double)loss_acc - (double)loss_comp);
+  } else {
+    // Scorer warps of group grp, one per slot (the group's even or odd pairs): per pair the
+    // candidates marked in the slot are re-scored exactly (each by the whole warp), the first
+    // exact maximum (i*, j*) gives e = s~(i*, j*) - t, and e k~_j* and e q~_i* are added to
+    // G_q[i*] and G_k[j*] and e^2 / 2 to the loss.  The key stage is released after the
+    // operands are read.
+    const int grp = (warp - 2 - 4 * kDistQB) >> 1, which = (warp - 2 - 4 * kDistQB) & 1;
+    const int I = I0 + grp;
+    const bool active = I < nb;
+    const uint8_t* qtile = sqt + grp * C::TB;
+    float loss_acc = 0.f, loss_comp = 0.f;  // compensated sum of this scorer's e^2 / 2 (lane 0)
+    for (int P = grp + 2 * which; P < n_pairs; P += 4) {
+      const int u = P >> 1, slot = u & 1, s = u % JS, J = key_block(u);  // slot == which
+      const int sg = slot * kDistQB + grp;
+      if (!warp_wait(lready + sg, (u >> 1) & 1, a.status, abort_flag)) break;
+      const float T = fmaxf(fmaxf(gtmax[sg * 4], gtmax[sg * 4 + 1]), fmaxf(gtmax[sg * 4 + 2], gtmax[sg * 4 + 3]));
+      const uint8_t* ktile = skt + s * C::TB;
+      Score2 bv = {-INFINITY, 0.f};  // the same in every lane: exact_score_warp returns one value to all
+      int bi = 0x7fffffff, bj = 0x7fffffff;
+      for (int qc = 0; qc < 16; ++qc) {
+        const int qd = qc >> 2, cc = qc & 3;
+        if (!((cflag[sg * 4 + qd] >> cc) & 1u)) continue;
+        uint32_t cm = cmask[((sg * 4 + qd) * 4 + cc) * 32 + lane];
+        for (;;) {  // every candidate of the chunk: lowest lane (row), then lowest column
+          const unsigned who = __ballot_sync(0xffffffffu, cm != 0u);
+          if (who == 0u) break;
+          const int src = __ffs(who) - 1;
+          const int e = __ffs(__shfl_sync(0xffffffffu, cm, src)) - 1;
+          if (lane == src) cm &= cm - 1u;
+          const int crow = qd * 32 + src, j = cc * 32 + e;
+          const Score2 v = exact_score_warp<R>(qtile, crow, ktile, j, lane);
+          if (better(v, crow, j, bv, bi, bj)) {
+            bv = v;
+            bi = crow;
+            bj = j;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(lfree + sg);  // the slot's maxima and masks are read
+      if (active && bi < 128 && bj < 128) {
+        const float e = (bv.hi - T) + bv.lo;
+        const long long pair = (head_tiles + I) * nb + J;
+        if (lane == 0) {
+          const float y = 0.5f * e * e - loss_comp;
+          const float t1 = loss_acc + y;
+          loss_comp = (t1 - loss_acc) - y;
+          loss_acc = t1;
+          if (a.s_out) a.s_out[pair] = bv.hi;
+          if (a.t_out) a.t_out[pair] = T;
+        }
+        // the operand values leave the stage before it is released; the atomics follow
+        // the release (an arrive orders the thread's earlier memory operations before it,
+        // and would otherwise wait for these atomics to reach L2)
+        float kv[(R + 31) / 32], qv[(R + 31) / 32];
+#pragma unroll
+        for (int uu = 0; uu < (R + 31) / 32; ++uu) {
+          const int c = lane + 32 * uu;
+          kv[uu] = c < R ? bf16_at(ktile, bj, c, R) : 0.f;
+          qv[uu] = c < R ? bf16_at(qtile, bi, c, R) : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kempty + s);  // this group no longer reads stage s
+        const long long hrow = ((long long)a.b * a.Hh + h) * a.N;
+        float* gq = a.Gq + (hrow + block_row_token(a.g, I, bi)) * R;
+        float* gk = a.Gk + (hrow + block_row_token(a.g, J, bj)) * R;
+#pragma unroll
+        for (int uu = 0; uu < (R + 31) / 32; ++uu) {
+          const int c = lane + 32 * uu;
+          if (c < R) {
+            atomicAdd(gq + c, e * kv[uu]);
+            atomicAdd(gk + c, e * qv[uu]);
+          }
+        }
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kempty + s);
+      }
+    }
+    if (lane == 0 && loss_acc != 0.f) atomicAdd(a.loss, (double)loss_acc - (double)loss_comp);
   }
   __syncthreads();
   if (warp == 1) {
@@ -588,8 +588,10 @@ cudaError_t launch_distill(const Prob& p, const void* Q, const void* K, float* d
   tile_norm_kernel<R><<<nt_blocks, 256, 0, st>>>(w.qt, (long long)tiles, w.qnorm);
   tile_norm_kernel<R><<<nt_blocks, 256, 0, st>>>(w.kt, (long long)tiles, w.knorm);
   note_launches(2);
-  const size_t smem = 1024 + C::TILES_BYTES + 8 * (1 + 2 * C::JS + 5) + 8 + 16 * 4 + 8 + 8 * 8 + 16 * 4 +
-                      (size_t)p.g.nb + 64;
+  // tiles, the barriers (qfull, 2 JS ring, 2 accf, 2 accempty, drain, 4 kDistQB slot barriers), the TMEM
+  // slot and abort flag, the maxima and chunk flags (3 x [2][kDistQB][4] words), the candidate masks, fullb
+  const size_t smem = 1024 + C::TILES_BYTES + 8 * (1 + 2 * C::JS + 5 + 4 * kDistQB) + 8 + 3 * 2 * kDistQB * 4 * 4 +
+                      (size_t)kCandWords * 4 + (size_t)p.g.nb + 64;
   cudaError_t e = cudaFuncSetAttribute(distill_kernel<R, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const size_t per_batch = (size_t)p.N * p.Hh * p.d * 2;
