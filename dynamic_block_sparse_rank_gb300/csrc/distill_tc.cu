@@ -34,9 +34,10 @@ namespace sda {
 namespace {
 
 constexpr int kDistQB = 2;                     // query blocks per CTA (one per epilogue group)
-// warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups, warps 10-13 two scorers per group
-// (one per slot: alternate pairs)
-constexpr int kDistThreads = (2 + 6 * kDistQB) * 32;
+// warp 0 TMA, warps 1-2 one MMA issuer per group, warps 3-10 two epilogue groups, warps 11-14
+// two scorers per group (one per slot: alternate pairs)
+constexpr int kDistMma = 1, kDistEpi = kDistMma + kDistQB, kDistScore = kDistEpi + 4 * kDistQB;
+constexpr int kDistThreads = (kDistScore + 2 * kDistQB) * 32;
 constexpr int kCandWords = 2 * kDistQB * 4 * 4 * 32;  // candidate masks: [slot][group][quarter][chunk][lane]
 constexpr float kUnitF = 5.9604644775390625e-8f;  // 2^-24, fp32's unit roundoff
 
@@ -179,18 +180,22 @@ __global__ void __launch_bounds__(kDistThreads, 1)
   uint64_t* kfull = qfull + 1;        // JS
   uint64_t* kempty = kfull + JS;      // JS: the MMAs and both epilogue groups are done with the stage
   uint64_t* accf = kempty + JS;       // 2: a buffer pair holds a finished (S~, S)
-  uint64_t* accempty = accf + 2;      // 2: its four warps have read it out
-  uint64_t* drain = accempty + 2;
+  uint64_t* accempty = accf + 2;      // 2: its four warps have read the S~ half out
+  uint64_t* sempty = accempty + 2;    // 2: its four warps have read the S half out
+  uint64_t* drain = sempty + 2;
   // per [slot][group]: lready — the group's four warps published a pair's maxima and candidate
   // masks in the slot; lfree — the group's scorer has read them (the slot may be rewritten)
   uint64_t* lready = drain + 1;            // 2 * kDistQB
   uint64_t* lfree = lready + 2 * kDistQB;  // 2 * kDistQB
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lfree + 2 * kDistQB);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  float* gmax = reinterpret_cast<float*>(abort_flag + 1);  // [slot][group][quarter] max of S~
-  float* gtmax = gmax + 2 * kDistQB * 4;                   // [slot][group][quarter] max of S
-  uint32_t* cflag = reinterpret_cast<uint32_t*>(gtmax + 2 * kDistQB * 4);  // [slot][group][quarter]: chunks
-  uint32_t* cmask = cflag + 2 * kDistQB * 4;                                 // kCandWords
+  // 16-byte aligned from here (the barriers end on an 8-byte boundary; the slot and flag fill it):
+  // the scorer reads a group's four chunk flags as one uint4
+  uint32_t* cflag = reinterpret_cast<uint32_t*>(
+      (reinterpret_cast<uintptr_t>(abort_flag + 1) + 15) & ~uintptr_t(15));  // [slot][group][quarter]: chunks
+  float* gmax = reinterpret_cast<float*>(cflag + 2 * kDistQB * 4);         // [slot][group][quarter] max of S~
+  float* gtmax = gmax + 2 * kDistQB * 4;                                     // [slot][group][quarter] max of S
+  uint32_t* cmask = reinterpret_cast<uint32_t*>(gtmax + 2 * kDistQB * 4);   // kCandWords
   uint8_t* fullb = reinterpret_cast<uint8_t*>(cmask + kCandWords);  // nb: key block J lies inside the grid
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -198,13 +203,14 @@ __global__ void __launch_bounds__(kDistThreads, 1)
     mbar_init(qfull, 1);
     for (int s = 0; s < JS; ++s) {
       mbar_init(kfull + s, 1);
-      mbar_init(kempty + s, 1 + kDistQB);
+      mbar_init(kempty + s, 2 * kDistQB);  // each group's MMA issuer and scorer
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf + b, 1);
       mbar_init(accempty + b, 4);
+      mbar_init(sempty + b, 4);
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, kDistQB);
     for (int b = 0; b < 2 * kDistQB; ++b) {
       mbar_init(lready + b, 4);
       mbar_init(lfree + b, 1);
@@ -256,47 +262,50 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // Whole warp, one elected lane issues.  Pair P = 2 J + q goes to buffer pair q:
-    // S~ into columns [256 q, 256 q + 128), S into the next 128.
+  } else if (warp < kDistEpi) {
+    // MMA issuer of group q (whole warp, one elected lane issues): for every key block it
+    // issues S = Q_I K_J^T (K = d) into columns [256 q + 128, 256 q + 256) as soon as the
+    // group has read the previous S out, then S~ = q~_I k~_J^T (K = r) into [256 q, 256 q +
+    // 128) once the previous S~ is read out, and commits the pair.  One issuer per group:
+    // a commit covers only its own group's products.
+    const int q = warp - kDistMma;
     const uint32_t leader = elect_leader();
     constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t SBO = (R / 8) * 128;
     const uint64_t dA = smem_desc(smem_u32(sqt), 128, SBO, 0), dB = smem_desc(smem_u32(skt), 128, SBO, 0);
     const uint64_t dQd = smem_desc(smem_u32(sQ), 16, 1024, 2), dKd = smem_desc(smem_u32(sK), 16, 1024, 2);
+    const uint32_t tL = tmem + q * 256, tF = tL + 128;
     bool ok = warp_wait(qfull, 0, a.status, abort_flag);
     for (int it = 0; ok && it < nb; ++it) {
       const int s = it % JS;
       if (!(ok = warp_wait(kfull + s, (it / JS) & 1, a.status, abort_flag))) break;
-      for (int q = 0; q < kDistQB; ++q) {
-        const int P = it * kDistQB + q, buf = P & 1;
-        if (P >= 2 && !(ok = warp_wait(accempty + buf, ((P >> 1) - 1) & 1, a.status, abort_flag))) break;
-        tc_fence_after();
-        const uint32_t tL = tmem + buf * 256, tF = tL + 128;
+      if (it >= 1 && !(ok = warp_wait(sempty + q, (it - 1) & 1, a.status, abort_flag))) break;
+      tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < R / 16; ++kk)
-          mma_ss_by(leader, tL, dA + (uint64_t)((q * C::TB + kk * 256) >> 4),
-                    dB + (uint64_t)((s * C::TB + kk * 256) >> 4), id, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;  // 64-column chunk, 16-column step
-          mma_ss_by(leader, tF, dQd + (uint64_t)((q * C::TILE) >> 4) + off,
-                    dKd + (uint64_t)((s * C::TILE) >> 4) + off, id, kk > 0);
-        }
-        mma_commit_by(leader, accf + buf);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;  // 64-column chunk, 16-column step
+        mma_ss_by(leader, tF, dQd + (uint64_t)((q * C::TILE) >> 4) + off, dKd + (uint64_t)((s * C::TILE) >> 4) + off,
+                  id, kk > 0);
       }
+      if (it >= 1 && !(ok = warp_wait(accempty + q, (it - 1) & 1, a.status, abort_flag))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < R / 16; ++kk)
+        mma_ss_by(leader, tL, dA + (uint64_t)((q * C::TB + kk * 256) >> 4), dB + (uint64_t)((s * C::TB + kk * 256) >> 4),
+                  id, kk > 0);
+      mma_commit_by(leader, accf + q);
       mma_commit_by(leader, kempty + s);
     }
     mma_commit_by(leader, drain);
     wait_plain(drain, 0);
     __syncwarp();
-  } else if (warp < 2 + 4 * kDistQB) {
-    // Epilogue group grp (warps 2 + 4 grp .. 5 + 4 grp, one per TMEM lane quarter) handles
+  } else if (warp < kDistScore) {
+    // Epilogue group grp (warps kDistEpi + 4 grp .. + 3, one per TMEM lane quarter) handles
     // query block I0 + grp against every key block.  Thread = query row.  Per pair it reads
     // S~ and S out of TMEM, finds the maxima and marks the candidates for the exact maximum,
     // publishes them in slot u & 1 to the group's scorer warp and releases the TMEM pair.
-    const int grp = (warp - 2) >> 2;
-    const int quarter = warp & 3;
+    const int grp = (warp - kDistEpi) >> 2;
+    const int quarter = warp & 3;  // a warp reaches TMEM lanes 32 (warp % 4) .. + 31
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint32_t tL = tmem + grp * 256 + lane_base, tF = tL + 128;
@@ -319,6 +328,25 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       float cmx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // per 32 columns of S~
       if (okw) {
         tc_fence_after();
+        // S first: its half of the buffer goes back to the MMA issuer, whose next S product
+        // (the long one, K = d) then overlaps the rest of this epilogue
+#pragma unroll 1
+        for (int cc = 0; cc < 4; cc += 2) {
+          uint32_t w0[32], w1[32];
+          float x0, x1;
+          tmem_ld32_max(tF + cc * 32, w0, x0);
+          tmem_ld32_max(tF + cc * 32 + 32, w1, x1);
+          tmem_wait_ld();
+          if (fj) {
+            ti = fmaxf(ti, fmaxf(x0, x1));
+          } else {
+            ti = fmaxf(ti, masked_max64(block_rows_mask32(a.g, J, cc * 32), block_rows_mask32(a.g, J, cc * 32 + 32),
+                                        w0, w1));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sempty + grp);
 #pragma unroll
         for (int cc = 0; cc < 4; cc += 2) {
           uint32_t w0[32], w1[32];
@@ -334,20 +362,6 @@ __global__ void __launch_bounds__(kDistThreads, 1)
           cmx[cc + 1] = x1;
         }
         mi = fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3]));
-#pragma unroll 1
-        for (int cc = 0; cc < 4; cc += 2) {
-          uint32_t w0[32], w1[32];
-          float x0, x1;
-          tmem_ld32_max(tF + cc * 32, w0, x0);
-          tmem_ld32_max(tF + cc * 32 + 32, w1, x1);
-          tmem_wait_ld();
-          if (fj) {
-            ti = fmaxf(ti, fmaxf(x0, x1));
-          } else {
-            ti = fmaxf(ti, masked_max64(block_rows_mask32(a.g, J, cc * 32), block_rows_mask32(a.g, J, cc * 32 + 32),
-                                        w0, w1));
-          }
-        }
       }
       if (!row_ok) {
         mi = -INFINITY;
@@ -399,7 +413,7 @@ __global__ void __launch_bounds__(kDistThreads, 1)
         }
       }
       if (lane == 0) cflag[sg * 4 + quarter] = chunks;
-      // the TMEM pair is read out: the MMA warp may refill it; the slot goes to the scorer
+      // the S~ half is read out: the MMA issuer may refill it; the slot goes to the scorer
       tc_fence_before();
       __threadfence_block();  // this lane's masks before the arrive that publishes them
       __syncwarp();
@@ -414,7 +428,7 @@ __global__ void __launch_bounds__(kDistThreads, 1)
     // exact maximum (i*, j*) gives e = s~(i*, j*) - t, and e k~_j* and e q~_i* are added to
     // G_q[i*] and G_k[j*] and e^2 / 2 to the loss.  The key stage is released after the
     // operands are read.
-    const int grp = (warp - 2 - 4 * kDistQB) >> 1, which = (warp - 2 - 4 * kDistQB) & 1;
+    const int grp = (warp - kDistScore) >> 1, which = (warp - kDistScore) & 1;
     const int I = I0 + grp;
     const bool active = I < nb;
     const uint8_t* qtile = sqt + grp * C::TB;
@@ -427,9 +441,12 @@ __global__ void __launch_bounds__(kDistThreads, 1)
       const uint8_t* ktile = skt + s * C::TB;
       Score2 bv = {-INFINITY, 0.f};  // the same in every lane: exact_score_warp returns one value to all
       int bi = 0x7fffffff, bj = 0x7fffffff;
-      for (int qc = 0; qc < 16; ++qc) {
-        const int qd = qc >> 2, cc = qc & 3;
-        if (!((cflag[sg * 4 + qd] >> cc) & 1u)) continue;
+      // the (quarter, chunk) pairs holding candidates, as one 16-bit set: usually one bit
+      const uint4 f4 = *reinterpret_cast<const uint4*>(cflag + sg * 4);
+      uint32_t todo = f4.x | (f4.y << 4) | (f4.z << 8) | (f4.w << 12);
+      while (todo != 0u) {
+        const int qc = __ffs(todo) - 1, qd = qc >> 2, cc = qc & 3;
+        todo &= todo - 1u;
         uint32_t cm = cmask[((sg * 4 + qd) * 4 + cc) * 32 + lane];
         for (;;) {  // every candidate of the chunk: lowest lane (row), then lowest column
           const unsigned who = __ballot_sync(0xffffffffu, cm != 0u);
@@ -588,9 +605,10 @@ cudaError_t launch_distill(const Prob& p, const void* Q, const void* K, float* d
   tile_norm_kernel<R><<<nt_blocks, 256, 0, st>>>(w.qt, (long long)tiles, w.qnorm);
   tile_norm_kernel<R><<<nt_blocks, 256, 0, st>>>(w.kt, (long long)tiles, w.knorm);
   note_launches(2);
-  // tiles, the barriers (qfull, 2 JS ring, 2 accf, 2 accempty, drain, 4 kDistQB slot barriers), the TMEM
-  // slot and abort flag, the maxima and chunk flags (3 x [2][kDistQB][4] words), the candidate masks, fullb
-  const size_t smem = 1024 + C::TILES_BYTES + 8 * (1 + 2 * C::JS + 5 + 4 * kDistQB) + 8 + 3 * 2 * kDistQB * 4 * 4 +
+  // tiles, the barriers (qfull, 2 JS ring, 2 accf, 2 accempty, 2 sempty, drain, 4 kDistQB slot barriers),
+  // the TMEM slot and abort flag (with the padding to 16 bytes), the chunk flags and maxima
+  // (3 x [2][kDistQB][4] words), the candidate masks, fullb
+  const size_t smem = 1024 + C::TILES_BYTES + 8 * (1 + 2 * C::JS + 7 + 4 * kDistQB) + 16 + 3 * 2 * kDistQB * 4 * 4 +
                       (size_t)kCandWords * 4 + (size_t)p.g.nb + 64;
   cudaError_t e = cudaFuncSetAttribute(distill_kernel<R, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
