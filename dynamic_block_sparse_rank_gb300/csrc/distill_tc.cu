@@ -16,13 +16,16 @@
 //   tile_norm_kernel  the largest row norm of every q~ / k~ tile, which bounds the
 //                     fp32 rounding of any low-rank score of a tile pair;
 //   distill_kernel    per (2 query blocks, head): for every key block J and query
-//                     block q, S~ = q~_I k~_J^T (K = r) and S = Q_I K_J^T (K = d) on
-//                     the tensor cores into one of two TMEM buffer pairs; an epilogue
-//                     group of four warps takes t = max S and the first maximum of S~
-//                     (the fp32 entries within twice the rounding bound of the fp32
-//                     maximum re-scored from the bf16 operands, a compensated fp32 sum
-//                     of exact products good to about 2^-44; equal operands tie
-//                     exactly and go to the first row, then column), then adds
+//                     block q, S = Q_I K_J^T (K = d) and S~ = q~_I k~_J^T (K = r) on
+//                     the tensor cores (one MMA issuer warp per query block) into the
+//                     block's TMEM buffer pair; an epilogue group of four warps takes
+//                     t = max S, hands the S half back, finds the fp32 maximum of S~
+//                     and marks the entries within twice its rounding bound as
+//                     candidates, hands the S~ half back and passes the candidates to
+//                     a scorer warp (two per group, alternate pairs), which re-scores
+//                     them from the bf16 operands with the whole warp (a compensated
+//                     fp32 sum of exact products good to about 2^-44; equal operands
+//                     tie exactly and go to the first row, then column), then adds
 //                     e k~_j* to the query token's r-vector G_q[i*] and
 //                     e q~_i* to the key token's G_k[j*] (fp32 atomics) and e^2 / 2
 //                     to the loss;
