@@ -139,7 +139,8 @@ struct ScoreCfg {
 // warp 0 producer, warp 1 MMA, warps 2..17 epilogue in 4 groups of 4 (one warp
 // per TMEM lane quarter); group g drains accumulator buffer g.
 constexpr int kEpiWarps = 16;
-constexpr int kScoreThreads = (2 + kEpiWarps) * 32;
+// warp 0 copies, warps 1 and 2 + kEpiWarps issue the MMAs (even and odd pairs), warps 2 .. 1 + kEpiWarps drain
+constexpr int kScoreThreads = (3 + kEpiWarps) * 32;
 constexpr int kAccBufs = 4;  // TMEM accumulators of 128 columns: one (query block, key block) pair each
 
 struct ScoreArgs {
@@ -211,13 +212,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     mbar_init(afull_q, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(kfull + s, 1);
-      mbar_init(kempty + s, 1);
+      mbar_init(kempty + s, 2);  // both MMA issuers
     }
     for (int s = 0; s < kAccBufs; ++s) {
       mbar_init(accf + s, 1);
       drained[s] = 0u;
     }
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -255,9 +256,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // Whole warp, one elected lane issues; descriptors advance by adding to the
+  } else if (warp == 1 || warp == 2 + kEpiWarps) {
+    // Two issuers, each a whole warp with one elected lane issuing: warp 1 the even pairs,
+    // warp 2 + kEpiWarps the odd ones, so that one issuer's hand-offs (its counter poll, the
+    // fence, the commit) overlap the other's MMAs.  Both wait for every key stage and both
+    // release it, so neither can run a stage ahead.  Descriptors advance by adding to the
     // start-address field (16-byte units).
+    const int w = warp == 1 ? 0 : 1;
     const uint32_t leader = elect_leader();
     constexpr uint32_t id = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t SBO = (R / 8) * 128;
@@ -269,6 +274,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
 #pragma unroll
       for (int q = 0; q < QB; ++q) {
         const int P = J * QB + q, buf = P & (kAccBufs - 1);
+        if ((P & 1) != w) continue;
         // buffer `buf` was read out for its previous (P >> 2) uses: 4 warps each
         if (P >= kAccBufs && !(ok = warp_wait_count(drained + buf, 4u * (unsigned)(P >> 2), a.status, abort_flag)))
           break;
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     mma_commit_by(leader, drain);
     wait_plain(drain, 0);
     __syncwarp();
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     const int e = warp - 2;
     const int grp = e >> 2;         // accumulator buffer this warp drains
     const int quarter = warp & 3;   // TMEM lanes 32 quarter .. 32 quarter + 31 (query rows)
