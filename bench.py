@@ -54,7 +54,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum; sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active)
 # An entry goes back to None whenever its kernel changes, until it is captured again.
 NCU_COUNTERS = {
-    "score_kernel": {"dram_bytes": 8 * (0.0683e9 + 0.0052e9), "tensor_active": 0.555},
+    "score_kernel": {"dram_bytes": 8 * (0.0686e9 + 0.0051e9), "tensor_active": 0.586},
     "fwd_tc_kernel": {"dram_bytes": 8 * (7.670e9 + 0.570e9), "tensor_active": 0.635},
     "dqx_kernel": {"dram_bytes": 8 * (6.908e9 + 0.263e9), "tensor_active": 0.759},
     "dkdv_kernel": {"dram_bytes": 8 * (15.113e9 + 0.520e9), "tensor_active": 0.681},
