@@ -18,7 +18,7 @@
 //                 shared memory (else 2 or 1): streams every k~ tile through a
 //                 ring; each (key block, query block) pair is one M=128, N=128,
 //                 K=r accumulation in one of four 128-column TMEM buffers, issued
-//                 by a warp-converged MMA warp.  Four epilogue groups of four
+//                 by one of two warp-converged MMA warps (even and odd pairs).  Four epilogue groups of four
 //                 warps (one per TMEM lane quarter) each drain one buffer: the
 //                 reducing TMEM load gives each thread the max of its columns,
 //                 then one redux.sync over order-preserving keys and a shared-
@@ -136,8 +136,9 @@ struct ScoreCfg {
   static constexpr int TB = 128 * R * 2;      // bytes of one operand tile
   static constexpr int ST = R <= 32 ? 8 : 4;  // k~ ring depth
 };
-// warp 0 producer, warp 1 MMA, warps 2..17 epilogue in 4 groups of 4 (one warp
-// per TMEM lane quarter); group g drains accumulator buffer g.
+// warp 0 producer, warps 1 and 18 the MMA issuers (even and odd pairs), warps 2..17
+// epilogue in 4 groups of 4 (one warp per TMEM lane quarter); group g drains
+// accumulator buffer g.
 constexpr int kEpiWarps = 16;
 // warp 0 copies, warps 1 and 2 + kEpiWarps issue the MMAs (even and odd pairs), warps 2 .. 1 + kEpiWarps drain
 constexpr int kScoreThreads = (3 + kEpiWarps) * 32;

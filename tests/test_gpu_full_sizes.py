@@ -492,3 +492,17 @@ def test_dsa3d_524k_backward_sampled(sda, parity_report):
     _fp32_record(rec, "offset network dQ", dQn_s, rn[0][:, toks], rel)
     for name, g, r in zip(("dWc", "dbc", "dWl", "dbl"), gW, rn[1:]):
         _fp32_record(rec, name, g, r, rel)
+
+
+def test_predictor_with_two_query_blocks_per_cta(sda, parity_report):
+    """A grid whose score rows no longer fit four query blocks per CTA in shared memory (7,680 blocks of
+    2 x 8 x 8, 983,040 tokens; four fit up to about 7,500 blocks and the API admits 8,192): the score kernel
+    runs two query blocks per CTA, its two MMA issuers still splitting the pairs by parity.  One head,
+    d = 64, r = 32, 5% kept; the first, middle and last query blocks plus three seeded ones: selection by
+    the gap rule, scores, and the forward on those rows."""
+    wl = inputs.Workload("fwd_983k_qb2", 1, 1, 32, 128, 240, 64, 2, 8, 8, 32, 0.05, "bf16", 4.0, 32)
+    assert wl.n_blocks == 7680
+    qb = _samples(wl, 3, 53)
+    rec = _Record(parity_report, wl.name, f"1 head x {len(qb)} of {wl.n_blocks} query blocks (two query "
+                                          f"blocks per score CTA)")
+    _check_predictor_and_forward(sda, rec, wl, [0], qb)
