@@ -31,6 +31,24 @@
 //                         FMAs).  Positions are tested against the
 //                         raster in float before any index is formed, so a
 //                         non-finite offset only moves its sample outside.
+//
+// Backward (the loss reaching the attention through O):
+//   dsa3d_bwd_kernel      the forward's warp layout; one gather of the corners
+//                         per window point gives P_s, dP_s, k~_s and the
+//                         corner weights' derivatives, from which dq and the
+//                         offsets' gradient follow (both linear in D); each
+//                         sample's coefficients are stored and the sample is
+//                         counted in the cell of its floor position.
+//   dsa3d_cell_scan_kernel, dsa3d_cell_fill_kernel
+//                         bucket the samples by cell (exclusive scan of the
+//                         counts, then one record per sample in its cell).
+//   dsa3d_dkdv_kernel     each dK / dV row gathered from the records of the 8
+//                         cells it is a corner of: rows written once, no
+//                         atomics.
+//   dsa3d_offsets_bwd_kernel, dsa3d_offsets_bwd_conv_kernel
+//                         the offset network: dY, dWl, dbl per token tile,
+//                         then the transposed convolution into dQ with dWc
+//                         and dbc.
 #include <cuda_bf16.h>
 
 #include "internal.h"

@@ -18,8 +18,9 @@
 //                 shared memory (else 2 or 1): streams every k~ tile through a
 //                 ring; each (key block, query block) pair is one M=128, N=128,
 //                 K=r accumulation in one of four 128-column TMEM buffers, issued
-//                 by one of two warp-converged MMA warps (even and odd pairs).  Four epilogue groups of four
-//                 warps (one per TMEM lane quarter) each drain one buffer: the
+//                 by one of two warp-converged MMA warps (even and odd pairs).
+//                 Four epilogue groups of four warps (one per TMEM lane
+//                 quarter) each drain one buffer: the
 //                 reducing TMEM load gives each thread the max of its columns,
 //                 then one redux.sync over order-preserving keys and a shared-
 //                 memory atomic max per warp.  Four buffers let the MMA run
