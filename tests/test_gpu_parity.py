@@ -70,6 +70,11 @@ TILE_1X8X16 = inputs.Workload("tile_1x8x16_d64", 1, 2, 3, 20, 40, 64, 1, 8, 16, 
 TILE_1X1X128 = inputs.Workload("tile_1x1x128_d64", 1, 2, 4, 3, 200, 64, 1, 1, 128, 16, 0.5, "bf16", 3.0, 16,
                                backward=True)
 SMALL = [RAGGED_D64, RAGGED_D128, FULL_D128, TWO_BATCH, TILE_4X4X8, TILE_1X8X16, TILE_1X1X128]
+# The larger ranks the API admits (r = 48, 64): two low-rank columns per lane in the training signal's
+# warp-wide re-scoring, and the shallower k~ rings of the r = 64 score and training-signal kernels.
+RANK48_D64 = inputs.Workload("rank48_d64", 1, 2, 5, 12, 20, 64, 2, 8, 8, 48, 0.4, "bf16", 3.0, 16)
+RANK64_D128 = inputs.Workload("rank64_d128", 1, 2, 4, 16, 17, 128, 2, 8, 8, 64, 0.3, "bf16", 4.0, 32)
+RANKS = [RANK48_D64, RANK64_D128]
 # 20 key blocks at keep 0.35: 0.35 x 20 is not exact in binary floating point; both sides keep 7.
 KEEP_035 = inputs.Workload("keep035_20blocks", 1, 2, 10, 16, 16, 64, 2, 8, 8, 16, 0.35, "bf16", 3.0, 16)
 
@@ -80,7 +85,7 @@ def test_smoke_path():
     smoke_check.run()
 
 
-@pytest.mark.parametrize("wl", SMALL + [KEEP_035, inputs.WORKLOADS["tiny_f32_256"]], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", SMALL + RANKS + [KEEP_035, inputs.WORKLOADS["tiny_f32_256"]], ids=lambda w: w.name)
 def test_predictor_matches_oracle(sda, wl):
     x = inputs.generate(wl, names=("Q", "K", "Wq", "Wk"))
     assert sda.sda_num_blocks(sda.problem_from_workload(wl)) == (wl.n_blocks, orc.keep_count(wl.keep, wl.n_blocks))
@@ -571,7 +576,8 @@ def check_predictor_grad(got, ref, what):
     return mx / scale, rel
 
 
-@pytest.mark.parametrize("wl", [RAGGED_D64, RAGGED_D128, TILE_4X4X8, TWO_BATCH, TILE_1X1X128], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [RAGGED_D64, RAGGED_D128, TILE_4X4X8, TWO_BATCH, TILE_1X1X128] + RANKS,
+                         ids=lambda w: w.name)
 def test_predictor_training_signal_matches_oracle(sda, wl):
     """sda_predictor_grad against the oracle's distillation gradient: per (I, J) the low-rank block score s at
     its exact first maximum and the full-rank block max t, the loss, and dWq, dWk."""
@@ -620,7 +626,7 @@ def _tied_selection_inputs(wl, seed=7):
     return {"Q": Q, "K": K, "Wq": Wq, "Wk": Wk}, geom
 
 
-@pytest.mark.parametrize("wl", [RAGGED_D64, TILE_4X4X8], ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", [RAGGED_D64, TILE_4X4X8] + RANKS, ids=lambda w: w.name)
 def test_predictor_training_signal_takes_the_first_exact_maximum(sda, wl):
     """Reading 14's tie rule, pinned on the GPU: with exact low-rank operands the GPU's s must be the oracle's
     exact maximum rounded once to fp32 (no tolerance), and the planted four-way ties must go to the first query
