@@ -583,6 +583,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 // products then read only their B tile from shared memory and run at the tensor pipe's
 // full rate.  TMEM: S [0,128), dP [128,256), dQ [256,256+D), Q [256+D,256+3D/2),
 // dO [256+3D/2,256+2D) (A-operand layout: row = lane, elements 2c and 2c+1 in column c).
+// dS = P (dP - D) for 32 key columns of one query row, P = exp2(S scale log2(e) - LSE log2(e)),
+// packed to fp16 pairs; with kMask the keys outside the grid (clear bits of vm) get P = 0.
+template <bool kMask>
+__device__ __forceinline__ void ds_pairs(const uint32_t (&us)[32], const uint32_t (&up)[32], uint32_t vm, float2 sc2,
+                                         float2 nl2, float2 nD2, uint32_t (&pds)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float2 x2 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl2);
+    float p0 = ex2(x2.x), p1 = ex2(x2.y);
+    if (kMask) {
+      if (!((vm >> (2 * e)) & 1u)) p0 = 0.f;
+      if (!((vm >> (2 * e + 1)) & 1u)) p1 = 0.f;
+    }
+    const float2 d2 = fadd2(make_float2(__uint_as_float(up[2 * e]), __uint_as_float(up[2 * e + 1])), nD2);
+    const float2 r2 = fmul2(make_float2(p0, p1), d2);
+    pds[e] = pack_f16(r2.x, r2.y);
+  }
+}
+
 template <int D, bool F32OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     dqx_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -781,20 +800,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tdP + lane_base + col0, up);
         tmem_wait_ld();
         uint32_t pds[16];
-        const uint32_t vm = full ? 0xffffffffu : block_rows_mask32(a.g, J, col0);
-        // column pairs through the packed fp32x2 forms: the same roundings as the scalar ones
+        // column pairs through the packed fp32x2 forms: the same roundings as the scalar ones;
+        // full key blocks (all but the grid's edge tiles) skip the per-key mask
         const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nl2 = make_float2(-l2, -l2);
         const float2 nD2 = make_float2(-Dx, -Dx);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 x2 = ffma2(make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl2);
-          float p0 = ex2(x2.x), p1 = ex2(x2.y);
-          if (!((vm >> (2 * e)) & 1u)) p0 = 0.f;
-          if (!((vm >> (2 * e + 1)) & 1u)) p1 = 0.f;
-          const float2 d2 = fadd2(make_float2(__uint_as_float(up[2 * e]), __uint_as_float(up[2 * e + 1])), nD2);
-          const float2 r2 = fmul2(make_float2(p0, p1), d2);
-          pds[e] = pack_f16(r2.x, r2.y);
-        }
+        if (full)
+          ds_pairs<false>(us, up, 0xffffffffu, sc2, nl2, nD2, pds);
+        else
+          ds_pairs<true>(us, up, block_rows_mask32(a.g, J, col0), sc2, nl2, nD2, pds);
         tmem_st16(tS + lane_base + grp * 64 + cc * 16, pds);
       }
       tmem_wait_st();
