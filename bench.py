@@ -323,21 +323,32 @@ def main():
 
     main_set = dict(Q=Q, K=K, V=V, dO=dO, Wq=Wq, Wk=Wk, dQ=dQ, dK=dK, dV=dV)
 
-    def step(ev=None, b=None):
+    def step(ev=None, b=None, gate=None):
+        # gate(name), when given, runs before the predictor ("predict"), the forward ("fwd") and the
+        # backward ("bwd"), and once dQ is final ("dq"): the end-to-end loop waits there for that
+        # phase's inputs and starts dQ's copy to the host under the dK/dV phase.
         b = main_set if b is None else b
         if ev is not None:
             ev[0].record(stream)
+        if gate:
+            gate("predict")
         sda.sda_predict_blocks(p, b["Q"], b["K"], b["Wq"], b["Wk"], idx, None, ws_p, stream)
         if ev is not None:
             ev[1].record(stream)
+        if gate:
+            gate("fwd")
         sda.sda_attn_fwd_train(p, b["Q"], b["K"], b["V"], idx, O, LSE, ws_t, stream=stream)
         if ev is not None:
             ev[2].record(stream)
+        if gate:
+            gate("bwd")
         for i, ph in enumerate((1, 2, 4)):  # prepare, dQ, dK/dV: one call each so every phase is timed
             sda.sda_attn_bwd_train(p, LSE, b["dO"], idx, b["dQ"], b["dK"], b["dV"], "f32", ws_t, phases=ph,
                                    stream=stream)
             if ev is not None:
                 ev[3 + i].record(stream)
+            if gate and ph == 2:
+                gate("dq")
 
     def barrier():
         if dist is not None:
@@ -376,7 +387,10 @@ def main():
     # ---- end to end through host buffers (pinned), copies inside the timed region.
     # Every step copies its inputs host->device and its gradients device->host.  The
     # copies run on two copy streams against two sets of device buffers, so step i+1's
-    # inputs arrive and step i-1's gradients leave while step i computes.
+    # inputs arrive and step i-1's gradients leave while step i computes.  Each phase waits
+    # only for its own inputs (the predictor for Q, K, Wq, Wk; the forward for V; the
+    # backward for dO), and dQ leaves while dK, dV are computed, so the first step's wait
+    # and the last step's tail are one part of the copies, not all of them.
     e2e = None
     if not args.no_e2e:
         pin = {n: t.pin_memory() for n, t in host_bf16.items()}
@@ -389,8 +403,11 @@ def main():
         s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
+        groups = {"predict": ("Q", "K", "Wq", "Wk"), "fwd": ("V",), "bwd": ("dO",)}
+
         def run_e2e(nsteps):
-            h2d_done = [ev() for _ in range(nsteps)]
+            h2d_done = [{g: ev() for g in groups} for _ in range(nsteps)]
+            dq_done = [ev() for _ in range(nsteps)]
             comp_done = [ev() for _ in range(nsteps)]
             d2h_done = [ev() for _ in range(nsteps)]
 
@@ -399,9 +416,10 @@ def main():
                 if i >= 2:
                     s_h2d.wait_event(comp_done[i - 2])  # step i-2 no longer reads this set's inputs
                 with torch.cuda.stream(s_h2d):
-                    for n, t in pin.items():
-                        b[n].copy_(t, non_blocking=True)
-                h2d_done[i].record(s_h2d)
+                    for g, names in groups.items():
+                        for n in names:
+                            b[n].copy_(pin[n], non_blocking=True)
+                        h2d_done[i][g].record(s_h2d)
 
             t0 = ev()
             t0.record(s_h2d)
@@ -410,14 +428,23 @@ def main():
                 b = sets[i % 2]
                 if i + 1 < nsteps:
                     issue_h2d(i + 1)
-                stream.wait_event(h2d_done[i])
                 if i >= 2:
                     stream.wait_event(d2h_done[i - 2])  # step i-2's gradients have left this set
-                step(None, b)
+
+                def gate(name, i=i, b=b):
+                    if name in groups:
+                        stream.wait_event(h2d_done[i][name])
+                        return
+                    dq_done[i].record(stream)  # dQ is final: it leaves while dK, dV are computed
+                    s_d2h.wait_event(dq_done[i])
+                    with torch.cuda.stream(s_d2h):
+                        out_host[0].copy_(b["dQ"], non_blocking=True)
+
+                step(None, b, gate)
                 comp_done[i].record(stream)
                 s_d2h.wait_event(comp_done[i])
                 with torch.cuda.stream(s_d2h):
-                    for h, g in zip(out_host, (b["dQ"], b["dK"], b["dV"])):
+                    for h, g in zip(out_host[1:], (b["dK"], b["dV"])):
                         h.copy_(g, non_blocking=True)
                 d2h_done[i].record(s_d2h)
             stream.wait_event(d2h_done[nsteps - 1])
@@ -445,7 +472,7 @@ def main():
         ms_e2e = max_over_ranks(ms_e2e, dist, dev)
         e2e = {"value": whole_job_tflops(world, f_fwd + f_bwd, ms_e2e), "unit": "TFLOP/s",
                "ms_per_step": ms_e2e, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "copies": "two copy streams, double-buffered device sets",
+               "h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "copies": "two copy streams, double-buffered device sets, each phase gated on its own inputs",
                "tokens_per_s": world * wl.B * wl.N / (ms_e2e / 1e3)}
         del sets
 
