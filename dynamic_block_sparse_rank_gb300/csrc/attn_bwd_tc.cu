@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float Dt = a.Dv[tile_row];  // D~ from the stored O
     float dsum0 = 0.f, dsum1 = 0.f;   // this group's share of D = sum_j P_ij dP_ij
     for (int j = 0; j < n; ++j) {
-      if (!mbar_wait(sdpfull + grp, j & 1, a.status, abort_flag)) break;
+      if (!warp_wait(sdpfull + grp, j & 1, a.status, abort_flag)) break;
       tc_fence_after();
       const int J = a.all_full ? 0 : sel[j];
       const bool full = a.all_full || block_is_full(a.g, J);
@@ -764,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     // Q (group 0) or dO (group 1) into TMEM: this thread's row, 16-byte vectors of the
     // swizzled tile, 8 fp16 = 4 packed columns each.
-    if (n > 0 && mbar_wait(qfull, 0, a.status, abort_flag)) {
+    if (n > 0 && warp_wait(qfull, 0, a.status, abort_flag)) {
       const uint8_t* src = grp == 0 ? sQ : sdO;
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -788,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float l2 = a.L2v[tile_row];
     const float Dx = a.Dv[tile_row];  // exact D (from the fp32 O)
     for (int j = 0; j < n; ++j) {
-      if (!mbar_wait(sdpfull + grp, j & 1, a.status, abort_flag)) break;
+      if (!warp_wait(sdpfull + grp, j & 1, a.status, abort_flag)) break;
       tc_fence_after();
       const int J = a.all_full ? 0 : sel[j];
       const bool full = a.all_full || block_is_full(a.g, J);
@@ -1013,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const bool row_ok = block_row_token(a.g, J, row) >= 0;
     for (int u = 0; u < n; ++u) {
-      if (!mbar_wait(sdpfull + grp, u & 1, a.status, abort_flag)) break;
+      if (!warp_wait(sdpfull + grp, u & 1, a.status, abort_flag)) break;
       tc_fence_after();
       // LSE*log2e and D of this group's 64 query rows, indexed by the column c as l2[c]
       const float* l2 = reinterpret_cast<const float*>(rows + ((2 * u + grp) % HST) * 512) - grp * 64;

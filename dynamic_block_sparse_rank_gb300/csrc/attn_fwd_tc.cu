@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q into TMEM, the A operand of every S product (so S reads only K from shared
     // memory): this thread's row, elements [hf d/2, (hf + 1) d/2), 16-byte vectors of the
     // swizzled tile, 8 values = 4 packed columns each.
-    if (n_sel > 0 && mbar_wait(qfull, 0, a.status, abort_flag)) {
+    if (n_sel > 0 && warp_wait(qfull, 0, a.status, abort_flag)) {
       constexpr int kV = D / 16;  // vectors of this half row
       uint32_t u[kV * 4];
 #pragma unroll
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(qtmem);
     }
     for (int j = 0; j < n_sel; ++j) {
-      const bool okw = mbar_wait(sfull + j % kSBufs, (j / kSBufs) & 1, a.status, abort_flag);
+      const bool okw = warp_wait(sfull + j % kSBufs, (j / kSBufs) & 1, a.status, abort_flag);
       const uint32_t tS = tmem + (j % kSBufs) * 128 + lane_base + hf * 64;
       uint32_t u0[32], u1[32];
       uint32_t vm0 = ~0u, vm1 = ~0u;  // key rows of J inside the grid
