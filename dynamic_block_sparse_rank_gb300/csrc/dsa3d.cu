@@ -193,6 +193,20 @@ __global__ void __launch_bounds__(kDsaThreads) dsa3d_offsets_kernel(const __nv_b
   }
 }
 
+// Dot product of 8 bf16 pairs (4 packed words each): .x sums the low halves, .y the high
+// ones.  A mixed-precision FMA takes the bf16 operands as they are (their product is exact
+// in fp32) and adds it to the fp32 sum with one rounding, so neither row is unpacked.
+__device__ __forceinline__ float2 dot8_bf16(const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+  float lo = 0.f, hi = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(a[i]), "r"(b[i]));
+  return make_float2(lo, hi);
+}
+
 // A warp serves 256 / D tokens of one head: a token's row is split over D / 8 lanes, 8
 // channels (16 bytes) each.  Per window point the three axes give the two candidate grid
 // coordinates, their weights (1 - f, f) and whether each lies inside the raster; the 8
@@ -226,16 +240,13 @@ __global__ void __launch_bounds__(kDsaThreads) dsa3d_fwd_kernel(const __nv_bfloa
     int t, y, x;
     raster_coords(n, a.H, a.W, t, y, x);
     const long long row = ((long long)b * N + n) * rs + (long long)h * D + sl * 8;
-    float2 q[4];
+    // q stays in bf16: q . k is formed with mixed-precision FMAs (bf16 x bf16 products are
+    // exact in fp32), and the scale (to base-2 logits) is applied to the reduced sum.
+    const float qs = a.scale * kLog2e;
+    uint32_t q[4];
     {
       const uint4 qv = __ldg(reinterpret_cast<const uint4*>(Q + row));
-      const float qs = a.scale * kLog2e;  // logits in base 2
-      const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = bf16x2_to_f2(w4[i]);
-        q[i] = make_float2(f.x * qs, f.y * qs);
-      }
+      q[0] = qv.x, q[1] = qv.y, q[2] = qv.z, q[3] = qv.w;
     }
     const float* offn = off + (((long long)b * N + n) * a.heads + h) * (3LL * a.S);
     float m = -INFINITY, l = 0.f;
@@ -275,17 +286,15 @@ __global__ void __launch_bounds__(kDsaThreads) dsa3d_fwd_kernel(const __nv_bfloa
             const uint4 kv = __ldg(reinterpret_cast<const uint4*>(Kb + mrow));
             const uint4 vv = __ldg(reinterpret_cast<const uint4*>(Vb + mrow));
             const uint32_t kw4[4] = {kv.x, kv.y, kv.z, kv.w}, vw4[4] = {vv.x, vv.y, vv.z, vv.w};
-            float2 pd = make_float2(0.f, 0.f);
+            const float2 pd = dot8_bf16(q, kw4);
             const float2 w2 = make_float2(wgt, wgt);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              pd = ffma2(q[i], bf16x2_to_f2(kw4[i]), pd);
-              vs[i] = ffma2(w2, bf16x2_to_f2(vw4[i]), vs[i]);
-            }
+            for (int i = 0; i < 4; ++i) vs[i] = ffma2(w2, bf16x2_to_f2(vw4[i]), vs[i]);
             dot = fmaf(wgt, pd.x + pd.y, dot);
           }
 #pragma unroll
           for (int sh = LPT / 2; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+          dot *= qs;
           const float mn = fmaxf(m, dot);
           const float corr = exp2f(m - mn), p = exp2f(dot - mn);
           l = fmaf(l, corr, p);
@@ -420,9 +429,13 @@ __global__ void __launch_bounds__(kDsaThreads, 3) dsa3d_bwd_kernel(const __nv_bf
     const int n = valid ? n_raw : N - 1;  // lanes of a missing token compute a copy and write nothing
     int t, y, x;
     raster_coords(n, a.H, a.W, t, y, x);
-    float2 q[4], g[4];
+    float2 q[4];
     load8(Q + hb + (long long)n * rs, q);
-    load8(dO + hb + (long long)n * rs, g);
+    uint32_t g[4];  // dO stays in bf16: dO . V takes mixed-precision FMAs (dot8_bf16)
+    {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(dO + hb + (long long)n * rs));
+      g[0] = u.x, g[1] = u.y, g[2] = u.z, g[3] = u.w;
+    }
     const float lse2 = LSE[((long long)b * a.heads + h) * N + n] * kLog2e;
     const float sl2 = a.scale * kLog2e;
     const long long ns = ((long long)b * N + n) * a.heads + h;
@@ -454,15 +467,16 @@ __global__ void __launch_bounds__(kDsaThreads, 3) dsa3d_bwd_kernel(const __nv_bf
                         ww = cw ? c.f[2] : 1.f - c.f[2];
             const float w = wt * wh * ww;
             const long long row = (long long)(m000 + ct * HW + ch * a.W + cw) * rs;
-            float2 kv[4], vv[4];
+            float2 kv[4];
             load8(K + hb + row, kv);
-            load8(V + hb + row, vv);
-            float2 pq = make_float2(0.f, 0.f), pv = make_float2(0.f, 0.f);
+            const uint4 vu = __ldg(reinterpret_cast<const uint4*>(V + hb + row));
+            const uint32_t vv[4] = {vu.x, vu.y, vu.z, vu.w};
+            float2 pq = make_float2(0.f, 0.f);
+            const float2 pv = dot8_bf16(g, vv);
             const float2 w2 = make_float2(w, w);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               pq = ffma2(q[i], kv[i], pq);
-              pv = ffma2(g[i], vv[i], pv);
               ks[i] = ffma2(w2, kv[i], ks[i]);
             }
             const float pqs = pq.x + pq.y, pvs = pv.x + pv.y;
