@@ -253,13 +253,20 @@ __global__ void __launch_bounds__(kDsaThreads) dsa3d_fwd_kernel(const __nv_bfloa
     float2 o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = make_float2(0.f, 0.f);
+    // offsets of the current window point; the next point's are loaded one point ahead,
+    // so their latency overlaps this point's gathers
+    float ox = __ldg(offn), oy = __ldg(offn + 1), oz = __ldg(offn + 2);
     int s = 0;
     for (int wa = 0; wa < a.kt; ++wa)
       for (int wb = 0; wb < a.kh; ++wb)
         for (int wc = 0; wc < a.kw; ++wc, ++s) {
-          const float pt = (float)(t + wa - rt) + __ldg(offn + 3 * s);
-          const float ph = (float)(y + wb - rh) + __ldg(offn + 3 * s + 1);
-          const float pw = (float)(x + wc - rw) + __ldg(offn + 3 * s + 2);
+          const float pt = (float)(t + wa - rt) + ox;
+          const float ph = (float)(y + wb - rh) + oy;
+          const float pw = (float)(x + wc - rw) + oz;
+          {
+            const int sn = s + 1 < a.S ? s + 1 : s;
+            ox = __ldg(offn + 3 * sn), oy = __ldg(offn + 3 * sn + 1), oz = __ldg(offn + 3 * sn + 2);
+          }
           const float bt = floorf(pt), bh = floorf(ph), bw = floorf(pw);
           const float ft = pt - bt, fh = ph - bh, fw = pw - bw;
           // per axis: is coordinate base (+1) inside the raster; tested in float, so NaN or
